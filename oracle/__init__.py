@@ -1,0 +1,8 @@
+"""CPU oracle for the dense half-precision GEMM (test infrastructure only).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline and
+reference legs may import this package. The product path never does.
+"""
+
+from .hgemm_oracle import (FORMATS, decode, flops, gemm, gemm_cols, gemm_f64,  # noqa: F401
+                           gemm_rows, round_rne)
