@@ -1,0 +1,451 @@
+// hgemm_api.cu - the C ABI (include/hgemm.h): argument checks, the planner,
+// TMA descriptor encoding and the launch of the persistent tcgen05 kernel.
+#include <atomic>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "hgemm.h"
+#include "launch.h"
+
+namespace {
+
+using hg::TcParams;
+
+thread_local std::string t_last_error;
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+
+hgemm_status_t cuda_fail(cudaError_t e, const char* where) {
+    t_last_error = std::string(where) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+    return HGEMM_ERR_CUDA;
+}
+
+// ------------------------------------------------------------ device facts
+struct DeviceInfo {
+    bool probed = false;
+    int major = 0, minor = 0, sms = 0;
+};
+
+hgemm_status_t device_info(int* dev_out, DeviceInfo* out) {
+    static std::mutex mu;
+    static DeviceInfo cache[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        t_last_error = std::string("cudaGetDevice: ") + cudaGetErrorString(e);
+        return HGEMM_ERR_UNSUPPORTED_DEVICE;
+    }
+    if (dev < 0 || dev >= 64) return HGEMM_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lk(mu);
+    DeviceInfo& d = cache[dev];
+    if (!d.probed) {
+        if ((e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) {
+            t_last_error = std::string("cudaDeviceGetAttribute: ") + cudaGetErrorString(e);
+            return HGEMM_ERR_UNSUPPORTED_DEVICE;
+        }
+        d.probed = true;
+    }
+    *out = d;
+    *dev_out = dev;
+    if (d.major != 10 || d.minor != 3) {
+        t_last_error = "device is compute capability " + std::to_string(d.major) + "." +
+                       std::to_string(d.minor) + "; this library runs on 10.3 (sm_103a) only";
+        return HGEMM_ERR_UNSUPPORTED_DEVICE;
+    }
+    return HGEMM_OK;
+}
+
+// ------------------------------------------------- cuTensorMapEncodeTiled
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// A 2-D row-major matrix of 16-bit values: `cols` contiguous values per row,
+// `ld` values between rows; box = box_cols x box_rows, 128-byte swizzle,
+// out-of-range elements read as zero.
+hgemm_status_t encode_2d(CUtensorMap* m, hgemm_dtype_t dt, const void* base, int64_t rows,
+                         int64_t cols, int64_t ld, uint32_t box_cols, uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) {
+        t_last_error = "cuTensorMapEncodeTiled is not available from the driver";
+        return HGEMM_ERR_CUDA;
+    }
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, dt == HGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                    2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        t_last_error = "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(static_cast<int>(r));
+        return HGEMM_ERR_CUDA;
+    }
+    return HGEMM_OK;
+}
+
+// ----------------------------------------------------------------- planner
+bool valid_shape_config(int cg, int bn) {
+    return (cg == 1 && (bn == 64 || bn == 128 || bn == 256)) || (cg == 2 && (bn == 128 || bn == 256));
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Relative throughput of one SM running each tile shape on a long K loop
+// (1.0 = the tensor-core peak). CTA pairs halve each SM's B traffic through
+// shared memory; narrower tiles pay more shared-memory bytes per MMA.
+double shape_efficiency(int cg, int bn) {
+    if (cg == 2 && bn == 256) return 1.00;
+    if (cg == 2 && bn == 128) return 0.93;
+    if (cg == 1 && bn == 256) return 0.93;
+    if (cg == 1 && bn == 128) return 0.85;
+    return 0.70;  // cg 1, bn 64
+}
+
+// Pick (cta_group, block_n) minimising the estimated time: whole waves of
+// tiles over the resident clusters, each tile costing its padded area over the
+// shape's efficiency, plus a per-tile fixed cost that favours fewer, larger
+// tiles when the K loop is short.
+void choose_shape(int64_t M, int64_t N, int64_t K, int sms, int* cg_out, int* bn_out) {
+    static const int cand[5][2] = {{2, 256}, {2, 128}, {1, 256}, {1, 128}, {1, 64}};
+    double best = 1e300;
+    int bcg = 2, bbn = 256;
+    const int64_t kb = cdiv(K, hg::kBlockK);
+    for (const auto& c : cand) {
+        const int cg = c[0], bn = c[1];
+        const int64_t tiles = cdiv(M, 128 * cg) * cdiv(N, bn);
+        const int64_t clusters = sms / cg;
+        if (clusters <= 0) continue;
+        const int64_t waves = cdiv(tiles, clusters);
+        const double tile_work = static_cast<double>(128 * cg) * bn * (kb * hg::kBlockK) / cg;  // per SM
+        const double tile_time = tile_work / shape_efficiency(cg, bn) + 128.0 * bn * 24.0;
+        const double t = static_cast<double>(waves) * tile_time;
+        if (t < best * 0.999) {
+            best = t;
+            bcg = cg;
+            bbn = bn;
+        }
+    }
+    *cg_out = bcg;
+    *bn_out = bbn;
+}
+
+hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, const hgemm_config_t* cfg, int sms,
+                         bool a_unaligned, bool b_unaligned, bool c_unaligned, hgemm_plan_t* pl) {
+    std::memset(pl, 0, sizeof(*pl));
+    hgemm_config_t c{};
+    if (cfg) c = *cfg;
+    int cg = c.cta_group, bn = c.block_n;
+    if (cg == 0 || bn == 0) {
+        int acg, abn;
+        choose_shape(M, N, K, sms, &acg, &abn);
+        if (cg == 0 && bn == 0) {
+            cg = acg;
+            bn = abn;
+        } else if (cg == 0) {
+            cg = (bn >= 128) ? acg : 1;
+        } else {
+            bn = (cg == 2 && abn < 128) ? 128 : abn;
+        }
+    }
+    if (!valid_shape_config(cg, bn)) {
+        t_last_error = "unsupported (cta_group, block_n) pair";
+        return HGEMM_ERR_INVALID_ARG;
+    }
+    if (c.group_m < 0 || c.max_clusters < 0 || c.store_mode < 0 || c.store_mode > 2) {
+        t_last_error = "negative or unknown config field";
+        return HGEMM_ERR_INVALID_ARG;
+    }
+    pl->cta_group = cg;
+    pl->block_m = 128 * cg;
+    pl->block_n = bn;
+    pl->block_k = hg::kBlockK;
+    pl->stages = hg::tc_stages(cg, bn);
+    pl->smem_bytes = hg::tc_smem_bytes(cg, bn);
+    pl->tmem_cols = 2 * bn;
+    pl->tiles_m = static_cast<int32_t>(cdiv(M, pl->block_m));
+    pl->tiles_n = static_cast<int32_t>(cdiv(N, bn));
+    pl->num_tiles = pl->tiles_m * pl->tiles_n;
+    pl->group_m = c.group_m > 0 ? c.group_m : (pl->tiles_m < 8 ? (pl->tiles_m > 0 ? pl->tiles_m : 1) : 8);
+    int64_t clusters = sms / cg;
+    if (c.max_clusters > 0 && c.max_clusters < clusters) clusters = c.max_clusters;
+    if (clusters > pl->num_tiles) clusters = pl->num_tiles;
+    if (clusters < 1) clusters = 1;
+    pl->grid_ctas = static_cast<int32_t>(clusters * cg);
+    pl->repack_a = a_unaligned ? 1 : 0;
+    pl->repack_b = b_unaligned ? 1 : 0;
+    pl->store_mode = (c.store_mode != 0) ? c.store_mode : (c_unaligned ? 2 : 1);
+    if (c_unaligned && pl->store_mode == 1) {
+        t_last_error = "TMA stores need a 16-byte aligned C with an 16-byte row pitch";
+        return HGEMM_ERR_INVALID_ARG;
+    }
+    return HGEMM_OK;
+}
+
+bool misaligned16(const void* p, int64_t cols) {
+    return (reinterpret_cast<uintptr_t>(p) & 15u) != 0 || ((cols * 2) & 15) != 0;
+}
+
+bool overlaps(const void* a, int64_t abytes, const void* b, int64_t bbytes) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + static_cast<uintptr_t>(bbytes) && b0 < a0 + static_cast<uintptr_t>(abytes);
+}
+
+hgemm_status_t check_args(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                          hgemm_dtype_t dtype) {
+    const int64_t kMax = 2147483647LL;
+    if (M < 0 || N < 0 || K < 0 || M > kMax || N > kMax || K > kMax) {
+        t_last_error = "dimensions must be in [0, 2^31 - 1]";
+        return HGEMM_ERR_INVALID_ARG;
+    }
+    if (dtype != HGEMM_F16 && dtype != HGEMM_BF16) {
+        t_last_error = "unknown dtype";
+        return HGEMM_ERR_INVALID_ARG;
+    }
+    if (M == 0 || N == 0) return HGEMM_OK;
+    if (!C || (K > 0 && (!A || !B))) {
+        t_last_error = "null pointer for a non-empty operand";
+        return HGEMM_ERR_INVALID_ARG;
+    }
+    if ((reinterpret_cast<uintptr_t>(C) & 1u) || (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 1u) ||
+                                                           (reinterpret_cast<uintptr_t>(B) & 1u)))) {
+        t_last_error = "operands must be 2-byte aligned";
+        return HGEMM_ERR_INVALID_ARG;
+    }
+    if (K > 0 && (overlaps(C, 2 * M * N, A, 2 * M * K) || overlaps(C, 2 * M * N, B, 2 * K * N))) {
+        t_last_error = "C overlaps A or B";
+        return HGEMM_ERR_INVALID_ARG;
+    }
+    return HGEMM_OK;
+}
+
+hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                   hgemm_dtype_t dtype, const hgemm_config_t* cfg, cudaStream_t stream) {
+    t_last_error.clear();
+    hgemm_status_t st = check_args(A, B, C, M, N, K, dtype);
+    if (st != HGEMM_OK || M == 0 || N == 0) return st;
+    int dev = 0;
+    DeviceInfo info;
+    if ((st = device_info(&dev, &info)) != HGEMM_OK) return st;
+    cudaError_t e;
+    if (K == 0) {
+        if ((e = hg::launch_zero(static_cast<uint16_t*>(C), M * N, stream)) != cudaSuccess)
+            return cuda_fail(e, "zero fill");
+        return HGEMM_OK;
+    }
+
+    hgemm_plan_t pl;
+    const bool a_bad = misaligned16(A, K), b_bad = misaligned16(B, N), c_bad = misaligned16(C, N);
+    if ((st = make_plan(M, N, K, cfg, info.sms, a_bad, b_bad, c_bad, &pl)) != HGEMM_OK) return st;
+
+    // Resident clusters bound the persistent grid.
+    const int cg = pl.cta_group, bn = pl.block_n;
+    int resident = dtype == HGEMM_BF16 ? hg::max_active_clusters_bf16(cg, bn)
+                                       : hg::max_active_clusters_f16(cg, bn);
+    if (resident <= 0) resident = info.sms / cg;
+    int clusters = pl.grid_ctas / cg;
+    if (clusters > resident) clusters = resident;
+
+    // Operands TMA cannot address get a 16-byte-pitched copy.
+    const int64_t lda = pl.repack_a ? (K + 7) / 8 * 8 : K;
+    const int64_t ldb = pl.repack_b ? (N + 7) / 8 * 8 : N;
+    void* work = nullptr;
+    const void* a_use = A;
+    const void* b_use = B;
+    if (pl.repack_a || pl.repack_b) {
+        const int64_t bytes_a = pl.repack_a ? 2 * M * lda : 0;
+        const int64_t bytes_b = pl.repack_b ? 2 * K * ldb : 0;
+        const int64_t off_b = (bytes_a + 255) / 256 * 256;
+        if ((e = cudaMallocAsync(&work, static_cast<size_t>(off_b + bytes_b), stream)) != cudaSuccess) {
+            cuda_fail(e, "cudaMallocAsync (repack workspace)");
+            return HGEMM_ERR_ALLOC;
+        }
+        uint8_t* w8 = static_cast<uint8_t*>(work);
+        if (pl.repack_a) {
+            if ((e = hg::launch_repack(static_cast<const uint16_t*>(A), M, K,
+                                       reinterpret_cast<uint16_t*>(w8), lda, stream)) != cudaSuccess) {
+                cudaFreeAsync(work, stream);
+                return cuda_fail(e, "repack A");
+            }
+            a_use = w8;
+        }
+        if (pl.repack_b) {
+            if ((e = hg::launch_repack(static_cast<const uint16_t*>(B), K, N,
+                                       reinterpret_cast<uint16_t*>(w8 + off_b), ldb, stream)) != cudaSuccess) {
+                cudaFreeAsync(work, stream);
+                return cuda_fail(e, "repack B");
+            }
+            b_use = w8 + off_b;
+        }
+    }
+
+    CUtensorMap ta, tb, tc;
+    std::memset(&tc, 0, sizeof(tc));
+    if ((st = encode_2d(&ta, dtype, a_use, M, K, lda, hg::kBlockK, hg::kBlockMCta)) != HGEMM_OK ||
+        (st = encode_2d(&tb, dtype, b_use, K, N, ldb, 64, hg::kBlockK)) != HGEMM_OK ||
+        (pl.store_mode == 1 &&
+         (st = encode_2d(&tc, dtype, C, M, N, N, hg::kEpiBoxCols, hg::kEpiBoxRows)) != HGEMM_OK)) {
+        if (work) cudaFreeAsync(work, stream);
+        return st;
+    }
+
+    TcParams p{};
+    p.M = static_cast<int32_t>(M);
+    p.N = static_cast<int32_t>(N);
+    p.K = static_cast<int32_t>(K);
+    p.tiles_m = pl.tiles_m;
+    p.tiles_n = pl.tiles_n;
+    p.num_tiles = pl.num_tiles;
+    p.group_m = pl.group_m;
+    p.num_kb = static_cast<int32_t>(cdiv(K, hg::kBlockK));
+    const uint32_t fmt = dtype == HGEMM_BF16 ? 1u : 0u;
+    // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B format
+    // (bits 7-9, 10-12: 0 f16, 1 bf16), A K-major (bit 15 = 0), B MN-major
+    // (bit 16 = 1), N >> 3 (bits 17-22), M >> 4 (bits 24-28).
+    p.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | (0u << 15) | (1u << 16) |
+              (static_cast<uint32_t>(bn >> 3) << 17) | (static_cast<uint32_t>((128 * cg) >> 4) << 24);
+    p.store_mode = pl.store_mode;
+    p.C = static_cast<uint16_t*>(C);
+    p.ldc = N;
+    p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+    if ((e = hg::status_word_ptr(&p.status)) != cudaSuccess) {
+        if (work) cudaFreeAsync(work, stream);
+        return cuda_fail(e, "status word");
+    }
+
+    e = dtype == HGEMM_BF16 ? hg::launch_tc_bf16(cg, bn, ta, tb, tc, p, clusters, stream)
+                            : hg::launch_tc_f16(cg, bn, ta, tb, tc, p, clusters, stream);
+    if (work) cudaFreeAsync(work, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    return HGEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+hgemm_status_t hgemm(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                     hgemm_dtype_t dtype, void* stream) {
+    return run(A, B, C, M, N, K, dtype, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+hgemm_status_t hgemm_ex(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                        hgemm_dtype_t dtype, const hgemm_config_t* cfg, void* stream) {
+    return run(A, B, C, M, N, K, dtype, cfg, static_cast<cudaStream_t>(stream));
+}
+
+hgemm_status_t hgemm_host(const void* hA, const void* hB, void* hC, int64_t M, int64_t N,
+                          int64_t K, hgemm_dtype_t dtype, void* dA, void* dB, void* dC,
+                          void* stream) {
+    t_last_error.clear();
+    hgemm_status_t st = check_args(dA, dB, dC, M, N, K, dtype);
+    if (st != HGEMM_OK) return st;
+    if (M == 0 || N == 0) return HGEMM_OK;
+    if (!hC || (K > 0 && (!hA || !hB))) {
+        t_last_error = "null host pointer for a non-empty operand";
+        return HGEMM_ERR_INVALID_ARG;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (K > 0) {
+        if ((e = cudaMemcpyAsync(dA, hA, static_cast<size_t>(2 * M * K), cudaMemcpyHostToDevice, s)) != cudaSuccess)
+            return cuda_fail(e, "copy A to device");
+        if ((e = cudaMemcpyAsync(dB, hB, static_cast<size_t>(2 * K * N), cudaMemcpyHostToDevice, s)) != cudaSuccess)
+            return cuda_fail(e, "copy B to device");
+    }
+    if ((st = run(dA, dB, dC, M, N, K, dtype, nullptr, s)) != HGEMM_OK) return st;
+    if ((e = cudaMemcpyAsync(hC, dC, static_cast<size_t>(2 * M * N), cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+        return cuda_fail(e, "copy C to host");
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "stream synchronize");
+    return HGEMM_OK;
+}
+
+hgemm_status_t hgemm_plan(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dtype,
+                          const hgemm_config_t* cfg, int32_t sm_count, hgemm_plan_t* out) {
+    t_last_error.clear();
+    if (!out) return HGEMM_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K < 0 || M > 2147483647LL || N > 2147483647LL || K > 2147483647LL ||
+        (dtype != HGEMM_F16 && dtype != HGEMM_BF16))
+        return HGEMM_ERR_INVALID_ARG;
+    int sms = sm_count;
+    if (sms <= 0) {
+        int dev = 0;
+        DeviceInfo info;
+        hgemm_status_t st = device_info(&dev, &info);
+        if (st != HGEMM_OK) return st;
+        sms = info.sms;
+    }
+    const bool a_bad = ((K * 2) & 15) != 0, b_bad = ((N * 2) & 15) != 0, c_bad = ((N * 2) & 15) != 0;
+    return make_plan(M, N, K, cfg, sms, a_bad, b_bad, c_bad, out);
+}
+
+void hgemm_tile_coord(int32_t t, int32_t tiles_m, int32_t tiles_n, int32_t group_m, int32_t* tm,
+                      int32_t* tn) {
+    int32_t a = 0, b = 0;
+    if (tiles_m > 0 && tiles_n > 0 && group_m > 0) hg::tile_coord(t, tiles_m, tiles_n, group_m, a, b);
+    if (tm) *tm = a;
+    if (tn) *tn = b;
+}
+
+hgemm_status_t hgemm_get_device_status(int32_t device, int32_t reset, uint32_t* info) {
+    t_last_error.clear();
+    int prev = 0;
+    cudaError_t e = cudaGetDevice(&prev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (device != prev && (e = cudaSetDevice(device)) != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+    unsigned long long* ptr = nullptr;
+    unsigned long long word = 0;
+    hgemm_status_t st = HGEMM_OK;
+    if ((e = hg::status_word_ptr(&ptr)) != cudaSuccess ||
+        (e = cudaMemcpy(&word, ptr, sizeof(word), cudaMemcpyDeviceToHost)) != cudaSuccess) {
+        st = cuda_fail(e, "read status word");
+    } else {
+        if (info) *info = static_cast<uint32_t>(word >> 32);
+        st = static_cast<hgemm_status_t>(word & 0xFFFFFFFFull);
+        if (reset && word != 0) {
+            const unsigned long long zero = 0;
+            if ((e = cudaMemcpy(ptr, &zero, sizeof(zero), cudaMemcpyHostToDevice)) != cudaSuccess)
+                st = cuda_fail(e, "reset status word");
+        }
+    }
+    if (device != prev) cudaSetDevice(prev);
+    return st;
+}
+
+void hgemm_set_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 1, std::memory_order_relaxed); }
+
+const char* hgemm_status_string(hgemm_status_t s) {
+    switch (s) {
+        case HGEMM_OK: return "HGEMM_OK";
+        case HGEMM_ERR_INVALID_ARG: return "HGEMM_ERR_INVALID_ARG: invalid argument";
+        case HGEMM_ERR_UNSUPPORTED_DEVICE: return "HGEMM_ERR_UNSUPPORTED_DEVICE: needs a compute capability 10.3 GPU";
+        case HGEMM_ERR_CUDA: return "HGEMM_ERR_CUDA: a CUDA call failed";
+        case HGEMM_ERR_ALLOC: return "HGEMM_ERR_ALLOC: workspace allocation failed";
+        case HGEMM_ERR_TIMEOUT: return "HGEMM_ERR_TIMEOUT: a bounded wait in the kernel ran out";
+    }
+    return "unknown hgemm status";
+}
+
+const char* hgemm_last_error(void) { return t_last_error.c_str(); }
+
+int32_t hgemm_version(void) { return 100; }
+
+}  // extern "C"

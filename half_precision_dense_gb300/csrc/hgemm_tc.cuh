@@ -1,0 +1,420 @@
+// hgemm_tc.cuh - the persistent, warp-specialised tcgen05 GEMM kernel for
+// sm_103a: C = A.B, A (M x K) and B (K x N) row-major fp16/bf16, fp32
+// accumulation in tensor memory, C rounded to the input dtype.
+//
+// Prior art: "[CUDA 优化实战] hgemm - 超越 cuBLAS" builds the same product on an
+// RTX 5060 mobile from cp.async + ldmatrix + mma.sync m16n8k16 (section 1),
+// XOR-swizzled shared memory (section 2), a double-buffered cp.async pipeline
+// (section 3) and a shared-memory-staged, coalesced C write-back (section 4).
+// Each idea has a Blackwell-native counterpart here:
+//
+//   page (sm_80-class instructions)          this kernel (sm_103a)
+//   cp.async 16 B per thread + commit/wait   TMA box loads, mbarrier transaction counts
+//   SWIZZLE_A / SWIZZLE_B (16 B chunk XOR)   the TMA/UMMA 128-byte swizzle (chunk ^= row % 8)
+//   double buffer                            an S-stage full/empty mbarrier ring
+//   mma.sync m16n8k16, fp32 in registers     tcgen05.mma kind::f16, fp32 in tensor memory
+//   grid swizzle (SWIZZLE_W)                 persistent CTAs walking a grouped raster
+//   Cs staging + SWIZZLE_C + float4 stores   tcgen05.ld -> cvt.rn -> swizzled smem -> TMA store
+//
+// Roles (192 threads, one CTA per SM):
+//   warps 0-3  epilogue: warp w reads TMEM lanes 32w..32w+31 (C rows of the tile)
+//   warp 4     producer: one thread issues the TMA loads of A and B per stage
+//   warp 5     MMA: allocates TMEM; one thread of the leader CTA issues tcgen05.mma
+//
+// CTA pairs (CG = 2, a cluster of two): the pair owns a 256-row tile. Each CTA
+// loads its own 128 rows of A and its own half of the tile's B columns; the
+// leader's single thread issues tcgen05.mma.cta_group::2, which reads both
+// CTAs' shared memory and accumulates each CTA's 128 rows in that CTA's TMEM.
+//
+// Every wait is bounded (TcParams::timeout_ns). A wait that runs out records
+// HGEMM_ERR_TIMEOUT with the role and barrier in the device status word, sets a
+// CTA-wide abort flag that ends the other roles' loops, lets in-flight copies
+// and MMAs finish, frees TMEM and returns; it never traps.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ptx.cuh"
+#include "schedule.h"
+
+namespace hg {
+
+constexpr int kBlockMCta = 128;   // C rows per CTA = TMEM lanes
+constexpr int kBlockK = 64;       // K per stage: 64 half-precision values = one 128 B swizzle row
+constexpr int kUmmaK = 16;        // K of one kind::f16 MMA
+constexpr int kEpiWarps = 4;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kThreads = 192;
+constexpr int kEpiBoxRows = 32;   // one epilogue warp's rows
+constexpr int kEpiBoxCols = 64;   // 128 B of half-precision values
+constexpr int kEpiBoxBytes = kEpiBoxRows * kEpiBoxCols * 2;
+constexpr int kSmemLimit = 232448;  // 227 KiB: the opt-in maximum per block
+
+constexpr uint32_t kStatusTimeout = 5;  // == HGEMM_ERR_TIMEOUT
+enum : uint32_t { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3 };
+
+struct TcParams {
+    int32_t M, N, K;
+    int32_t tiles_m, tiles_n, num_tiles, group_m;
+    int32_t num_kb;                 // ceil(K / kBlockK)
+    uint32_t idesc;                 // tcgen05 instruction descriptor
+    int32_t store_mode;             // 1: TMA stores of C; 2: plain stores through `C`
+    uint16_t* C;                    // used by store_mode 2
+    int64_t ldc;                    // elements between C rows (store_mode 2)
+    uint64_t timeout_ns;
+    unsigned long long* status;     // device status word
+};
+
+template <int CG, int BN>
+struct TcCfg {
+    static constexpr int kBnCta = BN / CG;                 // B columns loaded by each CTA
+    static constexpr int kABytes = kBlockMCta * kBlockK * 2;
+    static constexpr int kBBytes = kBlockK * kBnCta * 2;
+    static constexpr int kBAtomBytes = kBlockK * 128;      // 64 columns x 64 k-rows
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBoxBytes;
+    static constexpr int kBarBytes = 256;
+    static constexpr int kStagesFit = (kSmemLimit - 1024 - kEpiBytes - kBarBytes) / kStageBytes;
+    static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiBytes + kBarBytes;
+    static constexpr int kTmemCols = 2 * BN;               // two accumulators of BN fp32 columns
+    static constexpr uint32_t kTxBytes = CG * kStageBytes; // bytes landing per stage on the leader's barrier
+    static_assert(CG == 1 || CG == 2, "cta group");
+    static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
+    static_assert(kBnCta % 64 == 0, "B is loaded in 64-column swizzle atoms");
+    static_assert(kStages >= 2, "pipeline depth");
+    static_assert(kSmemBytes <= kSmemLimit, "shared memory");
+    static_assert((2 * kStages + 5) * 8 + 8 <= kBarBytes, "barrier area");
+};
+
+// Shared-memory matrix descriptor (tcgen05), 128-byte swizzle.
+//   bits  0-13  start address >> 4
+//   bits 16-29  leading-dimension byte offset >> 4
+//   bits 32-45  stride-dimension byte offset >> 4
+//   bits 46-48  fixed 0b001
+//   bits 49-51  base offset (0: every tile starts on a 1024 B boundary)
+//   bits 61-63  layout: 2 = 128-byte swizzle
+// K-major A (rows of 128 B holding 64 K values, 8-row swizzle atoms stacked
+// along M): SBO = 1024 B between 8-row groups; LBO unused. The K offset of the
+// j-th 16-wide MMA inside the 64-wide stage is +32 j bytes of start address.
+// MN-major B (each 64-column atom is 64 k-rows of 128 B): LBO = distance
+// between 64-column atoms, SBO = 1024 B between 8-row k groups; the j-th MMA
+// starts 16 j rows = 2048 j bytes further.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+           (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+           (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) |
+           (1ull << 46) | (2ull << 61);
+}
+
+template <bool kBF16>
+__device__ __forceinline__ uint32_t pack_rn(uint32_t lo, uint32_t hi) {
+    if constexpr (kBF16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(lo), __uint_as_float(hi));
+        return *reinterpret_cast<uint32_t*>(&v);
+    } else {
+        __half2 v = __floats2half2_rn(__uint_as_float(lo), __uint_as_float(hi));
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+}
+
+struct Waiter {
+    volatile uint32_t* abort;
+    uint64_t timeout_ns;
+    unsigned long long* status;
+};
+
+static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Waiter& w,
+                                       uint32_t role, uint32_t which) {
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*w.abort) return false;
+        if (globaltimer_ns() - t0 > w.timeout_ns) {
+            const unsigned long long info =
+                (static_cast<unsigned long long>(role) << 56) |
+                (static_cast<unsigned long long>(which & 0xFFu) << 48) |
+                (static_cast<unsigned long long>(blockIdx.x & 0xFFFFu) << 32);
+            atomicCAS(w.status, 0ull, info | kStatusTimeout);
+            *w.abort = 1;
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Waiter& w,
+                                         uint32_t role, uint32_t which) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_slow(bar, parity, w, role, which);
+}
+
+// Pins the 32 registers after tcgen05.wait::ld so no use is scheduled above it.
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i]));
+}
+
+template <int CG, int BN, bool kBF16>
+__global__ void __launch_bounds__(kThreads, 1)
+hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmC, const TcParams p) {
+#if defined(__CUDA_ARCH__) && defined(__CUDA_ARCH_FEAT_SM103_ALL)
+    using Cfg = TcCfg<CG, BN>;
+    constexpr int S = Cfg::kStages;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* const smem = smem_raw + (base - raw);
+    const uint32_t sA = base;                                   // S x 16 KiB
+    const uint32_t sB = sA + S * Cfg::kABytes;                  // S x kBBytes
+    const uint32_t sEpi = sB + S * Cfg::kBBytes;                // 4 warps x 2 x 4 KiB
+    const uint32_t sBar = sEpi + Cfg::kEpiBytes;
+    const uint32_t bar_full = sBar;                             // [S]
+    const uint32_t bar_empty = sBar + 8 * S;                    // [S]
+    const uint32_t bar_tfull = sBar + 16 * S;                   // [2]
+    const uint32_t bar_tempty = bar_tfull + 16;                 // [2]
+    const uint32_t bar_drain = bar_tempty + 16;
+    uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(smem + (bar_drain + 8 - base));
+    volatile uint32_t* const abort_flag = tmem_slot + 1;
+
+    const int warp = static_cast<int>(threadIdx.x >> 5);
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
+    const int cluster_id = static_cast<int>(blockIdx.x) / CG;
+    const int num_clusters = static_cast<int>(gridDim.x) / CG;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(bar_tfull + 8 * a, 1);
+            mbar_init(bar_tempty + 8 * a, kEpiWarps * CG);
+        }
+        mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init_cluster();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        if (p.store_mode == 1) tma_prefetch_desc(&tmC);
+    }
+    if (warp == kMmaWarp) tmem_alloc<CG>(smem_addr(tmem_slot), Cfg::kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    if constexpr (CG == 2) cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+    const Waiter w{abort_flag, p.timeout_ns, p.status};
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            bool ok = true;
+            for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters) {
+                int32_t tm, tn;
+                tile_coord(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+                const int32_t m0 = tm * (kBlockMCta * CG) + static_cast<int32_t>(rank) * kBlockMCta;
+                const int32_t n0 = tn * BN + static_cast<int32_t>(rank) * Cfg::kBnCta;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bar(bar_empty + 8 * stage, phase ^ 1u, w, kRoleProducer, stage)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t a_dst = sA + stage * Cfg::kABytes;
+                    const uint32_t b_dst = sB + stage * Cfg::kBBytes;
+                    const uint32_t fb = bar_full + 8 * stage;
+                    const int32_t k0 = kb * kBlockK;
+                    if constexpr (CG == 1) {
+                        mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
+                        tma_load_2d(a_dst, &tmA, fb, k0, m0);
+#pragma unroll
+                        for (int j = 0; j < Cfg::kBnCta / 64; ++j)
+                            tma_load_2d(b_dst + j * Cfg::kBAtomBytes, &tmB, fb, n0 + 64 * j, k0);
+                    } else {
+                        const uint32_t fb_leader = mapa_shared(fb, 0);
+                        if (rank == 0) mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
+                        tma_load_2d_pair(a_dst, &tmA, fb_leader, k0, m0);
+#pragma unroll
+                        for (int j = 0; j < Cfg::kBnCta / 64; ++j)
+                            tma_load_2d_pair(b_dst + j * Cfg::kBAtomBytes, &tmB, fb_leader,
+                                             n0 + 64 * j, k0);
+                    }
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // Loads already issued still land in this CTA's shared memory:
+                // give them time before the CTA may exit.
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 50000ull) {}
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ----------------------------------------------------------------- MMA
+        if (rank == 0 && lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            bool ok = true;
+            bool issued = false;
+            int it = 0;
+            for (int t = cluster_id; t < p.num_tiles; t += num_clusters, ++it) {
+                const uint32_t acc = static_cast<uint32_t>(it) & 1u;
+                const uint32_t acc_phase = (static_cast<uint32_t>(it) >> 1) & 1u;
+                if (!wait_bar(bar_tempty + 8 * acc, acc_phase ^ 1u, w, kRoleMma, 32 + acc)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bar(bar_full + 8 * stage, phase, w, kRoleMma, stage)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = sA + stage * Cfg::kABytes;
+                    const uint32_t b0 = sB + stage * Cfg::kBBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kBlockK / kUmmaK; ++kk) {
+                        const uint64_t ad = sdesc_sw128(a0 + 32u * kk, 16u, 1024u);
+                        const uint64_t bd = sdesc_sw128(b0 + 2048u * kk, Cfg::kBAtomBytes, 1024u);
+                        umma_f16<CG>(d_tmem, ad, bd, p.idesc, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    issued = true;
+                    if constexpr (CG == 1) umma_commit(bar_empty + 8 * stage);
+                    else umma_commit_pair(bar_empty + 8 * stage, 0x3);
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                if constexpr (CG == 1) umma_commit(bar_tfull + 8 * acc);
+                else umma_commit_pair(bar_tfull + 8 * acc, 0x3);
+            }
+            if (!ok && issued) {
+                // TMEM may only be freed once every issued MMA has completed.
+                if constexpr (CG == 1) umma_commit(bar_drain);
+                else umma_commit_pair(bar_drain, 0x1);
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(bar_drain, 0) && globaltimer_ns() - t0 < p.timeout_ns) {}
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        int it = 0;
+        uint32_t buf = 0;
+        const uint32_t my_boxes = sEpi + static_cast<uint32_t>(warp) * 2u * kEpiBoxBytes;
+        for (int t = cluster_id; t < p.num_tiles; t += num_clusters, ++it) {
+            const uint32_t acc = static_cast<uint32_t>(it) & 1u;
+            const uint32_t acc_phase = (static_cast<uint32_t>(it) >> 1) & 1u;
+            if (!wait_bar(bar_tfull + 8 * acc, acc_phase, w, kRoleEpilogue, 32 + acc)) break;
+            tc_fence_after();
+            int32_t tm, tn;
+            tile_coord(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+            const int32_t row0 = tm * (kBlockMCta * CG) + static_cast<int32_t>(rank) * kBlockMCta +
+                                 warp * kEpiBoxRows;
+            const int32_t col0 = tn * BN;
+            const uint32_t t_row = tmem_base + acc * BN + (static_cast<uint32_t>(warp * 32) << 16);
+#pragma unroll 1
+            for (int c = 0; c < BN / 64; ++c) {
+                uint32_t r0[32], r1[32];
+                tmem_ld_32x32b_x32(t_row + 64u * c, r0);
+                tmem_ld_32x32b_x32(t_row + 64u * c + 32u, r1);
+                tmem_ld_wait();
+                reg_fence(r0);
+                reg_fence(r1);
+                if (c == BN / 64 - 1) {
+                    // Every TMEM read of this accumulator is done: hand it back.
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (CG == 1) {
+                            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];"
+                                         :: "r"(bar_tempty + 8 * acc) : "memory");
+                        } else {
+                            mbar_arrive_cluster(mapa_shared(bar_tempty + 8 * acc, 0));
+                        }
+                    }
+                }
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    pk[i] = pack_rn<kBF16>(r0[2 * i], r0[2 * i + 1]);
+                    pk[16 + i] = pack_rn<kBF16>(r1[2 * i], r1[2 * i + 1]);
+                }
+                const uint32_t box = my_boxes + buf * kEpiBoxBytes;
+                if (p.store_mode == 1) {
+                    // The store issued from this box two chunks ago must have read it.
+                    if (lane == 0) bulk_wait_group_read<1>();
+                    __syncwarp();
+                }
+                // Row `lane` of the box: 16 B chunk j goes to chunk j ^ (row % 8),
+                // the 128-byte swizzle that the TMA store undoes. Each group of 8
+                // lanes covers 8 distinct chunk positions: no bank conflicts.
+                const uint32_t row_addr = box + lane * 128u;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4),
+                                 pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                const int32_t ccol = col0 + 64 * c;
+                if (p.store_mode == 1) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (row0 < p.M && ccol < p.N) tma_store_2d(&tmC, box, ccol, row0);
+                        bulk_commit_group();
+                    }
+                    buf ^= 1u;
+                } else {
+                    __syncwarp();
+                    const uint8_t* bx = smem + (box - base);
+#pragma unroll 1
+                    for (int rr = 0; rr < kEpiBoxRows; ++rr) {
+                        const int32_t row = row0 + rr;
+                        if (row >= p.M) break;
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) {
+                            const uint32_t cc = lane * 2u + q;          // column in the box
+                            const int32_t col = ccol + static_cast<int32_t>(cc);
+                            if (col < p.N) {
+                                const uint32_t off = rr * 128u +
+                                                     (((cc >> 3) ^ (static_cast<uint32_t>(rr) & 7u)) << 4) +
+                                                     ((cc & 7u) << 1);
+                                p.C[static_cast<int64_t>(row) * p.ldc + col] =
+                                    *reinterpret_cast<const uint16_t*>(bx + off);
+                            }
+                        }
+                    }
+                    __syncwarp();
+                }
+            }
+        }
+        if (lane == 0) bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    // ------------------------------------------------------------ teardown
+    __syncthreads();
+    if constexpr (CG == 2) cluster_sync();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc<CG>(tmem_base, Cfg::kTmemCols);
+    }
+#endif
+}
+
+}  // namespace hg

@@ -1,0 +1,18 @@
+// bf16 instantiations of the tcgen05 GEMM kernel.
+#include "tc_instances.cuh"
+
+namespace hg {
+
+cudaError_t launch_tc_bf16(int cta_group, int block_n, const CUtensorMap& a, const CUtensorMap& b,
+                           const CUtensorMap& c, const TcParams& p, int clusters,
+                           cudaStream_t stream) {
+    HG_TC_DISPATCH(true, launch(a, b, c, p, clusters, stream))
+    return cudaErrorInvalidValue;
+}
+
+int max_active_clusters_bf16(int cta_group, int block_n) {
+    HG_TC_DISPATCH(true, max_clusters())
+    return 0;
+}
+
+}  // namespace hg

@@ -1,0 +1,18 @@
+// fp16 instantiations of the tcgen05 GEMM kernel.
+#include "tc_instances.cuh"
+
+namespace hg {
+
+cudaError_t launch_tc_f16(int cta_group, int block_n, const CUtensorMap& a, const CUtensorMap& b,
+                          const CUtensorMap& c, const TcParams& p, int clusters,
+                          cudaStream_t stream) {
+    HG_TC_DISPATCH(false, launch(a, b, c, p, clusters, stream))
+    return cudaErrorInvalidValue;
+}
+
+int max_active_clusters_f16(int cta_group, int block_n) {
+    HG_TC_DISPATCH(false, max_clusters())
+    return 0;
+}
+
+}  // namespace hg

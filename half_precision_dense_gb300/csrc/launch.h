@@ -1,0 +1,38 @@
+// launch.h - internal interface between the C-ABI front end (hgemm_api.cu)
+// and the translation units that hold the kernel instantiations.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "hgemm_tc.cuh"
+
+namespace hg {
+
+// Launch the tcgen05 kernel for (cta_group, block_n) with `clusters` CTA
+// clusters on `stream`. Returns cudaErrorInvalidValue for an unknown pair.
+cudaError_t launch_tc_bf16(int cta_group, int block_n, const CUtensorMap& a, const CUtensorMap& b,
+                           const CUtensorMap& c, const TcParams& p, int clusters,
+                           cudaStream_t stream);
+cudaError_t launch_tc_f16(int cta_group, int block_n, const CUtensorMap& a, const CUtensorMap& b,
+                          const CUtensorMap& c, const TcParams& p, int clusters,
+                          cudaStream_t stream);
+
+// Most CTA clusters of the (cta_group, block_n) kernel that can be resident at
+// once on the current device (0 on error).
+int max_active_clusters_bf16(int cta_group, int block_n);
+int max_active_clusters_f16(int cta_group, int block_n);
+
+// Shared-memory ring depth and bytes of an instantiation (host constants).
+int tc_stages(int cta_group, int block_n);
+int tc_smem_bytes(int cta_group, int block_n);
+
+// Auxiliary kernels (hgemm_aux.cu).
+cudaError_t launch_repack(const uint16_t* src, int64_t rows, int64_t cols, uint16_t* dst,
+                          int64_t dst_ld, cudaStream_t stream);
+cudaError_t launch_zero(uint16_t* dst, int64_t count, cudaStream_t stream);
+// Device address of the status word on the current device (cached per device).
+cudaError_t status_word_ptr(unsigned long long** out);
+
+}  // namespace hg

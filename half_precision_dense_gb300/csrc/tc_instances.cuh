@@ -1,0 +1,76 @@
+// tc_instances.cuh - host launch helpers for the kernel instantiations of one
+// dtype. Included once by hgemm_tc_bf16.cu and once by hgemm_tc_f16.cu so the
+// two dtypes compile in parallel.
+#pragma once
+
+#include <mutex>
+
+#include "launch.h"
+
+namespace hg {
+
+template <int CG, int BN, bool kBF16>
+struct TcInstance {
+    using Cfg = TcCfg<CG, BN>;
+    static constexpr auto kernel() { return &hgemm_tc_kernel<CG, BN, kBF16>; }
+
+    // The dynamic shared-memory opt-in is per device; set it once per device.
+    static cudaError_t prepare() {
+        static std::mutex mu;
+        static uint64_t done_mask = 0;
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        std::lock_guard<std::mutex> lk(mu);
+        const uint64_t bit = 1ull << (dev & 63);
+        if (done_mask & bit) return cudaSuccess;
+        e = cudaFuncSetAttribute(kernel(), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Cfg::kSmemBytes);
+        if (e == cudaSuccess) done_mask |= bit;
+        return e;
+    }
+
+    static void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int clusters,
+                            cudaStream_t stream) {
+        cfg = cudaLaunchConfig_t{};
+        cfg.gridDim = dim3(static_cast<unsigned>(clusters * CG), 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+        cfg.stream = stream;
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = CG;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+
+    static cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                              const TcParams& p, int clusters, cudaStream_t stream) {
+        cudaError_t e = prepare();
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg;
+        cudaLaunchAttribute attr[1];
+        fill_config(cfg, attr, clusters, stream);
+        return cudaLaunchKernelEx(&cfg, kernel(), a, b, c, p);
+    }
+
+    static int max_clusters() {
+        if (prepare() != cudaSuccess) return 0;
+        cudaLaunchConfig_t cfg;
+        cudaLaunchAttribute attr[1];
+        fill_config(cfg, attr, 1, nullptr);
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kernel(), &cfg) != cudaSuccess) return 0;
+        return n;
+    }
+};
+
+#define HG_TC_DISPATCH(KBF16, CALL)                                                          \
+    if (cta_group == 1 && block_n == 64) return TcInstance<1, 64, KBF16>::CALL;              \
+    if (cta_group == 1 && block_n == 128) return TcInstance<1, 128, KBF16>::CALL;            \
+    if (cta_group == 1 && block_n == 256) return TcInstance<1, 256, KBF16>::CALL;            \
+    if (cta_group == 2 && block_n == 128) return TcInstance<2, 128, KBF16>::CALL;            \
+    if (cta_group == 2 && block_n == 256) return TcInstance<2, 256, KBF16>::CALL;
+
+}  // namespace hg

@@ -1,0 +1,176 @@
+/*
+ * hgemm.h - C ABI of the GB300 (sm_103a) dense half-precision GEMM library.
+ *
+ * The operation ("[CUDA 优化实战] hgemm - 超越 cuBLAS", section 1, the kernel
+ * signature hgemm_*_kernel(T *a, T *b, T *c, int m, int n, int k)):
+ *
+ *     C[i][j] = round_to_nearest_even( sum_k A[i][k] * B[k][j] )
+ *
+ *   A  M x K, row-major (element (i, k) at A[i*K + k])     fp16 or bf16
+ *   B  K x N, row-major (element (k, j) at B[k*N + j])     same dtype as A
+ *   C  M x N, row-major (element (i, j) at C[i*N + j])     same dtype as A
+ *
+ * Products are accumulated in fp32 (in tensor memory) and each C element is
+ * rounded once to the input dtype, as the page's mma.sync ... .f32 accumulate
+ * and __float22half2_rn / __float22bfloat162_rn write-back do. The order of the
+ * fp32 additions is unspecified, so results agree with an exact sum within the
+ * rounding of fp32 accumulation, not bit for bit.
+ *
+ * Edge shapes ("CUDA GEMM 优化实践笔记", the register-tiled kernel's
+ * bounds-checked tile loads fill out-of-range elements with zero): any M, N, K
+ * >= 0 is accepted; elements outside the matrices contribute nothing and no
+ * element outside C is written. M == 0 or N == 0 does nothing; K == 0 writes
+ * zeros to C.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named A, B, C are DEVICE pointers on the calling thread's
+ *     current CUDA device, dense and contiguous as above, owned by the caller.
+ *     The library never frees or retains them past the call's stream work.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream). Work is enqueued asynchronously; no entry point synchronises
+ *     the stream unless its comment says so.
+ *   - C must not overlap A or B (checked; HGEMM_ERR_INVALID_ARG).
+ *   - Return values are hgemm_status_t. On HGEMM_ERR_CUDA the CUDA error text
+ *     is available from hgemm_last_error() on the same thread.
+ *   - There is no CPU fallback: a device that is not compute capability 10.3
+ *     gives HGEMM_ERR_UNSUPPORTED_DEVICE.
+ */
+#ifndef HGEMM_H_
+#define HGEMM_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    HGEMM_F16 = 0,  /* IEEE binary16 */
+    HGEMM_BF16 = 1  /* bfloat16 */
+} hgemm_dtype_t;
+
+typedef enum {
+    HGEMM_OK = 0,
+    HGEMM_ERR_INVALID_ARG = 1,        /* null pointer with a non-empty shape, negative or too large
+                                         dimension, unknown dtype, C overlapping A or B, bad config */
+    HGEMM_ERR_UNSUPPORTED_DEVICE = 2, /* no CUDA device, or not compute capability 10.3 */
+    HGEMM_ERR_CUDA = 3,               /* a CUDA runtime/driver call failed (see hgemm_last_error) */
+    HGEMM_ERR_ALLOC = 4,              /* the stream-ordered workspace could not be allocated */
+    HGEMM_ERR_TIMEOUT = 5             /* reported by hgemm_get_device_status: a bounded wait in the
+                                         kernel ran out and the kernel returned early */
+} hgemm_status_t;
+
+/*
+ * hgemm - C = A.B as described above, enqueued on `stream`.
+ *
+ * A, B: device pointers to the operands (read only). C: device pointer to the
+ * result (written). M, N, K: dimensions, each in [0, 2^31 - 1]. dtype:
+ * HGEMM_F16 or HGEMM_BF16 (A, B and C share it).
+ *
+ * Operands whose row pitch (2K bytes for A, 2N bytes for B) or base address is
+ * not a multiple of 16 bytes are first copied into a 16-byte-pitched
+ * workspace taken from the device's stream-ordered allocator
+ * (cudaMallocAsync / cudaFreeAsync on `stream`); such a C is written with
+ * plain stores. Otherwise the call allocates nothing.
+ */
+hgemm_status_t hgemm(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                     hgemm_dtype_t dtype, void* stream);
+
+/*
+ * Launch configuration, for tuning sweeps and tests. Zero in any field means
+ * "let the planner choose".
+ *   cta_group:     1 = one CTA per 128-row tile; 2 = a CTA pair (cluster of 2)
+ *                  sharing a 256-row tile through tcgen05 cta_group::2.
+ *   block_n:       columns of C per tile: 64, 128 or 256.
+ *   group_m:       tile rows per raster group (L2 reuse), >= 1.
+ *   max_clusters:  cap on resident CTA clusters (forces more tiles per CTA).
+ *   store_mode:    1 = TMA tensor stores of C, 2 = plain per-element stores.
+ */
+typedef struct {
+    int32_t cta_group;
+    int32_t block_n;
+    int32_t group_m;
+    int32_t max_clusters;
+    int32_t store_mode;
+} hgemm_config_t;
+
+/* hgemm with an explicit configuration (cfg may be NULL = all zero). */
+hgemm_status_t hgemm_ex(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                        hgemm_dtype_t dtype, const hgemm_config_t* cfg, void* stream);
+
+/*
+ * hgemm_host - the same product for operands in HOST memory.
+ *
+ * hA, hB: host operands; hC: host result. dA, dB, dC: caller-owned device
+ * buffers of at least 2*M*K, 2*K*N and 2*M*N bytes. Enqueues on `stream`: the
+ * copies hA->dA and hB->dB, hgemm(dA, dB, dC, ...), and the copy dC->hC; then
+ * synchronises `stream`, so hC holds the result when it returns HGEMM_OK.
+ * Host buffers should be page-locked for the copies to overlap other work.
+ */
+hgemm_status_t hgemm_host(const void* hA, const void* hB, void* hC, int64_t M, int64_t N,
+                          int64_t K, hgemm_dtype_t dtype, void* dA, void* dB, void* dC,
+                          void* stream);
+
+/*
+ * Planner output for a problem (host-only; needs no GPU unless sm_count is 0,
+ * in which case the current device is queried).
+ */
+typedef struct {
+    int32_t cta_group;     /* 1 or 2 */
+    int32_t block_m;       /* rows of C per tile: 128 * cta_group */
+    int32_t block_n;       /* columns of C per tile */
+    int32_t block_k;       /* K per pipeline stage (64) */
+    int32_t stages;        /* depth of the shared-memory ring */
+    int32_t group_m;       /* raster group height in tiles */
+    int32_t tiles_m;       /* ceil(M / block_m) */
+    int32_t tiles_n;       /* ceil(N / block_n) */
+    int32_t num_tiles;     /* tiles_m * tiles_n */
+    int32_t grid_ctas;     /* CTAs launched (a multiple of cta_group) */
+    int32_t smem_bytes;    /* dynamic shared memory per CTA */
+    int32_t tmem_cols;     /* tensor-memory columns allocated per CTA */
+    int32_t repack_a;      /* 1 if A goes through the 16-byte-pitch workspace */
+    int32_t repack_b;      /* 1 if B does */
+    int32_t store_mode;    /* 1 = TMA stores, 2 = plain stores */
+} hgemm_plan_t;
+
+/* Fill *out with the plan hgemm_ex would use. sm_count > 0 plans for that many
+ * SMs without touching a device (pointers are then assumed 16-byte aligned). */
+hgemm_status_t hgemm_plan(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dtype,
+                          const hgemm_config_t* cfg, int32_t sm_count, hgemm_plan_t* out);
+
+/*
+ * Tile raster used by every CTA role (host copy of the device function).
+ * Tile index t in [0, tiles_m*tiles_n) maps to tile row *tm and column *tn:
+ * tiles are taken in groups of group_m tile rows; inside a group the row index
+ * varies fastest ("[CUDA 优化实战] hgemm - 超越 cuBLAS", section 1, grid
+ * swizzling with SWIZZLE_W: neighbouring CTAs share operand panels in L2).
+ */
+void hgemm_tile_coord(int32_t t, int32_t tiles_m, int32_t tiles_n, int32_t group_m,
+                      int32_t* tm, int32_t* tn);
+
+/*
+ * Device-side status word of `device`, set by a kernel whose bounded wait ran
+ * out (HGEMM_ERR_TIMEOUT) and left unchanged otherwise. Call after the stream
+ * that ran the GEMM has been synchronised. *info (may be NULL) receives the
+ * role and barrier that timed out. reset != 0 clears the word. Synchronous.
+ */
+hgemm_status_t hgemm_get_device_status(int32_t device, int32_t reset, uint32_t* info);
+
+/* Upper bound, in nanoseconds, on any single wait inside the kernels
+ * (default 2e9). Applies to launches made after the call, from any thread. */
+void hgemm_set_timeout_ns(uint64_t ns);
+
+/* Static text for a status code. */
+const char* hgemm_status_string(hgemm_status_t s);
+
+/* Text of the last CUDA error seen by an entry point on this thread ("" if none). */
+const char* hgemm_last_error(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int32_t hgemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HGEMM_H_ */

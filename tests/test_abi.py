@@ -1,0 +1,170 @@
+"""Host-side checks of the C-ABI library that need no GPU: it builds for
+sm_103a, loads, exports every entry point the header declares, validates
+arguments before touching a device, and plans tiles as documented."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from half_precision_dense_gb300 import binding
+from half_precision_dense_gb300 import build as hbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "hgemm.h")
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    hbuild.build()
+    return binding.load_library()
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w \t\*]*?\b(hgemm_?\w*)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ["hgemm", "hgemm_ex", "hgemm_host", "hgemm_plan", "hgemm_tile_coord",
+              "hgemm_get_device_status", "hgemm_set_timeout_ns", "hgemm_status_string",
+              "hgemm_last_error", "hgemm_version"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_library_is_sm103a_only():
+    # Every kernel is compiled for sm_103a and nothing else.
+    assert hbuild.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_version_and_strings(lib):
+    assert binding.version() == 100
+    for s, frag in [(0, "OK"), (1, "INVALID_ARG"), (2, "UNSUPPORTED_DEVICE"), (5, "TIMEOUT")]:
+        assert frag in binding.status_string(s)
+
+
+@pytest.mark.parametrize("args", [
+    (1, 1, 1, -1, 4, 4, 1),     # negative M
+    (1, 1, 1, 4, 4, 1 << 31, 1),  # K too large
+    (1, 1, 1, 4, 4, 4, 7),      # unknown dtype
+    (0, 16, 32, 4, 4, 4, 1),    # null A
+    (16, 16, 0, 4, 4, 4, 0),    # null C
+    (3, 16, 32, 4, 4, 4, 1),    # odd address
+])
+def test_invalid_arguments_rejected_without_device(lib, args):
+    a, b, c, M, N, K, dt = args
+    st = lib.hgemm(a, b, c, M, N, K, dt, None)
+    assert st == 1, binding.STATUS_NAMES.get(st)
+
+
+def test_overlap_rejected(lib):
+    base = 1 << 20
+    # C = [base, base + 2*4*4) overlaps A = [base + 16, ...)
+    assert lib.hgemm(base + 16, base + 4096, base, 4, 4, 4, 1, None) == 1
+
+
+def test_empty_shapes_are_noops(lib):
+    assert lib.hgemm(None, None, None, 0, 5, 3, 1, None) == 0
+    assert lib.hgemm(None, None, None, 5, 0, 3, 0, None) == 0
+
+
+def test_no_cpu_fallback(lib):
+    # A well-formed call on a machine without a GB300 must fail loudly.
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    st = lib.hgemm(1 << 20, 2 << 20, 3 << 20, 64, 64, 64, 1, None)
+    assert st == 2
+
+
+def test_tile_coord_is_a_bijection(lib):
+    for tiles_m, tiles_n, group in [(16, 16, 8), (7, 5, 3), (1, 32, 8), (64, 56, 8), (5, 9, 16)]:
+        seen = set()
+        for t in range(tiles_m * tiles_n):
+            tm, tn = binding.tile_coord(t, tiles_m, tiles_n, group)
+            assert 0 <= tm < tiles_m and 0 <= tn < tiles_n
+            seen.add((tm, tn))
+        assert len(seen) == tiles_m * tiles_n
+
+
+def test_tile_coord_groups_rows_first(lib):
+    # inside a group the row index varies fastest
+    coords = [binding.tile_coord(t, 16, 4, 8) for t in range(10)]
+    assert coords[:8] == [(r, 0) for r in range(8)]
+    assert coords[8:10] == [(0, 1), (1, 1)]
+
+
+def test_plan_shapes(lib):
+    p = binding.plan(4096, 4096, 4096, "bf16", sm_count=148)
+    assert p["cta_group"] in (1, 2) and p["block_n"] in (64, 128, 256)
+    assert p["tiles_m"] * p["block_m"] >= 4096 and p["tiles_n"] * p["block_n"] >= 4096
+    assert p["grid_ctas"] % p["cta_group"] == 0 and p["grid_ctas"] <= 148
+    assert p["tmem_cols"] == 2 * p["block_n"]
+    assert p["smem_bytes"] <= 232448 and p["stages"] >= 2
+    assert p["repack_a"] == 0 and p["repack_b"] == 0 and p["store_mode"] == 1
+    t = binding.plan(1000, 4095, 4104, "bf16", sm_count=148)
+    assert t["repack_b"] == 1 and t["repack_a"] == 0 and t["store_mode"] == 2
+    forced = binding.plan(512, 512, 512, "f16",
+                          binding.Config(cta_group=1, block_n=64, max_clusters=3), sm_count=148)
+    assert (forced["cta_group"], forced["block_n"], forced["grid_ctas"]) == (1, 64, 3)
+    with pytest.raises(binding.HgemmError):
+        binding.plan(512, 512, 512, "f16", binding.Config(cta_group=2, block_n=64), sm_count=148)
+
+
+def test_plan_skinny_prefers_narrow_tiles(lib):
+    p = binding.plan(128, 8192, 8192, "bf16", sm_count=148)
+    assert p["block_m"] == 128  # one tile row: no half-empty CTA pairs
+
+
+# --- the epilogue's shared-memory staging layout, modelled on the CPU -------
+
+def bank_of(byte_addr):
+    return (byte_addr // 4) % 32
+
+
+def test_page_swizzle_c_example_is_conflict_free():
+    """The page's SWIZZLE_C worked example: warp 0's 32 lanes write 4 bytes each
+    to 32 distinct banks of the 128-wide half-precision tile."""
+    rows = {}
+    for ln in open(os.path.join(GOLDEN, "swizzle_c_warp0.txt"), encoding="utf-8"):
+        if ln.strip() and not ln.startswith("#"):
+            k, *vals = ln.split()
+            rows[k] = [int(v) for v in vals]
+    banks = []
+    for r, c in zip(rows["row"], rows["col"]):
+        sc = c ^ ((r & 7) << 3)
+        banks.append(bank_of((r * 128 + sc) * 2))
+    assert sorted(banks) == list(range(32))
+    unswizzled = {bank_of((r * 128 + c) * 2) for r, c in zip(rows["row"], rows["col"])}
+    assert len(unswizzled) < 32  # the 8-way conflict the page describes
+
+
+def test_epilogue_staging_layout_is_conflict_free_and_tma_compatible():
+    """Our staging box: lane l owns row l (128 B); its 16-byte chunk j goes to
+    chunk j ^ (l % 8). Each 8-lane phase of a 16-byte store then covers all 32
+    banks once, and the layout is exactly the TMA 128-byte swizzle (chunk bits
+    4-6 of the address XOR row bits 7-9)."""
+    for j in range(8):
+        for phase in range(4):
+            lanes = range(8 * phase, 8 * phase + 8)
+            banks = []
+            for l in lanes:
+                addr = l * 128 + ((j ^ (l & 7)) << 4)
+                banks.extend(bank_of(addr + 4 * w) for w in range(4))
+            assert sorted(banks) == list(range(32))
+    for l in range(32):
+        for j in range(8):
+            addr = l * 128 + ((j ^ (l & 7)) << 4)
+            logical = l * 128 + j * 16
+            tma = logical ^ (((logical >> 7) & 7) << 4)
+            assert addr == tma

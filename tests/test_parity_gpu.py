@@ -1,0 +1,265 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs, elementwise, within the stated tolerance; bit-exact where
+every product and sum is exact. Shapes span several tiles and ragged tails,
+every kernel configuration, the persistent loop (few CTAs, many tiles each),
+unaligned pitches, the degenerate shapes, and every workload at full size
+(sampled rows and columns where the full oracle would be too slow)."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from half_precision_dense_gb300 import binding as hg
+from half_precision_dense_gb300 import inputs
+from tests._check import compare
+
+pytestmark = pytest.mark.gpu
+
+CONFIGS = [
+    hg.Config(cta_group=1, block_n=64),
+    hg.Config(cta_group=1, block_n=128),
+    hg.Config(cta_group=1, block_n=256),
+    hg.Config(cta_group=2, block_n=128),
+    hg.Config(cta_group=2, block_n=256),
+]
+CFG_IDS = ["cg1_n64", "cg1_n128", "cg1_n256", "cg2_n128", "cg2_n256"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from half_precision_dense_gb300 import build as hbuild
+    hbuild.build()
+    hg.load_library()
+    hg.get_device_status(0, reset=True)
+    yield
+    st, info = hg.get_device_status(0)
+    assert st == 0, f"a kernel reported status {st} (info {info:#x})"
+
+
+def run_gpu(A, B, dtype, config=None, guard=0):
+    """C through the C ABI; with guard > 0 the output sits between canary bands."""
+    M, K = A.shape
+    N = B.shape[1]
+    dA = A.cuda()
+    dB = B.cuda()
+    t = inputs.TORCH_DTYPES[dtype]
+    buf = torch.full((2 * guard + M * N,), -7.0, dtype=t, device="cuda")
+    C = buf[guard:guard + M * N]
+    hg.hgemm_ex(dA, dB, C, M, N, K, dtype, config)
+    torch.cuda.synchronize()
+    if guard:
+        canary = torch.full((guard,), -7.0, dtype=t, device="cuda")
+        assert torch.equal(buf[:guard], canary) and torch.equal(buf[guard + M * N:], canary), \
+            "write outside C"
+    return inputs.bits(C.view(M, N).cpu())
+
+
+def check_full(A, B, dtype, config=None, guard=64):
+    a, b = inputs.bits(A), inputs.bits(B)
+    got = run_gpu(A, B, dtype, config, guard)
+    ref64 = oracle.gemm_f64(a, b, dtype)
+    ref = oracle.round_rne(ref64, dtype)
+    r = compare(got, ref, ref64, dtype, A.shape[1])
+    assert r["ok"], r
+    return got, ref
+
+
+def operands(M, N, K, dtype, seed, dist="uniform", sigma=1.0):
+    return (inputs.generate((M, K), dtype, seed, 0, dist, sigma),
+            inputs.generate((K, N), dtype, seed, 1, dist, sigma))
+
+
+def int_operands(M, N, K, dtype, seed):
+    rng = np.random.default_rng(seed)
+    t = inputs.TORCH_DTYPES[dtype]
+    Ai = rng.integers(-3, 4, (M, K)).astype(np.float32)
+    Bi = rng.integers(-3, 4, (K, N)).astype(np.float32)
+    return torch.from_numpy(Ai).to(t), torch.from_numpy(Bi).to(t)
+
+
+# ------------------------------------------------------------ exact cases
+
+@pytest.mark.parametrize("cfg", CONFIGS, ids=CFG_IDS)
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_small_integers_bit_exact(cfg, dtype):
+    # |C| <= 9 * 28 = 252: exact in fp32 accumulation and in both output types
+    A, B = int_operands(300, 520, 28, dtype, 11)
+    got = run_gpu(A, B, dtype, cfg, guard=64)
+    assert np.array_equal(got, oracle.gemm(inputs.bits(A), inputs.bits(B), dtype))
+
+
+@pytest.mark.parametrize("cfg", CONFIGS, ids=CFG_IDS)
+def test_identity_and_unit_vectors(cfg):
+    dtype = "bf16"
+    _, B = operands(384, 320, 384, dtype, 21)
+    eye = torch.eye(384, dtype=torch.bfloat16)
+    got = run_gpu(eye, B, dtype, cfg)
+    assert np.array_equal(got, inputs.bits(B))          # I . B = B exactly
+    A, _ = operands(200, 1, 192, dtype, 22)
+    eyeK = torch.eye(192, dtype=torch.bfloat16)
+    got = run_gpu(A, eyeK, dtype, cfg)
+    assert np.array_equal(got, inputs.bits(A))          # A . I = A exactly
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_all_ones_gives_k(dtype):
+    K = 256 if dtype == "bf16" else 2048
+    t = inputs.TORCH_DTYPES[dtype]
+    A = torch.ones((256, K), dtype=t)
+    B = torch.ones((K, 384), dtype=t)
+    got = run_gpu(A, B, dtype)
+    assert np.all(got == inputs.bits(torch.tensor([float(K)], dtype=t))[0])
+
+
+def test_transpose_identity():
+    A, B = operands(320, 448, 512, "bf16", 23)
+    c1 = run_gpu(A, B, "bf16")
+    c2 = run_gpu(B.t().contiguous(), A.t().contiguous(), "bf16")
+    r = compare(c2, np.ascontiguousarray(c1.T), oracle.gemm_f64(inputs.bits(A), inputs.bits(B), "bf16").T,
+                "bf16", 512)
+    assert r["ok"], r
+
+
+# ----------------------------------------------------- random shapes, tails
+
+SHAPES = [(256, 256, 256), (128, 64, 64), (1, 1, 1), (7, 9, 11), (129, 65, 63), (255, 257, 130),
+          (300, 520, 1000), (511, 383, 129), (640, 768, 576), (1000, 1000, 72)]
+
+
+@pytest.mark.parametrize("cfg", CONFIGS, ids=CFG_IDS)
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_random_shapes(cfg, shape):
+    M, N, K = shape
+    A, B = operands(M, N, K, "bf16", 5)
+    check_full(A, B, "bf16", cfg)
+
+
+@pytest.mark.parametrize("cfg", CONFIGS, ids=CFG_IDS)
+@pytest.mark.parametrize("max_clusters", [1, 3])
+def test_persistent_loop_many_tiles_per_cta(cfg, max_clusters):
+    # few CTAs walk many tiles: ring phases and both accumulators wrap many times
+    c = hg.Config(cfg.cta_group, cfg.block_n, 0, max_clusters, 0)
+    A, B = operands(1024, 1280, 320, "f16", 6)
+    check_full(A, B, "f16", c)
+
+
+@pytest.mark.parametrize("group_m", [1, 2, 5, 64])
+def test_raster_groups(group_m):
+    A, B = operands(1536, 1024, 256, "bf16", 7)
+    check_full(A, B, "bf16", hg.Config(cta_group=2, block_n=128, group_m=group_m))
+
+
+def test_plain_store_mode_matches():
+    A, B = operands(700, 520, 300, "bf16", 8)
+    check_full(A, B, "bf16", hg.Config(store_mode=2))
+
+
+@pytest.mark.parametrize("shape", [(300, 517, 264), (129, 4095, 257), (64, 100, 1001), (33, 7, 5)])
+def test_unaligned_pitches(shape):
+    # N or K not a multiple of 8: repacked operand and/or plain stores of C
+    M, N, K = shape
+    A, B = operands(M, N, K, "bf16", 9)
+    check_full(A, B, "bf16")
+
+
+def test_unaligned_base_pointers():
+    M, N, K = 200, 264, 136
+    A, B = operands(M, N, K, "f16", 10)
+    dA = torch.empty(M * K + 1, dtype=torch.float16, device="cuda")[1:]
+    dB = torch.empty(K * N + 3, dtype=torch.float16, device="cuda")[3:]
+    dC = torch.zeros(M * N + 5, dtype=torch.float16, device="cuda")[5:]
+    dA.copy_(A.reshape(-1))
+    dB.copy_(B.reshape(-1))
+    hg.hgemm(dA, dB, dC, M, N, K, "f16")
+    torch.cuda.synchronize()
+    got = inputs.bits(dC.view(M, N).cpu())
+    a, b = inputs.bits(A), inputs.bits(B)
+    ref64 = oracle.gemm_f64(a, b, "f16")
+    r = compare(got, oracle.round_rne(ref64, "f16"), ref64, "f16", K)
+    assert r["ok"], r
+
+
+def test_k_zero_writes_zeros_and_empty_is_noop():
+    C = torch.full((37, 41), 3.0, dtype=torch.bfloat16, device="cuda")
+    a = torch.empty((37, 0), dtype=torch.bfloat16, device="cuda")
+    b = torch.empty((0, 41), dtype=torch.bfloat16, device="cuda")
+    hg.hgemm(a, b, C, 37, 41, 0, "bf16")
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(C).item() == 0
+    D = torch.full((4, 4), 3.0, dtype=torch.bfloat16, device="cuda")
+    hg.hgemm(None, None, D, 0, 4, 4, "bf16")
+    torch.cuda.synchronize()
+    assert torch.all(D == 3.0)
+
+
+def test_overlap_rejected_on_device():
+    X = torch.zeros(4096, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(hg.HgemmError):
+        hg.hgemm(X[:1024], X[1024:2048], X[512:1536], 32, 32, 32, "bf16")
+
+
+def test_host_entry_point():
+    M, N, K = 512, 384, 256
+    A, B = operands(M, N, K, "bf16", 12)
+    hA, hB = A.pin_memory(), B.pin_memory()
+    hC = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    dA = torch.empty_like(A, device="cuda")
+    dB = torch.empty_like(B, device="cuda")
+    dC = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    hg.hgemm_host(hA, hB, hC, M, N, K, "bf16", dA, dB, dC, torch.cuda.current_stream())
+    a, b = inputs.bits(A), inputs.bits(B)
+    ref64 = oracle.gemm_f64(a, b, "bf16")
+    r = compare(inputs.bits(hC), oracle.round_rne(ref64, "bf16"), ref64, "bf16", K)
+    assert r["ok"], r
+
+
+def test_matmul_wrapper_and_stream():
+    A, B = operands(256, 192, 320, "f16", 13)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        C = hg.matmul(A.cuda(), B.cuda())
+    s.synchronize()
+    a, b = inputs.bits(A), inputs.bits(B)
+    ref64 = oracle.gemm_f64(a, b, "f16")
+    r = compare(inputs.bits(C.cpu()), oracle.round_rne(ref64, "f16"), ref64, "f16", 320)
+    assert r["ok"], r
+
+
+# --------------------------------------------------------- the workloads
+
+FULL = ["square256_bf16", "square4096_f16", "square4096_bf16", "skinny_bf16", "tails_bf16",
+        "shortk_bf16"]
+SAMPLED = ["square8192_bf16", "mlp_up_bf16", "mlp_down_bf16"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_workload_full_oracle(name):
+    A, B, (M, N, K, dtype) = inputs.workload_operands(name)
+    check_full(A, B, dtype, guard=256)
+
+
+def sample_indices(n, seed):
+    rng = np.random.default_rng(seed)
+    fixed = [0, 127, 128, 255, 256, n - 1]
+    return np.unique(np.concatenate([rng.integers(0, n, 32), [i for i in fixed if i < n]]))
+
+
+@pytest.mark.parametrize("name", SAMPLED)
+def test_workload_sampled_rows_and_cols(name):
+    A, B, (M, N, K, dtype) = inputs.workload_operands(name)
+    got = run_gpu(A, B, dtype, guard=256)
+    a, b = inputs.bits(A), inputs.bits(B)
+    rows = sample_indices(M, 1)
+    cols = sample_indices(N, 2)
+    ref_r, ref64_r = oracle.gemm_rows(a, b, dtype, rows)
+    r = compare(got[rows], ref_r, ref64_r, dtype, K)
+    assert r["ok"], ("rows", r)
+    ref_c, ref64_c = oracle.gemm_cols(a, b, dtype, cols)
+    r = compare(got[:, cols], ref_c, ref64_c, dtype, K)
+    assert r["ok"], ("cols", r)
+    # a property at any size: every element is finite
+    v = torch.from_numpy(got.view(np.int16).copy()).view(inputs.TORCH_DTYPES[dtype]).double()
+    assert torch.isfinite(v).all()
