@@ -1,0 +1,431 @@
+"""Benchmark of the dense half-precision GEMM (TFLOP/s at M = N = K = 4096).
+
+One step = the 4096^3 GEMM once in bf16 and once in fp16 (A, B row-major,
+entries U[-1, 1) from seed 1, fp32 accumulation, C in the input dtype), each
+through the C ABI with operands resident in HBM. L2 is flushed (a 256 MiB
+device write) before every GEMM; only the GEMM is inside the CUDA-event
+interval. `value` = 2MNK x GEMMs / summed GEMM time, over all ranks.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+`--impl reference` times the CPU oracle instead (the only other place this
+file runs the oracle), on a bounded row sample of the same workload.
+For N > 1 (torchrun), every rank runs its own independent problem (no
+collective on the data path; the barrier and the max over ranks are timing
+only): weak scaling.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+# BLAS threads for the oracle legs: every core this process may use.
+_CORES = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+os.environ.setdefault("OPENBLAS_NUM_THREADS", str(_CORES))
+os.environ.setdefault("OMP_NUM_THREADS", str(_CORES))
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fp16/bf16 GEMM TFLOP/s at M=N=K=4096; % of GB300 dense tensor-core peak"
+UNIT = "TFLOP/s"
+L2_FLUSH_BYTES = 256 << 20
+
+# name -> list of (M, N, K, dtype, dist, sigma, seed) GEMMs making up one step
+WORKLOADS = {
+    "square4096": [(4096, 4096, 4096, "bf16", "uniform", 1.0, 1),
+                   (4096, 4096, 4096, "f16", "uniform", 1.0, 1)],
+    "square8192_bf16": [(8192, 8192, 8192, "bf16", "normal", 1.0, 2)],
+    "mlp_up_bf16": [(16384, 14336, 4096, "bf16", "normal", 0.02, 3)],
+    "mlp_down_bf16": [(16384, 4096, 14336, "bf16", "normal", 0.02, 3)],
+    "mlp_bf16": [(16384, 14336, 4096, "bf16", "normal", 0.02, 3),
+                 (16384, 4096, 14336, "bf16", "normal", 0.02, 3)],
+    "skinny_bf16": [(128, 8192, 8192, "bf16", "uniform", 1.0, 4)],
+    "tails_bf16": [(1000, 4095, 4104, "bf16", "uniform", 1.0, 4)],
+    "shortk_bf16": [(4096, 4096, 64, "bf16", "uniform", 1.0, 4)],
+    "square256_bf16": [(256, 256, 256, "bf16", "uniform", 1.0, 0)],
+}
+DESCRIPTIONS = {
+    "square4096": "GEMM M=N=K=4096, once bf16 and once fp16, A/B row-major, U[-1,1) seed 1",
+}
+
+
+def flops(M, N, K):
+    return 2 * M * N * K
+
+
+def hbm_bytes(M, N, K):
+    return 2 * (M * K + K * N + M * N)
+
+
+def read_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.dev)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.samples = []
+        if self.proc is None:
+            return False
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append(parts)
+        return False
+
+    def summary(self):
+        if not getattr(self, "samples", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        sm = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        mx = [float(s[2]) for s in self.samples if s[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in self.samples:
+            for name, v in zip(names, s[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        pw = [float(s[3]) for s in self.samples if s[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(self.samples),
+                "power_w_max": max(pw) if pw else None}
+
+
+# --------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    from half_precision_dense_gb300 import binding as hg
+    from half_precision_dense_gb300 import build as hbuild
+    from half_precision_dense_gb300 import inputs
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if rank == 0 or not os.path.exists(hbuild.LIB_PATH):
+        hbuild.build()
+    if world > 1:
+        torch.distributed.barrier()
+    hg.load_library()
+
+    gemms = WORKLOADS[args.workload]
+    ops = []
+    for (M, N, K, dt, dist, sigma, seed) in gemms:
+        A = inputs.generate((M, K), dt, seed, 0, dist, sigma)
+        B = inputs.generate((K, N), dt, seed, 1, dist, sigma)
+        ops.append(dict(M=M, N=N, K=K, dt=dt, hA=A, hB=B, A=A.to(dev), B=B.to(dev),
+                        C=torch.empty((M, N), dtype=inputs.TORCH_DTYPES[dt], device=dev)))
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def one_gemm(o):
+        hg.hgemm(o["A"], o["B"], o["C"], o["M"], o["N"], o["K"], o["dt"], stream)
+
+    for _ in range(args.warmup):
+        for o in ops:
+            flush.zero_()
+            one_gemm(o)
+    torch.cuda.synchronize(dev)
+    hg.get_device_status(local_rank, reset=True)
+
+    n_ev = args.steps * len(ops)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local_rank) as clk:
+        wall0 = time.perf_counter()
+        i = 0
+        for _ in range(args.steps):
+            for o in ops:
+                flush.zero_()
+                starts[i].record(stream)
+                one_gemm(o)
+                ends[i].record(stream)
+                i += 1
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - wall0
+    if world > 1:
+        torch.distributed.barrier()
+    times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(times_ms)
+    st, info = hg.get_device_status(local_rank)
+    if st != 0:
+        raise RuntimeError(f"kernel status {st} info {info:#x}")
+
+    # per-GEMM-kind averages (the dominant kernel is the GEMM kernel itself)
+    per_kind = {}
+    for j, o in enumerate(ops):
+        ts = times_ms[j::len(ops)]
+        per_kind[f"{o['dt']}_{o['M']}x{o['N']}x{o['K']}"] = {
+            "ms": statistics.mean(ts),
+            "tflops": flops(o["M"], o["N"], o["K"]) / (statistics.mean(ts) * 1e-3) / 1e12}
+    step_flops = sum(flops(o["M"], o["N"], o["K"]) for o in ops)
+
+    # e2e: host operands -> device -> GEMM -> host result, through hgemm_host
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    pinned = []
+    for o in ops:
+        pinned.append((o["hA"].pin_memory(), o["hB"].pin_memory(),
+                       torch.empty((o["M"], o["N"]), dtype=o["C"].dtype).pin_memory()))
+    for o, (pa, pb, pc) in zip(ops, pinned):   # warm the copy path
+        hg.hgemm_host(pa, pb, pc, o["M"], o["N"], o["K"], o["dt"], o["A"], o["B"], o["C"], stream)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    e0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        for o, (pa, pb, pc) in zip(ops, pinned):
+            hg.hgemm_host(pa, pb, pc, o["M"], o["N"], o["K"], o["dt"], o["A"], o["B"], o["C"], stream)
+    torch.cuda.synchronize(dev)
+    e2e_s = time.perf_counter() - e0
+
+    # max over ranks
+    import torch.distributed as tdist
+    vals = torch.tensor([total_ms, e2e_s, wall], dtype=torch.float64, device=dev)
+    if world > 1:
+        tdist.all_reduce(vals, op=tdist.ReduceOp.MAX)
+    total_ms, e2e_s, wall = vals.tolist()
+    if rank != 0:
+        return None
+
+    peaks, peak_src = read_peaks()
+    value = world * args.steps * step_flops / (total_ms * 1e-3) / 1e12
+    avg_launch_ms = total_ms / n_ev
+    achieved = step_flops / len(ops) / (avg_launch_ms * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    clocks = clk.summary()
+    e2e_value = world * e2e_steps * step_flops / e2e_s / 1e12
+    h2d = sum(2 * (o["M"] * o["K"] + o["K"] * o["N"]) for o in ops)
+    d2h = sum(2 * o["M"] * o["N"] for o in ops)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "+".join(sorted({o["dt"] for o in ops})) + " in, f32 accumulate",
+        "data": "synthetic (seeded SplitMix64 inputs)",
+        "config": {
+            "workload": DESCRIPTIONS.get(args.workload, args.workload),
+            "gemms_per_step": len(ops),
+            "shapes": [[o["M"], o["N"], o["K"], o["dt"]] for o in ops],
+            "l2": f"flushed before every GEMM ({L2_FLUSH_BYTES >> 20} MiB device write, outside the timed interval)",
+            "parallelism": f"independent problem per GPU x{world}" if world > 1 else "single GPU",
+        },
+        "pct_of_peak": round(100.0 * value / world / peak, 2),
+        "per_gemm": {k: {"ms": round(v["ms"], 5), "tflops": round(v["tflops"], 1)} for k, v in per_kind.items()},
+        "roofline": {
+            "bound": "tensor",
+            "kernel": "hg::hgemm_tc_kernel",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_source": f"{peak_src} bf16 dense (cuBLAS burst); fp16 has the same nominal rate (ratio 1)",
+            "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": None,
+            "algorithmic_bytes_per_launch": hbm_bytes(ops[0]["M"], ops[0]["N"], ops[0]["K"]),
+        },
+        "clocks": clocks,
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "path": "hgemm_host: pinned host A,B -> device, GEMM, C -> pinned host, per GEMM"},
+        "gpu_launches": n_ev,
+        "wall_s_timed_region": round(wall, 4),
+    }
+    if args.traffic_file and os.path.exists(args.traffic_file):
+        try:
+            with open(args.traffic_file) as f:
+                tr = json.load(f)
+            line["roofline"]["traffic"] = tr.get("dram_bytes_per_launch")
+            line["roofline"]["traffic_source"] = tr.get("source")
+        except (OSError, ValueError):
+            pass
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_budget)
+    return line
+
+
+# ---------------------------------------------------- oracle (CPU) timing
+def _oracle_sample(workload, rows, cols):
+    """A sampled sub-problem of each GEMM of the workload: the C block at
+    `rows` evenly spaced rows and `cols` evenly spaced columns, i.e. the rows
+    of A and the columns of B it needs (uint16 bit patterns)."""
+    import numpy as np
+
+    from half_precision_dense_gb300 import inputs
+
+    out = []
+    for (M, N, K, dt, dist, sigma, seed) in WORKLOADS[workload]:
+        A = inputs.bits(inputs.generate((M, K), dt, seed, 0, dist, sigma))
+        B = inputs.bits(inputs.generate((K, N), dt, seed, 1, dist, sigma))
+        ri = np.linspace(0, M - 1, min(rows, M)).astype(np.int64)
+        ci = np.linspace(0, N - 1, min(cols, N)).astype(np.int64)
+        out.append((np.ascontiguousarray(A[ri]), np.ascontiguousarray(B[:, ci]), dt, K))
+    return out
+
+
+def _oracle_step(sample):
+    import oracle
+
+    f = 0
+    for (a, b, dt, K) in sample:
+        oracle.gemm(a, b, dt)
+        f += flops(a.shape[0], b.shape[1], K)
+    return f
+
+
+def _calibrated_sample(workload, seconds_per_step):
+    side = 256
+    for _ in range(3):
+        sample = _oracle_sample(workload, side, side)
+        t0 = time.perf_counter()
+        _oracle_step(sample)
+        el = max(time.perf_counter() - t0, 1e-6)
+        new = int(side * (seconds_per_step / el) ** 0.5)
+        new = max(16, min(4096, new))
+        if abs(new - side) <= side // 8:
+            break
+        side = new
+    return _oracle_sample(workload, side, side), side
+
+
+def _sample_desc(side, workload):
+    return (f"each step: the {side} x {side} block of C at evenly spaced rows and columns of every "
+            f"GEMM of {workload}, computed by the CPU oracle (numpy fp64 product + bit-level RNE)")
+
+
+def cpu_baseline(workload, budget_s=15.0):
+    sample, side = _calibrated_sample(workload, 1.0)
+    done = 0
+    reps = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < budget_s and reps < 200:
+        done += _oracle_step(sample)
+        reps += 1
+    el = time.perf_counter() - t0
+    return {"value": round(done / el / 1e12, 6), "unit": UNIT, "cores": _CORES, "kind": "oracle",
+            "sample": _sample_desc(side, workload) + f"; {reps} steps in {el:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    budget = min(150.0, max(20.0, 0.5 * (args.steps + args.warmup)))
+    sample, side = _calibrated_sample(args.workload, budget / (args.steps + args.warmup))
+    for _ in range(args.warmup):
+        _oracle_step(sample)
+    t0 = time.perf_counter()
+    f = 0
+    for _ in range(args.steps):
+        f += _oracle_step(sample)
+    el = time.perf_counter() - t0
+    value = f / el / 1e12
+    desc = _sample_desc(side, args.workload)
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 6),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1e3 * el / args.steps, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64 (oracle)",
+        "data": "synthetic (seeded SplitMix64 inputs)",
+        "config": {"workload": DESCRIPTIONS.get(args.workload, args.workload), "sample": desc},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": _CORES, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="square4096")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic-file", default=os.path.join(ROOT, "profiles", "traffic_square4096.json"))
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        if world == 1 and args.gpus > 1:
+            ap.error("for --gpus N > 1 launch under torch.distributed.run with N processes")
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(local_rank)
+        tdist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        line = run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as tdist
+            tdist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()
