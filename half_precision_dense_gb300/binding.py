@@ -74,6 +74,10 @@ def load_library():
         lib.hgemm.restype = ctypes.c_int
         lib.hgemm_ex.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.c_int, ctypes.POINTER(_Config), vp]
         lib.hgemm_ex.restype = ctypes.c_int
+        lib.hgemm_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.c_int, vp]
+        lib.hgemm_noalloc.restype = ctypes.c_int
+        lib.hgemm_noalloc_scratch_bytes.argtypes = []
+        lib.hgemm_noalloc_scratch_bytes.restype = ctypes.c_uint64
         lib.hgemm_host.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.c_int, vp, vp, vp, vp]
         lib.hgemm_host.restype = ctypes.c_int
         lib.hgemm_plan.argtypes = [i64, i64, i64, ctypes.c_int, ctypes.POINTER(_Config), i32,
@@ -132,6 +136,13 @@ def hgemm(A, B, C, M: int, N: int, K: int, dtype, stream=None) -> None:
     """C = A.B (device pointers or CUDA tensors), enqueued on ``stream``."""
     lib = load_library()
     _check(lib.hgemm(_ptr(A), _ptr(B), _ptr(C), M, N, K, _dtype_code(dtype), _stream(stream)))
+
+
+def hgemm_noalloc(A, B, C, M: int, N: int, K: int, dtype, stream=None) -> None:
+    """hgemm for callers that cannot allocate: any workspace comes from the
+    library's fixed scratch array (see include/hgemm.h)."""
+    lib = load_library()
+    _check(lib.hgemm_noalloc(_ptr(A), _ptr(B), _ptr(C), M, N, K, _dtype_code(dtype), _stream(stream)))
 
 
 def hgemm_ex(A, B, C, M: int, N: int, K: int, dtype, config: Config | None = None,

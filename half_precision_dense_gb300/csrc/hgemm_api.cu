@@ -237,8 +237,11 @@ hgemm_status_t check_args(const void* A, const void* B, void* C, int64_t M, int6
     return HGEMM_OK;
 }
 
+// `scratch` (nullptr: none) is caller-provided device memory of `scratch_bytes`
+// used instead of the stream-ordered allocator for the repack workspace.
 hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
-                   hgemm_dtype_t dtype, const hgemm_config_t* cfg, cudaStream_t stream) {
+                   hgemm_dtype_t dtype, const hgemm_config_t* cfg, cudaStream_t stream,
+                   void* scratch = nullptr, size_t scratch_bytes = 0) {
     t_last_error.clear();
     hgemm_status_t st = check_args(A, B, C, M, N, K, dtype);
     if (st != HGEMM_OK || M == 0 || N == 0) return st;
@@ -274,7 +277,16 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
         const int64_t bytes_a = pl.repack_a ? 2 * M * lda : 0;
         const int64_t bytes_b = pl.repack_b ? 2 * K * ldb : 0;
         const int64_t off_b = (bytes_a + 255) / 256 * 256;
-        if ((e = cudaMallocAsync(&work, static_cast<size_t>(off_b + bytes_b), stream)) != cudaSuccess) {
+        const size_t need = static_cast<size_t>(off_b + bytes_b);
+        if (scratch) {
+            if (need > scratch_bytes) {
+                t_last_error = "this shape needs " + std::to_string(need) +
+                               " bytes of repack workspace; the scratch holds " +
+                               std::to_string(scratch_bytes);
+                return HGEMM_ERR_INVALID_ARG;
+            }
+            work = scratch;
+        } else if ((e = cudaMallocAsync(&work, need, stream)) != cudaSuccess) {
             cuda_fail(e, "cudaMallocAsync (repack workspace)");
             return HGEMM_ERR_ALLOC;
         }
@@ -282,7 +294,7 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
         if (pl.repack_a) {
             if ((e = hg::launch_repack(static_cast<const uint16_t*>(A), M, K,
                                        reinterpret_cast<uint16_t*>(w8), lda, stream)) != cudaSuccess) {
-                cudaFreeAsync(work, stream);
+                if (work != scratch) cudaFreeAsync(work, stream);
                 return cuda_fail(e, "repack A");
             }
             a_use = w8;
@@ -290,7 +302,7 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
         if (pl.repack_b) {
             if ((e = hg::launch_repack(static_cast<const uint16_t*>(B), K, N,
                                        reinterpret_cast<uint16_t*>(w8 + off_b), ldb, stream)) != cudaSuccess) {
-                cudaFreeAsync(work, stream);
+                if (work != scratch) cudaFreeAsync(work, stream);
                 return cuda_fail(e, "repack B");
             }
             b_use = w8 + off_b;
@@ -303,7 +315,7 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
         (st = encode_2d(&tb, dtype, b_use, K, N, ldb, 64, hg::kBlockK)) != HGEMM_OK ||
         (pl.store_mode == 1 &&
          (st = encode_2d(&tc, dtype, C, M, N, N, hg::kEpiBoxCols, hg::kEpiBoxRows)) != HGEMM_OK)) {
-        if (work) cudaFreeAsync(work, stream);
+        if (work && work != scratch) cudaFreeAsync(work, stream);
         return st;
     }
 
@@ -327,18 +339,32 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
     p.ldc = N;
     p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
     if ((e = hg::status_word_ptr(&p.status)) != cudaSuccess) {
-        if (work) cudaFreeAsync(work, stream);
+        if (work && work != scratch) cudaFreeAsync(work, stream);
         return cuda_fail(e, "status word");
     }
 
     e = dtype == HGEMM_BF16 ? hg::launch_tc_bf16(cg, bn, ta, tb, tc, p, clusters, stream)
                             : hg::launch_tc_f16(cg, bn, ta, tb, tc, p, clusters, stream);
-    if (work) cudaFreeAsync(work, stream);
+    if (work && work != scratch) cudaFreeAsync(work, stream);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     return HGEMM_OK;
 }
 
 }  // namespace
+
+namespace hg {
+
+hgemm_status_t gemm_in_scratch(const void* A, const void* B, void* C, int64_t M, int64_t N,
+                               int64_t K, hgemm_dtype_t dtype, cudaStream_t stream, void* scratch,
+                               size_t scratch_bytes) {
+    return run(A, B, C, M, N, K, dtype, nullptr, stream, scratch, scratch_bytes);
+}
+
+hgemm_status_t set_last_error(const char* what, cudaError_t e) {
+    return cuda_fail(e, what);
+}
+
+}  // namespace hg
 
 extern "C" {
 

@@ -77,6 +77,38 @@ hgemm_status_t hgemm(const void* A, const void* B, void* C, int64_t M, int64_t N
                      hgemm_dtype_t dtype, void* stream);
 
 /*
+ * hgemm_noalloc - hgemm for callers that must not allocate device memory.
+ *
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot call cudaMalloc on the GEMM path: work recorded into a CUDA
+ * graph whose capture forbids allocation, real-time or embedded pipelines
+ * that reserve all memory up front, and hosts whose device memory belongs to
+ * another runtime's pool.
+ *
+ * Same operation and arguments as hgemm(), and the same results. The only
+ * workspace the GEMM can need (the 16-byte-pitch copy of A or B when a row
+ * pitch or base address is not 16-byte aligned) comes from a fixed 64 MiB
+ * array inside the library (hgemm_noalloc_scratch_bytes()); the call makes no
+ * cudaMalloc, cudaMallocAsync, cudaFree or other allocating call.
+ *   - A shape whose workspace would exceed the array returns
+ *     HGEMM_ERR_INVALID_ARG (hgemm_last_error() gives the sizes) and enqueues
+ *     nothing. Aligned shapes need no workspace and have no such limit.
+ *   - Every call on a device shares that device's array, which keeps the last
+ *     call's contents (nothing in it needs to start at zero). Calls whose GPU
+ *     work overlaps - on different streams, or from different host threads -
+ *     race on the array: serialise them (one stream, or events).
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture begins.
+ *   - Every GPU that loads the library holds the array until the process exits.
+ */
+hgemm_status_t hgemm_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N,
+                             int64_t K, hgemm_dtype_t dtype, void* stream);
+
+/* Size in bytes of hgemm_noalloc's fixed scratch array. */
+uint64_t hgemm_noalloc_scratch_bytes(void);
+
+/*
  * Launch configuration, for tuning sweeps and tests. Zero in any field means
  * "let the planner choose".
  *   cta_group:     1 = one CTA per 128-row tile; 2 = a CTA pair (cluster of 2)

@@ -1,0 +1,95 @@
+"""hgemm_noalloc: the entry point for callers that cannot allocate device
+memory (graph captures that forbid allocation, pipelines that reserve all
+memory up front, hosts whose memory belongs to another runtime's pool).
+
+It must give the same results as hgemm on shapes that need the repack
+workspace, call after call (the library's fixed scratch array is shared and
+keeps the previous call's contents), and refuse shapes whose workspace would
+not fit. This file is collected last so that a first-failure run has already
+run every other test; it also passes on its own in a fresh process."""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from half_precision_dense_gb300 import binding as hg
+from half_precision_dense_gb300 import inputs
+from tests._check import compare
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from half_precision_dense_gb300 import build as hbuild
+    hbuild.build()
+    return hg.load_library()
+
+
+def _call(lib, fn, A, B, C, M, N, K, dtype):
+    code = hg.HGEMM_BF16 if dtype == "bf16" else hg.HGEMM_F16
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    st = fn(ctypes.c_void_p(A.data_ptr()), ctypes.c_void_p(B.data_ptr()),
+            ctypes.c_void_p(C.data_ptr()), M, N, K, code, stream)
+    return st
+
+
+# Each shape needs the workspace: N (and for the second, K) not a multiple of 8.
+CALLS = [((300, 517, 264), "bf16", 31), ((129, 4095, 257), "f16", 32), ((1000, 4095, 4104), "bf16", 33)]
+
+
+def test_noalloc_matches_hgemm_on_consecutive_calls(lib):
+    assert lib.hgemm_noalloc_scratch_bytes() == 64 << 20
+    for (M, N, K), dtype, seed in CALLS:
+        A = inputs.generate((M, K), dtype, seed, 0)
+        B = inputs.generate((K, N), dtype, seed, 1)
+        dA, dB = A.cuda(), B.cuda()
+        t = inputs.TORCH_DTYPES[dtype]
+        C_ref = torch.full((M, N), -3.0, dtype=t, device="cuda")
+        C_new = torch.full((M, N), -5.0, dtype=t, device="cuda")
+        assert _call(lib, lib.hgemm, dA, dB, C_ref, M, N, K, dtype) == 0
+        assert _call(lib, lib.hgemm_noalloc, dA, dB, C_new, M, N, K, dtype) == 0
+        torch.cuda.synchronize()
+        got_ref = inputs.bits(C_ref.cpu())
+        got_new = inputs.bits(C_new.cpu())
+        # against the existing entry point, with the parity tolerance
+        ref64 = oracle.gemm_f64(inputs.bits(A), inputs.bits(B), dtype)
+        r = compare(got_new, got_ref, ref64, dtype, K)
+        assert r["ok"], r
+        # and both against the oracle
+        want = oracle.round_rne(ref64, dtype)
+        assert compare(got_new, want, ref64, dtype, K)["ok"]
+        assert compare(got_ref, want, ref64, dtype, K)["ok"]
+    st, info = hg.get_device_status(0)
+    assert st == 0, (st, info)
+
+
+def test_noalloc_rejects_workspace_beyond_its_scratch(lib):
+    # B of 8200 x 4097 needs 8200 * 4104 * 2 bytes (> 64 MiB) once repacked
+    M, N, K = 1, 4097, 8200
+    A = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros((K, N), dtype=torch.bfloat16, device="cuda")
+    C = torch.full((M, N), 7.0, dtype=torch.bfloat16, device="cuda")
+    st = _call(lib, lib.hgemm_noalloc, A, B, C, M, N, K, "bf16")
+    assert st == 1
+    assert b"scratch" in lib.hgemm_last_error()
+    torch.cuda.synchronize()
+    assert torch.all(C == 7.0)  # nothing was enqueued
+
+
+def test_noalloc_aligned_shape_needs_no_scratch(lib):
+    M, N, K = 512, 1024, 8192  # aligned: no workspace at all, any size
+    A = inputs.generate((M, K), "bf16", 34, 0)
+    B = inputs.generate((K, N), "bf16", 34, 1)
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    assert _call(lib, lib.hgemm_noalloc, A.cuda(), B.cuda(), C, M, N, K, "bf16") == 0
+    torch.cuda.synchronize()
+    a, b = inputs.bits(A), inputs.bits(B)
+    ref64 = oracle.gemm_f64(a, b, "bf16")
+    r = compare(inputs.bits(C.cpu()), oracle.round_rne(ref64, "bf16"), ref64, "bf16", K)
+    assert r["ok"], r
