@@ -33,13 +33,14 @@ class HgemmError(RuntimeError):
 class _Config(ctypes.Structure):
     _fields_ = [("cta_group", ctypes.c_int32), ("block_n", ctypes.c_int32),
                 ("group_m", ctypes.c_int32), ("max_clusters", ctypes.c_int32),
-                ("store_mode", ctypes.c_int32)]
+                ("store_mode", ctypes.c_int32), ("split_k", ctypes.c_int32)]
 
 
 class _Plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "cta_group", "block_m", "block_n", "block_k", "stages", "group_m", "tiles_m", "tiles_n",
-        "num_tiles", "grid_ctas", "smem_bytes", "tmem_cols", "repack_a", "repack_b", "store_mode")]
+        "num_tiles", "grid_ctas", "smem_bytes", "tmem_cols", "repack_a", "repack_b", "store_mode",
+        "dp_tiles", "split_k", "num_units", "reserved")] + [("workspace_bytes", ctypes.c_int64)]
 
 
 @dataclass
@@ -50,9 +51,11 @@ class Config:
     group_m: int = 0
     max_clusters: int = 0
     store_mode: int = 0
+    split_k: int = 0
 
     def _c(self) -> _Config:
-        return _Config(self.cta_group, self.block_n, self.group_m, self.max_clusters, self.store_mode)
+        return _Config(self.cta_group, self.block_n, self.group_m, self.max_clusters, self.store_mode,
+                       self.split_k)
 
 
 def library_path() -> str:
@@ -89,6 +92,8 @@ def load_library():
         lib.hgemm_get_device_status.restype = ctypes.c_int
         lib.hgemm_set_timeout_ns.argtypes = [ctypes.c_uint64]
         lib.hgemm_set_timeout_ns.restype = None
+        lib.hgemm_test_inject.argtypes = [ctypes.c_int32]
+        lib.hgemm_test_inject.restype = None
         lib.hgemm_status_string.argtypes = [ctypes.c_int]
         lib.hgemm_status_string.restype = ctypes.c_char_p
         lib.hgemm_last_error.argtypes = []
@@ -165,7 +170,7 @@ def plan(M: int, N: int, K: int, dtype="bf16", config: Config | None = None, sm_
     out = _Plan()
     cfg = ctypes.byref(config._c()) if config is not None else None
     _check(lib.hgemm_plan(M, N, K, _dtype_code(dtype), cfg, sm_count, ctypes.byref(out)))
-    return {name: getattr(out, name) for name, _ in _Plan._fields_}
+    return {name: getattr(out, name) for name, _ in _Plan._fields_ if name != "reserved"}
 
 
 def tile_coord(t: int, tiles_m: int, tiles_n: int, group_m: int) -> tuple[int, int]:
@@ -187,6 +192,11 @@ def get_device_status(device: int = 0, reset: bool = False) -> tuple[int, int]:
 
 def set_timeout_ns(ns: int) -> None:
     load_library().hgemm_set_timeout_ns(int(ns))
+
+
+def test_inject(kind: int) -> None:
+    """Test hook of the failure path (see include/hgemm.h); 0 turns it off."""
+    load_library().hgemm_test_inject(int(kind))
 
 
 def status_string(s: int) -> str:

@@ -1,6 +1,7 @@
 // hgemm_api.cu - the C ABI (include/hgemm.h): argument checks, the planner,
 // TMA descriptor encoding and the launch of the persistent tcgen05 kernel.
 #include <atomic>
+#include <chrono>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -14,6 +15,7 @@ using hg::TcParams;
 
 thread_local std::string t_last_error;
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+std::atomic<int> g_inject{0};
 
 hgemm_status_t cuda_fail(cudaError_t e, const char* where) {
     t_last_error = std::string(where) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
@@ -110,34 +112,107 @@ bool valid_shape_config(int cg, int bn) {
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Relative throughput of one SM running each tile shape on a long K loop
-// (1.0 = the tensor-core peak). CTA pairs halve each SM's B traffic through
-// shared memory; narrower tiles pay more shared-memory bytes per MMA.
+// (1.0 = the pair 256x256 tile), measured on GB300 with L2 flushed: the pair
+// tile halves each SM's B traffic through shared memory, and narrower tiles
+// re-read A for fewer columns per MMA.
 double shape_efficiency(int cg, int bn) {
     if (cg == 2 && bn == 256) return 1.00;
-    if (cg == 2 && bn == 128) return 0.93;
-    if (cg == 1 && bn == 256) return 0.93;
-    if (cg == 1 && bn == 128) return 0.85;
-    return 0.70;  // cg 1, bn 64
+    if (cg == 1 && bn == 256) return 0.84;
+    if (cg == 1 && bn == 128) return 0.62;
+    if (cg == 2 && bn == 128) return 0.61;
+    return 0.31;  // cg 1, bn 64
+}
+
+// K parts for the `rem` tiles left after the last whole wave on `clusters`
+// clusters: as many as keep every part on its own cluster, at most one per K
+// block and at most 8; 1 = no split.
+int64_t auto_split(int64_t rem, int64_t clusters, int64_t num_kb) {
+    if (rem <= 0) return 1;
+    int64_t s = clusters / rem;
+    if (s > num_kb) s = num_kb;
+    if (s > 8) s = 8;
+    return s >= 2 ? s : 1;
+}
+
+// Fill the schedule fields of `pl` (tiles already set) for `clusters`
+// resident clusters: whole-tile units first, then the K-split tail.
+void schedule_plan(hgemm_plan_t* pl, int64_t clusters, int split_cfg, int64_t num_kb) {
+    const int64_t tiles = pl->num_tiles;
+    if (clusters < 1) clusters = 1;
+    const int64_t rem = tiles % clusters;
+    int64_t s = 1;
+    if (split_cfg >= 2) s = rem > 0 ? (split_cfg < num_kb ? split_cfg : num_kb) : 1;
+    else if (split_cfg == 0) s = auto_split(rem, clusters, num_kb);
+    if (s < 2) s = 1;
+    pl->split_k = static_cast<int32_t>(s);
+    pl->dp_tiles = static_cast<int32_t>(s > 1 ? tiles - rem : tiles);
+    pl->num_units = hg::work_units(pl->num_tiles, pl->dp_tiles, pl->split_k);
+    int64_t grid = clusters < pl->num_units ? clusters : pl->num_units;
+    if (grid < 1) grid = 1;
+    pl->grid_ctas = static_cast<int32_t>(grid * pl->cta_group);
+}
+
+// Bytes of fp32 partial sums (and their flags) for a plan's K-split tail.
+int64_t partial_bytes(const hgemm_plan_t& pl) {
+    if (pl.split_k <= 1) return 0;
+    const int64_t blocks = static_cast<int64_t>(pl.num_tiles - pl.dp_tiles) * (pl.split_k - 1) *
+                           pl.cta_group * hg::kEpiWarps;
+    return blocks * hg::kEpiBoxRows * pl.block_n * 4;
+}
+
+int64_t flag_bytes(const hgemm_plan_t& pl) {
+    if (pl.split_k <= 1) return 0;
+    return static_cast<int64_t>(pl.num_tiles - pl.dp_tiles) * (pl.split_k - 1) * pl.cta_group *
+           hg::kEpiWarps * 8;
+}
+
+int64_t align256(int64_t x) { return (x + 255) / 256 * 256; }
+
+// Workspace layout: [A repack][B repack][partials][flags], each 256-aligned.
+struct WorkspaceLayout {
+    int64_t off_a, off_b, off_part, off_flags, total;
+};
+
+WorkspaceLayout workspace_layout(const hgemm_plan_t& pl, int64_t M, int64_t N, int64_t K) {
+    WorkspaceLayout w{};
+    const int64_t lda = (K + 7) / 8 * 8, ldb = (N + 7) / 8 * 8;
+    int64_t off = 0;
+    w.off_a = off;
+    off += pl.repack_a ? align256(2 * M * lda) : 0;
+    w.off_b = off;
+    off += pl.repack_b ? align256(2 * K * ldb) : 0;
+    w.off_part = off;
+    off += align256(partial_bytes(pl));
+    w.off_flags = off;
+    off += align256(flag_bytes(pl));
+    w.total = off;
+    return w;
 }
 
 // Pick (cta_group, block_n) minimising the estimated time: whole waves of
-// tiles over the resident clusters, each tile costing its padded area over the
-// shape's efficiency, plus a per-tile fixed cost that favours fewer, larger
-// tiles when the K loop is short.
-void choose_shape(int64_t M, int64_t N, int64_t K, int sms, int* cg_out, int* bn_out) {
-    static const int cand[5][2] = {{2, 256}, {2, 128}, {1, 256}, {1, 128}, {1, 64}};
+// tiles over the resident clusters plus the (K-split) tail, each tile costing
+// its padded area over the shape's efficiency, plus a per-unit fixed cost that
+// favours fewer, larger tiles when the K loop is short. A problem with a
+// single 128-row tile row keeps one CTA per tile (a pair would compute an
+// empty half).
+void choose_shape(int64_t M, int64_t N, int64_t K, int sms, int max_clusters, int* cg_out, int* bn_out) {
+    static const int cand[5][2] = {{2, 256}, {1, 256}, {1, 128}, {2, 128}, {1, 64}};
     double best = 1e300;
     int bcg = 2, bbn = 256;
     const int64_t kb = cdiv(K, hg::kBlockK);
     for (const auto& c : cand) {
         const int cg = c[0], bn = c[1];
+        if (cg == 2 && M <= 128) continue;
         const int64_t tiles = cdiv(M, 128 * cg) * cdiv(N, bn);
-        const int64_t clusters = sms / cg;
+        int64_t clusters = sms / cg;
+        if (max_clusters > 0 && max_clusters < clusters) clusters = max_clusters;
         if (clusters <= 0) continue;
-        const int64_t waves = cdiv(tiles, clusters);
-        const double tile_work = static_cast<double>(128 * cg) * bn * (kb * hg::kBlockK) / cg;  // per SM
-        const double tile_time = tile_work / shape_efficiency(cg, bn) + 128.0 * bn * 24.0;
-        const double t = static_cast<double>(waves) * tile_time;
+        const int64_t rem = tiles % clusters;
+        const int64_t split = auto_split(rem, clusters, kb);
+        const double waves = static_cast<double>(tiles / clusters) + (rem ? 1.0 / split : 0.0);
+        const double tile_work = static_cast<double>(128) * bn * (kb * hg::kBlockK);  // per SM
+        const double tile_time = tile_work / shape_efficiency(cg, bn) + 128.0 * bn * 64.0;
+        const double t = waves * tile_time;
         if (t < best * 0.999) {
             best = t;
             bcg = cg;
@@ -153,10 +228,14 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, const hgemm_config_t* 
     std::memset(pl, 0, sizeof(*pl));
     hgemm_config_t c{};
     if (cfg) c = *cfg;
+    if (c.group_m < 0 || c.max_clusters < 0 || c.store_mode < 0 || c.store_mode > 2 || c.split_k < 0) {
+        t_last_error = "negative or unknown config field";
+        return HGEMM_ERR_INVALID_ARG;
+    }
     int cg = c.cta_group, bn = c.block_n;
     if (cg == 0 || bn == 0) {
         int acg, abn;
-        choose_shape(M, N, K, sms, &acg, &abn);
+        choose_shape(M, N, K, sms, c.max_clusters, &acg, &abn);
         if (cg == 0 && bn == 0) {
             cg = acg;
             bn = abn;
@@ -168,10 +247,6 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, const hgemm_config_t* 
     }
     if (!valid_shape_config(cg, bn)) {
         t_last_error = "unsupported (cta_group, block_n) pair";
-        return HGEMM_ERR_INVALID_ARG;
-    }
-    if (c.group_m < 0 || c.max_clusters < 0 || c.store_mode < 0 || c.store_mode > 2) {
-        t_last_error = "negative or unknown config field";
         return HGEMM_ERR_INVALID_ARG;
     }
     pl->cta_group = cg;
@@ -187,9 +262,7 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, const hgemm_config_t* 
     pl->group_m = c.group_m > 0 ? c.group_m : (pl->tiles_m < 8 ? (pl->tiles_m > 0 ? pl->tiles_m : 1) : 8);
     int64_t clusters = sms / cg;
     if (c.max_clusters > 0 && c.max_clusters < clusters) clusters = c.max_clusters;
-    if (clusters > pl->num_tiles) clusters = pl->num_tiles;
-    if (clusters < 1) clusters = 1;
-    pl->grid_ctas = static_cast<int32_t>(clusters * cg);
+    schedule_plan(pl, clusters, c.split_k, cdiv(K, hg::kBlockK));
     pl->repack_a = a_unaligned ? 1 : 0;
     pl->repack_b = b_unaligned ? 1 : 0;
     pl->store_mode = (c.store_mode != 0) ? c.store_mode : (c_unaligned ? 2 : 1);
@@ -197,7 +270,44 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, const hgemm_config_t* 
         t_last_error = "TMA stores need a 16-byte aligned C with an 16-byte row pitch";
         return HGEMM_ERR_INVALID_ARG;
     }
+    pl->workspace_bytes = workspace_layout(*pl, M, N, K).total;
     return HGEMM_OK;
+}
+
+// --------------------------------------------------------------- workspace
+// One stream-ordered pool per device, owned by the library, that keeps up to
+// 256 MiB cached between calls so steady-state calls do not go to the driver.
+hgemm_status_t pool_for_device(int dev, cudaMemPool_t* out) {
+    static std::mutex mu;
+    static cudaMemPool_t pools[64] = {};
+    if (dev < 0 || dev >= 64) return HGEMM_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!pools[dev]) {
+        cudaMemPoolProps props{};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool = nullptr;
+        cudaError_t e = cudaMemPoolCreate(&pool, &props);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemPoolCreate");
+        uint64_t keep = uint64_t{256} << 20;
+        e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        if (e != cudaSuccess) {
+            cudaMemPoolDestroy(pool);
+            return cuda_fail(e, "cudaMemPoolSetAttribute");
+        }
+        pools[dev] = pool;
+    }
+    *out = pools[dev];
+    return HGEMM_OK;
+}
+
+// A number unique to each launch (split-K parts mark their partials with it).
+unsigned long long next_epoch() {
+    static std::atomic<unsigned long long> counter{
+        (static_cast<unsigned long long>(
+             std::chrono::steady_clock::now().time_since_epoch().count()) << 20) | (1ull << 63)};
+    return counter.fetch_add(1, std::memory_order_relaxed);
 }
 
 bool misaligned16(const void* p, int64_t cols) {
@@ -259,53 +369,60 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
     const bool a_bad = misaligned16(A, K), b_bad = misaligned16(B, N), c_bad = misaligned16(C, N);
     if ((st = make_plan(M, N, K, cfg, info.sms, a_bad, b_bad, c_bad, &pl)) != HGEMM_OK) return st;
 
-    // Resident clusters bound the persistent grid.
+    // Resident clusters bound the persistent grid; re-plan the schedule if
+    // fewer fit than the planner assumed.
     const int cg = pl.cta_group, bn = pl.block_n;
+    const int64_t num_kb = cdiv(K, hg::kBlockK);
     int resident = dtype == HGEMM_BF16 ? hg::max_active_clusters_bf16(cg, bn)
                                        : hg::max_active_clusters_f16(cg, bn);
-    if (resident <= 0) resident = info.sms / cg;
-    int clusters = pl.grid_ctas / cg;
-    if (clusters > resident) clusters = resident;
+    if (resident > 0 && resident < pl.grid_ctas / cg) {
+        schedule_plan(&pl, resident, cfg ? cfg->split_k : 0, num_kb);
+        pl.workspace_bytes = workspace_layout(pl, M, N, K).total;
+    }
+    const int clusters = pl.grid_ctas / cg;
 
-    // Operands TMA cannot address get a 16-byte-pitched copy.
+    // Workspace: 16-byte-pitched copies of operands TMA cannot address, and
+    // the fp32 partial sums of a K-split tail.
+    const WorkspaceLayout wl = workspace_layout(pl, M, N, K);
     const int64_t lda = pl.repack_a ? (K + 7) / 8 * 8 : K;
     const int64_t ldb = pl.repack_b ? (N + 7) / 8 * 8 : N;
     void* work = nullptr;
     const void* a_use = A;
     const void* b_use = B;
-    if (pl.repack_a || pl.repack_b) {
-        const int64_t bytes_a = pl.repack_a ? 2 * M * lda : 0;
-        const int64_t bytes_b = pl.repack_b ? 2 * K * ldb : 0;
-        const int64_t off_b = (bytes_a + 255) / 256 * 256;
-        const size_t need = static_cast<size_t>(off_b + bytes_b);
+    if (wl.total > 0) {
+        const size_t need = static_cast<size_t>(wl.total);
         if (scratch) {
             if (need > scratch_bytes) {
                 t_last_error = "this shape needs " + std::to_string(need) +
-                               " bytes of repack workspace; the scratch holds " +
+                               " bytes of workspace; the scratch holds " +
                                std::to_string(scratch_bytes);
                 return HGEMM_ERR_INVALID_ARG;
             }
             work = scratch;
-        } else if ((e = cudaMallocAsync(&work, need, stream)) != cudaSuccess) {
-            cuda_fail(e, "cudaMallocAsync (repack workspace)");
-            return HGEMM_ERR_ALLOC;
+        } else {
+            cudaMemPool_t pool = nullptr;
+            if ((st = pool_for_device(dev, &pool)) != HGEMM_OK) return st;
+            if ((e = cudaMallocFromPoolAsync(&work, need, pool, stream)) != cudaSuccess) {
+                cuda_fail(e, "cudaMallocFromPoolAsync (workspace)");
+                return HGEMM_ERR_ALLOC;
+            }
         }
         uint8_t* w8 = static_cast<uint8_t*>(work);
         if (pl.repack_a) {
             if ((e = hg::launch_repack(static_cast<const uint16_t*>(A), M, K,
-                                       reinterpret_cast<uint16_t*>(w8), lda, stream)) != cudaSuccess) {
+                                       reinterpret_cast<uint16_t*>(w8 + wl.off_a), lda, stream)) != cudaSuccess) {
                 if (work != scratch) cudaFreeAsync(work, stream);
                 return cuda_fail(e, "repack A");
             }
-            a_use = w8;
+            a_use = w8 + wl.off_a;
         }
         if (pl.repack_b) {
             if ((e = hg::launch_repack(static_cast<const uint16_t*>(B), K, N,
-                                       reinterpret_cast<uint16_t*>(w8 + off_b), ldb, stream)) != cudaSuccess) {
+                                       reinterpret_cast<uint16_t*>(w8 + wl.off_b), ldb, stream)) != cudaSuccess) {
                 if (work != scratch) cudaFreeAsync(work, stream);
                 return cuda_fail(e, "repack B");
             }
-            b_use = w8 + off_b;
+            b_use = w8 + wl.off_b;
         }
     }
 
@@ -338,6 +455,15 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
     p.C = static_cast<uint16_t*>(C);
     p.ldc = N;
     p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+    p.dp_units = pl.dp_tiles;
+    p.split = pl.split_k;
+    p.num_units = pl.num_units;
+    p.partials = pl.split_k > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(work) + wl.off_part) : nullptr;
+    p.flags = pl.split_k > 1
+                  ? reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(work) + wl.off_flags)
+                  : nullptr;
+    p.epoch = next_epoch();
+    p.inject = g_inject.load(std::memory_order_relaxed);
     if ((e = hg::status_word_ptr(&p.status)) != cudaSuccess) {
         if (work && work != scratch) cudaFreeAsync(work, stream);
         return cuda_fail(e, "status word");
@@ -457,6 +583,8 @@ hgemm_status_t hgemm_get_device_status(int32_t device, int32_t reset, uint32_t* 
 }
 
 void hgemm_set_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 1, std::memory_order_relaxed); }
+
+void hgemm_test_inject(int32_t kind) { g_inject.store(kind == 1 ? 1 : 0, std::memory_order_relaxed); }
 
 const char* hgemm_status_string(hgemm_status_t s) {
     switch (s) {

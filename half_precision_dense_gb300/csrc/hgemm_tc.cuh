@@ -68,7 +68,24 @@ struct TcParams {
     int64_t ldc;                    // elements between C rows (store_mode 2)
     uint64_t timeout_ns;
     unsigned long long* status;     // device status word
+    // split-K tail (see work_unit): units [0, dp_units) are whole tiles, the
+    // rest are `split` K-parts of each remaining tile.
+    int32_t dp_units, split, num_units;
+    float* partials;                // (split - 1) fp32 partial tiles per split tile
+    unsigned long long* flags;      // one per partial block: == epoch once written
+    unsigned long long epoch;       // unique per launch
+    int32_t inject;                 // test hook: 1 = the owner of split tile 0 waits for a
+                                    // partial that is never published (its wait runs out)
 };
+
+// Index of the partial block written by part `part` (< split - 1) of split
+// tile `split_idx` for CTA rank `rank` and epilogue warp `warp`: 32 rows x BN
+// fp32.
+template <int CG>
+__device__ __forceinline__ int64_t partial_block(int32_t split_idx, int32_t part, int32_t split,
+                                                 uint32_t rank, int warp) {
+    return ((static_cast<int64_t>(split_idx) * (split - 1) + part) * CG + rank) * kEpiWarps + warp;
+}
 
 template <int CG, int BN>
 struct TcCfg {
@@ -154,6 +171,39 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Wa
     return wait_slow(bar, parity, w, role, which);
 }
 
+__device__ __forceinline__ unsigned long long ld_acquire_gpu(const unsigned long long* ptr) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ptr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(unsigned long long* ptr, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" :: "l"(ptr), "l"(v) : "memory");
+}
+
+// Bounded wait until another CTA has published `epoch` at `flag`.
+static __device__ __noinline__ bool wait_flag(const unsigned long long* flag, unsigned long long epoch,
+                                              const Waiter& w, uint32_t which) {
+    if (ld_acquire_gpu(flag) == epoch) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        for (int i = 0; i < 16; ++i) {
+            if (ld_acquire_gpu(flag) == epoch) return true;
+            __nanosleep(32);
+        }
+        if (*w.abort) return false;
+        if (globaltimer_ns() - t0 > w.timeout_ns) {
+            const unsigned long long info =
+                (static_cast<unsigned long long>(kRoleEpilogue) << 56) |
+                (static_cast<unsigned long long>(which & 0xFFu) << 48) |
+                (static_cast<unsigned long long>(blockIdx.x & 0xFFFFu) << 32);
+            atomicCAS(w.status, 0ull, info | kStatusTimeout);
+            *w.abort = 1;
+            return false;
+        }
+    }
+}
+
 // Pins the 32 registers after tcgen05.wait::ld so no use is scheduled above it.
 __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
 #pragma unroll
@@ -221,12 +271,13 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         if (lane == 0) {
             uint32_t stage = 0, phase = 0;
             bool ok = true;
-            for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters) {
+            for (int u = cluster_id; u < p.num_units && ok; u += num_clusters) {
+                const WorkUnit wu = work_unit(u, p.dp_units, p.split, p.num_kb);
                 int32_t tm, tn;
-                tile_coord(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+                tile_coord(wu.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
                 const int32_t m0 = tm * (kBlockMCta * CG) + static_cast<int32_t>(rank) * kBlockMCta;
                 const int32_t n0 = tn * BN + static_cast<int32_t>(rank) * Cfg::kBnCta;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = wu.kb0; kb < wu.kb1; ++kb) {
                     if (!wait_bar(bar_empty + 8 * stage, phase ^ 1u, w, kRoleProducer, stage)) {
                         ok = false;
                         break;
@@ -270,7 +321,8 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             bool ok = true;
             bool issued = false;
             int it = 0;
-            for (int t = cluster_id; t < p.num_tiles; t += num_clusters, ++it) {
+            for (int u = cluster_id; u < p.num_units; u += num_clusters, ++it) {
+                const WorkUnit wu = work_unit(u, p.dp_units, p.split, p.num_kb);
                 const uint32_t acc = static_cast<uint32_t>(it) & 1u;
                 const uint32_t acc_phase = (static_cast<uint32_t>(it) >> 1) & 1u;
                 if (!wait_bar(bar_tempty + 8 * acc, acc_phase ^ 1u, w, kRoleMma, 32 + acc)) {
@@ -279,7 +331,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = wu.kb0; kb < wu.kb1; ++kb) {
                     if (!wait_bar(bar_full + 8 * stage, phase, w, kRoleMma, stage)) {
                         ok = false;
                         break;
@@ -291,7 +343,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     for (int kk = 0; kk < kBlockK / kUmmaK; ++kk) {
                         const uint64_t ad = sdesc_sw128(a0 + 32u * kk, 16u, 1024u);
                         const uint64_t bd = sdesc_sw128(b0 + 2048u * kk, Cfg::kBAtomBytes, 1024u);
-                        umma_f16<CG>(d_tmem, ad, bd, p.idesc, (kb | kk) != 0 ? 1u : 0u);
+                        umma_f16<CG>(d_tmem, ad, bd, p.idesc, (kb > wu.kb0 || kk != 0) ? 1u : 0u);
                     }
                     issued = true;
                     if constexpr (CG == 1) umma_commit(bar_empty + 8 * stage);
@@ -318,13 +370,14 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         int it = 0;
         uint32_t buf = 0;
         const uint32_t my_boxes = sEpi + static_cast<uint32_t>(warp) * 2u * kEpiBoxBytes;
-        for (int t = cluster_id; t < p.num_tiles; t += num_clusters, ++it) {
+        for (int u = cluster_id; u < p.num_units; u += num_clusters, ++it) {
+            const WorkUnit wu = work_unit(u, p.dp_units, p.split, p.num_kb);
             const uint32_t acc = static_cast<uint32_t>(it) & 1u;
             const uint32_t acc_phase = (static_cast<uint32_t>(it) >> 1) & 1u;
             if (!wait_bar(bar_tfull + 8 * acc, acc_phase, w, kRoleEpilogue, 32 + acc)) break;
             tc_fence_after();
             int32_t tm, tn;
-            tile_coord(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+            tile_coord(wu.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
             const int32_t row0 = tm * (kBlockMCta * CG) + static_cast<int32_t>(rank) * kBlockMCta +
                                  warp * kEpiBoxRows;
             const int32_t col0 = tn * BN;
@@ -347,6 +400,66 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                                          :: "r"(bar_tempty + 8 * acc) : "memory");
                         } else {
                             mbar_arrive_cluster(mapa_shared(bar_tempty + 8 * acc, 0));
+                        }
+                    }
+                }
+                if (wu.split_idx >= 0) {
+                    if (wu.part != p.split - 1) {
+                        // A non-owning K part: publish this chunk's fp32 partial
+                        // sums (lane-interleaved, so each warp store is 512
+                        // contiguous bytes) instead of writing C.
+                        float4* dst = reinterpret_cast<float4*>(p.partials) +
+                                      partial_block<CG>(wu.split_idx, wu.part, p.split, rank, warp) *
+                                          (kEpiBoxRows * BN / 4);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            dst[(c * 16 + j) * 32 + lane] =
+                                make_float4(__uint_as_float(r0[4 * j]), __uint_as_float(r0[4 * j + 1]),
+                                            __uint_as_float(r0[4 * j + 2]), __uint_as_float(r0[4 * j + 3]));
+                            dst[(c * 16 + 8 + j) * 32 + lane] =
+                                make_float4(__uint_as_float(r1[4 * j]), __uint_as_float(r1[4 * j + 1]),
+                                            __uint_as_float(r1[4 * j + 2]), __uint_as_float(r1[4 * j + 3]));
+                        }
+                        if (c == BN / 64 - 1) {
+                            __threadfence();
+                            __syncwarp();
+                            if (lane == 0)
+                                st_release_gpu(p.flags + partial_block<CG>(wu.split_idx, wu.part, p.split,
+                                                                            rank, warp),
+                                               p.epoch);
+                        }
+                        continue;
+                    }
+                    // The owning part (the last one: every part it waits for has
+                    // a lower unit index, so no cluster ever waits on work
+                    // queued behind itself): add the other parts' partial sums.
+                    if (c == 0) {
+                        // Test hook: wait for a mark no part ever writes. Split
+                        // units are a cluster's last, so nothing else is in
+                        // flight in this CTA when the wait gives up.
+                        const unsigned long long want =
+                            (p.inject == 1 && wu.split_idx == 0) ? ~p.epoch : p.epoch;
+                        for (int q = 0; q < p.split - 1; ++q)
+                            if (!wait_flag(p.flags + partial_block<CG>(wu.split_idx, q, p.split, rank, warp),
+                                           want, w, 64 + q))
+                                break;
+                    }
+                    for (int q = 0; q < p.split - 1; ++q) {
+                        const float4* src = reinterpret_cast<const float4*>(p.partials) +
+                                            partial_block<CG>(wu.split_idx, q, p.split, rank, warp) *
+                                                (kEpiBoxRows * BN / 4);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const float4 a = __ldcg(src + (c * 16 + j) * 32 + lane);
+                            const float4 b = __ldcg(src + (c * 16 + 8 + j) * 32 + lane);
+                            r0[4 * j] = __float_as_uint(__uint_as_float(r0[4 * j]) + a.x);
+                            r0[4 * j + 1] = __float_as_uint(__uint_as_float(r0[4 * j + 1]) + a.y);
+                            r0[4 * j + 2] = __float_as_uint(__uint_as_float(r0[4 * j + 2]) + a.z);
+                            r0[4 * j + 3] = __float_as_uint(__uint_as_float(r0[4 * j + 3]) + a.w);
+                            r1[4 * j] = __float_as_uint(__uint_as_float(r1[4 * j]) + b.x);
+                            r1[4 * j + 1] = __float_as_uint(__uint_as_float(r1[4 * j + 1]) + b.y);
+                            r1[4 * j + 2] = __float_as_uint(__uint_as_float(r1[4 * j + 2]) + b.z);
+                            r1[4 * j + 3] = __float_as_uint(__uint_as_float(r1[4 * j + 3]) + b.w);
                         }
                     }
                 }

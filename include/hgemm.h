@@ -67,11 +67,14 @@ typedef enum {
  * result (written). M, N, K: dimensions, each in [0, 2^31 - 1]. dtype:
  * HGEMM_F16 or HGEMM_BF16 (A, B and C share it).
  *
- * Operands whose row pitch (2K bytes for A, 2N bytes for B) or base address is
- * not a multiple of 16 bytes are first copied into a 16-byte-pitched
- * workspace taken from the device's stream-ordered allocator
- * (cudaMallocAsync / cudaFreeAsync on `stream`); such a C is written with
- * plain stores. Otherwise the call allocates nothing.
+ * Workspace: operands whose row pitch (2K bytes for A, 2N bytes for B) or base
+ * address is not a multiple of 16 bytes are first copied into a
+ * 16-byte-pitched workspace (such a C is written with plain stores), and when
+ * the last wave of tiles is split along K the parts' fp32 partial sums go
+ * through the workspace too. It comes from a stream-ordered memory pool owned
+ * by the library (one per device, cudaMallocFromPoolAsync / cudaFreeAsync on
+ * `stream`; the pool keeps up to 256 MiB cached between calls). Calls that need
+ * no workspace allocate nothing; hgemm_plan reports the bytes.
  */
 hgemm_status_t hgemm(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
                      hgemm_dtype_t dtype, void* stream);
@@ -87,14 +90,18 @@ hgemm_status_t hgemm(const void* A, const void* B, void* C, int64_t M, int64_t N
  *
  * Same operation and arguments as hgemm(), and the same results. The only
  * workspace the GEMM can need (the 16-byte-pitch copy of A or B when a row
- * pitch or base address is not 16-byte aligned) comes from a fixed 64 MiB
- * array inside the library (hgemm_noalloc_scratch_bytes()); the call makes no
- * cudaMalloc, cudaMallocAsync, cudaFree or other allocating call.
+ * pitch or base address is not 16-byte aligned, and the fp32 partial sums of
+ * a K-split last wave) comes from a fixed 64 MiB array inside the library
+ * (hgemm_noalloc_scratch_bytes()); the call makes no cudaMalloc,
+ * cudaMallocAsync, cudaFree or other allocating call.
  *   - A shape whose workspace would exceed the array returns
  *     HGEMM_ERR_INVALID_ARG (hgemm_last_error() gives the sizes) and enqueues
- *     nothing. Aligned shapes need no workspace and have no such limit.
+ *     nothing. The K-split partial sums never need more than 20 MiB, so the
+ *     limit only bites on unaligned operands (their 16-byte-pitch copies).
  *   - Every call on a device shares that device's array, which keeps the last
- *     call's contents (nothing in it needs to start at zero). Calls whose GPU
+ *     call's contents (nothing in it needs to start at zero: the K-split
+ *     parts mark their partial sums with a number unique to each launch, so
+ *     stale marks are never mistaken for fresh ones). Calls whose GPU
  *     work overlaps - on different streams, or from different host threads -
  *     race on the array: serialise them (one stream, or events).
  *   - The first call on each device looks up the array's device address
@@ -117,6 +124,9 @@ uint64_t hgemm_noalloc_scratch_bytes(void);
  *   group_m:       tile rows per raster group (L2 reuse), >= 1.
  *   max_clusters:  cap on resident CTA clusters (forces more tiles per CTA).
  *   store_mode:    1 = TMA tensor stores of C, 2 = plain per-element stores.
+ *   split_k:       K-split of the tiles left over after the last whole wave
+ *                  (0 = planner's choice, 1 = never split, s >= 2 = s parts,
+ *                  capped at the number of 64-deep K blocks).
  */
 typedef struct {
     int32_t cta_group;
@@ -124,6 +134,7 @@ typedef struct {
     int32_t group_m;
     int32_t max_clusters;
     int32_t store_mode;
+    int32_t split_k;
 } hgemm_config_t;
 
 /* hgemm with an explicit configuration (cfg may be NULL = all zero). */
@@ -163,6 +174,11 @@ typedef struct {
     int32_t repack_a;      /* 1 if A goes through the 16-byte-pitch workspace */
     int32_t repack_b;      /* 1 if B does */
     int32_t store_mode;    /* 1 = TMA stores, 2 = plain stores */
+    int32_t dp_tiles;      /* tiles computed whole (the first dp_tiles in raster order) */
+    int32_t split_k;       /* K parts of each remaining tile (1 = no split) */
+    int32_t num_units;     /* work units: dp_tiles + (num_tiles - dp_tiles) * split_k */
+    int32_t reserved;
+    int64_t workspace_bytes; /* stream-ordered workspace: repacked operands + fp32 partials */
 } hgemm_plan_t;
 
 /* Fill *out with the plan hgemm_ex would use. sm_count > 0 plans for that many
@@ -191,6 +207,18 @@ hgemm_status_t hgemm_get_device_status(int32_t device, int32_t reset, uint32_t* 
 /* Upper bound, in nanoseconds, on any single wait inside the kernels
  * (default 2e9). Applies to launches made after the call, from any thread. */
 void hgemm_set_timeout_ns(uint64_t ns);
+
+/*
+ * Test hook for the failure path (not for production use; affects launches
+ * made after the call, from any thread, until reset with 0).
+ * kind 1: in each launch that splits its last wave along K, the CTAs owning
+ * the first split tile wait for partial sums that are never published. That
+ * wait runs out after the timeout set by hgemm_set_timeout_ns; the kernel
+ * records HGEMM_ERR_TIMEOUT in the device status word, writes that tile
+ * without the missing parts, and returns normally. The waiting CTAs have no
+ * copies or MMAs in flight, and nothing traps or hangs.
+ */
+void hgemm_test_inject(int32_t kind);
 
 /* Static text for a status code. */
 const char* hgemm_status_string(hgemm_status_t s);

@@ -121,6 +121,26 @@ def test_plan_shapes(lib):
         binding.plan(512, 512, 512, "f16", binding.Config(cta_group=2, block_n=64), sm_count=148)
 
 
+def test_plan_split_tail(lib):
+    # 4096^3 on 152 SMs with pair tiles: 256 tiles, 76 clusters, 3 whole waves,
+    # the 28 leftover tiles split 2 ways over 56 clusters
+    p = binding.plan(4096, 4096, 4096, "bf16", binding.Config(cta_group=2, block_n=256), sm_count=152)
+    assert (p["num_tiles"], p["dp_tiles"], p["split_k"], p["num_units"]) == (256, 228, 2, 284)
+    assert p["grid_ctas"] == 152
+    assert p["workspace_bytes"] >= 28 * 1 * 2 * 4 * 32 * 256 * 4
+    # fewer leftover tiles allow more parts (capped at 8 and at the K blocks)
+    q = binding.plan(512, 1024, 8192, "bf16", binding.Config(cta_group=2, block_n=256), sm_count=152)
+    assert (q["num_tiles"], q["dp_tiles"], q["split_k"], q["num_units"]) == (8, 0, 8, 64)
+    r = binding.plan(512, 1024, 128, "bf16", binding.Config(cta_group=2, block_n=256), sm_count=152)
+    assert r["split_k"] == 2  # only two K blocks
+    # split_k = 1 disables it; whole waves leave nothing to split
+    off = binding.plan(4096, 4096, 4096, "bf16",
+                       binding.Config(cta_group=2, block_n=256, split_k=1), sm_count=152)
+    assert (off["split_k"], off["dp_tiles"], off["num_units"], off["workspace_bytes"]) == (1, 256, 256, 0)
+    even = binding.plan(128 * 76, 256, 4096, "bf16", binding.Config(cta_group=1, block_n=256), sm_count=76)
+    assert even["split_k"] == 1 and even["num_units"] == 76
+
+
 def test_plan_skinny_prefers_narrow_tiles(lib):
     p = binding.plan(128, 8192, 8192, "bf16", sm_count=148)
     assert p["block_m"] == 128  # one tile row: no half-empty CTA pairs

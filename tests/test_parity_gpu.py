@@ -146,6 +146,44 @@ def test_persistent_loop_many_tiles_per_cta(cfg, max_clusters):
     check_full(A, B, "f16", c)
 
 
+@pytest.mark.parametrize("cfg", CONFIGS, ids=CFG_IDS)
+@pytest.mark.parametrize("split", [2, 3, 5])
+def test_split_k_tail(cfg, split):
+    # 3 clusters over 8 x 10 (or 4 x 10) tiles leave a remainder; its tiles are
+    # split `split` ways along K and the parts' partial sums meet in the owner
+    c = hg.Config(cfg.cta_group, cfg.block_n, 0, 3, 0, split)
+    A, B = operands(1024, 1280, 704, "bf16", 14)
+    check_full(A, B, "bf16", c)
+
+
+@pytest.mark.parametrize("shape", [(512, 1024, 8192), (300, 700, 130), (128, 2048, 4096), (256, 512, 64)])
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_split_k_auto(shape, dtype):
+    # fewer tiles than clusters: the planner splits every tile (up to 8 ways,
+    # at most one part per K block; K = 64 leaves nothing to split)
+    M, N, K = shape
+    A, B = operands(M, N, K, dtype, 15)
+    p = hg.plan(M, N, K, dtype)
+    assert p["split_k"] >= 1
+    check_full(A, B, dtype)
+
+
+def test_split_k_repeated_calls_reuse_workspace():
+    # the pool hands the same workspace back; fresh launch epochs keep stale
+    # partial-sum marks from being taken for new ones
+    A, B = operands(512, 1024, 2048, "f16", 16)
+    a, b = inputs.bits(A), inputs.bits(B)
+    ref64 = oracle.gemm_f64(a, b, "f16")
+    ref = oracle.round_rne(ref64, "f16")
+    dA, dB = A.cuda(), B.cuda()
+    for i in range(4):
+        C = torch.empty((512, 1024), dtype=torch.float16, device="cuda")
+        hg.hgemm(dA, dB, C, 512, 1024, 2048, "f16")
+        torch.cuda.synchronize()
+        r = compare(inputs.bits(C.cpu()), ref, ref64, "f16", 2048)
+        assert r["ok"], (i, r)
+
+
 @pytest.mark.parametrize("group_m", [1, 2, 5, 64])
 def test_raster_groups(group_m):
     A, B = operands(1536, 1024, 256, "bf16", 7)
