@@ -37,6 +37,9 @@ sys.path.insert(0, ROOT)
 METRIC = "fp16/bf16 GEMM TFLOP/s at M=N=K=4096; % of GB300 dense tensor-core peak"
 UNIT = "TFLOP/s"
 L2_FLUSH_BYTES = 256 << 20
+# Bumped whenever the GEMM kernel changes, so ncu figures taken on an older
+# kernel are not reported as current.
+KERNEL_REV = 3
 
 # name -> list of (M, N, K, dtype, dist, sigma, seed) GEMMs making up one step
 WORKLOADS = {
@@ -275,12 +278,22 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": n_ev,
         "wall_s_timed_region": round(wall, 4),
     }
+    o = ops[0]
+    plan = hg.plan(o["M"], o["N"], o["K"], o["dt"])
+    plan_key = [plan["cta_group"], plan["block_n"], plan["split_k"], plan["grid_ctas"]]
+    line["roofline"]["plan"] = {"cta_group": plan_key[0], "block_n": plan_key[1],
+                                "split_k": plan_key[2], "grid_ctas": plan_key[3]}
     if args.traffic_file and os.path.exists(args.traffic_file):
+        # DRAM bytes from an ncu capture count only while the kernel and plan
+        # they were taken on are the ones running now.
         try:
             with open(args.traffic_file) as f:
                 tr = json.load(f)
-            line["roofline"]["traffic"] = tr.get("dram_bytes_per_launch")
-            line["roofline"]["traffic_source"] = tr.get("source")
+            if tr.get("plan") == plan_key and tr.get("kernel_rev") == KERNEL_REV:
+                line["roofline"]["traffic"] = tr.get("dram_bytes_per_launch")
+                line["roofline"]["traffic_source"] = tr.get("source")
+            else:
+                line["roofline"]["traffic_source"] = "stale capture (kernel or plan changed); null"
         except (OSError, ValueError):
             pass
     if world == 1 and not args.no_cpu_baseline:

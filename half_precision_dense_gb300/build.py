@@ -40,8 +40,24 @@ def _headers():
         glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
+def _extra_flags() -> list[str]:
+    """Extra nvcc flags from HGEMM_NVCC_FLAGS (e.g. -DHG_TRACE for a build that
+    records kernel timelines)."""
+    return os.environ.get("HGEMM_NVCC_FLAGS", "").split()
+
+
+def _flags_stamp() -> str:
+    return os.path.join(BUILD_DIR, "flags.txt")
+
+
 def _stale(obj: str, src: str) -> bool:
     if not os.path.exists(obj):
+        return True
+    try:
+        with open(_flags_stamp()) as f:
+            if f.read() != " ".join(_extra_flags()):
+                return True
+    except OSError:
         return True
     t = os.path.getmtime(obj)
     return any(os.path.getmtime(d) > t for d in [src, __file__] + _headers())
@@ -52,7 +68,7 @@ def _compile(src_name: str, verbose: bool) -> tuple[str, str]:
     obj = os.path.join(BUILD_DIR, src_name.replace(".cu", ".o"))
     if not _stale(obj, src):
         return obj, ""
-    cmd = [nvcc(), *ARCH, *CFLAGS, "-c", src, "-o", obj]
+    cmd = [nvcc(), *ARCH, *CFLAGS, *_extra_flags(), "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed on {src_name}:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
@@ -67,6 +83,8 @@ def build(verbose: bool = False) -> str:
     os.makedirs(LIB_DIR, exist_ok=True)
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         results = list(ex.map(lambda s: _compile(s, verbose), SOURCES))
+    with open(_flags_stamp(), "w") as f:
+        f.write(" ".join(_extra_flags()))
     objs = [o for o, _ in results]
     if not os.path.exists(LIB_PATH) or any(os.path.getmtime(o) > os.path.getmtime(LIB_PATH) for o in objs):
         tmp = LIB_PATH + ".tmp"

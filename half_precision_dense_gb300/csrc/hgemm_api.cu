@@ -16,6 +16,7 @@ using hg::TcParams;
 thread_local std::string t_last_error;
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 std::atomic<int> g_inject{0};
+std::atomic<unsigned long long*> g_trace{nullptr};
 
 hgemm_status_t cuda_fail(cudaError_t e, const char* where) {
     t_last_error = std::string(where) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
@@ -81,9 +82,10 @@ EncodeTiledFn encode_fn() {
 
 // A 2-D row-major matrix of 16-bit values: `cols` contiguous values per row,
 // `ld` values between rows; box = box_cols x box_rows, 128-byte swizzle,
-// out-of-range elements read as zero.
+// out-of-range elements read as zero. 128-byte swizzle unless given.
 hgemm_status_t encode_2d(CUtensorMap* m, hgemm_dtype_t dt, const void* base, int64_t rows,
-                         int64_t cols, int64_t ld, uint32_t box_cols, uint32_t box_rows) {
+                         int64_t cols, int64_t ld, uint32_t box_cols, uint32_t box_rows,
+                         CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) {
         t_last_error = "cuTensorMapEncodeTiled is not available from the driver";
@@ -95,7 +97,7 @@ hgemm_status_t encode_2d(CUtensorMap* m, hgemm_dtype_t dt, const void* base, int
     const cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(m, dt == HGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                     2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         t_last_error = "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(static_cast<int>(r));
@@ -106,7 +108,8 @@ hgemm_status_t encode_2d(CUtensorMap* m, hgemm_dtype_t dt, const void* base, int
 
 // ----------------------------------------------------------------- planner
 bool valid_shape_config(int cg, int bn) {
-    return (cg == 1 && (bn == 64 || bn == 128 || bn == 256)) || (cg == 2 && (bn == 128 || bn == 256));
+    return (cg == 1 && (bn == 64 || bn == 128 || bn == 256)) ||
+           (cg == 2 && (bn == 128 || bn == 224 || bn == 256));
 }
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -117,11 +120,27 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // re-read A for fewer columns per MMA.
 double shape_efficiency(int cg, int bn) {
     if (cg == 2 && bn == 256) return 1.00;
+    if (cg == 2 && bn == 224) return 0.86;
     if (cg == 1 && bn == 256) return 0.84;
     if (cg == 1 && bn == 128) return 0.62;
     if (cg == 2 && bn == 128) return 0.61;
     return 0.31;  // cg 1, bn 64
 }
+
+// Measured time constants of the kernel on GB300: the mainloop rate of one SM
+// at efficiency 1 (flop/s), the start-up plus last-epilogue time that no tile
+// overlaps, and the fixed cost of a K-split tail (its parts' partial sums
+// written, waited for and added) per extra part, for a 256-wide tile.
+constexpr double kSmFlops = 13.4e12;
+constexpr double kFixedSec = 4.5e-6;
+constexpr double kSplitBaseSec = 12.0e-6;
+constexpr double kSplitPartSec = 2.0e-6;
+// Epilogue time per 64-column chunk of a CTA's 128-row tile (TMEM load,
+// conversion, staging, TMA store); a CTA pair hands tensor memory back across
+// the pair, which costs about half as much again. A tile takes at least this
+// long even when its K loop is short: the epilogue of one tile overlaps the
+// mainloop of the next, so the slower of the two sets the pace.
+constexpr double kEpiChunkSec = 0.45e-6;
 
 // K parts for the `rem` tiles left after the last whole wave on `clusters`
 // clusters: as many as keep every part on its own cluster, at most one per K
@@ -134,16 +153,45 @@ int64_t auto_split(int64_t rem, int64_t clusters, int64_t num_kb) {
     return s >= 2 ? s : 1;
 }
 
+double tile_seconds(int cg, int bn, int64_t num_kb) {
+    const double mainloop = 2.0 * 128 * bn * (num_kb * hg::kBlockK) / (kSmFlops * shape_efficiency(cg, bn));
+    const double epilogue = kEpiChunkSec * ((bn + 63) / 64) * (cg == 2 ? 1.5 : 1.0);
+    return mainloop > epilogue ? mainloop : epilogue;
+}
+
+double split_fixup_seconds(int bn, int64_t split) {
+    return (kSplitBaseSec + kSplitPartSec * (split - 1)) * bn / 256.0;
+}
+
+// The K-split of the last wave, or 1 when the parts' fix-up (partial sums
+// written, waited for and added) would cost more than the shorter wave saves.
+int64_t worthwhile_split(int cg, int bn, int64_t rem, int64_t clusters, int64_t num_kb) {
+    const int64_t s = auto_split(rem, clusters, num_kb);
+    if (s < 2) return 1;
+    const double t = tile_seconds(cg, bn, num_kb);
+    return (t / s + split_fixup_seconds(bn, s) < t) ? s : 1;
+}
+
 // Fill the schedule fields of `pl` (tiles already set) for `clusters`
 // resident clusters: whole-tile units first, then the K-split tail.
 void schedule_plan(hgemm_plan_t* pl, int64_t clusters, int split_cfg, int64_t num_kb) {
     const int64_t tiles = pl->num_tiles;
     if (clusters < 1) clusters = 1;
-    const int64_t rem = tiles % clusters;
+    int64_t rem = tiles % clusters;
     int64_t s = 1;
-    if (split_cfg >= 2) s = rem > 0 ? (split_cfg < num_kb ? split_cfg : num_kb) : 1;
-    else if (split_cfg == 0) s = auto_split(rem, clusters, num_kb);
+    if (split_cfg >= 2) {
+        s = rem > 0 ? (split_cfg < num_kb ? split_cfg : num_kb) : 1;
+    } else if (split_cfg == 0) {
+        s = worthwhile_split(pl->cta_group, pl->block_n, rem, clusters, num_kb);
+    }
     if (s < 2) s = 1;
+    if (s == 1 && rem > 0) {
+        // Whole waves only: spread them over as few clusters as give the same
+        // wave count (less contention for L2 and HBM, same finish time).
+        const int64_t waves = (tiles + clusters - 1) / clusters;
+        clusters = (tiles + waves - 1) / waves;
+        rem = tiles % clusters;
+    }
     pl->split_k = static_cast<int32_t>(s);
     pl->dp_tiles = static_cast<int32_t>(s > 1 ? tiles - rem : tiles);
     pl->num_units = hg::work_units(pl->num_tiles, pl->dp_tiles, pl->split_k);
@@ -191,28 +239,31 @@ WorkspaceLayout workspace_layout(const hgemm_plan_t& pl, int64_t M, int64_t N, i
 
 // Pick (cta_group, block_n) minimising the estimated time: whole waves of
 // tiles over the resident clusters plus the (K-split) tail, each tile costing
-// its padded area over the shape's efficiency, plus a per-unit fixed cost that
-// favours fewer, larger tiles when the K loop is short. A problem with a
-// single 128-row tile row keeps one CTA per tile (a pair would compute an
-// empty half).
+// its padded area at the shape's efficiency, plus the fixed costs above. A
+// problem with a single 128-row tile row keeps one CTA per tile (a pair would
+// compute an empty half).
+double estimate_seconds(int64_t M, int64_t N, int64_t K, int cg, int bn, int64_t clusters) {
+    const int64_t kb = cdiv(K, hg::kBlockK);
+    const int64_t tiles = cdiv(M, 128 * cg) * cdiv(N, bn);
+    const int64_t rem = tiles % clusters;
+    const int64_t split = worthwhile_split(cg, bn, rem, clusters, kb);
+    const double tile_sec = tile_seconds(cg, bn, kb);
+    double t = static_cast<double>(tiles / clusters) * tile_sec;
+    if (rem > 0) t += split > 1 ? tile_sec / split + split_fixup_seconds(bn, split) : tile_sec;
+    return t + kFixedSec;
+}
+
 void choose_shape(int64_t M, int64_t N, int64_t K, int sms, int max_clusters, int* cg_out, int* bn_out) {
-    static const int cand[5][2] = {{2, 256}, {1, 256}, {1, 128}, {2, 128}, {1, 64}};
+    static const int cand[6][2] = {{2, 256}, {2, 224}, {1, 256}, {1, 128}, {2, 128}, {1, 64}};
     double best = 1e300;
     int bcg = 2, bbn = 256;
-    const int64_t kb = cdiv(K, hg::kBlockK);
     for (const auto& c : cand) {
         const int cg = c[0], bn = c[1];
         if (cg == 2 && M <= 128) continue;
-        const int64_t tiles = cdiv(M, 128 * cg) * cdiv(N, bn);
         int64_t clusters = sms / cg;
         if (max_clusters > 0 && max_clusters < clusters) clusters = max_clusters;
         if (clusters <= 0) continue;
-        const int64_t rem = tiles % clusters;
-        const int64_t split = auto_split(rem, clusters, kb);
-        const double waves = static_cast<double>(tiles / clusters) + (rem ? 1.0 / split : 0.0);
-        const double tile_work = static_cast<double>(128) * bn * (kb * hg::kBlockK);  // per SM
-        const double tile_time = tile_work / shape_efficiency(cg, bn) + 128.0 * bn * 64.0;
-        const double t = waves * tile_time;
+        const double t = estimate_seconds(M, N, K, cg, bn, clusters);
         if (t < best * 0.999) {
             best = t;
             bcg = cg;
@@ -228,7 +279,7 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, const hgemm_config_t* 
     std::memset(pl, 0, sizeof(*pl));
     hgemm_config_t c{};
     if (cfg) c = *cfg;
-    if (c.group_m < 0 || c.max_clusters < 0 || c.store_mode < 0 || c.store_mode > 2 || c.split_k < 0) {
+    if (c.group_m < 0 || c.max_clusters < 0 || c.store_mode < 0 || c.store_mode > 3 || c.split_k < 0) {
         t_last_error = "negative or unknown config field";
         return HGEMM_ERR_INVALID_ARG;
     }
@@ -255,7 +306,7 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, const hgemm_config_t* 
     pl->block_k = hg::kBlockK;
     pl->stages = hg::tc_stages(cg, bn);
     pl->smem_bytes = hg::tc_smem_bytes(cg, bn);
-    pl->tmem_cols = 2 * bn;
+    pl->tmem_cols = hg::tc_tmem_cols(cg, bn);
     pl->tiles_m = static_cast<int32_t>(cdiv(M, pl->block_m));
     pl->tiles_n = static_cast<int32_t>(cdiv(N, bn));
     pl->num_tiles = pl->tiles_m * pl->tiles_n;
@@ -266,8 +317,8 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, const hgemm_config_t* 
     pl->repack_a = a_unaligned ? 1 : 0;
     pl->repack_b = b_unaligned ? 1 : 0;
     pl->store_mode = (c.store_mode != 0) ? c.store_mode : (c_unaligned ? 2 : 1);
-    if (c_unaligned && pl->store_mode == 1) {
-        t_last_error = "TMA stores need a 16-byte aligned C with an 16-byte row pitch";
+    if (c_unaligned && (pl->store_mode == 1 || pl->store_mode == 3)) {
+        t_last_error = "vector and TMA stores need a 16-byte aligned C with a 16-byte row pitch";
         return HGEMM_ERR_INVALID_ARG;
     }
     pl->workspace_bytes = workspace_layout(*pl, M, N, K).total;
@@ -426,12 +477,16 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
         }
     }
 
-    CUtensorMap ta, tb, tc;
+    CUtensorMap ta, tb, tc, tc32;
     std::memset(&tc, 0, sizeof(tc));
+    std::memset(&tc32, 0, sizeof(tc32));
     if ((st = encode_2d(&ta, dtype, a_use, M, K, lda, hg::kBlockK, hg::kBlockMCta)) != HGEMM_OK ||
         (st = encode_2d(&tb, dtype, b_use, K, N, ldb, 64, hg::kBlockK)) != HGEMM_OK ||
         (pl.store_mode == 1 &&
-         (st = encode_2d(&tc, dtype, C, M, N, N, hg::kEpiBoxCols, hg::kEpiBoxRows)) != HGEMM_OK)) {
+         (st = encode_2d(&tc, dtype, C, M, N, N, hg::kEpiBoxCols, hg::kEpiBoxRows)) != HGEMM_OK) ||
+        (pl.store_mode == 1 && bn % 64 != 0 &&
+         (st = encode_2d(&tc32, dtype, C, M, N, N, 32, hg::kEpiBoxRows, CU_TENSOR_MAP_SWIZZLE_64B)) !=
+             HGEMM_OK)) {
         if (work && work != scratch) cudaFreeAsync(work, stream);
         return st;
     }
@@ -464,13 +519,14 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
                   : nullptr;
     p.epoch = next_epoch();
     p.inject = g_inject.load(std::memory_order_relaxed);
+    p.trace = g_trace.load(std::memory_order_relaxed);
     if ((e = hg::status_word_ptr(&p.status)) != cudaSuccess) {
         if (work && work != scratch) cudaFreeAsync(work, stream);
         return cuda_fail(e, "status word");
     }
 
-    e = dtype == HGEMM_BF16 ? hg::launch_tc_bf16(cg, bn, ta, tb, tc, p, clusters, stream)
-                            : hg::launch_tc_f16(cg, bn, ta, tb, tc, p, clusters, stream);
+    e = dtype == HGEMM_BF16 ? hg::launch_tc_bf16(cg, bn, ta, tb, tc, tc32, p, clusters, stream)
+                            : hg::launch_tc_f16(cg, bn, ta, tb, tc, tc32, p, clusters, stream);
     if (work && work != scratch) cudaFreeAsync(work, stream);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     return HGEMM_OK;
@@ -583,6 +639,12 @@ hgemm_status_t hgemm_get_device_status(int32_t device, int32_t reset, uint32_t* 
 }
 
 void hgemm_set_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 1, std::memory_order_relaxed); }
+
+#ifdef HG_TRACE
+// Traced builds only: device buffer for the kernels' timeline records
+// (grid_ctas x kTraceUnits x kTraceFields u64), or null.
+void hgemm_trace_set(void* buf) { g_trace.store(static_cast<unsigned long long*>(buf)); }
+#endif
 
 void hgemm_test_inject(int32_t kind) { g_inject.store(kind == 1 ? 1 : 0, std::memory_order_relaxed); }
 

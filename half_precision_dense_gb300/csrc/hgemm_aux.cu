@@ -90,7 +90,18 @@ int tc_stages(int cta_group, int block_n) {
     if (cta_group == 1 && block_n == 128) return TcCfg<1, 128>::kStages;
     if (cta_group == 1 && block_n == 256) return TcCfg<1, 256>::kStages;
     if (cta_group == 2 && block_n == 128) return TcCfg<2, 128>::kStages;
+    if (cta_group == 2 && block_n == 224) return TcCfg<2, 224>::kStages;
     if (cta_group == 2 && block_n == 256) return TcCfg<2, 256>::kStages;
+    return 0;
+}
+
+int tc_tmem_cols(int cta_group, int block_n) {
+    if (cta_group == 1 && block_n == 64) return TcCfg<1, 64>::kTmemCols;
+    if (cta_group == 1 && block_n == 128) return TcCfg<1, 128>::kTmemCols;
+    if (cta_group == 1 && block_n == 256) return TcCfg<1, 256>::kTmemCols;
+    if (cta_group == 2 && block_n == 128) return TcCfg<2, 128>::kTmemCols;
+    if (cta_group == 2 && block_n == 224) return TcCfg<2, 224>::kTmemCols;
+    if (cta_group == 2 && block_n == 256) return TcCfg<2, 256>::kTmemCols;
     return 0;
 }
 
@@ -99,6 +110,7 @@ int tc_smem_bytes(int cta_group, int block_n) {
     if (cta_group == 1 && block_n == 128) return TcCfg<1, 128>::kSmemBytes;
     if (cta_group == 1 && block_n == 256) return TcCfg<1, 256>::kSmemBytes;
     if (cta_group == 2 && block_n == 128) return TcCfg<2, 128>::kSmemBytes;
+    if (cta_group == 2 && block_n == 224) return TcCfg<2, 224>::kSmemBytes;
     if (cta_group == 2 && block_n == 256) return TcCfg<2, 256>::kSmemBytes;
     return 0;
 }

@@ -63,7 +63,8 @@ struct TcParams {
     int32_t tiles_m, tiles_n, num_tiles, group_m;
     int32_t num_kb;                 // ceil(K / kBlockK)
     uint32_t idesc;                 // tcgen05 instruction descriptor
-    int32_t store_mode;             // 1: TMA stores of C; 2: plain stores through `C`
+    int32_t store_mode;             // 1: TMA stores of C; 2: plain 2-byte stores through `C`;
+                                    // 3: direct 16-byte stores through `C` (aligned C only)
     uint16_t* C;                    // used by store_mode 2
     int64_t ldc;                    // elements between C rows (store_mode 2)
     uint64_t timeout_ns;
@@ -76,7 +77,36 @@ struct TcParams {
     unsigned long long epoch;       // unique per launch
     int32_t inject;                 // test hook: 1 = the owner of split tile 0 waits for a
                                     // partial that is never published (its wait runs out)
+    unsigned long long* trace;      // timeline records (builds with HG_TRACE only), or null
 };
+
+// Timeline records of a traced build: per CTA, per unit it takes (up to
+// kTraceUnits), kTraceFields %globaltimer stamps.
+constexpr int kTraceUnits = 32;
+constexpr int kTraceFields = 8;
+enum : int { kTrProdFirst = 0, kTrMmaFirst = 1, kTrMmaLast = 2, kTrEpiStart = 3, kTrEpiTmemFree = 4,
+             kTrEpiEnd = 5, kTrUnit = 6, kTrSetup = 7 };
+// Epilogue detail of a CTA's first unit (warp 0): slot 16 + c, field f.
+enum : int { kTcLdDone = 0, kTcWaitRead = 1, kTcStaged = 2, kTcIssued = 3 };
+__device__ __forceinline__ void trace_chunk(const TcParams& p, int it, int c, int field) {
+#ifdef HG_TRACE
+    if (p.trace && it == 0 && c < 16)
+        p.trace[(static_cast<int64_t>(blockIdx.x) * kTraceUnits + 16 + c) * kTraceFields + field] =
+            globaltimer_ns();
+#else
+    (void)p; (void)it; (void)c; (void)field;
+#endif
+}
+
+__device__ __forceinline__ void trace_stamp(const TcParams& p, int local_unit, int field) {
+#ifdef HG_TRACE
+    if (p.trace && local_unit < kTraceUnits)
+        p.trace[(static_cast<int64_t>(blockIdx.x) * kTraceUnits + local_unit) * kTraceFields + field] =
+            globaltimer_ns();
+#else
+    (void)p; (void)local_unit; (void)field;
+#endif
+}
 
 // Index of the partial block written by part `part` (< split - 1) of split
 // tile `split_idx` for CTA rank `rank` and epilogue warp `warp`: 32 rows x BN
@@ -87,23 +117,33 @@ __device__ __forceinline__ int64_t partial_block(int32_t split_idx, int32_t part
     return ((static_cast<int64_t>(split_idx) * (split - 1) + part) * CG + rank) * kEpiWarps + warp;
 }
 
+constexpr int pow2_at_least(int x) {
+    int p = 32;
+    while (p < x) p *= 2;
+    return p;
+}
+
 template <int CG, int BN>
 struct TcCfg {
-    static constexpr int kBnCta = BN / CG;                 // B columns loaded by each CTA
+    static constexpr int kBnCta = BN / CG;                 // B columns each CTA feeds the MMA
     static constexpr int kABytes = kBlockMCta * kBlockK * 2;
-    static constexpr int kBBytes = kBlockK * kBnCta * 2;
+    static constexpr int kBAtoms = (kBnCta + 63) / 64;     // 64-column swizzle atoms loaded
     static constexpr int kBAtomBytes = kBlockK * 128;      // 64 columns x 64 k-rows
+    static constexpr int kBBytes = kBAtoms * kBAtomBytes;
+    static constexpr int kChunks = (BN + 63) / 64;         // epilogue chunks of 64 columns
+    static constexpr bool kHalfLast = (BN % 64) != 0;      // the last chunk is 32 columns
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBoxBytes;
     static constexpr int kBarBytes = 256;
     static constexpr int kStagesFit = (kSmemLimit - 1024 - kEpiBytes - kBarBytes) / kStageBytes;
     static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
     static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiBytes + kBarBytes;
-    static constexpr int kTmemCols = 2 * BN;               // two accumulators of BN fp32 columns
+    static constexpr int kTmemCols = pow2_at_least(2 * BN);  // two accumulators of BN fp32 columns
     static constexpr uint32_t kTxBytes = CG * kStageBytes; // bytes landing per stage on the leader's barrier
     static_assert(CG == 1 || CG == 2, "cta group");
-    static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
-    static_assert(kBnCta % 64 == 0, "B is loaded in 64-column swizzle atoms");
+    static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "tile width");
+    static_assert(kBnCta % 16 == 0, "MMA N per CTA");
+    static_assert(kTmemCols <= 512, "tensor memory");
     static_assert(kStages >= 2, "pipeline depth");
     static_assert(kSmemBytes <= kSmemLimit, "shared memory");
     static_assert((2 * kStages + 5) * 8 + 8 <= kBarBytes, "barrier area");
@@ -213,7 +253,8 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
 template <int CG, int BN, bool kBF16>
 __global__ void __launch_bounds__(kThreads, 1)
 hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmC, const TcParams p) {
+                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC32,
+                const TcParams p) {
 #if defined(__CUDA_ARCH__) && defined(__CUDA_ARCH_FEAT_SM103_ALL)
     using Cfg = TcCfg<CG, BN>;
     constexpr int S = Cfg::kStages;
@@ -257,6 +298,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
         if (p.store_mode == 1) tma_prefetch_desc(&tmC);
+        if (p.store_mode == 1 && Cfg::kHalfLast) tma_prefetch_desc(&tmC32);
     }
     if (warp == kMmaWarp) tmem_alloc<CG>(smem_addr(tmem_slot), Cfg::kTmemCols);
     tc_fence_before();
@@ -265,14 +307,17 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
     const Waiter w{abort_flag, p.timeout_ns, p.status};
+    if (threadIdx.x == 0) trace_stamp(p, 0, kTrSetup);
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             uint32_t stage = 0, phase = 0;
             bool ok = true;
-            for (int u = cluster_id; u < p.num_units && ok; u += num_clusters) {
+            int lu = 0;
+            for (int u = cluster_id; u < p.num_units && ok; u += num_clusters, ++lu) {
                 const WorkUnit wu = work_unit(u, p.dp_units, p.split, p.num_kb);
+                trace_stamp(p, lu, kTrProdFirst);
                 int32_t tm, tn;
                 tile_coord(wu.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
                 const int32_t m0 = tm * (kBlockMCta * CG) + static_cast<int32_t>(rank) * kBlockMCta;
@@ -290,14 +335,14 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
                         tma_load_2d(a_dst, &tmA, fb, k0, m0);
 #pragma unroll
-                        for (int j = 0; j < Cfg::kBnCta / 64; ++j)
+                        for (int j = 0; j < Cfg::kBAtoms; ++j)
                             tma_load_2d(b_dst + j * Cfg::kBAtomBytes, &tmB, fb, n0 + 64 * j, k0);
                     } else {
                         const uint32_t fb_leader = mapa_shared(fb, 0);
                         if (rank == 0) mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
                         tma_load_2d_pair(a_dst, &tmA, fb_leader, k0, m0);
 #pragma unroll
-                        for (int j = 0; j < Cfg::kBnCta / 64; ++j)
+                        for (int j = 0; j < Cfg::kBAtoms; ++j)
                             tma_load_2d_pair(b_dst + j * Cfg::kBAtomBytes, &tmB, fb_leader,
                                              n0 + 64 * j, k0);
                     }
@@ -337,6 +382,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         break;
                     }
                     tc_fence_after();
+                    if (kb == wu.kb0) trace_stamp(p, it, kTrMmaFirst);
                     const uint32_t a0 = sA + stage * Cfg::kABytes;
                     const uint32_t b0 = sB + stage * Cfg::kBBytes;
 #pragma unroll
@@ -356,6 +402,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 if (!ok) break;
                 if constexpr (CG == 1) umma_commit(bar_tfull + 8 * acc);
                 else umma_commit_pair(bar_tfull + 8 * acc, 0x3);
+                trace_stamp(p, it, kTrMmaLast);
             }
             if (!ok && issued) {
                 // TMEM may only be freed once every issued MMA has completed.
@@ -376,6 +423,14 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             const uint32_t acc_phase = (static_cast<uint32_t>(it) >> 1) & 1u;
             if (!wait_bar(bar_tfull + 8 * acc, acc_phase, w, kRoleEpilogue, 32 + acc)) break;
             tc_fence_after();
+            if (warp == 0 && lane == 0) {
+                trace_stamp(p, it, kTrEpiStart);
+#ifdef HG_TRACE
+                if (p.trace && it < kTraceUnits)
+                    p.trace[(static_cast<int64_t>(blockIdx.x) * kTraceUnits + it) * kTraceFields + kTrUnit] =
+                        static_cast<unsigned long long>(u);
+#endif
+            }
             int32_t tm, tn;
             tile_coord(wu.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
             const int32_t row0 = tm * (kBlockMCta * CG) + static_cast<int32_t>(rank) * kBlockMCta +
@@ -383,14 +438,23 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             const int32_t col0 = tn * BN;
             const uint32_t t_row = tmem_base + acc * BN + (static_cast<uint32_t>(warp * 32) << 16);
 #pragma unroll 1
-            for (int c = 0; c < BN / 64; ++c) {
+            for (int c = 0; c < Cfg::kChunks; ++c) {
+                // A chunk is 64 columns (two 32-column TMEM loads), or 32 for the
+                // last chunk of a tile whose width is an odd multiple of 32.
+                const bool half = Cfg::kHalfLast && c == Cfg::kChunks - 1;
+                const bool last = c == Cfg::kChunks - 1;
                 uint32_t r0[32], r1[32];
                 tmem_ld_32x32b_x32(t_row + 64u * c, r0);
-                tmem_ld_32x32b_x32(t_row + 64u * c + 32u, r1);
+                if (!half) tmem_ld_32x32b_x32(t_row + 64u * c + 32u, r1);
                 tmem_ld_wait();
                 reg_fence(r0);
+                if (half) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r1[i] = 0u;
+                }
                 reg_fence(r1);
-                if (c == BN / 64 - 1) {
+                if (warp == 0 && lane == 0) trace_chunk(p, it, c, kTcLdDone);
+                if (last) {
                     // Every TMEM read of this accumulator is done: hand it back.
                     tc_fence_before();
                     __syncwarp();
@@ -401,6 +465,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         } else {
                             mbar_arrive_cluster(mapa_shared(bar_tempty + 8 * acc, 0));
                         }
+                        if (warp == 0) trace_stamp(p, it, kTrEpiTmemFree);
                     }
                 }
                 if (wu.split_idx >= 0) {
@@ -416,11 +481,12 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                             dst[(c * 16 + j) * 32 + lane] =
                                 make_float4(__uint_as_float(r0[4 * j]), __uint_as_float(r0[4 * j + 1]),
                                             __uint_as_float(r0[4 * j + 2]), __uint_as_float(r0[4 * j + 3]));
-                            dst[(c * 16 + 8 + j) * 32 + lane] =
-                                make_float4(__uint_as_float(r1[4 * j]), __uint_as_float(r1[4 * j + 1]),
-                                            __uint_as_float(r1[4 * j + 2]), __uint_as_float(r1[4 * j + 3]));
+                            if (!half)
+                                dst[(c * 16 + 8 + j) * 32 + lane] =
+                                    make_float4(__uint_as_float(r1[4 * j]), __uint_as_float(r1[4 * j + 1]),
+                                                __uint_as_float(r1[4 * j + 2]), __uint_as_float(r1[4 * j + 3]));
                         }
-                        if (c == BN / 64 - 1) {
+                        if (last) {
                             __threadfence();
                             __syncwarp();
                             if (lane == 0)
@@ -451,15 +517,17 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
                             const float4 a = __ldcg(src + (c * 16 + j) * 32 + lane);
-                            const float4 b = __ldcg(src + (c * 16 + 8 + j) * 32 + lane);
                             r0[4 * j] = __float_as_uint(__uint_as_float(r0[4 * j]) + a.x);
                             r0[4 * j + 1] = __float_as_uint(__uint_as_float(r0[4 * j + 1]) + a.y);
                             r0[4 * j + 2] = __float_as_uint(__uint_as_float(r0[4 * j + 2]) + a.z);
                             r0[4 * j + 3] = __float_as_uint(__uint_as_float(r0[4 * j + 3]) + a.w);
-                            r1[4 * j] = __float_as_uint(__uint_as_float(r1[4 * j]) + b.x);
-                            r1[4 * j + 1] = __float_as_uint(__uint_as_float(r1[4 * j + 1]) + b.y);
-                            r1[4 * j + 2] = __float_as_uint(__uint_as_float(r1[4 * j + 2]) + b.z);
-                            r1[4 * j + 3] = __float_as_uint(__uint_as_float(r1[4 * j + 3]) + b.w);
+                            if (!half) {
+                                const float4 b = __ldcg(src + (c * 16 + 8 + j) * 32 + lane);
+                                r1[4 * j] = __float_as_uint(__uint_as_float(r1[4 * j]) + b.x);
+                                r1[4 * j + 1] = __float_as_uint(__uint_as_float(r1[4 * j + 1]) + b.y);
+                                r1[4 * j + 2] = __float_as_uint(__uint_as_float(r1[4 * j + 2]) + b.z);
+                                r1[4 * j + 3] = __float_as_uint(__uint_as_float(r1[4 * j + 3]) + b.w);
+                            }
                         }
                     }
                 }
@@ -469,44 +537,80 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     pk[i] = pack_rn<kBF16>(r0[2 * i], r0[2 * i + 1]);
                     pk[16 + i] = pack_rn<kBF16>(r1[2 * i], r1[2 * i + 1]);
                 }
+                const int32_t ccol = col0 + 64 * c;
+                if (p.store_mode == 3) {
+                    // Direct 16-byte stores: thread `lane` writes its own row of the
+                    // chunk (C is 16-byte aligned with a pitch of a multiple of 8
+                    // elements, and N is a multiple of 8, so a vector is either
+                    // wholly inside C or wholly outside).
+                    const int32_t row = row0 + static_cast<int32_t>(lane);
+                    if (row < p.M) {
+                        uint16_t* crow = p.C + static_cast<int64_t>(row) * p.ldc;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const int32_t col = ccol + 8 * j;
+                            if ((!half || j < 4) && col < p.N)
+                                *reinterpret_cast<uint4*>(crow + col) =
+                                    make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                        }
+                    }
+                    continue;
+                }
                 const uint32_t box = my_boxes + buf * kEpiBoxBytes;
                 if (p.store_mode == 1) {
                     // The store issued from this box two chunks ago must have read it.
                     if (lane == 0) bulk_wait_group_read<1>();
                     __syncwarp();
+                    if (warp == 0 && lane == 0) trace_chunk(p, it, c, kTcWaitRead);
                 }
-                // Row `lane` of the box: 16 B chunk j goes to chunk j ^ (row % 8),
-                // the 128-byte swizzle that the TMA store undoes. Each group of 8
-                // lanes covers 8 distinct chunk positions: no bank conflicts.
-                const uint32_t row_addr = box + lane * 128u;
+                // Row `lane` of the box. A 64-column box has 128-byte rows and
+                // the 128-byte swizzle: 16 B chunk j goes to j ^ (row % 8). A
+                // 32-column box has 64-byte rows and the 64-byte swizzle: chunk j
+                // goes to j ^ ((row / 2) % 4). Either way each group of 8 lanes
+                // covers all 32 banks once, and the TMA store undoes the swizzle.
+                if (!half) {
+                    const uint32_t row_addr = box + lane * 128u;
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4),
-                                 pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-                const int32_t ccol = col0 + 64 * c;
+                    for (int j = 0; j < 8; ++j)
+                        st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4),
+                                     pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                } else {
+                    const uint32_t row_addr = box + lane * 64u;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ ((lane >> 1) & 3u)) << 4),
+                                     pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                }
                 if (p.store_mode == 1) {
                     fence_proxy_async_smem();
                     __syncwarp();
+                    if (warp == 0 && lane == 0) trace_chunk(p, it, c, kTcStaged);
                     if (lane == 0) {
-                        if (row0 < p.M && ccol < p.N) tma_store_2d(&tmC, box, ccol, row0);
+                        if (row0 < p.M && ccol < p.N) {
+                            if (half) tma_store_2d(&tmC32, box, ccol, row0);
+                            else tma_store_2d(&tmC, box, ccol, row0);
+                        }
                         bulk_commit_group();
                     }
+                    if (warp == 0 && lane == 0) trace_chunk(p, it, c, kTcIssued);
                     buf ^= 1u;
                 } else {
                     __syncwarp();
                     const uint8_t* bx = smem + (box - base);
+                    const uint32_t width = half ? 32u : 64u;
 #pragma unroll 1
                     for (int rr = 0; rr < kEpiBoxRows; ++rr) {
                         const int32_t row = row0 + rr;
                         if (row >= p.M) break;
+                        const uint32_t urr = static_cast<uint32_t>(rr);
 #pragma unroll
                         for (int q = 0; q < 2; ++q) {
                             const uint32_t cc = lane * 2u + q;          // column in the box
                             const int32_t col = ccol + static_cast<int32_t>(cc);
-                            if (col < p.N) {
-                                const uint32_t off = rr * 128u +
-                                                     (((cc >> 3) ^ (static_cast<uint32_t>(rr) & 7u)) << 4) +
-                                                     ((cc & 7u) << 1);
+                            if (cc < width && col < p.N) {
+                                const uint32_t off =
+                                    half ? urr * 64u + (((cc >> 3) ^ ((urr >> 1) & 3u)) << 4) + ((cc & 7u) << 1)
+                                         : urr * 128u + (((cc >> 3) ^ (urr & 7u)) << 4) + ((cc & 7u) << 1);
                                 p.C[static_cast<int64_t>(row) * p.ldc + col] =
                                     *reinterpret_cast<const uint16_t*>(bx + off);
                             }
@@ -515,6 +619,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     __syncwarp();
                 }
             }
+            if (warp == 0 && lane == 0) trace_stamp(p, it, kTrEpiEnd);
         }
         if (lane == 0) bulk_wait_group<0>();
         __syncwarp();

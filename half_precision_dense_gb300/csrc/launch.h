@@ -13,12 +13,14 @@ namespace hg {
 
 // Launch the tcgen05 kernel for (cta_group, block_n) with `clusters` CTA
 // clusters on `stream`. Returns cudaErrorInvalidValue for an unknown pair.
+// `c` stores 64-column chunks of C; `c32` the 32-column last chunk of tiles
+// whose width is an odd multiple of 32.
 cudaError_t launch_tc_bf16(int cta_group, int block_n, const CUtensorMap& a, const CUtensorMap& b,
-                           const CUtensorMap& c, const TcParams& p, int clusters,
-                           cudaStream_t stream);
+                           const CUtensorMap& c, const CUtensorMap& c32, const TcParams& p,
+                           int clusters, cudaStream_t stream);
 cudaError_t launch_tc_f16(int cta_group, int block_n, const CUtensorMap& a, const CUtensorMap& b,
-                          const CUtensorMap& c, const TcParams& p, int clusters,
-                          cudaStream_t stream);
+                          const CUtensorMap& c, const CUtensorMap& c32, const TcParams& p,
+                          int clusters, cudaStream_t stream);
 
 // Most CTA clusters of the (cta_group, block_n) kernel that can be resident at
 // once on the current device (0 on error).
@@ -28,6 +30,7 @@ int max_active_clusters_f16(int cta_group, int block_n);
 // Shared-memory ring depth and bytes of an instantiation (host constants).
 int tc_stages(int cta_group, int block_n);
 int tc_smem_bytes(int cta_group, int block_n);
+int tc_tmem_cols(int cta_group, int block_n);
 
 // Auxiliary kernels (hgemm_aux.cu).
 cudaError_t launch_repack(const uint16_t* src, int64_t rows, int64_t cols, uint16_t* dst,

@@ -46,22 +46,34 @@ struct TcInstance {
     }
 
     static cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                              const TcParams& p, int clusters, cudaStream_t stream) {
+                              const CUtensorMap& c32, const TcParams& p, int clusters,
+                              cudaStream_t stream) {
         cudaError_t e = prepare();
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t cfg;
         cudaLaunchAttribute attr[1];
         fill_config(cfg, attr, clusters, stream);
-        return cudaLaunchKernelEx(&cfg, kernel(), a, b, c, p);
+        return cudaLaunchKernelEx(&cfg, kernel(), a, b, c, c32, p);
     }
 
+    // Resident clusters per device, queried once per device.
     static int max_clusters() {
+        static std::mutex mu;
+        static int cache[64] = {};
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+        {
+            std::lock_guard<std::mutex> lk(mu);
+            if (cache[dev] > 0) return cache[dev];
+        }
         if (prepare() != cudaSuccess) return 0;
         cudaLaunchConfig_t cfg;
         cudaLaunchAttribute attr[1];
         fill_config(cfg, attr, 1, nullptr);
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, kernel(), &cfg) != cudaSuccess) return 0;
+        std::lock_guard<std::mutex> lk(mu);
+        cache[dev] = n;
         return n;
     }
 };
@@ -71,6 +83,7 @@ struct TcInstance {
     if (cta_group == 1 && block_n == 128) return TcInstance<1, 128, KBF16>::CALL;            \
     if (cta_group == 1 && block_n == 256) return TcInstance<1, 256, KBF16>::CALL;            \
     if (cta_group == 2 && block_n == 128) return TcInstance<2, 128, KBF16>::CALL;            \
+    if (cta_group == 2 && block_n == 224) return TcInstance<2, 224, KBF16>::CALL;            \
     if (cta_group == 2 && block_n == 256) return TcInstance<2, 256, KBF16>::CALL;
 
 }  // namespace hg

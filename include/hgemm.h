@@ -120,10 +120,14 @@ uint64_t hgemm_noalloc_scratch_bytes(void);
  * "let the planner choose".
  *   cta_group:     1 = one CTA per 128-row tile; 2 = a CTA pair (cluster of 2)
  *                  sharing a 256-row tile through tcgen05 cta_group::2.
- *   block_n:       columns of C per tile: 64, 128 or 256.
+ *   block_n:       columns of C per tile: 64, 128 or 256 with cta_group 1;
+ *                  128, 224 or 256 with cta_group 2.
  *   group_m:       tile rows per raster group (L2 reuse), >= 1.
  *   max_clusters:  cap on resident CTA clusters (forces more tiles per CTA).
- *   store_mode:    1 = TMA tensor stores of C, 2 = plain per-element stores.
+ *   store_mode:    1 = TMA tensor stores of C (through a swizzled smem box),
+ *                  2 = plain per-element stores, 3 = 16-byte vector stores
+ *                  straight from registers (1 and 3 need a 16-byte aligned C
+ *                  whose row pitch is a multiple of 16 bytes).
  *   split_k:       K-split of the tiles left over after the last whole wave
  *                  (0 = planner's choice, 1 = never split, s >= 2 = s parts,
  *                  capped at the number of 64-deep K blocks).
@@ -173,7 +177,7 @@ typedef struct {
     int32_t tmem_cols;     /* tensor-memory columns allocated per CTA */
     int32_t repack_a;      /* 1 if A goes through the 16-byte-pitch workspace */
     int32_t repack_b;      /* 1 if B does */
-    int32_t store_mode;    /* 1 = TMA stores, 2 = plain stores */
+    int32_t store_mode;    /* 1 = TMA stores, 2 = plain stores, 3 = vector stores */
     int32_t dp_tiles;      /* tiles computed whole (the first dp_tiles in raster order) */
     int32_t split_k;       /* K parts of each remaining tile (1 = no split) */
     int32_t num_units;     /* work units: dp_tiles + (num_tiles - dp_tiles) * split_k */

@@ -123,15 +123,24 @@ def test_plan_shapes(lib):
 
 def test_plan_split_tail(lib):
     # 4096^3 on 152 SMs with pair tiles: 256 tiles, 76 clusters, 3 whole waves,
-    # the 28 leftover tiles split 2 ways over 56 clusters
-    p = binding.plan(4096, 4096, 4096, "bf16", binding.Config(cta_group=2, block_n=256), sm_count=152)
+    # the 28 leftover tiles split 2 ways over 56 clusters when asked
+    p = binding.plan(4096, 4096, 4096, "bf16", binding.Config(cta_group=2, block_n=256, split_k=2),
+                     sm_count=152)
     assert (p["num_tiles"], p["dp_tiles"], p["split_k"], p["num_units"]) == (256, 228, 2, 284)
     assert p["grid_ctas"] == 152
     assert p["workspace_bytes"] >= 28 * 1 * 2 * 4 * 32 * 256 * 4
+    # left to itself, the planner splits a long-K last wave (8192^3) ...
+    q8 = binding.plan(8192, 8192, 8192, "bf16", binding.Config(cta_group=2, block_n=256), sm_count=152)
+    assert (q8["num_tiles"], q8["dp_tiles"], q8["split_k"], q8["num_units"]) == (1024, 988, 2, 1060)
+    # ... but at 4096^3 the fix-up outweighs the half wave: whole waves, spread
+    # evenly (4 waves of 64 clusters instead of 3.37 of 76)
+    b = binding.plan(4096, 4096, 4096, "bf16", binding.Config(cta_group=2, block_n=256), sm_count=152)
+    assert (b["split_k"], b["num_units"], b["grid_ctas"]) == (1, 256, 128)
     # fewer leftover tiles allow more parts (capped at 8 and at the K blocks)
     q = binding.plan(512, 1024, 8192, "bf16", binding.Config(cta_group=2, block_n=256), sm_count=152)
     assert (q["num_tiles"], q["dp_tiles"], q["split_k"], q["num_units"]) == (8, 0, 8, 64)
-    r = binding.plan(512, 1024, 128, "bf16", binding.Config(cta_group=2, block_n=256), sm_count=152)
+    r = binding.plan(512, 1024, 128, "bf16", binding.Config(cta_group=2, block_n=256, split_k=4),
+                     sm_count=152)
     assert r["split_k"] == 2  # only two K blocks
     # split_k = 1 disables it; whole waves leave nothing to split
     off = binding.plan(4096, 4096, 4096, "bf16",

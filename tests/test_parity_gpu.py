@@ -21,9 +21,10 @@ CONFIGS = [
     hg.Config(cta_group=1, block_n=128),
     hg.Config(cta_group=1, block_n=256),
     hg.Config(cta_group=2, block_n=128),
+    hg.Config(cta_group=2, block_n=224),
     hg.Config(cta_group=2, block_n=256),
 ]
-CFG_IDS = ["cg1_n64", "cg1_n128", "cg1_n256", "cg2_n128", "cg2_n256"]
+CFG_IDS = ["cg1_n64", "cg1_n128", "cg1_n256", "cg2_n128", "cg2_n224", "cg2_n256"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -190,9 +191,20 @@ def test_raster_groups(group_m):
     check_full(A, B, "bf16", hg.Config(cta_group=2, block_n=128, group_m=group_m))
 
 
-def test_plain_store_mode_matches():
+@pytest.mark.parametrize("cfg", CONFIGS, ids=CFG_IDS)
+@pytest.mark.parametrize("store_mode", [2, 3])
+def test_store_modes_match(cfg, store_mode):
+    # plain 2-byte stores and direct 16-byte vector stores, ragged M and N
+    c = hg.Config(cfg.cta_group, cfg.block_n, 0, 0, store_mode)
     A, B = operands(700, 520, 300, "bf16", 8)
-    check_full(A, B, "bf16", hg.Config(store_mode=2))
+    check_full(A, B, "bf16", c)
+
+
+@pytest.mark.parametrize("store_mode", [1, 3])
+def test_store_modes_with_split_tail(store_mode):
+    c = hg.Config(2, 224, 0, 3, store_mode, 3)
+    A, B = operands(1024, 1344, 512, "f16", 17)
+    check_full(A, B, "f16", c)
 
 
 @pytest.mark.parametrize("shape", [(300, 517, 264), (129, 4095, 257), (64, 100, 1001), (33, 7, 5)])
