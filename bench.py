@@ -39,7 +39,7 @@ UNIT = "TFLOP/s"
 L2_FLUSH_BYTES = 256 << 20
 # Bumped whenever the GEMM kernel changes, so ncu figures taken on an older
 # kernel are not reported as current.
-KERNEL_REV = 3
+KERNEL_REV = 4
 
 # name -> list of (M, N, K, dtype, dist, sigma, seed) GEMMs making up one step
 WORKLOADS = {
@@ -280,9 +280,9 @@ def run_ours(args, rank, world, local_rank):
     }
     o = ops[0]
     plan = hg.plan(o["M"], o["N"], o["K"], o["dt"])
-    plan_key = [plan["cta_group"], plan["block_n"], plan["split_k"], plan["grid_ctas"]]
+    plan_key = [plan["cta_group"], plan["block_n"], plan["sk_tiles"], plan["grid_ctas"]]
     line["roofline"]["plan"] = {"cta_group": plan_key[0], "block_n": plan_key[1],
-                                "split_k": plan_key[2], "grid_ctas": plan_key[3]}
+                                "stream_k_tiles": plan_key[2], "grid_ctas": plan_key[3]}
     if args.traffic_file and os.path.exists(args.traffic_file):
         # DRAM bytes from an ncu capture count only while the kernel and plan
         # they were taken on are the ones running now.

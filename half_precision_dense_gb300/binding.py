@@ -33,14 +33,15 @@ class HgemmError(RuntimeError):
 class _Config(ctypes.Structure):
     _fields_ = [("cta_group", ctypes.c_int32), ("block_n", ctypes.c_int32),
                 ("group_m", ctypes.c_int32), ("max_clusters", ctypes.c_int32),
-                ("store_mode", ctypes.c_int32), ("split_k", ctypes.c_int32)]
+                ("store_mode", ctypes.c_int32), ("stream_k", ctypes.c_int32)]
 
 
 class _Plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "cta_group", "block_m", "block_n", "block_k", "stages", "group_m", "tiles_m", "tiles_n",
         "num_tiles", "grid_ctas", "smem_bytes", "tmem_cols", "repack_a", "repack_b", "store_mode",
-        "dp_tiles", "split_k", "num_units", "reserved")] + [("workspace_bytes", ctypes.c_int64)]
+        "dp_tiles", "sk_tiles", "sk_blocks", "sk_extra", "num_kb", "reserved")] + \
+        [("workspace_bytes", ctypes.c_int64)]
 
 
 @dataclass
@@ -51,11 +52,11 @@ class Config:
     group_m: int = 0
     max_clusters: int = 0
     store_mode: int = 0
-    split_k: int = 0
+    stream_k: int = 0
 
     def _c(self) -> _Config:
         return _Config(self.cta_group, self.block_n, self.group_m, self.max_clusters, self.store_mode,
-                       self.split_k)
+                       self.stream_k)
 
 
 def library_path() -> str:
@@ -86,6 +87,8 @@ def load_library():
         lib.hgemm_plan.argtypes = [i64, i64, i64, ctypes.c_int, ctypes.POINTER(_Config), i32,
                                    ctypes.POINTER(_Plan)]
         lib.hgemm_plan.restype = ctypes.c_int
+        lib.hgemm_work_unit.argtypes = [ctypes.POINTER(_Plan), i32, i32] + [ctypes.POINTER(i32)] * 4
+        lib.hgemm_work_unit.restype = i32
         lib.hgemm_tile_coord.argtypes = [i32, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
         lib.hgemm_tile_coord.restype = None
         lib.hgemm_get_device_status.argtypes = [i32, i32, ctypes.POINTER(ctypes.c_uint32)]
@@ -171,6 +174,19 @@ def plan(M: int, N: int, K: int, dtype="bf16", config: Config | None = None, sm_
     cfg = ctypes.byref(config._c()) if config is not None else None
     _check(lib.hgemm_plan(M, N, K, _dtype_code(dtype), cfg, sm_count, ctypes.byref(out)))
     return {name: getattr(out, name) for name, _ in _Plan._fields_ if name != "reserved"}
+
+
+def work_units(plan_dict: dict, cluster: int) -> list[tuple[int, int, int, int]]:
+    """The (tile, kb0, kb1, kind) units of one cluster under a plan from plan()."""
+    lib = load_library()
+    pl = _Plan(**{k: v for k, v in plan_dict.items() if k in dict(_Plan._fields_)})
+    out = []
+    vals = [ctypes.c_int32() for _ in range(4)]
+    i = 0
+    while lib.hgemm_work_unit(ctypes.byref(pl), cluster, i, *[ctypes.byref(v) for v in vals]):
+        out.append(tuple(v.value for v in vals))
+        i += 1
+    return out
 
 
 def tile_coord(t: int, tiles_m: int, tiles_n: int, group_m: int) -> tuple[int, int]:

@@ -129,12 +129,11 @@ double shape_efficiency(int cg, int bn) {
 
 // Measured time constants of the kernel on GB300: the mainloop rate of one SM
 // at efficiency 1 (flop/s), the start-up plus last-epilogue time that no tile
-// overlaps, and the fixed cost of a K-split tail (its parts' partial sums
-// written, waited for and added) per extra part, for a 256-wide tile.
+// overlaps, and the owners' stream-K fix-up (reading and adding the partners'
+// partial sums after the last unit) for a 256-wide tile.
 constexpr double kSmFlops = 13.4e12;
 constexpr double kFixedSec = 4.5e-6;
-constexpr double kSplitBaseSec = 12.0e-6;
-constexpr double kSplitPartSec = 2.0e-6;
+constexpr double kStreamKFixupSec = 3.0e-6;
 // Epilogue time per 64-column chunk of a CTA's 128-row tile (TMEM load,
 // conversion, staging, TMA store); a CTA pair hands tensor memory back across
 // the pair, which costs about half as much again. A tile takes at least this
@@ -142,76 +141,88 @@ constexpr double kSplitPartSec = 2.0e-6;
 // mainloop of the next, so the slower of the two sets the pace.
 constexpr double kEpiChunkSec = 0.45e-6;
 
-// K parts for the `rem` tiles left after the last whole wave on `clusters`
-// clusters: as many as keep every part on its own cluster, at most one per K
-// block and at most 8; 1 = no split.
-int64_t auto_split(int64_t rem, int64_t clusters, int64_t num_kb) {
-    if (rem <= 0) return 1;
-    int64_t s = clusters / rem;
-    if (s > num_kb) s = num_kb;
-    if (s > 8) s = 8;
-    return s >= 2 ? s : 1;
-}
-
 double tile_seconds(int cg, int bn, int64_t num_kb) {
     const double mainloop = 2.0 * 128 * bn * (num_kb * hg::kBlockK) / (kSmFlops * shape_efficiency(cg, bn));
     const double epilogue = kEpiChunkSec * ((bn + 63) / 64) * (cg == 2 ? 1.5 : 1.0);
     return mainloop > epilogue ? mainloop : epilogue;
 }
 
-double split_fixup_seconds(int bn, int64_t split) {
-    return (kSplitBaseSec + kSplitPartSec * (split - 1)) * bn / 256.0;
+// Stream-K tiles for `tiles` tiles on `clusters` clusters: the leftover
+// tiles of a partial last wave plus one full wave (all tiles when there are
+// fewer than clusters), or 0 when the waves come out whole. mode 3 = all.
+int64_t stream_k_tiles(int64_t tiles, int64_t clusters, int mode) {
+    if (mode == 3) return tiles;
+    const int64_t rem = tiles % clusters;
+    if (rem == 0) return 0;
+    return tiles < clusters ? tiles : rem + clusters;
 }
 
-// The K-split of the last wave, or 1 when the parts' fix-up (partial sums
-// written, waited for and added) would cost more than the shorter wave saves.
-int64_t worthwhile_split(int cg, int bn, int64_t rem, int64_t clusters, int64_t num_kb) {
-    const int64_t s = auto_split(rem, clusters, num_kb);
-    if (s < 2) return 1;
-    const double t = tile_seconds(cg, bn, num_kb);
-    return (t / s + split_fixup_seconds(bn, s) < t) ? s : 1;
+// Estimated seconds of a plan: data-parallel waves, then the stream-K phase
+// (each cluster's equal share of K blocks, plus the owners' fix-up: reading
+// the partners' partial sums after the last unit).
+double schedule_seconds(int cg, int bn, int64_t tiles, int64_t clusters, int64_t num_kb,
+                        int64_t sk_tiles) {
+    const double tile_sec = tile_seconds(cg, bn, num_kb);
+    const int64_t dp = tiles - sk_tiles;
+    double t = static_cast<double>((dp + clusters - 1) / clusters) * tile_sec;
+    if (sk_tiles > 0) {
+        const int64_t blocks = (sk_tiles * num_kb + clusters - 1) / clusters;
+        t += tile_sec * static_cast<double>(blocks) / static_cast<double>(num_kb) +
+             kStreamKFixupSec * bn / 256.0;
+    }
+    return t + kFixedSec;
 }
 
 // Fill the schedule fields of `pl` (tiles already set) for `clusters`
-// resident clusters: whole-tile units first, then the K-split tail.
-void schedule_plan(hgemm_plan_t* pl, int64_t clusters, int split_cfg, int64_t num_kb) {
+// resident clusters.
+void schedule_plan(hgemm_plan_t* pl, int64_t clusters, int sk_mode, int64_t num_kb) {
     const int64_t tiles = pl->num_tiles;
     if (clusters < 1) clusters = 1;
-    int64_t rem = tiles % clusters;
-    int64_t s = 1;
-    if (split_cfg >= 2) {
-        s = rem > 0 ? (split_cfg < num_kb ? split_cfg : num_kb) : 1;
-    } else if (split_cfg == 0) {
-        s = worthwhile_split(pl->cta_group, pl->block_n, rem, clusters, num_kb);
+    int64_t sk = 0;
+    if (sk_mode >= 2) {
+        sk = stream_k_tiles(tiles, clusters, sk_mode);
+        if (sk == 0 && sk_mode == 2 && tiles % clusters == 0 && tiles >= clusters) sk = clusters;
+    } else if (sk_mode == 0) {
+        // Measured on GB300: stream-K pays only where whole tiles would leave
+        // most SMs idle on a long K loop (single-CTA tiles, fewer tiles than
+        // clusters). With every SM fed, each tile runs slower than on the
+        // fewer, evenly loaded clusters of whole waves, which costs more than
+        // the balance gains on the pair-tile shapes.
+        const int64_t cand = (pl->cta_group == 1 && tiles * 2 <= clusters && num_kb >= 16)
+                                 ? stream_k_tiles(tiles, clusters, 2) : 0;
+        if (cand > 0) {
+            const int64_t waves = (tiles + clusters - 1) / clusters;
+            const int64_t even = (tiles + waves - 1) / waves;  // also caps clusters at tiles
+            const double t_dp = schedule_seconds(pl->cta_group, pl->block_n, tiles, even, num_kb, 0);
+            const double t_sk = schedule_seconds(pl->cta_group, pl->block_n, tiles, clusters, num_kb, cand);
+            if (t_sk < t_dp) sk = cand;
+        }
     }
-    if (s < 2) s = 1;
-    if (s == 1 && rem > 0) {
+    if (sk * num_kb < clusters) sk = 0;  // fewer K blocks than clusters: nothing to share
+    if (sk == 0) {
         // Whole waves only: spread them over as few clusters as give the same
         // wave count (less contention for L2 and HBM, same finish time).
         const int64_t waves = (tiles + clusters - 1) / clusters;
         clusters = (tiles + waves - 1) / waves;
-        rem = tiles % clusters;
     }
-    pl->split_k = static_cast<int32_t>(s);
-    pl->dp_tiles = static_cast<int32_t>(s > 1 ? tiles - rem : tiles);
-    pl->num_units = hg::work_units(pl->num_tiles, pl->dp_tiles, pl->split_k);
-    int64_t grid = clusters < pl->num_units ? clusters : pl->num_units;
-    if (grid < 1) grid = 1;
-    pl->grid_ctas = static_cast<int32_t>(grid * pl->cta_group);
+    const int64_t total = sk * num_kb;
+    pl->dp_tiles = static_cast<int32_t>(tiles - sk);
+    pl->sk_tiles = static_cast<int32_t>(sk);
+    pl->sk_blocks = static_cast<int32_t>(sk ? total / clusters : 0);
+    pl->sk_extra = static_cast<int32_t>(sk ? total % clusters : 0);
+    pl->grid_ctas = static_cast<int32_t>(clusters * pl->cta_group);
+    pl->num_kb = static_cast<int32_t>(num_kb);
 }
 
-// Bytes of fp32 partial sums (and their flags) for a plan's K-split tail.
+// Bytes of fp32 partial sums (one block per CTA) and their flags.
 int64_t partial_bytes(const hgemm_plan_t& pl) {
-    if (pl.split_k <= 1) return 0;
-    const int64_t blocks = static_cast<int64_t>(pl.num_tiles - pl.dp_tiles) * (pl.split_k - 1) *
-                           pl.cta_group * hg::kEpiWarps;
-    return blocks * hg::kEpiBoxRows * pl.block_n * 4;
+    if (pl.sk_tiles == 0) return 0;
+    return static_cast<int64_t>(pl.grid_ctas) * hg::kEpiQuarters * hg::kEpiBoxRows * pl.block_n * 4;
 }
 
 int64_t flag_bytes(const hgemm_plan_t& pl) {
-    if (pl.split_k <= 1) return 0;
-    return static_cast<int64_t>(pl.num_tiles - pl.dp_tiles) * (pl.split_k - 1) * pl.cta_group *
-           hg::kEpiWarps * 8;
+    if (pl.sk_tiles == 0) return 0;
+    return static_cast<int64_t>(pl.grid_ctas) * hg::kEpiQuarters * 2 * 8;
 }
 
 int64_t align256(int64_t x) { return (x + 255) / 256 * 256; }
@@ -245,12 +256,12 @@ WorkspaceLayout workspace_layout(const hgemm_plan_t& pl, int64_t M, int64_t N, i
 double estimate_seconds(int64_t M, int64_t N, int64_t K, int cg, int bn, int64_t clusters) {
     const int64_t kb = cdiv(K, hg::kBlockK);
     const int64_t tiles = cdiv(M, 128 * cg) * cdiv(N, bn);
-    const int64_t rem = tiles % clusters;
-    const int64_t split = worthwhile_split(cg, bn, rem, clusters, kb);
-    const double tile_sec = tile_seconds(cg, bn, kb);
-    double t = static_cast<double>(tiles / clusters) * tile_sec;
-    if (rem > 0) t += split > 1 ? tile_sec / split + split_fixup_seconds(bn, split) : tile_sec;
-    return t + kFixedSec;
+    hgemm_plan_t pl{};
+    pl.cta_group = cg;
+    pl.block_n = bn;
+    pl.num_tiles = static_cast<int32_t>(tiles);
+    schedule_plan(&pl, clusters, 0, kb);
+    return schedule_seconds(cg, bn, tiles, pl.grid_ctas / cg, kb, pl.sk_tiles);
 }
 
 void choose_shape(int64_t M, int64_t N, int64_t K, int sms, int max_clusters, int* cg_out, int* bn_out) {
@@ -260,6 +271,10 @@ void choose_shape(int64_t M, int64_t N, int64_t K, int sms, int max_clusters, in
     for (const auto& c : cand) {
         const int cg = c[0], bn = c[1];
         if (cg == 2 && M <= 128) continue;
+        // A single tile row on a long K loop is HBM-bound: 128-wide tiles give
+        // twice the tiles of 256-wide ones for stream-K to spread (measured
+        // best on GB300); the time model above assumes compute-bound tiles.
+        if (M <= 128 && K >= 16 * hg::kBlockK && bn != 128) continue;
         int64_t clusters = sms / cg;
         if (max_clusters > 0 && max_clusters < clusters) clusters = max_clusters;
         if (clusters <= 0) continue;
@@ -279,7 +294,8 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, const hgemm_config_t* 
     std::memset(pl, 0, sizeof(*pl));
     hgemm_config_t c{};
     if (cfg) c = *cfg;
-    if (c.group_m < 0 || c.max_clusters < 0 || c.store_mode < 0 || c.store_mode > 3 || c.split_k < 0) {
+    if (c.group_m < 0 || c.max_clusters < 0 || c.store_mode < 0 || c.store_mode > 4 || c.stream_k < 0 ||
+        c.stream_k > 3) {
         t_last_error = "negative or unknown config field";
         return HGEMM_ERR_INVALID_ARG;
     }
@@ -313,11 +329,11 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, const hgemm_config_t* 
     pl->group_m = c.group_m > 0 ? c.group_m : (pl->tiles_m < 8 ? (pl->tiles_m > 0 ? pl->tiles_m : 1) : 8);
     int64_t clusters = sms / cg;
     if (c.max_clusters > 0 && c.max_clusters < clusters) clusters = c.max_clusters;
-    schedule_plan(pl, clusters, c.split_k, cdiv(K, hg::kBlockK));
+    schedule_plan(pl, clusters, c.stream_k, cdiv(K, hg::kBlockK));
     pl->repack_a = a_unaligned ? 1 : 0;
     pl->repack_b = b_unaligned ? 1 : 0;
     pl->store_mode = (c.store_mode != 0) ? c.store_mode : (c_unaligned ? 2 : 1);
-    if (c_unaligned && (pl->store_mode == 1 || pl->store_mode == 3)) {
+    if (c_unaligned && pl->store_mode != 2) {
         t_last_error = "vector and TMA stores need a 16-byte aligned C with a 16-byte row pitch";
         return HGEMM_ERR_INVALID_ARG;
     }
@@ -427,7 +443,7 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
     int resident = dtype == HGEMM_BF16 ? hg::max_active_clusters_bf16(cg, bn)
                                        : hg::max_active_clusters_f16(cg, bn);
     if (resident > 0 && resident < pl.grid_ctas / cg) {
-        schedule_plan(&pl, resident, cfg ? cfg->split_k : 0, num_kb);
+        schedule_plan(&pl, resident, cfg ? cfg->stream_k : 0, num_kb);
         pl.workspace_bytes = workspace_layout(pl, M, N, K).total;
     }
     const int clusters = pl.grid_ctas / cg;
@@ -510,11 +526,14 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
     p.C = static_cast<uint16_t*>(C);
     p.ldc = N;
     p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
-    p.dp_units = pl.dp_tiles;
-    p.split = pl.split_k;
-    p.num_units = pl.num_units;
-    p.partials = pl.split_k > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(work) + wl.off_part) : nullptr;
-    p.flags = pl.split_k > 1
+    p.sched.num_tiles = pl.num_tiles;
+    p.sched.dp_tiles = pl.dp_tiles;
+    p.sched.num_kb = p.num_kb;
+    p.sched.clusters = clusters;
+    p.sched.sk_base = pl.sk_blocks;
+    p.sched.sk_extra = pl.sk_extra;
+    p.partials = pl.sk_tiles > 0 ? reinterpret_cast<float*>(static_cast<uint8_t*>(work) + wl.off_part) : nullptr;
+    p.flags = pl.sk_tiles > 0
                   ? reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(work) + wl.off_flags)
                   : nullptr;
     p.epoch = next_epoch();
@@ -603,6 +622,27 @@ hgemm_status_t hgemm_plan(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dtype,
     }
     const bool a_bad = ((K * 2) & 15) != 0, b_bad = ((N * 2) & 15) != 0, c_bad = ((N * 2) & 15) != 0;
     return make_plan(M, N, K, cfg, sms, a_bad, b_bad, c_bad, out);
+}
+
+int32_t hgemm_work_unit(const hgemm_plan_t* plan, int32_t cluster, int32_t i, int32_t* tile,
+                        int32_t* kb0, int32_t* kb1, int32_t* kind) {
+    if (!plan || plan->cta_group < 1 || cluster < 0 || cluster >= plan->grid_ctas / plan->cta_group ||
+        i < 0 || plan->num_kb < 1)
+        return 0;
+    hg::Schedule sc{};
+    sc.num_tiles = plan->num_tiles;
+    sc.dp_tiles = plan->dp_tiles;
+    sc.num_kb = plan->num_kb;
+    sc.clusters = plan->grid_ctas / plan->cta_group;
+    sc.sk_base = plan->sk_blocks;
+    sc.sk_extra = plan->sk_extra;
+    hg::WorkUnit w;
+    if (!hg::next_unit(sc, cluster, i, w)) return 0;
+    if (tile) *tile = w.tile;
+    if (kb0) *kb0 = w.kb0;
+    if (kb1) *kb1 = w.kb1;
+    if (kind) *kind = w.kind;
+    return 1;
 }
 
 void hgemm_tile_coord(int32_t t, int32_t tiles_m, int32_t tiles_n, int32_t group_m, int32_t* tm,

@@ -16,10 +16,11 @@
 //   grid swizzle (SWIZZLE_W)                 persistent CTAs walking a grouped raster
 //   Cs staging + SWIZZLE_C + float4 stores   tcgen05.ld -> cvt.rn -> swizzled smem -> TMA store
 //
-// Roles (192 threads, one CTA per SM):
-//   warps 0-3  epilogue: warp w reads TMEM lanes 32w..32w+31 (C rows of the tile)
-//   warp 4     producer: one thread issues the TMA loads of A and B per stage
-//   warp 5     MMA: allocates TMEM; one thread of the leader CTA issues tcgen05.mma
+// Roles (320 threads, one CTA per SM):
+//   warps 0-7  epilogue: warp w reads TMEM lanes 32(w % 4)..+31 (C rows of the
+//              tile) and every other 64-column chunk, starting at chunk w / 4
+//   warp 8     producer: one thread issues the TMA loads of A and B per stage
+//   warp 9     MMA: allocates TMEM; one thread of the leader CTA issues tcgen05.mma
 //
 // CTA pairs (CG = 2, a cluster of two): the pair owns a 256-row tile. Each CTA
 // loads its own 128 rows of A and its own half of the tile's B columns; the
@@ -46,10 +47,11 @@ namespace hg {
 constexpr int kBlockMCta = 128;   // C rows per CTA = TMEM lanes
 constexpr int kBlockK = 64;       // K per stage: 64 half-precision values = one 128 B swizzle row
 constexpr int kUmmaK = 16;        // K of one kind::f16 MMA
-constexpr int kEpiWarps = 4;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;      // two per TMEM lane quarter, splitting the columns
+constexpr int kEpiQuarters = 4;   // TMEM lane quarters (32 rows each)
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
 constexpr int kEpiBoxRows = 32;   // one epilogue warp's rows
 constexpr int kEpiBoxCols = 64;   // 128 B of half-precision values
 constexpr int kEpiBoxBytes = kEpiBoxRows * kEpiBoxCols * 2;
@@ -64,19 +66,19 @@ struct TcParams {
     int32_t num_kb;                 // ceil(K / kBlockK)
     uint32_t idesc;                 // tcgen05 instruction descriptor
     int32_t store_mode;             // 1: TMA stores of C; 2: plain 2-byte stores through `C`;
-                                    // 3: direct 16-byte stores through `C` (aligned C only)
+                                    // 3: direct 16-byte stores through `C` (aligned C only);
+                                    // 4: smem-staged, coalesced 16-byte stores (aligned C only)
     uint16_t* C;                    // used by store_mode 2
     int64_t ldc;                    // elements between C rows (store_mode 2)
     uint64_t timeout_ns;
     unsigned long long* status;     // device status word
-    // split-K tail (see work_unit): units [0, dp_units) are whole tiles, the
-    // rest are `split` K-parts of each remaining tile.
-    int32_t dp_units, split, num_units;
-    float* partials;                // (split - 1) fp32 partial tiles per split tile
-    unsigned long long* flags;      // one per partial block: == epoch once written
+    Schedule sched;                 // data-parallel tiles, then stream-K ranges (schedule.h)
+    float* partials;                // per cluster: the fp32 partial sums of its first,
+                                    // non-owning stream-K unit
+    unsigned long long* flags;      // one per (partial block, column half): == epoch once written
     unsigned long long epoch;       // unique per launch
-    int32_t inject;                 // test hook: 1 = the owner of split tile 0 waits for a
-                                    // partial that is never published (its wait runs out)
+    int32_t inject;                 // test hook: 1 = stream-K owners wait for partial sums
+                                    // that are never published (the waits run out)
     unsigned long long* trace;      // timeline records (builds with HG_TRACE only), or null
 };
 
@@ -108,13 +110,13 @@ __device__ __forceinline__ void trace_stamp(const TcParams& p, int local_unit, i
 #endif
 }
 
-// Index of the partial block written by part `part` (< split - 1) of split
-// tile `split_idx` for CTA rank `rank` and epilogue warp `warp`: 32 rows x BN
-// fp32.
+// Index of the partial block published by cluster `cluster` (its one
+// non-owning stream-K unit) for CTA rank `rank` and TMEM lane quarter
+// `quarter`: 32 rows x BN fp32. Its two epilogue warps (column halves) each
+// mark their own chunks with flag 2 * block + half.
 template <int CG>
-__device__ __forceinline__ int64_t partial_block(int32_t split_idx, int32_t part, int32_t split,
-                                                 uint32_t rank, int warp) {
-    return ((static_cast<int64_t>(split_idx) * (split - 1) + part) * CG + rank) * kEpiWarps + warp;
+__device__ __forceinline__ int64_t partial_block(int32_t cluster, uint32_t rank, int quarter) {
+    return (static_cast<int64_t>(cluster) * CG + rank) * kEpiQuarters + quarter;
 }
 
 constexpr int pow2_at_least(int x) {
@@ -133,7 +135,7 @@ struct TcCfg {
     static constexpr int kChunks = (BN + 63) / 64;         // epilogue chunks of 64 columns
     static constexpr bool kHalfLast = (BN % 64) != 0;      // the last chunk is 32 columns
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBoxBytes;
+    static constexpr int kEpiBytes = kEpiWarps * kEpiBoxBytes;  // one staging box per warp
     static constexpr int kBarBytes = 256;
     static constexpr int kStagesFit = (kSmemLimit - 1024 - kEpiBytes - kBarBytes) / kStageBytes;
     static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
@@ -146,7 +148,7 @@ struct TcCfg {
     static_assert(kTmemCols <= 512, "tensor memory");
     static_assert(kStages >= 2, "pipeline depth");
     static_assert(kSmemBytes <= kSmemLimit, "shared memory");
-    static_assert((2 * kStages + 5) * 8 + 8 <= kBarBytes, "barrier area");
+    static_assert((2 * kStages + 7) * 8 + 8 <= kBarBytes, "barrier area");
 };
 
 // Shared-memory matrix descriptor (tcgen05), 128-byte swizzle.
@@ -272,14 +274,14 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const uint32_t bar_tfull = sBar + 16 * S;                   // [2]
     const uint32_t bar_tempty = bar_tfull + 16;                 // [2]
     const uint32_t bar_drain = bar_tempty + 16;
-    uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(smem + (bar_drain + 8 - base));
+    const uint32_t bar_pre = bar_drain + 8;                     // [2]
+    uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(smem + (bar_pre + 16 - base));
     volatile uint32_t* const abort_flag = tmem_slot + 1;
 
     const int warp = static_cast<int>(threadIdx.x >> 5);
     const uint32_t lane = threadIdx.x & 31u;
     const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
     const int cluster_id = static_cast<int>(blockIdx.x) / CG;
-    const int num_clusters = static_cast<int>(gridDim.x) / CG;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -291,6 +293,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             mbar_init(bar_tempty + 8 * a, kEpiWarps * CG);
         }
         mbar_init(bar_drain, 1);
+        for (int a = 0; a < 2; ++a) mbar_init(bar_pre + 8 * a, kEpiWarps * CG);
         *abort_flag = 0;
         fence_mbarrier_init_cluster();
     }
@@ -314,9 +317,8 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         if (lane == 0) {
             uint32_t stage = 0, phase = 0;
             bool ok = true;
-            int lu = 0;
-            for (int u = cluster_id; u < p.num_units && ok; u += num_clusters, ++lu) {
-                const WorkUnit wu = work_unit(u, p.dp_units, p.split, p.num_kb);
+            WorkUnit wu;
+            for (int lu = 0; ok && next_unit(p.sched, cluster_id, lu, wu); ++lu) {
                 trace_stamp(p, lu, kTrProdFirst);
                 int32_t tm, tn;
                 tile_coord(wu.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
@@ -365,14 +367,23 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             uint32_t stage = 0, phase = 0;
             bool ok = true;
             bool issued = false;
-            int it = 0;
-            for (int u = cluster_id; u < p.num_units; u += num_clusters, ++it) {
-                const WorkUnit wu = work_unit(u, p.dp_units, p.split, p.num_kb);
+            uint32_t pre_phase[2] = {0u, 0u};
+            WorkUnit wu;
+            for (int it = 0; next_unit(p.sched, cluster_id, it, wu); ++it) {
                 const uint32_t acc = static_cast<uint32_t>(it) & 1u;
                 const uint32_t acc_phase = (static_cast<uint32_t>(it) >> 1) & 1u;
                 if (!wait_bar(bar_tempty + 8 * acc, acc_phase ^ 1u, w, kRoleMma, 32 + acc)) {
                     ok = false;
                     break;
+                }
+                if (wu.kind == 1) {
+                    // A stream-K owner accumulates on top of its partners' partial
+                    // sums, which the epilogue warps load into this buffer.
+                    if (!wait_bar(bar_pre + 8 * acc, pre_phase[acc], w, kRoleMma, 40 + acc)) {
+                        ok = false;
+                        break;
+                    }
+                    pre_phase[acc] ^= 1u;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
@@ -389,7 +400,8 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     for (int kk = 0; kk < kBlockK / kUmmaK; ++kk) {
                         const uint64_t ad = sdesc_sw128(a0 + 32u * kk, 16u, 1024u);
                         const uint64_t bd = sdesc_sw128(b0 + 2048u * kk, Cfg::kBAtomBytes, 1024u);
-                        umma_f16<CG>(d_tmem, ad, bd, p.idesc, (kb > wu.kb0 || kk != 0) ? 1u : 0u);
+                        umma_f16<CG>(d_tmem, ad, bd, p.idesc,
+                                     (kb > wu.kb0 || kk != 0 || wu.kind == 1) ? 1u : 0u);
                     }
                     issued = true;
                     if constexpr (CG == 1) umma_commit(bar_empty + 8 * stage);
@@ -414,11 +426,81 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        int it = 0;
-        uint32_t buf = 0;
-        const uint32_t my_boxes = sEpi + static_cast<uint32_t>(warp) * 2u * kEpiBoxBytes;
-        for (int u = cluster_id; u < p.num_units; u += num_clusters, ++it) {
-            const WorkUnit wu = work_unit(u, p.dp_units, p.split, p.num_kb);
+        // Warp w reads TMEM lane quarter w % 4 (rows 32(w % 4) .. +31 of the
+        // CTA's tile) and every other 64-column chunk, starting at chunk w / 4.
+        const int quarter = warp & 3;
+        const int colhalf = warp >> 2;
+        const uint32_t box = sEpi + static_cast<uint32_t>(warp) * kEpiBoxBytes;
+        uint8_t* const box_ptr = smem + (box - base);
+        // Stream-K owner unit `j` (the cluster's last): before its MMAs start,
+        // put the partners' partial sums into its accumulator buffer (this
+        // warp's lanes and chunks), so its own epilogue is a plain one. The
+        // partners publish them with the first units of their ranges, usually
+        // long before; if a partner's mark is not there yet the warp writes
+        // zeros instead and adds the partial sums in the owner's epilogue (it
+        // never blocks here, so no wait can chain across clusters). The
+        // buffer's previous contents were read by this warp already.
+        bool owner_preloaded = false;
+        auto preload_owner = [&](int j, const WorkUnit& ou) {
+            const uint32_t pacc = static_cast<uint32_t>(j) & 1u;
+            const uint32_t p_row = tmem_base + pacc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
+            const int32_t contrib_last = sk_last_contributor(p.sched, ou.tile);
+            // Test hook: look for a mark no part ever writes.
+            const unsigned long long want = p.inject == 1 ? ~p.epoch : p.epoch;
+            bool have = true;
+            for (int32_t q = cluster_id + 1; q <= contrib_last && have; ++q)
+                have = ld_acquire_gpu(p.flags + 2 * partial_block<CG>(q, rank, quarter) + colhalf) == want;
+            owner_preloaded = have;
+#pragma unroll 1
+            for (int c = colhalf; c < Cfg::kChunks; c += 2) {
+                const bool half = Cfg::kHalfLast && c == Cfg::kChunks - 1;
+                uint32_t r0[32], r1[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    r0[i] = 0u;
+                    r1[i] = 0u;
+                }
+                for (int32_t q = cluster_id + 1; q <= contrib_last && have; ++q) {
+                    const float4* src = reinterpret_cast<const float4*>(p.partials) +
+                                        partial_block<CG>(q, rank, quarter) * (kEpiBoxRows * BN / 4);
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj) {
+                        const float4 a = __ldcg(src + (c * 16 + jj) * 32 + lane);
+                        r0[4 * jj] = __float_as_uint(__uint_as_float(r0[4 * jj]) + a.x);
+                        r0[4 * jj + 1] = __float_as_uint(__uint_as_float(r0[4 * jj + 1]) + a.y);
+                        r0[4 * jj + 2] = __float_as_uint(__uint_as_float(r0[4 * jj + 2]) + a.z);
+                        r0[4 * jj + 3] = __float_as_uint(__uint_as_float(r0[4 * jj + 3]) + a.w);
+                        if (!half) {
+                            const float4 b = __ldcg(src + (c * 16 + 8 + jj) * 32 + lane);
+                            r1[4 * jj] = __float_as_uint(__uint_as_float(r1[4 * jj]) + b.x);
+                            r1[4 * jj + 1] = __float_as_uint(__uint_as_float(r1[4 * jj + 1]) + b.y);
+                            r1[4 * jj + 2] = __float_as_uint(__uint_as_float(r1[4 * jj + 2]) + b.z);
+                            r1[4 * jj + 3] = __float_as_uint(__uint_as_float(r1[4 * jj + 3]) + b.w);
+                        }
+                    }
+                }
+                tmem_st_32x32b_x32(p_row + 64u * c, r0);
+                if (!half) tmem_st_32x32b_x32(p_row + 64u * c + 32u, r1);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if constexpr (CG == 1) {
+                    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar_pre + 8 * pacc) : "memory");
+                } else {
+                    mbar_arrive_cluster(mapa_shared(bar_pre + 8 * pacc, 0));
+                }
+            }
+        };
+        auto preload_if_owner = [&](int j) {
+            WorkUnit ou;
+            if (next_unit(p.sched, cluster_id, j, ou) && ou.kind == 1) preload_owner(j, ou);
+        };
+        preload_if_owner(0);
+        preload_if_owner(1);
+        WorkUnit wu;
+        for (int it = 0; next_unit(p.sched, cluster_id, it, wu); ++it) {
             const uint32_t acc = static_cast<uint32_t>(it) & 1u;
             const uint32_t acc_phase = (static_cast<uint32_t>(it) >> 1) & 1u;
             if (!wait_bar(bar_tfull + 8 * acc, acc_phase, w, kRoleEpilogue, 32 + acc)) break;
@@ -428,21 +510,52 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 #ifdef HG_TRACE
                 if (p.trace && it < kTraceUnits)
                     p.trace[(static_cast<int64_t>(blockIdx.x) * kTraceUnits + it) * kTraceFields + kTrUnit] =
-                        static_cast<unsigned long long>(u);
+                        (static_cast<unsigned long long>(wu.tile) << 32) |
+                        (static_cast<unsigned long long>(wu.kb0) << 16) | static_cast<unsigned long long>(wu.kb1);
 #endif
             }
             int32_t tm, tn;
             tile_coord(wu.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
             const int32_t row0 = tm * (kBlockMCta * CG) + static_cast<int32_t>(rank) * kBlockMCta +
-                                 warp * kEpiBoxRows;
+                                 quarter * kEpiBoxRows;
             const int32_t col0 = tn * BN;
-            const uint32_t t_row = tmem_base + acc * BN + (static_cast<uint32_t>(warp * 32) << 16);
+            const uint32_t t_row = tmem_base + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
+            const bool is_split = wu.kind != 0;
+            const bool owner = wu.kind != 2;
+            if (colhalf >= Cfg::kChunks) {
+                // No chunk for this warp (a 64-wide tile): release at once.
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (CG == 1) {
+                        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];"
+                                     :: "r"(bar_tempty + 8 * acc) : "memory");
+                    } else {
+                        mbar_arrive_cluster(mapa_shared(bar_tempty + 8 * acc, 0));
+                    }
+                }
+                preload_if_owner(it + 2);
+                continue;
+            }
+            const int32_t contrib_last = (is_split && owner) ? sk_last_contributor(p.sched, wu.tile)
+                                                             : cluster_id;
+            const bool owner_adds = is_split && owner && !owner_preloaded;
+            if (owner_adds) {
+                // The preload found a partner's mark missing: wait for the marks
+                // now (this is the cluster's last unit; nothing else of this CTA
+                // is in flight) and add the partial sums below. Test hook: wait
+                // for a mark no part ever writes; the wait runs out.
+                const unsigned long long want = p.inject == 1 ? ~p.epoch : p.epoch;
+                for (int32_t q = cluster_id + 1; q <= contrib_last; ++q)
+                    if (!wait_flag(p.flags + 2 * partial_block<CG>(q, rank, quarter) + colhalf, want, w,
+                                   64 + ((q - cluster_id) & 63)))
+                        break;
+            }
 #pragma unroll 1
-            for (int c = 0; c < Cfg::kChunks; ++c) {
+            for (int c = colhalf; c < Cfg::kChunks; c += 2) {
                 // A chunk is 64 columns (two 32-column TMEM loads), or 32 for the
                 // last chunk of a tile whose width is an odd multiple of 32.
                 const bool half = Cfg::kHalfLast && c == Cfg::kChunks - 1;
-                const bool last = c == Cfg::kChunks - 1;
+                const bool last = c + 2 >= Cfg::kChunks;
                 uint32_t r0[32], r1[32];
                 tmem_ld_32x32b_x32(t_row + 64u * c, r0);
                 if (!half) tmem_ld_32x32b_x32(t_row + 64u * c + 32u, r1);
@@ -455,7 +568,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 reg_fence(r1);
                 if (warp == 0 && lane == 0) trace_chunk(p, it, c, kTcLdDone);
                 if (last) {
-                    // Every TMEM read of this accumulator is done: hand it back.
+                    // This warp's TMEM reads of the accumulator are done.
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) {
@@ -468,14 +581,13 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         if (warp == 0) trace_stamp(p, it, kTrEpiTmemFree);
                     }
                 }
-                if (wu.split_idx >= 0) {
-                    if (wu.part != p.split - 1) {
+                if (is_split) {
+                    if (!owner) {
                         // A non-owning K part: publish this chunk's fp32 partial
                         // sums (lane-interleaved, so each warp store is 512
                         // contiguous bytes) instead of writing C.
                         float4* dst = reinterpret_cast<float4*>(p.partials) +
-                                      partial_block<CG>(wu.split_idx, wu.part, p.split, rank, warp) *
-                                          (kEpiBoxRows * BN / 4);
+                                      partial_block<CG>(cluster_id, rank, quarter) * (kEpiBoxRows * BN / 4);
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
                             dst[(c * 16 + j) * 32 + lane] =
@@ -490,43 +602,29 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                             __threadfence();
                             __syncwarp();
                             if (lane == 0)
-                                st_release_gpu(p.flags + partial_block<CG>(wu.split_idx, wu.part, p.split,
-                                                                            rank, warp),
+                                st_release_gpu(p.flags + 2 * partial_block<CG>(cluster_id, rank, quarter) + colhalf,
                                                p.epoch);
                         }
                         continue;
                     }
-                    // The owning part (the last one: every part it waits for has
-                    // a lower unit index, so no cluster ever waits on work
-                    // queued behind itself): add the other parts' partial sums.
-                    if (c == 0) {
-                        // Test hook: wait for a mark no part ever writes. Split
-                        // units are a cluster's last, so nothing else is in
-                        // flight in this CTA when the wait gives up.
-                        const unsigned long long want =
-                            (p.inject == 1 && wu.split_idx == 0) ? ~p.epoch : p.epoch;
-                        for (int q = 0; q < p.split - 1; ++q)
-                            if (!wait_flag(p.flags + partial_block<CG>(wu.split_idx, q, p.split, rank, warp),
-                                           want, w, 64 + q))
-                                break;
-                    }
-                    for (int q = 0; q < p.split - 1; ++q) {
-                        const float4* src = reinterpret_cast<const float4*>(p.partials) +
-                                            partial_block<CG>(wu.split_idx, q, p.split, rank, warp) *
-                                                (kEpiBoxRows * BN / 4);
+                    if (owner_adds) {
+                        for (int32_t q = cluster_id + 1; q <= contrib_last; ++q) {
+                            const float4* src = reinterpret_cast<const float4*>(p.partials) +
+                                                partial_block<CG>(q, rank, quarter) * (kEpiBoxRows * BN / 4);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const float4 a = __ldcg(src + (c * 16 + j) * 32 + lane);
-                            r0[4 * j] = __float_as_uint(__uint_as_float(r0[4 * j]) + a.x);
-                            r0[4 * j + 1] = __float_as_uint(__uint_as_float(r0[4 * j + 1]) + a.y);
-                            r0[4 * j + 2] = __float_as_uint(__uint_as_float(r0[4 * j + 2]) + a.z);
-                            r0[4 * j + 3] = __float_as_uint(__uint_as_float(r0[4 * j + 3]) + a.w);
-                            if (!half) {
-                                const float4 b = __ldcg(src + (c * 16 + 8 + j) * 32 + lane);
-                                r1[4 * j] = __float_as_uint(__uint_as_float(r1[4 * j]) + b.x);
-                                r1[4 * j + 1] = __float_as_uint(__uint_as_float(r1[4 * j + 1]) + b.y);
-                                r1[4 * j + 2] = __float_as_uint(__uint_as_float(r1[4 * j + 2]) + b.z);
-                                r1[4 * j + 3] = __float_as_uint(__uint_as_float(r1[4 * j + 3]) + b.w);
+                            for (int j = 0; j < 8; ++j) {
+                                const float4 a = __ldcg(src + (c * 16 + j) * 32 + lane);
+                                r0[4 * j] = __float_as_uint(__uint_as_float(r0[4 * j]) + a.x);
+                                r0[4 * j + 1] = __float_as_uint(__uint_as_float(r0[4 * j + 1]) + a.y);
+                                r0[4 * j + 2] = __float_as_uint(__uint_as_float(r0[4 * j + 2]) + a.z);
+                                r0[4 * j + 3] = __float_as_uint(__uint_as_float(r0[4 * j + 3]) + a.w);
+                                if (!half) {
+                                    const float4 b = __ldcg(src + (c * 16 + 8 + j) * 32 + lane);
+                                    r1[4 * j] = __float_as_uint(__uint_as_float(r1[4 * j]) + b.x);
+                                    r1[4 * j + 1] = __float_as_uint(__uint_as_float(r1[4 * j + 1]) + b.y);
+                                    r1[4 * j + 2] = __float_as_uint(__uint_as_float(r1[4 * j + 2]) + b.z);
+                                    r1[4 * j + 3] = __float_as_uint(__uint_as_float(r1[4 * j + 3]) + b.w);
+                                }
                             }
                         }
                     }
@@ -556,10 +654,9 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     }
                     continue;
                 }
-                const uint32_t box = my_boxes + buf * kEpiBoxBytes;
                 if (p.store_mode == 1) {
-                    // The store issued from this box two chunks ago must have read it.
-                    if (lane == 0) bulk_wait_group_read<1>();
+                    // The TMA store issued from this box before must have read it.
+                    if (lane == 0) bulk_wait_group_read<0>();
                     __syncwarp();
                     if (warp == 0 && lane == 0) trace_chunk(p, it, c, kTcWaitRead);
                 }
@@ -567,7 +664,8 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 // the 128-byte swizzle: 16 B chunk j goes to j ^ (row % 8). A
                 // 32-column box has 64-byte rows and the 64-byte swizzle: chunk j
                 // goes to j ^ ((row / 2) % 4). Either way each group of 8 lanes
-                // covers all 32 banks once, and the TMA store undoes the swizzle.
+                // covers all 32 banks once (the SWIZZLE_C idea of the page's
+                // coalesced write-back), and the TMA store undoes the swizzle.
                 if (!half) {
                     const uint32_t row_addr = box + lane * 128u;
 #pragma unroll
@@ -593,10 +691,30 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         bulk_commit_group();
                     }
                     if (warp == 0 && lane == 0) trace_chunk(p, it, c, kTcIssued);
-                    buf ^= 1u;
+                } else if (p.store_mode == 4) {
+                    // Read the box back row-contiguously: 8 lanes cover one row's
+                    // 128 bytes (64-column box) or 4 lanes its 64 bytes (32-column
+                    // box), so every warp store writes whole 128-byte lines.
+                    __syncwarp();
+                    const uint32_t per_row = half ? 4u : 8u;
+                    const int n_inst = half ? 4 : 8;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        if (i < n_inst) {
+                            const uint32_t piece = static_cast<uint32_t>(i) * 32u + lane;
+                            const uint32_t rr = piece / per_row, ch = piece % per_row;
+                            const uint32_t phys = half ? (ch ^ ((rr >> 1) & 3u)) : (ch ^ (rr & 7u));
+                            const uint4 v = *reinterpret_cast<const uint4*>(
+                                box_ptr + rr * (half ? 64u : 128u) + (phys << 4));
+                            const int32_t row = row0 + static_cast<int32_t>(rr);
+                            const int32_t col = ccol + static_cast<int32_t>(ch * 8u);
+                            if (row < p.M && col < p.N)
+                                *reinterpret_cast<uint4*>(p.C + static_cast<int64_t>(row) * p.ldc + col) = v;
+                        }
+                    }
+                    __syncwarp();
                 } else {
                     __syncwarp();
-                    const uint8_t* bx = smem + (box - base);
                     const uint32_t width = half ? 32u : 64u;
 #pragma unroll 1
                     for (int rr = 0; rr < kEpiBoxRows; ++rr) {
@@ -612,7 +730,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                                     half ? urr * 64u + (((cc >> 3) ^ ((urr >> 1) & 3u)) << 4) + ((cc & 7u) << 1)
                                          : urr * 128u + (((cc >> 3) ^ (urr & 7u)) << 4) + ((cc & 7u) << 1);
                                 p.C[static_cast<int64_t>(row) * p.ldc + col] =
-                                    *reinterpret_cast<const uint16_t*>(bx + off);
+                                    *reinterpret_cast<const uint16_t*>(box_ptr + off);
                             }
                         }
                     }
@@ -620,6 +738,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 }
             }
             if (warp == 0 && lane == 0) trace_stamp(p, it, kTrEpiEnd);
+            preload_if_owner(it + 2);
         }
         if (lane == 0) bulk_wait_group<0>();
         __syncwarp();

@@ -31,48 +31,76 @@ HG_HD void tile_coord(int32_t t, int32_t tiles_m, int32_t tiles_n, int32_t group
     tn = r / rows;
 }
 
-// One unit of work: K blocks [kb0, kb1) of tile `tile`.
-//
-// Units [0, dp_units) are whole tiles (tile = unit). The tiles after them are
-// split along K into `split` parts each, so that a last, partial wave of
-// tiles becomes split x as many shorter units and keeps every cluster busy:
-// unit dp_units + split * s + part is part `part` of tile dp_units + s, and
-// `split_idx` = s numbers the split tiles. The last part owns the tile: it
-// adds the other parts' fp32 partial sums to its own and writes C. Every part
-// it waits for has a lower unit index; clusters take units in increasing
-// order, so these waits never form a cycle, however many parts one cluster
-// holds.
+// The schedule: tiles [0, dp_tiles) are data-parallel (cluster c takes tiles
+// c, c + C, c + 2C, ... whole); the remaining tiles [dp_tiles, num_tiles) are
+// stream-K: their K blocks, numbered g = (t - dp_tiles) * num_kb + kb, are cut
+// into C contiguous ranges of sk_base or sk_base + 1 blocks (the first
+// sk_extra clusters take one more), and cluster c walks its range after its
+// data-parallel tiles, one unit per tile it touches.
+struct Schedule {
+    int32_t num_tiles, dp_tiles, num_kb, clusters;
+    int32_t sk_base, sk_extra;  // total stream-K blocks = sk_base * clusters + sk_extra
+};
+
+// A unit: K blocks [kb0, kb1) of tile `tile`. `kind` 0 = the whole tile;
+// 1 = the stream-K part holding K block 0 of a tile split across clusters (the
+// owner: it adds the other parts' fp32 partial sums and writes C); 2 = any
+// other stream-K part (it publishes its partial sums). An owner part is the
+// last unit of its cluster's range and the other parts of its tile are the
+// first units of the following clusters' ranges, which never wait: waits
+// cannot form a cycle.
 struct WorkUnit {
     int32_t tile;
     int32_t kb0, kb1;
-    int32_t part;       // 0 for whole tiles
-    int32_t split_idx;  // -1 for whole tiles
+    int32_t kind;
 };
 
-HG_HD WorkUnit work_unit(int32_t u, int32_t dp_units, int32_t split, int32_t num_kb) {
-    WorkUnit w;
-    if (u < dp_units || split <= 1) {
-        w.tile = u;
-        w.kb0 = 0;
-        w.kb1 = num_kb;
-        w.part = 0;
-        w.split_idx = -1;
-    } else {
-        const int32_t v = u - dp_units;
-        const int32_t s = v / split;
-        w.part = v - s * split;
-        w.tile = dp_units + s;
-        w.split_idx = s;
-        w.kb0 = static_cast<int32_t>(static_cast<int64_t>(w.part) * num_kb / split);
-        w.kb1 = static_cast<int32_t>(static_cast<int64_t>(w.part + 1) * num_kb / split);
-    }
-    return w;
+HG_HD int64_t sk_range_start(const Schedule& s, int32_t c) {
+    return static_cast<int64_t>(c) * s.sk_base + (c < s.sk_extra ? c : s.sk_extra);
 }
 
-// Number of work units for `num_tiles` tiles of which the first `dp_units`
-// are whole.
-HG_HD int32_t work_units(int32_t num_tiles, int32_t dp_units, int32_t split) {
-    return split <= 1 ? num_tiles : dp_units + (num_tiles - dp_units) * split;
+// Cluster whose stream-K range holds block g.
+HG_HD int32_t sk_cluster_of(const Schedule& s, int64_t g) {
+    const int64_t big = static_cast<int64_t>(s.sk_extra) * (s.sk_base + 1);
+    if (g < big) return static_cast<int32_t>(g / (s.sk_base + 1));
+    return static_cast<int32_t>(s.sk_extra + (g - big) / s.sk_base);
+}
+
+HG_HD int32_t dp_tiles_of(const Schedule& s, int32_t c) {
+    return c < s.dp_tiles ? (s.dp_tiles - c + s.clusters - 1) / s.clusters : 0;
+}
+
+// The i-th unit of cluster c; false once its work is done.
+HG_HD bool next_unit(const Schedule& s, int32_t c, int32_t i, WorkUnit& w) {
+    const int32_t ndp = dp_tiles_of(s, c);
+    if (i < ndp) {
+        w.tile = c + i * s.clusters;
+        w.kb0 = 0;
+        w.kb1 = s.num_kb;
+        w.kind = 0;
+        return true;
+    }
+    const int64_t start = sk_range_start(s, c);
+    const int64_t end = start + s.sk_base + (c < s.sk_extra ? 1 : 0);
+    const int32_t j = i - ndp;
+    const int64_t t_first = start / s.num_kb;
+    const int64_t t = t_first + j;
+    const int64_t t_begin = t * s.num_kb;
+    if (end <= start || t_begin >= end) return false;
+    const int64_t lo = j == 0 ? start : t_begin;
+    const int64_t hi = end < t_begin + s.num_kb ? end : t_begin + s.num_kb;
+    w.tile = s.dp_tiles + static_cast<int32_t>(t);
+    w.kb0 = static_cast<int32_t>(lo - t_begin);
+    w.kb1 = static_cast<int32_t>(hi - t_begin);
+    w.kind = (w.kb0 == 0 && w.kb1 == s.num_kb) ? 0 : (w.kb0 == 0 ? 1 : 2);
+    return true;
+}
+
+// For an owner unit of stream-K tile `tile`, the last cluster holding part of
+// it (the contributors are the owner's cluster + 1 .. that cluster).
+HG_HD int32_t sk_last_contributor(const Schedule& s, int32_t tile) {
+    const int64_t g_last = static_cast<int64_t>(tile - s.dp_tiles) * s.num_kb + s.num_kb - 1;
+    return sk_cluster_of(s, g_last);
 }
 
 }  // namespace hg

@@ -70,8 +70,8 @@ typedef enum {
  * Workspace: operands whose row pitch (2K bytes for A, 2N bytes for B) or base
  * address is not a multiple of 16 bytes are first copied into a
  * 16-byte-pitched workspace (such a C is written with plain stores), and when
- * the last wave of tiles is split along K the parts' fp32 partial sums go
- * through the workspace too. It comes from a stream-ordered memory pool owned
+ * tiles are shared by stream-K ranges the parts' fp32 partial sums go through
+ * the workspace too. It comes from a stream-ordered memory pool owned
  * by the library (one per device, cudaMallocFromPoolAsync / cudaFreeAsync on
  * `stream`; the pool keeps up to 256 MiB cached between calls). Calls that need
  * no workspace allocate nothing; hgemm_plan reports the bytes.
@@ -91,17 +91,18 @@ hgemm_status_t hgemm(const void* A, const void* B, void* C, int64_t M, int64_t N
  * Same operation and arguments as hgemm(), and the same results. The only
  * workspace the GEMM can need (the 16-byte-pitch copy of A or B when a row
  * pitch or base address is not 16-byte aligned, and the fp32 partial sums of
- * a K-split last wave) comes from a fixed 64 MiB array inside the library
+ * the stream-K phase) comes from a fixed 64 MiB array inside the library
  * (hgemm_noalloc_scratch_bytes()); the call makes no cudaMalloc,
  * cudaMallocAsync, cudaFree or other allocating call.
  *   - A shape whose workspace would exceed the array returns
  *     HGEMM_ERR_INVALID_ARG (hgemm_last_error() gives the sizes) and enqueues
- *     nothing. The K-split partial sums never need more than 20 MiB, so the
- *     limit only bites on unaligned operands (their 16-byte-pitch copies).
+ *     nothing. The stream-K partial sums need at most one 128 x 256 fp32
+ *     block per CTA (under 20 MiB), so the limit only bites on unaligned
+ *     operands (their 16-byte-pitch copies).
  *   - Every call on a device shares that device's array, which keeps the last
- *     call's contents (nothing in it needs to start at zero: the K-split
- *     parts mark their partial sums with a number unique to each launch, so
- *     stale marks are never mistaken for fresh ones). Calls whose GPU
+ *     call's contents (nothing in it needs to start at zero: stream-K parts
+ *     mark their partial sums with a number unique to each launch, so stale
+ *     marks are never mistaken for fresh ones). Calls whose GPU
  *     work overlaps - on different streams, or from different host threads -
  *     race on the array: serialise them (one stream, or events).
  *   - The first call on each device looks up the array's device address
@@ -126,11 +127,17 @@ uint64_t hgemm_noalloc_scratch_bytes(void);
  *   max_clusters:  cap on resident CTA clusters (forces more tiles per CTA).
  *   store_mode:    1 = TMA tensor stores of C (through a swizzled smem box),
  *                  2 = plain per-element stores, 3 = 16-byte vector stores
- *                  straight from registers (1 and 3 need a 16-byte aligned C
- *                  whose row pitch is a multiple of 16 bytes).
- *   split_k:       K-split of the tiles left over after the last whole wave
- *                  (0 = planner's choice, 1 = never split, s >= 2 = s parts,
- *                  capped at the number of 64-deep K blocks).
+ *                  straight from registers, 4 = 16-byte vector stores of whole
+ *                  rows read back from the swizzled smem box (1, 3 and 4 need
+ *                  a 16-byte aligned C whose row pitch is a multiple of 16
+ *                  bytes).
+ *   stream_k:      how the tiles past the last whole wave are shared:
+ *                  0 = planner's choice; 1 = never (whole tiles only, spread
+ *                  over as few clusters as keep the wave count); 2 = stream-K
+ *                  over the leftover tiles plus one full wave (or all tiles
+ *                  when there are fewer than clusters): their 64-deep K blocks
+ *                  are cut into equal contiguous ranges, one per cluster;
+ *                  3 = stream-K over every tile.
  */
 typedef struct {
     int32_t cta_group;
@@ -138,7 +145,7 @@ typedef struct {
     int32_t group_m;
     int32_t max_clusters;
     int32_t store_mode;
-    int32_t split_k;
+    int32_t stream_k;
 } hgemm_config_t;
 
 /* hgemm with an explicit configuration (cfg may be NULL = all zero). */
@@ -177,10 +184,13 @@ typedef struct {
     int32_t tmem_cols;     /* tensor-memory columns allocated per CTA */
     int32_t repack_a;      /* 1 if A goes through the 16-byte-pitch workspace */
     int32_t repack_b;      /* 1 if B does */
-    int32_t store_mode;    /* 1 = TMA stores, 2 = plain stores, 3 = vector stores */
-    int32_t dp_tiles;      /* tiles computed whole (the first dp_tiles in raster order) */
-    int32_t split_k;       /* K parts of each remaining tile (1 = no split) */
-    int32_t num_units;     /* work units: dp_tiles + (num_tiles - dp_tiles) * split_k */
+    int32_t store_mode;    /* 1 = TMA, 2 = plain, 3 = vector, 4 = staged vector stores */
+    int32_t dp_tiles;      /* tiles computed whole, round-robin (the first dp_tiles in raster order) */
+    int32_t sk_tiles;      /* tiles after them shared by stream-K ranges (0 = none) */
+    int32_t sk_blocks;     /* K blocks per cluster in the stream-K phase (the first
+                              sk_extra clusters take one more) */
+    int32_t sk_extra;
+    int32_t num_kb;        /* 64-deep K blocks per tile: ceil(K / 64) */
     int32_t reserved;
     int64_t workspace_bytes; /* stream-ordered workspace: repacked operands + fp32 partials */
 } hgemm_plan_t;
@@ -189,6 +199,16 @@ typedef struct {
  * SMs without touching a device (pointers are then assumed 16-byte aligned). */
 hgemm_status_t hgemm_plan(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dtype,
                           const hgemm_config_t* cfg, int32_t sm_count, hgemm_plan_t* out);
+
+/*
+ * The i-th work unit of cluster `cluster` under `plan` (host copy of the
+ * device schedule): K blocks [*kb0, *kb1) of tile *tile; *kind 0 = whole tile,
+ * 1 = stream-K part owning the tile (holds K block 0; adds the partners'
+ * partial sums), 2 = other stream-K part. Returns 0 when the cluster has no
+ * i-th unit (then the outputs are untouched), 1 otherwise.
+ */
+int32_t hgemm_work_unit(const hgemm_plan_t* plan, int32_t cluster, int32_t i, int32_t* tile,
+                        int32_t* kb0, int32_t* kb1, int32_t* kind);
 
 /*
  * Tile raster used by every CTA role (host copy of the device function).
@@ -215,12 +235,13 @@ void hgemm_set_timeout_ns(uint64_t ns);
 /*
  * Test hook for the failure path (not for production use; affects launches
  * made after the call, from any thread, until reset with 0).
- * kind 1: in each launch that splits its last wave along K, the CTAs owning
- * the first split tile wait for partial sums that are never published. That
+ * kind 1: in each launch with a stream-K phase, the CTAs owning a tile shared
+ * across clusters wait for partial sums that are never published. Each such
  * wait runs out after the timeout set by hgemm_set_timeout_ns; the kernel
- * records HGEMM_ERR_TIMEOUT in the device status word, writes that tile
- * without the missing parts, and returns normally. The waiting CTAs have no
- * copies or MMAs in flight, and nothing traps or hangs.
+ * records HGEMM_ERR_TIMEOUT in the device status word, writes those tiles
+ * without the missing parts, and returns normally. An owner's unit is the last
+ * of its CTA, so the waiting CTAs have no copies or MMAs in flight, and
+ * nothing traps or hangs.
  */
 void hgemm_test_inject(int32_t kind);
 

@@ -121,33 +121,86 @@ def test_plan_shapes(lib):
         binding.plan(512, 512, 512, "f16", binding.Config(cta_group=2, block_n=64), sm_count=148)
 
 
-def test_plan_split_tail(lib):
-    # 4096^3 on 152 SMs with pair tiles: 256 tiles, 76 clusters, 3 whole waves,
-    # the 28 leftover tiles split 2 ways over 56 clusters when asked
-    p = binding.plan(4096, 4096, 4096, "bf16", binding.Config(cta_group=2, block_n=256, split_k=2),
+def test_plan_stream_k(lib):
+    # 4096^3 on 152 SMs with pair tiles: 256 tiles, 76 clusters, 3.37 waves.
+    # Two data-parallel waves (152 tiles), then the last 104 tiles' 6656 K
+    # blocks in 76 equal ranges of 87 or 88 blocks.
+    p = binding.plan(4096, 4096, 4096, "bf16", binding.Config(cta_group=2, block_n=256, stream_k=2),
                      sm_count=152)
-    assert (p["num_tiles"], p["dp_tiles"], p["split_k"], p["num_units"]) == (256, 228, 2, 284)
-    assert p["grid_ctas"] == 152
-    assert p["workspace_bytes"] >= 28 * 1 * 2 * 4 * 32 * 256 * 4
-    # left to itself, the planner splits a long-K last wave (8192^3) ...
-    q8 = binding.plan(8192, 8192, 8192, "bf16", binding.Config(cta_group=2, block_n=256), sm_count=152)
-    assert (q8["num_tiles"], q8["dp_tiles"], q8["split_k"], q8["num_units"]) == (1024, 988, 2, 1060)
-    # ... but at 4096^3 the fix-up outweighs the half wave: whole waves, spread
-    # evenly (4 waves of 64 clusters instead of 3.37 of 76)
-    b = binding.plan(4096, 4096, 4096, "bf16", binding.Config(cta_group=2, block_n=256), sm_count=152)
-    assert (b["split_k"], b["num_units"], b["grid_ctas"]) == (1, 256, 128)
-    # fewer leftover tiles allow more parts (capped at 8 and at the K blocks)
-    q = binding.plan(512, 1024, 8192, "bf16", binding.Config(cta_group=2, block_n=256), sm_count=152)
-    assert (q["num_tiles"], q["dp_tiles"], q["split_k"], q["num_units"]) == (8, 0, 8, 64)
-    r = binding.plan(512, 1024, 128, "bf16", binding.Config(cta_group=2, block_n=256, split_k=4),
-                     sm_count=152)
-    assert r["split_k"] == 2  # only two K blocks
-    # split_k = 1 disables it; whole waves leave nothing to split
-    off = binding.plan(4096, 4096, 4096, "bf16",
-                       binding.Config(cta_group=2, block_n=256, split_k=1), sm_count=152)
-    assert (off["split_k"], off["dp_tiles"], off["num_units"], off["workspace_bytes"]) == (1, 256, 256, 0)
+    assert (p["num_tiles"], p["dp_tiles"], p["sk_tiles"]) == (256, 152, 104)
+    assert (p["sk_blocks"], p["sk_extra"], p["grid_ctas"], p["num_kb"]) == (87, 44, 152, 64)
+    assert p["workspace_bytes"] >= 152 * 4 * 32 * 256 * 4
+    # stream_k = 1, and the planner's own choice for pair tiles: whole waves
+    # only, spread evenly (4 waves of 64 clusters)
+    for mode in (1, 0):
+        off = binding.plan(4096, 4096, 4096, "bf16",
+                           binding.Config(cta_group=2, block_n=256, stream_k=mode), sm_count=152)
+        assert (off["sk_tiles"], off["dp_tiles"], off["grid_ctas"], off["workspace_bytes"]) == (0, 256, 128, 0)
+    # a single tile row on a long K loop: 128-wide one-CTA tiles, all stream-K
+    sk = binding.plan(128, 8192, 8192, "bf16", sm_count=152)
+    assert (sk["cta_group"], sk["block_n"], sk["sk_tiles"], sk["grid_ctas"]) == (1, 128, 64, 152)
+    # whole waves leave nothing to share; one K block leaves nothing to cut
     even = binding.plan(128 * 76, 256, 4096, "bf16", binding.Config(cta_group=1, block_n=256), sm_count=76)
-    assert even["split_k"] == 1 and even["num_units"] == 76
+    assert even["sk_tiles"] == 0 and even["grid_ctas"] == 76
+    short = binding.plan(4096, 4096, 64, "bf16", binding.Config(cta_group=2, block_n=256), sm_count=152)
+    assert short["sk_tiles"] == 0
+    # mode 3 shares every tile
+    every = binding.plan(1024, 1024, 1024, "f16",
+                         binding.Config(cta_group=1, block_n=128, stream_k=3), sm_count=20)
+    assert every["sk_tiles"] == every["num_tiles"] and every["dp_tiles"] == 0
+
+
+def _check_schedule(p):
+    clusters = p["grid_ctas"] // p["cta_group"]
+    kb = p["num_kb"]
+    seen = {}
+    units_of = {}
+    for c in range(clusters):
+        units = binding.work_units(p, c)
+        units_of[c] = units
+        for i, (tile, kb0, kb1, kind) in enumerate(units):
+            assert 0 <= tile < p["num_tiles"] and 0 <= kb0 < kb1 <= kb
+            for k in range(kb0, kb1):
+                assert (tile, k) not in seen, "K block computed twice"
+                seen[(tile, k)] = (c, i, kind)
+            if tile < p["dp_tiles"]:
+                assert (kb0, kb1, kind) == (0, kb, 0) and tile % clusters == c
+            if kind == 0:
+                assert (kb0, kb1) == (0, kb)
+            if kind == 1:
+                assert kb0 == 0 and kb1 < kb and i == len(units) - 1  # owner: last unit, holds block 0
+            if kind == 2:
+                assert kb0 > 0
+                ndp = sum(1 for u in units if u[0] < p["dp_tiles"])
+                assert i == ndp  # a non-owning part is the first stream-K unit: it never waits
+    assert len(seen) == p["num_tiles"] * kb, "some K block never computed"
+    for tile in range(p["num_tiles"]):
+        holders = sorted({seen[(tile, k)][0] for k in range(kb)})
+        kinds = {seen[(tile, k)][2] for k in range(kb)}
+        if len(holders) == 1:
+            assert kinds == {0}
+        else:
+            owner = seen[(tile, 0)][0]
+            assert seen[(tile, 0)][2] == 1 and owner == holders[0]
+            # every partner of the owner is a later cluster, in one contiguous run
+            assert holders == list(range(owner, owner + len(holders)))
+            for c in holders[1:]:
+                assert all(seen[(tile, k)][2] == 2 for k in range(kb) if seen[(tile, k)][0] == c)
+
+
+@pytest.mark.parametrize("shape,cfg,sms", [
+    ((4096, 4096, 4096), dict(cta_group=2, block_n=256), 152),
+    ((8192, 8192, 8192), dict(), 152),
+    ((128, 8192, 8192), dict(), 152),
+    ((1000, 4095, 4104), dict(), 152),
+    ((1024, 1280, 704), dict(cta_group=1, block_n=128, max_clusters=3, stream_k=2), 152),
+    ((1024, 1280, 704), dict(cta_group=2, block_n=224, max_clusters=5, stream_k=3), 152),
+    ((300, 700, 130), dict(cta_group=1, block_n=64, stream_k=3), 152),
+    ((777, 999, 4444), dict(stream_k=2), 37),
+])
+def test_schedule_covers_every_block_once_without_wait_cycles(lib, shape, cfg, sms):
+    p = binding.plan(*shape, "bf16", binding.Config(**cfg), sm_count=sms)
+    _check_schedule(p)
 
 
 def test_plan_skinny_prefers_narrow_tiles(lib):

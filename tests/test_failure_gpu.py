@@ -28,10 +28,10 @@ def lib():
 
 
 def test_wait_that_runs_out_reports_timeout_and_context_survives():
-    M, N, K = 512, 1024, 2048  # 8 pair tiles on 76 clusters: every tile K-split
+    M, N, K = 512, 1024, 2048  # fewer tiles than clusters: every tile shared by stream-K
     A = inputs.generate((M, K), "bf16", 40, 0).cuda()
     B = inputs.generate((K, N), "bf16", 40, 1).cuda()
-    assert hg.plan(M, N, K, "bf16")["split_k"] > 1
+    assert hg.plan(M, N, K, "bf16")["sk_tiles"] > 0
     C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     hg.set_timeout_ns(50_000_000)  # 50 ms
     hg.test_inject(1)
@@ -39,8 +39,8 @@ def test_wait_that_runs_out_reports_timeout_and_context_survives():
     torch.cuda.synchronize()  # the kernel returned on its own
     st, info = hg.get_device_status(0, reset=True)
     assert st == 5, (st, hex(info))
-    assert (info >> 24) == 3  # the epilogue role recorded it
-    assert 64 <= ((info >> 16) & 0xFF) < 72  # while waiting for a partial-sum mark
+    role, which = info >> 24, (info >> 16) & 0xFF
+    assert role == 3 and which >= 64, hex(info)  # the epilogue, waiting for a partial-sum mark
     # the context is intact: the next GEMM is correct and reports nothing
     hg.test_inject(0)
     hg.set_timeout_ns(2_000_000_000)

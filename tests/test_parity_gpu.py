@@ -148,31 +148,31 @@ def test_persistent_loop_many_tiles_per_cta(cfg, max_clusters):
 
 
 @pytest.mark.parametrize("cfg", CONFIGS, ids=CFG_IDS)
-@pytest.mark.parametrize("split", [2, 3, 5])
-def test_split_k_tail(cfg, split):
-    # 3 clusters over 8 x 10 (or 4 x 10) tiles leave a remainder; its tiles are
-    # split `split` ways along K and the parts' partial sums meet in the owner
-    c = hg.Config(cfg.cta_group, cfg.block_n, 0, 3, 0, split)
+@pytest.mark.parametrize("mode,clusters", [(2, 3), (3, 3), (3, 7)])
+def test_stream_k(cfg, mode, clusters):
+    # a few clusters share the leftover (mode 2) or every (mode 3) tile's K
+    # blocks in equal ranges; owners add their partners' partial sums
+    c = hg.Config(cfg.cta_group, cfg.block_n, 0, clusters, 0, mode)
     A, B = operands(1024, 1280, 704, "bf16", 14)
     check_full(A, B, "bf16", c)
 
 
-@pytest.mark.parametrize("shape", [(512, 1024, 8192), (300, 700, 130), (128, 2048, 4096), (256, 512, 64)])
+@pytest.mark.parametrize("shape", [(512, 1024, 8192), (300, 700, 130), (128, 2048, 4096), (256, 512, 64),
+                                   (128, 1000, 3000)])
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
-def test_split_k_auto(shape, dtype):
-    # fewer tiles than clusters: the planner splits every tile (up to 8 ways,
-    # at most one part per K block; K = 64 leaves nothing to split)
+def test_planner_choices(shape, dtype):
+    # whatever the planner picks (stream-K for one tile row on a long K loop,
+    # whole tiles otherwise; K = 64 leaves nothing to share)
     M, N, K = shape
     A, B = operands(M, N, K, dtype, 15)
-    p = hg.plan(M, N, K, dtype)
-    assert p["split_k"] >= 1
     check_full(A, B, dtype)
 
 
-def test_split_k_repeated_calls_reuse_workspace():
+def test_stream_k_repeated_calls_reuse_workspace():
     # the pool hands the same workspace back; fresh launch epochs keep stale
     # partial-sum marks from being taken for new ones
     A, B = operands(512, 1024, 2048, "f16", 16)
+    assert hg.plan(512, 1024, 2048, "f16")["sk_tiles"] > 0
     a, b = inputs.bits(A), inputs.bits(B)
     ref64 = oracle.gemm_f64(a, b, "f16")
     ref = oracle.round_rne(ref64, "f16")
@@ -192,16 +192,17 @@ def test_raster_groups(group_m):
 
 
 @pytest.mark.parametrize("cfg", CONFIGS, ids=CFG_IDS)
-@pytest.mark.parametrize("store_mode", [2, 3])
+@pytest.mark.parametrize("store_mode", [2, 3, 4])
 def test_store_modes_match(cfg, store_mode):
-    # plain 2-byte stores and direct 16-byte vector stores, ragged M and N
+    # plain 2-byte stores, direct 16-byte vector stores and smem-staged
+    # coalesced stores, ragged M and N
     c = hg.Config(cfg.cta_group, cfg.block_n, 0, 0, store_mode)
     A, B = operands(700, 520, 300, "bf16", 8)
     check_full(A, B, "bf16", c)
 
 
-@pytest.mark.parametrize("store_mode", [1, 3])
-def test_store_modes_with_split_tail(store_mode):
+@pytest.mark.parametrize("store_mode", [1, 3, 4])
+def test_store_modes_with_stream_k(store_mode):
     c = hg.Config(2, 224, 0, 3, store_mode, 3)
     A, B = operands(1024, 1344, 512, "f16", 17)
     check_full(A, B, "f16", c)

@@ -82,10 +82,11 @@ def test_noalloc_rejects_workspace_beyond_its_scratch(lib):
     assert torch.all(C == 7.0)  # nothing was enqueued
 
 
-def test_noalloc_aligned_shape_with_split_tail(lib):
-    # aligned operands; the only workspace is the K-split partial sums of the
-    # tail (8 pair tiles on 76 clusters: every tile split 8 ways)
-    M, N, K = 512, 1024, 8192
+def test_noalloc_aligned_shape_with_stream_k(lib):
+    # aligned operands; the only workspace is the stream-K partial sums (one
+    # tile row on a long K loop: every tile's K blocks are shared)
+    M, N, K = 128, 2048, 4096
+    assert hg.plan(M, N, K, "bf16")["sk_tiles"] > 0
     A = inputs.generate((M, K), "bf16", 34, 0)
     B = inputs.generate((K, N), "bf16", 34, 1)
     C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
