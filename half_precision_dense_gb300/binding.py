@@ -33,14 +33,15 @@ class HgemmError(RuntimeError):
 class _Config(ctypes.Structure):
     _fields_ = [("cta_group", ctypes.c_int32), ("block_n", ctypes.c_int32),
                 ("group_m", ctypes.c_int32), ("max_clusters", ctypes.c_int32),
-                ("store_mode", ctypes.c_int32), ("stream_k", ctypes.c_int32)]
+                ("store_mode", ctypes.c_int32), ("stream_k", ctypes.c_int32),
+                ("multicast", ctypes.c_int32)]
 
 
 class _Plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "cta_group", "block_m", "block_n", "block_k", "stages", "group_m", "tiles_m", "tiles_n",
         "num_tiles", "grid_ctas", "smem_bytes", "tmem_cols", "repack_a", "repack_b", "store_mode",
-        "dp_tiles", "sk_tiles", "sk_blocks", "sk_extra", "num_kb", "reserved")] + \
+        "dp_tiles", "sk_tiles", "sk_blocks", "sk_extra", "num_kb", "multicast")] + \
         [("workspace_bytes", ctypes.c_int64)]
 
 
@@ -53,10 +54,11 @@ class Config:
     max_clusters: int = 0
     store_mode: int = 0
     stream_k: int = 0
+    multicast: int = 0
 
     def _c(self) -> _Config:
         return _Config(self.cta_group, self.block_n, self.group_m, self.max_clusters, self.store_mode,
-                       self.stream_k)
+                       self.stream_k, self.multicast)
 
 
 def library_path() -> str:
@@ -173,7 +175,7 @@ def plan(M: int, N: int, K: int, dtype="bf16", config: Config | None = None, sm_
     out = _Plan()
     cfg = ctypes.byref(config._c()) if config is not None else None
     _check(lib.hgemm_plan(M, N, K, _dtype_code(dtype), cfg, sm_count, ctypes.byref(out)))
-    return {name: getattr(out, name) for name, _ in _Plan._fields_ if name != "reserved"}
+    return {name: getattr(out, name) for name, _ in _Plan._fields_}
 
 
 def work_units(plan_dict: dict, cluster: int) -> list[tuple[int, int, int, int]]:

@@ -210,7 +210,7 @@ void schedule_plan(hgemm_plan_t* pl, int64_t clusters, int sk_mode, int64_t num_
     pl->sk_tiles = static_cast<int32_t>(sk);
     pl->sk_blocks = static_cast<int32_t>(sk ? total / clusters : 0);
     pl->sk_extra = static_cast<int32_t>(sk ? total % clusters : 0);
-    pl->grid_ctas = static_cast<int32_t>(clusters * pl->cta_group);
+    pl->grid_ctas = static_cast<int32_t>(clusters * pl->cta_group * (pl->multicast > 1 ? pl->multicast : 1));
     pl->num_kb = static_cast<int32_t>(num_kb);
 }
 
@@ -259,6 +259,7 @@ double estimate_seconds(int64_t M, int64_t N, int64_t K, int cg, int bn, int64_t
     hgemm_plan_t pl{};
     pl.cta_group = cg;
     pl.block_n = bn;
+    pl.multicast = 1;
     pl.num_tiles = static_cast<int32_t>(tiles);
     schedule_plan(&pl, clusters, 0, kb);
     return schedule_seconds(cg, bn, tiles, pl.grid_ctas / cg, kb, pl.sk_tiles);
@@ -316,8 +317,14 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, const hgemm_config_t* 
         t_last_error = "unsupported (cta_group, block_n) pair";
         return HGEMM_ERR_INVALID_ARG;
     }
+    if (c.multicast < 0 || c.multicast > 2 || (c.multicast == 2 && !(cg == 2 && bn == 256))) {
+        t_last_error = "multicast = 2 needs cta_group 2 and block_n 256";
+        return HGEMM_ERR_INVALID_ARG;
+    }
+    const int mc = c.multicast == 2 ? 2 : 1;
     pl->cta_group = cg;
-    pl->block_m = 128 * cg;
+    pl->multicast = mc;
+    pl->block_m = 128 * cg * mc;
     pl->block_n = bn;
     pl->block_k = hg::kBlockK;
     pl->stages = hg::tc_stages(cg, bn);
@@ -327,7 +334,7 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, const hgemm_config_t* 
     pl->tiles_n = static_cast<int32_t>(cdiv(N, bn));
     pl->num_tiles = pl->tiles_m * pl->tiles_n;
     pl->group_m = c.group_m > 0 ? c.group_m : (pl->tiles_m < 8 ? (pl->tiles_m > 0 ? pl->tiles_m : 1) : 8);
-    int64_t clusters = sms / cg;
+    int64_t clusters = sms / (cg * mc);
     if (c.max_clusters > 0 && c.max_clusters < clusters) clusters = c.max_clusters;
     schedule_plan(pl, clusters, c.stream_k, cdiv(K, hg::kBlockK));
     pl->repack_a = a_unaligned ? 1 : 0;
@@ -438,15 +445,15 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
 
     // Resident clusters bound the persistent grid; re-plan the schedule if
     // fewer fit than the planner assumed.
-    const int cg = pl.cta_group, bn = pl.block_n;
+    const int cg = pl.cta_group, bn = pl.block_n, mc = pl.multicast;
     const int64_t num_kb = cdiv(K, hg::kBlockK);
-    int resident = dtype == HGEMM_BF16 ? hg::max_active_clusters_bf16(cg, bn)
-                                       : hg::max_active_clusters_f16(cg, bn);
-    if (resident > 0 && resident < pl.grid_ctas / cg) {
+    int resident = dtype == HGEMM_BF16 ? hg::max_active_clusters_bf16(cg, bn, mc)
+                                       : hg::max_active_clusters_f16(cg, bn, mc);
+    if (resident > 0 && resident < pl.grid_ctas / (cg * mc)) {
         schedule_plan(&pl, resident, cfg ? cfg->stream_k : 0, num_kb);
         pl.workspace_bytes = workspace_layout(pl, M, N, K).total;
     }
-    const int clusters = pl.grid_ctas / cg;
+    const int clusters = pl.grid_ctas / (cg * mc);
 
     // Workspace: 16-byte-pitched copies of operands TMA cannot address, and
     // the fp32 partial sums of a K-split tail.
@@ -544,8 +551,8 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
         return cuda_fail(e, "status word");
     }
 
-    e = dtype == HGEMM_BF16 ? hg::launch_tc_bf16(cg, bn, ta, tb, tc, tc32, p, clusters, stream)
-                            : hg::launch_tc_f16(cg, bn, ta, tb, tc, tc32, p, clusters, stream);
+    e = dtype == HGEMM_BF16 ? hg::launch_tc_bf16(cg, bn, mc, ta, tb, tc, tc32, p, clusters, stream)
+                            : hg::launch_tc_f16(cg, bn, mc, ta, tb, tc, tc32, p, clusters, stream);
     if (work && work != scratch) cudaFreeAsync(work, stream);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     return HGEMM_OK;
@@ -626,14 +633,15 @@ hgemm_status_t hgemm_plan(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dtype,
 
 int32_t hgemm_work_unit(const hgemm_plan_t* plan, int32_t cluster, int32_t i, int32_t* tile,
                         int32_t* kb0, int32_t* kb1, int32_t* kind) {
-    if (!plan || plan->cta_group < 1 || cluster < 0 || cluster >= plan->grid_ctas / plan->cta_group ||
-        i < 0 || plan->num_kb < 1)
+    const int32_t csize = plan ? plan->cta_group * (plan->multicast > 1 ? plan->multicast : 1) : 1;
+    if (!plan || plan->cta_group < 1 || cluster < 0 || cluster >= plan->grid_ctas / csize || i < 0 ||
+        plan->num_kb < 1)
         return 0;
     hg::Schedule sc{};
     sc.num_tiles = plan->num_tiles;
     sc.dp_tiles = plan->dp_tiles;
     sc.num_kb = plan->num_kb;
-    sc.clusters = plan->grid_ctas / plan->cta_group;
+    sc.clusters = plan->grid_ctas / csize;
     sc.sk_base = plan->sk_blocks;
     sc.sk_extra = plan->sk_extra;
     hg::WorkUnit w;

@@ -111,12 +111,12 @@ __device__ __forceinline__ void trace_stamp(const TcParams& p, int local_unit, i
 }
 
 // Index of the partial block published by cluster `cluster` (its one
-// non-owning stream-K unit) for CTA rank `rank` and TMEM lane quarter
-// `quarter`: 32 rows x BN fp32. Its two epilogue warps (column halves) each
-// mark their own chunks with flag 2 * block + half.
-template <int CG>
-__device__ __forceinline__ int64_t partial_block(int32_t cluster, uint32_t rank, int quarter) {
-    return (static_cast<int64_t>(cluster) * CG + rank) * kEpiQuarters + quarter;
+// non-owning stream-K unit) for the CTA of cluster rank `crank` and TMEM lane
+// quarter `quarter`: 32 rows x BN fp32. Its two epilogue warps (column halves)
+// each mark their own chunks with flag 2 * block + half.
+template <int kCluster>
+__device__ __forceinline__ int64_t partial_block(int32_t cluster, uint32_t crank, int quarter) {
+    return (static_cast<int64_t>(cluster) * kCluster + crank) * kEpiQuarters + quarter;
 }
 
 constexpr int pow2_at_least(int x) {
@@ -252,7 +252,11 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
     for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i]));
 }
 
-template <int CG, int BN, bool kBF16>
+// MC = CTA pairs per cluster (CG = 2 only): with MC = 2 a cluster of four
+// stacks two pairs along M; they need the same B columns, so each CTA loads
+// only one of its two 64-column B atoms and multicasts it to the matching CTA
+// of the other pair (a quarter less operand traffic through L2).
+template <int CG, int BN, bool kBF16, int MC>
 __global__ void __launch_bounds__(kThreads, 1)
 hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC32,
@@ -260,6 +264,8 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 #if defined(__CUDA_ARCH__) && defined(__CUDA_ARCH_FEAT_SM103_ALL)
     using Cfg = TcCfg<CG, BN>;
     constexpr int S = Cfg::kStages;
+    constexpr int kCluster = CG * MC;
+    static_assert(MC == 1 || (CG == 2 && MC == 2 && Cfg::kBAtoms == 2), "B multicast across pairs");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
@@ -280,13 +286,17 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 
     const int warp = static_cast<int>(threadIdx.x >> 5);
     const uint32_t lane = threadIdx.x & 31u;
-    const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
-    const int cluster_id = static_cast<int>(blockIdx.x) / CG;
+    const uint32_t crank = (kCluster > 1) ? cluster_ctarank() : 0u;  // rank in the cluster
+    const uint32_t rank = crank & static_cast<uint32_t>(CG - 1);        // rank in the CTA pair
+    const uint32_t pair = crank / CG;                                   // pair in the cluster
+    const uint32_t leader = pair * CG;                                  // the pair's MMA CTA
+    const int cluster_id = static_cast<int>(blockIdx.x) / kCluster;
+    constexpr int kRowsPerUnit = kBlockMCta * kCluster;                 // C rows per work unit
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, MC);  // each pair's MMA frees the stage
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bar_tfull + 8 * a, 1);
@@ -306,7 +316,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     if (warp == kMmaWarp) tmem_alloc<CG>(smem_addr(tmem_slot), Cfg::kTmemCols);
     tc_fence_before();
     __syncthreads();
-    if constexpr (CG == 2) cluster_sync();
+    if constexpr (kCluster > 1) cluster_sync();
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
     const Waiter w{abort_flag, p.timeout_ns, p.status};
@@ -322,7 +332,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 trace_stamp(p, lu, kTrProdFirst);
                 int32_t tm, tn;
                 tile_coord(wu.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-                const int32_t m0 = tm * (kBlockMCta * CG) + static_cast<int32_t>(rank) * kBlockMCta;
+                const int32_t m0 = tm * kRowsPerUnit + static_cast<int32_t>(pair * CG + rank) * kBlockMCta;
                 const int32_t n0 = tn * BN + static_cast<int32_t>(rank) * Cfg::kBnCta;
                 for (int kb = wu.kb0; kb < wu.kb1; ++kb) {
                     if (!wait_bar(bar_empty + 8 * stage, phase ^ 1u, w, kRoleProducer, stage)) {
@@ -340,13 +350,21 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         for (int j = 0; j < Cfg::kBAtoms; ++j)
                             tma_load_2d(b_dst + j * Cfg::kBAtomBytes, &tmB, fb, n0 + 64 * j, k0);
                     } else {
-                        const uint32_t fb_leader = mapa_shared(fb, 0);
+                        const uint32_t fb_leader = mapa_shared(fb, leader);
                         if (rank == 0) mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
                         tma_load_2d_pair(a_dst, &tmA, fb_leader, k0, m0);
+                        if constexpr (MC == 1) {
 #pragma unroll
-                        for (int j = 0; j < Cfg::kBAtoms; ++j)
-                            tma_load_2d_pair(b_dst + j * Cfg::kBAtomBytes, &tmB, fb_leader,
-                                             n0 + 64 * j, k0);
+                            for (int j = 0; j < Cfg::kBAtoms; ++j)
+                                tma_load_2d_pair(b_dst + j * Cfg::kBAtomBytes, &tmB, fb_leader,
+                                                 n0 + 64 * j, k0);
+                        } else {
+                            // Atom `pair` of this B half, for this CTA and its
+                            // counterpart in the other pair.
+                            const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << (CG + rank)));
+                            tma_load_2d_pair_mc(b_dst + pair * Cfg::kBAtomBytes, &tmB, fb_leader,
+                                                n0 + 64 * static_cast<int32_t>(pair), k0, mask);
+                        }
                     }
                     if (++stage == S) {
                         stage = 0;
@@ -404,8 +422,12 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                                      (kb > wu.kb0 || kk != 0 || wu.kind == 1) ? 1u : 0u);
                     }
                     issued = true;
+                    // A stage is free once every pair that reads it is done:
+                    // with B multicast, both pairs read every CTA's B atoms.
                     if constexpr (CG == 1) umma_commit(bar_empty + 8 * stage);
-                    else umma_commit_pair(bar_empty + 8 * stage, 0x3);
+                    else umma_commit_pair(bar_empty + 8 * stage,
+                                          MC == 1 ? static_cast<uint16_t>(0x3u << leader)
+                                                  : static_cast<uint16_t>((1u << kCluster) - 1u));
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
@@ -413,13 +435,13 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 }
                 if (!ok) break;
                 if constexpr (CG == 1) umma_commit(bar_tfull + 8 * acc);
-                else umma_commit_pair(bar_tfull + 8 * acc, 0x3);
+                else umma_commit_pair(bar_tfull + 8 * acc, static_cast<uint16_t>(0x3u << leader));
                 trace_stamp(p, it, kTrMmaLast);
             }
             if (!ok && issued) {
                 // TMEM may only be freed once every issued MMA has completed.
                 if constexpr (CG == 1) umma_commit(bar_drain);
-                else umma_commit_pair(bar_drain, 0x1);
+                else umma_commit_pair(bar_drain, static_cast<uint16_t>(1u << leader));
                 const uint64_t t0 = globaltimer_ns();
                 while (!mbar_try_wait(bar_drain, 0) && globaltimer_ns() - t0 < p.timeout_ns) {}
             }
@@ -449,7 +471,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             const unsigned long long want = p.inject == 1 ? ~p.epoch : p.epoch;
             bool have = true;
             for (int32_t q = cluster_id + 1; q <= contrib_last && have; ++q)
-                have = ld_acquire_gpu(p.flags + 2 * partial_block<CG>(q, rank, quarter) + colhalf) == want;
+                have = ld_acquire_gpu(p.flags + 2 * partial_block<kCluster>(q, crank, quarter) + colhalf) == want;
             owner_preloaded = have;
 #pragma unroll 1
             for (int c = colhalf; c < Cfg::kChunks; c += 2) {
@@ -462,7 +484,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 }
                 for (int32_t q = cluster_id + 1; q <= contrib_last && have; ++q) {
                     const float4* src = reinterpret_cast<const float4*>(p.partials) +
-                                        partial_block<CG>(q, rank, quarter) * (kEpiBoxRows * BN / 4);
+                                        partial_block<kCluster>(q, crank, quarter) * (kEpiBoxRows * BN / 4);
 #pragma unroll
                     for (int jj = 0; jj < 8; ++jj) {
                         const float4 a = __ldcg(src + (c * 16 + jj) * 32 + lane);
@@ -489,7 +511,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 if constexpr (CG == 1) {
                     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar_pre + 8 * pacc) : "memory");
                 } else {
-                    mbar_arrive_cluster(mapa_shared(bar_pre + 8 * pacc, 0));
+                    mbar_arrive_cluster(mapa_shared(bar_pre + 8 * pacc, leader));
                 }
             }
         };
@@ -516,7 +538,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             }
             int32_t tm, tn;
             tile_coord(wu.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-            const int32_t row0 = tm * (kBlockMCta * CG) + static_cast<int32_t>(rank) * kBlockMCta +
+            const int32_t row0 = tm * kRowsPerUnit + static_cast<int32_t>(pair * CG + rank) * kBlockMCta +
                                  quarter * kEpiBoxRows;
             const int32_t col0 = tn * BN;
             const uint32_t t_row = tmem_base + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
@@ -530,7 +552,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];"
                                      :: "r"(bar_tempty + 8 * acc) : "memory");
                     } else {
-                        mbar_arrive_cluster(mapa_shared(bar_tempty + 8 * acc, 0));
+                        mbar_arrive_cluster(mapa_shared(bar_tempty + 8 * acc, leader));
                     }
                 }
                 preload_if_owner(it + 2);
@@ -546,7 +568,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 // for a mark no part ever writes; the wait runs out.
                 const unsigned long long want = p.inject == 1 ? ~p.epoch : p.epoch;
                 for (int32_t q = cluster_id + 1; q <= contrib_last; ++q)
-                    if (!wait_flag(p.flags + 2 * partial_block<CG>(q, rank, quarter) + colhalf, want, w,
+                    if (!wait_flag(p.flags + 2 * partial_block<kCluster>(q, crank, quarter) + colhalf, want, w,
                                    64 + ((q - cluster_id) & 63)))
                         break;
             }
@@ -576,7 +598,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                             asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];"
                                          :: "r"(bar_tempty + 8 * acc) : "memory");
                         } else {
-                            mbar_arrive_cluster(mapa_shared(bar_tempty + 8 * acc, 0));
+                            mbar_arrive_cluster(mapa_shared(bar_tempty + 8 * acc, leader));
                         }
                         if (warp == 0) trace_stamp(p, it, kTrEpiTmemFree);
                     }
@@ -587,7 +609,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         // sums (lane-interleaved, so each warp store is 512
                         // contiguous bytes) instead of writing C.
                         float4* dst = reinterpret_cast<float4*>(p.partials) +
-                                      partial_block<CG>(cluster_id, rank, quarter) * (kEpiBoxRows * BN / 4);
+                                      partial_block<kCluster>(cluster_id, crank, quarter) * (kEpiBoxRows * BN / 4);
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
                             dst[(c * 16 + j) * 32 + lane] =
@@ -602,7 +624,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                             __threadfence();
                             __syncwarp();
                             if (lane == 0)
-                                st_release_gpu(p.flags + 2 * partial_block<CG>(cluster_id, rank, quarter) + colhalf,
+                                st_release_gpu(p.flags + 2 * partial_block<kCluster>(cluster_id, crank, quarter) + colhalf,
                                                p.epoch);
                         }
                         continue;
@@ -610,7 +632,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     if (owner_adds) {
                         for (int32_t q = cluster_id + 1; q <= contrib_last; ++q) {
                             const float4* src = reinterpret_cast<const float4*>(p.partials) +
-                                                partial_block<CG>(q, rank, quarter) * (kEpiBoxRows * BN / 4);
+                                                partial_block<kCluster>(q, crank, quarter) * (kEpiBoxRows * BN / 4);
 #pragma unroll
                             for (int j = 0; j < 8; ++j) {
                                 const float4 a = __ldcg(src + (c * 16 + j) * 32 + lane);
@@ -746,7 +768,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 
     // ------------------------------------------------------------ teardown
     __syncthreads();
-    if constexpr (CG == 2) cluster_sync();
+    if constexpr (kCluster > 1) cluster_sync();
     if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc<CG>(tmem_base, Cfg::kTmemCols);

@@ -11,21 +11,22 @@
 
 namespace hg {
 
-// Launch the tcgen05 kernel for (cta_group, block_n) with `clusters` CTA
-// clusters on `stream`. Returns cudaErrorInvalidValue for an unknown pair.
+// Launch the tcgen05 kernel for (cta_group, block_n, mc) with `clusters` CTA
+// clusters (of cta_group * mc CTAs) on `stream`. Returns cudaErrorInvalidValue
+// for a combination that is not instantiated.
 // `c` stores 64-column chunks of C; `c32` the 32-column last chunk of tiles
 // whose width is an odd multiple of 32.
-cudaError_t launch_tc_bf16(int cta_group, int block_n, const CUtensorMap& a, const CUtensorMap& b,
+cudaError_t launch_tc_bf16(int cta_group, int block_n, int mc, const CUtensorMap& a, const CUtensorMap& b,
                            const CUtensorMap& c, const CUtensorMap& c32, const TcParams& p,
                            int clusters, cudaStream_t stream);
-cudaError_t launch_tc_f16(int cta_group, int block_n, const CUtensorMap& a, const CUtensorMap& b,
+cudaError_t launch_tc_f16(int cta_group, int block_n, int mc, const CUtensorMap& a, const CUtensorMap& b,
                           const CUtensorMap& c, const CUtensorMap& c32, const TcParams& p,
                           int clusters, cudaStream_t stream);
 
 // Most CTA clusters of the (cta_group, block_n) kernel that can be resident at
 // once on the current device (0 on error).
-int max_active_clusters_bf16(int cta_group, int block_n);
-int max_active_clusters_f16(int cta_group, int block_n);
+int max_active_clusters_bf16(int cta_group, int block_n, int mc);
+int max_active_clusters_f16(int cta_group, int block_n, int mc);
 
 // Shared-memory ring depth and bytes of an instantiation (host constants).
 int tc_stages(int cta_group, int block_n);

@@ -9,10 +9,11 @@
 
 namespace hg {
 
-template <int CG, int BN, bool kBF16>
+template <int CG, int BN, bool kBF16, int MC = 1>
 struct TcInstance {
     using Cfg = TcCfg<CG, BN>;
-    static constexpr auto kernel() { return &hgemm_tc_kernel<CG, BN, kBF16>; }
+    static constexpr int kCluster = CG * MC;
+    static constexpr auto kernel() { return &hgemm_tc_kernel<CG, BN, kBF16, MC>; }
 
     // The dynamic shared-memory opt-in is per device; set it once per device.
     static cudaError_t prepare() {
@@ -33,12 +34,12 @@ struct TcInstance {
     static void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int clusters,
                             cudaStream_t stream) {
         cfg = cudaLaunchConfig_t{};
-        cfg.gridDim = dim3(static_cast<unsigned>(clusters * CG), 1, 1);
+        cfg.gridDim = dim3(static_cast<unsigned>(clusters * kCluster), 1, 1);
         cfg.blockDim = dim3(kThreads, 1, 1);
         cfg.dynamicSmemBytes = Cfg::kSmemBytes;
         cfg.stream = stream;
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = CG;
+        attr[0].val.clusterDim.x = kCluster;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
@@ -79,11 +80,12 @@ struct TcInstance {
 };
 
 #define HG_TC_DISPATCH(KBF16, CALL)                                                          \
-    if (cta_group == 1 && block_n == 64) return TcInstance<1, 64, KBF16>::CALL;              \
-    if (cta_group == 1 && block_n == 128) return TcInstance<1, 128, KBF16>::CALL;            \
-    if (cta_group == 1 && block_n == 256) return TcInstance<1, 256, KBF16>::CALL;            \
-    if (cta_group == 2 && block_n == 128) return TcInstance<2, 128, KBF16>::CALL;            \
-    if (cta_group == 2 && block_n == 224) return TcInstance<2, 224, KBF16>::CALL;            \
-    if (cta_group == 2 && block_n == 256) return TcInstance<2, 256, KBF16>::CALL;
+    if (mc == 1 && cta_group == 1 && block_n == 64) return TcInstance<1, 64, KBF16>::CALL;   \
+    if (mc == 1 && cta_group == 1 && block_n == 128) return TcInstance<1, 128, KBF16>::CALL; \
+    if (mc == 1 && cta_group == 1 && block_n == 256) return TcInstance<1, 256, KBF16>::CALL; \
+    if (mc == 1 && cta_group == 2 && block_n == 128) return TcInstance<2, 128, KBF16>::CALL; \
+    if (mc == 1 && cta_group == 2 && block_n == 224) return TcInstance<2, 224, KBF16>::CALL; \
+    if (mc == 1 && cta_group == 2 && block_n == 256) return TcInstance<2, 256, KBF16>::CALL; \
+    if (mc == 2 && cta_group == 2 && block_n == 256) return TcInstance<2, 256, KBF16, 2>::CALL;
 
 }  // namespace hg

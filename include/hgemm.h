@@ -138,6 +138,10 @@ uint64_t hgemm_noalloc_scratch_bytes(void);
  *                  when there are fewer than clusters): their 64-deep K blocks
  *                  are cut into equal contiguous ranges, one per cluster;
  *                  3 = stream-K over every tile.
+ *   multicast:     CTA pairs per cluster (cta_group 2, block_n 256 only):
+ *                  0 = planner's choice, 1 = one pair, 2 = two pairs stacked
+ *                  along M that load their shared B columns once, by TMA
+ *                  multicast (tiles of 512 rows).
  */
 typedef struct {
     int32_t cta_group;
@@ -146,6 +150,7 @@ typedef struct {
     int32_t max_clusters;
     int32_t store_mode;
     int32_t stream_k;
+    int32_t multicast;
 } hgemm_config_t;
 
 /* hgemm with an explicit configuration (cfg may be NULL = all zero). */
@@ -171,7 +176,7 @@ hgemm_status_t hgemm_host(const void* hA, const void* hB, void* hC, int64_t M, i
  */
 typedef struct {
     int32_t cta_group;     /* 1 or 2 */
-    int32_t block_m;       /* rows of C per tile: 128 * cta_group */
+    int32_t block_m;       /* rows of C per tile: 128 * cta_group * multicast */
     int32_t block_n;       /* columns of C per tile */
     int32_t block_k;       /* K per pipeline stage (64) */
     int32_t stages;        /* depth of the shared-memory ring */
@@ -191,7 +196,7 @@ typedef struct {
                               sk_extra clusters take one more) */
     int32_t sk_extra;
     int32_t num_kb;        /* 64-deep K blocks per tile: ceil(K / 64) */
-    int32_t reserved;
+    int32_t multicast;     /* CTA pairs per cluster sharing B by multicast (1 = none) */
     int64_t workspace_bytes; /* stream-ordered workspace: repacked operands + fp32 partials */
 } hgemm_plan_t;
 

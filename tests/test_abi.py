@@ -151,7 +151,7 @@ def test_plan_stream_k(lib):
 
 
 def _check_schedule(p):
-    clusters = p["grid_ctas"] // p["cta_group"]
+    clusters = p["grid_ctas"] // (p["cta_group"] * p["multicast"])
     kb = p["num_kb"]
     seen = {}
     units_of = {}
@@ -197,6 +197,7 @@ def _check_schedule(p):
     ((1024, 1280, 704), dict(cta_group=2, block_n=224, max_clusters=5, stream_k=3), 152),
     ((300, 700, 130), dict(cta_group=1, block_n=64, stream_k=3), 152),
     ((777, 999, 4444), dict(stream_k=2), 37),
+    ((4096, 4096, 4096), dict(cta_group=2, block_n=256, multicast=2, stream_k=2), 152),
 ])
 def test_schedule_covers_every_block_once_without_wait_cycles(lib, shape, cfg, sms):
     p = binding.plan(*shape, "bf16", binding.Config(**cfg), sm_count=sms)

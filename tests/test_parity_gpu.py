@@ -23,8 +23,9 @@ CONFIGS = [
     hg.Config(cta_group=2, block_n=128),
     hg.Config(cta_group=2, block_n=224),
     hg.Config(cta_group=2, block_n=256),
+    hg.Config(cta_group=2, block_n=256, multicast=2),
 ]
-CFG_IDS = ["cg1_n64", "cg1_n128", "cg1_n256", "cg2_n128", "cg2_n224", "cg2_n256"]
+CFG_IDS = ["cg1_n64", "cg1_n128", "cg1_n256", "cg2_n128", "cg2_n224", "cg2_n256", "cg2_n256_mc2"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -142,7 +143,7 @@ def test_random_shapes(cfg, shape):
 @pytest.mark.parametrize("max_clusters", [1, 3])
 def test_persistent_loop_many_tiles_per_cta(cfg, max_clusters):
     # few CTAs walk many tiles: ring phases and both accumulators wrap many times
-    c = hg.Config(cfg.cta_group, cfg.block_n, 0, max_clusters, 0)
+    c = hg.Config(cfg.cta_group, cfg.block_n, 0, max_clusters, 0, 0, cfg.multicast)
     A, B = operands(1024, 1280, 320, "f16", 6)
     check_full(A, B, "f16", c)
 
@@ -152,7 +153,7 @@ def test_persistent_loop_many_tiles_per_cta(cfg, max_clusters):
 def test_stream_k(cfg, mode, clusters):
     # a few clusters share the leftover (mode 2) or every (mode 3) tile's K
     # blocks in equal ranges; owners add their partners' partial sums
-    c = hg.Config(cfg.cta_group, cfg.block_n, 0, clusters, 0, mode)
+    c = hg.Config(cfg.cta_group, cfg.block_n, 0, clusters, 0, mode, cfg.multicast)
     A, B = operands(1024, 1280, 704, "bf16", 14)
     check_full(A, B, "bf16", c)
 
@@ -196,7 +197,7 @@ def test_raster_groups(group_m):
 def test_store_modes_match(cfg, store_mode):
     # plain 2-byte stores, direct 16-byte vector stores and smem-staged
     # coalesced stores, ragged M and N
-    c = hg.Config(cfg.cta_group, cfg.block_n, 0, 0, store_mode)
+    c = hg.Config(cfg.cta_group, cfg.block_n, 0, 0, store_mode, 0, cfg.multicast)
     A, B = operands(700, 520, 300, "bf16", 8)
     check_full(A, B, "bf16", c)
 
