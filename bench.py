@@ -131,6 +131,24 @@ class ClockSampler:
                 "power_w_max": max(pw) if pw else None}
 
 
+# ------------------------------------------------------- multi-rank timing
+def max_over_ranks(values, device, world):
+    """Element-wise max of `values` over all ranks (each rank ran its own
+    independent problem; the slowest one sets the job time)."""
+    import torch
+
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_throughput(world, steps, step_flops, total_ms):
+    """Whole-job TFLOP/s: every rank's steps over the slowest rank's time."""
+    return world * steps * step_flops / (total_ms * 1e-3) / 1e12
+
+
 # --------------------------------------------------------------- our arm
 def run_ours(args, rank, world, local_rank):
     import torch
@@ -220,22 +238,17 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     e2e_s = time.perf_counter() - e0
 
-    # max over ranks
-    import torch.distributed as tdist
-    vals = torch.tensor([total_ms, e2e_s, wall], dtype=torch.float64, device=dev)
-    if world > 1:
-        tdist.all_reduce(vals, op=tdist.ReduceOp.MAX)
-    total_ms, e2e_s, wall = vals.tolist()
+    total_ms, e2e_s, wall = max_over_ranks([total_ms, e2e_s, wall], dev, world)
     if rank != 0:
         return None
 
     peaks, peak_src = read_peaks()
-    value = world * args.steps * step_flops / (total_ms * 1e-3) / 1e12
+    value = job_throughput(world, args.steps, step_flops, total_ms)
     avg_launch_ms = total_ms / n_ev
     achieved = step_flops / len(ops) / (avg_launch_ms * 1e-3) / 1e12
     peak = float(peaks["bf16_tflops"])
     clocks = clk.summary()
-    e2e_value = world * e2e_steps * step_flops / e2e_s / 1e12
+    e2e_value = job_throughput(world, e2e_steps, step_flops, e2e_s * 1e3)
     h2d = sum(2 * (o["M"] * o["K"] + o["K"] * o["N"]) for o in ops)
     d2h = sum(2 * o["M"] * o["N"] for o in ops)
     line = {
