@@ -16,10 +16,11 @@
 //   grid swizzle (SWIZZLE_W)                 persistent CTAs walking a grouped raster
 //   Cs staging + SWIZZLE_C + float4 stores   tcgen05.ld -> cvt.rn -> swizzled smem -> TMA store
 //
-// Roles (320 threads, one CTA per SM):
+// Roles (352 threads, one CTA per SM):
 //   warps 0-7  epilogue: warp w reads TMEM lanes 32(w % 4)..+31 (C rows of the
 //              tile) and every other 64-column chunk, starting at chunk w / 4
-//   warp 8     producer: one thread issues the TMA loads of A and B per stage
+//   warps 8,10 producers: one thread each issues the TMA loads of A and B for
+//              alternate stages (even / odd K blocks)
 //   warp 9     MMA: allocates TMEM; one thread of the leader CTA issues tcgen05.mma
 //
 // CTA pairs (CG = 2, a cluster of two): the pair owns a 256-row tile. Each CTA
@@ -49,9 +50,10 @@ constexpr int kBlockK = 64;       // K per stage: 64 half-precision values = one
 constexpr int kUmmaK = 16;        // K of one kind::f16 MMA
 constexpr int kEpiWarps = 8;      // two per TMEM lane quarter, splitting the columns
 constexpr int kEpiQuarters = 4;   // TMEM lane quarters (32 rows each)
-constexpr int kProducerWarp = 8;
+constexpr int kProducerWarp = 8;   // first producer: even K blocks of the CTA's sequence
 constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kProducerWarp2 = 10; // second producer: odd K blocks
+constexpr int kThreads = 352;
 constexpr int kEpiBoxRows = 32;   // one epilogue warp's rows
 constexpr int kEpiBoxCols = 64;   // 128 B of half-precision values
 constexpr int kEpiBoxBytes = kEpiBoxRows * kEpiBoxCols * 2;
@@ -109,6 +111,27 @@ __device__ __forceinline__ void trace_stamp(const TcParams& p, int local_unit, i
     (void)p; (void)local_unit; (void)field;
 #endif
 }
+
+// Wait-time counters of a traced build: per CTA, clock64 cycles the producers
+// and the MMA thread spent in barrier waits (unit slot kTraceUnits - 1).
+enum : int { kTwProdEmpty0 = 0, kTwProdEmpty1 = 1, kTwMmaFull = 2, kTwMmaTempty = 3, kTwMmaStages = 4,
+             kTwMmaSpan = 5 };
+__device__ __forceinline__ void trace_wait_total(const TcParams& p, int field, long long cycles) {
+#ifdef HG_TRACE
+    if (p.trace)
+        p.trace[(static_cast<int64_t>(blockIdx.x) * kTraceUnits + kTraceUnits - 1) * kTraceFields + field] =
+            static_cast<unsigned long long>(cycles);
+#else
+    (void)p; (void)field; (void)cycles;
+#endif
+}
+#ifdef HG_TRACE
+#define HG_TW_BEGIN() const long long hg_tw0 = clock64()
+#define HG_TW_END(acc) (acc) += clock64() - hg_tw0
+#else
+#define HG_TW_BEGIN() do {} while (0)
+#define HG_TW_END(acc) do {} while (0)
+#endif
 
 // Index of the partial block published by cluster `cluster` (its one
 // non-owning stream-K unit) for the CTA of cluster rank `crank` and TMEM lane
@@ -266,6 +289,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     constexpr int S = Cfg::kStages;
     constexpr int kCluster = CG * MC;
     static_assert(MC == 1 || (CG == 2 && MC == 2 && Cfg::kBAtoms == 2), "B multicast across pairs");
+    static_assert(S >= 2, "the two producers take alternate stages");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
@@ -322,20 +346,32 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const Waiter w{abort_flag, p.timeout_ns, p.status};
     if (threadIdx.x == 0) trace_stamp(p, 0, kTrSetup);
 
-    if (warp == kProducerWarp) {
+    if (warp == kProducerWarp || warp == kProducerWarp2) {
         // ------------------------------------------------------------ producer
+        // Two producer threads take alternate K blocks of the CTA's sequence
+        // (block g of the sequence goes to stage g mod S): one thread needs
+        // longer to issue a stage (a barrier wait, the expected-bytes arrive,
+        // the TMA copies) than a 256-wide pair MMA takes to consume it, so a
+        // single producer would starve the tensor core.
         if (lane == 0) {
-            uint32_t stage = 0, phase = 0;
+            const uint32_t pid = warp == kProducerWarp ? 0u : 1u;
+            uint32_t stage = pid, phase = 0;
+            uint32_t g = 0;
             bool ok = true;
+            long long tw_empty = 0;
             WorkUnit wu;
             for (int lu = 0; ok && next_unit(p.sched, cluster_id, lu, wu); ++lu) {
-                trace_stamp(p, lu, kTrProdFirst);
+                if (pid == 0) trace_stamp(p, lu, kTrProdFirst);
                 int32_t tm, tn;
                 tile_coord(wu.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
                 const int32_t m0 = tm * kRowsPerUnit + static_cast<int32_t>(pair * CG + rank) * kBlockMCta;
                 const int32_t n0 = tn * BN + static_cast<int32_t>(rank) * Cfg::kBnCta;
-                for (int kb = wu.kb0; kb < wu.kb1; ++kb) {
-                    if (!wait_bar(bar_empty + 8 * stage, phase ^ 1u, w, kRoleProducer, stage)) {
+                for (int kb = wu.kb0; kb < wu.kb1; ++kb, ++g) {
+                    if ((g & 1u) != pid) continue;
+                    HG_TW_BEGIN();
+                    const bool got = wait_bar(bar_empty + 8 * stage, phase ^ 1u, w, kRoleProducer, stage);
+                    HG_TW_END(tw_empty);
+                    if (!got) {
                         ok = false;
                         break;
                     }
@@ -366,12 +402,14 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                                                 n0 + 64 * static_cast<int32_t>(pair), k0, mask);
                         }
                     }
-                    if (++stage == S) {
-                        stage = 0;
+                    stage += 2;
+                    if (stage >= static_cast<uint32_t>(S)) {
+                        stage -= S;
                         phase ^= 1u;
                     }
                 }
             }
+            trace_wait_total(p, pid == 0 ? kTwProdEmpty0 : kTwProdEmpty1, tw_empty);
             if (!ok) {
                 // Loads already issued still land in this CTA's shared memory:
                 // give them time before the CTA may exit.
@@ -386,11 +424,20 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             bool ok = true;
             bool issued = false;
             uint32_t pre_phase[2] = {0u, 0u};
+            long long tw_full = 0, tw_tempty = 0, n_stages = 0;
+#ifdef HG_TRACE
+            const long long t_span0 = clock64();
+#endif
+            const uint64_t a_desc0 = sdesc_sw128(sA, 16u, 1024u);
+            const uint64_t b_desc0 = sdesc_sw128(sB, Cfg::kBAtomBytes, 1024u);
             WorkUnit wu;
             for (int it = 0; next_unit(p.sched, cluster_id, it, wu); ++it) {
                 const uint32_t acc = static_cast<uint32_t>(it) & 1u;
                 const uint32_t acc_phase = (static_cast<uint32_t>(it) >> 1) & 1u;
-                if (!wait_bar(bar_tempty + 8 * acc, acc_phase ^ 1u, w, kRoleMma, 32 + acc)) {
+                HG_TW_BEGIN();
+                const bool got_acc = wait_bar(bar_tempty + 8 * acc, acc_phase ^ 1u, w, kRoleMma, 32 + acc);
+                HG_TW_END(tw_tempty);
+                if (!got_acc) {
                     ok = false;
                     break;
                 }
@@ -405,21 +452,28 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
+                // An owner's first MMA adds to the preloaded partial sums.
+                uint32_t accum = wu.kind == 1 ? 1u : 0u;
                 for (int kb = wu.kb0; kb < wu.kb1; ++kb) {
-                    if (!wait_bar(bar_full + 8 * stage, phase, w, kRoleMma, stage)) {
+                    HG_TW_BEGIN();
+                    const bool got_full = wait_bar(bar_full + 8 * stage, phase, w, kRoleMma, stage);
+                    HG_TW_END(tw_full);
+                    if (!got_full) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
+                    ++n_stages;
                     if (kb == wu.kb0) trace_stamp(p, it, kTrMmaFirst);
-                    const uint32_t a0 = sA + stage * Cfg::kABytes;
-                    const uint32_t b0 = sB + stage * Cfg::kBBytes;
+                    // Descriptor start addresses are in 16-byte units: stage s
+                    // adds s * stage bytes / 16; each K = 16 step moves 32 bytes
+                    // along A's swizzled rows and 16 rows (2 KiB) down B's atoms.
+                    const uint64_t ad = a_desc0 + ((stage * Cfg::kABytes) >> 4);
+                    const uint64_t bd = b_desc0 + ((stage * Cfg::kBBytes) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < kBlockK / kUmmaK; ++kk) {
-                        const uint64_t ad = sdesc_sw128(a0 + 32u * kk, 16u, 1024u);
-                        const uint64_t bd = sdesc_sw128(b0 + 2048u * kk, Cfg::kBAtomBytes, 1024u);
-                        umma_f16<CG>(d_tmem, ad, bd, p.idesc,
-                                     (kb > wu.kb0 || kk != 0 || wu.kind == 1) ? 1u : 0u);
+                        umma_f16<CG>(d_tmem, ad + 2u * kk, bd + 128u * kk, p.idesc, accum);
+                        accum = 1u;
                     }
                     issued = true;
                     // A stage is free once every pair that reads it is done:
@@ -438,6 +492,12 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 else umma_commit_pair(bar_tfull + 8 * acc, static_cast<uint16_t>(0x3u << leader));
                 trace_stamp(p, it, kTrMmaLast);
             }
+            trace_wait_total(p, kTwMmaFull, tw_full);
+            trace_wait_total(p, kTwMmaTempty, tw_tempty);
+            trace_wait_total(p, kTwMmaStages, n_stages);
+#ifdef HG_TRACE
+            trace_wait_total(p, kTwMmaSpan, clock64() - t_span0);
+#endif
             if (!ok && issued) {
                 // TMEM may only be freed once every issued MMA has completed.
                 if constexpr (CG == 1) umma_commit(bar_drain);
