@@ -148,13 +148,15 @@ double tile_seconds(int cg, int bn, int64_t num_kb) {
 }
 
 // Stream-K tiles for `tiles` tiles on `clusters` clusters: the leftover
-// tiles of a partial last wave plus one full wave (all tiles when there are
-// fewer than clusters), or 0 when the waves come out whole. mode 3 = all.
+// tiles of a partial last wave plus one full wave (mode 2) or the leftover
+// tiles alone (mode 4); all tiles when there are fewer than clusters; 0 when
+// the waves come out whole. mode 3 = all.
 int64_t stream_k_tiles(int64_t tiles, int64_t clusters, int mode) {
     if (mode == 3) return tiles;
     const int64_t rem = tiles % clusters;
     if (rem == 0) return 0;
-    return tiles < clusters ? tiles : rem + clusters;
+    if (tiles < clusters) return tiles;
+    return mode == 4 ? rem : rem + clusters;
 }
 
 // Estimated seconds of a plan: data-parallel waves, then the stream-K phase
@@ -296,7 +298,7 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, const hgemm_config_t* 
     hgemm_config_t c{};
     if (cfg) c = *cfg;
     if (c.group_m < 0 || c.max_clusters < 0 || c.store_mode < 0 || c.store_mode > 4 || c.stream_k < 0 ||
-        c.stream_k > 3) {
+        c.stream_k > 4) {
         t_last_error = "negative or unknown config field";
         return HGEMM_ERR_INVALID_ARG;
     }

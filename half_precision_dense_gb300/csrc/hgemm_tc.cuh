@@ -125,6 +125,18 @@ __device__ __forceinline__ void trace_wait_total(const TcParams& p, int field, l
     (void)p; (void)field; (void)cycles;
 #endif
 }
+// Stream-K fix-up stamps of a traced build: unit slot 30 = the owner unit
+// (0: partners' marks seen, 1: chunk loop done, 2: last store drained, 3+j:
+// warp 0's j-th chunk done), slot 29 = the first partner unit (0: epilogue
+// start, 1: partial sums published).
+__device__ __forceinline__ void trace_slot(const TcParams& p, int slot, int field) {
+#ifdef HG_TRACE
+    if (p.trace)
+        p.trace[(static_cast<int64_t>(blockIdx.x) * kTraceUnits + slot) * kTraceFields + field] = globaltimer_ns();
+#else
+    (void)p; (void)slot; (void)field;
+#endif
+}
 #ifdef HG_TRACE
 #define HG_TW_BEGIN() const long long hg_tw0 = clock64()
 #define HG_TW_END(acc) (acc) += clock64() - hg_tw0
@@ -171,7 +183,12 @@ struct TcCfg {
     static_assert(kTmemCols <= 512, "tensor memory");
     static_assert(kStages >= 2, "pipeline depth");
     static_assert(kSmemBytes <= kSmemLimit, "shared memory");
-    static_assert((2 * kStages + 7) * 8 + 8 <= kBarBytes, "barrier area");
+    // full[S], empty[S], tmem_full[2], tmem_empty[2], drain, pre[2], the TMEM
+    // slot and abort flag, one partial-sum barrier per epilogue warp
+    static_assert((2 * kStages + 7) * 8 + 8 + 8 * kEpiWarps <= kBarBytes, "barrier area");
+    // A stream-K owner's epilogue lands its partners' partial sums in the
+    // (then idle) stage ring: per epilogue warp and partner one 8 KiB chunk.
+    static constexpr int kBulkPartners = kStages * kStageBytes / (kEpiWarps * 8192);
 };
 
 // Shared-memory matrix descriptor (tcgen05), 128-byte swizzle.
@@ -307,6 +324,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const uint32_t bar_pre = bar_drain + 8;                     // [2]
     uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(smem + (bar_pre + 16 - base));
     volatile uint32_t* const abort_flag = tmem_slot + 1;
+    const uint32_t bar_part = bar_pre + 24;                     // [kEpiWarps]
 
     const int warp = static_cast<int>(threadIdx.x >> 5);
     const uint32_t lane = threadIdx.x & 31u;
@@ -328,6 +346,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         }
         mbar_init(bar_drain, 1);
         for (int a = 0; a < 2; ++a) mbar_init(bar_pre + 8 * a, kEpiWarps * CG);
+        for (int e = 0; e < kEpiWarps; ++e) mbar_init(bar_part + 8 * e, 1);
         *abort_flag = 0;
         fence_mbarrier_init_cluster();
     }
@@ -631,13 +650,36 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     if (!wait_flag(p.flags + 2 * partial_block<kCluster>(q, crank, quarter) + colhalf, want, w,
                                    64 + ((q - cluster_id) & 63)))
                         break;
+                if (warp == 0 && lane == 0) trace_slot(p, 30, 0);
             }
+            if (is_split && !owner && warp == 0 && lane == 0) trace_slot(p, 29, 0);
+            // An owner adding its partners' partial sums copies them, a chunk at
+            // a time, into the stage ring by bulk copies: its unit is the
+            // CTA's last, so once its MMAs are done (the tmem_full wait above)
+            // the ring is idle and no load is in flight. The copies of a chunk
+            // run while its TMEM loads do.
+            const int32_t n_part = contrib_last - cluster_id;
+            const bool bulk_adds = owner_adds && n_part <= Cfg::kBulkPartners;
+            const uint32_t part_buf = sA + static_cast<uint32_t>(warp) * static_cast<uint32_t>(n_part) * 8192u;
+            uint32_t part_phase = 0;
 #pragma unroll 1
             for (int c = colhalf; c < Cfg::kChunks; c += 2) {
                 // A chunk is 64 columns (two 32-column TMEM loads), or 32 for the
                 // last chunk of a tile whose width is an odd multiple of 32.
                 const bool half = Cfg::kHalfLast && c == Cfg::kChunks - 1;
                 const bool last = c + 2 >= Cfg::kChunks;
+                if (bulk_adds && lane == 0) {
+                    // chunk c of a partial block: float4s [16c * 32, 16(c + 1) * 32)
+                    const uint32_t bytes = half ? 4096u : 8192u;
+                    fence_proxy_async_all();
+                    mbar_arrive_expect_tx(bar_part + 8 * warp, bytes * static_cast<uint32_t>(n_part));
+                    for (int32_t q = 0; q < n_part; ++q)
+                        bulk_load(part_buf + static_cast<uint32_t>(q) * 8192u,
+                                  reinterpret_cast<const float4*>(p.partials) +
+                                      partial_block<kCluster>(cluster_id + 1 + q, crank, quarter) * (kEpiBoxRows * BN / 4) +
+                                      c * 16 * 32,
+                                  bytes, bar_part + 8 * warp);
+                }
                 uint32_t r0[32], r1[32];
                 tmem_ld_32x32b_x32(t_row + 64u * c, r0);
                 if (!half) tmem_ld_32x32b_x32(t_row + 64u * c + 32u, r1);
@@ -686,10 +728,39 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                             if (lane == 0)
                                 st_release_gpu(p.flags + 2 * partial_block<kCluster>(cluster_id, crank, quarter) + colhalf,
                                                p.epoch);
+                            if (warp == 0 && lane == 0) trace_slot(p, 29, 1);
                         }
                         continue;
                     }
-                    if (owner_adds) {
+                    if (bulk_adds) {
+                        if (wait_bar(bar_part + 8 * warp, part_phase, w, kRoleEpilogue, 80 + warp)) {
+                            for (int32_t q = 0; q < n_part; ++q) {
+                                const uint32_t src = part_buf + static_cast<uint32_t>(q) * 8192u + lane * 16u;
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) {
+                                    const float4 a = ld_shared_f4(src + static_cast<uint32_t>(j) * 512u);
+                                    r0[4 * j] = __float_as_uint(__uint_as_float(r0[4 * j]) + a.x);
+                                    r0[4 * j + 1] = __float_as_uint(__uint_as_float(r0[4 * j + 1]) + a.y);
+                                    r0[4 * j + 2] = __float_as_uint(__uint_as_float(r0[4 * j + 2]) + a.z);
+                                    r0[4 * j + 3] = __float_as_uint(__uint_as_float(r0[4 * j + 3]) + a.w);
+                                    if (!half) {
+                                        const float4 b = ld_shared_f4(src + static_cast<uint32_t>(8 + j) * 512u);
+                                        r1[4 * j] = __float_as_uint(__uint_as_float(r1[4 * j]) + b.x);
+                                        r1[4 * j + 1] = __float_as_uint(__uint_as_float(r1[4 * j + 1]) + b.y);
+                                        r1[4 * j + 2] = __float_as_uint(__uint_as_float(r1[4 * j + 2]) + b.z);
+                                        r1[4 * j + 3] = __float_as_uint(__uint_as_float(r1[4 * j + 3]) + b.w);
+                                    }
+                                }
+                            }
+                        } else if (lane == 0) {
+                            // The wait ran out (the status word says so): let the
+                            // copies still in flight land before the CTA can exit.
+                            const uint64_t t0 = globaltimer_ns();
+                            while (globaltimer_ns() - t0 < 50000ull) {}
+                        }
+                        part_phase ^= 1u;
+                        __syncwarp();
+                    } else if (owner_adds) {
                         for (int32_t q = cluster_id + 1; q <= contrib_last; ++q) {
                             const float4* src = reinterpret_cast<const float4*>(p.partials) +
                                                 partial_block<kCluster>(q, crank, quarter) * (kEpiBoxRows * BN / 4);
@@ -773,6 +844,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         bulk_commit_group();
                     }
                     if (warp == 0 && lane == 0) trace_chunk(p, it, c, kTcIssued);
+                    if (is_split && owner && warp == 0 && lane == 0) trace_slot(p, 30, 3 + (c >> 1));
                 } else if (p.store_mode == 4) {
                     // Read the box back row-contiguously: 8 lanes cover one row's
                     // 128 bytes (64-column box) or 4 lanes its 64 bytes (32-column
@@ -819,10 +891,14 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     __syncwarp();
                 }
             }
-            if (warp == 0 && lane == 0) trace_stamp(p, it, kTrEpiEnd);
+            if (warp == 0 && lane == 0) {
+                trace_stamp(p, it, kTrEpiEnd);
+                if (is_split && owner) trace_slot(p, 30, 1);
+            }
             preload_if_owner(it + 2);
         }
         if (lane == 0) bulk_wait_group<0>();
+        if (warp == 0 && lane == 0) trace_slot(p, 30, 2);
         __syncwarp();
     }
 

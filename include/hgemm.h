@@ -137,7 +137,8 @@ uint64_t hgemm_noalloc_scratch_bytes(void);
  *                  over the leftover tiles plus one full wave (or all tiles
  *                  when there are fewer than clusters): their 64-deep K blocks
  *                  are cut into equal contiguous ranges, one per cluster;
- *                  3 = stream-K over every tile.
+ *                  3 = stream-K over every tile; 4 = stream-K over the
+ *                  leftover tiles of the partial last wave only.
  *   multicast:     CTA pairs per cluster (cta_group 2, block_n 256 only):
  *                  0 = planner's choice, 1 = one pair, 2 = two pairs stacked
  *                  along M that load their shared B columns once, by TMA

@@ -144,6 +144,12 @@ def test_plan_stream_k(lib):
     assert even["sk_tiles"] == 0 and even["grid_ctas"] == 76
     short = binding.plan(4096, 4096, 64, "bf16", binding.Config(cta_group=2, block_n=256), sm_count=152)
     assert short["sk_tiles"] == 0
+    # mode 4: three whole waves of 76, then only the 28 leftover tiles' 1792
+    # K blocks, 23 or 24 per cluster
+    left = binding.plan(4096, 4096, 4096, "bf16", binding.Config(cta_group=2, block_n=256, stream_k=4),
+                        sm_count=152)
+    assert (left["dp_tiles"], left["sk_tiles"], left["sk_blocks"], left["sk_extra"]) == (228, 28, 23, 44)
+    assert left["grid_ctas"] == 152
     # mode 3 shares every tile
     every = binding.plan(1024, 1024, 1024, "f16",
                          binding.Config(cta_group=1, block_n=128, stream_k=3), sm_count=20)
@@ -198,6 +204,8 @@ def _check_schedule(p):
     ((300, 700, 130), dict(cta_group=1, block_n=64, stream_k=3), 152),
     ((777, 999, 4444), dict(stream_k=2), 37),
     ((4096, 4096, 4096), dict(cta_group=2, block_n=256, multicast=2, stream_k=2), 152),
+    ((4096, 4096, 4096), dict(cta_group=2, block_n=256, stream_k=4), 152),
+    ((1024, 1280, 704), dict(cta_group=1, block_n=128, max_clusters=7, stream_k=4), 152),
 ])
 def test_schedule_covers_every_block_once_without_wait_cycles(lib, shape, cfg, sms):
     p = binding.plan(*shape, "bf16", binding.Config(**cfg), sm_count=sms)

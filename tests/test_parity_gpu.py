@@ -149,10 +149,11 @@ def test_persistent_loop_many_tiles_per_cta(cfg, max_clusters):
 
 
 @pytest.mark.parametrize("cfg", CONFIGS, ids=CFG_IDS)
-@pytest.mark.parametrize("mode,clusters", [(2, 3), (3, 3), (3, 7)])
+@pytest.mark.parametrize("mode,clusters", [(2, 3), (3, 3), (3, 7), (4, 7)])
 def test_stream_k(cfg, mode, clusters):
-    # a few clusters share the leftover (mode 2) or every (mode 3) tile's K
-    # blocks in equal ranges; owners add their partners' partial sums
+    # a few clusters share the leftover tiles plus a wave (mode 2), every tile
+    # (mode 3) or the leftover tiles alone (mode 4) in equal ranges of K
+    # blocks; owners add their partners' partial sums
     c = hg.Config(cfg.cta_group, cfg.block_n, 0, clusters, 0, mode, cfg.multicast)
     A, B = operands(1024, 1280, 704, "bf16", 14)
     check_full(A, B, "bf16", c)
