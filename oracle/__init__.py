@@ -1,4 +1,6 @@
-"""CPU oracle for the dense half-precision GEMM (test infrastructure only).
+"""CPU oracles for the dense GEMM (test infrastructure only): the fp16/bf16
+product (``hgemm_oracle``, re-exported here) and the TF32 variant
+(``oracle.tf32_oracle``).
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline and
 reference legs may import this package. The product path never does.
