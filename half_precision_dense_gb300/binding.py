@@ -19,6 +19,7 @@ _lock = threading.Lock()
 
 HGEMM_F16 = 0
 HGEMM_BF16 = 1
+HGEMM_TF32 = 2
 STATUS_NAMES = {0: "HGEMM_OK", 1: "HGEMM_ERR_INVALID_ARG", 2: "HGEMM_ERR_UNSUPPORTED_DEVICE",
                 3: "HGEMM_ERR_CUDA", 4: "HGEMM_ERR_ALLOC", 5: "HGEMM_ERR_TIMEOUT"}
 
@@ -110,13 +111,15 @@ def load_library():
 
 
 def _dtype_code(dtype) -> int:
-    if dtype in (HGEMM_F16, HGEMM_BF16):
+    if dtype in (HGEMM_F16, HGEMM_BF16, HGEMM_TF32):
         return int(dtype)
     name = str(dtype)
     if name in ("bf16", "bfloat16", "torch.bfloat16"):
         return HGEMM_BF16
     if name in ("f16", "fp16", "float16", "half", "torch.float16"):
         return HGEMM_F16
+    if name in ("tf32", "f32", "fp32", "float32", "torch.float32"):
+        return HGEMM_TF32
     raise ValueError(f"unsupported dtype {dtype!r}")
 
 
@@ -226,13 +229,14 @@ def version() -> int:
 
 
 def matmul(a, b, out=None, config: Config | None = None, stream=None):
-    """C = a @ b for 2-D contiguous CUDA tensors of dtype float16 or bfloat16."""
+    """C = a @ b for 2-D contiguous CUDA tensors of dtype float16, bfloat16 or
+    float32 (float32 operands are multiplied as tf32: see include/hgemm.h)."""
     import torch
 
     if a.dim() != 2 or b.dim() != 2 or a.shape[1] != b.shape[0]:
         raise ValueError(f"shapes {tuple(a.shape)} and {tuple(b.shape)} do not chain")
-    if a.dtype != b.dtype or a.dtype not in (torch.float16, torch.bfloat16):
-        raise ValueError("a and b must share dtype float16 or bfloat16")
+    if a.dtype != b.dtype or a.dtype not in (torch.float16, torch.bfloat16, torch.float32):
+        raise ValueError("a and b must share dtype float16, bfloat16 or float32")
     if not (a.is_cuda and b.is_cuda and a.is_contiguous() and b.is_contiguous()):
         raise ValueError("a and b must be contiguous CUDA tensors")
     M, K = a.shape

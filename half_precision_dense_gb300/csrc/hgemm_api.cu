@@ -60,6 +60,11 @@ hgemm_status_t device_info(int* dev_out, DeviceInfo* out) {
     return HGEMM_OK;
 }
 
+// Element bytes and K per pipeline stage (one 128-byte row of A) of a dtype.
+bool valid_dtype(int dt) { return dt == HGEMM_F16 || dt == HGEMM_BF16 || dt == HGEMM_TF32; }
+int esize_of(hgemm_dtype_t dt) { return dt == HGEMM_TF32 ? 4 : 2; }
+int64_t bk_of(hgemm_dtype_t dt) { return 128 / esize_of(dt); }
+
 // ------------------------------------------------- cuTensorMapEncodeTiled
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -80,7 +85,7 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// A 2-D row-major matrix of 16-bit values: `cols` contiguous values per row,
+// A 2-D row-major matrix of `dt` values: `cols` contiguous values per row,
 // `ld` values between rows; box = box_cols x box_rows, 128-byte swizzle,
 // out-of-range elements read as zero. 128-byte swizzle unless given.
 hgemm_status_t encode_2d(CUtensorMap* m, hgemm_dtype_t dt, const void* base, int64_t rows,
@@ -92,10 +97,13 @@ hgemm_status_t encode_2d(CUtensorMap* m, hgemm_dtype_t dt, const void* base, int
         return HGEMM_ERR_CUDA;
     }
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * esize_of(dt)};
     const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(m, dt == HGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+    const CUtensorMapDataType type = dt == HGEMM_TF32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                     : dt == HGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUresult r = fn(m, type,
                     2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -107,9 +115,9 @@ hgemm_status_t encode_2d(CUtensorMap* m, hgemm_dtype_t dt, const void* base, int
 }
 
 // ----------------------------------------------------------------- planner
-bool valid_shape_config(int cg, int bn) {
+bool valid_shape_config(int cg, int bn, hgemm_dtype_t dt) {
     return (cg == 1 && (bn == 64 || bn == 128 || bn == 256)) ||
-           (cg == 2 && (bn == 128 || bn == 224 || bn == 256));
+           (cg == 2 && (bn == 128 || (bn == 224 && dt != HGEMM_TF32) || bn == 256));
 }
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -234,14 +242,23 @@ struct WorkspaceLayout {
     int64_t off_a, off_b, off_part, off_flags, total;
 };
 
-WorkspaceLayout workspace_layout(const hgemm_plan_t& pl, int64_t M, int64_t N, int64_t K) {
+// Rows of `cols` elements padded to a 16-byte pitch.
+int64_t pitch16(int64_t cols, int esize) {
+    const int64_t per = 16 / esize;
+    return (cols + per - 1) / per * per;
+}
+
+// The B copy of a tf32 GEMM is B transposed (N x K, K padded to a 16-byte
+// pitch): kind::tf32 takes both operands K-major.
+WorkspaceLayout workspace_layout(const hgemm_plan_t& pl, int64_t M, int64_t N, int64_t K, int esize) {
     WorkspaceLayout w{};
-    const int64_t lda = (K + 7) / 8 * 8, ldb = (N + 7) / 8 * 8;
+    const int64_t lda = pitch16(K, esize), ldb = pitch16(N, esize);
+    const bool bt = esize == 4;
     int64_t off = 0;
     w.off_a = off;
-    off += pl.repack_a ? align256(2 * M * lda) : 0;
+    off += pl.repack_a ? align256(esize * M * lda) : 0;
     w.off_b = off;
-    off += pl.repack_b ? align256(2 * K * ldb) : 0;
+    off += pl.repack_b ? align256(bt ? esize * N * pitch16(K, esize) : esize * K * ldb) : 0;
     w.off_part = off;
     off += align256(partial_bytes(pl));
     w.off_flags = off;
@@ -255,8 +272,10 @@ WorkspaceLayout workspace_layout(const hgemm_plan_t& pl, int64_t M, int64_t N, i
 // its padded area at the shape's efficiency, plus the fixed costs above. A
 // problem with a single 128-row tile row keeps one CTA per tile (a pair would
 // compute an empty half).
-double estimate_seconds(int64_t M, int64_t N, int64_t K, int cg, int bn, int64_t clusters) {
-    const int64_t kb = cdiv(K, hg::kBlockK);
+// A stage costs the same time for every dtype (128 bytes of K of A per row:
+// 64 fp16/bf16 values, or 32 tf32 values at half the tensor rate).
+double estimate_seconds(int64_t M, int64_t N, int64_t K, int cg, int bn, int64_t clusters, hgemm_dtype_t dt) {
+    const int64_t kb = cdiv(K, bk_of(dt));
     const int64_t tiles = cdiv(M, 128 * cg) * cdiv(N, bn);
     hgemm_plan_t pl{};
     pl.cta_group = cg;
@@ -267,21 +286,23 @@ double estimate_seconds(int64_t M, int64_t N, int64_t K, int cg, int bn, int64_t
     return schedule_seconds(cg, bn, tiles, pl.grid_ctas / cg, kb, pl.sk_tiles);
 }
 
-void choose_shape(int64_t M, int64_t N, int64_t K, int sms, int max_clusters, int* cg_out, int* bn_out) {
+void choose_shape(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dt, int sms, int max_clusters, int* cg_out,
+                  int* bn_out) {
     static const int cand[6][2] = {{2, 256}, {2, 224}, {1, 256}, {1, 128}, {2, 128}, {1, 64}};
     double best = 1e300;
     int bcg = 2, bbn = 256;
     for (const auto& c : cand) {
         const int cg = c[0], bn = c[1];
         if (cg == 2 && M <= 128) continue;
+        if (!valid_shape_config(cg, bn, dt)) continue;
         // A single tile row on a long K loop is HBM-bound: 128-wide tiles give
         // twice the tiles of 256-wide ones for stream-K to spread (measured
         // best on GB300); the time model above assumes compute-bound tiles.
-        if (M <= 128 && K >= 16 * hg::kBlockK && bn != 128) continue;
+        if (M <= 128 && K >= 16 * bk_of(dt) && bn != 128) continue;
         int64_t clusters = sms / cg;
         if (max_clusters > 0 && max_clusters < clusters) clusters = max_clusters;
         if (clusters <= 0) continue;
-        const double t = estimate_seconds(M, N, K, cg, bn, clusters);
+        const double t = estimate_seconds(M, N, K, cg, bn, clusters, dt);
         if (t < best * 0.999) {
             best = t;
             bcg = cg;
@@ -292,7 +313,7 @@ void choose_shape(int64_t M, int64_t N, int64_t K, int sms, int max_clusters, in
     *bn_out = bbn;
 }
 
-hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, const hgemm_config_t* cfg, int sms,
+hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dt, const hgemm_config_t* cfg, int sms,
                          bool a_unaligned, bool b_unaligned, bool c_unaligned, hgemm_plan_t* pl) {
     std::memset(pl, 0, sizeof(*pl));
     hgemm_config_t c{};
@@ -305,7 +326,7 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, const hgemm_config_t* 
     int cg = c.cta_group, bn = c.block_n;
     if (cg == 0 || bn == 0) {
         int acg, abn;
-        choose_shape(M, N, K, sms, c.max_clusters, &acg, &abn);
+        choose_shape(M, N, K, dt, sms, c.max_clusters, &acg, &abn);
         if (cg == 0 && bn == 0) {
             cg = acg;
             bn = abn;
@@ -315,12 +336,13 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, const hgemm_config_t* 
             bn = (cg == 2 && abn < 128) ? 128 : abn;
         }
     }
-    if (!valid_shape_config(cg, bn)) {
+    if (!valid_shape_config(cg, bn, dt)) {
         t_last_error = "unsupported (cta_group, block_n) pair";
         return HGEMM_ERR_INVALID_ARG;
     }
-    if (c.multicast < 0 || c.multicast > 2 || (c.multicast == 2 && !(cg == 2 && bn == 256))) {
-        t_last_error = "multicast = 2 needs cta_group 2 and block_n 256";
+    if (c.multicast < 0 || c.multicast > 2 ||
+        (c.multicast == 2 && !(cg == 2 && bn == 256 && dt != HGEMM_TF32))) {
+        t_last_error = "multicast = 2 needs cta_group 2, block_n 256 and a 16-bit dtype";
         return HGEMM_ERR_INVALID_ARG;
     }
     const int mc = c.multicast == 2 ? 2 : 1;
@@ -328,7 +350,7 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, const hgemm_config_t* 
     pl->multicast = mc;
     pl->block_m = 128 * cg * mc;
     pl->block_n = bn;
-    pl->block_k = hg::kBlockK;
+    pl->block_k = static_cast<int32_t>(bk_of(dt));
     pl->stages = hg::tc_stages(cg, bn);
     pl->smem_bytes = hg::tc_smem_bytes(cg, bn);
     pl->tmem_cols = hg::tc_tmem_cols(cg, bn);
@@ -338,15 +360,15 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, const hgemm_config_t* 
     pl->group_m = c.group_m > 0 ? c.group_m : (pl->tiles_m < 8 ? (pl->tiles_m > 0 ? pl->tiles_m : 1) : 8);
     int64_t clusters = sms / (cg * mc);
     if (c.max_clusters > 0 && c.max_clusters < clusters) clusters = c.max_clusters;
-    schedule_plan(pl, clusters, c.stream_k, cdiv(K, hg::kBlockK));
+    schedule_plan(pl, clusters, c.stream_k, cdiv(K, bk_of(dt)));
     pl->repack_a = a_unaligned ? 1 : 0;
-    pl->repack_b = b_unaligned ? 1 : 0;
+    pl->repack_b = (b_unaligned || dt == HGEMM_TF32) ? 1 : 0;
     pl->store_mode = (c.store_mode != 0) ? c.store_mode : (c_unaligned ? 2 : 1);
     if (c_unaligned && pl->store_mode != 2) {
         t_last_error = "vector and TMA stores need a 16-byte aligned C with a 16-byte row pitch";
         return HGEMM_ERR_INVALID_ARG;
     }
-    pl->workspace_bytes = workspace_layout(*pl, M, N, K).total;
+    pl->workspace_bytes = workspace_layout(*pl, M, N, K, esize_of(dt)).total;
     return HGEMM_OK;
 }
 
@@ -386,8 +408,8 @@ unsigned long long next_epoch() {
     return counter.fetch_add(1, std::memory_order_relaxed);
 }
 
-bool misaligned16(const void* p, int64_t cols) {
-    return (reinterpret_cast<uintptr_t>(p) & 15u) != 0 || ((cols * 2) & 15) != 0;
+bool misaligned16(const void* p, int64_t cols, int esize) {
+    return (reinterpret_cast<uintptr_t>(p) & 15u) != 0 || ((cols * esize) & 15) != 0;
 }
 
 bool overlaps(const void* a, int64_t abytes, const void* b, int64_t bbytes) {
@@ -402,21 +424,23 @@ hgemm_status_t check_args(const void* A, const void* B, void* C, int64_t M, int6
         t_last_error = "dimensions must be in [0, 2^31 - 1]";
         return HGEMM_ERR_INVALID_ARG;
     }
-    if (dtype != HGEMM_F16 && dtype != HGEMM_BF16) {
+    if (!valid_dtype(dtype)) {
         t_last_error = "unknown dtype";
         return HGEMM_ERR_INVALID_ARG;
     }
     if (M == 0 || N == 0) return HGEMM_OK;
+    const int es = esize_of(dtype);
+    const uintptr_t amask = static_cast<uintptr_t>(es - 1);
     if (!C || (K > 0 && (!A || !B))) {
         t_last_error = "null pointer for a non-empty operand";
         return HGEMM_ERR_INVALID_ARG;
     }
-    if ((reinterpret_cast<uintptr_t>(C) & 1u) || (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 1u) ||
-                                                           (reinterpret_cast<uintptr_t>(B) & 1u)))) {
-        t_last_error = "operands must be 2-byte aligned";
+    if ((reinterpret_cast<uintptr_t>(C) & amask) ||
+        (K > 0 && ((reinterpret_cast<uintptr_t>(A) & amask) || (reinterpret_cast<uintptr_t>(B) & amask)))) {
+        t_last_error = "operands must be aligned to their element size";
         return HGEMM_ERR_INVALID_ARG;
     }
-    if (K > 0 && (overlaps(C, 2 * M * N, A, 2 * M * K) || overlaps(C, 2 * M * N, B, 2 * K * N))) {
+    if (K > 0 && (overlaps(C, es * M * N, A, es * M * K) || overlaps(C, es * M * N, B, es * K * N))) {
         t_last_error = "C overlaps A or B";
         return HGEMM_ERR_INVALID_ARG;
     }
@@ -435,33 +459,39 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
     DeviceInfo info;
     if ((st = device_info(&dev, &info)) != HGEMM_OK) return st;
     cudaError_t e;
+    const int es = esize_of(dtype);
+    const int64_t bk = bk_of(dtype);
     if (K == 0) {
-        if ((e = hg::launch_zero(static_cast<uint16_t*>(C), M * N, stream)) != cudaSuccess)
+        // zero bits are +0.0 in every dtype; the fill counts 16-bit words
+        if ((e = hg::launch_zero(static_cast<uint16_t*>(C), M * N * (es / 2), stream)) != cudaSuccess)
             return cuda_fail(e, "zero fill");
         return HGEMM_OK;
     }
 
     hgemm_plan_t pl;
-    const bool a_bad = misaligned16(A, K), b_bad = misaligned16(B, N), c_bad = misaligned16(C, N);
-    if ((st = make_plan(M, N, K, cfg, info.sms, a_bad, b_bad, c_bad, &pl)) != HGEMM_OK) return st;
+    const bool a_bad = misaligned16(A, K, es), b_bad = misaligned16(B, N, es), c_bad = misaligned16(C, N, es);
+    if ((st = make_plan(M, N, K, dtype, cfg, info.sms, a_bad, b_bad, c_bad, &pl)) != HGEMM_OK) return st;
 
     // Resident clusters bound the persistent grid; re-plan the schedule if
     // fewer fit than the planner assumed.
     const int cg = pl.cta_group, bn = pl.block_n, mc = pl.multicast;
-    const int64_t num_kb = cdiv(K, hg::kBlockK);
-    int resident = dtype == HGEMM_BF16 ? hg::max_active_clusters_bf16(cg, bn, mc)
-                                       : hg::max_active_clusters_f16(cg, bn, mc);
+    const int64_t num_kb = cdiv(K, bk);
+    int resident = dtype == HGEMM_BF16   ? hg::max_active_clusters_bf16(cg, bn, mc)
+                   : dtype == HGEMM_TF32 ? hg::max_active_clusters_tf32(cg, bn, mc)
+                                         : hg::max_active_clusters_f16(cg, bn, mc);
     if (resident > 0 && resident < pl.grid_ctas / (cg * mc)) {
         schedule_plan(&pl, resident, cfg ? cfg->stream_k : 0, num_kb);
-        pl.workspace_bytes = workspace_layout(pl, M, N, K).total;
+        pl.workspace_bytes = workspace_layout(pl, M, N, K, es).total;
     }
     const int clusters = pl.grid_ctas / (cg * mc);
 
     // Workspace: 16-byte-pitched copies of operands TMA cannot address, and
     // the fp32 partial sums of a K-split tail.
-    const WorkspaceLayout wl = workspace_layout(pl, M, N, K);
-    const int64_t lda = pl.repack_a ? (K + 7) / 8 * 8 : K;
-    const int64_t ldb = pl.repack_b ? (N + 7) / 8 * 8 : N;
+    const WorkspaceLayout wl = workspace_layout(pl, M, N, K, es);
+    const int64_t lda = pl.repack_a ? pitch16(K, es) : K;
+    // tf32: B always goes through the workspace, transposed to N x K
+    const bool b_t = dtype == HGEMM_TF32;
+    const int64_t ldb = b_t ? pitch16(K, es) : pl.repack_b ? pitch16(N, es) : N;
     void* work = nullptr;
     const void* a_use = A;
     const void* b_use = B;
@@ -485,16 +515,16 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
         }
         uint8_t* w8 = static_cast<uint8_t*>(work);
         if (pl.repack_a) {
-            if ((e = hg::launch_repack(static_cast<const uint16_t*>(A), M, K,
-                                       reinterpret_cast<uint16_t*>(w8 + wl.off_a), lda, stream)) != cudaSuccess) {
+            if ((e = hg::launch_repack(A, M, K, es, w8 + wl.off_a, lda, stream)) != cudaSuccess) {
                 if (work != scratch) cudaFreeAsync(work, stream);
                 return cuda_fail(e, "repack A");
             }
             a_use = w8 + wl.off_a;
         }
         if (pl.repack_b) {
-            if ((e = hg::launch_repack(static_cast<const uint16_t*>(B), K, N,
-                                       reinterpret_cast<uint16_t*>(w8 + wl.off_b), ldb, stream)) != cudaSuccess) {
+            if ((e = b_t ? hg::launch_transpose_f32(static_cast<const float*>(B), K, N,
+                                                    reinterpret_cast<float*>(w8 + wl.off_b), ldb, stream)
+                         : hg::launch_repack(B, K, N, es, w8 + wl.off_b, ldb, stream)) != cudaSuccess) {
                 if (work != scratch) cudaFreeAsync(work, stream);
                 return cuda_fail(e, "repack B");
             }
@@ -505,10 +535,14 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
     CUtensorMap ta, tb, tc, tc32;
     std::memset(&tc, 0, sizeof(tc));
     std::memset(&tc32, 0, sizeof(tc32));
-    if ((st = encode_2d(&ta, dtype, a_use, M, K, lda, hg::kBlockK, hg::kBlockMCta)) != HGEMM_OK ||
-        (st = encode_2d(&tb, dtype, b_use, K, N, ldb, 64, hg::kBlockK)) != HGEMM_OK ||
+    // A boxes: 128 rows x one 128-byte row of K; B boxes: bk k-rows x one
+    // 128-byte swizzle atom of columns; C boxes: 32 rows x 128 bytes.
+    const uint32_t ubk = static_cast<uint32_t>(bk);
+    if ((st = encode_2d(&ta, dtype, a_use, M, K, lda, ubk, hg::kBlockMCta)) != HGEMM_OK ||
+        (st = b_t ? encode_2d(&tb, dtype, b_use, N, K, ldb, ubk, static_cast<uint32_t>(bn / cg))
+                  : encode_2d(&tb, dtype, b_use, K, N, ldb, ubk, ubk)) != HGEMM_OK ||
         (pl.store_mode == 1 &&
-         (st = encode_2d(&tc, dtype, C, M, N, N, hg::kEpiBoxCols, hg::kEpiBoxRows)) != HGEMM_OK) ||
+         (st = encode_2d(&tc, dtype, C, M, N, N, static_cast<uint32_t>(128 / es), hg::kEpiBoxRows)) != HGEMM_OK) ||
         (pl.store_mode == 1 && bn % 64 != 0 &&
          (st = encode_2d(&tc32, dtype, C, M, N, N, 32, hg::kEpiBoxRows, CU_TENSOR_MAP_SWIZZLE_64B)) !=
              HGEMM_OK)) {
@@ -524,12 +558,14 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
     p.tiles_n = pl.tiles_n;
     p.num_tiles = pl.num_tiles;
     p.group_m = pl.group_m;
-    p.num_kb = static_cast<int32_t>(cdiv(K, hg::kBlockK));
-    const uint32_t fmt = dtype == HGEMM_BF16 ? 1u : 0u;
-    // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B format
-    // (bits 7-9, 10-12: 0 f16, 1 bf16), A K-major (bit 15 = 0), B MN-major
-    // (bit 16 = 1), N >> 3 (bits 17-22), M >> 4 (bits 24-28).
-    p.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | (0u << 15) | (1u << 16) |
+    p.num_kb = static_cast<int32_t>(cdiv(K, bk));
+    const uint32_t fmt = dtype == HGEMM_BF16 ? 1u : dtype == HGEMM_TF32 ? 2u : 0u;
+    // Instruction descriptor, kind::f16 / kind::tf32: D fp32 (bits 4-5 = 1),
+    // A and B format (bits 7-9, 10-12: 0 f16, 1 bf16, 2 tf32), A K-major
+    // (bit 15 = 0), B MN-major (bit 16 = 1), N >> 3 (bits 17-22), M >> 4
+    // (bits 24-28).
+    const uint32_t b_mn = b_t ? 0u : 1u;  // tf32: B K-major (transposed copy)
+    p.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | (0u << 15) | (b_mn << 16) |
               (static_cast<uint32_t>(bn >> 3) << 17) | (static_cast<uint32_t>((128 * cg) >> 4) << 24);
     p.store_mode = pl.store_mode;
     p.C = static_cast<uint16_t*>(C);
@@ -553,7 +589,8 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
         return cuda_fail(e, "status word");
     }
 
-    e = dtype == HGEMM_BF16 ? hg::launch_tc_bf16(cg, bn, mc, ta, tb, tc, tc32, p, clusters, stream)
+    e = dtype == HGEMM_BF16   ? hg::launch_tc_bf16(cg, bn, mc, ta, tb, tc, tc32, p, clusters, stream)
+        : dtype == HGEMM_TF32 ? hg::launch_tc_tf32(cg, bn, mc, ta, tb, tc, tc32, p, clusters, stream)
                             : hg::launch_tc_f16(cg, bn, mc, ta, tb, tc, tc32, p, clusters, stream);
     if (work && work != scratch) cudaFreeAsync(work, stream);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
@@ -601,14 +638,15 @@ hgemm_status_t hgemm_host(const void* hA, const void* hB, void* hC, int64_t M, i
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
+    const int64_t es = esize_of(dtype);
     if (K > 0) {
-        if ((e = cudaMemcpyAsync(dA, hA, static_cast<size_t>(2 * M * K), cudaMemcpyHostToDevice, s)) != cudaSuccess)
+        if ((e = cudaMemcpyAsync(dA, hA, static_cast<size_t>(es * M * K), cudaMemcpyHostToDevice, s)) != cudaSuccess)
             return cuda_fail(e, "copy A to device");
-        if ((e = cudaMemcpyAsync(dB, hB, static_cast<size_t>(2 * K * N), cudaMemcpyHostToDevice, s)) != cudaSuccess)
+        if ((e = cudaMemcpyAsync(dB, hB, static_cast<size_t>(es * K * N), cudaMemcpyHostToDevice, s)) != cudaSuccess)
             return cuda_fail(e, "copy B to device");
     }
     if ((st = run(dA, dB, dC, M, N, K, dtype, nullptr, s)) != HGEMM_OK) return st;
-    if ((e = cudaMemcpyAsync(hC, dC, static_cast<size_t>(2 * M * N), cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+    if ((e = cudaMemcpyAsync(hC, dC, static_cast<size_t>(es * M * N), cudaMemcpyDeviceToHost, s)) != cudaSuccess)
         return cuda_fail(e, "copy C to host");
     if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "stream synchronize");
     return HGEMM_OK;
@@ -619,7 +657,7 @@ hgemm_status_t hgemm_plan(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dtype,
     t_last_error.clear();
     if (!out) return HGEMM_ERR_INVALID_ARG;
     if (M < 0 || N < 0 || K < 0 || M > 2147483647LL || N > 2147483647LL || K > 2147483647LL ||
-        (dtype != HGEMM_F16 && dtype != HGEMM_BF16))
+        !valid_dtype(dtype))
         return HGEMM_ERR_INVALID_ARG;
     int sms = sm_count;
     if (sms <= 0) {
@@ -629,8 +667,9 @@ hgemm_status_t hgemm_plan(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dtype,
         if (st != HGEMM_OK) return st;
         sms = info.sms;
     }
-    const bool a_bad = ((K * 2) & 15) != 0, b_bad = ((N * 2) & 15) != 0, c_bad = ((N * 2) & 15) != 0;
-    return make_plan(M, N, K, cfg, sms, a_bad, b_bad, c_bad, out);
+    const int64_t es = esize_of(dtype);
+    const bool a_bad = ((K * es) & 15) != 0, b_bad = ((N * es) & 15) != 0, c_bad = ((N * es) & 15) != 0;
+    return make_plan(M, N, K, dtype, cfg, sms, a_bad, b_bad, c_bad, out);
 }
 
 int32_t hgemm_work_unit(const hgemm_plan_t* plan, int32_t cluster, int32_t i, int32_t* tile,

@@ -9,35 +9,74 @@ namespace hg {
 
 __device__ unsigned long long g_status_word;
 
-// Copy a rows x cols matrix of 16-bit values with row pitch `cols` (any base
-// alignment of 2 bytes) into `dst` with row pitch `dst_ld` (a multiple of 8
-// elements, 16-byte aligned base). Each thread moves 8 consecutive elements
-// of one row: 2-byte loads (the source rows are not 16-byte aligned), one
-// 16-byte store. Elements past `cols` in the destination row are not written.
-__global__ void repack_rows_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t cols,
-                                   uint16_t* __restrict__ dst, int64_t dst_ld) {
-    const int64_t chunks = (cols + 7) / 8;
+// Copy a rows x cols matrix of E-byte values (E = 2 or 4) with row pitch
+// `cols` (any base alignment of E bytes) into `dst` with row pitch `dst_ld`
+// (16-byte aligned base, dst_ld * E a multiple of 16). Each thread moves 16
+// bytes of one row: E-byte loads (the source rows are not 16-byte aligned),
+// one 16-byte store. Elements past `cols` in the destination row are not
+// written.
+template <typename T>
+__global__ void repack_rows_kernel(const T* __restrict__ src, int64_t rows, int64_t cols,
+                                   T* __restrict__ dst, int64_t dst_ld) {
+    constexpr int kPer = 16 / sizeof(T);
+    const int64_t chunks = (cols + kPer - 1) / kPer;
     for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
-        const uint16_t* s = src + r * cols;
-        uint16_t* d = dst + r * dst_ld;
+        const T* s = src + r * cols;
+        T* d = dst + r * dst_ld;
         for (int64_t ch = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; ch < chunks;
              ch += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-            const int64_t c0 = ch * 8;
-            if (c0 + 8 <= cols) {
-                uint16_t v[8];
+            const int64_t c0 = ch * kPer;
+            if (c0 + kPer <= cols) {
+                union {
+                    T v[kPer];
+                    uint4 u;
+                } packed;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) v[i] = s[c0 + i];
-                uint4 packed;
-                packed.x = v[0] | (static_cast<uint32_t>(v[1]) << 16);
-                packed.y = v[2] | (static_cast<uint32_t>(v[3]) << 16);
-                packed.z = v[4] | (static_cast<uint32_t>(v[5]) << 16);
-                packed.w = v[6] | (static_cast<uint32_t>(v[7]) << 16);
-                *reinterpret_cast<uint4*>(d + c0) = packed;
+                for (int i = 0; i < kPer; ++i) packed.v[i] = s[c0 + i];
+                *reinterpret_cast<uint4*>(d + c0) = packed.u;
             } else {
                 for (int64_t c = c0; c < cols; ++c) d[c] = s[c];
             }
         }
     }
+}
+
+// Bt (N x K, row pitch ldt) = transpose of B (K x N, row pitch N), fp32.
+// 32 x 32 tiles through shared memory (one padding column keeps the
+// column-wise reads conflict-free): reads along B's rows and writes along
+// Bt's rows are both coalesced. Grid: x over N tiles, y over K tiles.
+__global__ void transpose_f32_kernel(const float* __restrict__ B, int64_t K, int64_t N,
+                                     float* __restrict__ Bt, int64_t ldt) {
+    __shared__ float tile[32][33];
+    for (int64_t kt = blockIdx.y; kt * 32 < K; kt += gridDim.y) {
+        for (int64_t nt = blockIdx.x; nt * 32 < N; nt += gridDim.x) {
+            const int64_t n = nt * 32 + threadIdx.x;
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+                const int64_t k = kt * 32 + threadIdx.y + i;
+                tile[threadIdx.y + i][threadIdx.x] = (k < K && n < N) ? B[k * N + n] : 0.0f;
+            }
+            __syncthreads();
+            const int64_t k = kt * 32 + threadIdx.x;
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+                const int64_t nn = nt * 32 + threadIdx.y + i;
+                if (nn < N && k < K) Bt[nn * ldt + k] = tile[threadIdx.x][threadIdx.y + i];
+            }
+            __syncthreads();
+        }
+    }
+}
+
+cudaError_t launch_transpose_f32(const float* B, int64_t K, int64_t N, float* Bt, int64_t ldt,
+                                 cudaStream_t stream) {
+    if (K <= 0 || N <= 0) return cudaSuccess;
+    int64_t gx = (N + 31) / 32, gy = (K + 31) / 32;
+    if (gx > 65535) gx = 65535;
+    if (gy > 65535) gy = 65535;
+    transpose_f32_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), dim3(32, 8), 0, stream>>>(
+        B, K, N, Bt, ldt);
+    return cudaGetLastError();
 }
 
 __global__ void zero_kernel(uint16_t* __restrict__ dst, int64_t count) {
@@ -46,16 +85,22 @@ __global__ void zero_kernel(uint16_t* __restrict__ dst, int64_t count) {
         dst[i] = 0;
 }
 
-cudaError_t launch_repack(const uint16_t* src, int64_t rows, int64_t cols, uint16_t* dst,
+cudaError_t launch_repack(const void* src, int64_t rows, int64_t cols, int esize, void* dst,
                           int64_t dst_ld, cudaStream_t stream) {
     if (rows <= 0 || cols <= 0) return cudaSuccess;
-    const int64_t chunks = (cols + 7) / 8;
+    if (esize != 2 && esize != 4) return cudaErrorInvalidValue;
+    const int64_t chunks = (cols * esize + 15) / 16;
     const int threads = 128;
     int64_t gx = (chunks + threads - 1) / threads;
     if (gx > 1024) gx = 1024;
     int64_t gy = rows < 32768 ? rows : 32768;
-    repack_rows_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), threads, 0,
-                         stream>>>(src, rows, cols, dst, dst_ld);
+    const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
+    if (esize == 2)
+        repack_rows_kernel<uint16_t><<<grid, threads, 0, stream>>>(static_cast<const uint16_t*>(src), rows, cols,
+                                                                   static_cast<uint16_t*>(dst), dst_ld);
+    else
+        repack_rows_kernel<uint32_t><<<grid, threads, 0, stream>>>(static_cast<const uint32_t*>(src), rows, cols,
+                                                                   static_cast<uint32_t*>(dst), dst_ld);
     return cudaGetLastError();
 }
 

@@ -46,8 +46,12 @@
 namespace hg {
 
 constexpr int kBlockMCta = 128;   // C rows per CTA = TMEM lanes
-constexpr int kBlockK = 64;       // K per stage: 64 half-precision values = one 128 B swizzle row
+constexpr int kBlockK = 64;       // K per stage for 16-bit inputs: one 128 B swizzle row
 constexpr int kUmmaK = 16;        // K of one kind::f16 MMA
+// Input kinds: 0 = fp16, 1 = bf16 (kind::f16, C in the input type), 2 = tf32
+// (kind::tf32 on fp32 operands, C in fp32). A stage row is always 128 B of K.
+__host__ __device__ constexpr int elem_bytes(int dt) { return dt == 2 ? 4 : 2; }
+__host__ __device__ constexpr int block_k(int dt) { return 128 / elem_bytes(dt); }
 constexpr int kEpiWarps = 8;      // two per TMEM lane quarter, splitting the columns
 constexpr int kEpiQuarters = 4;   // TMEM lane quarters (32 rows each)
 constexpr int kProducerWarp = 8;   // first producer: even K blocks of the CTA's sequence
@@ -70,7 +74,7 @@ struct TcParams {
     int32_t store_mode;             // 1: TMA stores of C; 2: plain 2-byte stores through `C`;
                                     // 3: direct 16-byte stores through `C` (aligned C only);
                                     // 4: smem-staged, coalesced 16-byte stores (aligned C only)
-    uint16_t* C;                    // used by store_mode 2
+    uint16_t* C;                    // used by store modes 2-4 (fp32 elements for tf32)
     int64_t ldc;                    // elements between C rows (store_mode 2)
     uint64_t timeout_ns;
     unsigned long long* status;     // device status word
@@ -160,12 +164,15 @@ constexpr int pow2_at_least(int x) {
     return p;
 }
 
-template <int CG, int BN>
+template <int CG, int BN, int kElem = 2>
 struct TcCfg {
+    static constexpr int kBK = 128 / kElem;                // K per stage: one 128 B row of A
+    static constexpr int kUK = 32 / kElem;                 // K of one MMA (32 bytes of K)
+    static constexpr int kAtomCols = 128 / kElem;          // columns of one B swizzle atom
     static constexpr int kBnCta = BN / CG;                 // B columns each CTA feeds the MMA
-    static constexpr int kABytes = kBlockMCta * kBlockK * 2;
-    static constexpr int kBAtoms = (kBnCta + 63) / 64;     // 64-column swizzle atoms loaded
-    static constexpr int kBAtomBytes = kBlockK * 128;      // 64 columns x 64 k-rows
+    static constexpr int kABytes = kBlockMCta * 128;
+    static constexpr int kBAtoms = (kBnCta + kAtomCols - 1) / kAtomCols;  // B swizzle atoms loaded
+    static constexpr int kBAtomBytes = kBK * 128;          // kAtomCols columns x kBK k-rows
     static constexpr int kBBytes = kBAtoms * kBAtomBytes;
     static constexpr int kChunks = (BN + 63) / 64;         // epilogue chunks of 64 columns
     static constexpr bool kHalfLast = (BN % 64) != 0;      // the last chunk is 32 columns
@@ -211,9 +218,9 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
            (1ull << 46) | (2ull << 61);
 }
 
-template <bool kBF16>
+template <int kDt>
 __device__ __forceinline__ uint32_t pack_rn(uint32_t lo, uint32_t hi) {
-    if constexpr (kBF16) {
+    if constexpr (kDt == 1) {
         __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(lo), __uint_as_float(hi));
         return *reinterpret_cast<uint32_t*>(&v);
     } else {
@@ -296,13 +303,19 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
 // stacks two pairs along M; they need the same B columns, so each CTA loads
 // only one of its two 64-column B atoms and multicasts it to the matching CTA
 // of the other pair (a quarter less operand traffic through L2).
-template <int CG, int BN, bool kBF16, int MC>
+template <int CG, int BN, int kDt, int MC>
 __global__ void __launch_bounds__(kThreads, 1)
 hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC32,
                 const TcParams p) {
 #if defined(__CUDA_ARCH__) && defined(__CUDA_ARCH_FEAT_SM103_ALL)
-    using Cfg = TcCfg<CG, BN>;
+    using Cfg = TcCfg<CG, BN, elem_bytes(kDt)>;
+    static_assert(kDt != 2 || !Cfg::kHalfLast, "tf32 tiles are whole 64-column chunks");
+    // kind::tf32 takes both operands K-major (an MN-major tf32 operand
+    // multiplies as zero on this GPU): the host hands B over transposed, N x K,
+    // and one TMA box per stage brings the CTA's kBnCta rows of it.
+    constexpr bool kBKMajor = kDt == 2;
+    static_assert(!kBKMajor || (Cfg::kBnCta * 128 == Cfg::kBBytes && MC == 1), "K-major B box");
     constexpr int S = Cfg::kStages;
     constexpr int kCluster = CG * MC;
     static_assert(MC == 1 || (CG == 2 && MC == 2 && Cfg::kBAtoms == 2), "B multicast across pairs");
@@ -397,28 +410,34 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     const uint32_t a_dst = sA + stage * Cfg::kABytes;
                     const uint32_t b_dst = sB + stage * Cfg::kBBytes;
                     const uint32_t fb = bar_full + 8 * stage;
-                    const int32_t k0 = kb * kBlockK;
+                    const int32_t k0 = kb * Cfg::kBK;
                     if constexpr (CG == 1) {
                         mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
                         tma_load_2d(a_dst, &tmA, fb, k0, m0);
+                        if constexpr (kBKMajor) {
+                            tma_load_2d(b_dst, &tmB, fb, k0, n0);
+                        } else {
 #pragma unroll
-                        for (int j = 0; j < Cfg::kBAtoms; ++j)
-                            tma_load_2d(b_dst + j * Cfg::kBAtomBytes, &tmB, fb, n0 + 64 * j, k0);
+                            for (int j = 0; j < Cfg::kBAtoms; ++j)
+                                tma_load_2d(b_dst + j * Cfg::kBAtomBytes, &tmB, fb, n0 + Cfg::kAtomCols * j, k0);
+                        }
                     } else {
                         const uint32_t fb_leader = mapa_shared(fb, leader);
                         if (rank == 0) mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
                         tma_load_2d_pair(a_dst, &tmA, fb_leader, k0, m0);
-                        if constexpr (MC == 1) {
+                        if constexpr (kBKMajor) {
+                            tma_load_2d_pair(b_dst, &tmB, fb_leader, k0, n0);
+                        } else if constexpr (MC == 1) {
 #pragma unroll
                             for (int j = 0; j < Cfg::kBAtoms; ++j)
                                 tma_load_2d_pair(b_dst + j * Cfg::kBAtomBytes, &tmB, fb_leader,
-                                                 n0 + 64 * j, k0);
+                                                 n0 + Cfg::kAtomCols * j, k0);
                         } else {
                             // Atom `pair` of this B half, for this CTA and its
                             // counterpart in the other pair.
                             const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << (CG + rank)));
                             tma_load_2d_pair_mc(b_dst + pair * Cfg::kBAtomBytes, &tmB, fb_leader,
-                                                n0 + 64 * static_cast<int32_t>(pair), k0, mask);
+                                                n0 + Cfg::kAtomCols * static_cast<int32_t>(pair), k0, mask);
                         }
                     }
                     stage += 2;
@@ -448,7 +467,10 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             const long long t_span0 = clock64();
 #endif
             const uint64_t a_desc0 = sdesc_sw128(sA, 16u, 1024u);
-            const uint64_t b_desc0 = sdesc_sw128(sB, Cfg::kBAtomBytes, 1024u);
+            // MN-major B: atoms kBAtomBytes apart; K-major B (tf32): rows of
+            // 128 B like A.
+            const uint64_t b_desc0 = kBKMajor ? sdesc_sw128(sB, 16u, 1024u)
+                                              : sdesc_sw128(sB, Cfg::kBAtomBytes, 1024u);
             WorkUnit wu;
             for (int it = 0; next_unit(p.sched, cluster_id, it, wu); ++it) {
                 const uint32_t acc = static_cast<uint32_t>(it) & 1u;
@@ -485,13 +507,17 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     ++n_stages;
                     if (kb == wu.kb0) trace_stamp(p, it, kTrMmaFirst);
                     // Descriptor start addresses are in 16-byte units: stage s
-                    // adds s * stage bytes / 16; each K = 16 step moves 32 bytes
-                    // along A's swizzled rows and 16 rows (2 KiB) down B's atoms.
+                    // adds s * stage bytes / 16; each MMA step (32 bytes of K)
+                    // moves 32 bytes along A's swizzled rows and kUK rows of
+                    // 128 B down B's atoms.
                     const uint64_t ad = a_desc0 + ((stage * Cfg::kABytes) >> 4);
                     const uint64_t bd = b_desc0 + ((stage * Cfg::kBBytes) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < kBlockK / kUmmaK; ++kk) {
-                        umma_f16<CG>(d_tmem, ad + 2u * kk, bd + 128u * kk, p.idesc, accum);
+                    for (int kk = 0; kk < Cfg::kBK / Cfg::kUK; ++kk) {
+                        if constexpr (kDt == 2)
+                            umma_tf32<CG>(d_tmem, ad + 2u * kk, bd + 2u * kk, p.idesc, accum);
+                        else
+                            umma_f16<CG>(d_tmem, ad + 2u * kk, bd + 8u * Cfg::kUK * kk, p.idesc, accum);
                         accum = 1u;
                     }
                     issued = true;
@@ -782,11 +808,86 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         }
                     }
                 }
+                if constexpr (kDt == 2) {
+                    // fp32 C: the chunk goes out as two 32-column halves (r0, r1),
+                    // each a 32 x 32 fp32 box of 128-byte rows in the same
+                    // swizzle as the 16-bit boxes (16 B chunk j of row r at
+                    // j ^ (r % 8)).
+                    float* const Cf = reinterpret_cast<float*>(p.C);
+#pragma unroll 1
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t* v = h == 0 ? r0 : r1;
+                        const int32_t hcol = col0 + 64 * c + 32 * h;
+                        if (p.store_mode == 3) {
+                            // C 16-byte aligned, pitch and N multiples of 4 floats
+                            const int32_t row = row0 + static_cast<int32_t>(lane);
+                            if (row < p.M) {
+                                float* crow = Cf + static_cast<int64_t>(row) * p.ldc;
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) {
+                                    const int32_t col = hcol + 4 * j;
+                                    if (col < p.N)
+                                        *reinterpret_cast<uint4*>(crow + col) =
+                                            make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                                }
+                            }
+                            continue;
+                        }
+                        if (p.store_mode == 1) {
+                            if (lane == 0) bulk_wait_group_read<0>();
+                            __syncwarp();
+                        }
+                        const uint32_t row_addr = box + lane * 128u;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4),
+                                         v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                        if (p.store_mode == 1) {
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                if (row0 < p.M && hcol < p.N) tma_store_2d(&tmC, box, hcol, row0);
+                                bulk_commit_group();
+                            }
+                        } else if (p.store_mode == 4) {
+                            // read back row-contiguously: 8 lanes per 128-byte row
+                            __syncwarp();
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const uint32_t piece = static_cast<uint32_t>(i) * 32u + lane;
+                                const uint32_t rr = piece >> 3, ch = piece & 7u;
+                                const uint4 q4 = *reinterpret_cast<const uint4*>(
+                                    box_ptr + rr * 128u + ((ch ^ (rr & 7u)) << 4));
+                                const int32_t row = row0 + static_cast<int32_t>(rr);
+                                const int32_t col = hcol + static_cast<int32_t>(ch * 4u);
+                                if (row < p.M && col < p.N)
+                                    *reinterpret_cast<uint4*>(Cf + static_cast<int64_t>(row) * p.ldc + col) = q4;
+                            }
+                            __syncwarp();
+                        } else {
+                            // plain stores, any pitch: lane = column of the half
+                            __syncwarp();
+                            const int32_t col = hcol + static_cast<int32_t>(lane);
+#pragma unroll 1
+                            for (int rr = 0; rr < kEpiBoxRows; ++rr) {
+                                const int32_t row = row0 + rr;
+                                if (row >= p.M) break;
+                                const uint32_t urr = static_cast<uint32_t>(rr);
+                                if (col < p.N)
+                                    Cf[static_cast<int64_t>(row) * p.ldc + col] = *reinterpret_cast<const float*>(
+                                        box_ptr + urr * 128u + (((lane >> 2) ^ (urr & 7u)) << 4) + ((lane & 3u) << 2));
+                            }
+                            __syncwarp();
+                        }
+                    }
+                    if (is_split && owner && warp == 0 && lane == 0) trace_slot(p, 30, 3 + (c >> 1));
+                    continue;
+                } else {
                 uint32_t pk[32];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    pk[i] = pack_rn<kBF16>(r0[2 * i], r0[2 * i + 1]);
-                    pk[16 + i] = pack_rn<kBF16>(r1[2 * i], r1[2 * i + 1]);
+                    pk[i] = pack_rn<kDt>(r0[2 * i], r0[2 * i + 1]);
+                    pk[16 + i] = pack_rn<kDt>(r1[2 * i], r1[2 * i + 1]);
                 }
                 const int32_t ccol = col0 + 64 * c;
                 if (p.store_mode == 3) {
@@ -890,6 +991,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     }
                     __syncwarp();
                 }
+                }  // 16-bit output
             }
             if (warp == 0 && lane == 0) {
                 trace_stamp(p, it, kTrEpiEnd);

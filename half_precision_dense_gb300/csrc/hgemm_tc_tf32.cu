@@ -1,0 +1,18 @@
+// tf32 instantiations of the tcgen05 GEMM kernel (fp32 operands and C).
+#include "tc_instances.cuh"
+
+namespace hg {
+
+cudaError_t launch_tc_tf32(int cta_group, int block_n, int mc, const CUtensorMap& a, const CUtensorMap& b,
+                           const CUtensorMap& c, const CUtensorMap& c32, const TcParams& p, int clusters,
+                           cudaStream_t stream) {
+    HG_TC_DISPATCH_TF32(launch(a, b, c, c32, p, clusters, stream))
+    return cudaErrorInvalidValue;
+}
+
+int max_active_clusters_tf32(int cta_group, int block_n, int mc) {
+    HG_TC_DISPATCH_TF32(max_clusters())
+    return 0;
+}
+
+}  // namespace hg

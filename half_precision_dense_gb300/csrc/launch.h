@@ -22,21 +22,31 @@ cudaError_t launch_tc_bf16(int cta_group, int block_n, int mc, const CUtensorMap
 cudaError_t launch_tc_f16(int cta_group, int block_n, int mc, const CUtensorMap& a, const CUtensorMap& b,
                           const CUtensorMap& c, const CUtensorMap& c32, const TcParams& p,
                           int clusters, cudaStream_t stream);
+// tf32: fp32 A, B and C; (cta_group, block_n) in (1, 64|128|256), (2, 128|256); mc 1.
+cudaError_t launch_tc_tf32(int cta_group, int block_n, int mc, const CUtensorMap& a, const CUtensorMap& b,
+                           const CUtensorMap& c, const CUtensorMap& c32, const TcParams& p,
+                           int clusters, cudaStream_t stream);
 
 // Most CTA clusters of the (cta_group, block_n) kernel that can be resident at
 // once on the current device (0 on error).
 int max_active_clusters_bf16(int cta_group, int block_n, int mc);
 int max_active_clusters_f16(int cta_group, int block_n, int mc);
+int max_active_clusters_tf32(int cta_group, int block_n, int mc);
 
 // Shared-memory ring depth and bytes of an instantiation (host constants).
 int tc_stages(int cta_group, int block_n);
 int tc_smem_bytes(int cta_group, int block_n);
 int tc_tmem_cols(int cta_group, int block_n);
 
-// Auxiliary kernels (hgemm_aux.cu).
-cudaError_t launch_repack(const uint16_t* src, int64_t rows, int64_t cols, uint16_t* dst,
+// Auxiliary kernels (hgemm_aux.cu). The repack copies rows of `cols`
+// elements of `esize` (2 or 4) bytes from a dense source into rows `dst_ld`
+// elements apart (dst 16-byte aligned, dst_ld * esize a multiple of 16).
+cudaError_t launch_repack(const void* src, int64_t rows, int64_t cols, int esize, void* dst,
                           int64_t dst_ld, cudaStream_t stream);
 cudaError_t launch_zero(uint16_t* dst, int64_t count, cudaStream_t stream);
+// Bt (N x K, row pitch ldt floats) = B^T for fp32 B (K x N, dense).
+cudaError_t launch_transpose_f32(const float* B, int64_t K, int64_t N, float* Bt, int64_t ldt,
+                                 cudaStream_t stream);
 // Device address of the status word on the current device (cached per device).
 cudaError_t status_word_ptr(unsigned long long** out);
 

@@ -217,6 +217,26 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint6
     }
 }
 
+// D[tmem] (+)= A[smem desc] . B[smem desc], kind::tf32 (fp32 words in shared
+// memory, of which the tensor core multiplies the tf32 part; fp32 accumulator).
+template <int CG>
+__device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accum) {
+    if constexpr (CG == 1) {
+        asm volatile("{\n\t.reg .pred p;\n\t"
+                     "setp.ne.b32 p, %4, 0;\n\t"
+                     "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
+                     :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accum)
+                     : "memory");
+    } else {
+        asm volatile("{\n\t.reg .pred p;\n\t"
+                     "setp.ne.b32 p, %4, 0;\n\t"
+                     "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
+                     :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accum)
+                     : "memory");
+    }
+}
+
 // Arrive once on `bar` (this CTA) when all prior tcgen05 async operations of
 // the issuing thread have completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {

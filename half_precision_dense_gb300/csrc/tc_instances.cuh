@@ -9,11 +9,11 @@
 
 namespace hg {
 
-template <int CG, int BN, bool kBF16, int MC = 1>
+template <int CG, int BN, int kDt, int MC = 1>
 struct TcInstance {
     using Cfg = TcCfg<CG, BN>;
     static constexpr int kCluster = CG * MC;
-    static constexpr auto kernel() { return &hgemm_tc_kernel<CG, BN, kBF16, MC>; }
+    static constexpr auto kernel() { return &hgemm_tc_kernel<CG, BN, kDt, MC>; }
 
     // The dynamic shared-memory opt-in is per device; set it once per device.
     static cudaError_t prepare() {
@@ -79,13 +79,22 @@ struct TcInstance {
     }
 };
 
-#define HG_TC_DISPATCH(KBF16, CALL)                                                          \
-    if (mc == 1 && cta_group == 1 && block_n == 64) return TcInstance<1, 64, KBF16>::CALL;   \
-    if (mc == 1 && cta_group == 1 && block_n == 128) return TcInstance<1, 128, KBF16>::CALL; \
-    if (mc == 1 && cta_group == 1 && block_n == 256) return TcInstance<1, 256, KBF16>::CALL; \
-    if (mc == 1 && cta_group == 2 && block_n == 128) return TcInstance<2, 128, KBF16>::CALL; \
-    if (mc == 1 && cta_group == 2 && block_n == 224) return TcInstance<2, 224, KBF16>::CALL; \
-    if (mc == 1 && cta_group == 2 && block_n == 256) return TcInstance<2, 256, KBF16>::CALL; \
-    if (mc == 2 && cta_group == 2 && block_n == 256) return TcInstance<2, 256, KBF16, 2>::CALL;
+// Every tile shape of the 16-bit kinds (KDT 0 = fp16, 1 = bf16).
+#define HG_TC_DISPATCH(KDT, CALL)                                                          \
+    if (mc == 1 && cta_group == 1 && block_n == 64) return TcInstance<1, 64, KDT>::CALL;   \
+    if (mc == 1 && cta_group == 1 && block_n == 128) return TcInstance<1, 128, KDT>::CALL; \
+    if (mc == 1 && cta_group == 1 && block_n == 256) return TcInstance<1, 256, KDT>::CALL; \
+    if (mc == 1 && cta_group == 2 && block_n == 128) return TcInstance<2, 128, KDT>::CALL; \
+    if (mc == 1 && cta_group == 2 && block_n == 224) return TcInstance<2, 224, KDT>::CALL; \
+    if (mc == 1 && cta_group == 2 && block_n == 256) return TcInstance<2, 256, KDT>::CALL; \
+    if (mc == 2 && cta_group == 2 && block_n == 256) return TcInstance<2, 256, KDT, 2>::CALL;
+
+// The tf32 tile shapes: whole 64-column chunks, no B multicast.
+#define HG_TC_DISPATCH_TF32(CALL)                                                        \
+    if (mc == 1 && cta_group == 1 && block_n == 64) return TcInstance<1, 64, 2>::CALL;   \
+    if (mc == 1 && cta_group == 1 && block_n == 128) return TcInstance<1, 128, 2>::CALL; \
+    if (mc == 1 && cta_group == 1 && block_n == 256) return TcInstance<1, 256, 2>::CALL; \
+    if (mc == 1 && cta_group == 2 && block_n == 128) return TcInstance<2, 128, 2>::CALL; \
+    if (mc == 1 && cta_group == 2 && block_n == 256) return TcInstance<2, 256, 2>::CALL;
 
 }  // namespace hg

@@ -37,7 +37,7 @@ _GAMMA = np.uint64(0x9E3779B97F4A7C15)
 _MIX1 = np.uint64(0xBF58476D1CE4E5B9)
 _MIX2 = np.uint64(0x94D049BB133111EB)
 
-TORCH_DTYPES = {"bf16": torch.bfloat16, "f16": torch.float16}
+TORCH_DTYPES = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
 
 # Elements generated per chunk: bounds the temporaries to a few hundred MB.
 _CHUNK = 1 << 24
@@ -84,7 +84,8 @@ def _normal_f32(seed: int, tensor_id: int, start: int, count: int, sigma: float)
 
 def generate(shape, dtype: str, seed: int, tensor_id: int, dist: str = "uniform",
              sigma: float = 1.0) -> torch.Tensor:
-    """A contiguous CPU tensor of ``shape`` in ``dtype`` ("bf16" or "f16").
+    """A contiguous CPU tensor of ``shape`` in ``dtype`` ("bf16", "f16" or "f32";
+    the uniform draw k / 2^23 - 1 is exact in f32).
 
     Elements are numbered in row-major order; element ``e`` is the ``e``-th
     stream output, so a sub-block of a large matrix can be regenerated alone.

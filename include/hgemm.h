@@ -16,6 +16,13 @@
  * fp32 additions is unspecified, so results agree with an exact sum within the
  * rounding of fp32 accumulation, not bit for bit.
  *
+ * TF32 variant (dtype HGEMM_TF32; the series' earlier kernel multiplied tf32
+ * operands with the m16n8k8 tensor-core shape, same page, section 1): A, B
+ * and C are fp32 arrays with the same layouts. Each operand enters the
+ * product as its tf32 part - the sign, the 8 exponent bits and the top 10
+ * fraction bits, the low 13 fraction bits ignored - the products (exact in
+ * fp32) are accumulated in fp32, and C receives that fp32 accumulator.
+ *
  * Edge shapes ("CUDA GEMM 优化实践笔记", the register-tiled kernel's
  * bounds-checked tile loads fill out-of-range elements with zero): any M, N, K
  * >= 0 is accepted; elements outside the matrices contribute nothing and no
@@ -45,8 +52,9 @@ extern "C" {
 #endif
 
 typedef enum {
-    HGEMM_F16 = 0,  /* IEEE binary16 */
-    HGEMM_BF16 = 1  /* bfloat16 */
+    HGEMM_F16 = 0,  /* IEEE binary16 A, B and C */
+    HGEMM_BF16 = 1, /* bfloat16 A, B and C */
+    HGEMM_TF32 = 2  /* fp32 A, B and C, multiplied as tf32 (see above) */
 } hgemm_dtype_t;
 
 typedef enum {
@@ -65,10 +73,11 @@ typedef enum {
  *
  * A, B: device pointers to the operands (read only). C: device pointer to the
  * result (written). M, N, K: dimensions, each in [0, 2^31 - 1]. dtype:
- * HGEMM_F16 or HGEMM_BF16 (A, B and C share it).
+ * HGEMM_F16, HGEMM_BF16 or HGEMM_TF32 (A, B and C share the element type;
+ * pointers aligned to it).
  *
- * Workspace: operands whose row pitch (2K bytes for A, 2N bytes for B) or base
- * address is not a multiple of 16 bytes are first copied into a
+ * Workspace: operands whose row pitch (K or N elements) or base address is
+ * not a multiple of 16 bytes are first copied into a
  * 16-byte-pitched workspace (such a C is written with plain stores), and when
  * tiles are shared by stream-K ranges the parts' fp32 partial sums go through
  * the workspace too. It comes from a stream-ordered memory pool owned
@@ -189,7 +198,8 @@ typedef struct {
     int32_t smem_bytes;    /* dynamic shared memory per CTA */
     int32_t tmem_cols;     /* tensor-memory columns allocated per CTA */
     int32_t repack_a;      /* 1 if A goes through the 16-byte-pitch workspace */
-    int32_t repack_b;      /* 1 if B does */
+    int32_t repack_b;      /* 1 if B does (always for HGEMM_TF32: B is copied transposed,
+                              N x K, because kind::tf32 takes K-major operands) */
     int32_t store_mode;    /* 1 = TMA, 2 = plain, 3 = vector, 4 = staged vector stores */
     int32_t dp_tiles;      /* tiles computed whole, round-robin (the first dp_tiles in raster order) */
     int32_t sk_tiles;      /* tiles after them shared by stream-K ranges (0 = none) */

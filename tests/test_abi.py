@@ -259,3 +259,23 @@ def test_epilogue_staging_layout_is_conflict_free_and_tma_compatible():
             logical = l * 128 + j * 16
             tma = logical ^ (((logical >> 7) & 7) << 4)
             assert addr == tma
+
+
+def test_plan_tf32(lib):
+    # fp32 operands: 32 K values per 128-byte stage row, same tiles and ring
+    p = binding.plan(4096, 4096, 4096, "tf32", sm_count=152)
+    assert (p["cta_group"], p["block_n"], p["block_k"], p["num_kb"]) == (2, 256, 32, 128)
+    assert p["stages"] == binding.plan(4096, 4096, 4096, "bf16", binding.Config(2, 256), sm_count=152)["stages"]
+    # K = 1001 floats is not a 16-byte pitch: A is repacked; N = 1024 is
+    assert binding.plan(64, 1024, 1001, "tf32", sm_count=152)["repack_a"] == 1
+    # B always goes through the workspace, transposed (N x K, K padded to 4)
+    tp = binding.plan(64, 1024, 1001, "tf32", sm_count=152)
+    assert tp["repack_b"] == 1 and tp["workspace_bytes"] >= 4 * 1024 * 1004
+    assert binding.plan(64, 1024, 1000, "tf32", sm_count=152)["repack_a"] == 0
+    # no 224-wide tiles and no B multicast for tf32
+    for cfg in (binding.Config(cta_group=2, block_n=224), binding.Config(cta_group=2, block_n=256, multicast=2)):
+        with pytest.raises(binding.HgemmError):
+            binding.plan(1024, 1024, 1024, "tf32", cfg, sm_count=152)
+    # an unknown dtype code is refused by the library itself
+    out = binding._Plan()
+    assert lib.hgemm_plan(64, 64, 64, 3, None, 152, ctypes.byref(out)) == 1
