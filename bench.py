@@ -54,18 +54,27 @@ WORKLOADS = {
     "tails_bf16": [(1000, 4095, 4104, "bf16", "uniform", 1.0, 4)],
     "shortk_bf16": [(4096, 4096, 64, "bf16", "uniform", 1.0, 4)],
     "square256_bf16": [(256, 256, 256, "bf16", "uniform", 1.0, 0)],
+    # the TF32 variant: fp32 A, B, C ("f32" inputs multiplied as tf32)
+    "tf32_4096": [(4096, 4096, 4096, "f32", "uniform", 1.0, 1)],
 }
 DESCRIPTIONS = {
     "square4096": "GEMM M=N=K=4096, once bf16 and once fp16, A/B row-major, U[-1,1) seed 1",
+    "tf32_4096": "TF32 GEMM M=N=K=4096, fp32 A/B/C row-major, U[-1,1) seed 1",
 }
+METRICS = {
+    "tf32_4096": "TF32 GEMM TFLOP/s at M=N=K=4096 (fp32 in and out); % of GB300 dense tf32 tensor-core peak",
+}
+# Nominal dense tensor rates relative to bf16 (2.25 PFLOP/s): tf32 1.1 PFLOP/s.
+NOMINAL_RATIO = {"bf16": 1.0, "f16": 1.0, "f32": 1.1 / 2.25}
+ESIZE = {"bf16": 2, "f16": 2, "f32": 4}
 
 
 def flops(M, N, K):
     return 2 * M * N * K
 
 
-def hbm_bytes(M, N, K):
-    return 2 * (M * K + K * N + M * N)
+def hbm_bytes(M, N, K, esize=2):
+    return esize * (M * K + K * N + M * N)
 
 
 def read_peaks():
@@ -246,13 +255,18 @@ def run_ours(args, rank, world, local_rank):
     value = job_throughput(world, args.steps, step_flops, total_ms)
     avg_launch_ms = total_ms / n_ev
     achieved = step_flops / len(ops) / (avg_launch_ms * 1e-3) / 1e12
-    peak = float(peaks["bf16_tflops"])
+    dts = {o["dt"] for o in ops}
+    ratio = min(NOMINAL_RATIO[d] for d in dts)
+    peak = round(float(peaks["bf16_tflops"]) * ratio, 1)
+    peak_desc = (f"{peak_src} bf16 dense (cuBLAS burst); fp16 has the same nominal rate (ratio 1)"
+                 if ratio == 1.0 else
+                 f"{peak_src} bf16 dense (cuBLAS burst) x nominal tf32/bf16 ratio 1.1/2.25")
     clocks = clk.summary()
     e2e_value = job_throughput(world, e2e_steps, step_flops, e2e_s * 1e3)
-    h2d = sum(2 * (o["M"] * o["K"] + o["K"] * o["N"]) for o in ops)
-    d2h = sum(2 * o["M"] * o["N"] for o in ops)
+    h2d = sum(ESIZE[o["dt"]] * (o["M"] * o["K"] + o["K"] * o["N"]) for o in ops)
+    d2h = sum(ESIZE[o["dt"]] * o["M"] * o["N"] for o in ops)
     line = {
-        "metric": METRIC,
+        "metric": METRICS.get(args.workload, METRIC),
         "value": round(value, 2),
         "unit": UNIT,
         "n_gpus": world,
@@ -262,7 +276,8 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "+".join(sorted({o["dt"] for o in ops})) + " in, f32 accumulate",
+        "dtype": ("f32 in (multiplied as tf32), f32 accumulate and out" if dts == {"f32"} else
+                  "+".join(sorted(dts)) + " in, f32 accumulate"),
         "data": "synthetic (seeded SplitMix64 inputs)",
         "config": {
             "workload": DESCRIPTIONS.get(args.workload, args.workload),
@@ -278,11 +293,11 @@ def run_ours(args, rank, world, local_rank):
             "kernel": "hg::hgemm_tc_kernel",
             "achieved": round(achieved, 1),
             "peak": peak,
-            "peak_source": f"{peak_src} bf16 dense (cuBLAS burst); fp16 has the same nominal rate (ratio 1)",
+            "peak_source": peak_desc,
             "unit": "TFLOP/s",
             "frac": round(achieved / peak, 4),
             "traffic": None,
-            "algorithmic_bytes_per_launch": hbm_bytes(ops[0]["M"], ops[0]["N"], ops[0]["K"]),
+            "algorithmic_bytes_per_launch": hbm_bytes(ops[0]["M"], ops[0]["N"], ops[0]["K"], ESIZE[ops[0]["dt"]]),
         },
         "clocks": clocks,
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -302,7 +317,8 @@ def run_ours(args, rank, world, local_rank):
         try:
             with open(args.traffic_file) as f:
                 tr = json.load(f)
-            if tr.get("plan") == plan_key and tr.get("kernel_rev") == KERNEL_REV:
+            if (tr.get("plan") == plan_key and tr.get("kernel_rev") == KERNEL_REV and
+                    tr.get("dtype", "bf16") in {o["dt"] for o in ops}):
                 line["roofline"]["traffic"] = tr.get("dram_bytes_per_launch")
                 line["roofline"]["traffic_source"] = tr.get("source")
             else:
@@ -325,8 +341,9 @@ def _oracle_sample(workload, rows, cols):
 
     out = []
     for (M, N, K, dt, dist, sigma, seed) in WORKLOADS[workload]:
-        A = inputs.bits(inputs.generate((M, K), dt, seed, 0, dist, sigma))
-        B = inputs.bits(inputs.generate((K, N), dt, seed, 1, dist, sigma))
+        conv = (lambda t: t.numpy()) if dt == "f32" else inputs.bits
+        A = conv(inputs.generate((M, K), dt, seed, 0, dist, sigma))
+        B = conv(inputs.generate((K, N), dt, seed, 1, dist, sigma))
         ri = np.linspace(0, M - 1, min(rows, M)).astype(np.int64)
         ci = np.linspace(0, N - 1, min(cols, N)).astype(np.int64)
         out.append((np.ascontiguousarray(A[ri]), np.ascontiguousarray(B[:, ci]), dt, K))
@@ -335,10 +352,14 @@ def _oracle_sample(workload, rows, cols):
 
 def _oracle_step(sample):
     import oracle
+    from oracle import tf32_oracle
 
     f = 0
     for (a, b, dt, K) in sample:
-        oracle.gemm(a, b, dt)
+        if dt == "f32":
+            tf32_oracle.gemm(a, b)
+        else:
+            oracle.gemm(a, b, dt)
         f += flops(a.shape[0], b.shape[1], K)
     return f
 
@@ -359,8 +380,10 @@ def _calibrated_sample(workload, seconds_per_step):
 
 
 def _sample_desc(side, workload):
+    how = ("numpy fp64 product of the tf32-truncated operands, rounded to fp32"
+           if all(g[3] == "f32" for g in WORKLOADS[workload]) else "numpy fp64 product + bit-level RNE")
     return (f"each step: the {side} x {side} block of C at evenly spaced rows and columns of every "
-            f"GEMM of {workload}, computed by the CPU oracle (numpy fp64 product + bit-level RNE)")
+            f"GEMM of {workload}, computed by the CPU oracle ({how})")
 
 
 def cpu_baseline(workload, budget_s=15.0):
@@ -392,7 +415,7 @@ def run_reference(args, rank, world):
     desc = _sample_desc(side, args.workload)
     return {
         "impl": "reference",
-        "metric": METRIC,
+        "metric": METRICS.get(args.workload, METRIC),
         "value": round(value, 6),
         "unit": UNIT,
         "n_gpus": world,
