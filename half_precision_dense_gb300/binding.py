@@ -20,6 +20,8 @@ _lock = threading.Lock()
 HGEMM_F16 = 0
 HGEMM_BF16 = 1
 HGEMM_TF32 = 2
+HGEMM_E4M3 = 3
+HGEMM_E5M2 = 4
 STATUS_NAMES = {0: "HGEMM_OK", 1: "HGEMM_ERR_INVALID_ARG", 2: "HGEMM_ERR_UNSUPPORTED_DEVICE",
                 3: "HGEMM_ERR_CUDA", 4: "HGEMM_ERR_ALLOC", 5: "HGEMM_ERR_TIMEOUT"}
 
@@ -83,6 +85,11 @@ def load_library():
         lib.hgemm_ex.restype = ctypes.c_int
         lib.hgemm_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.c_int, vp]
         lib.hgemm_noalloc.restype = ctypes.c_int
+        lib.hgemm_fp8.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ctypes.c_int, vp]
+        lib.hgemm_fp8.restype = ctypes.c_int
+        lib.hgemm_fp8_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ctypes.c_int,
+                                     ctypes.POINTER(_Config), vp]
+        lib.hgemm_fp8_ex.restype = ctypes.c_int
         lib.hgemm_noalloc_scratch_bytes.argtypes = []
         lib.hgemm_noalloc_scratch_bytes.restype = ctypes.c_uint64
         lib.hgemm_host.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.c_int, vp, vp, vp, vp]
@@ -111,7 +118,7 @@ def load_library():
 
 
 def _dtype_code(dtype) -> int:
-    if dtype in (HGEMM_F16, HGEMM_BF16, HGEMM_TF32):
+    if dtype in (HGEMM_F16, HGEMM_BF16, HGEMM_TF32, HGEMM_E4M3, HGEMM_E5M2):
         return int(dtype)
     name = str(dtype)
     if name in ("bf16", "bfloat16", "torch.bfloat16"):
@@ -120,6 +127,10 @@ def _dtype_code(dtype) -> int:
         return HGEMM_F16
     if name in ("tf32", "f32", "fp32", "float32", "torch.float32"):
         return HGEMM_TF32
+    if name in ("e4m3", "fp8_e4m3", "torch.float8_e4m3fn"):
+        return HGEMM_E4M3
+    if name in ("e5m2", "fp8_e5m2", "torch.float8_e5m2"):
+        return HGEMM_E5M2
     raise ValueError(f"unsupported dtype {dtype!r}")
 
 
@@ -163,6 +174,20 @@ def hgemm_ex(A, B, C, M: int, N: int, K: int, dtype, config: Config | None = Non
     lib = load_library()
     cfg = ctypes.byref(config._c()) if config is not None else None
     _check(lib.hgemm_ex(_ptr(A), _ptr(B), _ptr(C), M, N, K, _dtype_code(dtype), cfg, _stream(stream)))
+
+
+def hgemm_fp8(A, B, C, a_scale, b_scale, M: int, N: int, K: int, dtype, config: Config | None = None,
+              stream=None) -> None:
+    """C (bf16) = a_scale[i] * b_scale[j] * sum_k A[i,k] B[k,j] for 8-bit E4M3 / E5M2
+    operands (device pointers or CUDA tensors; scales fp32 arrays or None)."""
+    lib = load_library()
+    code = _dtype_code(dtype)
+    if config is None:
+        _check(lib.hgemm_fp8(_ptr(A), _ptr(B), _ptr(C), _ptr(a_scale), _ptr(b_scale), M, N, K, code,
+                             _stream(stream)))
+    else:
+        _check(lib.hgemm_fp8_ex(_ptr(A), _ptr(B), _ptr(C), _ptr(a_scale), _ptr(b_scale), M, N, K, code,
+                                ctypes.byref(config._c()), _stream(stream)))
 
 
 def hgemm_host(hA, hB, hC, M: int, N: int, K: int, dtype, dA, dB, dC, stream=None) -> None:

@@ -61,8 +61,16 @@ hgemm_status_t device_info(int* dev_out, DeviceInfo* out) {
 }
 
 // Element bytes and K per pipeline stage (one 128-byte row of A) of a dtype.
-bool valid_dtype(int dt) { return dt == HGEMM_F16 || dt == HGEMM_BF16 || dt == HGEMM_TF32; }
-int esize_of(hgemm_dtype_t dt) { return dt == HGEMM_TF32 ? 4 : 2; }
+bool valid_dtype(int dt) {
+    return dt == HGEMM_F16 || dt == HGEMM_BF16 || dt == HGEMM_TF32 || dt == HGEMM_E4M3 || dt == HGEMM_E5M2;
+}
+bool is_fp8(hgemm_dtype_t dt) { return dt == HGEMM_E4M3 || dt == HGEMM_E5M2; }
+// operand bytes; C is fp32 for tf32, bf16 for fp8, else the operand type
+int esize_of(hgemm_dtype_t dt) { return dt == HGEMM_TF32 ? 4 : is_fp8(dt) ? 1 : 2; }
+hgemm_dtype_t c_dtype_of(hgemm_dtype_t dt) { return is_fp8(dt) ? HGEMM_BF16 : dt; }
+int c_esize_of(hgemm_dtype_t dt) { return esize_of(c_dtype_of(dt)); }
+// tf32 and fp8 B is transposed (N x K) into the workspace and read K-major
+bool b_transposed(hgemm_dtype_t dt) { return dt == HGEMM_TF32 || is_fp8(dt); }
 int64_t bk_of(hgemm_dtype_t dt) { return 128 / esize_of(dt); }
 
 // ------------------------------------------------- cuTensorMapEncodeTiled
@@ -102,6 +110,7 @@ hgemm_status_t encode_2d(CUtensorMap* m, hgemm_dtype_t dt, const void* base, int
     const cuuint32_t estr[2] = {1, 1};
     const CUtensorMapDataType type = dt == HGEMM_TF32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                      : dt == HGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                     : is_fp8(dt)       ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     CUresult r = fn(m, type,
                     2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -117,7 +126,7 @@ hgemm_status_t encode_2d(CUtensorMap* m, hgemm_dtype_t dt, const void* base, int
 // ----------------------------------------------------------------- planner
 bool valid_shape_config(int cg, int bn, hgemm_dtype_t dt) {
     return (cg == 1 && (bn == 64 || bn == 128 || bn == 256)) ||
-           (cg == 2 && (bn == 128 || (bn == 224 && dt != HGEMM_TF32) || bn == 256));
+           (cg == 2 && (bn == 128 || (bn == 224 && !b_transposed(dt)) || bn == 256));
 }
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -248,12 +257,12 @@ int64_t pitch16(int64_t cols, int esize) {
     return (cols + per - 1) / per * per;
 }
 
-// The B copy of a tf32 GEMM is B transposed (N x K, K padded to a 16-byte
-// pitch): kind::tf32 takes both operands K-major.
+// The B copy of a tf32 or fp8 GEMM is B transposed (N x K, K padded to a
+// 16-byte pitch): those operands are read K-major.
 WorkspaceLayout workspace_layout(const hgemm_plan_t& pl, int64_t M, int64_t N, int64_t K, int esize) {
     WorkspaceLayout w{};
     const int64_t lda = pitch16(K, esize), ldb = pitch16(N, esize);
-    const bool bt = esize == 4;
+    const bool bt = esize != 2;
     int64_t off = 0;
     w.off_a = off;
     off += pl.repack_a ? align256(esize * M * lda) : 0;
@@ -341,7 +350,7 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dt, cons
         return HGEMM_ERR_INVALID_ARG;
     }
     if (c.multicast < 0 || c.multicast > 2 ||
-        (c.multicast == 2 && !(cg == 2 && bn == 256 && dt != HGEMM_TF32))) {
+        (c.multicast == 2 && !(cg == 2 && bn == 256 && !b_transposed(dt)))) {
         t_last_error = "multicast = 2 needs cta_group 2, block_n 256 and a 16-bit dtype";
         return HGEMM_ERR_INVALID_ARG;
     }
@@ -351,8 +360,8 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dt, cons
     pl->block_m = 128 * cg * mc;
     pl->block_n = bn;
     pl->block_k = static_cast<int32_t>(bk_of(dt));
-    pl->stages = hg::tc_stages(cg, bn);
-    pl->smem_bytes = hg::tc_smem_bytes(cg, bn);
+    pl->stages = hg::tc_stages(cg, bn, esize_of(dt));
+    pl->smem_bytes = hg::tc_smem_bytes(cg, bn, esize_of(dt));
     pl->tmem_cols = hg::tc_tmem_cols(cg, bn);
     pl->tiles_m = static_cast<int32_t>(cdiv(M, pl->block_m));
     pl->tiles_n = static_cast<int32_t>(cdiv(N, bn));
@@ -362,7 +371,7 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dt, cons
     if (c.max_clusters > 0 && c.max_clusters < clusters) clusters = c.max_clusters;
     schedule_plan(pl, clusters, c.stream_k, cdiv(K, bk_of(dt)));
     pl->repack_a = a_unaligned ? 1 : 0;
-    pl->repack_b = (b_unaligned || dt == HGEMM_TF32) ? 1 : 0;
+    pl->repack_b = (b_unaligned || b_transposed(dt)) ? 1 : 0;
     pl->store_mode = (c.store_mode != 0) ? c.store_mode : (c_unaligned ? 2 : 1);
     if (c_unaligned && pl->store_mode != 2) {
         t_last_error = "vector and TMA stores need a 16-byte aligned C with a 16-byte row pitch";
@@ -429,18 +438,18 @@ hgemm_status_t check_args(const void* A, const void* B, void* C, int64_t M, int6
         return HGEMM_ERR_INVALID_ARG;
     }
     if (M == 0 || N == 0) return HGEMM_OK;
-    const int es = esize_of(dtype);
-    const uintptr_t amask = static_cast<uintptr_t>(es - 1);
+    const int es = esize_of(dtype), ces = c_esize_of(dtype);
+    const uintptr_t amask = static_cast<uintptr_t>(es - 1), cmask = static_cast<uintptr_t>(ces - 1);
     if (!C || (K > 0 && (!A || !B))) {
         t_last_error = "null pointer for a non-empty operand";
         return HGEMM_ERR_INVALID_ARG;
     }
-    if ((reinterpret_cast<uintptr_t>(C) & amask) ||
+    if ((reinterpret_cast<uintptr_t>(C) & cmask) ||
         (K > 0 && ((reinterpret_cast<uintptr_t>(A) & amask) || (reinterpret_cast<uintptr_t>(B) & amask)))) {
         t_last_error = "operands must be aligned to their element size";
         return HGEMM_ERR_INVALID_ARG;
     }
-    if (K > 0 && (overlaps(C, es * M * N, A, es * M * K) || overlaps(C, es * M * N, B, es * K * N))) {
+    if (K > 0 && (overlaps(C, ces * M * N, A, es * M * K) || overlaps(C, ces * M * N, B, es * K * N))) {
         t_last_error = "C overlaps A or B";
         return HGEMM_ERR_INVALID_ARG;
     }
@@ -449,9 +458,11 @@ hgemm_status_t check_args(const void* A, const void* B, void* C, int64_t M, int6
 
 // `scratch` (nullptr: none) is caller-provided device memory of `scratch_bytes`
 // used instead of the stream-ordered allocator for the repack workspace.
+// `a_scale` / `b_scale` (fp8 only; nullptr = 1) are the per-channel factors.
 hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
                    hgemm_dtype_t dtype, const hgemm_config_t* cfg, cudaStream_t stream,
-                   void* scratch = nullptr, size_t scratch_bytes = 0) {
+                   void* scratch = nullptr, size_t scratch_bytes = 0, const float* a_scale = nullptr,
+                   const float* b_scale = nullptr) {
     t_last_error.clear();
     hgemm_status_t st = check_args(A, B, C, M, N, K, dtype);
     if (st != HGEMM_OK || M == 0 || N == 0) return st;
@@ -459,17 +470,17 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
     DeviceInfo info;
     if ((st = device_info(&dev, &info)) != HGEMM_OK) return st;
     cudaError_t e;
-    const int es = esize_of(dtype);
+    const int es = esize_of(dtype), ces = c_esize_of(dtype);
     const int64_t bk = bk_of(dtype);
     if (K == 0) {
         // zero bits are +0.0 in every dtype; the fill counts 16-bit words
-        if ((e = hg::launch_zero(static_cast<uint16_t*>(C), M * N * (es / 2), stream)) != cudaSuccess)
+        if ((e = hg::launch_zero(static_cast<uint16_t*>(C), M * N * (ces / 2), stream)) != cudaSuccess)
             return cuda_fail(e, "zero fill");
         return HGEMM_OK;
     }
 
     hgemm_plan_t pl;
-    const bool a_bad = misaligned16(A, K, es), b_bad = misaligned16(B, N, es), c_bad = misaligned16(C, N, es);
+    const bool a_bad = misaligned16(A, K, es), b_bad = misaligned16(B, N, es), c_bad = misaligned16(C, N, ces);
     if ((st = make_plan(M, N, K, dtype, cfg, info.sms, a_bad, b_bad, c_bad, &pl)) != HGEMM_OK) return st;
 
     // Resident clusters bound the persistent grid; re-plan the schedule if
@@ -478,6 +489,7 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
     const int64_t num_kb = cdiv(K, bk);
     int resident = dtype == HGEMM_BF16   ? hg::max_active_clusters_bf16(cg, bn, mc)
                    : dtype == HGEMM_TF32 ? hg::max_active_clusters_tf32(cg, bn, mc)
+                   : is_fp8(dtype)       ? hg::max_active_clusters_fp8(static_cast<int>(dtype), cg, bn, mc)
                                          : hg::max_active_clusters_f16(cg, bn, mc);
     if (resident > 0 && resident < pl.grid_ctas / (cg * mc)) {
         schedule_plan(&pl, resident, cfg ? cfg->stream_k : 0, num_kb);
@@ -489,8 +501,8 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
     // the fp32 partial sums of a K-split tail.
     const WorkspaceLayout wl = workspace_layout(pl, M, N, K, es);
     const int64_t lda = pl.repack_a ? pitch16(K, es) : K;
-    // tf32: B always goes through the workspace, transposed to N x K
-    const bool b_t = dtype == HGEMM_TF32;
+    // tf32 and fp8: B always goes through the workspace, transposed to N x K
+    const bool b_t = b_transposed(dtype);
     const int64_t ldb = b_t ? pitch16(K, es) : pl.repack_b ? pitch16(N, es) : N;
     void* work = nullptr;
     const void* a_use = A;
@@ -522,8 +534,7 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
             a_use = w8 + wl.off_a;
         }
         if (pl.repack_b) {
-            if ((e = b_t ? hg::launch_transpose_f32(static_cast<const float*>(B), K, N,
-                                                    reinterpret_cast<float*>(w8 + wl.off_b), ldb, stream)
+            if ((e = b_t ? hg::launch_transpose(B, K, N, es, w8 + wl.off_b, ldb, stream)
                          : hg::launch_repack(B, K, N, es, w8 + wl.off_b, ldb, stream)) != cudaSuccess) {
                 if (work != scratch) cudaFreeAsync(work, stream);
                 return cuda_fail(e, "repack B");
@@ -542,9 +553,10 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
         (st = b_t ? encode_2d(&tb, dtype, b_use, N, K, ldb, ubk, static_cast<uint32_t>(bn / cg))
                   : encode_2d(&tb, dtype, b_use, K, N, ldb, ubk, ubk)) != HGEMM_OK ||
         (pl.store_mode == 1 &&
-         (st = encode_2d(&tc, dtype, C, M, N, N, static_cast<uint32_t>(128 / es), hg::kEpiBoxRows)) != HGEMM_OK) ||
+         (st = encode_2d(&tc, c_dtype_of(dtype), C, M, N, N, static_cast<uint32_t>(128 / ces), hg::kEpiBoxRows)) !=
+             HGEMM_OK) ||
         (pl.store_mode == 1 && bn % 64 != 0 &&
-         (st = encode_2d(&tc32, dtype, C, M, N, N, 32, hg::kEpiBoxRows, CU_TENSOR_MAP_SWIZZLE_64B)) !=
+         (st = encode_2d(&tc32, c_dtype_of(dtype), C, M, N, N, 32, hg::kEpiBoxRows, CU_TENSOR_MAP_SWIZZLE_64B)) !=
              HGEMM_OK)) {
         if (work && work != scratch) cudaFreeAsync(work, stream);
         return st;
@@ -559,16 +571,23 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
     p.num_tiles = pl.num_tiles;
     p.group_m = pl.group_m;
     p.num_kb = static_cast<int32_t>(cdiv(K, bk));
-    const uint32_t fmt = dtype == HGEMM_BF16 ? 1u : dtype == HGEMM_TF32 ? 2u : 0u;
+    // operand format codes: kind::f16 0 f16, 1 bf16; kind::tf32 2; kind::f8f6f4
+    // 0 E4M3, 1 E5M2
+    const uint32_t fmt = dtype == HGEMM_BF16   ? 1u
+                         : dtype == HGEMM_TF32 ? 2u
+                         : dtype == HGEMM_E5M2 ? 1u
+                                               : 0u;
     // Instruction descriptor, kind::f16 / kind::tf32: D fp32 (bits 4-5 = 1),
     // A and B format (bits 7-9, 10-12: 0 f16, 1 bf16, 2 tf32), A K-major
     // (bit 15 = 0), B MN-major (bit 16 = 1), N >> 3 (bits 17-22), M >> 4
     // (bits 24-28).
-    const uint32_t b_mn = b_t ? 0u : 1u;  // tf32: B K-major (transposed copy)
+    const uint32_t b_mn = b_t ? 0u : 1u;  // tf32, fp8: B K-major (transposed copy)
     p.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | (0u << 15) | (b_mn << 16) |
               (static_cast<uint32_t>(bn >> 3) << 17) | (static_cast<uint32_t>((128 * cg) >> 4) << 24);
     p.store_mode = pl.store_mode;
     p.C = static_cast<uint16_t*>(C);
+    p.a_scale = a_scale;
+    p.b_scale = b_scale;
     p.ldc = N;
     p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
     p.sched.num_tiles = pl.num_tiles;
@@ -591,6 +610,8 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
 
     e = dtype == HGEMM_BF16   ? hg::launch_tc_bf16(cg, bn, mc, ta, tb, tc, tc32, p, clusters, stream)
         : dtype == HGEMM_TF32 ? hg::launch_tc_tf32(cg, bn, mc, ta, tb, tc, tc32, p, clusters, stream)
+        : is_fp8(dtype)       ? hg::launch_tc_fp8(static_cast<int>(dtype), cg, bn, mc, ta, tb, tc, tc32, p, clusters,
+                                                  stream)
                             : hg::launch_tc_f16(cg, bn, mc, ta, tb, tc, tc32, p, clusters, stream);
     if (work && work != scratch) cudaFreeAsync(work, stream);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
@@ -625,6 +646,25 @@ hgemm_status_t hgemm_ex(const void* A, const void* B, void* C, int64_t M, int64_
     return run(A, B, C, M, N, K, dtype, cfg, static_cast<cudaStream_t>(stream));
 }
 
+hgemm_status_t hgemm_fp8(const void* A, const void* B, void* C, const float* a_scale, const float* b_scale,
+                         int64_t M, int64_t N, int64_t K, hgemm_dtype_t dtype, void* stream) {
+    if (!is_fp8(dtype)) {
+        t_last_error = "hgemm_fp8 takes HGEMM_E4M3 or HGEMM_E5M2";
+        return HGEMM_ERR_INVALID_ARG;
+    }
+    return run(A, B, C, M, N, K, dtype, nullptr, static_cast<cudaStream_t>(stream), nullptr, 0, a_scale, b_scale);
+}
+
+hgemm_status_t hgemm_fp8_ex(const void* A, const void* B, void* C, const float* a_scale, const float* b_scale,
+                            int64_t M, int64_t N, int64_t K, hgemm_dtype_t dtype, const hgemm_config_t* cfg,
+                            void* stream) {
+    if (!is_fp8(dtype)) {
+        t_last_error = "hgemm_fp8_ex takes HGEMM_E4M3 or HGEMM_E5M2";
+        return HGEMM_ERR_INVALID_ARG;
+    }
+    return run(A, B, C, M, N, K, dtype, cfg, static_cast<cudaStream_t>(stream), nullptr, 0, a_scale, b_scale);
+}
+
 hgemm_status_t hgemm_host(const void* hA, const void* hB, void* hC, int64_t M, int64_t N,
                           int64_t K, hgemm_dtype_t dtype, void* dA, void* dB, void* dC,
                           void* stream) {
@@ -638,7 +678,7 @@ hgemm_status_t hgemm_host(const void* hA, const void* hB, void* hC, int64_t M, i
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
-    const int64_t es = esize_of(dtype);
+    const int64_t es = esize_of(dtype), ces = c_esize_of(dtype);
     if (K > 0) {
         if ((e = cudaMemcpyAsync(dA, hA, static_cast<size_t>(es * M * K), cudaMemcpyHostToDevice, s)) != cudaSuccess)
             return cuda_fail(e, "copy A to device");
@@ -646,7 +686,7 @@ hgemm_status_t hgemm_host(const void* hA, const void* hB, void* hC, int64_t M, i
             return cuda_fail(e, "copy B to device");
     }
     if ((st = run(dA, dB, dC, M, N, K, dtype, nullptr, s)) != HGEMM_OK) return st;
-    if ((e = cudaMemcpyAsync(hC, dC, static_cast<size_t>(es * M * N), cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+    if ((e = cudaMemcpyAsync(hC, dC, static_cast<size_t>(ces * M * N), cudaMemcpyDeviceToHost, s)) != cudaSuccess)
         return cuda_fail(e, "copy C to host");
     if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "stream synchronize");
     return HGEMM_OK;
@@ -667,8 +707,8 @@ hgemm_status_t hgemm_plan(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dtype,
         if (st != HGEMM_OK) return st;
         sms = info.sms;
     }
-    const int64_t es = esize_of(dtype);
-    const bool a_bad = ((K * es) & 15) != 0, b_bad = ((N * es) & 15) != 0, c_bad = ((N * es) & 15) != 0;
+    const int64_t es = esize_of(dtype), ces = c_esize_of(dtype);
+    const bool a_bad = ((K * es) & 15) != 0, b_bad = ((N * es) & 15) != 0, c_bad = ((N * ces) & 15) != 0;
     return make_plan(M, N, K, dtype, cfg, sms, a_bad, b_bad, c_bad, out);
 }
 

@@ -9,7 +9,7 @@ namespace hg {
 
 __device__ unsigned long long g_status_word;
 
-// Copy a rows x cols matrix of E-byte values (E = 2 or 4) with row pitch
+// Copy a rows x cols matrix of E-byte values (E = 1, 2 or 4) with row pitch
 // `cols` (any base alignment of E bytes) into `dst` with row pitch `dst_ld`
 // (16-byte aligned base, dst_ld * E a multiple of 16). Each thread moves 16
 // bytes of one row: E-byte loads (the source rows are not 16-byte aligned),
@@ -41,20 +41,21 @@ __global__ void repack_rows_kernel(const T* __restrict__ src, int64_t rows, int6
     }
 }
 
-// Bt (N x K, row pitch ldt) = transpose of B (K x N, row pitch N), fp32.
-// 32 x 32 tiles through shared memory (one padding column keeps the
-// column-wise reads conflict-free): reads along B's rows and writes along
-// Bt's rows are both coalesced. Grid: x over N tiles, y over K tiles.
-__global__ void transpose_f32_kernel(const float* __restrict__ B, int64_t K, int64_t N,
-                                     float* __restrict__ Bt, int64_t ldt) {
-    __shared__ float tile[32][33];
+// Bt (N x K, row pitch ldt) = transpose of B (K x N, row pitch N), for fp32
+// or 8-bit elements. 32 x 32 tiles through shared memory (one padding
+// column keeps the column-wise reads conflict-free): reads along B's rows and
+// writes along Bt's rows are both coalesced. Grid: x over N tiles, y over K.
+template <typename T>
+__global__ void transpose_kernel(const T* __restrict__ B, int64_t K, int64_t N, T* __restrict__ Bt,
+                                 int64_t ldt) {
+    __shared__ T tile[32][33];
     for (int64_t kt = blockIdx.y; kt * 32 < K; kt += gridDim.y) {
         for (int64_t nt = blockIdx.x; nt * 32 < N; nt += gridDim.x) {
             const int64_t n = nt * 32 + threadIdx.x;
 #pragma unroll
             for (int i = 0; i < 32; i += 8) {
                 const int64_t k = kt * 32 + threadIdx.y + i;
-                tile[threadIdx.y + i][threadIdx.x] = (k < K && n < N) ? B[k * N + n] : 0.0f;
+                tile[threadIdx.y + i][threadIdx.x] = (k < K && n < N) ? B[k * N + n] : T(0);
             }
             __syncthreads();
             const int64_t k = kt * 32 + threadIdx.x;
@@ -68,14 +69,21 @@ __global__ void transpose_f32_kernel(const float* __restrict__ B, int64_t K, int
     }
 }
 
-cudaError_t launch_transpose_f32(const float* B, int64_t K, int64_t N, float* Bt, int64_t ldt,
-                                 cudaStream_t stream) {
+cudaError_t launch_transpose(const void* B, int64_t K, int64_t N, int esize, void* Bt, int64_t ldt,
+                             cudaStream_t stream) {
     if (K <= 0 || N <= 0) return cudaSuccess;
     int64_t gx = (N + 31) / 32, gy = (K + 31) / 32;
     if (gx > 65535) gx = 65535;
     if (gy > 65535) gy = 65535;
-    transpose_f32_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), dim3(32, 8), 0, stream>>>(
-        B, K, N, Bt, ldt);
+    const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), block(32, 8);
+    if (esize == 4)
+        transpose_kernel<float><<<grid, block, 0, stream>>>(static_cast<const float*>(B), K, N,
+                                                            static_cast<float*>(Bt), ldt);
+    else if (esize == 1)
+        transpose_kernel<uint8_t><<<grid, block, 0, stream>>>(static_cast<const uint8_t*>(B), K, N,
+                                                              static_cast<uint8_t*>(Bt), ldt);
+    else
+        return cudaErrorInvalidValue;
     return cudaGetLastError();
 }
 
@@ -88,14 +96,17 @@ __global__ void zero_kernel(uint16_t* __restrict__ dst, int64_t count) {
 cudaError_t launch_repack(const void* src, int64_t rows, int64_t cols, int esize, void* dst,
                           int64_t dst_ld, cudaStream_t stream) {
     if (rows <= 0 || cols <= 0) return cudaSuccess;
-    if (esize != 2 && esize != 4) return cudaErrorInvalidValue;
+    if (esize != 1 && esize != 2 && esize != 4) return cudaErrorInvalidValue;
     const int64_t chunks = (cols * esize + 15) / 16;
     const int threads = 128;
     int64_t gx = (chunks + threads - 1) / threads;
     if (gx > 1024) gx = 1024;
     int64_t gy = rows < 32768 ? rows : 32768;
     const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
-    if (esize == 2)
+    if (esize == 1)
+        repack_rows_kernel<uint8_t><<<grid, threads, 0, stream>>>(static_cast<const uint8_t*>(src), rows, cols,
+                                                                  static_cast<uint8_t*>(dst), dst_ld);
+    else if (esize == 2)
         repack_rows_kernel<uint16_t><<<grid, threads, 0, stream>>>(static_cast<const uint16_t*>(src), rows, cols,
                                                                    static_cast<uint16_t*>(dst), dst_ld);
     else
@@ -130,15 +141,26 @@ cudaError_t status_word_ptr(unsigned long long** out) {
     return cudaSuccess;
 }
 
-int tc_stages(int cta_group, int block_n) {
-    if (cta_group == 1 && block_n == 64) return TcCfg<1, 64>::kStages;
-    if (cta_group == 1 && block_n == 128) return TcCfg<1, 128>::kStages;
-    if (cta_group == 1 && block_n == 256) return TcCfg<1, 256>::kStages;
-    if (cta_group == 2 && block_n == 128) return TcCfg<2, 128>::kStages;
-    if (cta_group == 2 && block_n == 224) return TcCfg<2, 224>::kStages;
-    if (cta_group == 2 && block_n == 256) return TcCfg<2, 256>::kStages;
+// Stage counts and shared-memory bytes per (cta_group, block_n, operand
+// bytes): K-major B (tf32, fp8) of narrow tiles needs less of the ring.
+#define HG_CFG_SWITCH(FIELD)                                                                   \
+    if (esize == 2) {                                                                          \
+        if (cta_group == 1 && block_n == 64) return TcCfg<1, 64, 2>::FIELD;                    \
+        if (cta_group == 1 && block_n == 128) return TcCfg<1, 128, 2>::FIELD;                  \
+        if (cta_group == 1 && block_n == 256) return TcCfg<1, 256, 2>::FIELD;                  \
+        if (cta_group == 2 && block_n == 128) return TcCfg<2, 128, 2>::FIELD;                  \
+        if (cta_group == 2 && block_n == 224) return TcCfg<2, 224, 2>::FIELD;                  \
+        if (cta_group == 2 && block_n == 256) return TcCfg<2, 256, 2>::FIELD;                  \
+    } else if (esize == 4 || esize == 1) {                                                     \
+        if (cta_group == 1 && block_n == 64) return esize == 4 ? TcCfg<1, 64, 4>::FIELD : TcCfg<1, 64, 1>::FIELD;     \
+        if (cta_group == 1 && block_n == 128) return esize == 4 ? TcCfg<1, 128, 4>::FIELD : TcCfg<1, 128, 1>::FIELD;  \
+        if (cta_group == 1 && block_n == 256) return esize == 4 ? TcCfg<1, 256, 4>::FIELD : TcCfg<1, 256, 1>::FIELD;  \
+        if (cta_group == 2 && block_n == 128) return esize == 4 ? TcCfg<2, 128, 4>::FIELD : TcCfg<2, 128, 1>::FIELD;  \
+        if (cta_group == 2 && block_n == 256) return esize == 4 ? TcCfg<2, 256, 4>::FIELD : TcCfg<2, 256, 1>::FIELD;  \
+    }                                                                                          \
     return 0;
-}
+
+int tc_stages(int cta_group, int block_n, int esize) { HG_CFG_SWITCH(kStages) }
 
 int tc_tmem_cols(int cta_group, int block_n) {
     if (cta_group == 1 && block_n == 64) return TcCfg<1, 64>::kTmemCols;
@@ -150,14 +172,6 @@ int tc_tmem_cols(int cta_group, int block_n) {
     return 0;
 }
 
-int tc_smem_bytes(int cta_group, int block_n) {
-    if (cta_group == 1 && block_n == 64) return TcCfg<1, 64>::kSmemBytes;
-    if (cta_group == 1 && block_n == 128) return TcCfg<1, 128>::kSmemBytes;
-    if (cta_group == 1 && block_n == 256) return TcCfg<1, 256>::kSmemBytes;
-    if (cta_group == 2 && block_n == 128) return TcCfg<2, 128>::kSmemBytes;
-    if (cta_group == 2 && block_n == 224) return TcCfg<2, 224>::kSmemBytes;
-    if (cta_group == 2 && block_n == 256) return TcCfg<2, 256>::kSmemBytes;
-    return 0;
-}
+int tc_smem_bytes(int cta_group, int block_n, int esize) { HG_CFG_SWITCH(kSmemBytes) }
 
 }  // namespace hg

@@ -49,8 +49,10 @@ constexpr int kBlockMCta = 128;   // C rows per CTA = TMEM lanes
 constexpr int kBlockK = 64;       // K per stage for 16-bit inputs: one 128 B swizzle row
 constexpr int kUmmaK = 16;        // K of one kind::f16 MMA
 // Input kinds: 0 = fp16, 1 = bf16 (kind::f16, C in the input type), 2 = tf32
-// (kind::tf32 on fp32 operands, C in fp32). A stage row is always 128 B of K.
-__host__ __device__ constexpr int elem_bytes(int dt) { return dt == 2 ? 4 : 2; }
+// (kind::tf32 on fp32 operands, C in fp32), 3 = E4M3, 4 = E5M2 (kind::f8f6f4
+// on 8-bit operands, C in bf16 after the per-channel scales). A stage row is
+// always 128 B of K.
+__host__ __device__ constexpr int elem_bytes(int dt) { return dt == 2 ? 4 : dt >= 3 ? 1 : 2; }
 __host__ __device__ constexpr int block_k(int dt) { return 128 / elem_bytes(dt); }
 constexpr int kEpiWarps = 8;      // two per TMEM lane quarter, splitting the columns
 constexpr int kEpiQuarters = 4;   // TMEM lane quarters (32 rows each)
@@ -75,6 +77,8 @@ struct TcParams {
                                     // 3: direct 16-byte stores through `C` (aligned C only);
                                     // 4: smem-staged, coalesced 16-byte stores (aligned C only)
     uint16_t* C;                    // used by store modes 2-4 (fp32 elements for tf32)
+    const float* a_scale;           // fp8: one factor per row of A, or null (1)
+    const float* b_scale;           // fp8: one factor per column of B, or null (1)
     int64_t ldc;                    // elements between C rows (store_mode 2)
     uint64_t timeout_ns;
     unsigned long long* status;     // device status word
@@ -173,7 +177,10 @@ struct TcCfg {
     static constexpr int kABytes = kBlockMCta * 128;
     static constexpr int kBAtoms = (kBnCta + kAtomCols - 1) / kAtomCols;  // B swizzle atoms loaded
     static constexpr int kBAtomBytes = kBK * 128;          // kAtomCols columns x kBK k-rows
-    static constexpr int kBBytes = kBAtoms * kBAtomBytes;
+    // 16-bit B is read MN-major in swizzle atoms; tf32 and fp8 B come
+    // transposed (N x K) and are read K-major: kBnCta rows of 128 B.
+    static constexpr bool kBKMajor = kElem != 2;
+    static constexpr int kBBytes = kBKMajor ? kBnCta * 128 : kBAtoms * kBAtomBytes;
     static constexpr int kChunks = (BN + 63) / 64;         // epilogue chunks of 64 columns
     static constexpr bool kHalfLast = (BN % 64) != 0;      // the last chunk is 32 columns
     static constexpr int kStageBytes = kABytes + kBBytes;
@@ -220,7 +227,7 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
 
 template <int kDt>
 __device__ __forceinline__ uint32_t pack_rn(uint32_t lo, uint32_t hi) {
-    if constexpr (kDt == 1) {
+    if constexpr (kDt == 1 || kDt >= 3) {
         __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(lo), __uint_as_float(hi));
         return *reinterpret_cast<uint32_t*>(&v);
     } else {
@@ -310,11 +317,13 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 const TcParams p) {
 #if defined(__CUDA_ARCH__) && defined(__CUDA_ARCH_FEAT_SM103_ALL)
     using Cfg = TcCfg<CG, BN, elem_bytes(kDt)>;
-    static_assert(kDt != 2 || !Cfg::kHalfLast, "tf32 tiles are whole 64-column chunks");
+    static_assert(kDt < 2 || !Cfg::kHalfLast, "tf32 and fp8 tiles are whole 64-column chunks");
     // kind::tf32 takes both operands K-major (an MN-major tf32 operand
-    // multiplies as zero on this GPU): the host hands B over transposed, N x K,
-    // and one TMA box per stage brings the CTA's kBnCta rows of it.
-    constexpr bool kBKMajor = kDt == 2;
+    // multiplies as zero on this GPU), and so does this kernel's fp8 path:
+    // the host hands B over transposed, N x K, and one TMA box per stage
+    // brings the CTA's kBnCta rows of it.
+    constexpr bool kBKMajor = Cfg::kBKMajor;
+    static_assert(kBKMajor == (kDt >= 2), "K-major B for tf32 and fp8");
     static_assert(!kBKMajor || (Cfg::kBnCta * 128 == Cfg::kBBytes && MC == 1), "K-major B box");
     constexpr int S = Cfg::kStages;
     constexpr int kCluster = CG * MC;
@@ -516,6 +525,8 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     for (int kk = 0; kk < Cfg::kBK / Cfg::kUK; ++kk) {
                         if constexpr (kDt == 2)
                             umma_tf32<CG>(d_tmem, ad + 2u * kk, bd + 2u * kk, p.idesc, accum);
+                        else if constexpr (kDt >= 3)
+                            umma_f8<CG>(d_tmem, ad + 2u * kk, bd + 2u * kk, p.idesc, accum);
                         else
                             umma_f16<CG>(d_tmem, ad + 2u * kk, bd + 8u * Cfg::kUK * kk, p.idesc, accum);
                         accum = 1u;
@@ -883,6 +894,21 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     if (is_split && owner && warp == 0 && lane == 0) trace_slot(p, 30, 3 + (c >> 1));
                     continue;
                 } else {
+                if constexpr (kDt >= 3) {
+                    // fp8: C = bf16(acc * (a_scale[row] * b_scale[col])), the
+                    // per-channel scales applied in fp32 once the sum is done
+                    const int32_t srow = row0 + static_cast<int32_t>(lane);
+                    const float sa = (p.a_scale && srow < p.M) ? __ldg(p.a_scale + srow) : 1.0f;
+                    const int32_t scol = col0 + 64 * c;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int32_t c0i = scol + i, c1i = scol + 32 + i;
+                        const float sb0 = (p.b_scale && c0i < p.N) ? __ldg(p.b_scale + c0i) : 1.0f;
+                        const float sb1 = (p.b_scale && c1i < p.N) ? __ldg(p.b_scale + c1i) : 1.0f;
+                        r0[i] = __float_as_uint(__uint_as_float(r0[i]) * (sa * sb0));
+                        r1[i] = __float_as_uint(__uint_as_float(r1[i]) * (sa * sb1));
+                    }
+                }
                 uint32_t pk[32];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {

@@ -32,21 +32,29 @@ cudaError_t launch_tc_tf32(int cta_group, int block_n, int mc, const CUtensorMap
 int max_active_clusters_bf16(int cta_group, int block_n, int mc);
 int max_active_clusters_f16(int cta_group, int block_n, int mc);
 int max_active_clusters_tf32(int cta_group, int block_n, int mc);
+// fp8: kind 3 = E4M3, 4 = E5M2 operands (B transposed, N x K), bf16 C; the
+// tf32 tile shapes.
+cudaError_t launch_tc_fp8(int kind, int cta_group, int block_n, int mc, const CUtensorMap& a,
+                          const CUtensorMap& b, const CUtensorMap& c, const CUtensorMap& c32,
+                          const TcParams& p, int clusters, cudaStream_t stream);
+int max_active_clusters_fp8(int kind, int cta_group, int block_n, int mc);
 
-// Shared-memory ring depth and bytes of an instantiation (host constants).
-int tc_stages(int cta_group, int block_n);
-int tc_smem_bytes(int cta_group, int block_n);
+// Shared-memory ring depth and bytes of an instantiation (host constants) for
+// operands of `esize` bytes (2: fp16/bf16, 4: tf32, 1: fp8).
+int tc_stages(int cta_group, int block_n, int esize);
+int tc_smem_bytes(int cta_group, int block_n, int esize);
 int tc_tmem_cols(int cta_group, int block_n);
 
 // Auxiliary kernels (hgemm_aux.cu). The repack copies rows of `cols`
-// elements of `esize` (2 or 4) bytes from a dense source into rows `dst_ld`
+// elements of `esize` (1, 2 or 4) bytes from a dense source into rows `dst_ld`
 // elements apart (dst 16-byte aligned, dst_ld * esize a multiple of 16).
 cudaError_t launch_repack(const void* src, int64_t rows, int64_t cols, int esize, void* dst,
                           int64_t dst_ld, cudaStream_t stream);
 cudaError_t launch_zero(uint16_t* dst, int64_t count, cudaStream_t stream);
-// Bt (N x K, row pitch ldt floats) = B^T for fp32 B (K x N, dense).
-cudaError_t launch_transpose_f32(const float* B, int64_t K, int64_t N, float* Bt, int64_t ldt,
-                                 cudaStream_t stream);
+// Bt (N x K, row pitch ldt elements) = B^T for B (K x N, dense) of `esize`
+// (4: fp32, 1: fp8) bytes per element.
+cudaError_t launch_transpose(const void* B, int64_t K, int64_t N, int esize, void* Bt, int64_t ldt,
+                             cudaStream_t stream);
 // Device address of the status word on the current device (cached per device).
 cudaError_t status_word_ptr(unsigned long long** out);
 

@@ -237,6 +237,26 @@ __device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t a_desc, uint
     }
 }
 
+// D[tmem] (+)= A[smem desc] . B[smem desc], kind::f8f6f4 with 8-bit operands
+// (E4M3 or E5M2, K = 32 per instruction), fp32 accumulator.
+template <int CG>
+__device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accum) {
+    if constexpr (CG == 1) {
+        asm volatile("{\n\t.reg .pred p;\n\t"
+                     "setp.ne.b32 p, %4, 0;\n\t"
+                     "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+                     :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accum)
+                     : "memory");
+    } else {
+        asm volatile("{\n\t.reg .pred p;\n\t"
+                     "setp.ne.b32 p, %4, 0;\n\t"
+                     "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+                     :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accum)
+                     : "memory");
+    }
+}
+
 // Arrive once on `bar` (this CTA) when all prior tcgen05 async operations of
 // the issuing thread have completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {

@@ -89,12 +89,14 @@ struct TcInstance {
     if (mc == 1 && cta_group == 2 && block_n == 256) return TcInstance<2, 256, KDT>::CALL; \
     if (mc == 2 && cta_group == 2 && block_n == 256) return TcInstance<2, 256, KDT, 2>::CALL;
 
-// The tf32 tile shapes: whole 64-column chunks, no B multicast.
-#define HG_TC_DISPATCH_TF32(CALL)                                                        \
-    if (mc == 1 && cta_group == 1 && block_n == 64) return TcInstance<1, 64, 2>::CALL;   \
-    if (mc == 1 && cta_group == 1 && block_n == 128) return TcInstance<1, 128, 2>::CALL; \
-    if (mc == 1 && cta_group == 1 && block_n == 256) return TcInstance<1, 256, 2>::CALL; \
-    if (mc == 1 && cta_group == 2 && block_n == 128) return TcInstance<2, 128, 2>::CALL; \
-    if (mc == 1 && cta_group == 2 && block_n == 256) return TcInstance<2, 256, 2>::CALL;
+// The tf32 (KDT 2) and fp8 (KDT 3 = E4M3, 4 = E5M2) tile shapes: whole
+// 64-column chunks, no B multicast.
+#define HG_TC_DISPATCH_K(KDT, CALL)                                                        \
+    if (mc == 1 && cta_group == 1 && block_n == 64) return TcInstance<1, 64, KDT>::CALL;   \
+    if (mc == 1 && cta_group == 1 && block_n == 128) return TcInstance<1, 128, KDT>::CALL; \
+    if (mc == 1 && cta_group == 1 && block_n == 256) return TcInstance<1, 256, KDT>::CALL; \
+    if (mc == 1 && cta_group == 2 && block_n == 128) return TcInstance<2, 128, KDT>::CALL; \
+    if (mc == 1 && cta_group == 2 && block_n == 256) return TcInstance<2, 256, KDT>::CALL;
+#define HG_TC_DISPATCH_TF32(CALL) HG_TC_DISPATCH_K(2, CALL)
 
 }  // namespace hg

@@ -138,3 +138,21 @@ def workload_operands(name: str):
     A = generate((M, K), dtype, seed, 0, dist, sigma)
     B = generate((K, N), dtype, seed, 1, dist, sigma)
     return A, B, (M, N, K, dtype)
+
+
+FP8_TORCH = {"e4m3": "float8_e4m3fn", "e5m2": "float8_e5m2"}
+
+
+def generate_fp8(shape, fmt: str, seed: int, tensor_id: int, spread: float = 8.0):
+    """8-bit patterns (uint8 numpy array) of ``shape``: the uniform stream
+    scaled to [-spread, spread) and rounded to the fp8 format by PyTorch."""
+    rows, cols = int(shape[0]), int(shape[1])
+    f = _uniform_f32(seed, tensor_id, 0, rows * cols) * np.float32(spread)
+    t = torch.from_numpy(f).to(getattr(torch, FP8_TORCH[fmt]))
+    return t.view(torch.uint8).numpy().reshape(rows, cols)
+
+
+def generate_scales(n: int, seed: int, tensor_id: int, lo: float = 0.5, hi: float = 2.0) -> np.ndarray:
+    """``n`` fp32 factors uniform in [lo, hi) from the stream."""
+    u = (_uniform_f32(seed, tensor_id, 0, n) + np.float32(1.0)) * np.float32(0.5)   # [0, 1)
+    return (np.float32(lo) + u * np.float32(hi - lo)).astype(np.float32)

@@ -23,6 +23,17 @@
  * fraction bits, the low 13 fraction bits ignored - the products (exact in
  * fp32) are accumulated in fp32, and C receives that fp32 accumulator.
  *
+ * FP8 variant (dtypes HGEMM_E4M3 / HGEMM_E5M2; "深度学习加速核心：GEMM优化从分块到
+ * TensorCore的实战解析", sections 2.3 and 4.3: E4M3 and E5M2 operands used with
+ * per-layer or per-channel scale factors): A and B hold 8-bit OCP floats of
+ * one format (E4M3: bias 7, no infinities, S.1111.111 NaN; E5M2: bias 15,
+ * IEEE infinities and NaNs) in the same layouts; C is bfloat16:
+ *
+ *     C[i][j] = round_to_nearest_even_bf16( a_scale[i] * b_scale[j] * sum_k A[i][k] * B[k][j] )
+ *
+ * with the products (exact) accumulated in fp32 and the two fp32 scales
+ * applied to the fp32 sum (hgemm_fp8; hgemm() with an fp8 dtype uses 1).
+ *
  * Edge shapes ("CUDA GEMM 优化实践笔记", the register-tiled kernel's
  * bounds-checked tile loads fill out-of-range elements with zero): any M, N, K
  * >= 0 is accepted; elements outside the matrices contribute nothing and no
@@ -54,7 +65,9 @@ extern "C" {
 typedef enum {
     HGEMM_F16 = 0,  /* IEEE binary16 A, B and C */
     HGEMM_BF16 = 1, /* bfloat16 A, B and C */
-    HGEMM_TF32 = 2  /* fp32 A, B and C, multiplied as tf32 (see above) */
+    HGEMM_TF32 = 2, /* fp32 A, B and C, multiplied as tf32 (see above) */
+    HGEMM_E4M3 = 3, /* 8-bit E4M3 A and B, bfloat16 C (see hgemm_fp8) */
+    HGEMM_E5M2 = 4  /* 8-bit E5M2 A and B, bfloat16 C (see hgemm_fp8) */
 } hgemm_dtype_t;
 
 typedef enum {
@@ -166,6 +179,27 @@ typedef struct {
 /* hgemm with an explicit configuration (cfg may be NULL = all zero). */
 hgemm_status_t hgemm_ex(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
                         hgemm_dtype_t dtype, const hgemm_config_t* cfg, void* stream);
+
+/*
+ * hgemm_fp8 - the FP8 variant: C (bf16, M x N) = per-channel-scaled A.B.
+ *
+ * A (M x K) and B (K x N) are row-major 8-bit E4M3 or E5M2 patterns (dtype
+ * HGEMM_E4M3 or HGEMM_E5M2, both operands the same format), C row-major
+ * bfloat16. a_scale: device array of M fp32 factors, one per row of A;
+ * b_scale: device array of N fp32 factors, one per column of B; either may be
+ * NULL (all ones). Scale arrays are read only and need 4-byte alignment.
+ * B is first transposed (N x K) into the library's workspace, as for tf32;
+ * tiles are (1, 64 | 128 | 256) or (2, 128 | 256). Errors as for hgemm();
+ * a dtype other than HGEMM_E4M3 / HGEMM_E5M2 is HGEMM_ERR_INVALID_ARG.
+ */
+hgemm_status_t hgemm_fp8(const void* A, const void* B, void* C, const float* a_scale, const float* b_scale,
+                         int64_t M, int64_t N, int64_t K, hgemm_dtype_t dtype, void* stream);
+
+/* hgemm_fp8 with a forced launch configuration (see hgemm_config_t). */
+hgemm_status_t hgemm_fp8_ex(const void* A, const void* B, void* C, const float* a_scale, const float* b_scale,
+                            int64_t M, int64_t N, int64_t K, hgemm_dtype_t dtype, const hgemm_config_t* cfg,
+                            void* stream);
+
 
 /*
  * hgemm_host - the same product for operands in HOST memory.

@@ -278,4 +278,21 @@ def test_plan_tf32(lib):
             binding.plan(1024, 1024, 1024, "tf32", cfg, sm_count=152)
     # an unknown dtype code is refused by the library itself
     out = binding._Plan()
-    assert lib.hgemm_plan(64, 64, 64, 3, None, 152, ctypes.byref(out)) == 1
+    assert lib.hgemm_plan(64, 64, 64, 5, None, 152, ctypes.byref(out)) == 1
+
+
+def test_plan_fp8(lib):
+    # 8-bit operands: 128 K values per 128-byte stage row; B transposed
+    for code in (binding.HGEMM_E4M3, binding.HGEMM_E5M2):
+        p = binding.plan(4096, 4096, 4096, code, sm_count=152)
+        assert (p["cta_group"], p["block_n"], p["block_k"], p["num_kb"]) == (2, 256, 128, 32)
+        assert p["repack_b"] == 1 and p["workspace_bytes"] >= 4096 * 4096
+    # K = 1000 bytes is not a 16-byte pitch (A repacked); 1008 is
+    assert binding.plan(64, 1024, 1000, "e4m3", sm_count=152)["repack_a"] == 1
+    assert binding.plan(64, 1024, 1008, "e4m3", sm_count=152)["repack_a"] == 0
+    # C is bf16: N = 1004 gives a 2008-byte pitch, not a multiple of 16 -> plain stores
+    assert binding.plan(64, 1004, 1024, "e5m2", sm_count=152)["store_mode"] == 2
+    with pytest.raises(binding.HgemmError):
+        binding.plan(1024, 1024, 1024, "e4m3", binding.Config(cta_group=2, block_n=224), sm_count=152)
+    # the fp8 entry point refuses other dtypes
+    assert lib.hgemm_fp8(None, None, None, None, None, 0, 0, 0, 1, None) == 1
