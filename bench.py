@@ -56,17 +56,24 @@ WORKLOADS = {
     "square256_bf16": [(256, 256, 256, "bf16", "uniform", 1.0, 0)],
     # the TF32 variant: fp32 A, B, C ("f32" inputs multiplied as tf32)
     "tf32_4096": [(4096, 4096, 4096, "f32", "uniform", 1.0, 1)],
+    # the FP8 variant: E4M3 operands (uniform over [-8, 8) rounded to E4M3),
+    # per-channel scales uniform in [0.5, 2), bf16 C
+    "fp8_4096": [(4096, 4096, 4096, "e4m3", "uniform", 8.0, 1)],
 }
 DESCRIPTIONS = {
     "square4096": "GEMM M=N=K=4096, once bf16 and once fp16, A/B row-major, U[-1,1) seed 1",
     "tf32_4096": "TF32 GEMM M=N=K=4096, fp32 A/B/C row-major, U[-1,1) seed 1",
+    "fp8_4096": "FP8 GEMM M=N=K=4096, E4M3 A/B row-major (U[-8,8) rounded), per-channel scales, bf16 C, seed 1",
 }
 METRICS = {
     "tf32_4096": "TF32 GEMM TFLOP/s at M=N=K=4096 (fp32 in and out); % of GB300 dense tf32 tensor-core peak",
+    "fp8_4096": "FP8 (E4M3) GEMM TFLOP/s at M=N=K=4096 with per-channel scales; % of GB300 dense fp8 tensor-core peak",
 }
 # Nominal dense tensor rates relative to bf16 (2.25 PFLOP/s): tf32 1.1 PFLOP/s.
-NOMINAL_RATIO = {"bf16": 1.0, "f16": 1.0, "f32": 1.1 / 2.25}
-ESIZE = {"bf16": 2, "f16": 2, "f32": 4}
+NOMINAL_RATIO = {"bf16": 1.0, "f16": 1.0, "f32": 1.1 / 2.25, "e4m3": 4.5 / 2.25, "e5m2": 4.5 / 2.25}
+ESIZE = {"bf16": 2, "f16": 2, "f32": 4, "e4m3": 1, "e5m2": 1}
+C_ESIZE = {"bf16": 2, "f16": 2, "f32": 4, "e4m3": 2, "e5m2": 2}
+FP8 = ("e4m3", "e5m2")
 
 
 def flops(M, N, K):
@@ -177,15 +184,27 @@ def run_ours(args, rank, world, local_rank):
     gemms = WORKLOADS[args.workload]
     ops = []
     for (M, N, K, dt, dist, sigma, seed) in gemms:
-        A = inputs.generate((M, K), dt, seed, 0, dist, sigma)
-        B = inputs.generate((K, N), dt, seed, 1, dist, sigma)
-        ops.append(dict(M=M, N=N, K=K, dt=dt, hA=A, hB=B, A=A.to(dev), B=B.to(dev),
-                        C=torch.empty((M, N), dtype=inputs.TORCH_DTYPES[dt], device=dev)))
+        if dt in FP8:
+            A = torch.from_numpy(inputs.generate_fp8((M, K), dt, seed, 0, sigma))
+            B = torch.from_numpy(inputs.generate_fp8((K, N), dt, seed, 1, sigma))
+            sa = torch.from_numpy(inputs.generate_scales(M, seed, 2)).to(dev)
+            sb = torch.from_numpy(inputs.generate_scales(N, seed, 3)).to(dev)
+            cdt = torch.bfloat16
+        else:
+            A = inputs.generate((M, K), dt, seed, 0, dist, sigma)
+            B = inputs.generate((K, N), dt, seed, 1, dist, sigma)
+            sa = sb = None
+            cdt = inputs.TORCH_DTYPES[dt]
+        ops.append(dict(M=M, N=N, K=K, dt=dt, hA=A, hB=B, A=A.to(dev), B=B.to(dev), sa=sa, sb=sb,
+                        C=torch.empty((M, N), dtype=cdt, device=dev)))
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def one_gemm(o):
-        hg.hgemm(o["A"], o["B"], o["C"], o["M"], o["N"], o["K"], o["dt"], stream)
+        if o["dt"] in FP8:
+            hg.hgemm_fp8(o["A"], o["B"], o["C"], o["sa"], o["sb"], o["M"], o["N"], o["K"], o["dt"], None, stream)
+        else:
+            hg.hgemm(o["A"], o["B"], o["C"], o["M"], o["N"], o["K"], o["dt"], stream)
 
     for _ in range(args.warmup):
         for o in ops:
@@ -260,11 +279,12 @@ def run_ours(args, rank, world, local_rank):
     peak = round(float(peaks["bf16_tflops"]) * ratio, 1)
     peak_desc = (f"{peak_src} bf16 dense (cuBLAS burst); fp16 has the same nominal rate (ratio 1)"
                  if ratio == 1.0 else
+                 f"{peak_src} bf16 dense (cuBLAS burst) x nominal fp8/bf16 ratio 4.5/2.25" if ratio > 1.0 else
                  f"{peak_src} bf16 dense (cuBLAS burst) x nominal tf32/bf16 ratio 1.1/2.25")
     clocks = clk.summary()
     e2e_value = job_throughput(world, e2e_steps, step_flops, e2e_s * 1e3)
     h2d = sum(ESIZE[o["dt"]] * (o["M"] * o["K"] + o["K"] * o["N"]) for o in ops)
-    d2h = sum(ESIZE[o["dt"]] * o["M"] * o["N"] for o in ops)
+    d2h = sum(C_ESIZE[o["dt"]] * o["M"] * o["N"] for o in ops)
     line = {
         "metric": METRICS.get(args.workload, METRIC),
         "value": round(value, 2),
@@ -277,6 +297,7 @@ def run_ours(args, rank, world, local_rank):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": ("f32 in (multiplied as tf32), f32 accumulate and out" if dts == {"f32"} else
+                  "+".join(sorted(dts)) + " in, f32 accumulate, bf16 out" if dts <= set(FP8) else
                   "+".join(sorted(dts)) + " in, f32 accumulate"),
         "data": "synthetic (seeded SplitMix64 inputs)",
         "config": {
@@ -297,7 +318,8 @@ def run_ours(args, rank, world, local_rank):
             "unit": "TFLOP/s",
             "frac": round(achieved / peak, 4),
             "traffic": None,
-            "algorithmic_bytes_per_launch": hbm_bytes(ops[0]["M"], ops[0]["N"], ops[0]["K"], ESIZE[ops[0]["dt"]]),
+            "algorithmic_bytes_per_launch": (ESIZE[ops[0]["dt"]] * (ops[0]["M"] + ops[0]["N"]) * ops[0]["K"] +
+                                             C_ESIZE[ops[0]["dt"]] * ops[0]["M"] * ops[0]["N"]),
         },
         "clocks": clocks,
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -341,23 +363,31 @@ def _oracle_sample(workload, rows, cols):
 
     out = []
     for (M, N, K, dt, dist, sigma, seed) in WORKLOADS[workload]:
-        conv = (lambda t: t.numpy()) if dt == "f32" else inputs.bits
-        A = conv(inputs.generate((M, K), dt, seed, 0, dist, sigma))
-        B = conv(inputs.generate((K, N), dt, seed, 1, dist, sigma))
         ri = np.linspace(0, M - 1, min(rows, M)).astype(np.int64)
         ci = np.linspace(0, N - 1, min(cols, N)).astype(np.int64)
-        out.append((np.ascontiguousarray(A[ri]), np.ascontiguousarray(B[:, ci]), dt, K))
+        if dt in FP8:
+            A = inputs.generate_fp8((M, K), dt, seed, 0, sigma)
+            B = inputs.generate_fp8((K, N), dt, seed, 1, sigma)
+            scales = (inputs.generate_scales(M, seed, 2)[ri], inputs.generate_scales(N, seed, 3)[ci])
+        else:
+            conv = (lambda t: t.numpy()) if dt == "f32" else inputs.bits
+            A = conv(inputs.generate((M, K), dt, seed, 0, dist, sigma))
+            B = conv(inputs.generate((K, N), dt, seed, 1, dist, sigma))
+            scales = None
+        out.append((np.ascontiguousarray(A[ri]), np.ascontiguousarray(B[:, ci]), dt, K, scales))
     return out
 
 
 def _oracle_step(sample):
     import oracle
-    from oracle import tf32_oracle
+    from oracle import fp8_oracle, tf32_oracle
 
     f = 0
-    for (a, b, dt, K) in sample:
+    for (a, b, dt, K, scales) in sample:
         if dt == "f32":
             tf32_oracle.gemm(a, b)
+        elif dt in FP8:
+            fp8_oracle.gemm(a, b, dt, scales[0], scales[1])
         else:
             oracle.gemm(a, b, dt)
         f += flops(a.shape[0], b.shape[1], K)
@@ -380,8 +410,10 @@ def _calibrated_sample(workload, seconds_per_step):
 
 
 def _sample_desc(side, workload):
-    how = ("numpy fp64 product of the tf32-truncated operands, rounded to fp32"
-           if all(g[3] == "f32" for g in WORKLOADS[workload]) else "numpy fp64 product + bit-level RNE")
+    dts = {g[3] for g in WORKLOADS[workload]}
+    how = ("numpy fp64 product of the tf32-truncated operands, rounded to fp32" if dts == {"f32"} else
+           "fp8 decode, numpy fp64 product, per-channel scales, bit-level RNE to bf16" if dts <= set(FP8) else
+           "numpy fp64 product + bit-level RNE")
     return (f"each step: the {side} x {side} block of C at evenly spaced rows and columns of every "
             f"GEMM of {workload}, computed by the CPU oracle ({how})")
 

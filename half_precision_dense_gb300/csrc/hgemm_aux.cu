@@ -69,6 +69,50 @@ __global__ void transpose_kernel(const T* __restrict__ B, int64_t K, int64_t N, 
     }
 }
 
+// The 8-bit transpose in 64 x 64-byte tiles with 16-byte accesses: thread t
+// loads 16 bytes of B row (t / 4) (a vector load when the whole vector is in
+// range and aligned, bytes otherwise) and later writes 16 consecutive k-bytes
+// of Bt row (t / 4) gathered from the tile's column (Bt rows are 16-byte
+// aligned: ldt is a multiple of 16). 256 threads.
+__global__ void transpose_u8_kernel(const uint8_t* __restrict__ B, int64_t K, int64_t N,
+                                    uint8_t* __restrict__ Bt, int64_t ldt) {
+    __shared__ __align__(16) uint8_t tile[64][80];
+    const int t = threadIdx.x;
+    const int r = t >> 2, seg = (t & 3) * 16;
+    const bool b_vec = (N & 15) == 0 && (reinterpret_cast<uintptr_t>(B) & 15) == 0;
+    for (int64_t kt = blockIdx.y; kt * 64 < K; kt += gridDim.y) {
+        for (int64_t nt = blockIdx.x; nt * 64 < N; nt += gridDim.x) {
+            const int64_t k = kt * 64 + r, n0 = nt * 64 + seg;
+            if (k < K && b_vec && n0 + 16 <= N) {
+                *reinterpret_cast<uint4*>(&tile[r][seg]) = *reinterpret_cast<const uint4*>(B + k * N + n0);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    tile[r][seg + j] = (k < K && n0 + j < N) ? B[k * N + n0 + j] : uint8_t(0);
+            }
+            __syncthreads();
+            const int64_t n = nt * 64 + r, k0 = kt * 64 + seg;
+            if (n < N) {
+                uint8_t v[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] = tile[seg + j][r];
+                uint8_t* dst = Bt + n * ldt + k0;
+                if (k0 + 16 <= K) {
+                    uint4 w;
+                    w.x = v[0] | (v[1] << 8) | (v[2] << 16) | (static_cast<uint32_t>(v[3]) << 24);
+                    w.y = v[4] | (v[5] << 8) | (v[6] << 16) | (static_cast<uint32_t>(v[7]) << 24);
+                    w.z = v[8] | (v[9] << 8) | (v[10] << 16) | (static_cast<uint32_t>(v[11]) << 24);
+                    w.w = v[12] | (v[13] << 8) | (v[14] << 16) | (static_cast<uint32_t>(v[15]) << 24);
+                    *reinterpret_cast<uint4*>(dst) = w;
+                } else {
+                    for (int j = 0; j < 16 && k0 + j < K; ++j) dst[j] = v[j];
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
 cudaError_t launch_transpose(const void* B, int64_t K, int64_t N, int esize, void* Bt, int64_t ldt,
                              cudaStream_t stream) {
     if (K <= 0 || N <= 0) return cudaSuccess;
@@ -79,9 +123,14 @@ cudaError_t launch_transpose(const void* B, int64_t K, int64_t N, int esize, voi
     if (esize == 4)
         transpose_kernel<float><<<grid, block, 0, stream>>>(static_cast<const float*>(B), K, N,
                                                             static_cast<float*>(Bt), ldt);
-    else if (esize == 1)
-        transpose_kernel<uint8_t><<<grid, block, 0, stream>>>(static_cast<const uint8_t*>(B), K, N,
-                                                              static_cast<uint8_t*>(Bt), ldt);
+    else if (esize == 1) {
+        int64_t gx8 = (N + 63) / 64, gy8 = (K + 63) / 64;
+        if (gx8 > 65535) gx8 = 65535;
+        if (gy8 > 65535) gy8 = 65535;
+        if ((reinterpret_cast<uintptr_t>(Bt) & 15) != 0 || (ldt & 15) != 0) return cudaErrorInvalidValue;
+        transpose_u8_kernel<<<dim3(static_cast<unsigned>(gx8), static_cast<unsigned>(gy8)), 256, 0, stream>>>(
+            static_cast<const uint8_t*>(B), K, N, static_cast<uint8_t*>(Bt), ldt);
+    }
     else
         return cudaErrorInvalidValue;
     return cudaGetLastError();
