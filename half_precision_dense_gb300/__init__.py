@@ -11,7 +11,7 @@ library on first use and raises if it is missing.
 __version__ = "0.1.0"
 
 _BINDING_NAMES = {
-    "hgemm", "hgemm_ex", "hgemm_fp8", "hgemm_noalloc", "hgemm_host", "matmul", "status_string", "version",
+    "hgemm", "hgemm_ex", "hgemm_fp8", "hgemm_conv2d", "conv2d_nhwc", "hgemm_noalloc", "hgemm_host", "matmul", "status_string", "version",
     "get_device_status", "plan", "tile_coord", "HgemmError", "Config", "load_library",
     "set_timeout_ns",
 }

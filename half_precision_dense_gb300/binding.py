@@ -90,6 +90,8 @@ def load_library():
         lib.hgemm_fp8_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ctypes.c_int,
                                      ctypes.POINTER(_Config), vp]
         lib.hgemm_fp8_ex.restype = ctypes.c_int
+        lib.hgemm_conv2d.argtypes = [vp, vp, vp] + [i32] * 9 + [ctypes.c_int, vp]
+        lib.hgemm_conv2d.restype = ctypes.c_int
         lib.hgemm_noalloc_scratch_bytes.argtypes = []
         lib.hgemm_noalloc_scratch_bytes.restype = ctypes.c_uint64
         lib.hgemm_host.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.c_int, vp, vp, vp, vp]
@@ -188,6 +190,35 @@ def hgemm_fp8(A, B, C, a_scale, b_scale, M: int, N: int, K: int, dtype, config: 
     else:
         _check(lib.hgemm_fp8_ex(_ptr(A), _ptr(B), _ptr(C), _ptr(a_scale), _ptr(b_scale), M, N, K, code,
                                 ctypes.byref(config._c()), _stream(stream)))
+
+
+def hgemm_conv2d(x, w, y, N: int, H: int, W: int, C: int, K: int, R: int, S: int, stride: int, pad: int,
+                 dtype, stream=None) -> None:
+    """y (N x P x Q x K) = conv2d(x (N x H x W x C), w (R x S x C x K)) through im2col
+    and the GEMM (device pointers or CUDA tensors; see include/hgemm.h)."""
+    lib = load_library()
+    _check(lib.hgemm_conv2d(_ptr(x), _ptr(w), _ptr(y), N, H, W, C, K, R, S, stride, pad, _dtype_code(dtype),
+                            _stream(stream)))
+
+
+def conv2d_nhwc(x, w, stride: int = 1, pad: int = 0, stream=None):
+    """Channels-last convolution of CUDA tensors x (N, H, W, C) and w (R, S, C, K)
+    of dtype float16, bfloat16 or float32 (multiplied as tf32); returns y (N, P, Q, K)."""
+    import torch
+
+    if x.dim() != 4 or w.dim() != 4 or x.shape[3] != w.shape[2]:
+        raise ValueError(f"x {tuple(x.shape)} (N,H,W,C) and w {tuple(w.shape)} (R,S,C,K) do not match")
+    if x.dtype != w.dtype or not (x.is_cuda and w.is_cuda and x.is_contiguous() and w.is_contiguous()):
+        raise ValueError("x and w must be contiguous CUDA tensors of one dtype")
+    N, H, W, C = x.shape
+    R, S, _, K = w.shape
+    P = (H + 2 * pad - R) // stride + 1
+    Q = (W + 2 * pad - S) // stride + 1
+    y = torch.empty((N, max(P, 0), max(Q, 0), K), dtype=x.dtype, device=x.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device)
+    hgemm_conv2d(x, w, y, N, H, W, C, K, R, S, stride, pad, str(x.dtype), stream)
+    return y
 
 
 def hgemm_host(hA, hB, hC, M: int, N: int, K: int, dtype, dA, dB, dC, stream=None) -> None:

@@ -459,10 +459,12 @@ hgemm_status_t check_args(const void* A, const void* B, void* C, int64_t M, int6
 // `scratch` (nullptr: none) is caller-provided device memory of `scratch_bytes`
 // used instead of the stream-ordered allocator for the repack workspace.
 // `a_scale` / `b_scale` (fp8 only; nullptr = 1) are the per-channel factors.
+// `lda_in` > 0: A's rows are lda_in elements apart (a 16-byte pitch, 16-byte
+// aligned base: the library's own im2col matrix), so A needs no repack.
 hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
                    hgemm_dtype_t dtype, const hgemm_config_t* cfg, cudaStream_t stream,
                    void* scratch = nullptr, size_t scratch_bytes = 0, const float* a_scale = nullptr,
-                   const float* b_scale = nullptr) {
+                   const float* b_scale = nullptr, int64_t lda_in = 0) {
     t_last_error.clear();
     hgemm_status_t st = check_args(A, B, C, M, N, K, dtype);
     if (st != HGEMM_OK || M == 0 || N == 0) return st;
@@ -480,7 +482,8 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
     }
 
     hgemm_plan_t pl;
-    const bool a_bad = misaligned16(A, K, es), b_bad = misaligned16(B, N, es), c_bad = misaligned16(C, N, ces);
+    const bool a_bad = lda_in > 0 ? false : misaligned16(A, K, es);
+    const bool b_bad = misaligned16(B, N, es), c_bad = misaligned16(C, N, ces);
     if ((st = make_plan(M, N, K, dtype, cfg, info.sms, a_bad, b_bad, c_bad, &pl)) != HGEMM_OK) return st;
 
     // Resident clusters bound the persistent grid; re-plan the schedule if
@@ -500,7 +503,7 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
     // Workspace: 16-byte-pitched copies of operands TMA cannot address, and
     // the fp32 partial sums of a K-split tail.
     const WorkspaceLayout wl = workspace_layout(pl, M, N, K, es);
-    const int64_t lda = pl.repack_a ? pitch16(K, es) : K;
+    const int64_t lda = lda_in > 0 ? lda_in : pl.repack_a ? pitch16(K, es) : K;
     // tf32 and fp8: B always goes through the workspace, transposed to N x K
     const bool b_t = b_transposed(dtype);
     const int64_t ldb = b_t ? pitch16(K, es) : pl.repack_b ? pitch16(N, es) : N;
@@ -663,6 +666,70 @@ hgemm_status_t hgemm_fp8_ex(const void* A, const void* B, void* C, const float* 
         return HGEMM_ERR_INVALID_ARG;
     }
     return run(A, B, C, M, N, K, dtype, cfg, static_cast<cudaStream_t>(stream), nullptr, 0, a_scale, b_scale);
+}
+
+hgemm_status_t hgemm_conv2d(const void* x, const void* w, void* y, int32_t N, int32_t H, int32_t W, int32_t C,
+                            int32_t K, int32_t R, int32_t S, int32_t stride, int32_t pad, hgemm_dtype_t dtype,
+                            void* stream) {
+    t_last_error.clear();
+    if (N < 0 || H < 1 || W < 1 || C < 1 || K < 1 || R < 1 || S < 1 || stride < 1 || pad < 0) {
+        t_last_error = "conv2d needs N >= 0, H, W, C, K, R, S, stride >= 1 and pad >= 0";
+        return HGEMM_ERR_INVALID_ARG;
+    }
+    if (dtype != HGEMM_F16 && dtype != HGEMM_BF16 && dtype != HGEMM_TF32) {
+        t_last_error = "conv2d takes HGEMM_F16, HGEMM_BF16 or HGEMM_TF32";
+        return HGEMM_ERR_INVALID_ARG;
+    }
+    const int64_t Pl = (static_cast<int64_t>(H) + 2 * pad - R) / stride + 1;
+    const int64_t Ql = (static_cast<int64_t>(W) + 2 * pad - S) / stride + 1;
+    if (static_cast<int64_t>(H) + 2 * pad < R || static_cast<int64_t>(W) + 2 * pad < S || N == 0) return HGEMM_OK;
+    const int es = esize_of(dtype);
+    const int64_t M = static_cast<int64_t>(N) * Pl * Ql;
+    const int64_t Kg = static_cast<int64_t>(R) * S * C;
+    if (M > 2147483647LL || Kg > 2147483647LL || Pl > 2147483647LL || Ql > 2147483647LL) {
+        t_last_error = "conv2d shape too large";
+        return HGEMM_ERR_INVALID_ARG;
+    }
+    if (!x || !w || !y) {
+        t_last_error = "null pointer for a non-empty operand";
+        return HGEMM_ERR_INVALID_ARG;
+    }
+    const uintptr_t amask = static_cast<uintptr_t>(es - 1);
+    if ((reinterpret_cast<uintptr_t>(x) & amask) || (reinterpret_cast<uintptr_t>(w) & amask) ||
+        (reinterpret_cast<uintptr_t>(y) & amask)) {
+        t_last_error = "operands must be aligned to their element size";
+        return HGEMM_ERR_INVALID_ARG;
+    }
+    const int64_t xbytes = static_cast<int64_t>(es) * N * H * W * C;
+    const int64_t wbytes = static_cast<int64_t>(es) * Kg * K;
+    const int64_t ybytes = static_cast<int64_t>(es) * M * K;
+    if (overlaps(y, ybytes, x, xbytes) || overlaps(y, ybytes, w, wbytes)) {
+        t_last_error = "y overlaps x or w";
+        return HGEMM_ERR_INVALID_ARG;
+    }
+    int dev = 0;
+    DeviceInfo info;
+    hgemm_status_t st = device_info(&dev, &info);
+    if (st != HGEMM_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the im2col matrix: M rows of Kg elements, padded to a 16-byte pitch
+    const int64_t lda = pitch16(Kg, es);
+    cudaMemPool_t pool;
+    if ((st = pool_for_device(dev, &pool)) != HGEMM_OK) return st;
+    void* A = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&A, static_cast<size_t>(align256(es * M * lda)), pool, s);
+    if (e != cudaSuccess) {
+        cuda_fail(e, "cudaMallocFromPoolAsync (im2col matrix)");
+        return HGEMM_ERR_ALLOC;
+    }
+    hg::ConvShape cs{N, H, W, C, K, R, S, stride, pad, static_cast<int32_t>(Pl), static_cast<int32_t>(Ql)};
+    if ((e = hg::launch_im2col(x, cs, es, A, lda, s)) != cudaSuccess) {
+        cudaFreeAsync(A, s);
+        return cuda_fail(e, "im2col");
+    }
+    st = run(A, w, y, M, K, Kg, dtype, nullptr, s, nullptr, 0, nullptr, nullptr, lda);
+    cudaFreeAsync(A, s);
+    return st;
 }
 
 hgemm_status_t hgemm_host(const void* hA, const void* hB, void* hC, int64_t M, int64_t N,

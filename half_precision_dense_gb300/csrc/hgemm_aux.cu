@@ -136,6 +136,77 @@ cudaError_t launch_transpose(const void* B, int64_t K, int64_t N, int esize, voi
     return cudaGetLastError();
 }
 
+// im2col for channels-last convolution: row m = (n, p, q) of A holds the
+// receptive field of output pixel (n, p, q) in (r, s, c) order, c fastest:
+//   A[m][(r*S + s)*C + c] = x[n][p*stride - pad + r][q*stride - pad + s][c]
+// (0 outside the image), and columns [R*S*C, lda) are 0. Each thread writes
+// 16 bytes of one row: a vector copy when those bytes lie in one tap's run of
+// channels and the source is 16-byte aligned, element by element otherwise.
+template <typename T>
+__global__ void im2col_kernel(const T* __restrict__ x, ConvShape cs, T* __restrict__ A, int64_t lda) {
+    constexpr int kPer = 16 / sizeof(T);
+    const int64_t chunks = lda / kPer;
+    const int64_t rows = static_cast<int64_t>(cs.N) * cs.P * cs.Q;
+    const int64_t taps = static_cast<int64_t>(cs.R) * cs.S * cs.C;
+    const bool vec = (cs.C % kPer) == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < rows * chunks;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t m = i / chunks, k0 = (i - m * chunks) * kPer;
+        const int q = static_cast<int>(m % cs.Q);
+        const int64_t np = m / cs.Q;
+        const int p = static_cast<int>(np % cs.P);
+        const int n = static_cast<int>(np / cs.P);
+        union {
+            T v[kPer];
+            uint4 u;
+        } out;
+        if (vec && k0 + kPer <= taps) {
+            const int c = static_cast<int>(k0 % cs.C);
+            const int64_t rs = k0 / cs.C;
+            const int r = static_cast<int>(rs / cs.S), s = static_cast<int>(rs % cs.S);
+            const int h = p * cs.stride - cs.pad + r, w = q * cs.stride - cs.pad + s;
+            if (h >= 0 && h < cs.H && w >= 0 && w < cs.W)
+                out.u = *reinterpret_cast<const uint4*>(x + ((static_cast<int64_t>(n) * cs.H + h) * cs.W + w) * cs.C + c);
+            else
+                out.u = make_uint4(0, 0, 0, 0);
+        } else {
+#pragma unroll
+            for (int j = 0; j < kPer; ++j) {
+                const int64_t kk = k0 + j;
+                T v = T(0);
+                if (kk < taps) {
+                    const int c = static_cast<int>(kk % cs.C);
+                    const int64_t rs = kk / cs.C;
+                    const int r = static_cast<int>(rs / cs.S), s = static_cast<int>(rs % cs.S);
+                    const int h = p * cs.stride - cs.pad + r, w = q * cs.stride - cs.pad + s;
+                    if (h >= 0 && h < cs.H && w >= 0 && w < cs.W)
+                        v = x[((static_cast<int64_t>(n) * cs.H + h) * cs.W + w) * cs.C + c];
+                }
+                out.v[j] = v;
+            }
+        }
+        *reinterpret_cast<uint4*>(A + m * lda + k0) = out.u;
+    }
+}
+
+cudaError_t launch_im2col(const void* x, const ConvShape& cs, int esize, void* A, int64_t lda,
+                          cudaStream_t stream) {
+    const int64_t rows = static_cast<int64_t>(cs.N) * cs.P * cs.Q;
+    if (rows <= 0) return cudaSuccess;
+    if ((esize != 2 && esize != 4) || (lda * esize) % 16 != 0 || (reinterpret_cast<uintptr_t>(A) & 15) != 0)
+        return cudaErrorInvalidValue;
+    const int64_t total = rows * (lda * esize / 16);
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > 152 * 64) blocks = 152 * 64;
+    if (esize == 2)
+        im2col_kernel<uint16_t><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+            static_cast<const uint16_t*>(x), cs, static_cast<uint16_t*>(A), lda);
+    else
+        im2col_kernel<uint32_t><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+            static_cast<const uint32_t*>(x), cs, static_cast<uint32_t*>(A), lda);
+    return cudaGetLastError();
+}
+
 __global__ void zero_kernel(uint16_t* __restrict__ dst, int64_t count) {
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < count;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x)

@@ -55,6 +55,15 @@ cudaError_t launch_zero(uint16_t* dst, int64_t count, cudaStream_t stream);
 // (4: fp32, 1: fp8) bytes per element.
 cudaError_t launch_transpose(const void* B, int64_t K, int64_t N, int esize, void* Bt, int64_t ldt,
                              cudaStream_t stream);
+// Convolution geometry (channels-last): x N x H x W x C, filters R x S x C x K,
+// output N x P x Q x K.
+struct ConvShape {
+    int32_t N, H, W, C, K, R, S, stride, pad, P, Q;
+};
+// A (N*P*Q rows of `lda` elements of `esize` = 2 or 4 bytes; lda * esize a
+// multiple of 16, A 16-byte aligned) = the im2col matrix of x.
+cudaError_t launch_im2col(const void* x, const ConvShape& cs, int esize, void* A, int64_t lda,
+                          cudaStream_t stream);
 // Device address of the status word on the current device (cached per device).
 cudaError_t status_word_ptr(unsigned long long** out);
 

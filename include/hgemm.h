@@ -102,6 +102,32 @@ hgemm_status_t hgemm(const void* A, const void* B, void* C, int64_t M, int64_t N
                      hgemm_dtype_t dtype, void* stream);
 
 /*
+ * hgemm_conv2d - 2-D convolution as one GEMM through im2col
+ * ("深度学习加速核心：GEMM优化从分块到TensorCore的实战解析", section 1.1: the
+ * input feature map rearranged by the kernel's receptive fields into one large
+ * matrix turns the convolution into a GEMM).
+ *
+ *   x  N x H x W x C  (channels last), device
+ *   w  R x S x C x K  (read as an (R*S*C) x K row-major matrix), device
+ *   y  N x P x Q x K  (written), device, P = (H + 2 pad - R) / stride + 1,
+ *                      Q = (W + 2 pad - S) / stride + 1
+ *
+ *   y[n][p][q][k] = round( sum_{r,s,c} x[n][p*stride-pad+r][q*stride-pad+s][c] * w[r][s][c][k] )
+ *
+ * (cross-correlation; x is zero outside the image; fp32 accumulation; the
+ * rounding and element types are those of hgemm() for dtype HGEMM_F16,
+ * HGEMM_BF16 or HGEMM_TF32). The im2col matrix (N*P*Q rows of R*S*C elements,
+ * padded to a 16-byte pitch) lives in the library's stream-ordered pool for
+ * the duration of the call's stream work; then hgemm's path computes
+ * y = A . w. N == 0 or an output with no pixels does nothing. Errors as for
+ * hgemm(); a negative or zero size (other than N), stride < 1 or pad < 0 is
+ * HGEMM_ERR_INVALID_ARG.
+ */
+hgemm_status_t hgemm_conv2d(const void* x, const void* w, void* y, int32_t N, int32_t H, int32_t W, int32_t C,
+                            int32_t K, int32_t R, int32_t S, int32_t stride, int32_t pad, hgemm_dtype_t dtype,
+                            void* stream);
+
+/*
  * hgemm_noalloc - hgemm for callers that must not allocate device memory.
  *
  * The pages have no counterpart to this entry point; it exists for callers
