@@ -60,14 +60,21 @@ WORKLOADS = {
     # per-channel scales uniform in [0.5, 2), bf16 C
     "fp8_4096": [(4096, 4096, 4096, "e4m3", "uniform", 8.0, 1)],
 }
+# convolution workloads (im2col + GEMM): name -> (N, H, W, C, R, S, K, stride, pad, dtype, seed)
+CONV_WORKLOADS = {
+    "conv3x3_resnet": (32, 28, 28, 256, 3, 3, 512, 1, 1, "bf16", 1),
+}
 DESCRIPTIONS = {
     "square4096": "GEMM M=N=K=4096, once bf16 and once fp16, A/B row-major, U[-1,1) seed 1",
     "tf32_4096": "TF32 GEMM M=N=K=4096, fp32 A/B/C row-major, U[-1,1) seed 1",
     "fp8_4096": "FP8 GEMM M=N=K=4096, E4M3 A/B row-major (U[-8,8) rounded), per-channel scales, bf16 C, seed 1",
+    "conv3x3_resnet": ("conv2d through im2col + GEMM: x 32x28x28x256 (NHWC), w 3x3x256x512 (RSCK), "
+                       "stride 1, pad 1, bf16, U[-1,1) seed 1"),
 }
 METRICS = {
     "tf32_4096": "TF32 GEMM TFLOP/s at M=N=K=4096 (fp32 in and out); % of GB300 dense tf32 tensor-core peak",
     "fp8_4096": "FP8 (E4M3) GEMM TFLOP/s at M=N=K=4096 with per-channel scales; % of GB300 dense fp8 tensor-core peak",
+    "conv3x3_resnet": "conv2d (im2col + GEMM) TFLOP/s, 2*N*P*Q*K*R*S*C flops; % of GB300 dense bf16 tensor-core peak",
 }
 # Nominal dense tensor rates relative to bf16 (2.25 PFLOP/s): tf32 1.1 PFLOP/s.
 NOMINAL_RATIO = {"bf16": 1.0, "f16": 1.0, "f32": 1.1 / 2.25, "e4m3": 4.5 / 2.25, "e5m2": 4.5 / 2.25}
@@ -181,8 +188,17 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     hg.load_library()
 
-    gemms = WORKLOADS[args.workload]
+    gemms = WORKLOADS.get(args.workload, [])
     ops = []
+    if args.workload in CONV_WORKLOADS:
+        (cN, cH, cW, cC, cR, cS, cK, cst, cpd, dt, seed) = CONV_WORKLOADS[args.workload]
+        cP = (cH + 2 * cpd - cR) // cst + 1
+        cQ = (cW + 2 * cpd - cS) // cst + 1
+        x = inputs.generate((1, cN * cH * cW * cC), dt, seed, 0).view(cN, cH, cW, cC)
+        w = inputs.generate((1, cR * cS * cC * cK), dt, seed, 1).view(cR, cS, cC, cK)
+        ops.append(dict(kind="conv", M=cN * cP * cQ, N=cK, K=cR * cS * cC, dt=dt, hA=x, hB=w, A=x.to(dev),
+                        B=w.to(dev), sa=None, sb=None, conv=(cN, cH, cW, cC, cK, cR, cS, cst, cpd),
+                        C=torch.empty((cN, cP, cQ, cK), dtype=inputs.TORCH_DTYPES[dt], device=dev)))
     for (M, N, K, dt, dist, sigma, seed) in gemms:
         if dt in FP8:
             A = torch.from_numpy(inputs.generate_fp8((M, K), dt, seed, 0, sigma))
@@ -201,7 +217,9 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream(dev)
 
     def one_gemm(o):
-        if o["dt"] in FP8:
+        if o.get("kind") == "conv":
+            hg.hgemm_conv2d(o["A"], o["B"], o["C"], *o["conv"], o["dt"], stream)
+        elif o["dt"] in FP8:
             hg.hgemm_fp8(o["A"], o["B"], o["C"], o["sa"], o["sb"], o["M"], o["N"], o["K"], o["dt"], None, stream)
         else:
             hg.hgemm(o["A"], o["B"], o["C"], o["M"], o["N"], o["K"], o["dt"], stream)
@@ -254,15 +272,26 @@ def run_ours(args, rank, world, local_rank):
     for o in ops:
         pinned.append((o["hA"].pin_memory(), o["hB"].pin_memory(),
                        torch.empty((o["M"], o["N"]), dtype=o["C"].dtype).pin_memory()))
+    def host_step(o, pa, pb, pc):
+        if o.get("kind") == "conv":
+            # host x, w -> device, convolution, y -> host, through the binding
+            o["A"].copy_(pa, non_blocking=True)
+            o["B"].copy_(pb, non_blocking=True)
+            one_gemm(o)
+            pc.view(o["C"].shape).copy_(o["C"], non_blocking=True)
+            stream.synchronize()
+        else:
+            hg.hgemm_host(pa, pb, pc, o["M"], o["N"], o["K"], o["dt"], o["A"], o["B"], o["C"], stream)
+
     for o, (pa, pb, pc) in zip(ops, pinned):   # warm the copy path
-        hg.hgemm_host(pa, pb, pc, o["M"], o["N"], o["K"], o["dt"], o["A"], o["B"], o["C"], stream)
+        host_step(o, pa, pb, pc)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     e0 = time.perf_counter()
     for _ in range(e2e_steps):
         for o, (pa, pb, pc) in zip(ops, pinned):
-            hg.hgemm_host(pa, pb, pc, o["M"], o["N"], o["K"], o["dt"], o["A"], o["B"], o["C"], stream)
+            host_step(o, pa, pb, pc)
     torch.cuda.synchronize(dev)
     e2e_s = time.perf_counter() - e0
 
@@ -283,7 +312,7 @@ def run_ours(args, rank, world, local_rank):
                  f"{peak_src} bf16 dense (cuBLAS burst) x nominal tf32/bf16 ratio 1.1/2.25")
     clocks = clk.summary()
     e2e_value = job_throughput(world, e2e_steps, step_flops, e2e_s * 1e3)
-    h2d = sum(ESIZE[o["dt"]] * (o["M"] * o["K"] + o["K"] * o["N"]) for o in ops)
+    h2d = sum(ESIZE[o["dt"]] * (o["hA"].numel() + o["hB"].numel()) for o in ops)
     d2h = sum(C_ESIZE[o["dt"]] * o["M"] * o["N"] for o in ops)
     line = {
         "metric": METRICS.get(args.workload, METRIC),
@@ -318,7 +347,7 @@ def run_ours(args, rank, world, local_rank):
             "unit": "TFLOP/s",
             "frac": round(achieved / peak, 4),
             "traffic": None,
-            "algorithmic_bytes_per_launch": (ESIZE[ops[0]["dt"]] * (ops[0]["M"] + ops[0]["N"]) * ops[0]["K"] +
+            "algorithmic_bytes_per_launch": (ESIZE[ops[0]["dt"]] * (ops[0]["hA"].numel() + ops[0]["hB"].numel()) +
                                              C_ESIZE[ops[0]["dt"]] * ops[0]["M"] * ops[0]["N"]),
         },
         "clocks": clocks,
@@ -353,6 +382,24 @@ def run_ours(args, rank, world, local_rank):
 
 
 # ---------------------------------------------------- oracle (CPU) timing
+def _conv_sample(workload, npts):
+    """``npts`` evenly spaced output pixels of a convolution workload, every
+    output channel: the oracle evaluates each from the convolution's
+    definition (uint16 bit patterns in, one row of K exact sums out)."""
+    import numpy as np
+
+    from half_precision_dense_gb300 import inputs
+
+    (N, H, W, C, R, S, K, st, pd, dt, seed) = CONV_WORKLOADS[workload]
+    P = (H + 2 * pd - R) // st + 1
+    Q = (W + 2 * pd - S) // st + 1
+    x = inputs.bits(inputs.generate((1, N * H * W * C), dt, seed, 0)).reshape(N, H, W, C)
+    w = inputs.bits(inputs.generate((1, R * S * C * K), dt, seed, 1)).reshape(R, S, C, K)
+    idx = np.linspace(0, N * P * Q - 1, max(1, npts)).astype(np.int64)
+    pts = [(int(i // (P * Q)), int(i // Q % P), int(i % Q)) for i in idx]
+    return ("conv", x, w, dt, st, pd, pts, 2 * len(pts) * K * R * S * C)
+
+
 def _oracle_sample(workload, rows, cols):
     """A sampled sub-problem of each GEMM of the workload: the C block at
     `rows` evenly spaced rows and `cols` evenly spaced columns, i.e. the rows
@@ -382,6 +429,11 @@ def _oracle_step(sample):
     import oracle
     from oracle import fp8_oracle, tf32_oracle
 
+    if isinstance(sample, tuple) and sample and sample[0] == "conv":
+        from oracle import conv_oracle
+        _, x, w, dt, st, pd, pts, fl = sample
+        oracle.round_rne(conv_oracle.conv_at(x, w, dt, st, pd, pts), dt)
+        return fl
     f = 0
     for (a, b, dt, K, scales) in sample:
         if dt == "f32":
@@ -395,6 +447,18 @@ def _oracle_step(sample):
 
 
 def _calibrated_sample(workload, seconds_per_step):
+    if workload in CONV_WORKLOADS:
+        npts = 64
+        for _ in range(3):
+            sample = _conv_sample(workload, npts)
+            t0 = time.perf_counter()
+            _oracle_step(sample)
+            el = max(time.perf_counter() - t0, 1e-6)
+            new = max(8, min(20000, int(npts * seconds_per_step / el)))
+            if abs(new - npts) <= npts // 8:
+                break
+            npts = new
+        return _conv_sample(workload, npts), npts
     side = 256
     for _ in range(3):
         sample = _oracle_sample(workload, side, side)
@@ -410,6 +474,9 @@ def _calibrated_sample(workload, seconds_per_step):
 
 
 def _sample_desc(side, workload):
+    if workload in CONV_WORKLOADS:
+        return (f"each step: {side} evenly spaced output pixels (every output channel) of {workload}, "
+                f"computed by the CPU oracle from the convolution's definition (fp64 taps + bit-level RNE)")
     dts = {g[3] for g in WORKLOADS[workload]}
     how = ("numpy fp64 product of the tf32-truncated operands, rounded to fp32" if dts == {"f32"} else
            "fp8 decode, numpy fp64 product, per-channel scales, bit-level RNE to bf16" if dts <= set(FP8) else
@@ -473,7 +540,7 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="square4096")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(CONV_WORKLOADS), default="square4096")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -707,11 +707,14 @@ hgemm_status_t hgemm_conv2d(const void* x, const void* w, void* y, int32_t N, in
         t_last_error = "y overlaps x or w";
         return HGEMM_ERR_INVALID_ARG;
     }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // A pointwise, stride-1, unpadded convolution is the GEMM itself: x is
+    // already the (N*H*W) x C matrix.
+    if (R == 1 && S == 1 && stride == 1 && pad == 0) return run(x, w, y, M, K, Kg, dtype, nullptr, s);
     int dev = 0;
     DeviceInfo info;
     hgemm_status_t st = device_info(&dev, &info);
     if (st != HGEMM_OK) return st;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     // the im2col matrix: M rows of Kg elements, padded to a 16-byte pitch
     const int64_t lda = pitch16(Kg, es);
     cudaMemPool_t pool;

@@ -119,7 +119,9 @@ hgemm_status_t hgemm(const void* A, const void* B, void* C, int64_t M, int64_t N
  * HGEMM_BF16 or HGEMM_TF32). The im2col matrix (N*P*Q rows of R*S*C elements,
  * padded to a 16-byte pitch) lives in the library's stream-ordered pool for
  * the duration of the call's stream work; then hgemm's path computes
- * y = A . w. N == 0 or an output with no pixels does nothing. Errors as for
+ * y = A . w. A 1 x 1 filter with stride 1 and no padding needs no im2col (x
+ * is the (N*H*W) x C matrix) and goes straight to the GEMM. N == 0 or an
+ * output with no pixels does nothing. Errors as for
  * hgemm(); a negative or zero size (other than N), stride < 1 or pad < 0 is
  * HGEMM_ERR_INVALID_ARG.
  */

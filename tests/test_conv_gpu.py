@@ -48,6 +48,9 @@ CASES = [
     (1, 17, 9, 3, 3, 3, 16, 1, 0),      # C = 3: element-wise im2col copies, R*S*C = 27
     (1, 20, 20, 12, 7, 1, 8, 3, 3),
     (3, 8, 8, 32, 3, 3, 264, 2, 1),     # ragged output tile in N (K = 264)
+    (2, 7, 9, 40, 1, 1, 48, 1, 0),      # pointwise: straight to the GEMM
+    (2, 7, 9, 40, 1, 1, 48, 2, 0),      # strided pointwise: im2col
+    (1, 6, 6, 12, 1, 1, 20, 1, 0),      # pointwise with C * 2 bytes not a 16-byte pitch
 ]
 
 
