@@ -139,16 +139,63 @@ cudaError_t launch_transpose(const void* B, int64_t K, int64_t N, int esize, voi
 // im2col for channels-last convolution: row m = (n, p, q) of A holds the
 // receptive field of output pixel (n, p, q) in (r, s, c) order, c fastest:
 //   A[m][(r*S + s)*C + c] = x[n][p*stride - pad + r][q*stride - pad + s][c]
-// (0 outside the image), and columns [R*S*C, lda) are 0. Each thread writes
-// 16 bytes of one row: a vector copy when those bytes lie in one tap's run of
-// channels and the source is 16-byte aligned, element by element otherwise.
+// (0 outside the image), and columns [R*S*C, lda) are 0.
+//
+// Vector form (C a multiple of 16 bytes, x 16-byte aligned): one warp per
+// (row, tap) segment copies that tap's C channels in 16-byte pieces, so the
+// index arithmetic is done once per segment; the padding columns are one
+// more segment per row. Element form otherwise: one thread per 16 bytes of a
+// row, element by element.
+template <typename T>
+__global__ void im2col_vec_kernel(const T* __restrict__ x, ConvShape cs, T* __restrict__ A, int64_t lda) {
+    constexpr int kPer = 16 / sizeof(T);
+    const int lane = threadIdx.x & 31;
+    const int64_t rows = static_cast<int64_t>(cs.N) * cs.P * cs.Q;
+    const int taps = cs.R * cs.S;
+    const int64_t taps_cols = static_cast<int64_t>(taps) * cs.C;
+    const int segs = taps + (lda > taps_cols ? 1 : 0);
+    const int cpieces = cs.C / kPer;
+    // narrow taps (fewer than 32 pieces): a warp takes several segments at
+    // once, lane = (segment within the group, piece)
+    const int group = cpieces >= 32 ? 1 : 32 / cpieces;
+    const int sub = cpieces >= 32 ? 0 : lane / cpieces;
+    const int sl = cpieces >= 32 ? lane : lane - sub * cpieces;
+    const int step = cpieces >= 32 ? 32 : cpieces;
+    const int64_t total = rows * segs;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t g0 = (static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5)) * group;
+         g0 < total; g0 += warps * group) {
+        const int64_t g = g0 + sub;
+        if (sub >= group || g >= total) continue;
+        const int64_t m = g / segs;
+        const int seg = static_cast<int>(g - m * segs);
+        T* dst = A + m * lda;
+        if (seg == taps) {
+            for (int64_t k = taps_cols + static_cast<int64_t>(sl) * kPer; k < lda; k += static_cast<int64_t>(step) * kPer)
+                *reinterpret_cast<uint4*>(dst + k) = make_uint4(0, 0, 0, 0);
+            continue;
+        }
+        const int q = static_cast<int>(m % cs.Q);
+        const int64_t np = m / cs.Q;
+        const int p = static_cast<int>(np % cs.P);
+        const int n = static_cast<int>(np / cs.P);
+        const int r = seg / cs.S, sx = seg - (seg / cs.S) * cs.S;
+        const int h = p * cs.stride - cs.pad + r, w = q * cs.stride - cs.pad + sx;
+        const bool inside = h >= 0 && h < cs.H && w >= 0 && w < cs.W;
+        const T* src = x + ((static_cast<int64_t>(n) * cs.H + h) * cs.W + w) * cs.C;
+        T* d = dst + static_cast<int64_t>(seg) * cs.C;
+        for (int j = sl; j < cpieces; j += step)
+            *reinterpret_cast<uint4*>(d + j * kPer) =
+                inside ? *reinterpret_cast<const uint4*>(src + j * kPer) : make_uint4(0, 0, 0, 0);
+    }
+}
+
 template <typename T>
 __global__ void im2col_kernel(const T* __restrict__ x, ConvShape cs, T* __restrict__ A, int64_t lda) {
     constexpr int kPer = 16 / sizeof(T);
     const int64_t chunks = lda / kPer;
     const int64_t rows = static_cast<int64_t>(cs.N) * cs.P * cs.Q;
     const int64_t taps = static_cast<int64_t>(cs.R) * cs.S * cs.C;
-    const bool vec = (cs.C % kPer) == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < rows * chunks;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t m = i / chunks, k0 = (i - m * chunks) * kPer;
@@ -160,30 +207,19 @@ __global__ void im2col_kernel(const T* __restrict__ x, ConvShape cs, T* __restri
             T v[kPer];
             uint4 u;
         } out;
-        if (vec && k0 + kPer <= taps) {
-            const int c = static_cast<int>(k0 % cs.C);
-            const int64_t rs = k0 / cs.C;
-            const int r = static_cast<int>(rs / cs.S), s = static_cast<int>(rs % cs.S);
-            const int h = p * cs.stride - cs.pad + r, w = q * cs.stride - cs.pad + s;
-            if (h >= 0 && h < cs.H && w >= 0 && w < cs.W)
-                out.u = *reinterpret_cast<const uint4*>(x + ((static_cast<int64_t>(n) * cs.H + h) * cs.W + w) * cs.C + c);
-            else
-                out.u = make_uint4(0, 0, 0, 0);
-        } else {
 #pragma unroll
-            for (int j = 0; j < kPer; ++j) {
-                const int64_t kk = k0 + j;
-                T v = T(0);
-                if (kk < taps) {
-                    const int c = static_cast<int>(kk % cs.C);
-                    const int64_t rs = kk / cs.C;
-                    const int r = static_cast<int>(rs / cs.S), s = static_cast<int>(rs % cs.S);
-                    const int h = p * cs.stride - cs.pad + r, w = q * cs.stride - cs.pad + s;
-                    if (h >= 0 && h < cs.H && w >= 0 && w < cs.W)
-                        v = x[((static_cast<int64_t>(n) * cs.H + h) * cs.W + w) * cs.C + c];
-                }
-                out.v[j] = v;
+        for (int j = 0; j < kPer; ++j) {
+            const int64_t kk = k0 + j;
+            T v = T(0);
+            if (kk < taps) {
+                const int c = static_cast<int>(kk % cs.C);
+                const int64_t rs = kk / cs.C;
+                const int r = static_cast<int>(rs / cs.S), s = static_cast<int>(rs % cs.S);
+                const int h = p * cs.stride - cs.pad + r, w = q * cs.stride - cs.pad + s;
+                if (h >= 0 && h < cs.H && w >= 0 && w < cs.W)
+                    v = x[((static_cast<int64_t>(n) * cs.H + h) * cs.W + w) * cs.C + c];
             }
+            out.v[j] = v;
         }
         *reinterpret_cast<uint4*>(A + m * lda + k0) = out.u;
     }
@@ -195,15 +231,33 @@ cudaError_t launch_im2col(const void* x, const ConvShape& cs, int esize, void* A
     if (rows <= 0) return cudaSuccess;
     if ((esize != 2 && esize != 4) || (lda * esize) % 16 != 0 || (reinterpret_cast<uintptr_t>(A) & 15) != 0)
         return cudaErrorInvalidValue;
-    const int64_t total = rows * (lda * esize / 16);
-    int64_t blocks = (total + 255) / 256;
+    const bool vec = (static_cast<int64_t>(cs.C) * esize) % 16 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0;
+    int64_t blocks;
+    if (vec) {
+        const int64_t cpieces = static_cast<int64_t>(cs.C) * esize / 16;
+        const int64_t group = cpieces >= 32 ? 1 : 32 / cpieces;
+        const int64_t segs = rows * (static_cast<int64_t>(cs.R) * cs.S + 1);
+        blocks = (segs / group + 7) / 8 + 1;  // 8 warps per block, `group` segments per warp
+    } else {
+        blocks = (rows * (lda * esize / 16) + 255) / 256;
+    }
     if (blocks > 152 * 64) blocks = 152 * 64;
-    if (esize == 2)
-        im2col_kernel<uint16_t><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-            static_cast<const uint16_t*>(x), cs, static_cast<uint16_t*>(A), lda);
-    else
-        im2col_kernel<uint32_t><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-            static_cast<const uint32_t*>(x), cs, static_cast<uint32_t*>(A), lda);
+    const unsigned b = static_cast<unsigned>(blocks);
+    if (esize == 2) {
+        if (vec)
+            im2col_vec_kernel<uint16_t><<<b, 256, 0, stream>>>(static_cast<const uint16_t*>(x), cs,
+                                                                static_cast<uint16_t*>(A), lda);
+        else
+            im2col_kernel<uint16_t><<<b, 256, 0, stream>>>(static_cast<const uint16_t*>(x), cs,
+                                                            static_cast<uint16_t*>(A), lda);
+    } else {
+        if (vec)
+            im2col_vec_kernel<uint32_t><<<b, 256, 0, stream>>>(static_cast<const uint32_t*>(x), cs,
+                                                                static_cast<uint32_t*>(A), lda);
+        else
+            im2col_kernel<uint32_t><<<b, 256, 0, stream>>>(static_cast<const uint32_t*>(x), cs,
+                                                            static_cast<uint32_t*>(A), lda);
+    }
     return cudaGetLastError();
 }
 
