@@ -92,6 +92,8 @@ def load_library():
         lib.hgemm_fp8_ex.restype = ctypes.c_int
         lib.hgemm_conv2d.argtypes = [vp, vp, vp] + [i32] * 9 + [ctypes.c_int, vp]
         lib.hgemm_conv2d.restype = ctypes.c_int
+        lib.hgemm_conv2d_set_mode.argtypes = [ctypes.c_int32]
+        lib.hgemm_conv2d_set_mode.restype = None
         lib.hgemm_noalloc_scratch_bytes.argtypes = []
         lib.hgemm_noalloc_scratch_bytes.restype = ctypes.c_uint64
         lib.hgemm_host.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.c_int, vp, vp, vp, vp]
@@ -199,6 +201,11 @@ def hgemm_conv2d(x, w, y, N: int, H: int, W: int, C: int, K: int, R: int, S: int
     lib = load_library()
     _check(lib.hgemm_conv2d(_ptr(x), _ptr(w), _ptr(y), N, H, W, C, K, R, S, stride, pad, _dtype_code(dtype),
                             _stream(stream)))
+
+
+def conv2d_set_mode(mode: int) -> None:
+    """0: implicit GEMM where the shape allows (default); 1: always explicit im2col."""
+    load_library().hgemm_conv2d_set_mode(mode)
 
 
 def conv2d_nhwc(x, w, stride: int = 1, pad: int = 0, stream=None):

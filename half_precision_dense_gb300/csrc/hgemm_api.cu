@@ -16,6 +16,9 @@ using hg::TcParams;
 thread_local std::string t_last_error;
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 std::atomic<int> g_inject{0};
+// hgemm_conv2d: 1 = implicit GEMM (TMA im2col) where the shape allows, 0 =
+// always the explicit im2col matrix
+std::atomic<bool> g_conv_implicit{true};
 std::atomic<unsigned long long*> g_trace{nullptr};
 
 hgemm_status_t cuda_fail(cudaError_t e, const char* where) {
@@ -91,6 +94,57 @@ EncodeTiledFn encode_fn() {
             fn = reinterpret_cast<EncodeTiledFn>(p);
     });
     return fn;
+}
+
+using EncodeIm2colFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                    const cuuint64_t*, const int*, const int*, cuuint32_t, cuuint32_t,
+                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeIm2colFn encode_im2col_fn() {
+    static std::once_flag once;
+    static EncodeIm2colFn fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeIm2col", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeIm2colFn>(p);
+    });
+    return fn;
+}
+
+// The channels-last activations x (N x H x W x C) of a convolution as an
+// im2col-mode tensor map: each copy brings `pixels` consecutive output pixels
+// (walked W-fastest inside the bounding box of receptive-field origins,
+// lower corner -pad, upper corner pad - (filter extent - 1), stepping by the
+// stride) times `chans` channels, in the 128-byte swizzle.
+hgemm_status_t encode_im2col(CUtensorMap* m, hgemm_dtype_t dt, const void* x, const hg::ConvShape& cs,
+                             uint32_t chans, uint32_t pixels) {
+    EncodeIm2colFn fn = encode_im2col_fn();
+    if (!fn) {
+        t_last_error = "cuTensorMapEncodeIm2col is not available from the driver";
+        return HGEMM_ERR_CUDA;
+    }
+    const int64_t es = esize_of(dt);
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(cs.C), static_cast<cuuint64_t>(cs.W),
+                                static_cast<cuuint64_t>(cs.H), static_cast<cuuint64_t>(cs.N)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(cs.C * es), static_cast<cuuint64_t>(cs.W) * cs.C * es,
+                                   static_cast<cuuint64_t>(cs.H) * cs.W * cs.C * es};
+    const int lower[2] = {-cs.pad, -cs.pad};
+    const int upper[2] = {cs.pad - (cs.S - 1), cs.pad - (cs.R - 1)};
+    const cuuint32_t estr[4] = {1, static_cast<cuuint32_t>(cs.stride), static_cast<cuuint32_t>(cs.stride), 1};
+    const CUtensorMapDataType type =
+        dt == HGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUresult r = fn(m, type, 4, const_cast<void*>(x), dims, strides, lower, upper, chans, pixels, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        t_last_error = "cuTensorMapEncodeIm2col failed with CUresult " + std::to_string(static_cast<int>(r));
+        return HGEMM_ERR_CUDA;
+    }
+    return HGEMM_OK;
 }
 
 // A 2-D row-major matrix of `dt` values: `cols` contiguous values per row,
@@ -461,12 +515,14 @@ hgemm_status_t check_args(const void* A, const void* B, void* C, int64_t M, int6
 // `a_scale` / `b_scale` (fp8 only; nullptr = 1) are the per-channel factors.
 // `lda_in` > 0: A's rows are lda_in elements apart (a 16-byte pitch, 16-byte
 // aligned base: the library's own im2col matrix), so A needs no repack.
+// `conv` (implicit-GEMM convolution): A is the activations x behind an
+// im2col-mode tensor map; hgemm_conv2d has checked the operands.
 hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
                    hgemm_dtype_t dtype, const hgemm_config_t* cfg, cudaStream_t stream,
                    void* scratch = nullptr, size_t scratch_bytes = 0, const float* a_scale = nullptr,
-                   const float* b_scale = nullptr, int64_t lda_in = 0) {
+                   const float* b_scale = nullptr, int64_t lda_in = 0, const hg::ConvShape* conv = nullptr) {
     t_last_error.clear();
-    hgemm_status_t st = check_args(A, B, C, M, N, K, dtype);
+    hgemm_status_t st = conv ? HGEMM_OK : check_args(A, B, C, M, N, K, dtype);
     if (st != HGEMM_OK || M == 0 || N == 0) return st;
     int dev = 0;
     DeviceInfo info;
@@ -482,7 +538,7 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
     }
 
     hgemm_plan_t pl;
-    const bool a_bad = lda_in > 0 ? false : misaligned16(A, K, es);
+    const bool a_bad = (lda_in > 0 || conv) ? false : misaligned16(A, K, es);
     const bool b_bad = misaligned16(B, N, es), c_bad = misaligned16(C, N, ces);
     if ((st = make_plan(M, N, K, dtype, cfg, info.sms, a_bad, b_bad, c_bad, &pl)) != HGEMM_OK) return st;
 
@@ -552,7 +608,8 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
     // A boxes: 128 rows x one 128-byte row of K; B boxes: bk k-rows x one
     // 128-byte swizzle atom of columns; C boxes: 32 rows x 128 bytes.
     const uint32_t ubk = static_cast<uint32_t>(bk);
-    if ((st = encode_2d(&ta, dtype, a_use, M, K, lda, ubk, hg::kBlockMCta)) != HGEMM_OK ||
+    if ((st = conv ? encode_im2col(&ta, dtype, A, *conv, ubk, hg::kBlockMCta)
+                   : encode_2d(&ta, dtype, a_use, M, K, lda, ubk, hg::kBlockMCta)) != HGEMM_OK ||
         (st = b_t ? encode_2d(&tb, dtype, b_use, N, K, ldb, ubk, static_cast<uint32_t>(bn / cg))
                   : encode_2d(&tb, dtype, b_use, K, N, ldb, ubk, ubk)) != HGEMM_OK ||
         (pl.store_mode == 1 &&
@@ -591,6 +648,15 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
     p.C = static_cast<uint16_t*>(C);
     p.a_scale = a_scale;
     p.b_scale = b_scale;
+    if (conv) {
+        p.im2col = 1;
+        p.cv_cblocks = static_cast<int32_t>(conv->C / bk);
+        p.cv_S = conv->S;
+        p.cv_P = conv->P;
+        p.cv_Q = conv->Q;
+        p.cv_stride = conv->stride;
+        p.cv_pad = conv->pad;
+    }
     p.ldc = N;
     p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
     p.sched.num_tiles = pl.num_tiles;
@@ -711,6 +777,13 @@ hgemm_status_t hgemm_conv2d(const void* x, const void* w, void* y, int32_t N, in
     // A pointwise, stride-1, unpadded convolution is the GEMM itself: x is
     // already the (N*H*W) x C matrix.
     if (R == 1 && S == 1 && stride == 1 && pad == 0) return run(x, w, y, M, K, Kg, dtype, nullptr, s);
+    hg::ConvShape cs{N, H, W, C, K, R, S, stride, pad, static_cast<int32_t>(Pl), static_cast<int32_t>(Ql)};
+    // Implicit GEMM: 16-bit activations whose channels come in whole 64-value
+    // (128-byte) blocks are read straight from x by TMA im2col copies; the
+    // im2col corners and offsets are 8-bit, the traversal stride at most 8.
+    const bool implicit = es == 2 && C % 64 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0 && pad <= 127 &&
+                          R <= 128 && S <= 128 && stride <= 8 && g_conv_implicit.load(std::memory_order_relaxed);
+    if (implicit) return run(x, w, y, M, K, Kg, dtype, nullptr, s, nullptr, 0, nullptr, nullptr, 0, &cs);
     int dev = 0;
     DeviceInfo info;
     hgemm_status_t st = device_info(&dev, &info);
@@ -725,7 +798,6 @@ hgemm_status_t hgemm_conv2d(const void* x, const void* w, void* y, int32_t N, in
         cuda_fail(e, "cudaMallocFromPoolAsync (im2col matrix)");
         return HGEMM_ERR_ALLOC;
     }
-    hg::ConvShape cs{N, H, W, C, K, R, S, stride, pad, static_cast<int32_t>(Pl), static_cast<int32_t>(Ql)};
     if ((e = hg::launch_im2col(x, cs, es, A, lda, s)) != cudaSuccess) {
         cudaFreeAsync(A, s);
         return cuda_fail(e, "im2col");
@@ -844,6 +916,8 @@ void hgemm_set_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 1, std::me
 // (grid_ctas x kTraceUnits x kTraceFields u64), or null.
 void hgemm_trace_set(void* buf) { g_trace.store(static_cast<unsigned long long*>(buf)); }
 #endif
+
+void hgemm_conv2d_set_mode(int32_t mode) { g_conv_implicit.store(mode == 0, std::memory_order_relaxed); }
 
 void hgemm_test_inject(int32_t kind) { g_inject.store(kind == 1 ? 1 : 0, std::memory_order_relaxed); }
 

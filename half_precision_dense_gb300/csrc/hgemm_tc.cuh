@@ -79,6 +79,13 @@ struct TcParams {
     uint16_t* C;                    // used by store modes 2-4 (fp32 elements for tf32)
     const float* a_scale;           // fp8: one factor per row of A, or null (1)
     const float* b_scale;           // fp8: one factor per column of B, or null (1)
+    // Implicit-GEMM convolution (im2col != 0): A is not a matrix but the
+    // channels-last activations behind an im2col-mode tensor map; row m of A
+    // is output pixel (n, p, q) = (m / (P Q), m / Q % P, m % Q), and K block
+    // kb is filter tap kb / cv_cblocks (r = tap / cv_S, s = tap % cv_S) at
+    // channels (kb % cv_cblocks) * kBK ..
+    int32_t im2col;
+    int32_t cv_cblocks, cv_S, cv_P, cv_Q, cv_stride, cv_pad;
     int64_t ldc;                    // elements between C rows (store_mode 2)
     uint64_t timeout_ns;
     unsigned long long* status;     // device status word
@@ -420,9 +427,26 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     const uint32_t b_dst = sB + stage * Cfg::kBBytes;
                     const uint32_t fb = bar_full + 8 * stage;
                     const int32_t k0 = kb * Cfg::kBK;
+                    // im2col: this CTA's 128 output pixels start at m0; the
+                    // copy walks them from the first one's receptive-field
+                    // origin, shifted by the K block's filter tap
+                    int32_t ic = 0, iw = 0, ih = 0, in_ = 0;
+                    uint16_t ow = 0, oh = 0;
+                    if (p.im2col) {
+                        const int32_t tap = kb / p.cv_cblocks;
+                        ic = (kb - tap * p.cv_cblocks) * Cfg::kBK;
+                        ow = static_cast<uint16_t>(tap % p.cv_S);
+                        oh = static_cast<uint16_t>(tap / p.cv_S);
+                        const int32_t q = m0 % p.cv_Q;
+                        const int32_t pq = m0 / p.cv_Q;
+                        iw = q * p.cv_stride - p.cv_pad;
+                        ih = (pq % p.cv_P) * p.cv_stride - p.cv_pad;
+                        in_ = pq / p.cv_P;
+                    }
                     if constexpr (CG == 1) {
                         mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
-                        tma_load_2d(a_dst, &tmA, fb, k0, m0);
+                        if (p.im2col) tma_load_im2col_4d(a_dst, &tmA, fb, ic, iw, ih, in_, ow, oh);
+                        else tma_load_2d(a_dst, &tmA, fb, k0, m0);
                         if constexpr (kBKMajor) {
                             tma_load_2d(b_dst, &tmB, fb, k0, n0);
                         } else {
@@ -433,7 +457,8 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     } else {
                         const uint32_t fb_leader = mapa_shared(fb, leader);
                         if (rank == 0) mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
-                        tma_load_2d_pair(a_dst, &tmA, fb_leader, k0, m0);
+                        if (p.im2col) tma_load_im2col_4d_pair(a_dst, &tmA, fb_leader, ic, iw, ih, in_, ow, oh);
+                        else tma_load_2d_pair(a_dst, &tmA, fb_leader, k0, m0);
                         if constexpr (kBKMajor) {
                             tma_load_2d_pair(b_dst, &tmB, fb_leader, k0, n0);
                         } else if constexpr (MC == 1) {

@@ -116,6 +116,35 @@ __device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const void* de
 }
 
 // 2-D tile store from shared memory, tracked by the bulk-group mechanism.
+// 4-D im2col-mode load (channels-last activations): `c`, `w`, `h`, `n` give
+// the first channel and the first output pixel's receptive-field origin in
+// the tensor map's bounding box; the copy walks the map's pixelsPerColumn
+// output pixels from there, each read at origin + (off_w, off_h) (the filter
+// tap), channelsPerPixel channels each. Out-of-image pixels read as zero.
+__device__ __forceinline__ void tma_load_im2col_4d(uint32_t dst, const void* desc, uint32_t bar, int32_t c,
+                                                   int32_t w, int32_t h, int32_t n, uint16_t off_w,
+                                                   uint16_t off_h) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.im2col.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2], {%7, %8};"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(desc)), "r"(bar), "r"(c), "r"(w), "r"(h), "r"(n),
+           "h"(off_w), "h"(off_h)
+        : "memory");
+}
+
+// The CTA-pair form: data lands in this CTA, the bytes are signalled on
+// `bar_cluster` (the pair leader's barrier).
+__device__ __forceinline__ void tma_load_im2col_4d_pair(uint32_t dst, const void* desc, uint32_t bar_cluster,
+                                                        int32_t c, int32_t w, int32_t h, int32_t n,
+                                                        uint16_t off_w, uint16_t off_h) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.im2col.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2], {%7, %8};"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(desc)), "r"(bar_cluster), "r"(c), "r"(w), "r"(h), "r"(n),
+           "h"(off_w), "h"(off_h)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_store_2d(const void* desc, uint32_t src, int32_t x, int32_t y) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];"
                  :: "l"(reinterpret_cast<uint64_t>(desc)), "r"(src), "r"(x), "r"(y) : "memory");

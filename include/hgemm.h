@@ -120,14 +120,24 @@ hgemm_status_t hgemm(const void* A, const void* B, void* C, int64_t M, int64_t N
  * padded to a 16-byte pitch) lives in the library's stream-ordered pool for
  * the duration of the call's stream work; then hgemm's path computes
  * y = A . w. A 1 x 1 filter with stride 1 and no padding needs no im2col (x
- * is the (N*H*W) x C matrix) and goes straight to the GEMM. N == 0 or an
- * output with no pixels does nothing. Errors as for
+ * is the (N*H*W) x C matrix) and goes straight to the GEMM. For fp16/bf16
+ * with C a multiple of 64 (16-byte aligned x, stride <= 8, pad <= 127) the
+ * matrix is never built: the GEMM's producer reads each 128-pixel x 64-channel
+ * tile of it straight from x with TMA im2col-mode copies (implicit GEMM).
+ * N == 0 or an output with no pixels does nothing. Errors as for
  * hgemm(); a negative or zero size (other than N), stride < 1 or pad < 0 is
  * HGEMM_ERR_INVALID_ARG.
  */
 hgemm_status_t hgemm_conv2d(const void* x, const void* w, void* y, int32_t N, int32_t H, int32_t W, int32_t C,
                             int32_t K, int32_t R, int32_t S, int32_t stride, int32_t pad, hgemm_dtype_t dtype,
                             void* stream);
+
+/*
+ * hgemm_conv2d_set_mode - 0 (default): hgemm_conv2d takes the implicit GEMM
+ * where the shape allows it; 1: always the explicit im2col matrix (the same
+ * results; for comparisons and tests). Process-wide.
+ */
+void hgemm_conv2d_set_mode(int32_t mode);
 
 /*
  * hgemm_noalloc - hgemm for callers that must not allocate device memory.

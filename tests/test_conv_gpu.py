@@ -41,7 +41,13 @@ def run_gpu(x, w, stride, pad):
 
 
 CASES = [
-    # (N, H, W, C, R, S, K, stride, pad)
+    # (N, H, W, C, R, S, K, stride, pad); C a multiple of 64 takes the
+    # implicit GEMM (TMA im2col), other C the explicit im2col matrix
+    (2, 9, 11, 64, 3, 3, 24, 1, 1),
+    (2, 13, 10, 128, 5, 5, 40, 2, 2),
+    (1, 20, 20, 64, 7, 1, 8, 3, 3),
+    (3, 8, 8, 192, 3, 3, 264, 2, 1),
+    (1, 15, 17, 64, 2, 4, 72, 1, 0),
     (2, 9, 11, 16, 3, 3, 24, 1, 1),
     (1, 14, 14, 64, 1, 1, 96, 1, 0),
     (2, 13, 10, 8, 5, 5, 40, 2, 2),
@@ -65,6 +71,17 @@ def test_conv_matches_definition(case, dtype):
     ref = co.conv(xb, wb, dtype, stride, pad).reshape(-1, K)
     r = compare(got, ref, ref64, dtype, R * S * C)
     assert r["ok"], r
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_implicit_and_explicit_paths_agree(mode):
+    # the same C % 64 == 0 shapes through either path
+    hg.conv2d_set_mode(mode)
+    try:
+        for case in [(2, 9, 11, 64, 3, 3, 24, 1, 1), (3, 8, 8, 192, 3, 3, 264, 2, 1)]:
+            test_conv_matches_definition(case, "bf16")
+    finally:
+        hg.conv2d_set_mode(0)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
