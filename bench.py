@@ -68,13 +68,14 @@ DESCRIPTIONS = {
     "square4096": "GEMM M=N=K=4096, once bf16 and once fp16, A/B row-major, U[-1,1) seed 1",
     "tf32_4096": "TF32 GEMM M=N=K=4096, fp32 A/B/C row-major, U[-1,1) seed 1",
     "fp8_4096": "FP8 GEMM M=N=K=4096, E4M3 A/B row-major (U[-8,8) rounded), per-channel scales, bf16 C, seed 1",
-    "conv3x3_resnet": ("conv2d through im2col + GEMM: x 32x28x28x256 (NHWC), w 3x3x256x512 (RSCK), "
+    "conv3x3_resnet": ("conv2d as a GEMM (implicit, TMA im2col): x 32x28x28x256 (NHWC), w 3x3x256x512 (RSCK), "
                        "stride 1, pad 1, bf16, U[-1,1) seed 1"),
 }
 METRICS = {
     "tf32_4096": "TF32 GEMM TFLOP/s at M=N=K=4096 (fp32 in and out); % of GB300 dense tf32 tensor-core peak",
     "fp8_4096": "FP8 (E4M3) GEMM TFLOP/s at M=N=K=4096 with per-channel scales; % of GB300 dense fp8 tensor-core peak",
-    "conv3x3_resnet": "conv2d (im2col + GEMM) TFLOP/s, 2*N*P*Q*K*R*S*C flops; % of GB300 dense bf16 tensor-core peak",
+    "conv3x3_resnet": ("conv2d as an implicit GEMM (TMA im2col) TFLOP/s, 2*N*P*Q*K*R*S*C flops; "
+                       "% of GB300 dense bf16 tensor-core peak"),
 }
 # Nominal dense tensor rates relative to bf16 (2.25 PFLOP/s): tf32 1.1 PFLOP/s.
 NOMINAL_RATIO = {"bf16": 1.0, "f16": 1.0, "f32": 1.1 / 2.25, "e4m3": 4.5 / 2.25, "e5m2": 4.5 / 2.25}
