@@ -135,8 +135,9 @@ hgemm_status_t encode_im2col(CUtensorMap* m, hgemm_dtype_t dt, const void* x, co
     const int lower[2] = {-cs.pad, -cs.pad};
     const int upper[2] = {cs.pad - (cs.S - 1), cs.pad - (cs.R - 1)};
     const cuuint32_t estr[4] = {1, static_cast<cuuint32_t>(cs.stride), static_cast<cuuint32_t>(cs.stride), 1};
-    const CUtensorMapDataType type =
-        dt == HGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUtensorMapDataType type = dt == HGEMM_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                     : dt == HGEMM_TF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     CUresult r = fn(m, type, 4, const_cast<void*>(x), dims, strides, lower, upper, chans, pixels, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -778,10 +779,11 @@ hgemm_status_t hgemm_conv2d(const void* x, const void* w, void* y, int32_t N, in
     // already the (N*H*W) x C matrix.
     if (R == 1 && S == 1 && stride == 1 && pad == 0) return run(x, w, y, M, K, Kg, dtype, nullptr, s);
     hg::ConvShape cs{N, H, W, C, K, R, S, stride, pad, static_cast<int32_t>(Pl), static_cast<int32_t>(Ql)};
-    // Implicit GEMM: 16-bit activations whose channels come in whole 64-value
-    // (128-byte) blocks are read straight from x by TMA im2col copies; the
-    // im2col corners and offsets are 8-bit, the traversal stride at most 8.
-    const bool implicit = es == 2 && C % 64 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0 && pad <= 127 &&
+    // Implicit GEMM: activations whose channels come in whole 128-byte blocks
+    // (64 fp16/bf16 or 32 fp32 values) are read straight from x by TMA im2col
+    // copies; the im2col corners and offsets are 8-bit, the traversal stride
+    // at most 8.
+    const bool implicit = C % bk_of(dtype) == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0 && pad <= 127 &&
                           R <= 128 && S <= 128 && stride <= 8 && g_conv_implicit.load(std::memory_order_relaxed);
     if (implicit) return run(x, w, y, M, K, Kg, dtype, nullptr, s, nullptr, 0, nullptr, nullptr, 0, &cs);
     int dev = 0;

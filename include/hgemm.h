@@ -120,10 +120,11 @@ hgemm_status_t hgemm(const void* A, const void* B, void* C, int64_t M, int64_t N
  * padded to a 16-byte pitch) lives in the library's stream-ordered pool for
  * the duration of the call's stream work; then hgemm's path computes
  * y = A . w. A 1 x 1 filter with stride 1 and no padding needs no im2col (x
- * is the (N*H*W) x C matrix) and goes straight to the GEMM. For fp16/bf16
- * with C a multiple of 64 (16-byte aligned x, stride <= 8, pad <= 127) the
- * matrix is never built: the GEMM's producer reads each 128-pixel x 64-channel
- * tile of it straight from x with TMA im2col-mode copies (implicit GEMM).
+ * is the (N*H*W) x C matrix) and goes straight to the GEMM. When C is a
+ * multiple of 64 (fp16/bf16) or 32 (tf32), x is 16-byte aligned, stride <= 8
+ * and pad <= 127, the matrix is never built: the GEMM's producer reads each
+ * 128-pixel x 128-byte tile of it straight from x with TMA im2col-mode copies
+ * (implicit GEMM).
  * N == 0 or an output with no pixels does nothing. Errors as for
  * hgemm(); a negative or zero size (other than N), stride < 1 or pad < 0 is
  * HGEMM_ERR_INVALID_ARG.

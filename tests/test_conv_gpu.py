@@ -96,9 +96,12 @@ def test_small_integers_bit_exact(dtype):
     assert np.array_equal(inputs.bits(got.reshape(1, -1)).reshape(got.shape), co.conv(xb, wb, dtype, 1, 1))
 
 
-def test_tf32_conv():
+@pytest.mark.parametrize("shape", [(2, 9, 9, 16, 3, 3, 32, 1, 1),     # explicit im2col (C = 16)
+                                   (2, 9, 9, 64, 3, 3, 32, 1, 1),     # implicit GEMM (C % 32 == 0)
+                                   (1, 11, 8, 32, 5, 3, 24, 2, 2)])
+def test_tf32_conv(shape):
     from oracle import tf32_oracle as tf
-    N, H, W, C, R, S, K, stride, pad = 2, 9, 9, 16, 3, 3, 32, 1, 1
+    N, H, W, C, R, S, K, stride, pad = shape
     x = inputs.generate((1, N * H * W * C), "f32", 4, 0).view(N, H, W, C)
     w = inputs.generate((1, R * S * C * K), "f32", 4, 1).view(R, S, C, K)
     got = run_gpu(x, w, stride, pad).numpy().reshape(-1, K)
@@ -106,7 +109,8 @@ def test_tf32_conv():
     # gather here; products and sums are the TF32 oracle's
     xp = np.pad(x.numpy(), ((0, 0), (pad, pad), (pad, pad), (0, 0)))
     P, Q = co.out_size(H, W, R, S, stride, pad)
-    cols = np.stack([xp[:, r:r + P, s:s + Q, :] for r in range(R) for s in range(S)], axis=3)
+    cols = np.stack([xp[:, r:r + stride * (P - 1) + 1:stride, s:s + stride * (Q - 1) + 1:stride, :]
+                     for r in range(R) for s in range(S)], axis=3)
     A = np.ascontiguousarray(cols.reshape(N * P * Q, R * S * C))
     Bm = np.ascontiguousarray(w.numpy().reshape(R * S * C, K))
     ref = tf.gemm(A, Bm)

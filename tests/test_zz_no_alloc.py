@@ -96,3 +96,25 @@ def test_noalloc_aligned_shape_with_stream_k(lib):
     ref64 = oracle.gemm_f64(a, b, "bf16")
     r = compare(inputs.bits(C.cpu()), oracle.round_rne(ref64, "bf16"), ref64, "bf16", K)
     assert r["ok"], r
+
+
+@pytest.mark.parametrize("dtype", ["tf32", "e4m3"])
+def test_other_dtypes_in_scratch(lib, dtype):
+    # tf32 and fp8 always stage B (transposed) in the workspace: here the
+    # fixed scratch array
+    import numpy as np
+    M, N, K = 512, 768, 1024
+    if dtype == "tf32":
+        A = torch.randn(M, K, device="cuda")
+        B = torch.randn(K, N, device="cuda")
+        C0 = torch.empty(M, N, device="cuda")
+        C1 = torch.empty(M, N, device="cuda")
+    else:
+        A = (torch.rand(M, K, device="cuda") * 8 - 4).to(torch.float8_e4m3fn)
+        B = (torch.rand(K, N, device="cuda") * 8 - 4).to(torch.float8_e4m3fn)
+        C0 = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
+        C1 = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
+    hg.hgemm(A, B, C0, M, N, K, dtype)
+    hg.hgemm_noalloc(A, B, C1, M, N, K, dtype)
+    torch.cuda.synchronize()
+    assert torch.equal(C0, C1)
