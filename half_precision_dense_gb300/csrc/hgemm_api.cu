@@ -671,6 +671,18 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
                   ? reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(work) + wl.off_flags)
                   : nullptr;
     p.epoch = next_epoch();
+    if (p.flags) {
+        // A graph replays this launch with the same epoch, so flags left by
+        // the previous replay would already read as published: a captured
+        // launch clears its flags first (an eager launch's epoch is new).
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if ((e = cudaStreamIsCapturing(stream, &cs)) != cudaSuccess ||
+            (cs == cudaStreamCaptureStatusActive &&
+             (e = cudaMemsetAsync(p.flags, 0, static_cast<size_t>(flag_bytes(pl)), stream)) != cudaSuccess)) {
+            if (work && work != scratch) cudaFreeAsync(work, stream);
+            return cuda_fail(e, "stream-K flags");
+        }
+    }
     p.inject = g_inject.load(std::memory_order_relaxed);
     p.trace = g_trace.load(std::memory_order_relaxed);
     if ((e = hg::status_word_ptr(&p.status)) != cudaSuccess) {

@@ -93,7 +93,7 @@ struct TcParams {
     float* partials;                // per cluster: the fp32 partial sums of its first,
                                     // non-owning stream-K unit
     unsigned long long* flags;      // one per (partial block, column half): == epoch once written
-    unsigned long long epoch;       // unique per launch
+    unsigned long long epoch;       // unique per launch (a captured launch clears the flags first)
     int32_t inject;                 // test hook: 1 = stream-K owners wait for partial sums
                                     // that are never published (the waits run out)
     unsigned long long* trace;      // timeline records (builds with HG_TRACE only), or null

@@ -97,6 +97,13 @@ typedef enum {
  * by the library (one per device, cudaMallocFromPoolAsync / cudaFreeAsync on
  * `stream`; the pool keeps up to 256 MiB cached between calls). Calls that need
  * no workspace allocate nothing; hgemm_plan reports the bytes.
+ *
+ * CUDA graphs: the call may be recorded by stream capture (the pool
+ * allocation becomes a graph allocation node). The capture holds the
+ * pointers, so replays read the operands' current values. Stream-K parts
+ * mark their partial sums with a number unique to each launch, which a graph
+ * replays unchanged, so a captured call with a stream-K phase first clears
+ * its marks (one small memset node in the graph).
  */
 hgemm_status_t hgemm(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
                      hgemm_dtype_t dtype, void* stream);
@@ -163,7 +170,8 @@ void hgemm_conv2d_set_mode(int32_t mode);
  *   - Every call on a device shares that device's array, which keeps the last
  *     call's contents (nothing in it needs to start at zero: stream-K parts
  *     mark their partial sums with a number unique to each launch, so stale
- *     marks are never mistaken for fresh ones). Calls whose GPU
+ *     marks are never mistaken for fresh ones; a captured call clears its
+ *     marks first, as for hgemm()). Calls whose GPU
  *     work overlaps - on different streams, or from different host threads -
  *     race on the array: serialise them (one stream, or events).
  *   - The first call on each device looks up the array's device address
