@@ -274,6 +274,15 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Wa
     return wait_slow(bar, parity, w, role, which);
 }
 
+// wait_bar for a whole warp: every lane waits, and lane 0's outcome is the
+// warp's (lanes could otherwise disagree when a wait runs out just as the
+// phase completes), so the warp's control flow stays uniform.
+__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, const Waiter& w,
+                                              uint32_t role, uint32_t which) {
+    const int got = wait_bar(bar, parity, w, role, which) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, got, 0) != 0;
+}
+
 __device__ __forceinline__ unsigned long long ld_acquire_gpu(const unsigned long long* ptr) {
     unsigned long long v;
     asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ptr) : "memory");
@@ -396,12 +405,14 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 
     if (warp == kProducerWarp || warp == kProducerWarp2) {
         // ------------------------------------------------------------ producer
-        // Two producer threads take alternate K blocks of the CTA's sequence
-        // (block g of the sequence goes to stage g mod S): one thread needs
+        // Two producer warps take alternate K blocks of the CTA's sequence
+        // (block g of the sequence goes to stage g mod S): one warp needs
         // longer to issue a stage (a barrier wait, the expected-bytes arrive,
         // the TMA copies) than a 256-wide pair MMA takes to consume it, so a
-        // single producer would starve the tensor core.
-        if (lane == 0) {
+        // single producer would starve the tensor core. The whole warp runs
+        // the loop and one elected lane issues the copies: with warp-uniform
+        // coordinates the copies issue faster than from a lone lane.
+        {
             const uint32_t pid = warp == kProducerWarp ? 0u : 1u;
             uint32_t stage = pid, phase = 0;
             uint32_t g = 0;
@@ -417,7 +428,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 for (int kb = wu.kb0; kb < wu.kb1; ++kb, ++g) {
                     if ((g & 1u) != pid) continue;
                     HG_TW_BEGIN();
-                    const bool got = wait_bar(bar_empty + 8 * stage, phase ^ 1u, w, kRoleProducer, stage);
+                    const bool got = wait_bar_warp(bar_empty + 8 * stage, phase ^ 1u, w, kRoleProducer, stage);
                     HG_TW_END(tw_empty);
                     if (!got) {
                         ok = false;
@@ -443,37 +454,40 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         ih = (pq % p.cv_P) * p.cv_stride - p.cv_pad;
                         in_ = pq / p.cv_P;
                     }
-                    if constexpr (CG == 1) {
-                        mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
-                        if (p.im2col) tma_load_im2col_4d(a_dst, &tmA, fb, ic, iw, ih, in_, ow, oh);
-                        else tma_load_2d(a_dst, &tmA, fb, k0, m0);
-                        if constexpr (kBKMajor) {
-                            tma_load_2d(b_dst, &tmB, fb, k0, n0);
-                        } else {
+                    if (elect_one_sync()) {
+                        if constexpr (CG == 1) {
+                            mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
+                            if (p.im2col) tma_load_im2col_4d(a_dst, &tmA, fb, ic, iw, ih, in_, ow, oh);
+                            else tma_load_2d(a_dst, &tmA, fb, k0, m0);
+                            if constexpr (kBKMajor) {
+                                tma_load_2d(b_dst, &tmB, fb, k0, n0);
+                            } else {
 #pragma unroll
-                            for (int j = 0; j < Cfg::kBAtoms; ++j)
-                                tma_load_2d(b_dst + j * Cfg::kBAtomBytes, &tmB, fb, n0 + Cfg::kAtomCols * j, k0);
-                        }
-                    } else {
-                        const uint32_t fb_leader = mapa_shared(fb, leader);
-                        if (rank == 0) mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
-                        if (p.im2col) tma_load_im2col_4d_pair(a_dst, &tmA, fb_leader, ic, iw, ih, in_, ow, oh);
-                        else tma_load_2d_pair(a_dst, &tmA, fb_leader, k0, m0);
-                        if constexpr (kBKMajor) {
-                            tma_load_2d_pair(b_dst, &tmB, fb_leader, k0, n0);
-                        } else if constexpr (MC == 1) {
-#pragma unroll
-                            for (int j = 0; j < Cfg::kBAtoms; ++j)
-                                tma_load_2d_pair(b_dst + j * Cfg::kBAtomBytes, &tmB, fb_leader,
-                                                 n0 + Cfg::kAtomCols * j, k0);
+                                for (int j = 0; j < Cfg::kBAtoms; ++j)
+                                    tma_load_2d(b_dst + j * Cfg::kBAtomBytes, &tmB, fb, n0 + Cfg::kAtomCols * j, k0);
+                            }
                         } else {
-                            // Atom `pair` of this B half, for this CTA and its
-                            // counterpart in the other pair.
-                            const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << (CG + rank)));
-                            tma_load_2d_pair_mc(b_dst + pair * Cfg::kBAtomBytes, &tmB, fb_leader,
-                                                n0 + Cfg::kAtomCols * static_cast<int32_t>(pair), k0, mask);
+                            const uint32_t fb_leader = mapa_shared(fb, leader);
+                            if (rank == 0) mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
+                            if (p.im2col) tma_load_im2col_4d_pair(a_dst, &tmA, fb_leader, ic, iw, ih, in_, ow, oh);
+                            else tma_load_2d_pair(a_dst, &tmA, fb_leader, k0, m0);
+                            if constexpr (kBKMajor) {
+                                tma_load_2d_pair(b_dst, &tmB, fb_leader, k0, n0);
+                            } else if constexpr (MC == 1) {
+#pragma unroll
+                                for (int j = 0; j < Cfg::kBAtoms; ++j)
+                                    tma_load_2d_pair(b_dst + j * Cfg::kBAtomBytes, &tmB, fb_leader,
+                                                     n0 + Cfg::kAtomCols * j, k0);
+                            } else {
+                                // Atom `pair` of this B half, for this CTA and its
+                                // counterpart in the other pair.
+                                const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << (CG + rank)));
+                                tma_load_2d_pair_mc(b_dst + pair * Cfg::kBAtomBytes, &tmB, fb_leader,
+                                                    n0 + Cfg::kAtomCols * static_cast<int32_t>(pair), k0, mask);
+                            }
                         }
                     }
+                    __syncwarp();
                     stage += 2;
                     if (stage >= static_cast<uint32_t>(S)) {
                         stage -= S;
@@ -491,7 +505,12 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         }
     } else if (warp == kMmaWarp) {
         // ----------------------------------------------------------------- MMA
-        if (rank == 0 && lane == 0) {
+        // The leader CTA's MMA warp runs the loop as a whole warp and one
+        // elected lane issues each stage's tcgen05.mma and commit: with
+        // warp-uniform descriptors and addresses the issue takes fewer cycles
+        // than from a lone lane, which matters because a 256-wide stage leaves
+        // the issuing thread little slack over the tensor core's 512 cycles.
+        if (rank == 0) {
             uint32_t stage = 0, phase = 0;
             bool ok = true;
             bool issued = false;
@@ -510,7 +529,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 const uint32_t acc = static_cast<uint32_t>(it) & 1u;
                 const uint32_t acc_phase = (static_cast<uint32_t>(it) >> 1) & 1u;
                 HG_TW_BEGIN();
-                const bool got_acc = wait_bar(bar_tempty + 8 * acc, acc_phase ^ 1u, w, kRoleMma, 32 + acc);
+                const bool got_acc = wait_bar_warp(bar_tempty + 8 * acc, acc_phase ^ 1u, w, kRoleMma, 32 + acc);
                 HG_TW_END(tw_tempty);
                 if (!got_acc) {
                     ok = false;
@@ -519,7 +538,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 if (wu.kind == 1) {
                     // A stream-K owner accumulates on top of its partners' partial
                     // sums, which the epilogue warps load into this buffer.
-                    if (!wait_bar(bar_pre + 8 * acc, pre_phase[acc], w, kRoleMma, 40 + acc)) {
+                    if (!wait_bar_warp(bar_pre + 8 * acc, pre_phase[acc], w, kRoleMma, 40 + acc)) {
                         ok = false;
                         break;
                     }
@@ -531,7 +550,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 uint32_t accum = wu.kind == 1 ? 1u : 0u;
                 for (int kb = wu.kb0; kb < wu.kb1; ++kb) {
                     HG_TW_BEGIN();
-                    const bool got_full = wait_bar(bar_full + 8 * stage, phase, w, kRoleMma, stage);
+                    const bool got_full = wait_bar_warp(bar_full + 8 * stage, phase, w, kRoleMma, stage);
                     HG_TW_END(tw_full);
                     if (!got_full) {
                         ok = false;
@@ -546,31 +565,38 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     // 128 B down B's atoms.
                     const uint64_t ad = a_desc0 + ((stage * Cfg::kABytes) >> 4);
                     const uint64_t bd = b_desc0 + ((stage * Cfg::kBBytes) >> 4);
+                    if (elect_one_sync()) {
 #pragma unroll
-                    for (int kk = 0; kk < Cfg::kBK / Cfg::kUK; ++kk) {
-                        if constexpr (kDt == 2)
-                            umma_tf32<CG>(d_tmem, ad + 2u * kk, bd + 2u * kk, p.idesc, accum);
-                        else if constexpr (kDt >= 3)
-                            umma_f8<CG>(d_tmem, ad + 2u * kk, bd + 2u * kk, p.idesc, accum);
-                        else
-                            umma_f16<CG>(d_tmem, ad + 2u * kk, bd + 8u * Cfg::kUK * kk, p.idesc, accum);
-                        accum = 1u;
+                        for (int kk = 0; kk < Cfg::kBK / Cfg::kUK; ++kk) {
+                            if constexpr (kDt == 2)
+                                umma_tf32<CG>(d_tmem, ad + 2u * kk, bd + 2u * kk, p.idesc, accum);
+                            else if constexpr (kDt >= 3)
+                                umma_f8<CG>(d_tmem, ad + 2u * kk, bd + 2u * kk, p.idesc, accum);
+                            else
+                                umma_f16<CG>(d_tmem, ad + 2u * kk, bd + 8u * Cfg::kUK * kk, p.idesc, accum);
+                            accum = 1u;
+                        }
+                        // A stage is free once every pair that reads it is done:
+                        // with B multicast, both pairs read every CTA's B atoms.
+                        if constexpr (CG == 1) umma_commit(bar_empty + 8 * stage);
+                        else umma_commit_pair(bar_empty + 8 * stage,
+                                              MC == 1 ? static_cast<uint16_t>(0x3u << leader)
+                                                      : static_cast<uint16_t>((1u << kCluster) - 1u));
                     }
+                    __syncwarp();
+                    accum = 1u;
                     issued = true;
-                    // A stage is free once every pair that reads it is done:
-                    // with B multicast, both pairs read every CTA's B atoms.
-                    if constexpr (CG == 1) umma_commit(bar_empty + 8 * stage);
-                    else umma_commit_pair(bar_empty + 8 * stage,
-                                          MC == 1 ? static_cast<uint16_t>(0x3u << leader)
-                                                  : static_cast<uint16_t>((1u << kCluster) - 1u));
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                if constexpr (CG == 1) umma_commit(bar_tfull + 8 * acc);
-                else umma_commit_pair(bar_tfull + 8 * acc, static_cast<uint16_t>(0x3u << leader));
+                if (elect_one_sync()) {
+                    if constexpr (CG == 1) umma_commit(bar_tfull + 8 * acc);
+                    else umma_commit_pair(bar_tfull + 8 * acc, static_cast<uint16_t>(0x3u << leader));
+                }
+                __syncwarp();
                 trace_stamp(p, it, kTrMmaLast);
             }
             trace_wait_total(p, kTwMmaFull, tw_full);
@@ -581,8 +607,11 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 #endif
             if (!ok && issued) {
                 // TMEM may only be freed once every issued MMA has completed.
-                if constexpr (CG == 1) umma_commit(bar_drain);
-                else umma_commit_pair(bar_drain, static_cast<uint16_t>(1u << leader));
+                if (elect_one_sync()) {
+                    if constexpr (CG == 1) umma_commit(bar_drain);
+                    else umma_commit_pair(bar_drain, static_cast<uint16_t>(1u << leader));
+                }
+                __syncwarp();
                 const uint64_t t0 = globaltimer_ns();
                 while (!mbar_try_wait(bar_drain, 0) && globaltimer_ns() - t0 < p.timeout_ns) {}
             }

@@ -64,6 +64,19 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
                  :: "r"(bar_cluster) : "memory");
 }
 
+// True in exactly one lane of the (converged) warp: elect.sync. Control flow
+// and the values computed before it stay warp-uniform, so the compiler can
+// keep them in uniform registers, which tcgen05.mma / tcgen05.commit and the
+// TMA copies take as operands.
+__device__ __forceinline__ bool elect_one_sync() {
+    uint32_t pred;
+    asm volatile("{\n\t.reg .b32 r;\n\t.reg .pred q;\n\t"
+                 "elect.sync r|q, 0xffffffff;\n\t"
+                 "selp.u32 %0, 1, 0, q;\n\t}"
+                 : "=r"(pred));
+    return pred != 0;
+}
+
 // True once the phase with parity `parity` has completed.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
