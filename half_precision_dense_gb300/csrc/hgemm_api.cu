@@ -187,23 +187,24 @@ bool valid_shape_config(int cg, int bn, hgemm_dtype_t dt) {
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Relative throughput of one SM running each tile shape on a long K loop
-// (1.0 = the pair 256x256 tile), measured on GB300 with L2 flushed: the pair
-// tile halves each SM's B traffic through shared memory, and narrower tiles
-// re-read A for fewer columns per MMA.
+// (1.0 = the pair 256x256 tile), measured on GB300 with L2 flushed, every SM
+// busy (whole waves) and the slope of time over K: the pair tile halves each
+// SM's B traffic through shared memory, and narrower tiles re-read A for
+// fewer columns per MMA.
 double shape_efficiency(int cg, int bn) {
     if (cg == 2 && bn == 256) return 1.00;
-    if (cg == 2 && bn == 224) return 0.86;
-    if (cg == 1 && bn == 256) return 0.84;
-    if (cg == 1 && bn == 128) return 0.62;
-    if (cg == 2 && bn == 128) return 0.61;
-    return 0.31;  // cg 1, bn 64
+    if (cg == 2 && bn == 224) return 0.97;
+    if (cg == 1 && bn == 256) return 0.845;
+    if (cg == 1 && bn == 128) return 0.71;
+    if (cg == 2 && bn == 128) return 0.83;
+    return 0.385;  // cg 1, bn 64
 }
 
 // Measured time constants of the kernel on GB300: the mainloop rate of one SM
 // at efficiency 1 (flop/s), the start-up plus last-epilogue time that no tile
 // overlaps, and the owners' stream-K fix-up (reading and adding the partners'
 // partial sums after the last unit) for a 256-wide tile.
-constexpr double kSmFlops = 13.4e12;
+constexpr double kSmFlops = 13.1e12;
 constexpr double kFixedSec = 4.5e-6;
 constexpr double kStreamKFixupSec = 3.0e-6;
 // Epilogue time per 64-column chunk of a CTA's 128-row tile (TMEM load,

@@ -97,6 +97,15 @@ def test_tile_coord_is_a_bijection(lib):
         assert len(seen) == tiles_m * tiles_n
 
 
+def test_plan_fills_the_machine_at_4096(lib):
+    # 152 SMs: 256-wide pair tiles give 256 tiles, 4 waves on 64 of the 76
+    # pairs; 224-wide ones give 16 x 19 = 304 tiles, 4 whole waves on all 76
+    # (and a 224-wide pair stage runs at 0.97 of a 256-wide one per flop)
+    p = binding.plan(4096, 4096, 4096, "bf16", sm_count=152)
+    assert (p["cta_group"], p["block_n"], p["grid_ctas"], p["num_tiles"]) == (2, 224, 152, 304)
+    assert p["num_tiles"] % (p["grid_ctas"] // p["cta_group"]) == 0 and p["sk_tiles"] == 0
+
+
 def test_tile_coord_groups_rows_first(lib):
     # inside a group the row index varies fastest
     coords = [binding.tile_coord(t, 16, 4, 8) for t in range(10)]
@@ -106,10 +115,10 @@ def test_tile_coord_groups_rows_first(lib):
 
 def test_plan_shapes(lib):
     p = binding.plan(4096, 4096, 4096, "bf16", sm_count=148)
-    assert p["cta_group"] in (1, 2) and p["block_n"] in (64, 128, 256)
+    assert p["cta_group"] in (1, 2) and p["block_n"] in (64, 128, 224, 256)
     assert p["tiles_m"] * p["block_m"] >= 4096 and p["tiles_n"] * p["block_n"] >= 4096
     assert p["grid_ctas"] % p["cta_group"] == 0 and p["grid_ctas"] <= 148
-    assert p["tmem_cols"] == 2 * p["block_n"]
+    assert p["tmem_cols"] >= 2 * p["block_n"] and p["tmem_cols"] & (p["tmem_cols"] - 1) == 0
     assert p["smem_bytes"] <= 232448 and p["stages"] >= 2
     assert p["repack_a"] == 0 and p["repack_b"] == 0 and p["store_mode"] == 1
     t = binding.plan(1000, 4095, 4104, "bf16", sm_count=148)
