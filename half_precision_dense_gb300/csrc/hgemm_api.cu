@@ -179,9 +179,12 @@ hgemm_status_t encode_2d(CUtensorMap* m, hgemm_dtype_t dt, const void* base, int
 }
 
 // ----------------------------------------------------------------- planner
+// The 224-wide pair tile ends in a 32-column epilogue chunk, which the
+// 16-bit C path (fp16, bf16, and the fp8 dtypes' bf16 C) stores; the fp32 C
+// of tf32 goes out in whole 64-column chunks, so tf32 does not take it.
 bool valid_shape_config(int cg, int bn, hgemm_dtype_t dt) {
     return (cg == 1 && (bn == 64 || bn == 128 || bn == 256)) ||
-           (cg == 2 && (bn == 128 || (bn == 224 && !b_transposed(dt)) || bn == 256));
+           (cg == 2 && (bn == 128 || (bn == 224 && dt != HGEMM_TF32) || bn == 256));
 }
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }

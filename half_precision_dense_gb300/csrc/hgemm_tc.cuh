@@ -333,7 +333,9 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 const TcParams p) {
 #if defined(__CUDA_ARCH__) && defined(__CUDA_ARCH_FEAT_SM103_ALL)
     using Cfg = TcCfg<CG, BN, elem_bytes(kDt)>;
-    static_assert(kDt < 2 || !Cfg::kHalfLast, "tf32 and fp8 tiles are whole 64-column chunks");
+    // fp32 C (tf32) leaves in whole 64-column chunks; 16-bit C (fp16, bf16
+    // and the fp8 dtypes' bf16) also handles a last chunk of 32 columns.
+    static_assert(kDt != 2 || !Cfg::kHalfLast, "tf32 tiles are whole 64-column chunks");
     // kind::tf32 takes both operands K-major (an MN-major tf32 operand
     // multiplies as zero on this GPU), and so does this kernel's fp8 path:
     // the host hands B over transposed, N x K, and one TMA box per stage

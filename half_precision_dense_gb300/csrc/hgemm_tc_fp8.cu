@@ -7,18 +7,18 @@ cudaError_t launch_tc_fp8(int kind, int cta_group, int block_n, int mc, const CU
                           const CUtensorMap& b, const CUtensorMap& c, const CUtensorMap& c32,
                           const TcParams& p, int clusters, cudaStream_t stream) {
     if (kind == 3) {
-        HG_TC_DISPATCH_K(3, launch(a, b, c, c32, p, clusters, stream))
+        HG_TC_DISPATCH_F8(3, launch(a, b, c, c32, p, clusters, stream))
     } else if (kind == 4) {
-        HG_TC_DISPATCH_K(4, launch(a, b, c, c32, p, clusters, stream))
+        HG_TC_DISPATCH_F8(4, launch(a, b, c, c32, p, clusters, stream))
     }
     return cudaErrorInvalidValue;
 }
 
 int max_active_clusters_fp8(int kind, int cta_group, int block_n, int mc) {
     if (kind == 3) {
-        HG_TC_DISPATCH_K(3, max_clusters())
+        HG_TC_DISPATCH_F8(3, max_clusters())
     } else if (kind == 4) {
-        HG_TC_DISPATCH_K(4, max_clusters())
+        HG_TC_DISPATCH_F8(4, max_clusters())
     }
     return 0;
 }

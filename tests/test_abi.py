@@ -294,14 +294,18 @@ def test_plan_fp8(lib):
     # 8-bit operands: 128 K values per 128-byte stage row; B transposed
     for code in (binding.HGEMM_E4M3, binding.HGEMM_E5M2):
         p = binding.plan(4096, 4096, 4096, code, sm_count=152)
-        assert (p["cta_group"], p["block_n"], p["block_k"], p["num_kb"]) == (2, 256, 128, 32)
+        # the 224-wide pair tile: 304 tiles, 4 whole waves on all 76 pairs
+        assert (p["cta_group"], p["block_n"], p["block_k"], p["num_kb"]) == (2, 224, 128, 32)
         assert p["repack_b"] == 1 and p["workspace_bytes"] >= 4096 * 4096
     # K = 1000 bytes is not a 16-byte pitch (A repacked); 1008 is
     assert binding.plan(64, 1024, 1000, "e4m3", sm_count=152)["repack_a"] == 1
     assert binding.plan(64, 1024, 1008, "e4m3", sm_count=152)["repack_a"] == 0
     # C is bf16: N = 1004 gives a 2008-byte pitch, not a multiple of 16 -> plain stores
     assert binding.plan(64, 1004, 1024, "e5m2", sm_count=152)["store_mode"] == 2
+    # tf32 (fp32 C in whole 64-column chunks) has no 224-wide tile
     with pytest.raises(binding.HgemmError):
-        binding.plan(1024, 1024, 1024, "e4m3", binding.Config(cta_group=2, block_n=224), sm_count=152)
+        binding.plan(1024, 1024, 1024, "tf32", binding.Config(cta_group=2, block_n=224), sm_count=152)
+    assert binding.plan(1024, 1024, 1024, "e4m3", binding.Config(cta_group=2, block_n=224),
+                        sm_count=152)["block_n"] == 224
     # the fp8 entry point refuses other dtypes
     assert lib.hgemm_fp8(None, None, None, None, None, 0, 0, 0, 1, None) == 1
