@@ -431,7 +431,12 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dt, cons
     schedule_plan(pl, clusters, c.stream_k, cdiv(K, bk_of(dt)));
     pl->repack_a = a_unaligned ? 1 : 0;
     pl->repack_b = (b_unaligned || b_transposed(dt)) ? 1 : 0;
-    pl->store_mode = (c.store_mode != 0) ? c.store_mode : (c_unaligned ? 2 : 1);
+    // Default for an aligned C: rows written back from the swizzled staging box
+    // with 16-byte vector stores (4). They go out through the load/store path,
+    // so they do not queue in the SM's TMA unit ahead of the next tile's
+    // operand loads, as TMA tensor stores (1) do: measured 0.5-1 % faster at
+    // 4096^3 to 16384x14336x4096, in 33 of 36 interleaved pairs.
+    pl->store_mode = (c.store_mode != 0) ? c.store_mode : (c_unaligned ? 2 : 4);
     if (c_unaligned && pl->store_mode != 2) {
         t_last_error = "vector and TMA stores need a 16-byte aligned C with a 16-byte row pitch";
         return HGEMM_ERR_INVALID_ARG;

@@ -199,7 +199,7 @@ uint64_t hgemm_noalloc_scratch_bytes(void);
  *                  straight from registers, 4 = 16-byte vector stores of whole
  *                  rows read back from the swizzled smem box (1, 3 and 4 need
  *                  a 16-byte aligned C whose row pitch is a multiple of 16
- *                  bytes).
+ *                  bytes). The planner takes 4 for such a C, else 2.
  *   stream_k:      how the tiles past the last whole wave are shared:
  *                  0 = planner's choice; 1 = never (whole tiles only, spread
  *                  over as few clusters as keep the wave count); 2 = stream-K

@@ -120,7 +120,8 @@ def test_plan_shapes(lib):
     assert p["grid_ctas"] % p["cta_group"] == 0 and p["grid_ctas"] <= 148
     assert p["tmem_cols"] >= 2 * p["block_n"] and p["tmem_cols"] & (p["tmem_cols"] - 1) == 0
     assert p["smem_bytes"] <= 232448 and p["stages"] >= 2
-    assert p["repack_a"] == 0 and p["repack_b"] == 0 and p["store_mode"] == 1
+    # aligned C: rows written back from the staging box by 16-byte stores
+    assert p["repack_a"] == 0 and p["repack_b"] == 0 and p["store_mode"] == 4
     t = binding.plan(1000, 4095, 4104, "bf16", sm_count=148)
     assert t["repack_b"] == 1 and t["repack_a"] == 0 and t["store_mode"] == 2
     forced = binding.plan(512, 512, 512, "f16",
