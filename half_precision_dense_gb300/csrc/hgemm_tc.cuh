@@ -283,6 +283,21 @@ __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, con
     return __shfl_sync(0xffffffffu, got, 0) != 0;
 }
 
+// An epilogue warp hands its accumulator buffer back to the MMA warp. The
+// arrive is relaxed: the warp's tcgen05.ld reads have completed
+// (tcgen05.wait::ld) before it, which is all the MMA warp needs, whereas a
+// release arrive at cluster scope also waits until the warp's earlier global
+// stores of C are acknowledged (measured 0.6 us of a tile's epilogue).
+template <int CG>
+__device__ __forceinline__ void release_accumulator(uint32_t bar, uint32_t leader) {
+    if constexpr (CG == 1) {
+        asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+    } else {
+        asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];"
+                     :: "r"(mapa_shared(bar, leader)) : "memory");
+    }
+}
+
 __device__ __forceinline__ unsigned long long ld_acquire_gpu(const unsigned long long* ptr) {
     unsigned long long v;
     asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ptr) : "memory");
@@ -719,14 +734,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             if (colhalf >= Cfg::kChunks) {
                 // No chunk for this warp (a 64-wide tile): release at once.
                 __syncwarp();
-                if (lane == 0) {
-                    if constexpr (CG == 1) {
-                        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];"
-                                     :: "r"(bar_tempty + 8 * acc) : "memory");
-                    } else {
-                        mbar_arrive_cluster(mapa_shared(bar_tempty + 8 * acc, leader));
-                    }
-                }
+                if (lane == 0) release_accumulator<CG>(bar_tempty + 8 * acc, leader);
                 preload_if_owner(it + 2);
                 continue;
             }
@@ -789,12 +797,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) {
-                        if constexpr (CG == 1) {
-                            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];"
-                                         :: "r"(bar_tempty + 8 * acc) : "memory");
-                        } else {
-                            mbar_arrive_cluster(mapa_shared(bar_tempty + 8 * acc, leader));
-                        }
+                        release_accumulator<CG>(bar_tempty + 8 * acc, leader);
                         if (warp == 0) trace_stamp(p, it, kTrEpiTmemFree);
                     }
                 }
