@@ -85,6 +85,8 @@ def load_library():
         lib.hgemm_ex.restype = ctypes.c_int
         lib.hgemm_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.c_int, vp]
         lib.hgemm_noalloc.restype = ctypes.c_int
+        lib.hgemm_noalloc_ex.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.c_int, ctypes.POINTER(_Config), vp]
+        lib.hgemm_noalloc_ex.restype = ctypes.c_int
         lib.hgemm_fp8.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ctypes.c_int, vp]
         lib.hgemm_fp8.restype = ctypes.c_int
         lib.hgemm_fp8_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ctypes.c_int,
@@ -166,11 +168,15 @@ def hgemm(A, B, C, M: int, N: int, K: int, dtype, stream=None) -> None:
     _check(lib.hgemm(_ptr(A), _ptr(B), _ptr(C), M, N, K, _dtype_code(dtype), _stream(stream)))
 
 
-def hgemm_noalloc(A, B, C, M: int, N: int, K: int, dtype, stream=None) -> None:
+def hgemm_noalloc(A, B, C, M: int, N: int, K: int, dtype, stream=None, config: Config | None = None) -> None:
     """hgemm for callers that cannot allocate: any workspace comes from the
-    library's fixed scratch array (see include/hgemm.h)."""
+    library's fixed scratch array (see include/hgemm.h); `config` as for hgemm_ex."""
     lib = load_library()
-    _check(lib.hgemm_noalloc(_ptr(A), _ptr(B), _ptr(C), M, N, K, _dtype_code(dtype), _stream(stream)))
+    if config is None:
+        _check(lib.hgemm_noalloc(_ptr(A), _ptr(B), _ptr(C), M, N, K, _dtype_code(dtype), _stream(stream)))
+    else:
+        _check(lib.hgemm_noalloc_ex(_ptr(A), _ptr(B), _ptr(C), M, N, K, _dtype_code(dtype),
+                                    ctypes.byref(config._c()), _stream(stream)))
 
 
 def hgemm_ex(A, B, C, M: int, N: int, K: int, dtype, config: Config | None = None,

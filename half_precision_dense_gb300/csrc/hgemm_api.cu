@@ -210,6 +210,10 @@ double shape_efficiency(int cg, int bn) {
 constexpr double kSmFlops = 13.1e12;
 constexpr double kFixedSec = 4.5e-6;
 constexpr double kStreamKFixupSec = 3.0e-6;
+// A CTA pair's extra start-up and hand-over latency per launch, visible on
+// short problems (1024^3: single-CTA 128-wide tiles 12.7 us, pair tiles
+// 13.9 us; 768^3: 12.1 against 12.5 us).
+constexpr double kPairFixedSec = 1.0e-6;
 // Epilogue time per 64-column chunk of a CTA's 128-row tile (TMEM load,
 // conversion, staging, TMA store); a CTA pair hands tensor memory back across
 // the pair, which costs about half as much again. A tile takes at least this
@@ -248,7 +252,7 @@ double schedule_seconds(int cg, int bn, int64_t tiles, int64_t clusters, int64_t
         t += tile_sec * static_cast<double>(blocks) / static_cast<double>(num_kb) +
              kStreamKFixupSec * bn / 256.0;
     }
-    return t + kFixedSec;
+    return t + kFixedSec + (cg == 2 ? kPairFixedSec : 0.0);
 }
 
 // Fill the schedule fields of `pl` (tiles already set) for `clusters`
@@ -260,22 +264,13 @@ void schedule_plan(hgemm_plan_t* pl, int64_t clusters, int sk_mode, int64_t num_
     if (sk_mode >= 2) {
         sk = stream_k_tiles(tiles, clusters, sk_mode);
         if (sk == 0 && sk_mode == 2 && tiles % clusters == 0 && tiles >= clusters) sk = clusters;
-    } else if (sk_mode == 0) {
-        // Measured on GB300: stream-K pays only where whole tiles would leave
-        // most SMs idle on a long K loop (single-CTA tiles, fewer tiles than
-        // clusters). With every SM fed, each tile runs slower than on the
-        // fewer, evenly loaded clusters of whole waves, which costs more than
-        // the balance gains on the pair-tile shapes.
-        const int64_t cand = (pl->cta_group == 1 && tiles * 2 <= clusters && num_kb >= 16)
-                                 ? stream_k_tiles(tiles, clusters, 2) : 0;
-        if (cand > 0) {
-            const int64_t waves = (tiles + clusters - 1) / clusters;
-            const int64_t even = (tiles + waves - 1) / waves;  // also caps clusters at tiles
-            const double t_dp = schedule_seconds(pl->cta_group, pl->block_n, tiles, even, num_kb, 0);
-            const double t_sk = schedule_seconds(pl->cta_group, pl->block_n, tiles, clusters, num_kb, cand);
-            if (t_sk < t_dp) sk = cand;
-        }
     }
+    // sk_mode 0 (the planner's choice) takes whole tiles. Measured on GB300
+    // with the current kernel over 14 shapes from 512^3 to 4096x8192x2048,
+    // including skinny 128 x 4096 x 4096 and 256 x 8192 x 8192, the best
+    // stream-K schedule never beat the best whole-tile one by more than 1 %
+    // and usually lost (by up to 30 %): the fix-up of shared tiles costs more
+    // than the balance gains.
     if (sk * num_kb < clusters) sk = 0;  // fewer K blocks than clusters: nothing to share
     if (sk == 0) {
         // Whole waves only: spread them over as few clusters as give the same
@@ -363,10 +358,14 @@ void choose_shape(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dt, int sms, in
         const int cg = c[0], bn = c[1];
         if (cg == 2 && M <= 128) continue;
         if (!valid_shape_config(cg, bn, dt)) continue;
-        // A single tile row on a long K loop is HBM-bound: 128-wide tiles give
-        // twice the tiles of 256-wide ones for stream-K to spread (measured
-        // best on GB300); the time model above assumes compute-bound tiles.
-        if (M <= 128 && K >= 16 * bk_of(dt) && bn != 128) continue;
+        // A single tile row on a long K loop is HBM-bound, which the time
+        // model above (compute-bound tiles) does not see: the narrowest tile
+        // that keeps every tile in one wave spreads B's stream over the most
+        // SMs (128 x 4096 x 4096: 64-wide 23.1 us, 128-wide 24.6 us).
+        if (M <= 128 && K >= 16 * bk_of(dt)) {
+            const int skinny_bn = cdiv(N, 64) <= sms ? 64 : 128;
+            if (cg != 1 || bn != skinny_bn) continue;
+        }
         int64_t clusters = sms / cg;
         if (max_clusters > 0 && max_clusters < clusters) clusters = max_clusters;
         if (clusters <= 0) continue;
@@ -722,9 +721,9 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
 namespace hg {
 
 hgemm_status_t gemm_in_scratch(const void* A, const void* B, void* C, int64_t M, int64_t N,
-                               int64_t K, hgemm_dtype_t dtype, cudaStream_t stream, void* scratch,
-                               size_t scratch_bytes) {
-    return run(A, B, C, M, N, K, dtype, nullptr, stream, scratch, scratch_bytes);
+                               int64_t K, hgemm_dtype_t dtype, const hgemm_config_t* config,
+                               cudaStream_t stream, void* scratch, size_t scratch_bytes) {
+    return run(A, B, C, M, N, K, dtype, config, stream, scratch, scratch_bytes);
 }
 
 hgemm_status_t set_last_error(const char* what, cudaError_t e) {

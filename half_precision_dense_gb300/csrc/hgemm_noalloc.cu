@@ -4,10 +4,11 @@
 // code running while a CUDA graph is being captured with allocation
 // disallowed, real-time or embedded pipelines that fix their memory at start
 // and treat any later allocation as a fault, and hosts whose device memory is
-// owned by another runtime's pool. For them, hgemm_noalloc() takes the one
+// owned by another runtime's pool. For them, hgemm_noalloc() takes the
 // workspace the GEMM may need - the 16-byte-pitch copy of an operand whose
-// rows TMA cannot address - from a fixed array compiled into this library
-// instead of from the stream-ordered allocator.
+// rows TMA cannot address, and the fp32 partial sums of a stream-K schedule
+// (hgemm_noalloc_ex with a config) - from a fixed array compiled into this
+// library instead of from the stream-ordered allocator.
 #include <mutex>
 
 #include "hgemm.h"
@@ -50,13 +51,19 @@ hgemm_status_t scratch_ptr(void** out) {
 
 }  // namespace
 
-extern "C" hgemm_status_t hgemm_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N,
-                                        int64_t K, hgemm_dtype_t dtype, void* stream) {
+extern "C" hgemm_status_t hgemm_noalloc_ex(const void* A, const void* B, void* C, int64_t M, int64_t N,
+                                           int64_t K, hgemm_dtype_t dtype, const hgemm_config_t* config,
+                                           void* stream) {
     void* scratch = nullptr;
     hgemm_status_t st = scratch_ptr(&scratch);
     if (st != HGEMM_OK) return st;
-    return hg::gemm_in_scratch(A, B, C, M, N, K, dtype, static_cast<cudaStream_t>(stream), scratch,
+    return hg::gemm_in_scratch(A, B, C, M, N, K, dtype, config, static_cast<cudaStream_t>(stream), scratch,
                                kScratchBytes);
+}
+
+extern "C" hgemm_status_t hgemm_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N,
+                                        int64_t K, hgemm_dtype_t dtype, void* stream) {
+    return hgemm_noalloc_ex(A, B, C, M, N, K, dtype, nullptr, stream);
 }
 
 extern "C" uint64_t hgemm_noalloc_scratch_bytes(void) { return kScratchBytes; }

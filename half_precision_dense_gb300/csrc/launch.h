@@ -67,12 +67,12 @@ cudaError_t launch_im2col(const void* x, const ConvShape& cs, int esize, void* A
 // Device address of the status word on the current device (cached per device).
 cudaError_t status_word_ptr(unsigned long long** out);
 
-// The GEMM of hgemm(), with the repack workspace taken from `scratch`
-// (`scratch_bytes` long) instead of the stream-ordered allocator
+// The GEMM of hgemm_ex() (config may be null), with the workspace taken from
+// `scratch` (`scratch_bytes` long) instead of the stream-ordered allocator
 // (hgemm_api.cu). Shapes needing more workspace give HGEMM_ERR_INVALID_ARG.
 hgemm_status_t gemm_in_scratch(const void* A, const void* B, void* C, int64_t M, int64_t N,
-                               int64_t K, hgemm_dtype_t dtype, cudaStream_t stream, void* scratch,
-                               size_t scratch_bytes);
+                               int64_t K, hgemm_dtype_t dtype, const hgemm_config_t* config,
+                               cudaStream_t stream, void* scratch, size_t scratch_bytes);
 // Record a failed CUDA call as this thread's last error; returns HGEMM_ERR_CUDA.
 hgemm_status_t set_last_error(const char* what, cudaError_t e);
 

@@ -228,6 +228,15 @@ hgemm_status_t hgemm_ex(const void* A, const void* B, void* C, int64_t M, int64_
                         hgemm_dtype_t dtype, const hgemm_config_t* cfg, void* stream);
 
 /*
+ * hgemm_noalloc_ex - hgemm_noalloc with a launch configuration (cfg may be
+ * NULL, as for hgemm_ex). A stream-K schedule (cfg->stream_k 2-4) keeps its
+ * fp32 partial sums and their marks in the fixed scratch array as well; the
+ * planner itself never picks stream-K.
+ */
+hgemm_status_t hgemm_noalloc_ex(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                                hgemm_dtype_t dtype, const hgemm_config_t* cfg, void* stream);
+
+/*
  * hgemm_fp8 - the FP8 variant: C (bf16, M x N) = per-channel-scaled A.B.
  *
  * A (M x K) and B (K x N) are row-major 8-bit E4M3 or E5M2 patterns (dtype
@@ -236,7 +245,7 @@ hgemm_status_t hgemm_ex(const void* A, const void* B, void* C, int64_t M, int64_
  * b_scale: device array of N fp32 factors, one per column of B; either may be
  * NULL (all ones). Scale arrays are read only and need 4-byte alignment.
  * B is first transposed (N x K) into the library's workspace, as for tf32;
- * tiles are (1, 64 | 128 | 256) or (2, 128 | 256). Errors as for hgemm();
+ * tiles are (1, 64 | 128 | 256) or (2, 128 | 224 | 256). Errors as for hgemm();
  * a dtype other than HGEMM_E4M3 / HGEMM_E5M2 is HGEMM_ERR_INVALID_ARG.
  */
 hgemm_status_t hgemm_fp8(const void* A, const void* B, void* C, const float* a_scale, const float* b_scale,

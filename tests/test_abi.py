@@ -146,9 +146,12 @@ def test_plan_stream_k(lib):
         off = binding.plan(4096, 4096, 4096, "bf16",
                            binding.Config(cta_group=2, block_n=256, stream_k=mode), sm_count=152)
         assert (off["sk_tiles"], off["dp_tiles"], off["grid_ctas"], off["workspace_bytes"]) == (0, 256, 128, 0)
-    # a single tile row on a long K loop: 128-wide one-CTA tiles, all stream-K
+    # a single tile row on a long K loop: the narrowest one-CTA tiles that
+    # keep every tile in one wave, whole (the planner never picks stream-K)
     sk = binding.plan(128, 8192, 8192, "bf16", sm_count=152)
-    assert (sk["cta_group"], sk["block_n"], sk["sk_tiles"], sk["grid_ctas"]) == (1, 128, 64, 152)
+    assert (sk["cta_group"], sk["block_n"], sk["sk_tiles"], sk["grid_ctas"]) == (1, 64, 0, 128)
+    wide = binding.plan(128, 16384, 8192, "bf16", sm_count=152)
+    assert (wide["cta_group"], wide["block_n"], wide["sk_tiles"]) == (1, 128, 0)
     # whole waves leave nothing to share; one K block leaves nothing to cut
     even = binding.plan(128 * 76, 256, 4096, "bf16", binding.Config(cta_group=1, block_n=256), sm_count=76)
     assert even["sk_tiles"] == 0 and even["grid_ctas"] == 76

@@ -28,14 +28,15 @@ def lib():
 
 
 def test_wait_that_runs_out_reports_timeout_and_context_survives():
-    M, N, K = 512, 1024, 2048  # fewer tiles than clusters: every tile shared by stream-K
+    M, N, K = 512, 1024, 2048  # stream-K over every tile: owners wait for partners' marks
+    cfg = hg.Config(stream_k=3)
     A = inputs.generate((M, K), "bf16", 40, 0).cuda()
     B = inputs.generate((K, N), "bf16", 40, 1).cuda()
-    assert hg.plan(M, N, K, "bf16")["sk_tiles"] > 0
+    assert hg.plan(M, N, K, "bf16", cfg)["sk_tiles"] > 0
     C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     hg.set_timeout_ns(50_000_000)  # 50 ms
     hg.test_inject(1)
-    hg.hgemm(A, B, C, M, N, K, "bf16")
+    hg.hgemm_ex(A, B, C, M, N, K, "bf16", cfg)
     torch.cuda.synchronize()  # the kernel returned on its own
     st, info = hg.get_device_status(0, reset=True)
     assert st == 5, (st, hex(info))
@@ -44,7 +45,7 @@ def test_wait_that_runs_out_reports_timeout_and_context_survives():
     # the context is intact: the next GEMM is correct and reports nothing
     hg.test_inject(0)
     hg.set_timeout_ns(2_000_000_000)
-    hg.hgemm(A, B, C, M, N, K, "bf16")
+    hg.hgemm_ex(A, B, C, M, N, K, "bf16", cfg)
     torch.cuda.synchronize()
     a, b = inputs.bits(A.cpu()), inputs.bits(B.cpu())
     ref64 = oracle.gemm_f64(a, b, "bf16")

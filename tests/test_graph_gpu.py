@@ -90,9 +90,6 @@ def test_gemm_stream_k(mode):
                 lambda: (A.copy_(rnd((M, K), torch.bfloat16)), B.copy_(rnd((K, N), torch.bfloat16))))
 
 
-def test_planner_shape_covers_stream_k():
-    # the skinny shape takes stream-K by the planner's own choice
-    assert hg.plan(128, 4096, 8192, "bf16")["sk_tiles"] > 0
 
 
 def test_gemm_unaligned_repack():
@@ -106,11 +103,15 @@ def test_gemm_unaligned_repack():
                 lambda: A.copy_(rnd((M, K), torch.bfloat16)))
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 4096, 8192), (2048, 2048, 2048)])
-def test_noalloc(M, N, K):
+@pytest.mark.parametrize("M,N,K,sk", [(128, 4096, 8192, 3), (128, 4096, 8192, 0), (2048, 2048, 2048, 0)])
+def test_noalloc(M, N, K, sk):
+    # sk 3: every tile's K blocks shared; partial sums and marks in the fixed array
+    cfg = hg.Config(stream_k=sk) if sk else None
+    if sk:
+        assert hg.plan(M, N, K, "bf16", cfg)["sk_tiles"] > 0
     A, B = rnd((M, K), torch.bfloat16), rnd((K, N), torch.bfloat16)
     C = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
-    check_graph(lambda s: hg.hgemm_noalloc(A, B, C, M, N, K, "bf16", s), (A, B), C,
+    check_graph(lambda s: hg.hgemm_noalloc(A, B, C, M, N, K, "bf16", s, config=cfg), (A, B), C,
                 lambda: B.copy_(rnd((K, N), torch.bfloat16)))
 
 

@@ -163,8 +163,8 @@ def test_stream_k(cfg, mode, clusters):
                                    (128, 1000, 3000)])
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 def test_planner_choices(shape, dtype):
-    # whatever the planner picks (stream-K for one tile row on a long K loop,
-    # whole tiles otherwise; K = 64 leaves nothing to share)
+    # whatever the planner picks (whole tiles; the narrowest single-CTA tiles
+    # for one tile row on a long K loop)
     M, N, K = shape
     A, B = operands(M, N, K, dtype, 15)
     check_full(A, B, dtype)
@@ -174,14 +174,15 @@ def test_stream_k_repeated_calls_reuse_workspace():
     # the pool hands the same workspace back; fresh launch epochs keep stale
     # partial-sum marks from being taken for new ones
     A, B = operands(512, 1024, 2048, "f16", 16)
-    assert hg.plan(512, 1024, 2048, "f16")["sk_tiles"] > 0
+    cfg = hg.Config(stream_k=3)
+    assert hg.plan(512, 1024, 2048, "f16", cfg)["sk_tiles"] > 0
     a, b = inputs.bits(A), inputs.bits(B)
     ref64 = oracle.gemm_f64(a, b, "f16")
     ref = oracle.round_rne(ref64, "f16")
     dA, dB = A.cuda(), B.cuda()
     for i in range(4):
         C = torch.empty((512, 1024), dtype=torch.float16, device="cuda")
-        hg.hgemm(dA, dB, C, 512, 1024, 2048, "f16")
+        hg.hgemm_ex(dA, dB, C, 512, 1024, 2048, "f16", cfg)
         torch.cuda.synchronize()
         r = compare(inputs.bits(C.cpu()), ref, ref64, "f16", 2048)
         assert r["ok"], (i, r)

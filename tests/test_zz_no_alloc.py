@@ -82,15 +82,17 @@ def test_noalloc_rejects_workspace_beyond_its_scratch(lib):
     assert torch.all(C == 7.0)  # nothing was enqueued
 
 
-def test_noalloc_aligned_shape_with_stream_k(lib):
-    # aligned operands; the only workspace is the stream-K partial sums (one
-    # tile row on a long K loop: every tile's K blocks are shared)
+@pytest.mark.parametrize("mode", [2, 3, 4])
+def test_noalloc_aligned_shape_with_stream_k(lib, mode):
+    # aligned operands; the only workspace is the stream-K partial sums (a
+    # stream-K schedule asked for through hgemm_noalloc_ex)
     M, N, K = 128, 2048, 4096
-    assert hg.plan(M, N, K, "bf16")["sk_tiles"] > 0
+    cfg = hg.Config(stream_k=mode)
+    assert hg.plan(M, N, K, "bf16", cfg)["sk_tiles"] > 0
     A = inputs.generate((M, K), "bf16", 34, 0)
     B = inputs.generate((K, N), "bf16", 34, 1)
     C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-    assert _call(lib, lib.hgemm_noalloc, A.cuda(), B.cuda(), C, M, N, K, "bf16") == 0
+    hg.hgemm_noalloc(A.cuda(), B.cuda(), C, M, N, K, "bf16", config=cfg)
     torch.cuda.synchronize()
     a, b = inputs.bits(A), inputs.bits(B)
     ref64 = oracle.gemm_f64(a, b, "bf16")
