@@ -179,12 +179,9 @@ hgemm_status_t encode_2d(CUtensorMap* m, hgemm_dtype_t dt, const void* base, int
 }
 
 // ----------------------------------------------------------------- planner
-// The 224-wide pair tile ends in a 32-column epilogue chunk, which the
-// 16-bit C path (fp16, bf16, and the fp8 dtypes' bf16 C) stores; the fp32 C
-// of tf32 goes out in whole 64-column chunks, so tf32 does not take it.
 bool valid_shape_config(int cg, int bn, hgemm_dtype_t dt) {
-    return (cg == 1 && (bn == 64 || bn == 128 || bn == 256)) ||
-           (cg == 2 && (bn == 128 || (bn == 224 && dt != HGEMM_TF32) || bn == 256));
+    (void)dt;
+    return (cg == 1 && (bn == 64 || bn == 128 || bn == 256)) || (cg == 2 && (bn == 128 || bn == 224 || bn == 256));
 }
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -632,7 +629,9 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
         (pl.store_mode == 1 &&
          (st = encode_2d(&tc, c_dtype_of(dtype), C, M, N, N, static_cast<uint32_t>(128 / ces), hg::kEpiBoxRows)) !=
              HGEMM_OK) ||
-        (pl.store_mode == 1 && bn % 64 != 0 &&
+        // the 32-column last chunk of a 16-bit C (fp32 C leaves in 32-column
+        // boxes throughout, through tc)
+        (pl.store_mode == 1 && bn % 64 != 0 && ces == 2 &&
          (st = encode_2d(&tc32, c_dtype_of(dtype), C, M, N, N, 32, hg::kEpiBoxRows, CU_TENSOR_MAP_SWIZZLE_64B)) !=
              HGEMM_OK)) {
         if (work && work != scratch) cudaFreeAsync(work, stream);

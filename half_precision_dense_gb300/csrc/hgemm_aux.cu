@@ -343,7 +343,7 @@ cudaError_t status_word_ptr(unsigned long long** out) {
         if (cta_group == 1 && block_n == 128) return esize == 4 ? TcCfg<1, 128, 4>::FIELD : TcCfg<1, 128, 1>::FIELD;  \
         if (cta_group == 1 && block_n == 256) return esize == 4 ? TcCfg<1, 256, 4>::FIELD : TcCfg<1, 256, 1>::FIELD;  \
         if (cta_group == 2 && block_n == 128) return esize == 4 ? TcCfg<2, 128, 4>::FIELD : TcCfg<2, 128, 1>::FIELD;  \
-        if (cta_group == 2 && block_n == 224 && esize == 1) return TcCfg<2, 224, 1>::FIELD;                           \
+        if (cta_group == 2 && block_n == 224) return esize == 4 ? TcCfg<2, 224, 4>::FIELD : TcCfg<2, 224, 1>::FIELD;  \
         if (cta_group == 2 && block_n == 256) return esize == 4 ? TcCfg<2, 256, 4>::FIELD : TcCfg<2, 256, 1>::FIELD;  \
     }                                                                                          \
     return 0;

@@ -348,9 +348,6 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 const TcParams p) {
 #if defined(__CUDA_ARCH__) && defined(__CUDA_ARCH_FEAT_SM103_ALL)
     using Cfg = TcCfg<CG, BN, elem_bytes(kDt)>;
-    // fp32 C (tf32) leaves in whole 64-column chunks; 16-bit C (fp16, bf16
-    // and the fp8 dtypes' bf16) also handles a last chunk of 32 columns.
-    static_assert(kDt != 2 || !Cfg::kHalfLast, "tf32 tiles are whole 64-column chunks");
     // kind::tf32 takes both operands K-major (an MN-major tf32 operand
     // multiplies as zero on this GPU), and so does this kernel's fp8 path:
     // the host hands B over transposed, N x K, and one TMA box per stage
@@ -409,7 +406,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
         if (p.store_mode == 1) tma_prefetch_desc(&tmC);
-        if (p.store_mode == 1 && Cfg::kHalfLast) tma_prefetch_desc(&tmC32);
+        if (p.store_mode == 1 && Cfg::kHalfLast && kDt != 2) tma_prefetch_desc(&tmC32);  // 16-bit C only
     }
     if (warp == kMmaWarp) tmem_alloc<CG>(smem_addr(tmem_slot), Cfg::kTmemCols);
     tc_fence_before();
@@ -883,9 +880,11 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     // each a 32 x 32 fp32 box of 128-byte rows in the same
                     // swizzle as the 16-bit boxes (16 B chunk j of row r at
                     // j ^ (r % 8)).
+                    // A tile whose width is an odd multiple of 32 ends in a
+                    // 32-column chunk: its first half only.
                     float* const Cf = reinterpret_cast<float*>(p.C);
 #pragma unroll 1
-                    for (int h = 0; h < 2; ++h) {
+                    for (int h = 0; h < (half ? 1 : 2); ++h) {
                         const uint32_t* v = h == 0 ? r0 : r1;
                         const int32_t hcol = col0 + 64 * c + 32 * h;
                         if (p.store_mode == 3) {

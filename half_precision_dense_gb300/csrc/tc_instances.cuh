@@ -97,10 +97,10 @@ struct TcInstance {
     if (mc == 1 && cta_group == 1 && block_n == 256) return TcInstance<1, 256, KDT>::CALL; \
     if (mc == 1 && cta_group == 2 && block_n == 128) return TcInstance<2, 128, KDT>::CALL; \
     if (mc == 1 && cta_group == 2 && block_n == 256) return TcInstance<2, 256, KDT>::CALL;
-// fp8 also takes the 224-wide pair tile (16-bit C epilogue).
+// tf32 and fp8 also take the 224-wide pair tile.
 #define HG_TC_DISPATCH_F8(KDT, CALL)                                                      \
     HG_TC_DISPATCH_K(KDT, CALL)                                                            \
     if (mc == 1 && cta_group == 2 && block_n == 224) return TcInstance<2, 224, KDT>::CALL;
-#define HG_TC_DISPATCH_TF32(CALL) HG_TC_DISPATCH_K(2, CALL)
+#define HG_TC_DISPATCH_TF32(CALL) HG_TC_DISPATCH_F8(2, CALL)
 
 }  // namespace hg

@@ -277,7 +277,7 @@ def test_epilogue_staging_layout_is_conflict_free_and_tma_compatible():
 def test_plan_tf32(lib):
     # fp32 operands: 32 K values per 128-byte stage row, same tiles and ring
     p = binding.plan(4096, 4096, 4096, "tf32", sm_count=152)
-    assert (p["cta_group"], p["block_n"], p["block_k"], p["num_kb"]) == (2, 256, 32, 128)
+    assert (p["cta_group"], p["block_n"], p["block_k"], p["num_kb"]) == (2, 224, 32, 128)
     assert p["stages"] == binding.plan(4096, 4096, 4096, "bf16", binding.Config(2, 256), sm_count=152)["stages"]
     # K = 1001 floats is not a 16-byte pitch: A is repacked; N = 1024 is
     assert binding.plan(64, 1024, 1001, "tf32", sm_count=152)["repack_a"] == 1
@@ -285,10 +285,9 @@ def test_plan_tf32(lib):
     tp = binding.plan(64, 1024, 1001, "tf32", sm_count=152)
     assert tp["repack_b"] == 1 and tp["workspace_bytes"] >= 4 * 1024 * 1004
     assert binding.plan(64, 1024, 1000, "tf32", sm_count=152)["repack_a"] == 0
-    # no 224-wide tiles and no B multicast for tf32
-    for cfg in (binding.Config(cta_group=2, block_n=224), binding.Config(cta_group=2, block_n=256, multicast=2)):
-        with pytest.raises(binding.HgemmError):
-            binding.plan(1024, 1024, 1024, "tf32", cfg, sm_count=152)
+    # no B multicast for tf32 (its B is a transposed, K-major copy)
+    with pytest.raises(binding.HgemmError):
+        binding.plan(1024, 1024, 1024, "tf32", binding.Config(cta_group=2, block_n=256, multicast=2), sm_count=152)
     # an unknown dtype code is refused by the library itself
     out = binding._Plan()
     assert lib.hgemm_plan(64, 64, 64, 5, None, 152, ctypes.byref(out)) == 1
@@ -306,10 +305,11 @@ def test_plan_fp8(lib):
     assert binding.plan(64, 1024, 1008, "e4m3", sm_count=152)["repack_a"] == 0
     # C is bf16: N = 1004 gives a 2008-byte pitch, not a multiple of 16 -> plain stores
     assert binding.plan(64, 1004, 1024, "e5m2", sm_count=152)["store_mode"] == 2
-    # tf32 (fp32 C in whole 64-column chunks) has no 224-wide tile
+    # every dtype takes the 224-wide pair tile (its last chunk is 32 columns)
+    for dt in ("tf32", "e4m3", "e5m2", "bf16", "f16"):
+        assert binding.plan(1024, 1024, 1024, dt, binding.Config(cta_group=2, block_n=224),
+                            sm_count=152)["block_n"] == 224
     with pytest.raises(binding.HgemmError):
-        binding.plan(1024, 1024, 1024, "tf32", binding.Config(cta_group=2, block_n=224), sm_count=152)
-    assert binding.plan(1024, 1024, 1024, "e4m3", binding.Config(cta_group=2, block_n=224),
-                        sm_count=152)["block_n"] == 224
+        binding.plan(1024, 1024, 1024, "tf32", binding.Config(cta_group=1, block_n=224), sm_count=152)
     # the fp8 entry point refuses other dtypes
     assert lib.hgemm_fp8(None, None, None, None, None, 0, 0, 0, 1, None) == 1

@@ -21,9 +21,10 @@ CONFIGS = [
     hg.Config(cta_group=1, block_n=128),
     hg.Config(cta_group=1, block_n=256),
     hg.Config(cta_group=2, block_n=128),
+    hg.Config(cta_group=2, block_n=224),
     hg.Config(cta_group=2, block_n=256),
 ]
-CFG_IDS = ["cg1_n64", "cg1_n128", "cg1_n256", "cg2_n128", "cg2_n256"]
+CFG_IDS = ["cg1_n64", "cg1_n128", "cg1_n256", "cg2_n128", "cg2_n224", "cg2_n256"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -110,14 +111,18 @@ def test_persistent_loop(cfg):
     check(1024, 1280, 320, 3, c)
 
 
+@pytest.mark.parametrize("block_n", [224, 256])
 @pytest.mark.parametrize("store_mode", [1, 2, 3, 4])
-def test_store_modes(store_mode):
-    check(700, 1024, 256, 4, hg.Config(cta_group=2, block_n=256, store_mode=store_mode))
+def test_store_modes(store_mode, block_n):
+    # 224: every tile's last chunk is one 32-column half, in each store path
+    check(700, 1024, 256, 4, hg.Config(cta_group=2, block_n=block_n, store_mode=store_mode))
 
 
+@pytest.mark.parametrize("block_n", [224, 256])
 @pytest.mark.parametrize("mode,clusters", [(2, 3), (3, 5), (4, 7)])
-def test_stream_k(mode, clusters):
-    check(1024, 1280, 704, 5, hg.Config(cta_group=2, block_n=256, max_clusters=clusters, stream_k=mode))
+def test_stream_k(mode, clusters, block_n):
+    check(1024, 1280, 704, 5,
+          hg.Config(cta_group=2, block_n=block_n, max_clusters=clusters, stream_k=mode))
 
 
 @pytest.mark.parametrize("shape", [(333, 517, 259), (256, 250, 130), (100, 3, 7)])
