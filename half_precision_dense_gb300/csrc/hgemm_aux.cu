@@ -41,8 +41,8 @@ __global__ void repack_rows_kernel(const T* __restrict__ src, int64_t rows, int6
     }
 }
 
-// Bt (N x K, row pitch ldt) = transpose of B (K x N, row pitch N), for fp32
-// or 8-bit elements. 32 x 32 tiles through shared memory (one padding
+// Bt (N x K, row pitch ldt) = transpose of B (K x N, row pitch N), for the
+// fp32 B of tf32 (kind::tf32 takes K-major operands). 32 x 32 tiles through shared memory (one padding
 // column keeps the column-wise reads conflict-free): reads along B's rows and
 // writes along Bt's rows are both coalesced. Grid: x over N tiles, y over K.
 template <typename T>
@@ -69,63 +69,6 @@ __global__ void transpose_kernel(const T* __restrict__ B, int64_t K, int64_t N, 
     }
 }
 
-// The 8-bit transpose in 64 x 64-byte tiles: thread t loads 16 bytes of B
-// row (t / 4) as four 32-bit words into the tile (a vector load when the 16
-// bytes are in range and aligned, bytes otherwise), then assembles 16
-// consecutive k-bytes of Bt row (t / 4) from the tile's words with byte
-// permutes and writes them as one 16-byte store (Bt rows are 16-byte aligned:
-// ldt is a multiple of 16). 256 threads.
-__global__ void transpose_u8_kernel(const uint8_t* __restrict__ B, int64_t K, int64_t N,
-                                    uint8_t* __restrict__ Bt, int64_t ldt) {
-    __shared__ uint32_t tile[64][17];  // 64 k-rows x 16 words of n-bytes (+1 pad)
-    const int t = threadIdx.x;
-    const int r = t >> 2, quad = t & 3;
-    const bool b_vec = (N & 15) == 0 && (reinterpret_cast<uintptr_t>(B) & 15) == 0;
-    for (int64_t kt = blockIdx.y; kt * 64 < K; kt += gridDim.y) {
-        for (int64_t nt = blockIdx.x; nt * 64 < N; nt += gridDim.x) {
-            const int64_t k = kt * 64 + r, n0 = nt * 64 + quad * 16;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (k < K) {
-                if (b_vec && n0 + 16 <= N) {
-                    v = *reinterpret_cast<const uint4*>(B + k * N + n0);
-                } else {
-                    uint32_t w[4] = {0, 0, 0, 0};
-                    for (int j = 0; j < 16; ++j)
-                        if (n0 + j < N) w[j >> 2] |= static_cast<uint32_t>(B[k * N + n0 + j]) << (8 * (j & 3));
-                    v = make_uint4(w[0], w[1], w[2], w[3]);
-                }
-            }
-            tile[r][quad * 4 + 0] = v.x;
-            tile[r][quad * 4 + 1] = v.y;
-            tile[r][quad * 4 + 2] = v.z;
-            tile[r][quad * 4 + 3] = v.w;
-            __syncthreads();
-            // output row n = nt*64 + r, k-bytes k0 .. k0 + 15 with k0 = kt*64 + 16 quad
-            const int64_t n = nt * 64 + r, k0 = kt * 64 + quad * 16;
-            if (n < N) {
-                const int col = r >> 2;
-                const uint32_t b = static_cast<uint32_t>(r & 3);
-                const uint32_t sel = b | ((b + 4) << 4);  // byte b of the first word, byte b of the second
-                uint32_t out[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int kk = quad * 16 + 4 * j;
-                    const uint32_t p01 = __byte_perm(tile[kk][col], tile[kk + 1][col], sel);
-                    const uint32_t p23 = __byte_perm(tile[kk + 2][col], tile[kk + 3][col], sel);
-                    out[j] = __byte_perm(p01, p23, 0x5410);
-                }
-                uint8_t* dst = Bt + n * ldt + k0;
-                if (k0 + 16 <= K) {
-                    *reinterpret_cast<uint4*>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
-                } else {
-                    for (int j = 0; j < 16 && k0 + j < K; ++j) dst[j] = static_cast<uint8_t>(out[j >> 2] >> (8 * (j & 3)));
-                }
-            }
-            __syncthreads();
-        }
-    }
-}
-
 cudaError_t launch_transpose(const void* B, int64_t K, int64_t N, int esize, void* Bt, int64_t ldt,
                              cudaStream_t stream) {
     if (K <= 0 || N <= 0) return cudaSuccess;
@@ -133,19 +76,9 @@ cudaError_t launch_transpose(const void* B, int64_t K, int64_t N, int esize, voi
     if (gx > 65535) gx = 65535;
     if (gy > 65535) gy = 65535;
     const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), block(32, 8);
-    if (esize == 4)
-        transpose_kernel<float><<<grid, block, 0, stream>>>(static_cast<const float*>(B), K, N,
-                                                            static_cast<float*>(Bt), ldt);
-    else if (esize == 1) {
-        int64_t gx8 = (N + 63) / 64, gy8 = (K + 63) / 64;
-        if (gx8 > 65535) gx8 = 65535;
-        if (gy8 > 65535) gy8 = 65535;
-        if ((reinterpret_cast<uintptr_t>(Bt) & 15) != 0 || (ldt & 15) != 0) return cudaErrorInvalidValue;
-        transpose_u8_kernel<<<dim3(static_cast<unsigned>(gx8), static_cast<unsigned>(gy8)), 256, 0, stream>>>(
-            static_cast<const uint8_t*>(B), K, N, static_cast<uint8_t*>(Bt), ldt);
-    }
-    else
-        return cudaErrorInvalidValue;
+    if (esize != 4) return cudaErrorInvalidValue;  // only tf32 B is transposed
+    transpose_kernel<float><<<grid, block, 0, stream>>>(static_cast<const float*>(B), K, N,
+                                                        static_cast<float*>(Bt), ldt);
     return cudaGetLastError();
 }
 

@@ -184,9 +184,10 @@ struct TcCfg {
     static constexpr int kABytes = kBlockMCta * 128;
     static constexpr int kBAtoms = (kBnCta + kAtomCols - 1) / kAtomCols;  // B swizzle atoms loaded
     static constexpr int kBAtomBytes = kBK * 128;          // kAtomCols columns x kBK k-rows
-    // 16-bit B is read MN-major in swizzle atoms; tf32 and fp8 B come
-    // transposed (N x K) and are read K-major: kBnCta rows of 128 B.
-    static constexpr bool kBKMajor = kElem != 2;
+    // 16-bit and 8-bit B is read MN-major in swizzle atoms (kAtomCols
+    // columns of 128 B rows); tf32 B comes transposed (N x K) and is read
+    // K-major: kBnCta rows of 128 B.
+    static constexpr bool kBKMajor = kElem == 4;
     static constexpr int kBBytes = kBKMajor ? kBnCta * 128 : kBAtoms * kBAtomBytes;
     static constexpr int kChunks = (BN + 63) / 64;         // epilogue chunks of 64 columns
     static constexpr bool kHalfLast = (BN % 64) != 0;      // the last chunk is 32 columns
@@ -222,9 +223,10 @@ struct TcCfg {
 // K-major A (rows of 128 B holding 64 K values, 8-row swizzle atoms stacked
 // along M): SBO = 1024 B between 8-row groups; LBO unused. The K offset of the
 // j-th 16-wide MMA inside the 64-wide stage is +32 j bytes of start address.
-// MN-major B (each 64-column atom is 64 k-rows of 128 B): LBO = distance
-// between 64-column atoms, SBO = 1024 B between 8-row k groups; the j-th MMA
-// starts 16 j rows = 2048 j bytes further.
+// MN-major B (each atom is kAtomCols columns = 128 B wide and kBK k-rows
+// deep: 64 x 64 for 16-bit, 128 x 128 for 8-bit): LBO = distance between
+// atoms, SBO = 1024 B between 8-row k groups; the j-th MMA starts kUK j rows
+// = 128 kUK j bytes further (2048 j for 16-bit, 4096 j for 8-bit).
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
     return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
            (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
@@ -349,11 +351,12 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 #if defined(__CUDA_ARCH__) && defined(__CUDA_ARCH_FEAT_SM103_ALL)
     using Cfg = TcCfg<CG, BN, elem_bytes(kDt)>;
     // kind::tf32 takes both operands K-major (an MN-major tf32 operand
-    // multiplies as zero on this GPU), and so does this kernel's fp8 path:
-    // the host hands B over transposed, N x K, and one TMA box per stage
-    // brings the CTA's kBnCta rows of it.
+    // multiplies as zero on this GPU): the host hands B over transposed,
+    // N x K, and one TMA box per stage brings the CTA's kBnCta rows of it.
+    // kind::f8f6f4 reads 8-bit B MN-major straight from the row-major
+    // matrix, as kind::f16 does (checked exactly on this GPU).
     constexpr bool kBKMajor = Cfg::kBKMajor;
-    static_assert(kBKMajor == (kDt >= 2), "K-major B for tf32 and fp8");
+    static_assert(kBKMajor == (kDt == 2), "K-major B for tf32 only");
     static_assert(!kBKMajor || (Cfg::kBnCta * 128 == Cfg::kBBytes && MC == 1), "K-major B box");
     constexpr int S = Cfg::kStages;
     constexpr int kCluster = CG * MC;
@@ -585,7 +588,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                             if constexpr (kDt == 2)
                                 umma_tf32<CG>(d_tmem, ad + 2u * kk, bd + 2u * kk, p.idesc, accum);
                             else if constexpr (kDt >= 3)
-                                umma_f8<CG>(d_tmem, ad + 2u * kk, bd + 2u * kk, p.idesc, accum);
+                                umma_f8<CG>(d_tmem, ad + 2u * kk, bd + 8u * Cfg::kUK * kk, p.idesc, accum);
                             else
                                 umma_f16<CG>(d_tmem, ad + 2u * kk, bd + 8u * Cfg::kUK * kk, p.idesc, accum);
                             accum = 1u;

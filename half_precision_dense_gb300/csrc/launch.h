@@ -32,8 +32,8 @@ cudaError_t launch_tc_tf32(int cta_group, int block_n, int mc, const CUtensorMap
 int max_active_clusters_bf16(int cta_group, int block_n, int mc);
 int max_active_clusters_f16(int cta_group, int block_n, int mc);
 int max_active_clusters_tf32(int cta_group, int block_n, int mc);
-// fp8: kind 3 = E4M3, 4 = E5M2 operands (B transposed, N x K), bf16 C; the
-// tf32 tile shapes.
+// fp8: kind 3 = E4M3, 4 = E5M2 operands (B row-major, read MN-major), bf16 C;
+// the tf32 tile shapes.
 cudaError_t launch_tc_fp8(int kind, int cta_group, int block_n, int mc, const CUtensorMap& a,
                           const CUtensorMap& b, const CUtensorMap& c, const CUtensorMap& c32,
                           const TcParams& p, int clusters, cudaStream_t stream);
@@ -51,8 +51,8 @@ int tc_tmem_cols(int cta_group, int block_n);
 cudaError_t launch_repack(const void* src, int64_t rows, int64_t cols, int esize, void* dst,
                           int64_t dst_ld, cudaStream_t stream);
 cudaError_t launch_zero(uint16_t* dst, int64_t count, cudaStream_t stream);
-// Bt (N x K, row pitch ldt elements) = B^T for B (K x N, dense) of `esize`
-// (4: fp32, 1: fp8) bytes per element.
+// Bt (N x K, row pitch ldt elements) = B^T for the fp32 B (K x N, dense) of
+// tf32; `esize` must be 4.
 cudaError_t launch_transpose(const void* B, int64_t K, int64_t N, int esize, void* Bt, int64_t ldt,
                              cudaStream_t stream);
 // Convolution geometry (channels-last): x N x H x W x C, filters R x S x C x K,

@@ -244,7 +244,8 @@ hgemm_status_t hgemm_noalloc_ex(const void* A, const void* B, void* C, int64_t M
  * bfloat16. a_scale: device array of M fp32 factors, one per row of A;
  * b_scale: device array of N fp32 factors, one per column of B; either may be
  * NULL (all ones). Scale arrays are read only and need 4-byte alignment.
- * B is first transposed (N x K) into the library's workspace, as for tf32;
+ * B is read in place, MN-major (a copy into the library's workspace only
+ * when N is not a multiple of 16, the row pitch TMA needs);
  * tiles are (1, 64 | 128 | 256) or (2, 128 | 224 | 256). Errors as for hgemm();
  * a dtype other than HGEMM_E4M3 / HGEMM_E5M2 is HGEMM_ERR_INVALID_ARG.
  */

@@ -297,9 +297,13 @@ def test_plan_fp8(lib):
     # 8-bit operands: 128 K values per 128-byte stage row; B transposed
     for code in (binding.HGEMM_E4M3, binding.HGEMM_E5M2):
         p = binding.plan(4096, 4096, 4096, code, sm_count=152)
-        # the 224-wide pair tile: 304 tiles, 4 whole waves on all 76 pairs
-        assert (p["cta_group"], p["block_n"], p["block_k"], p["num_kb"]) == (2, 224, 128, 32)
-        assert p["repack_b"] == 1 and p["workspace_bytes"] >= 4096 * 4096
+        # the 256-wide pair tile (the 224-wide one, which fills 8-bit B atoms
+        # badly, only when a config asks for it)
+        assert (p["cta_group"], p["block_n"], p["block_k"], p["num_kb"]) == (2, 256, 128, 32)
+        # B is read MN-major from the caller's matrix: no copy, no workspace
+        assert p["repack_b"] == 0 and p["workspace_bytes"] == 0
+    # N = 1000 bytes is not a 16-byte pitch: B is repacked
+    assert binding.plan(64, 1000, 1024, "e4m3", sm_count=152)["repack_b"] == 1
     # K = 1000 bytes is not a 16-byte pitch (A repacked); 1008 is
     assert binding.plan(64, 1024, 1000, "e4m3", sm_count=152)["repack_a"] == 1
     assert binding.plan(64, 1024, 1008, "e4m3", sm_count=152)["repack_a"] == 0
