@@ -72,10 +72,6 @@ bool is_fp8(hgemm_dtype_t dt) { return dt == HGEMM_E4M3 || dt == HGEMM_E5M2; }
 int esize_of(hgemm_dtype_t dt) { return dt == HGEMM_TF32 ? 4 : is_fp8(dt) ? 1 : 2; }
 hgemm_dtype_t c_dtype_of(hgemm_dtype_t dt) { return is_fp8(dt) ? HGEMM_BF16 : dt; }
 int c_esize_of(hgemm_dtype_t dt) { return esize_of(c_dtype_of(dt)); }
-// tf32 B is transposed (N x K) into the workspace and read K-major
-// (kind::tf32 takes no MN-major operand); fp8 and 16-bit B are read MN-major
-// from the caller's matrix
-bool b_transposed(hgemm_dtype_t dt) { return dt == HGEMM_TF32; }
 int64_t bk_of(hgemm_dtype_t dt) { return 128 / esize_of(dt); }
 
 // ------------------------------------------------- cuTensorMapEncodeTiled
@@ -310,17 +306,14 @@ int64_t pitch16(int64_t cols, int esize) {
     return (cols + per - 1) / per * per;
 }
 
-// The B copy of a tf32 or fp8 GEMM is B transposed (N x K, K padded to a
-// 16-byte pitch): those operands are read K-major.
 WorkspaceLayout workspace_layout(const hgemm_plan_t& pl, int64_t M, int64_t N, int64_t K, int esize) {
     WorkspaceLayout w{};
     const int64_t lda = pitch16(K, esize), ldb = pitch16(N, esize);
-    const bool bt = esize != 2;
     int64_t off = 0;
     w.off_a = off;
     off += pl.repack_a ? align256(esize * M * lda) : 0;
     w.off_b = off;
-    off += pl.repack_b ? align256(bt ? esize * N * pitch16(K, esize) : esize * K * ldb) : 0;
+    off += pl.repack_b ? align256(esize * K * ldb) : 0;
     w.off_part = off;
     off += align256(partial_bytes(pl));
     w.off_flags = off;
@@ -442,7 +435,7 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dt, cons
     if (c.max_clusters > 0 && c.max_clusters < clusters) clusters = c.max_clusters;
     schedule_plan(pl, clusters, c.stream_k, cdiv(K, bk_of(dt)));
     pl->repack_a = a_unaligned ? 1 : 0;
-    pl->repack_b = (b_unaligned || b_transposed(dt)) ? 1 : 0;
+    pl->repack_b = b_unaligned ? 1 : 0;
     // Default for an aligned C: rows written back from the swizzled staging box
     // with 16-byte vector stores (4). They go out through the load/store path,
     // so they do not queue in the SM's TMA unit ahead of the next tile's
@@ -582,9 +575,7 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
     // the fp32 partial sums of a K-split tail.
     const WorkspaceLayout wl = workspace_layout(pl, M, N, K, es);
     const int64_t lda = lda_in > 0 ? lda_in : pl.repack_a ? pitch16(K, es) : K;
-    // tf32 and fp8: B always goes through the workspace, transposed to N x K
-    const bool b_t = b_transposed(dtype);
-    const int64_t ldb = b_t ? pitch16(K, es) : pl.repack_b ? pitch16(N, es) : N;
+    const int64_t ldb = pl.repack_b ? pitch16(N, es) : N;
     void* work = nullptr;
     const void* a_use = A;
     const void* b_use = B;
@@ -615,8 +606,7 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
             a_use = w8 + wl.off_a;
         }
         if (pl.repack_b) {
-            if ((e = b_t ? hg::launch_transpose(B, K, N, es, w8 + wl.off_b, ldb, stream)
-                         : hg::launch_repack(B, K, N, es, w8 + wl.off_b, ldb, stream)) != cudaSuccess) {
+            if ((e = hg::launch_repack(B, K, N, es, w8 + wl.off_b, ldb, stream)) != cudaSuccess) {
                 if (work != scratch) cudaFreeAsync(work, stream);
                 return cuda_fail(e, "repack B");
             }
@@ -628,12 +618,15 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
     std::memset(&tc, 0, sizeof(tc));
     std::memset(&tc32, 0, sizeof(tc32));
     // A boxes: 128 rows x one 128-byte row of K; B boxes: bk k-rows x one
-    // 128-byte swizzle atom of columns; C boxes: 32 rows x 128 bytes.
+    // 128-byte swizzle atom of columns (tf32 B in the 32-byte-atom swizzle,
+    // which is how kind::tf32 reads an MN-major operand); C boxes: 32 rows x
+    // 128 bytes.
     const uint32_t ubk = static_cast<uint32_t>(bk);
     if ((st = conv ? encode_im2col(&ta, dtype, A, *conv, ubk, hg::kBlockMCta)
                    : encode_2d(&ta, dtype, a_use, M, K, lda, ubk, hg::kBlockMCta)) != HGEMM_OK ||
-        (st = b_t ? encode_2d(&tb, dtype, b_use, N, K, ldb, ubk, static_cast<uint32_t>(bn / cg))
-                  : encode_2d(&tb, dtype, b_use, K, N, ldb, ubk, ubk)) != HGEMM_OK ||
+        (st = encode_2d(&tb, dtype, b_use, K, N, ldb, ubk, ubk,
+                        dtype == HGEMM_TF32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B)) !=
+            HGEMM_OK ||
         (pl.store_mode == 1 &&
          (st = encode_2d(&tc, c_dtype_of(dtype), C, M, N, N, static_cast<uint32_t>(128 / ces), hg::kEpiBoxRows)) !=
              HGEMM_OK) ||
@@ -665,8 +658,7 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
     // A and B format (bits 7-9, 10-12: 0 f16, 1 bf16, 2 tf32), A K-major
     // (bit 15 = 0), B MN-major (bit 16 = 1), N >> 3 (bits 17-22), M >> 4
     // (bits 24-28).
-    const uint32_t b_mn = b_t ? 0u : 1u;  // tf32, fp8: B K-major (transposed copy)
-    p.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | (0u << 15) | (b_mn << 16) |
+    p.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | (0u << 15) | (1u << 16) |
               (static_cast<uint32_t>(bn >> 3) << 17) | (static_cast<uint32_t>((128 * cg) >> 4) << 24);
     p.store_mode = pl.store_mode;
     p.C = static_cast<uint16_t*>(C);

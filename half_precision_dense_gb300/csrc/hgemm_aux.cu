@@ -41,47 +41,6 @@ __global__ void repack_rows_kernel(const T* __restrict__ src, int64_t rows, int6
     }
 }
 
-// Bt (N x K, row pitch ldt) = transpose of B (K x N, row pitch N), for the
-// fp32 B of tf32 (kind::tf32 takes K-major operands). 32 x 32 tiles through shared memory (one padding
-// column keeps the column-wise reads conflict-free): reads along B's rows and
-// writes along Bt's rows are both coalesced. Grid: x over N tiles, y over K.
-template <typename T>
-__global__ void transpose_kernel(const T* __restrict__ B, int64_t K, int64_t N, T* __restrict__ Bt,
-                                 int64_t ldt) {
-    __shared__ T tile[32][33];
-    for (int64_t kt = blockIdx.y; kt * 32 < K; kt += gridDim.y) {
-        for (int64_t nt = blockIdx.x; nt * 32 < N; nt += gridDim.x) {
-            const int64_t n = nt * 32 + threadIdx.x;
-#pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-                const int64_t k = kt * 32 + threadIdx.y + i;
-                tile[threadIdx.y + i][threadIdx.x] = (k < K && n < N) ? B[k * N + n] : T(0);
-            }
-            __syncthreads();
-            const int64_t k = kt * 32 + threadIdx.x;
-#pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-                const int64_t nn = nt * 32 + threadIdx.y + i;
-                if (nn < N && k < K) Bt[nn * ldt + k] = tile[threadIdx.x][threadIdx.y + i];
-            }
-            __syncthreads();
-        }
-    }
-}
-
-cudaError_t launch_transpose(const void* B, int64_t K, int64_t N, int esize, void* Bt, int64_t ldt,
-                             cudaStream_t stream) {
-    if (K <= 0 || N <= 0) return cudaSuccess;
-    int64_t gx = (N + 31) / 32, gy = (K + 31) / 32;
-    if (gx > 65535) gx = 65535;
-    if (gy > 65535) gy = 65535;
-    const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), block(32, 8);
-    if (esize != 4) return cudaErrorInvalidValue;  // only tf32 B is transposed
-    transpose_kernel<float><<<grid, block, 0, stream>>>(static_cast<const float*>(B), K, N,
-                                                        static_cast<float*>(Bt), ldt);
-    return cudaGetLastError();
-}
-
 // im2col for channels-last convolution: row m = (n, p, q) of A holds the
 // receptive field of output pixel (n, p, q) in (r, s, c) order, c fastest:
 //   A[m][(r*S + s)*C + c] = x[n][p*stride - pad + r][q*stride - pad + s][c]

@@ -184,11 +184,9 @@ struct TcCfg {
     static constexpr int kABytes = kBlockMCta * 128;
     static constexpr int kBAtoms = (kBnCta + kAtomCols - 1) / kAtomCols;  // B swizzle atoms loaded
     static constexpr int kBAtomBytes = kBK * 128;          // kAtomCols columns x kBK k-rows
-    // 16-bit and 8-bit B is read MN-major in swizzle atoms (kAtomCols
-    // columns of 128 B rows); tf32 B comes transposed (N x K) and is read
-    // K-major: kBnCta rows of 128 B.
-    static constexpr bool kBKMajor = kElem == 4;
-    static constexpr int kBBytes = kBKMajor ? kBnCta * 128 : kBAtoms * kBAtomBytes;
+    // B is read MN-major in swizzle atoms of kAtomCols columns (128 B rows)
+    // by kBK k-rows, straight from the row-major matrix, for every dtype.
+    static constexpr int kBBytes = kBAtoms * kBAtomBytes;
     static constexpr int kChunks = (BN + 63) / 64;         // epilogue chunks of 64 columns
     static constexpr bool kHalfLast = (BN % 64) != 0;      // the last chunk is 32 columns
     static constexpr int kStageBytes = kABytes + kBBytes;
@@ -232,6 +230,15 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
            (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
            (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) |
            (1ull << 46) | (2ull << 61);
+}
+
+// MN-major tf32 B: descriptor layout 1 (128-byte swizzle, 32-byte atomicity),
+// LBO = distance between 32-column atoms, SBO = 512 B between 4-row cores.
+__device__ __forceinline__ uint64_t sdesc_mn_tf32(uint32_t saddr, uint32_t lbo) {
+    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+           (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+           (static_cast<uint64_t>((512u >> 4) & 0x3FFFu) << 32) |
+           (1ull << 46) | (1ull << 61);
 }
 
 template <int kDt>
@@ -350,14 +357,12 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 const TcParams p) {
 #if defined(__CUDA_ARCH__) && defined(__CUDA_ARCH_FEAT_SM103_ALL)
     using Cfg = TcCfg<CG, BN, elem_bytes(kDt)>;
-    // kind::tf32 takes both operands K-major (an MN-major tf32 operand
-    // multiplies as zero on this GPU): the host hands B over transposed,
-    // N x K, and one TMA box per stage brings the CTA's kBnCta rows of it.
-    // kind::f8f6f4 reads 8-bit B MN-major straight from the row-major
-    // matrix, as kind::f16 does (checked exactly on this GPU).
-    constexpr bool kBKMajor = Cfg::kBKMajor;
-    static_assert(kBKMajor == (kDt == 2), "K-major B for tf32 only");
-    static_assert(!kBKMajor || (Cfg::kBnCta * 128 == Cfg::kBBytes && MC == 1), "K-major B box");
+    // B is MN-major for every kind. kind::f16 and kind::f8f6f4 read it in the
+    // 128-byte swizzle (descriptor layout 2). kind::tf32 reads an MN-major
+    // operand only in the 128-byte swizzle with 32-byte atomicity (layout 1:
+    // 4-row cores of 128 B rows whose 32-byte units sit at unit ^ (row % 4);
+    // layout 2 multiplies as zero), which TMA writes with
+    // CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B. Both checked exactly on this GPU.
     constexpr int S = Cfg::kStages;
     constexpr int kCluster = CG * MC;
     static_assert(MC == 1 || (CG == 2 && MC == 2 && Cfg::kBAtoms == 2), "B multicast across pairs");
@@ -476,21 +481,15 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                             mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
                             if (p.im2col) tma_load_im2col_4d(a_dst, &tmA, fb, ic, iw, ih, in_, ow, oh);
                             else tma_load_2d(a_dst, &tmA, fb, k0, m0);
-                            if constexpr (kBKMajor) {
-                                tma_load_2d(b_dst, &tmB, fb, k0, n0);
-                            } else {
 #pragma unroll
-                                for (int j = 0; j < Cfg::kBAtoms; ++j)
-                                    tma_load_2d(b_dst + j * Cfg::kBAtomBytes, &tmB, fb, n0 + Cfg::kAtomCols * j, k0);
-                            }
+                            for (int j = 0; j < Cfg::kBAtoms; ++j)
+                                tma_load_2d(b_dst + j * Cfg::kBAtomBytes, &tmB, fb, n0 + Cfg::kAtomCols * j, k0);
                         } else {
                             const uint32_t fb_leader = mapa_shared(fb, leader);
                             if (rank == 0) mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
                             if (p.im2col) tma_load_im2col_4d_pair(a_dst, &tmA, fb_leader, ic, iw, ih, in_, ow, oh);
                             else tma_load_2d_pair(a_dst, &tmA, fb_leader, k0, m0);
-                            if constexpr (kBKMajor) {
-                                tma_load_2d_pair(b_dst, &tmB, fb_leader, k0, n0);
-                            } else if constexpr (MC == 1) {
+                            if constexpr (MC == 1) {
 #pragma unroll
                                 for (int j = 0; j < Cfg::kBAtoms; ++j)
                                     tma_load_2d_pair(b_dst + j * Cfg::kBAtomBytes, &tmB, fb_leader,
@@ -537,9 +536,9 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             const long long t_span0 = clock64();
 #endif
             const uint64_t a_desc0 = sdesc_sw128(sA, 16u, 1024u);
-            // MN-major B: atoms kBAtomBytes apart; K-major B (tf32): rows of
-            // 128 B like A.
-            const uint64_t b_desc0 = kBKMajor ? sdesc_sw128(sB, 16u, 1024u)
+            // MN-major B: atoms kBAtomBytes apart (tf32 in the 32-byte-atom
+            // layout, the others in the 128-byte swizzle).
+            const uint64_t b_desc0 = kDt == 2 ? sdesc_mn_tf32(sB, Cfg::kBAtomBytes)
                                               : sdesc_sw128(sB, Cfg::kBAtomBytes, 1024u);
             WorkUnit wu;
             for (int it = 0; next_unit(p.sched, cluster_id, it, wu); ++it) {
@@ -586,7 +585,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 #pragma unroll
                         for (int kk = 0; kk < Cfg::kBK / Cfg::kUK; ++kk) {
                             if constexpr (kDt == 2)
-                                umma_tf32<CG>(d_tmem, ad + 2u * kk, bd + 2u * kk, p.idesc, accum);
+                                umma_tf32<CG>(d_tmem, ad + 2u * kk, bd + 8u * Cfg::kUK * kk, p.idesc, accum);
                             else if constexpr (kDt >= 3)
                                 umma_f8<CG>(d_tmem, ad + 2u * kk, bd + 8u * Cfg::kUK * kk, p.idesc, accum);
                             else

@@ -51,10 +51,6 @@ int tc_tmem_cols(int cta_group, int block_n);
 cudaError_t launch_repack(const void* src, int64_t rows, int64_t cols, int esize, void* dst,
                           int64_t dst_ld, cudaStream_t stream);
 cudaError_t launch_zero(uint16_t* dst, int64_t count, cudaStream_t stream);
-// Bt (N x K, row pitch ldt elements) = B^T for the fp32 B (K x N, dense) of
-// tf32; `esize` must be 4.
-cudaError_t launch_transpose(const void* B, int64_t K, int64_t N, int esize, void* Bt, int64_t ldt,
-                             cudaStream_t stream);
 // Convolution geometry (channels-last): x N x H x W x C, filters R x S x C x K,
 // output N x P x Q x K.
 struct ConvShape {

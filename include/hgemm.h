@@ -289,8 +289,7 @@ typedef struct {
     int32_t smem_bytes;    /* dynamic shared memory per CTA */
     int32_t tmem_cols;     /* tensor-memory columns allocated per CTA */
     int32_t repack_a;      /* 1 if A goes through the 16-byte-pitch workspace */
-    int32_t repack_b;      /* 1 if B does (always for HGEMM_TF32: B is copied transposed,
-                              N x K, because kind::tf32 takes K-major operands) */
+    int32_t repack_b;      /* 1 if B does (B is otherwise read in place, MN-major, for every dtype) */
     int32_t store_mode;    /* 1 = TMA, 2 = plain, 3 = vector, 4 = staged vector stores */
     int32_t dp_tiles;      /* tiles computed whole, round-robin (the first dp_tiles in raster order) */
     int32_t sk_tiles;      /* tiles after them shared by stream-K ranges (0 = none) */

@@ -281,11 +281,13 @@ def test_plan_tf32(lib):
     assert p["stages"] == binding.plan(4096, 4096, 4096, "bf16", binding.Config(2, 256), sm_count=152)["stages"]
     # K = 1001 floats is not a 16-byte pitch: A is repacked; N = 1024 is
     assert binding.plan(64, 1024, 1001, "tf32", sm_count=152)["repack_a"] == 1
-    # B always goes through the workspace, transposed (N x K, K padded to 4)
+    # B is read in place (MN-major), unless its pitch is not 16-byte aligned
     tp = binding.plan(64, 1024, 1001, "tf32", sm_count=152)
-    assert tp["repack_b"] == 1 and tp["workspace_bytes"] >= 4 * 1024 * 1004
+    assert tp["repack_b"] == 0
+    assert binding.plan(4096, 4096, 4096, "tf32", sm_count=152)["workspace_bytes"] == 0
+    assert binding.plan(64, 1022, 1024, "tf32", sm_count=152)["repack_b"] == 1
     assert binding.plan(64, 1024, 1000, "tf32", sm_count=152)["repack_a"] == 0
-    # no B multicast for tf32 (its B is a transposed, K-major copy)
+    # B multicast across pairs is built for 16-bit B only
     with pytest.raises(binding.HgemmError):
         binding.plan(1024, 1024, 1024, "tf32", binding.Config(cta_group=2, block_n=256, multicast=2), sm_count=152)
     # an unknown dtype code is refused by the library itself
@@ -294,7 +296,7 @@ def test_plan_tf32(lib):
 
 
 def test_plan_fp8(lib):
-    # 8-bit operands: 128 K values per 128-byte stage row; B transposed
+    # 8-bit operands: 128 K values per 128-byte stage row; B read in place
     for code in (binding.HGEMM_E4M3, binding.HGEMM_E5M2):
         p = binding.plan(4096, 4096, 4096, code, sm_count=152)
         # the 256-wide pair tile (the 224-wide one, which fills 8-bit B atoms

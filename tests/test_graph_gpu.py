@@ -4,8 +4,7 @@ replay after replay, with the operands changed between replays (the graph
 holds pointers, not values). The cases cover the launches a graph must carry
 besides the GEMM kernel: the stream-K phase (its partial-sum marks are
 cleared by the captured call), the pool's workspace allocation, the
-16-byte-pitch repack, the B transpose of the TF32 path and the explicit
-im2col matrix; the no-alloc entry point captures with its fixed array."""
+16-byte-pitch repack and the explicit im2col matrix; the no-alloc entry point captures with its fixed array."""
 
 import pytest
 import torch

@@ -102,11 +102,11 @@ def test_noalloc_aligned_shape_with_stream_k(lib, mode):
 
 @pytest.mark.parametrize("dtype", ["tf32", "e4m3"])
 def test_other_dtypes_in_scratch(lib, dtype):
-    # tf32 always stages B (transposed) in the workspace; fp8 reads B in place
-    # unless its row pitch is not a multiple of 16 bytes (N = 776): here the
-    # workspace is the fixed scratch array
+    # B is read in place unless its row pitch is not a multiple of 16 bytes
+    # (N = 770 floats, 776 bytes): then it is repacked, here into the fixed
+    # scratch array
     import numpy as np
-    M, N, K = 512, (768 if dtype == "tf32" else 776), 1024
+    M, N, K = 512, (770 if dtype == "tf32" else 776), 1024
     assert hg.plan(M, N, K, dtype)["repack_b"] == 1
     if dtype == "tf32":
         A = torch.randn(M, K, device="cuda")
