@@ -351,10 +351,11 @@ void choose_shape(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dt, int sms, in
         if (cg == 2 && M <= 128) continue;
         if (!valid_shape_config(cg, bn, dt)) continue;
         // 8-bit B is read MN-major in 128-column atoms, which a CTA's 112
-        // columns of a 224-wide pair tile fill badly: measured 0.82 of the
-        // 256-wide tile's rate per flop (E4M3 8192^3: 2982 against 3649
-        // TFLOP/s; 4096^3: 2308 against 2725), against 0.97 for 16-bit. The
-        // planner leaves it out for fp8 (a config can still ask for it).
+        // columns of a 224-wide pair tile leave part-full: E4M3 4096^3 runs
+        // 51.6 us with 224-wide tiles on all SMs against 49.4 us with 256-wide
+        // ones on 128 (the part-full atom loaded whole: 59.4 us; 8192^3 then
+        // 2982 against 3649 TFLOP/s). The planner leaves it out for fp8 (a
+        // config can still ask for it).
         if (is_fp8(dt) && cg == 2 && bn == 224) continue;
         // A single tile row on a long K loop is HBM-bound, which the time
         // model above (compute-bound tiles) does not see: the narrowest tile
@@ -614,9 +615,14 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
         }
     }
 
-    CUtensorMap ta, tb, tc, tc32;
+    CUtensorMap ta, tb, tb2, tc, tc32;
+    std::memset(&tb2, 0, sizeof(tb2));
     std::memset(&tc, 0, sizeof(tc));
     std::memset(&tc32, 0, sizeof(tc32));
+    // A CTA's B columns (bn / cg) in 128-byte swizzle atoms; a part-full
+    // last atom is loaded with a box of its used columns only.
+    const int64_t atom_cols = 128 / es, bn_cta = bn / cg;
+    const int64_t b_last = bn_cta - ((bn_cta + atom_cols - 1) / atom_cols - 1) * atom_cols;
     // A boxes: 128 rows x one 128-byte row of K; B boxes: bk k-rows x one
     // 128-byte swizzle atom of columns (tf32 B in the 32-byte-atom swizzle,
     // which is how kind::tf32 reads an MN-major operand); C boxes: 32 rows x
@@ -627,6 +633,10 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
         (st = encode_2d(&tb, dtype, b_use, K, N, ldb, ubk, ubk,
                         dtype == HGEMM_TF32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B)) !=
             HGEMM_OK ||
+        (b_last != atom_cols &&
+         (st = encode_2d(&tb2, dtype, b_use, K, N, ldb, static_cast<uint32_t>(b_last), ubk,
+                         dtype == HGEMM_TF32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B)) !=
+             HGEMM_OK) ||
         (pl.store_mode == 1 &&
          (st = encode_2d(&tc, c_dtype_of(dtype), C, M, N, N, static_cast<uint32_t>(128 / ces), hg::kEpiBoxRows)) !=
              HGEMM_OK) ||
@@ -705,11 +715,11 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
         return cuda_fail(e, "status word");
     }
 
-    e = dtype == HGEMM_BF16   ? hg::launch_tc_bf16(cg, bn, mc, ta, tb, tc, tc32, p, clusters, stream)
-        : dtype == HGEMM_TF32 ? hg::launch_tc_tf32(cg, bn, mc, ta, tb, tc, tc32, p, clusters, stream)
-        : is_fp8(dtype)       ? hg::launch_tc_fp8(static_cast<int>(dtype), cg, bn, mc, ta, tb, tc, tc32, p, clusters,
+    e = dtype == HGEMM_BF16   ? hg::launch_tc_bf16(cg, bn, mc, ta, tb, tc, tc32, tb2, p, clusters, stream)
+        : dtype == HGEMM_TF32 ? hg::launch_tc_tf32(cg, bn, mc, ta, tb, tc, tc32, tb2, p, clusters, stream)
+        : is_fp8(dtype)       ? hg::launch_tc_fp8(static_cast<int>(dtype), cg, bn, mc, ta, tb, tc, tc32, tb2, p, clusters,
                                                   stream)
-                            : hg::launch_tc_f16(cg, bn, mc, ta, tb, tc, tc32, p, clusters, stream);
+                            : hg::launch_tc_f16(cg, bn, mc, ta, tb, tc, tc32, tb2, p, clusters, stream);
     if (work && work != scratch) cudaFreeAsync(work, stream);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     return HGEMM_OK;

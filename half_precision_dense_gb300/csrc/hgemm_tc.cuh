@@ -196,7 +196,13 @@ struct TcCfg {
     static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
     static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiBytes + kBarBytes;
     static constexpr int kTmemCols = pow2_at_least(2 * BN);  // two accumulators of BN fp32 columns
-    static constexpr uint32_t kTxBytes = CG * kStageBytes; // bytes landing per stage on the leader's barrier
+    // Columns of the last B atom a CTA uses (112 of a 224-wide pair tile's
+    // columns leave it part-full); it is loaded with a box of that width, so a
+    // stage brings only the bytes the MMA reads.
+    static constexpr int kBLastCols = kBnCta - (kBAtoms - 1) * kAtomCols;
+    static constexpr bool kBPartial = kBLastCols != kAtomCols;
+    static constexpr int kBLoadBytes = (kBAtoms - 1) * kBAtomBytes + kBK * kBLastCols * kElem;
+    static constexpr uint32_t kTxBytes = CG * (kABytes + kBLoadBytes); // bytes landing per stage on the leader's barrier
     static_assert(CG == 1 || CG == 2, "cta group");
     static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "tile width");
     static_assert(kBnCta % 16 == 0, "MMA N per CTA");
@@ -354,6 +360,7 @@ template <int CG, int BN, int kDt, int MC>
 __global__ void __launch_bounds__(kThreads, 1)
 hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC32,
+                const __grid_constant__ CUtensorMap tmB2,
                 const TcParams p) {
 #if defined(__CUDA_ARCH__) && defined(__CUDA_ARCH_FEAT_SM103_ALL)
     using Cfg = TcCfg<CG, BN, elem_bytes(kDt)>;
@@ -365,7 +372,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     // CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B. Both checked exactly on this GPU.
     constexpr int S = Cfg::kStages;
     constexpr int kCluster = CG * MC;
-    static_assert(MC == 1 || (CG == 2 && MC == 2 && Cfg::kBAtoms == 2), "B multicast across pairs");
+    static_assert(MC == 1 || (CG == 2 && MC == 2 && Cfg::kBAtoms == 2 && !Cfg::kBPartial), "B multicast across pairs");
     static_assert(S >= 2, "the two producers take alternate stages");
 
     extern __shared__ uint8_t smem_raw[];
@@ -413,6 +420,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     if (warp == kProducerWarp && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if (Cfg::kBPartial) tma_prefetch_desc(&tmB2);
         if (p.store_mode == 1) tma_prefetch_desc(&tmC);
         if (p.store_mode == 1 && Cfg::kHalfLast && kDt != 2) tma_prefetch_desc(&tmC32);  // 16-bit C only
     }
@@ -483,7 +491,9 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                             else tma_load_2d(a_dst, &tmA, fb, k0, m0);
 #pragma unroll
                             for (int j = 0; j < Cfg::kBAtoms; ++j)
-                                tma_load_2d(b_dst + j * Cfg::kBAtomBytes, &tmB, fb, n0 + Cfg::kAtomCols * j, k0);
+                                tma_load_2d(b_dst + j * Cfg::kBAtomBytes,
+                                            (Cfg::kBPartial && j == Cfg::kBAtoms - 1) ? &tmB2 : &tmB, fb,
+                                            n0 + Cfg::kAtomCols * j, k0);
                         } else {
                             const uint32_t fb_leader = mapa_shared(fb, leader);
                             if (rank == 0) mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
@@ -492,7 +502,9 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                             if constexpr (MC == 1) {
 #pragma unroll
                                 for (int j = 0; j < Cfg::kBAtoms; ++j)
-                                    tma_load_2d_pair(b_dst + j * Cfg::kBAtomBytes, &tmB, fb_leader,
+                                    tma_load_2d_pair(b_dst + j * Cfg::kBAtomBytes,
+                                                     (Cfg::kBPartial && j == Cfg::kBAtoms - 1) ? &tmB2 : &tmB,
+                                                     fb_leader,
                                                      n0 + Cfg::kAtomCols * j, k0);
                             } else {
                                 // Atom `pair` of this B half, for this CTA and its

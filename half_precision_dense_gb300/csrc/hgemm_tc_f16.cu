@@ -4,9 +4,9 @@
 namespace hg {
 
 cudaError_t launch_tc_f16(int cta_group, int block_n, int mc, const CUtensorMap& a, const CUtensorMap& b,
-                          const CUtensorMap& c, const CUtensorMap& c32, const TcParams& p, int clusters,
+                          const CUtensorMap& c, const CUtensorMap& c32, const CUtensorMap& b2, const TcParams& p, int clusters,
                           cudaStream_t stream) {
-    HG_TC_DISPATCH(0, launch(a, b, c, c32, p, clusters, stream))
+    HG_TC_DISPATCH(0, launch(a, b, c, c32, b2, p, clusters, stream))
     return cudaErrorInvalidValue;
 }
 

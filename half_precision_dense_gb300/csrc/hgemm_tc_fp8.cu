@@ -4,12 +4,12 @@
 namespace hg {
 
 cudaError_t launch_tc_fp8(int kind, int cta_group, int block_n, int mc, const CUtensorMap& a,
-                          const CUtensorMap& b, const CUtensorMap& c, const CUtensorMap& c32,
+                          const CUtensorMap& b, const CUtensorMap& c, const CUtensorMap& c32, const CUtensorMap& b2,
                           const TcParams& p, int clusters, cudaStream_t stream) {
     if (kind == 3) {
-        HG_TC_DISPATCH_F8(3, launch(a, b, c, c32, p, clusters, stream))
+        HG_TC_DISPATCH_F8(3, launch(a, b, c, c32, b2, p, clusters, stream))
     } else if (kind == 4) {
-        HG_TC_DISPATCH_F8(4, launch(a, b, c, c32, p, clusters, stream))
+        HG_TC_DISPATCH_F8(4, launch(a, b, c, c32, b2, p, clusters, stream))
     }
     return cudaErrorInvalidValue;
 }

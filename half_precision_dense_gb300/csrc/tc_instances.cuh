@@ -49,14 +49,14 @@ struct TcInstance {
     }
 
     static cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                              const CUtensorMap& c32, const TcParams& p, int clusters,
+                              const CUtensorMap& c32, const CUtensorMap& b2, const TcParams& p, int clusters,
                               cudaStream_t stream) {
         cudaError_t e = prepare();
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t cfg;
         cudaLaunchAttribute attr[1];
         fill_config(cfg, attr, clusters, stream);
-        return cudaLaunchKernelEx(&cfg, kernel(), a, b, c, c32, p);
+        return cudaLaunchKernelEx(&cfg, kernel(), a, b, c, c32, b2, p);
     }
 
     // Resident clusters per device, queried once per device.
