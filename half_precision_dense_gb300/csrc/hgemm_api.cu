@@ -846,6 +846,42 @@ hgemm_status_t hgemm_conv2d(const void* x, const void* w, void* y, int32_t N, in
     return st;
 }
 
+namespace {
+
+// Internal streams of hgemm_host, one set per device, created on first use and
+// kept for the process: copies in (B, then the bands of A), the band GEMMs,
+// and copies out (the bands of C).
+struct HostStreams {
+    cudaStream_t in = nullptr, compute = nullptr, out = nullptr;
+};
+
+hgemm_status_t host_streams(HostStreams* hs) {
+    static std::mutex mu;
+    static HostStreams cache[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return HGEMM_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lk(mu);
+    HostStreams& c = cache[dev];
+    if (!c.in) {
+        HostStreams n;
+        if ((e = cudaStreamCreateWithFlags(&n.in, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaStreamCreateWithFlags(&n.compute, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaStreamCreateWithFlags(&n.out, cudaStreamNonBlocking)) != cudaSuccess) {
+            if (n.in) cudaStreamDestroy(n.in);
+            if (n.compute) cudaStreamDestroy(n.compute);
+            if (n.out) cudaStreamDestroy(n.out);
+            return cuda_fail(e, "cudaStreamCreateWithFlags");
+        }
+        c = n;
+    }
+    *hs = c;
+    return HGEMM_OK;
+}
+
+}  // namespace
+
 hgemm_status_t hgemm_host(const void* hA, const void* hB, void* hC, int64_t M, int64_t N,
                           int64_t K, hgemm_dtype_t dtype, void* dA, void* dB, void* dC,
                           void* stream) {
@@ -860,16 +896,83 @@ hgemm_status_t hgemm_host(const void* hA, const void* hB, void* hC, int64_t M, i
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     const int64_t es = esize_of(dtype), ces = c_esize_of(dtype);
-    if (K > 0) {
-        if ((e = cudaMemcpyAsync(dA, hA, static_cast<size_t>(es * M * K), cudaMemcpyHostToDevice, s)) != cudaSuccess)
-            return cuda_fail(e, "copy A to device");
-        if ((e = cudaMemcpyAsync(dB, hB, static_cast<size_t>(es * K * N), cudaMemcpyHostToDevice, s)) != cudaSuccess)
-            return cuda_fail(e, "copy B to device");
+    // Row bands of A and C: band i's copy in, GEMM and copy out run on three
+    // streams, so copies of later bands overlap earlier bands' GEMMs and the
+    // copies out overlap the copies in (the two directions of the host link,
+    // about 190 and 180 GB/s on GB300, whatever the number of streams). The
+    // copies in set the pace; what is left after them is the last band's GEMM
+    // and copy out. Four bands, multiples of 256 rows and at least 512
+    // (4096^3: 1 band 0.594 ms, 2 bands 0.494, 4 bands 0.462, 8 bands 0.474).
+    // Small problems take one band.
+    int64_t bands = (M >= 1024 && K > 0) ? 4 : 1;
+    int64_t band_rows = (M + bands - 1) / bands;
+    band_rows = (band_rows + 255) / 256 * 256;
+    if (band_rows < 512) band_rows = bands > 1 ? 512 : M;
+    if (band_rows > M) band_rows = M;
+    bands = (M + band_rows - 1) / band_rows;
+    HostStreams hs;
+    if ((st = host_streams(&hs)) != HGEMM_OK) return st;
+    cudaEvent_t ev[2 * 8 + 2];
+    const int n_ev = static_cast<int>(2 * bands + 2);
+    for (int i = 0; i < n_ev; ++i) {
+        if ((e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming)) != cudaSuccess) {
+            for (int j = 0; j < i; ++j) cudaEventDestroy(ev[j]);
+            return cuda_fail(e, "cudaEventCreateWithFlags");
+        }
     }
-    if ((st = run(dA, dB, dC, M, N, K, dtype, nullptr, s)) != HGEMM_OK) return st;
-    if ((e = cudaMemcpyAsync(hC, dC, static_cast<size_t>(ces * M * N), cudaMemcpyDeviceToHost, s)) != cudaSuccess)
-        return cuda_fail(e, "copy C to host");
-    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "stream synchronize");
+    // On an error part of the pipeline may be enqueued: let it finish before
+    // the events go and the caller reuses its buffers.
+    auto drain = [&]() {
+        cudaStreamSynchronize(hs.in);
+        cudaStreamSynchronize(hs.compute);
+        cudaStreamSynchronize(hs.out);
+        for (int j = 0; j < n_ev; ++j) cudaEventDestroy(ev[j]);
+    };
+    auto fail = [&](cudaError_t err, const char* what) {
+        drain();
+        return cuda_fail(err, what);
+    };
+    // everything starts after the work already on `stream`
+    cudaEvent_t ev_start = ev[2 * bands], ev_end_out = ev[2 * bands + 1];
+    if ((e = cudaEventRecord(ev_start, s)) != cudaSuccess) return fail(e, "cudaEventRecord");
+    if ((e = cudaStreamWaitEvent(hs.in, ev_start, 0)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(hs.compute, ev_start, 0)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(hs.out, ev_start, 0)) != cudaSuccess)
+        return fail(e, "cudaStreamWaitEvent");
+    if (K > 0 &&
+        (e = cudaMemcpyAsync(dB, hB, static_cast<size_t>(es * K * N), cudaMemcpyHostToDevice, hs.in)) != cudaSuccess)
+        return fail(e, "copy B to device");
+    for (int64_t i = 0; i < bands; ++i) {
+        const int64_t r0 = i * band_rows, rows = (r0 + band_rows <= M) ? band_rows : M - r0;
+        cudaEvent_t ev_in = ev[2 * i], ev_done = ev[2 * i + 1];
+        if (K > 0 && (e = cudaMemcpyAsync(static_cast<uint8_t*>(dA) + es * r0 * K,
+                                          static_cast<const uint8_t*>(hA) + es * r0 * K,
+                                          static_cast<size_t>(es * rows * K), cudaMemcpyHostToDevice, hs.in)) !=
+                         cudaSuccess)
+            return fail(e, "copy A to device");
+        if ((e = cudaEventRecord(ev_in, hs.in)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(hs.compute, ev_in, 0)) != cudaSuccess)
+            return fail(e, "band event");
+        if ((st = run(static_cast<const uint8_t*>(dA) + es * r0 * K, dB, static_cast<uint8_t*>(dC) + ces * r0 * N,
+                      rows, N, K, dtype, nullptr, hs.compute)) != HGEMM_OK) {
+            drain();  // keeps run()'s error message
+            return st;
+        }
+        if ((e = cudaEventRecord(ev_done, hs.compute)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(hs.out, ev_done, 0)) != cudaSuccess)
+            return fail(e, "band event");
+        if ((e = cudaMemcpyAsync(static_cast<uint8_t*>(hC) + ces * r0 * N,
+                                 static_cast<const uint8_t*>(dC) + ces * r0 * N,
+                                 static_cast<size_t>(ces * rows * N), cudaMemcpyDeviceToHost, hs.out)) != cudaSuccess)
+            return fail(e, "copy C to host");
+    }
+    // `stream` resumes after the last copy out (which follows every band)
+    if ((e = cudaEventRecord(ev_end_out, hs.out)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(s, ev_end_out, 0)) != cudaSuccess)
+        return fail(e, "join");
+    e = cudaStreamSynchronize(s);
+    for (int j = 0; j < n_ev; ++j) cudaEventDestroy(ev[j]);
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
     return HGEMM_OK;
 }
 

@@ -262,10 +262,16 @@ hgemm_status_t hgemm_fp8_ex(const void* A, const void* B, void* C, const float* 
  * hgemm_host - the same product for operands in HOST memory.
  *
  * hA, hB: host operands; hC: host result. dA, dB, dC: caller-owned device
- * buffers of at least 2*M*K, 2*K*N and 2*M*N bytes. Enqueues on `stream`: the
- * copies hA->dA and hB->dB, hgemm(dA, dB, dC, ...), and the copy dC->hC; then
- * synchronises `stream`, so hC holds the result when it returns HGEMM_OK.
- * Host buffers should be page-locked for the copies to overlap other work.
+ * buffers of at least M*K, K*N and M*N elements of the operand / result
+ * type. After the work already enqueued on `stream`, it copies hB->dB and then,
+ * in row bands (up to 4 of at least 512 rows, for M >= 1024), copies each band
+ * of hA into dA,
+ * multiplies it (hgemm on that band) and copies the band of dC back to hC:
+ * band copies in, band GEMMs and band copies out run on three internal streams
+ * (created once per device), so they overlap. It then makes `stream` wait for
+ * the last copy out and synchronises it, so hC holds the result when it
+ * returns HGEMM_OK. Host buffers should be page-locked for the copies to run
+ * asynchronously. Concurrent calls share the internal streams.
  */
 hgemm_status_t hgemm_host(const void* hA, const void* hB, void* hC, int64_t M, int64_t N,
                           int64_t K, hgemm_dtype_t dtype, void* dA, void* dB, void* dC,

@@ -270,6 +270,33 @@ def test_host_entry_point():
     assert r["ok"], r
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_host_entry_point_in_bands(dtype):
+    # M = 4100: four row bands (three of 1280 rows and one of 260), each copied
+    # in, multiplied and copied out on the internal streams; work already on
+    # the caller's stream (a long fill of dC) runs first
+    M, N, K = 4100, 384, 256
+    A, B = operands(M, N, K, dtype, 17)
+    hA, hB = A.pin_memory(), B.pin_memory()
+    t = torch.bfloat16 if dtype == "bf16" else torch.float16
+    hC = torch.empty((M, N), dtype=t).pin_memory()
+    dA = torch.empty_like(A, device="cuda")
+    dB = torch.empty_like(B, device="cuda")
+    dC = torch.empty((M, N), dtype=t, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        torch.cuda._sleep(2_000_000)
+        dC.fill_(7)
+        hg.hgemm_host(hA, hB, hC, M, N, K, dtype, dA, dB, dC, s)
+    a, b = inputs.bits(A), inputs.bits(B)
+    ref64 = oracle.gemm_f64(a, b, dtype)
+    r = compare(inputs.bits(hC), oracle.round_rne(ref64, dtype), ref64, dtype, K)
+    assert r["ok"], r
+    # K = 0: every band writes zeros
+    hg.hgemm_host(hA, hB, hC, M, N, 0, dtype, dA, dB, dC)
+    assert bool((hC == 0).all())
+
+
 def test_matmul_wrapper_and_stream():
     A, B = operands(256, 192, 320, "f16", 13)
     s = torch.cuda.Stream()
