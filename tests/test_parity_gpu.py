@@ -270,12 +270,14 @@ def test_host_entry_point():
     assert r["ok"], r
 
 
+@pytest.mark.parametrize("M", [4100, 1100])
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
-def test_host_entry_point_in_bands(dtype):
-    # M = 4100: four row bands (three of 1280 rows and one of 260), each copied
-    # in, multiplied and copied out on the internal streams; work already on
-    # the caller's stream (a long fill of dC) runs first
-    M, N, K = 4100, 384, 256
+def test_host_entry_point_in_bands(dtype, M):
+    # M = 4100: four row bands (three of 1280 rows and one of 260); M = 1100:
+    # three (512, 512 and 76). Each band is copied in, multiplied and copied
+    # out on the internal streams; work already on the caller's stream (a
+    # long fill of dC) runs first
+    N, K = 384, 256
     A, B = operands(M, N, K, dtype, 17)
     hA, hB = A.pin_memory(), B.pin_memory()
     t = torch.bfloat16 if dtype == "bf16" else torch.float16
