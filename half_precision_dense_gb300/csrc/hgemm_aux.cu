@@ -221,7 +221,8 @@ cudaError_t status_word_ptr(unsigned long long** out) {
 }
 
 // Stage counts and shared-memory bytes per (cta_group, block_n, operand
-// bytes): K-major B (tf32, fp8) of narrow tiles needs less of the ring.
+// bytes): a B swizzle atom is 128 bytes of columns, so the stage size of a
+// narrow tile depends on the operand size.
 #define HG_CFG_SWITCH(FIELD)                                                                   \
     if (esize == 2) {                                                                          \
         if (cta_group == 1 && block_n == 64) return TcCfg<1, 64, 2>::FIELD;                    \

@@ -1,6 +1,8 @@
 // hgemm_tc.cuh - the persistent, warp-specialised tcgen05 GEMM kernel for
-// sm_103a: C = A.B, A (M x K) and B (K x N) row-major fp16/bf16, fp32
-// accumulation in tensor memory, C rounded to the input dtype.
+// sm_103a: C = A.B, A (M x K) and B (K x N) row-major, fp32 accumulation in
+// tensor memory. fp16/bf16 operands give C in the input dtype; the tf32 and
+// fp8 kinds (fp32 C; scaled bf16 C) and the implicit-GEMM convolution (A read
+// by TMA im2col copies) are instances of the same template.
 //
 // Prior art: "[CUDA 优化实战] hgemm - 超越 cuBLAS" builds the same product on an
 // RTX 5060 mobile from cp.async + ldmatrix + mma.sync m16n8k16 (section 1),
@@ -14,18 +16,19 @@
 //   double buffer                            an S-stage full/empty mbarrier ring
 //   mma.sync m16n8k16, fp32 in registers     tcgen05.mma kind::f16, fp32 in tensor memory
 //   grid swizzle (SWIZZLE_W)                 persistent CTAs walking a grouped raster
-//   Cs staging + SWIZZLE_C + float4 stores   tcgen05.ld -> cvt.rn -> swizzled smem -> TMA store
+//   Cs staging + SWIZZLE_C + float4 stores   tcgen05.ld -> cvt.rn -> swizzled smem -> row stores
 //
 // Roles (352 threads, one CTA per SM):
 //   warps 0-7  epilogue: warp w reads TMEM lanes 32(w % 4)..+31 (C rows of the
 //              tile) and every other 64-column chunk, starting at chunk w / 4
-//   warps 8,10 producers: one thread each issues the TMA loads of A and B for
-//              alternate stages (even / odd K blocks)
-//   warp 9     MMA: allocates TMEM; one thread of the leader CTA issues tcgen05.mma
+//   warps 8,10 producers: each warp takes alternate stages (even / odd K
+//              blocks); one elected lane issues the TMA loads of A and B
+//   warp 9     MMA: allocates TMEM; in the leader CTA the warp runs the loop and
+//              one elected lane issues tcgen05.mma and the commits
 //
 // CTA pairs (CG = 2, a cluster of two): the pair owns a 256-row tile. Each CTA
 // loads its own 128 rows of A and its own half of the tile's B columns; the
-// leader's single thread issues tcgen05.mma.cta_group::2, which reads both
+// leader's elected lane issues tcgen05.mma.cta_group::2, which reads both
 // CTAs' shared memory and accumulates each CTA's 128 rows in that CTA's TMEM.
 //
 // Every wait is bounded (TcParams::timeout_ns). A wait that runs out records
@@ -71,9 +74,9 @@ enum : uint32_t { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3 };
 struct TcParams {
     int32_t M, N, K;
     int32_t tiles_m, tiles_n, num_tiles, group_m;
-    int32_t num_kb;                 // ceil(K / kBlockK)
+    int32_t num_kb;                 // ceil(K / K per stage): 64 16-bit, 128 8-bit or 32 fp32 values
     uint32_t idesc;                 // tcgen05 instruction descriptor
-    int32_t store_mode;             // 1: TMA stores of C; 2: plain 2-byte stores through `C`;
+    int32_t store_mode;             // 1: TMA stores of C; 2: plain element stores through `C`;
                                     // 3: direct 16-byte stores through `C` (aligned C only);
                                     // 4: smem-staged, coalesced 16-byte stores (aligned C only)
     uint16_t* C;                    // used by store modes 2-4 (fp32 elements for tf32)
