@@ -4,7 +4,8 @@ replay after replay, with the operands changed between replays (the graph
 holds pointers, not values). The cases cover the launches a graph must carry
 besides the GEMM kernel: the stream-K phase (its partial-sum marks are
 cleared by the captured call), the pool's workspace allocation, the
-16-byte-pitch repack and the explicit im2col matrix; the no-alloc entry point captures with its fixed array."""
+16-byte-pitch repack and the explicit im2col matrix. The no-alloc entry
+point captures with its fixed array."""
 
 import pytest
 import torch
@@ -87,8 +88,6 @@ def test_gemm_stream_k(mode):
     C = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
     check_graph(lambda s: hg.hgemm_ex(A, B, C, M, N, K, "bf16", cfg, s), (A, B), C,
                 lambda: (A.copy_(rnd((M, K), torch.bfloat16)), B.copy_(rnd((K, N), torch.bfloat16))))
-
-
 
 
 def test_gemm_unaligned_repack():
