@@ -252,6 +252,13 @@ double schedule_seconds(int cg, int bn, int64_t tiles, int64_t clusters, int64_t
 
 // Fill the schedule fields of `pl` (tiles already set) for `clusters`
 // resident clusters.
+// CTAs per cluster: a CTA pair, times the pairs sharing B, times the CTAs
+// splitting a tile's K loop.
+int64_t cluster_ctas(const hgemm_plan_t& pl) {
+    return static_cast<int64_t>(pl.cta_group) * (pl.multicast > 1 ? pl.multicast : 1) *
+           (pl.split_k > 1 ? pl.split_k : 1);
+}
+
 void schedule_plan(hgemm_plan_t* pl, int64_t clusters, int sk_mode, int64_t num_kb) {
     const int64_t tiles = pl->num_tiles;
     if (clusters < 1) clusters = 1;
@@ -278,7 +285,7 @@ void schedule_plan(hgemm_plan_t* pl, int64_t clusters, int sk_mode, int64_t num_
     pl->sk_tiles = static_cast<int32_t>(sk);
     pl->sk_blocks = static_cast<int32_t>(sk ? total / clusters : 0);
     pl->sk_extra = static_cast<int32_t>(sk ? total % clusters : 0);
-    pl->grid_ctas = static_cast<int32_t>(clusters * pl->cta_group * (pl->multicast > 1 ? pl->multicast : 1));
+    pl->grid_ctas = static_cast<int32_t>(clusters * cluster_ctas(*pl));
     pl->num_kb = static_cast<int32_t>(num_kb);
 }
 
@@ -336,6 +343,7 @@ double estimate_seconds(int64_t M, int64_t N, int64_t K, int cg, int bn, int64_t
     pl.cta_group = cg;
     pl.block_n = bn;
     pl.multicast = 1;
+    pl.split_k = 1;
     pl.num_tiles = static_cast<int32_t>(tiles);
     schedule_plan(&pl, clusters, 0, kb);
     return schedule_seconds(cg, bn, tiles, pl.grid_ctas / cg, kb, pl.sk_tiles);
@@ -379,17 +387,48 @@ void choose_shape(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dt, int sms, in
     *bn_out = bbn;
 }
 
+// The planner's K split: clusters of `s` single CTAs on 128-wide tiles when
+// the K loop is long (at least 128 blocks, 32 per CTA) and the tiles, s CTAs
+// each, still fit on the SMs; the widest such s of 4 and 2. Measured on GB300
+// (bf16, L2 flushed, against the planner's whole tiles): 128 x 4096 x 14336
+// 57.1 -> 40.7 us (split 4), 128 x 2048 x 8192 35.8 -> 25.9 (4), 1024 x 1024
+// x 8192 34.4 -> 29.2 (2), 128 x 8192 x 8192 45.1 -> 41.4 (2), 16 and 64 x
+// 8192 x 8192 -10 % (2); at K = 4096 a tie (128 x 4096 x 4096: 23.0 -> 22.5),
+// at K = 2048 a loss (128 x 8192 x 2048: 18.1 -> 20.4). 256-wide split tiles
+// measured slower than 128-wide ones on every shape tried.
+int auto_split(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dt, int sms) {
+    if (esize_of(dt) != 2) return 1;
+    const int64_t num_kb = cdiv(K, bk_of(dt));
+    if (num_kb < 128) return 1;
+    const int64_t tiles = cdiv(M, 128) * cdiv(N, 128);
+    for (int s : {4, 2})
+        if (tiles * s <= sms && num_kb / s >= 32) return s;
+    return 1;
+}
+
 hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dt, const hgemm_config_t* cfg, int sms,
-                         bool a_unaligned, bool b_unaligned, bool c_unaligned, hgemm_plan_t* pl) {
+                         bool a_unaligned, bool b_unaligned, bool c_unaligned, hgemm_plan_t* pl,
+                         bool allow_auto_split = true) {
     std::memset(pl, 0, sizeof(*pl));
     hgemm_config_t c{};
     if (cfg) c = *cfg;
     if (c.group_m < 0 || c.max_clusters < 0 || c.store_mode < 0 || c.store_mode > 4 || c.stream_k < 0 ||
-        c.stream_k > 4) {
+        c.stream_k > 4 || c.split_k < 0 || c.split_k > 8) {
         t_last_error = "negative or unknown config field";
         return HGEMM_ERR_INVALID_ARG;
     }
     int cg = c.cta_group, bn = c.block_n;
+    int split = c.split_k > 1 ? c.split_k : 1;
+    if (c.split_k == 0 && allow_auto_split && cg == 0 && bn == 0 && c.multicast <= 1 && c.stream_k <= 1 &&
+        c.max_clusters == 0) {
+        split = auto_split(M, N, K, dt, sms);
+        if (split > 1) bn = 128;
+    }
+    if (split > 1) {
+        // K split across a cluster: single CTAs, a tile of 128 or 256 columns
+        if (cg == 0) cg = 1;
+        if (bn == 0) bn = 256;
+    }
     if (cg == 0 || bn == 0) {
         int acg, abn;
         choose_shape(M, N, K, dt, sms, c.max_clusters, &acg, &abn);
@@ -411,9 +450,16 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dt, cons
         t_last_error = "multicast = 2 needs cta_group 2, block_n 256 and a 16-bit dtype";
         return HGEMM_ERR_INVALID_ARG;
     }
+    if (split > 1 && !((split == 2 || split == 4 || split == 8) && cg == 1 && (bn == 128 || bn == 256) &&
+                       bn / split >= 32 && esize_of(dt) == 2 && c.multicast <= 1 && c.stream_k <= 1)) {
+        t_last_error = "split_k needs 2, 4 or 8 with cta_group 1, block_n 128 or 256 (at least 32 columns per "
+                       "CTA), a 16-bit dtype, no multicast and no stream-K";
+        return HGEMM_ERR_INVALID_ARG;
+    }
     const int mc = c.multicast == 2 ? 2 : 1;
     pl->cta_group = cg;
     pl->multicast = mc;
+    pl->split_k = split;
     pl->block_m = 128 * cg * mc;
     pl->block_n = bn;
     pl->block_k = static_cast<int32_t>(bk_of(dt));
@@ -432,8 +478,14 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dt, cons
     const int32_t gm_default = operand_bytes <= 96.0 * 1024 * 1024 ? 2 : 8;
     pl->group_m = c.group_m > 0 ? c.group_m
                                 : (pl->tiles_m < gm_default ? (pl->tiles_m > 0 ? pl->tiles_m : 1) : gm_default);
-    int64_t clusters = sms / (cg * mc);
+    int64_t clusters = sms / cluster_ctas(*pl);
     if (c.max_clusters > 0 && c.max_clusters < clusters) clusters = c.max_clusters;
+    if (split > 1 && pl->num_tiles > clusters) {
+        // the K split's reduction reuses each CTA's stage ring: one tile per cluster
+        t_last_error = "split_k needs one cluster per tile: " + std::to_string(pl->num_tiles) + " tiles, " +
+                       std::to_string(clusters) + " clusters";
+        return HGEMM_ERR_INVALID_ARG;
+    }
     schedule_plan(pl, clusters, c.stream_k, cdiv(K, bk_of(dt)));
     pl->repack_a = a_unaligned ? 1 : 0;
     pl->repack_b = b_unaligned ? 1 : 0;
@@ -556,17 +608,41 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
     hgemm_plan_t pl;
     const bool a_bad = (lda_in > 0 || conv) ? false : misaligned16(A, K, es);
     const bool b_bad = misaligned16(B, N, es), c_bad = misaligned16(C, N, ces);
-    if ((st = make_plan(M, N, K, dtype, cfg, info.sms, a_bad, b_bad, c_bad, &pl)) != HGEMM_OK) return st;
+    if ((st = make_plan(M, N, K, dtype, cfg, info.sms, a_bad, b_bad, c_bad, &pl, !conv)) != HGEMM_OK) return st;
+    if (conv && pl.split_k > 1) {
+        t_last_error = "split_k is not built for the convolution";
+        return HGEMM_ERR_INVALID_ARG;
+    }
 
     // Resident clusters bound the persistent grid; re-plan the schedule if
-    // fewer fit than the planner assumed.
-    const int cg = pl.cta_group, bn = pl.block_n, mc = pl.multicast;
+    // fewer fit than the planner assumed. The kernel's cluster multiplier is
+    // the pairs sharing B, or the CTAs splitting K.
+    auto resident_clusters = [&](const hgemm_plan_t& q) {
+        const int qm = q.split_k > 1 ? q.split_k : q.multicast;
+        return dtype == HGEMM_BF16   ? hg::max_active_clusters_bf16(q.cta_group, q.block_n, qm)
+               : dtype == HGEMM_TF32 ? hg::max_active_clusters_tf32(q.cta_group, q.block_n, qm)
+               : is_fp8(dtype)       ? hg::max_active_clusters_fp8(static_cast<int>(dtype), q.cta_group, q.block_n, qm)
+                                     : hg::max_active_clusters_f16(q.cta_group, q.block_n, qm);
+    };
+    int resident = resident_clusters(pl);
+    if (pl.split_k > 1 && !(cfg && cfg->split_k > 1) && resident > 0 && resident < pl.num_tiles) {
+        // the planner's K split does not fit (fewer clusters resident than
+        // tiles): whole tiles instead
+        hgemm_config_t no_split{};
+        if (cfg) no_split = *cfg;
+        no_split.split_k = 1;
+        if ((st = make_plan(M, N, K, dtype, &no_split, info.sms, a_bad, b_bad, c_bad, &pl, false)) != HGEMM_OK)
+            return st;
+        resident = resident_clusters(pl);
+    }
+    const int cg = pl.cta_group, bn = pl.block_n, mc = pl.split_k > 1 ? pl.split_k : pl.multicast;
     const int64_t num_kb = cdiv(K, bk);
-    int resident = dtype == HGEMM_BF16   ? hg::max_active_clusters_bf16(cg, bn, mc)
-                   : dtype == HGEMM_TF32 ? hg::max_active_clusters_tf32(cg, bn, mc)
-                   : is_fp8(dtype)       ? hg::max_active_clusters_fp8(static_cast<int>(dtype), cg, bn, mc)
-                                         : hg::max_active_clusters_f16(cg, bn, mc);
     if (resident > 0 && resident < pl.grid_ctas / (cg * mc)) {
+        if (pl.split_k > 1) {
+            t_last_error = "split_k needs one cluster per tile: " + std::to_string(pl.num_tiles) + " tiles, " +
+                           std::to_string(resident) + " clusters of " + std::to_string(mc) + " fit";
+            return HGEMM_ERR_INVALID_ARG;
+        }
         schedule_plan(&pl, resident, cfg ? cfg->stream_k : 0, num_kb);
         pl.workspace_bytes = workspace_layout(pl, M, N, K, es).total;
     }
@@ -998,7 +1074,7 @@ hgemm_status_t hgemm_plan(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dtype,
 
 int32_t hgemm_work_unit(const hgemm_plan_t* plan, int32_t cluster, int32_t i, int32_t* tile,
                         int32_t* kb0, int32_t* kb1, int32_t* kind) {
-    const int32_t csize = plan ? plan->cta_group * (plan->multicast > 1 ? plan->multicast : 1) : 1;
+    const int32_t csize = plan ? static_cast<int32_t>(cluster_ctas(*plan)) : 1;
     if (!plan || plan->cta_group < 1 || cluster < 0 || cluster >= plan->grid_ctas / csize || i < 0 ||
         plan->num_kb < 1)
         return 0;

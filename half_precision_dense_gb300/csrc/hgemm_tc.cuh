@@ -31,6 +31,11 @@
 // leader's elected lane issues tcgen05.mma.cta_group::2, which reads both
 // CTAs' shared memory and accumulates each CTA's 128 rows in that CTA's TMEM.
 //
+// Larger clusters (MC > 1): two CTA pairs stacked along M that share B by
+// TMA multicast, or 2, 4 or 8 single CTAs that split one tile's K loop and
+// add their partial sums through distributed shared memory (the template's
+// comment gives the details).
+//
 // Every wait is bounded (TcParams::timeout_ns). A wait that runs out records
 // HGEMM_ERR_TIMEOUT with the role and barrier in the device status word, sets a
 // CTA-wide abort flag that ends the other roles' loops, lets in-flight copies
@@ -292,6 +297,40 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Wa
     return wait_slow(bar, parity, w, role, which);
 }
 
+// wait_bar for a barrier that peer CTAs arrive on with release semantics at
+// cluster scope: the wait acquires at cluster scope, so what they wrote into
+// this CTA's shared memory before arriving is visible after it. Whole warp,
+// lane 0's outcome.
+static __device__ __noinline__ bool wait_bar_cluster_warp(uint32_t bar, uint32_t parity, const Waiter& w,
+                                                          uint32_t role, uint32_t which) {
+    bool got = mbar_try_wait_cluster(bar, parity);
+    const uint64_t t0 = globaltimer_ns();
+    while (!got) {
+        for (int i = 0; i < 64 && !got; ++i) got = mbar_try_wait_cluster(bar, parity);
+        if (got || *w.abort) break;
+        if (globaltimer_ns() - t0 > w.timeout_ns) {
+            const unsigned long long info =
+                (static_cast<unsigned long long>(role) << 56) |
+                (static_cast<unsigned long long>(which & 0xFFu) << 48) |
+                (static_cast<unsigned long long>(blockIdx.x & 0xFFFFu) << 32);
+            atomicCAS(w.status, 0ull, info | kStatusTimeout);
+            *w.abort = 1;
+            break;
+        }
+    }
+    return __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+}
+
+// The K blocks [lo, hi) of a unit's range [kb0, kb1) that CTA `crank` of a
+// K-split cluster of `parts` multiplies: equal shares, the remainder spread
+// one block each over the later ranks.
+__device__ __forceinline__ void split_share(int32_t kb0, int32_t kb1, uint32_t crank, int parts, int32_t& lo,
+                                            int32_t& hi) {
+    const int32_t n = kb1 - kb0;
+    lo = kb0 + static_cast<int32_t>((static_cast<int64_t>(n) * crank) / parts);
+    hi = kb0 + static_cast<int32_t>((static_cast<int64_t>(n) * (crank + 1)) / parts);
+}
+
 // wait_bar for a whole warp: every lane waits, and lane 0's outcome is the
 // warp's (lanes could otherwise disagree when a wait runs out just as the
 // phase completes), so the warp's control flow stays uniform.
@@ -355,10 +394,15 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
     for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i]));
 }
 
-// MC = CTA pairs per cluster (CG = 2 only): with MC = 2 a cluster of four
-// stacks two pairs along M; they need the same B columns, so each CTA loads
-// only one of its two 64-column B atoms and multicasts it to the matching CTA
-// of the other pair (a quarter less operand traffic through L2).
+// MC > 1 makes clusters whose CTAs share an operand block through TMA
+// multicast. CG = 2, MC = 2: a cluster of four stacks two pairs along M; they
+// need the same B columns, so each CTA loads only one of its two 64-column B
+// atoms and multicasts it to the matching CTA of the other pair (a quarter
+// less operand traffic through L2). CG = 1, MC = 2, 4 or 8: the MC CTAs of a
+// cluster split one 128 x BN tile's K loop (split-K within the cluster) and
+// reduce their fp32 partial sums through distributed shared memory; that
+// puts MC SMs on each tile of a shape with too few tiles to fill the GPU
+// (a skinny M), each reading 1/MC of the operands.
 template <int CG, int BN, int kDt, int MC>
 __global__ void __launch_bounds__(kThreads, 1)
 hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -375,7 +419,16 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     // CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B. Both checked exactly on this GPU.
     constexpr int S = Cfg::kStages;
     constexpr int kCluster = CG * MC;
-    static_assert(MC == 1 || (CG == 2 && MC == 2 && Cfg::kBAtoms == 2 && !Cfg::kBPartial), "B multicast across pairs");
+    constexpr bool kSplit = CG == 1 && MC > 1;               // K split across the cluster
+    static_assert(MC == 1 || (CG == 2 && MC == 2 && Cfg::kBAtoms == 2 && !Cfg::kBPartial) ||
+                      (kSplit && (MC == 2 || MC == 4 || MC == 8)),
+                  "B multicast across pairs, or a K split across 2, 4 or 8 single CTAs");
+    // The split's reduction: 16-bit C, whole 64-column chunks, column slices
+    // of at least eight 16-byte units, every CTA's slice received in the ring.
+    static_assert(!kSplit || (kDt <= 1 && !Cfg::kHalfLast && BN / MC >= 32 &&
+                              kBlockMCta * BN * 4 <= S * Cfg::kStageBytes),
+                  "K split shapes");
+    static_assert(!kSplit || (2 * S + 7) * 8 + 8 + 8 * kEpiWarps + 24 <= Cfg::kBarBytes, "barrier area");
     static_assert(S >= 2, "the two producers take alternate stages");
 
     extern __shared__ uint8_t smem_raw[];
@@ -395,6 +448,9 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(smem + (bar_pre + 16 - base));
     volatile uint32_t* const abort_flag = tmem_slot + 1;
     const uint32_t bar_part = bar_pre + 24;                     // [kEpiWarps]
+    const uint32_t bar_rok = bar_part + 8 * kEpiWarps;          // K split: peers' rings free
+    const uint32_t bar_rdy = bar_rok + 8;                       // K split: all CTAs' sums landed
+    const uint32_t bar_sent = bar_rdy + 8;                      // K split: this CTA's warps sent
 
     const int warp = static_cast<int>(threadIdx.x >> 5);
     const uint32_t lane = threadIdx.x & 31u;
@@ -403,12 +459,16 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const uint32_t pair = crank / CG;                                   // pair in the cluster
     const uint32_t leader = pair * CG;                                  // the pair's MMA CTA
     const int cluster_id = static_cast<int>(blockIdx.x) / kCluster;
-    constexpr int kRowsPerUnit = kBlockMCta * kCluster;                 // C rows per work unit
+    constexpr int kRowsPerUnit = kSplit ? kBlockMCta : kBlockMCta * kCluster;  // C rows per work unit
+    // This CTA's first row within the unit.
+    const int32_t m_in_unit = kSplit ? 0 : static_cast<int32_t>(pair * CG + rank) * kBlockMCta;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, MC);  // each pair's MMA frees the stage
+            // every MMA that reads the stage frees it: both pairs' with B
+            // multicast, this CTA's own otherwise (a K split included)
+            mbar_init(bar_empty + 8 * s, kSplit ? 1 : MC);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bar_tfull + 8 * a, 1);
@@ -417,6 +477,11 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         mbar_init(bar_drain, 1);
         for (int a = 0; a < 2; ++a) mbar_init(bar_pre + 8 * a, kEpiWarps * CG);
         for (int e = 0; e < kEpiWarps; ++e) mbar_init(bar_part + 8 * e, 1);
+        if constexpr (kSplit) {
+            mbar_init(bar_rok, MC - 1);
+            mbar_init(bar_rdy, MC);
+            mbar_init(bar_sent, kEpiWarps);
+        }
         *abort_flag = 0;
         fence_mbarrier_init_cluster();
     }
@@ -456,9 +521,11 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 if (pid == 0) trace_stamp(p, lu, kTrProdFirst);
                 int32_t tm, tn;
                 tile_coord(wu.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-                const int32_t m0 = tm * kRowsPerUnit + static_cast<int32_t>(pair * CG + rank) * kBlockMCta;
+                const int32_t m0 = tm * kRowsPerUnit + m_in_unit;
                 const int32_t n0 = tn * BN + static_cast<int32_t>(rank) * Cfg::kBnCta;
-                for (int kb = wu.kb0; kb < wu.kb1; ++kb, ++g) {
+                int32_t kb_lo = wu.kb0, kb_hi = wu.kb1;
+                if constexpr (kSplit) split_share(wu.kb0, wu.kb1, crank, MC, kb_lo, kb_hi);
+                for (int kb = kb_lo; kb < kb_hi; ++kb, ++g) {
                     if ((g & 1u) != pid) continue;
                     HG_TW_BEGIN();
                     const bool got = wait_bar_warp(bar_empty + 8 * stage, phase ^ 1u, w, kRoleProducer, stage);
@@ -579,7 +646,9 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 // An owner's first MMA adds to the preloaded partial sums.
                 uint32_t accum = wu.kind == 1 ? 1u : 0u;
-                for (int kb = wu.kb0; kb < wu.kb1; ++kb) {
+                int32_t kb_lo = wu.kb0, kb_hi = wu.kb1;
+                if constexpr (kSplit) split_share(wu.kb0, wu.kb1, crank, MC, kb_lo, kb_hi);
+                for (int kb = kb_lo; kb < kb_hi; ++kb) {
                     HG_TW_BEGIN();
                     const bool got_full = wait_bar_warp(bar_full + 8 * stage, phase, w, kRoleMma, stage);
                     HG_TW_END(tw_full);
@@ -589,7 +658,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     }
                     tc_fence_after();
                     ++n_stages;
-                    if (kb == wu.kb0) trace_stamp(p, it, kTrMmaFirst);
+                    if (kb == kb_lo) trace_stamp(p, it, kTrMmaFirst);
                     // Descriptor start addresses are in 16-byte units: stage s
                     // adds s * stage bytes / 16; each MMA step (32 bytes of K)
                     // moves 32 bytes along A's swizzled rows and kUK rows of
@@ -739,10 +808,123 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             }
             int32_t tm, tn;
             tile_coord(wu.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-            const int32_t row0 = tm * kRowsPerUnit + static_cast<int32_t>(pair * CG + rank) * kBlockMCta +
-                                 quarter * kEpiBoxRows;
+            const int32_t row0 = tm * kRowsPerUnit + m_in_unit + quarter * kEpiBoxRows;
             const int32_t col0 = tn * BN;
             const uint32_t t_row = tmem_base + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
+            if constexpr (kSplit) {
+                // K split across the cluster (one tile per cluster): each CTA
+                // holds the fp32 sum over its share of the K blocks. CTA j owns
+                // the tile's columns [j S, (j + 1) S), S = BN / MC, and receives
+                // every CTA's partial sums of them in its stage ring, idle once
+                // its MMAs are done: block q (the sender's rank) of 128 rows x S
+                // floats, 16-byte unit u of row r at unit u ^ (r % 8), so the
+                // 8 lanes of each store phase cover the 32 banks once.
+                constexpr uint32_t kSliceCols = BN / MC;
+                constexpr uint32_t kRowBytes = kSliceCols * 4u;
+                constexpr uint32_t kBlockBytes = kBlockMCta * kRowBytes;
+                constexpr int kUnitsPerRow = static_cast<int>(kSliceCols / 4u);
+                int32_t kb_lo, kb_hi;
+                split_share(wu.kb0, wu.kb1, crank, MC, kb_lo, kb_hi);
+                // 1. This CTA's MMAs have completed (tmem_full): its ring may
+                //    be written by the peers.
+                if (warp == 0 && lane == 0) {
+                    for (uint32_t q = 0; q < static_cast<uint32_t>(MC); ++q)
+                        if (q != crank) mbar_arrive_cluster(mapa_shared(bar_rok, q));
+                }
+                // 2. Once every peer's ring is free, send each owner its columns.
+                bool ok = wait_bar_cluster_warp(bar_rok, 0, w, kRoleEpilogue, 96);
+                const uint32_t r = static_cast<uint32_t>(quarter * 32) + lane;    // tile row
+                for (int c = colhalf; c < Cfg::kChunks && ok; c += 2) {
+                    uint32_t r0[32], r1[32];
+                    tmem_ld_32x32b_x32(t_row + 64u * c, r0);
+                    tmem_ld_32x32b_x32(t_row + 64u * c + 32u, r1);
+                    tmem_ld_wait();
+                    reg_fence(r0);
+                    reg_fence(r1);
+                    if (kb_hi == kb_lo) {
+                        // no K block in this CTA's share: its partial sum is zero
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            r0[i] = 0u;
+                            r1[i] = 0u;
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const uint32_t col = 64u * static_cast<uint32_t>(c) + 4u * static_cast<uint32_t>(j);
+                        const uint32_t owner_cta = col / kSliceCols;
+                        const uint32_t u = (col % kSliceCols) / 4u;
+                        const uint32_t off = crank * kBlockBytes + r * kRowBytes + ((u ^ (r & 7u)) << 4);
+                        const uint32_t* v = j < 8 ? r0 + 4 * j : r1 + 4 * (j - 8);
+                        st_cluster_v4(mapa_shared(sA + off, owner_cta), __uint_as_float(v[0]), __uint_as_float(v[1]),
+                                      __uint_as_float(v[2]), __uint_as_float(v[3]));
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    release_accumulator<CG>(bar_tempty + 8 * acc, leader);
+                    // 3. This warp's parts are sent (release at cluster scope).
+                    if (ok) mbar_arrive_cluster(mapa_shared(bar_sent, crank));
+                }
+                // Warp 0 collects the eight warps' arrivals (a bounded wait: a
+                // warp that gave up never arrives) and publishes the CTA's parts
+                // to every CTA of the cluster, this one included: its own warps
+                // read the block that its other warps wrote.
+                if (warp == 0) {
+                    const bool sent = wait_bar_cluster_warp(bar_sent, 0, w, kRoleEpilogue, 98);
+                    if (sent && lane == 0) {
+                        fence_acq_rel_cluster();
+                        for (uint32_t q = 0; q < static_cast<uint32_t>(MC); ++q)
+                            mbar_arrive_cluster(mapa_shared(bar_rdy, q));
+                    }
+                    ok = ok && sent;
+                }
+                // 4. Every CTA's block of this CTA's columns is in: sum the
+                //    blocks in rank order (the same order on every run), round,
+                //    store.
+                ok = wait_bar_cluster_warp(bar_rdy, 0, w, kRoleEpilogue, 97) && ok;
+                if (ok) {
+                    const int32_t row_base = tm * kBlockMCta;
+                    const int32_t col_base = col0 + static_cast<int32_t>(crank * kSliceCols);
+#pragma unroll 1
+                    for (int f = warp * 32 + static_cast<int>(lane); f < kBlockMCta * kUnitsPerRow;
+                         f += kEpiWarps * 32) {
+                        const uint32_t rr = static_cast<uint32_t>(f / kUnitsPerRow);
+                        const uint32_t u = static_cast<uint32_t>(f % kUnitsPerRow);
+                        const uint32_t off = rr * kRowBytes + ((u ^ (rr & 7u)) << 4);
+                        float4 acc4 = ld_shared_f4(sA + off);
+#pragma unroll
+                        for (int q = 1; q < MC; ++q) {
+                            const float4 t = ld_shared_f4(sA + static_cast<uint32_t>(q) * kBlockBytes + off);
+                            acc4.x += t.x;
+                            acc4.y += t.y;
+                            acc4.z += t.z;
+                            acc4.w += t.w;
+                        }
+                        const int32_t row = row_base + static_cast<int32_t>(rr);
+                        const int32_t col = col_base + 4 * static_cast<int32_t>(u);
+                        if (row < p.M && col < p.N) {
+                            const uint32_t lo = pack_rn<kDt>(__float_as_uint(acc4.x), __float_as_uint(acc4.y));
+                            const uint32_t hi = pack_rn<kDt>(__float_as_uint(acc4.z), __float_as_uint(acc4.w));
+                            uint16_t* dst = p.C + static_cast<int64_t>(row) * p.ldc + col;
+                            if (p.store_mode != 2 && col + 4 <= p.N) {
+                                // C 16-byte aligned with a 16-byte pitch, col a
+                                // multiple of 4: an 8-byte aligned store
+                                *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
+                            } else {
+                                const uint16_t e4[4] = {static_cast<uint16_t>(lo & 0xFFFFu), static_cast<uint16_t>(lo >> 16),
+                                                        static_cast<uint16_t>(hi & 0xFFFFu), static_cast<uint16_t>(hi >> 16)};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e)
+                                    if (col + e < p.N) dst[e] = e4[e];
+                            }
+                        }
+                    }
+                }
+                if (warp == 0 && lane == 0) trace_stamp(p, it, kTrEpiEnd);
+                continue;
+            }
             const bool is_split = wu.kind != 0;
             const bool owner = wu.kind != 2;
             if (colhalf >= Cfg::kChunks) {

@@ -212,6 +212,16 @@ uint64_t hgemm_noalloc_scratch_bytes(void);
  *                  0 = planner's choice, 1 = one pair, 2 = two pairs stacked
  *                  along M that load their shared B columns once, by TMA
  *                  multicast (tiles of 512 rows).
+ *   split_k:       CTAs per cluster that split each tile's K loop: 0 =
+ *                  planner's choice, 1 = none, 2, 4 or 8 = a cluster of that
+ *                  many single CTAs (cta_group 1, block_n 128 or 256, at least
+ *                  32 columns per CTA; 16-bit dtypes; no stream-K or
+ *                  multicast) per tile. CTA r multiplies K blocks
+ *                  [r n / s, (r + 1) n / s) of the tile's n; the fp32 partial
+ *                  sums meet through distributed shared memory and each CTA
+ *                  adds all of them, in rank order, for 1/s of the tile's
+ *                  columns. Needs a cluster per tile (HGEMM_ERR_INVALID_ARG
+ *                  otherwise).
  */
 typedef struct {
     int32_t cta_group;
@@ -221,6 +231,7 @@ typedef struct {
     int32_t store_mode;
     int32_t stream_k;
     int32_t multicast;
+    int32_t split_k;
 } hgemm_config_t;
 
 /* hgemm with an explicit configuration (cfg may be NULL = all zero). */
@@ -291,7 +302,7 @@ typedef struct {
     int32_t tiles_m;       /* ceil(M / block_m) */
     int32_t tiles_n;       /* ceil(N / block_n) */
     int32_t num_tiles;     /* tiles_m * tiles_n */
-    int32_t grid_ctas;     /* CTAs launched (a multiple of cta_group) */
+    int32_t grid_ctas;     /* CTAs launched (a multiple of cta_group * multicast * split_k) */
     int32_t smem_bytes;    /* dynamic shared memory per CTA */
     int32_t tmem_cols;     /* tensor-memory columns allocated per CTA */
     int32_t repack_a;      /* 1 if A goes through the 16-byte-pitch workspace */
@@ -304,6 +315,7 @@ typedef struct {
     int32_t sk_extra;
     int32_t num_kb;        /* 64-deep K blocks per tile: ceil(K / 64) */
     int32_t multicast;     /* CTA pairs per cluster sharing B by multicast (1 = none) */
+    int32_t split_k;       /* CTAs per cluster splitting a tile's K loop (1 = none) */
     int64_t workspace_bytes; /* stream-ordered workspace: repacked operands + fp32 partials */
 } hgemm_plan_t;
 

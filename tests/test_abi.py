@@ -146,10 +146,14 @@ def test_plan_stream_k(lib):
         off = binding.plan(4096, 4096, 4096, "bf16",
                            binding.Config(cta_group=2, block_n=256, stream_k=mode), sm_count=152)
         assert (off["sk_tiles"], off["dp_tiles"], off["grid_ctas"], off["workspace_bytes"]) == (0, 256, 128, 0)
-    # a single tile row on a long K loop: the narrowest one-CTA tiles that
-    # keep every tile in one wave, whole (the planner never picks stream-K)
+    # a single tile row on a long K loop: 128-wide one-CTA tiles, each K loop
+    # split over a cluster of two (the planner never picks stream-K)
     sk = binding.plan(128, 8192, 8192, "bf16", sm_count=152)
-    assert (sk["cta_group"], sk["block_n"], sk["sk_tiles"], sk["grid_ctas"]) == (1, 64, 0, 128)
+    assert (sk["cta_group"], sk["block_n"], sk["sk_tiles"], sk["grid_ctas"], sk["split_k"]) == (1, 128, 0, 128, 2)
+    # a shorter K loop: the narrowest one-CTA tiles that keep every tile in
+    # one wave, whole
+    sk = binding.plan(128, 8192, 4096, "bf16", sm_count=152)
+    assert (sk["cta_group"], sk["block_n"], sk["sk_tiles"], sk["grid_ctas"], sk["split_k"]) == (1, 64, 0, 128, 1)
     wide = binding.plan(128, 16384, 8192, "bf16", sm_count=152)
     assert (wide["cta_group"], wide["block_n"], wide["sk_tiles"]) == (1, 128, 0)
     # whole waves leave nothing to share; one K block leaves nothing to cut
@@ -170,7 +174,7 @@ def test_plan_stream_k(lib):
 
 
 def _check_schedule(p):
-    clusters = p["grid_ctas"] // (p["cta_group"] * p["multicast"])
+    clusters = p["grid_ctas"] // (p["cta_group"] * p["multicast"] * p["split_k"])
     kb = p["num_kb"]
     seen = {}
     units_of = {}
@@ -219,10 +223,53 @@ def _check_schedule(p):
     ((4096, 4096, 4096), dict(cta_group=2, block_n=256, multicast=2, stream_k=2), 152),
     ((4096, 4096, 4096), dict(cta_group=2, block_n=256, stream_k=4), 152),
     ((1024, 1280, 704), dict(cta_group=1, block_n=128, max_clusters=7, stream_k=4), 152),
+    ((128, 8192, 8192), dict(split_k=4), 152),
+    ((300, 1000, 704), dict(block_n=128, split_k=2), 152),
 ])
 def test_schedule_covers_every_block_once_without_wait_cycles(lib, shape, cfg, sms):
     p = binding.plan(*shape, "bf16", binding.Config(**cfg), sm_count=sms)
     _check_schedule(p)
+
+
+def test_plan_split_k_clusters(lib):
+    # split_k: a cluster of 2, 4 or 8 single CTAs per tile, one tile per cluster
+    p = binding.plan(128, 8192, 8192, "bf16", binding.Config(split_k=4), sm_count=152)
+    assert (p["cta_group"], p["block_m"], p["block_n"], p["split_k"], p["multicast"]) == (1, 128, 256, 4, 1)
+    assert (p["tiles_m"], p["tiles_n"], p["num_tiles"], p["grid_ctas"]) == (1, 32, 32, 128)
+    assert (p["sk_tiles"], p["workspace_bytes"]) == (0, 0)   # partial sums stay on chip
+    q = binding.plan(200, 1000, 300, "f16", binding.Config(block_n=128, split_k=2), sm_count=152)
+    assert (q["tiles_m"], q["tiles_n"], q["grid_ctas"]) == (2, 8, 32)
+    for c in range(q["grid_ctas"] // 2):
+        assert binding.work_units(q, c) == [(c, 0, 5, 0)]   # the whole K range; the CTAs share it
+    # the combinations that are not built, and too many tiles for one cluster each
+    for cfg, dt, shape in [(dict(split_k=3), "bf16", (128, 1024, 1024)),
+                           (dict(block_n=128, split_k=8), "bf16", (128, 1024, 1024)),
+                           (dict(block_n=64, split_k=2), "bf16", (128, 1024, 1024)),
+                           (dict(cta_group=2, block_n=256, split_k=2), "bf16", (128, 1024, 1024)),
+                           (dict(split_k=2), "tf32", (128, 1024, 1024)),
+                           (dict(split_k=2, stream_k=3), "bf16", (128, 1024, 1024)),
+                           (dict(split_k=2), "bf16", (4096, 4096, 4096))]:
+        with pytest.raises(binding.HgemmError):
+            binding.plan(*shape, dt, binding.Config(**cfg), sm_count=152)
+
+
+@pytest.mark.parametrize("shape,dtype,split", [
+    ((128, 4096, 14336), "bf16", 4),    # 32 tiles x 4 CTAs, 56 K blocks each
+    ((128, 2048, 8192), "f16", 4),
+    ((1024, 1024, 8192), "bf16", 2),    # 64 tiles: a split of 4 would need 256 SMs
+    ((128, 8192, 4096), "bf16", 1),     # 64 K blocks: too short a loop to split
+    ((8192, 8192, 8192), "bf16", 1),    # enough tiles already
+    ((128, 4096, 14336), "tf32", 1),    # 16-bit kinds only
+    ((128, 4096, 14336), "e4m3", 1),
+])
+def test_plan_auto_split(lib, shape, dtype, split):
+    p = binding.plan(*shape, dtype, sm_count=152)
+    assert p["split_k"] == split
+    if split > 1:
+        assert (p["cta_group"], p["block_n"]) == (1, 128)
+        assert p["grid_ctas"] == p["num_tiles"] * split <= 152
+    # a forced shape keeps whole tiles unless the split is asked for
+    assert binding.plan(*shape, dtype, binding.Config(cta_group=1, block_n=128), sm_count=152)["split_k"] == 1
 
 
 def test_plan_skinny_prefers_narrow_tiles(lib):

@@ -90,6 +90,17 @@ def test_gemm_stream_k(mode):
                 lambda: (A.copy_(rnd((M, K), torch.bfloat16)), B.copy_(rnd((K, N), torch.bfloat16))))
 
 
+@pytest.mark.parametrize("split,bn", [(4, 256), (2, 128)])
+def test_gemm_split_k(split, bn):
+    # the in-cluster K split: its barriers are initialised by each launch
+    M, N, K = 128, 2048, 4096
+    cfg = hg.Config(block_n=bn, split_k=split)
+    A, B = rnd((M, K), torch.bfloat16), rnd((K, N), torch.bfloat16)
+    C = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
+    check_graph(lambda s: hg.hgemm_ex(A, B, C, M, N, K, "bf16", cfg, s), (A, B), C,
+                lambda: (A.copy_(rnd((M, K), torch.bfloat16)), B.copy_(rnd((K, N), torch.bfloat16))))
+
+
 def test_gemm_unaligned_repack():
     # K = 1001: rows of A are not 16-byte multiples, so A is repacked in the
     # pool workspace inside the graph

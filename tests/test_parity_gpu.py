@@ -24,6 +24,7 @@ CONFIGS = [
     hg.Config(cta_group=2, block_n=224),
     hg.Config(cta_group=2, block_n=256),
     hg.Config(cta_group=2, block_n=256, multicast=2),
+
 ]
 CFG_IDS = ["cg1_n64", "cg1_n128", "cg1_n256", "cg2_n128", "cg2_n224", "cg2_n256", "cg2_n256_mc2"]
 
@@ -168,6 +169,43 @@ def test_planner_choices(shape, dtype):
     M, N, K = shape
     A, B = operands(M, N, K, dtype, 15)
     check_full(A, B, dtype)
+
+
+SPLITS = [(2, 128), (4, 128), (2, 256), (4, 256), (8, 256)]
+
+
+@pytest.mark.parametrize("split,bn", SPLITS, ids=[f"s{s}_n{b}" for s, b in SPLITS])
+@pytest.mark.parametrize("shape", [(128, 3072, 4096), (77, 1000, 2056), (1, 520, 4096), (200, 1536, 1000),
+                                   (129, 65, 63), (256, 1536, 2048)], ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_split_k(split, bn, shape, dtype):
+    # the K loop of each tile split over a cluster, the partial sums reduced
+    # through distributed shared memory: ragged M, N and K, a K shorter than
+    # the split (CTAs with no K block add zeros), several tile rows. At most
+    # 12 tiles under an 8-way split: 15 clusters of 8 fit on a 152-SM GB300.
+    M, N, K = shape
+    cfg = hg.Config(block_n=bn, split_k=split)
+    p = hg.plan(M, N, K, dtype, cfg)
+    assert p["split_k"] == split and p["grid_ctas"] == p["num_tiles"] * split
+    A, B = operands(M, N, K, dtype, 18)
+    check_full(A, B, dtype, cfg)
+
+
+@pytest.mark.parametrize("store_mode", [1, 2, 3, 4])
+def test_split_k_store_modes_and_repeat(store_mode):
+    # every store mode (the reduction writes C itself: 8-byte vectors, plain
+    # stores for mode 2), and the same bits on a second call
+    cfg = hg.Config(block_n=256, split_k=4, store_mode=store_mode)
+    A, B = operands(128, 2056, 3000, "bf16", 19)
+    got, _ = check_full(A, B, "bf16", cfg)
+    again, _ = check_full(A, B, "bf16", cfg)
+    assert np.array_equal(got, again)
+
+
+def test_split_k_unaligned_c():
+    # N = 1001: C rows are not 16-byte multiples, element stores only
+    A, B = operands(100, 1001, 2048, "f16", 20)
+    check_full(A, B, "f16", hg.Config(block_n=128, split_k=4))
 
 
 def test_stream_k_repeated_calls_reuse_workspace():
