@@ -39,7 +39,7 @@ UNIT = "TFLOP/s"
 L2_FLUSH_BYTES = 256 << 20
 # Bumped whenever the GEMM kernel or its default launch (store path) changes, so ncu figures taken on an older
 # kernel are not reported as current.
-KERNEL_REV = 14
+KERNEL_REV = 15
 
 # name -> list of (M, N, K, dtype, dist, sigma, seed) GEMMs making up one step
 WORKLOADS = {

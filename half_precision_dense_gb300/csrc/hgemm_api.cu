@@ -463,8 +463,8 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dt, cons
     pl->block_m = 128 * cg * mc;
     pl->block_n = bn;
     pl->block_k = static_cast<int32_t>(bk_of(dt));
-    pl->stages = hg::tc_stages(cg, bn, esize_of(dt));
-    pl->smem_bytes = hg::tc_smem_bytes(cg, bn, esize_of(dt));
+    pl->stages = hg::tc_stages(cg, bn, esize_of(dt), split);
+    pl->smem_bytes = hg::tc_smem_bytes(cg, bn, esize_of(dt), split);
     pl->tmem_cols = hg::tc_tmem_cols(cg, bn);
     pl->tiles_m = static_cast<int32_t>(cdiv(M, pl->block_m));
     pl->tiles_n = static_cast<int32_t>(cdiv(N, bn));

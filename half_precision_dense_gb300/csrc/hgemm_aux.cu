@@ -221,10 +221,14 @@ cudaError_t status_word_ptr(unsigned long long** out) {
 }
 
 // Stage counts and shared-memory bytes per (cta_group, block_n, operand
-// bytes): a B swizzle atom is 128 bytes of columns, so the stage size of a
-// narrow tile depends on the operand size.
+// bytes, K split): a B swizzle atom is 128 bytes of columns, so the stage
+// size of a narrow tile depends on the operand size; a K split has no
+// epilogue staging boxes.
 #define HG_CFG_SWITCH(FIELD)                                                                   \
-    if (esize == 2) {                                                                          \
+    if (esize == 2 && split > 1) {                                                             \
+        if (cta_group == 1 && block_n == 128) return TcCfg<1, 128, 2, 2>::FIELD;               \
+        if (cta_group == 1 && block_n == 256) return TcCfg<1, 256, 2, 2>::FIELD;               \
+    } else if (esize == 2) {                                                                   \
         if (cta_group == 1 && block_n == 64) return TcCfg<1, 64, 2>::FIELD;                    \
         if (cta_group == 1 && block_n == 128) return TcCfg<1, 128, 2>::FIELD;                  \
         if (cta_group == 1 && block_n == 256) return TcCfg<1, 256, 2>::FIELD;                  \
@@ -241,7 +245,7 @@ cudaError_t status_word_ptr(unsigned long long** out) {
     }                                                                                          \
     return 0;
 
-int tc_stages(int cta_group, int block_n, int esize) { HG_CFG_SWITCH(kStages) }
+int tc_stages(int cta_group, int block_n, int esize, int split) { HG_CFG_SWITCH(kStages) }
 
 int tc_tmem_cols(int cta_group, int block_n) {
     if (cta_group == 1 && block_n == 64) return TcCfg<1, 64>::kTmemCols;
@@ -253,6 +257,6 @@ int tc_tmem_cols(int cta_group, int block_n) {
     return 0;
 }
 
-int tc_smem_bytes(int cta_group, int block_n, int esize) { HG_CFG_SWITCH(kSmemBytes) }
+int tc_smem_bytes(int cta_group, int block_n, int esize, int split) { HG_CFG_SWITCH(kSmemBytes) }
 
 }  // namespace hg

@@ -183,7 +183,10 @@ constexpr int pow2_at_least(int x) {
     return p;
 }
 
-template <int CG, int BN, int kElem = 2>
+// kSplitK > 1: the K split within a cluster, whose epilogue adds the partial
+// sums in the stage ring and stores C from registers, so it needs no staging
+// boxes and the ring takes their space.
+template <int CG, int BN, int kElem = 2, int kSplitK = 1>
 struct TcCfg {
     static constexpr int kBK = 128 / kElem;                // K per stage: one 128 B row of A
     static constexpr int kUK = 32 / kElem;                 // K of one MMA (32 bytes of K)
@@ -198,8 +201,8 @@ struct TcCfg {
     static constexpr int kChunks = (BN + 63) / 64;         // epilogue chunks of 64 columns
     static constexpr bool kHalfLast = (BN % 64) != 0;      // the last chunk is 32 columns
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kEpiBytes = kEpiWarps * kEpiBoxBytes;  // one staging box per warp
-    static constexpr int kBarBytes = 256;
+    static constexpr int kEpiBytes = kSplitK > 1 ? 0 : kEpiWarps * kEpiBoxBytes;  // one staging box per warp
+    static constexpr int kBarBytes = kSplitK > 1 ? 512 : 256;  // a K split adds its three barriers
     static constexpr int kStagesFit = (kSmemLimit - 1024 - kEpiBytes - kBarBytes) / kStageBytes;
     static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
     static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiBytes + kBarBytes;
@@ -410,7 +413,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 const __grid_constant__ CUtensorMap tmB2,
                 const TcParams p) {
 #if defined(__CUDA_ARCH__) && defined(__CUDA_ARCH_FEAT_SM103_ALL)
-    using Cfg = TcCfg<CG, BN, elem_bytes(kDt)>;
+    using Cfg = TcCfg<CG, BN, elem_bytes(kDt), (CG == 1 && MC > 1) ? MC : 1>;
     // B is MN-major for every kind. kind::f16 and kind::f8f6f4 read it in the
     // 128-byte swizzle (descriptor layout 2). kind::tf32 reads an MN-major
     // operand only in the 128-byte swizzle with 32-byte atomicity (layout 1:

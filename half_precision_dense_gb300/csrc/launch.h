@@ -42,8 +42,8 @@ int max_active_clusters_fp8(int kind, int cta_group, int block_n, int mc);
 
 // Shared-memory ring depth and bytes of an instantiation (host constants) for
 // operands of `esize` bytes (2: fp16/bf16, 4: tf32, 1: fp8).
-int tc_stages(int cta_group, int block_n, int esize);
-int tc_smem_bytes(int cta_group, int block_n, int esize);
+int tc_stages(int cta_group, int block_n, int esize, int split);
+int tc_smem_bytes(int cta_group, int block_n, int esize, int split);
 int tc_tmem_cols(int cta_group, int block_n);
 
 // Auxiliary kernels (hgemm_aux.cu). The repack copies rows of `cols`

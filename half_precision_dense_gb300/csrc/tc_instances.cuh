@@ -13,7 +13,7 @@ template <int CG, int BN, int kDt, int MC = 1>
 struct TcInstance {
     // The kernel's own configuration (its operand size sets the stage bytes
     // and the ring depth), so the launch reserves the shared memory it uses.
-    using Cfg = TcCfg<CG, BN, elem_bytes(kDt)>;
+    using Cfg = TcCfg<CG, BN, elem_bytes(kDt), (CG == 1 && MC > 1) ? MC : 1>;
     static constexpr int kCluster = CG * MC;
     static constexpr auto kernel() { return &hgemm_tc_kernel<CG, BN, kDt, MC>; }
 
