@@ -209,16 +209,22 @@ constexpr double kStreamKFixupSec = 3.0e-6;
 // short problems (1024^3: single-CTA 128-wide tiles 12.7 us, pair tiles
 // 13.9 us; 768^3: 12.1 against 12.5 us).
 constexpr double kPairFixedSec = 1.0e-6;
-// Epilogue time per 64-column chunk of a CTA's 128-row tile (TMEM load,
-// conversion, staging, TMA store); a CTA pair hands tensor memory back across
-// the pair, which costs about half as much again. A tile takes at least this
-// long even when its K loop is short: the epilogue of one tile overlaps the
-// mainloop of the next, so the slower of the two sets the pace.
-constexpr double kEpiChunkSec = 0.45e-6;
+// Epilogue time of a tile: a fixed part (the accumulator hand-over, the
+// first TMEM load) plus a part per 64-column chunk that each epilogue warp
+// converts and stores (a CTA's 8 warps take its chunks two at a time); a CTA
+// pair hands tensor memory back across the pair, 1.6 times as long. A tile
+// takes at least this long even when its K loop is short: the epilogue of
+// one tile overlaps the mainloop of the next, so the slower of the two sets
+// the pace. Fitted on GB300 to K = 64 shapes with TMA stores of C (the
+// planner's store path for short K loops), per tile and wave: 1x64 1.08 us,
+// 1x128 1.18-1.23, 1x256 1.8-2.0, pair 256 1.83-1.98.
+constexpr double kEpiTileSec = 0.35e-6;
+constexpr double kEpiChunkSec = 0.8e-6;
 
 double tile_seconds(int cg, int bn, int64_t num_kb) {
     const double mainloop = 2.0 * 128 * bn * (num_kb * hg::kBlockK) / (kSmFlops * shape_efficiency(cg, bn));
-    const double epilogue = kEpiChunkSec * ((bn + 63) / 64) * (cg == 2 ? 1.5 : 1.0);
+    const int chunks_per_warp = ((bn / cg + 63) / 64 + 1) / 2;
+    const double epilogue = (kEpiTileSec + kEpiChunkSec * chunks_per_warp) * (cg == 2 ? 1.6 : 1.0);
     return mainloop > epilogue ? mainloop : epilogue;
 }
 
@@ -493,8 +499,12 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dt, cons
     // with 16-byte vector stores (4). They go out through the load/store path,
     // so they do not queue in the SM's TMA unit ahead of the next tile's
     // operand loads, as TMA tensor stores (1) do: measured 0.5-1 % faster at
-    // 4096^3 to 16384x14336x4096, in 33 of 36 interleaved pairs.
-    pl->store_mode = (c.store_mode != 0) ? c.store_mode : (c_unaligned ? 2 : 4);
+    // 4096^3 to 16384x14336x4096, in 33 of 36 interleaved pairs. A short K
+    // loop (at most 8 blocks) leaves the epilogue setting the pace, and there
+    // TMA stores are faster: 4096x4096x64 19.1 -> 16.6 us, 8192x8192x256
+    // 53.2 -> 46.7, 16384x16384x64 156 -> 105; even at 1024 (30.8 both).
+    const int64_t num_kb_plan = cdiv(K, bk_of(dt));
+    pl->store_mode = (c.store_mode != 0) ? c.store_mode : c_unaligned ? 2 : num_kb_plan <= 8 ? 1 : 4;
     if (c_unaligned && pl->store_mode != 2) {
         t_last_error = "vector and TMA stores need a 16-byte aligned C with a 16-byte row pitch";
         return HGEMM_ERR_INVALID_ARG;
