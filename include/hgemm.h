@@ -199,7 +199,9 @@ uint64_t hgemm_noalloc_scratch_bytes(void);
  *                  straight from registers, 4 = 16-byte vector stores of whole
  *                  rows read back from the swizzled smem box (1, 3 and 4 need
  *                  a 16-byte aligned C whose row pitch is a multiple of 16
- *                  bytes). The planner takes 4 for such a C, else 2.
+ *                  bytes). The planner takes 4 for such a C (1 when the K
+ *                  loop has at most 8 blocks: the epilogue then sets the
+ *                  pace, and TMA stores are faster), else 2.
  *   stream_k:      how the tiles past the last whole wave are shared:
  *                  0 = planner's choice; 1 = never (whole tiles only, spread
  *                  over as few clusters as keep the wave count); 2 = stream-K
