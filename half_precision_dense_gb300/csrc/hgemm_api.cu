@@ -1147,7 +1147,9 @@ void hgemm_trace_set(void* buf) { g_trace.store(static_cast<unsigned long long*>
 
 void hgemm_conv2d_set_mode(int32_t mode) { g_conv_implicit.store(mode == 0, std::memory_order_relaxed); }
 
-void hgemm_test_inject(int32_t kind) { g_inject.store(kind == 1 ? 1 : 0, std::memory_order_relaxed); }
+void hgemm_test_inject(int32_t kind) {
+    g_inject.store(kind == 1 || kind == 2 ? kind : 0, std::memory_order_relaxed);
+}
 
 const char* hgemm_status_string(hgemm_status_t s) {
     switch (s) {

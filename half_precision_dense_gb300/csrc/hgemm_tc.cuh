@@ -102,7 +102,7 @@ struct TcParams {
                                     // non-owning stream-K unit
     unsigned long long* flags;      // one per (partial block, column half): == epoch once written
     unsigned long long epoch;       // unique per launch (a captured launch clears the flags first)
-    int32_t inject;                 // test hook: 1 = stream-K owners wait for partial sums
+    int32_t inject;                 // test hook: 2 = a K-split cluster's rank 0 withholds an arrival; 1 = stream-K owners wait for partial sums
                                     // that are never published (the waits run out)
     unsigned long long* trace;      // timeline records (builds with HG_TRACE only), or null
 };
@@ -829,8 +829,9 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 int32_t kb_lo, kb_hi;
                 split_share(wu.kb0, wu.kb1, crank, MC, kb_lo, kb_hi);
                 // 1. This CTA's MMAs have completed (tmem_full): its ring may
-                //    be written by the peers.
-                if (warp == 0 && lane == 0) {
+                //    be written by the peers. Test hook: rank 0 never says so,
+                //    and its peers' waits run out.
+                if (warp == 0 && lane == 0 && !(p.inject == 2 && crank == 0)) {
                     for (uint32_t q = 0; q < static_cast<uint32_t>(MC); ++q)
                         if (q != crank) mbar_arrive_cluster(mapa_shared(bar_rok, q));
                 }

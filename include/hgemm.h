@@ -368,6 +368,11 @@ void hgemm_set_timeout_ns(uint64_t ns);
  * without the missing parts, and returns normally. An owner's unit is the last
  * of its CTA, so the waiting CTAs have no copies or MMAs in flight, and
  * nothing traps or hangs.
+ * kind 2: in each launch with a K split within clusters (split_k > 1), the
+ * first CTA of every cluster withholds its "ring free" arrival, so its peers'
+ * bounded waits run out. Each CTA records HGEMM_ERR_TIMEOUT, skips the rest
+ * of the reduction (C is left partly unwritten) and returns normally. By
+ * then every CTA's MMAs have completed, so nothing is in flight.
  */
 void hgemm_test_inject(int32_t kind);
 
