@@ -256,8 +256,6 @@ double schedule_seconds(int cg, int bn, int64_t tiles, int64_t clusters, int64_t
     return t + kFixedSec + (cg == 2 ? kPairFixedSec : 0.0);
 }
 
-// Fill the schedule fields of `pl` (tiles already set) for `clusters`
-// resident clusters.
 // CTAs per cluster: a CTA pair, times the pairs sharing B, times the CTAs
 // splitting a tile's K loop.
 int64_t cluster_ctas(const hgemm_plan_t& pl) {
@@ -265,6 +263,8 @@ int64_t cluster_ctas(const hgemm_plan_t& pl) {
            (pl.split_k > 1 ? pl.split_k : 1);
 }
 
+// Fill the schedule fields of `pl` (tiles already set) for `clusters`
+// resident clusters.
 void schedule_plan(hgemm_plan_t* pl, int64_t clusters, int sk_mode, int64_t num_kb) {
     const int64_t tiles = pl->num_tiles;
     if (clusters < 1) clusters = 1;
@@ -502,7 +502,8 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dt, cons
     // 4096^3 to 16384x14336x4096, in 33 of 36 interleaved pairs. A short K
     // loop (at most 8 blocks) leaves the epilogue setting the pace, and there
     // TMA stores are faster: 4096x4096x64 19.1 -> 16.6 us, 8192x8192x256
-    // 53.2 -> 46.7, 16384x16384x64 156 -> 105; even at 1024 (30.8 both).
+    // 53.2 -> 46.7, 16384x16384x64 156 -> 105. At K = 1024 the two modes
+    // tie (4096x4096x1024: 30.8 us each).
     const int64_t num_kb_plan = cdiv(K, bk_of(dt));
     pl->store_mode = (c.store_mode != 0) ? c.store_mode : c_unaligned ? 2 : num_kb_plan <= 8 ? 1 : 4;
     if (c_unaligned && pl->store_mode != 2) {

@@ -317,7 +317,9 @@ typedef struct {
     int32_t sk_extra;
     int32_t num_kb;        /* 64-deep K blocks per tile: ceil(K / 64) */
     int32_t multicast;     /* CTA pairs per cluster sharing B by multicast (1 = none) */
-    int32_t split_k;       /* CTAs per cluster splitting a tile's K loop (1 = none) */
+    int32_t split_k;       /* CTAs per cluster splitting a tile's K loop (1 = none). hgemm_plan
+                              assumes a cluster per tile fits; a launch whose planner-chosen
+                              split finds fewer clusters resident takes whole tiles instead */
     int64_t workspace_bytes; /* stream-ordered workspace: repacked operands + fp32 partials */
 } hgemm_plan_t;
 
