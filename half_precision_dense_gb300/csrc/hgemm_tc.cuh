@@ -102,8 +102,9 @@ struct TcParams {
                                     // non-owning stream-K unit
     unsigned long long* flags;      // one per (partial block, column half): == epoch once written
     unsigned long long epoch;       // unique per launch (a captured launch clears the flags first)
-    int32_t inject;                 // test hook: 2 = a K-split cluster's rank 0 withholds an arrival; 1 = stream-K owners wait for partial sums
-                                    // that are never published (the waits run out)
+    int32_t inject;                 // test hook: 1 = stream-K owners wait for partial sums
+                                    // that are never published; 2 = a K-split cluster's rank 0
+                                    // withholds its ring-free arrival (the waits run out)
     unsigned long long* trace;      // timeline records (builds with HG_TRACE only), or null
 };
 
@@ -325,8 +326,8 @@ static __device__ __noinline__ bool wait_bar_cluster_warp(uint32_t bar, uint32_t
 }
 
 // The K blocks [lo, hi) of a unit's range [kb0, kb1) that CTA `crank` of a
-// K-split cluster of `parts` multiplies: equal shares, the remainder spread
-// one block each over the later ranks.
+// K-split cluster of `parts` multiplies: contiguous shares in rank order,
+// equal to within one block.
 __device__ __forceinline__ void split_share(int32_t kb0, int32_t kb1, uint32_t crank, int parts, int32_t& lo,
                                             int32_t& hi) {
     const int32_t n = kb1 - kb0;
@@ -397,15 +398,14 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
     for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i]));
 }
 
-// MC > 1 makes clusters whose CTAs share an operand block through TMA
-// multicast. CG = 2, MC = 2: a cluster of four stacks two pairs along M; they
-// need the same B columns, so each CTA loads only one of its two 64-column B
-// atoms and multicasts it to the matching CTA of the other pair (a quarter
-// less operand traffic through L2). CG = 1, MC = 2, 4 or 8: the MC CTAs of a
-// cluster split one 128 x BN tile's K loop (split-K within the cluster) and
-// reduce their fp32 partial sums through distributed shared memory; that
-// puts MC SMs on each tile of a shape with too few tiles to fill the GPU
-// (a skinny M), each reading 1/MC of the operands.
+// MC > 1 makes larger clusters. CG = 2, MC = 2: a cluster of four stacks two
+// pairs along M; they need the same B columns, so each CTA loads only one of
+// its two 64-column B atoms and multicasts it to the matching CTA of the
+// other pair (a quarter less operand traffic through L2). CG = 1, MC = 2, 4
+// or 8: the MC CTAs of a cluster split one 128 x BN tile's K loop (split-K
+// within the cluster) and reduce their fp32 partial sums through distributed
+// shared memory; that puts MC SMs on each tile of a shape with too few tiles
+// to fill the GPU (a skinny M), each reading 1/MC of the tile's operands.
 template <int CG, int BN, int kDt, int MC>
 __global__ void __launch_bounds__(kThreads, 1)
 hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
