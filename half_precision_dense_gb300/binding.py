@@ -108,6 +108,8 @@ def load_library():
         lib.hgemm_work_unit.restype = i32
         lib.hgemm_tile_coord.argtypes = [i32, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
         lib.hgemm_tile_coord.restype = None
+        lib.hgemm_split_share.argtypes = [i32, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
+        lib.hgemm_split_share.restype = None
         lib.hgemm_get_device_status.argtypes = [i32, i32, ctypes.POINTER(ctypes.c_uint32)]
         lib.hgemm_get_device_status.restype = ctypes.c_int
         lib.hgemm_set_timeout_ns.argtypes = [ctypes.c_uint64]
@@ -262,6 +264,14 @@ def work_units(plan_dict: dict, cluster: int) -> list[tuple[int, int, int, int]]
         out.append(tuple(v.value for v in vals))
         i += 1
     return out
+
+
+def split_share(kb0: int, kb1: int, rank: int, parts: int) -> tuple[int, int]:
+    """K blocks [lo, hi) of [kb0, kb1) for rank `rank` of a K-split cluster of `parts`."""
+    lib = load_library()
+    a, b = ctypes.c_int32(-1), ctypes.c_int32(-1)
+    lib.hgemm_split_share(kb0, kb1, rank, parts, ctypes.byref(a), ctypes.byref(b))
+    return a.value, b.value
 
 
 def tile_coord(t: int, tiles_m: int, tiles_n: int, group_m: int) -> tuple[int, int]:

@@ -1113,6 +1113,14 @@ void hgemm_tile_coord(int32_t t, int32_t tiles_m, int32_t tiles_n, int32_t group
     if (tn) *tn = b;
 }
 
+void hgemm_split_share(int32_t kb0, int32_t kb1, int32_t rank, int32_t parts, int32_t* lo, int32_t* hi) {
+    if (!lo || !hi || parts < 1 || rank < 0 || rank >= parts || kb0 > kb1) return;
+    int32_t a, b;
+    hg::split_share(kb0, kb1, static_cast<uint32_t>(rank), parts, a, b);
+    *lo = a;
+    *hi = b;
+}
+
 hgemm_status_t hgemm_get_device_status(int32_t device, int32_t reset, uint32_t* info) {
     t_last_error.clear();
     int prev = 0;

@@ -325,16 +325,6 @@ static __device__ __noinline__ bool wait_bar_cluster_warp(uint32_t bar, uint32_t
     return __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
 }
 
-// The K blocks [lo, hi) of a unit's range [kb0, kb1) that CTA `crank` of a
-// K-split cluster of `parts` multiplies: contiguous shares in rank order,
-// equal to within one block.
-__device__ __forceinline__ void split_share(int32_t kb0, int32_t kb1, uint32_t crank, int parts, int32_t& lo,
-                                            int32_t& hi) {
-    const int32_t n = kb1 - kb0;
-    lo = kb0 + static_cast<int32_t>((static_cast<int64_t>(n) * crank) / parts);
-    hi = kb0 + static_cast<int32_t>((static_cast<int64_t>(n) * (crank + 1)) / parts);
-}
-
 // wait_bar for a whole warp: every lane waits, and lane 0's outcome is the
 // warp's (lanes could otherwise disagree when a wait runs out just as the
 // phase completes), so the warp's control flow stays uniform.

@@ -31,6 +31,15 @@ HG_HD void tile_coord(int32_t t, int32_t tiles_m, int32_t tiles_n, int32_t group
     tn = r / rows;
 }
 
+// The K blocks [lo, hi) of a unit's range [kb0, kb1) that rank `rank` of a
+// K-split cluster of `parts` CTAs multiplies: contiguous shares in rank
+// order, equal to within one block.
+HG_HD void split_share(int32_t kb0, int32_t kb1, uint32_t rank, int parts, int32_t& lo, int32_t& hi) {
+    const int32_t n = kb1 - kb0;
+    lo = kb0 + static_cast<int32_t>((static_cast<int64_t>(n) * rank) / parts);
+    hi = kb0 + static_cast<int32_t>((static_cast<int64_t>(n) * (rank + 1)) / parts);
+}
+
 // The schedule: tiles [0, dp_tiles) are data-parallel (cluster c takes tiles
 // c, c + C, c + 2C, ... whole); the remaining tiles [dp_tiles, num_tiles) are
 // stream-K: their K blocks, numbered g = (t - dp_tiles) * num_kb + kb, are cut

@@ -349,6 +349,15 @@ void hgemm_tile_coord(int32_t t, int32_t tiles_m, int32_t tiles_n, int32_t group
                       int32_t* tm, int32_t* tn);
 
 /*
+ * The K blocks [*lo, *hi) of a tile's range [kb0, kb1) that rank `rank` of a
+ * K-split cluster of `parts` CTAs multiplies (host copy of the device
+ * function; see hgemm_config_t.split_k): contiguous shares in rank order,
+ * equal to within one block. Leaves *lo and *hi untouched unless
+ * 0 <= rank < parts and kb0 <= kb1.
+ */
+void hgemm_split_share(int32_t kb0, int32_t kb1, int32_t rank, int32_t parts, int32_t* lo, int32_t* hi);
+
+/*
  * Device-side status word of `device`, set by a kernel whose bounded wait ran
  * out (HGEMM_ERR_TIMEOUT) and left unchanged otherwise. Call after the stream
  * that ran the GEMM has been synchronised. *info (may be NULL) receives the

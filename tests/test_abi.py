@@ -272,6 +272,25 @@ def test_plan_auto_split(lib, shape, dtype, split):
     assert binding.plan(*shape, dtype, binding.Config(cta_group=1, block_n=128), sm_count=152)["split_k"] == 1
 
 
+@pytest.mark.parametrize("n", [0, 1, 3, 7, 8, 63, 64, 127, 128, 224, 1001])
+@pytest.mark.parametrize("parts", [2, 4, 8])
+def test_split_share_partitions_the_k_range(lib, n, parts):
+    # the K split's shares (the kernel's own function): contiguous, in rank
+    # order, covering [kb0, kb1) exactly, sizes equal to within one block;
+    # with fewer blocks than CTAs some shares are empty (those CTAs add zeros)
+    kb0 = 5
+    shares = [binding.split_share(kb0, kb0 + n, r, parts) for r in range(parts)]
+    assert shares[0][0] == kb0 and shares[-1][1] == kb0 + n
+    for (lo, hi), (lo2, _) in zip(shares, shares[1:]):
+        assert lo <= hi == lo2
+    sizes = [hi - lo for lo, hi in shares]
+    assert max(sizes) - min(sizes) <= 1 and sum(sizes) == n
+    # out-of-range ranks and sizes leave the outputs untouched
+    assert binding.split_share(0, 10, parts, parts) == (-1, -1)
+    assert binding.split_share(0, 10, 0, 0) == (-1, -1)
+    assert binding.split_share(10, 0, 0, parts) == (-1, -1)
+
+
 def test_plan_skinny_prefers_narrow_tiles(lib):
     p = binding.plan(128, 8192, 8192, "bf16", sm_count=148)
     assert p["block_m"] == 128  # one tile row: no half-empty CTA pairs
