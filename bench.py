@@ -362,7 +362,8 @@ def run_ours(args, rank, world, local_rank):
     plan = hg.plan(o["M"], o["N"], o["K"], o["dt"])
     plan_key = [plan["cta_group"], plan["block_n"], plan["sk_tiles"], plan["grid_ctas"]]
     line["roofline"]["plan"] = {"cta_group": plan_key[0], "block_n": plan_key[1],
-                                "stream_k_tiles": plan_key[2], "grid_ctas": plan_key[3]}
+                                "stream_k_tiles": plan_key[2], "grid_ctas": plan_key[3],
+                                "split_k": plan["split_k"], "store_mode": plan["store_mode"]}
     if args.traffic_file and os.path.exists(args.traffic_file):
         # DRAM bytes from an ncu capture count only while the kernel and plan
         # they were taken on are the ones running now.
