@@ -636,13 +636,18 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
                                      : hg::max_active_clusters_f16(q.cta_group, q.block_n, qm);
     };
     int resident = resident_clusters(pl);
-    if (pl.split_k > 1 && !(cfg && cfg->split_k > 1) && resident > 0 && resident < pl.num_tiles) {
+    while (pl.split_k > 1 && !(cfg && cfg->split_k > 1) && resident > 0 && resident < pl.num_tiles) {
         // the planner's K split does not fit (fewer clusters resident than
-        // tiles): whole tiles instead
-        hgemm_config_t no_split{};
-        if (cfg) no_split = *cfg;
-        no_split.split_k = 1;
-        if ((st = make_plan(M, N, K, dtype, &no_split, info.sms, a_bad, b_bad, c_bad, &pl, false)) != HGEMM_OK)
+        // tiles; on a 152-SM GB300 32 clusters of 4 fit, not 38): the next
+        // smaller split on the same tiles, else whole tiles
+        hgemm_config_t smaller{};
+        if (cfg) smaller = *cfg;
+        smaller.split_k = pl.split_k / 2 > 1 ? pl.split_k / 2 : 1;
+        if (smaller.split_k > 1) {
+            smaller.cta_group = 1;
+            smaller.block_n = pl.block_n;
+        }
+        if ((st = make_plan(M, N, K, dtype, &smaller, info.sms, a_bad, b_bad, c_bad, &pl, false)) != HGEMM_OK)
             return st;
         resident = resident_clusters(pl);
     }

@@ -202,6 +202,17 @@ def test_split_k_store_modes_and_repeat(store_mode):
     assert np.array_equal(got, again)
 
 
+@pytest.mark.parametrize("shape", [(128, 4864, 8192), (100, 4736, 8200)])
+def test_split_k_planner_fallback(shape):
+    # the planner's split of 4 on 37-38 tiles: fewer clusters of 4 are
+    # resident than tiles, so the launch takes a split of 2 (or whole tiles)
+    M, N, K = shape
+    p = hg.plan(M, N, K, "bf16")
+    assert p["split_k"] == 4 and p["num_tiles"] * 4 <= 152 and p["num_tiles"] > 32
+    A, B = operands(M, N, K, "bf16", 21)
+    check_full(A, B, "bf16")
+
+
 def test_split_k_unaligned_c():
     # N = 1001: C rows are not 16-byte multiples, element stores only
     A, B = operands(100, 1001, 2048, "f16", 20)
