@@ -291,6 +291,23 @@ def test_split_share_partitions_the_k_range(lib, n, parts):
     assert binding.split_share(10, 0, 0, parts) == (-1, -1)
 
 
+@pytest.mark.parametrize("shape,store_mode,tile", [
+    ((4096, 4096, 64), 1, (1, 256)),      # one K block per tile: the epilogue sets the pace
+    ((8192, 8192, 64), 1, (2, 256)),
+    ((8192, 8192, 256), 1, (2, 256)),
+    ((16384, 16384, 64), 1, (2, 256)),
+    ((4096, 4096, 512), 1, (2, 224)),     # 8 blocks: still TMA stores
+    ((4096, 4096, 576), 4, (2, 224)),     # 9 blocks: row stores
+    ((4096, 4096, 4096), 4, (2, 224)),
+])
+def test_plan_short_k_uses_tma_stores(lib, shape, store_mode, tile):
+    p = binding.plan(*shape, "bf16", sm_count=152)
+    assert p["store_mode"] == store_mode and (p["cta_group"], p["block_n"]) == tile
+    # an unaligned C keeps plain stores; a forced mode is kept
+    assert binding.plan(shape[0], shape[1] + 1, shape[2], "bf16", sm_count=152)["store_mode"] == 2
+    assert binding.plan(*shape, "bf16", binding.Config(store_mode=3), sm_count=152)["store_mode"] == 3
+
+
 def test_plan_skinny_prefers_narrow_tiles(lib):
     p = binding.plan(128, 8192, 8192, "bf16", sm_count=148)
     assert p["block_m"] == 128  # one tile row: no half-empty CTA pairs
