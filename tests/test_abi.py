@@ -402,3 +402,65 @@ def test_plan_fp8(lib):
         binding.plan(1024, 1024, 1024, "tf32", binding.Config(cta_group=1, block_n=224), sm_count=152)
     # the fp8 entry point refuses other dtypes
     assert lib.hgemm_fp8(None, None, None, None, None, 0, 0, 0, 1, None) == 1
+
+
+# --- the K split's reduction layout, modelled on the CPU ---------------------
+
+SPLIT_SHAPES = [(128, 2), (128, 4), (256, 2), (256, 4), (256, 8)]
+
+
+def _split_slot(q, r, col, bn, parts):
+    """Owner CTA and byte offset in its ring of sender q's partial sum for tile
+    row r, columns col..col+3 (the kernel's push): owner col // S, block q of
+    128 rows x S floats, 16-byte unit u of row r at unit u ^ (r % 8)."""
+    s = bn // parts
+    u = (col % s) // 4
+    return col // s, q * 128 * s * 4 + r * s * 4 + ((u ^ (r & 7)) << 4)
+
+
+@pytest.mark.parametrize("bn,parts", SPLIT_SHAPES)
+def test_split_reduction_layout_covers_each_owner_block_once(bn, parts):
+    s = bn // parts
+    slots = {}
+    for q in range(parts):
+        for r in range(128):
+            for col in range(0, bn, 4):
+                owner, off = _split_slot(q, r, col, bn, parts)
+                assert 0 <= off < parts * 128 * s * 4 and off % 16 == 0
+                assert (owner, off) not in slots, "two partial sums in one slot"
+                slots[(owner, off)] = (q, r, col)
+    # every owner's region (parts blocks of 128 x S floats) is filled exactly
+    for owner in range(parts):
+        offs = sorted(off for (o, off) in slots if o == owner)
+        assert offs == list(range(0, parts * 128 * s * 4, 16))
+        # an owner receives only its own columns
+        assert all(slots[(owner, off)][2] // s == owner for off in offs)
+    # the region fits the ring of the split's tile (7 stages of 32 KiB for
+    # 128-wide tiles, 4 of 48 KiB for 256-wide ones)
+    ring = 7 * 32768 if bn == 128 else 4 * 49152
+    assert parts * 128 * s * 4 <= ring
+
+
+@pytest.mark.parametrize("bn,parts", SPLIT_SHAPES)
+def test_split_reduction_layout_is_bank_conflict_free(bn, parts):
+    s = bn // parts
+    # pushes: lane l of a warp holds tile row r0 + l and stores one 16-byte
+    # unit of the same columns; each 8-lane phase must cover the 32 banks once
+    for r0 in (0, 32, 64, 96):
+        for col in range(0, bn, 4):
+            for phase in range(4):
+                banks = []
+                for l in range(8 * phase, 8 * phase + 8):
+                    _, off = _split_slot(0, r0 + l, col, bn, parts)
+                    banks.extend(bank_of(off + 4 * w) for w in range(4))
+                assert sorted(banks) == list(range(32))
+    # reads: thread f takes unit f % (S/4) of row f // (S/4) of each block;
+    # eight consecutive threads must cover the 32 banks once
+    units = s // 4
+    for f0 in range(0, 128 * units, 8):
+        banks = []
+        for f in range(f0, f0 + 8):
+            rr, u = f // units, f % units
+            off = rr * s * 4 + ((u ^ (rr & 7)) << 4)
+            banks.extend(bank_of(off + 4 * w) for w in range(4))
+        assert sorted(banks) == list(range(32))
