@@ -256,11 +256,9 @@ double schedule_seconds(int cg, int bn, int64_t tiles, int64_t clusters, int64_t
     return t + kFixedSec + (cg == 2 ? kPairFixedSec : 0.0);
 }
 
-// CTAs per cluster: a CTA pair, times the pairs sharing B, times the CTAs
-// splitting a tile's K loop.
+// CTAs per cluster: a CTA pair, or the CTAs splitting a tile's K loop.
 int64_t cluster_ctas(const hgemm_plan_t& pl) {
-    return static_cast<int64_t>(pl.cta_group) * (pl.multicast > 1 ? pl.multicast : 1) *
-           (pl.split_k > 1 ? pl.split_k : 1);
+    return static_cast<int64_t>(pl.cta_group) * (pl.split_k > 1 ? pl.split_k : 1);
 }
 
 // Fill the schedule fields of `pl` (tiles already set) for `clusters`
@@ -423,9 +421,14 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dt, cons
         t_last_error = "negative or unknown config field";
         return HGEMM_ERR_INVALID_ARG;
     }
+    if (c.multicast != 0 && c.multicast != 1) {
+        // reserved: no operand is multicast across the CTAs of a cluster
+        t_last_error = "multicast is reserved: 0 or 1 (no operand multicast is built)";
+        return HGEMM_ERR_INVALID_ARG;
+    }
     int cg = c.cta_group, bn = c.block_n;
     int split = c.split_k > 1 ? c.split_k : 1;
-    if (c.split_k == 0 && allow_auto_split && cg == 0 && bn == 0 && c.multicast <= 1 && c.stream_k <= 1 &&
+    if (c.split_k == 0 && allow_auto_split && cg == 0 && bn == 0 && c.stream_k <= 1 &&
         c.max_clusters == 0) {
         split = auto_split(M, N, K, dt, sms);
         if (split > 1) bn = 128;
@@ -451,22 +454,16 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dt, cons
         t_last_error = "unsupported (cta_group, block_n) pair";
         return HGEMM_ERR_INVALID_ARG;
     }
-    if (c.multicast < 0 || c.multicast > 2 ||
-        (c.multicast == 2 && !(cg == 2 && bn == 256 && esize_of(dt) == 2))) {
-        t_last_error = "multicast = 2 needs cta_group 2, block_n 256 and a 16-bit dtype";
-        return HGEMM_ERR_INVALID_ARG;
-    }
     if (split > 1 && !((split == 2 || split == 4 || split == 8) && cg == 1 && (bn == 128 || bn == 256) &&
-                       bn / split >= 32 && esize_of(dt) == 2 && c.multicast <= 1 && c.stream_k <= 1)) {
+                       bn / split >= 32 && esize_of(dt) == 2 && c.stream_k <= 1)) {
         t_last_error = "split_k needs 2, 4 or 8 with cta_group 1, block_n 128 or 256 (at least 32 columns per "
-                       "CTA), a 16-bit dtype, no multicast and no stream-K";
+                       "CTA), a 16-bit dtype and no stream-K";
         return HGEMM_ERR_INVALID_ARG;
     }
-    const int mc = c.multicast == 2 ? 2 : 1;
     pl->cta_group = cg;
-    pl->multicast = mc;
+    pl->multicast = 1;
     pl->split_k = split;
-    pl->block_m = 128 * cg * mc;
+    pl->block_m = 128 * cg;
     pl->block_n = bn;
     pl->block_k = static_cast<int32_t>(bk_of(dt));
     pl->stages = hg::tc_stages(cg, bn, esize_of(dt), split);
@@ -589,6 +586,39 @@ hgemm_status_t check_args(const void* A, const void* B, void* C, int64_t M, int6
     return HGEMM_OK;
 }
 
+// Resident clusters of the kernel instance a plan launches, on the current
+// device (0 if the query fails).
+int resident_clusters(hgemm_dtype_t dtype, const hgemm_plan_t& q) {
+    const int qm = q.split_k > 1 ? q.split_k : 1;
+    return dtype == HGEMM_BF16   ? hg::max_active_clusters_bf16(q.cta_group, q.block_n, qm)
+           : dtype == HGEMM_TF32 ? hg::max_active_clusters_tf32(q.cta_group, q.block_n, qm)
+           : is_fp8(dtype)       ? hg::max_active_clusters_fp8(static_cast<int>(dtype), q.cta_group, q.block_n, qm)
+                                 : hg::max_active_clusters_f16(q.cta_group, q.block_n, qm);
+}
+
+// The planner's K split needs one resident cluster per tile. Where fewer
+// clusters of that size fit on the current device (on a 152-SM GB300, 32
+// clusters of 4 and 15 of 8), take half the split on the same tiles, then
+// whole tiles. A split asked for in `cfg` is kept (the launch then fails
+// with a message). *resident receives the resident clusters of the final plan.
+hgemm_status_t fit_split_to_device(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dtype, const hgemm_config_t* cfg,
+                                   int sms, bool a_bad, bool b_bad, bool c_bad, hgemm_plan_t* pl, int* resident) {
+    *resident = resident_clusters(dtype, *pl);
+    while (pl->split_k > 1 && !(cfg && cfg->split_k > 1) && *resident > 0 && *resident < pl->num_tiles) {
+        hgemm_config_t smaller{};
+        if (cfg) smaller = *cfg;
+        smaller.split_k = pl->split_k / 2 > 1 ? pl->split_k / 2 : 1;
+        if (smaller.split_k > 1) {
+            smaller.cta_group = 1;
+            smaller.block_n = pl->block_n;
+        }
+        hgemm_status_t st = make_plan(M, N, K, dtype, &smaller, sms, a_bad, b_bad, c_bad, pl, false);
+        if (st != HGEMM_OK) return st;
+        *resident = resident_clusters(dtype, *pl);
+    }
+    return HGEMM_OK;
+}
+
 // `scratch` (nullptr: none) is caller-provided device memory of `scratch_bytes`
 // used instead of the stream-ordered allocator for the repack workspace.
 // `a_scale` / `b_scale` (fp8 only; nullptr = 1) are the per-channel factors.
@@ -625,33 +655,14 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
         return HGEMM_ERR_INVALID_ARG;
     }
 
-    // Resident clusters bound the persistent grid; re-plan the schedule if
-    // fewer fit than the planner assumed. The kernel's cluster multiplier is
-    // the pairs sharing B, or the CTAs splitting K.
-    auto resident_clusters = [&](const hgemm_plan_t& q) {
-        const int qm = q.split_k > 1 ? q.split_k : q.multicast;
-        return dtype == HGEMM_BF16   ? hg::max_active_clusters_bf16(q.cta_group, q.block_n, qm)
-               : dtype == HGEMM_TF32 ? hg::max_active_clusters_tf32(q.cta_group, q.block_n, qm)
-               : is_fp8(dtype)       ? hg::max_active_clusters_fp8(static_cast<int>(dtype), q.cta_group, q.block_n, qm)
-                                     : hg::max_active_clusters_f16(q.cta_group, q.block_n, qm);
-    };
-    int resident = resident_clusters(pl);
-    while (pl.split_k > 1 && !(cfg && cfg->split_k > 1) && resident > 0 && resident < pl.num_tiles) {
-        // the planner's K split does not fit (fewer clusters resident than
-        // tiles; on a 152-SM GB300 32 clusters of 4 fit, not 38): the next
-        // smaller split on the same tiles, else whole tiles
-        hgemm_config_t smaller{};
-        if (cfg) smaller = *cfg;
-        smaller.split_k = pl.split_k / 2 > 1 ? pl.split_k / 2 : 1;
-        if (smaller.split_k > 1) {
-            smaller.cta_group = 1;
-            smaller.block_n = pl.block_n;
-        }
-        if ((st = make_plan(M, N, K, dtype, &smaller, info.sms, a_bad, b_bad, c_bad, &pl, false)) != HGEMM_OK)
-            return st;
-        resident = resident_clusters(pl);
-    }
-    const int cg = pl.cta_group, bn = pl.block_n, mc = pl.split_k > 1 ? pl.split_k : pl.multicast;
+    // Resident clusters bound the persistent grid: a K split that does not
+    // fit shrinks, and the schedule is re-planned if fewer clusters fit than
+    // the planner assumed. The kernel's cluster multiplier is the CTAs
+    // splitting K.
+    int resident = 0;
+    if ((st = fit_split_to_device(M, N, K, dtype, cfg, info.sms, a_bad, b_bad, c_bad, &pl, &resident)) != HGEMM_OK)
+        return st;
+    const int cg = pl.cta_group, bn = pl.block_n, mc = pl.split_k > 1 ? pl.split_k : 1;
     const int64_t num_kb = cdiv(K, bk);
     if (resident > 0 && resident < pl.grid_ctas / (cg * mc)) {
         if (pl.split_k > 1) {
@@ -1085,7 +1096,11 @@ hgemm_status_t hgemm_plan(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dtype,
     }
     const int64_t es = esize_of(dtype), ces = c_esize_of(dtype);
     const bool a_bad = ((K * es) & 15) != 0, b_bad = ((N * es) & 15) != 0, c_bad = ((N * ces) & 15) != 0;
-    return make_plan(M, N, K, dtype, cfg, sms, a_bad, b_bad, c_bad, out);
+    hgemm_status_t st = make_plan(M, N, K, dtype, cfg, sms, a_bad, b_bad, c_bad, out);
+    if (st != HGEMM_OK || sm_count > 0) return st;
+    // planning for the current device: the K split the launch would keep
+    int resident = 0;
+    return fit_split_to_device(M, N, K, dtype, cfg, sms, a_bad, b_bad, c_bad, out, &resident);
 }
 
 int32_t hgemm_work_unit(const hgemm_plan_t* plan, int32_t cluster, int32_t i, int32_t* tile,

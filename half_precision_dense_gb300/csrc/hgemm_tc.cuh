@@ -31,10 +31,9 @@
 // leader's elected lane issues tcgen05.mma.cta_group::2, which reads both
 // CTAs' shared memory and accumulates each CTA's 128 rows in that CTA's TMEM.
 //
-// Larger clusters (MC > 1): two CTA pairs stacked along M that share B by
-// TMA multicast, or 2, 4 or 8 single CTAs that split one tile's K loop and
-// add their partial sums through distributed shared memory (the template's
-// comment gives the details).
+// Larger clusters (MC > 1): 2, 4 or 8 single CTAs that split one tile's K
+// loop and add their partial sums through distributed shared memory (the
+// template's comment gives the details).
 //
 // Every wait is bounded (TcParams::timeout_ns). A wait that runs out records
 // HGEMM_ERR_TIMEOUT with the role and barrier in the device status word, sets a
@@ -388,14 +387,12 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
     for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i]));
 }
 
-// MC > 1 makes larger clusters. CG = 2, MC = 2: a cluster of four stacks two
-// pairs along M; they need the same B columns, so each CTA loads only one of
-// its two 64-column B atoms and multicasts it to the matching CTA of the
-// other pair (a quarter less operand traffic through L2). CG = 1, MC = 2, 4
-// or 8: the MC CTAs of a cluster split one 128 x BN tile's K loop (split-K
-// within the cluster) and reduce their fp32 partial sums through distributed
-// shared memory; that puts MC SMs on each tile of a shape with too few tiles
-// to fill the GPU (a skinny M), each reading 1/MC of the tile's operands.
+// MC > 1 (single CTAs only: CG = 1, MC = 2, 4 or 8): the MC CTAs of a
+// cluster split one 128 x BN tile's K loop (split-K within the cluster) and
+// reduce their fp32 partial sums through distributed shared memory; that puts
+// MC SMs on each tile of a shape with too few tiles to fill the GPU (a skinny
+// M), each reading 1/MC of the tile's operands. Every operand copy lands in
+// the issuing CTA's own shared memory (no cluster multicast).
 template <int CG, int BN, int kDt, int MC>
 __global__ void __launch_bounds__(kThreads, 1)
 hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -413,9 +410,8 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     constexpr int S = Cfg::kStages;
     constexpr int kCluster = CG * MC;
     constexpr bool kSplit = CG == 1 && MC > 1;               // K split across the cluster
-    static_assert(MC == 1 || (CG == 2 && MC == 2 && Cfg::kBAtoms == 2 && !Cfg::kBPartial) ||
-                      (kSplit && (MC == 2 || MC == 4 || MC == 8)),
-                  "B multicast across pairs, or a K split across 2, 4 or 8 single CTAs");
+    static_assert(MC == 1 || (kSplit && (MC == 2 || MC == 4 || MC == 8)),
+                  "a CTA pair, or a K split across 2, 4 or 8 single CTAs");
     // The split's reduction: 16-bit C, whole 64-column chunks, column slices
     // of at least eight 16-byte units, every CTA's slice received in the ring.
     static_assert(!kSplit || (kDt <= 1 && !Cfg::kHalfLast && BN / MC >= 32 &&
@@ -459,9 +455,9 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(bar_full + 8 * s, 1);
-            // every MMA that reads the stage frees it: both pairs' with B
-            // multicast, this CTA's own otherwise (a K split included)
-            mbar_init(bar_empty + 8 * s, kSplit ? 1 : MC);
+            // the one MMA issuer that reads the stage frees it (the pair
+            // leader's, or this CTA's own)
+            mbar_init(bar_empty + 8 * s, 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bar_tfull + 8 * a, 1);
@@ -562,20 +558,12 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                             if (rank == 0) mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
                             if (p.im2col) tma_load_im2col_4d_pair(a_dst, &tmA, fb_leader, ic, iw, ih, in_, ow, oh);
                             else tma_load_2d_pair(a_dst, &tmA, fb_leader, k0, m0);
-                            if constexpr (MC == 1) {
 #pragma unroll
-                                for (int j = 0; j < Cfg::kBAtoms; ++j)
-                                    tma_load_2d_pair(b_dst + j * Cfg::kBAtomBytes,
-                                                     (Cfg::kBPartial && j == Cfg::kBAtoms - 1) ? &tmB2 : &tmB,
-                                                     fb_leader,
-                                                     n0 + Cfg::kAtomCols * j, k0);
-                            } else {
-                                // Atom `pair` of this B half, for this CTA and its
-                                // counterpart in the other pair.
-                                const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << (CG + rank)));
-                                tma_load_2d_pair_mc(b_dst + pair * Cfg::kBAtomBytes, &tmB, fb_leader,
-                                                    n0 + Cfg::kAtomCols * static_cast<int32_t>(pair), k0, mask);
-                            }
+                            for (int j = 0; j < Cfg::kBAtoms; ++j)
+                                tma_load_2d_pair(b_dst + j * Cfg::kBAtomBytes,
+                                                 (Cfg::kBPartial && j == Cfg::kBAtoms - 1) ? &tmB2 : &tmB,
+                                                 fb_leader,
+                                                 n0 + Cfg::kAtomCols * j, k0);
                         }
                     }
                     __syncwarp();
@@ -669,12 +657,10 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                                 umma_f16<CG>(d_tmem, ad + 2u * kk, bd + 8u * Cfg::kUK * kk, p.idesc, accum);
                             accum = 1u;
                         }
-                        // A stage is free once every pair that reads it is done:
-                        // with B multicast, both pairs read every CTA's B atoms.
+                        // A stage is free once the MMAs that read it are done; a
+                        // pair's commit arrives on both CTAs' barriers.
                         if constexpr (CG == 1) umma_commit(bar_empty + 8 * stage);
-                        else umma_commit_pair(bar_empty + 8 * stage,
-                                              MC == 1 ? static_cast<uint16_t>(0x3u << leader)
-                                                      : static_cast<uint16_t>((1u << kCluster) - 1u));
+                        else umma_commit_pair(bar_empty + 8 * stage, static_cast<uint16_t>(0x3u << leader));
                     }
                     __syncwarp();
                     accum = 1u;

@@ -131,20 +131,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* desc,
         : "memory");
 }
 
-// Pair form with cluster multicast: the tile lands at the same offset in the
-// shared memory of every CTA in `cta_mask`, and each destination's bytes are
-// signalled on the barrier at `bar_cluster`'s offset in the leader CTA of that
-// destination's pair.
-__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const void* desc, uint32_t bar_cluster,
-                                                    int32_t x, int32_t y, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;"
-        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(desc)), "r"(bar_cluster), "r"(x), "r"(y), "h"(cta_mask)
-        : "memory");
-}
-
-// 2-D tile store from shared memory, tracked by the bulk-group mechanism.
 // 4-D im2col-mode load (channels-last activations): `c`, `w`, `h`, `n` give
 // the first channel and the first output pixel's receptive-field origin in
 // the tensor map's bounding box; the copy walks the map's pixelsPerColumn
@@ -174,6 +160,7 @@ __device__ __forceinline__ void tma_load_im2col_4d_pair(uint32_t dst, const void
         : "memory");
 }
 
+// 2-D tile store from shared memory, tracked by the bulk-group mechanism.
 __device__ __forceinline__ void tma_store_2d(const void* desc, uint32_t src, int32_t x, int32_t y) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];"
                  :: "l"(reinterpret_cast<uint64_t>(desc)), "r"(src), "r"(x), "r"(y) : "memory");

@@ -81,9 +81,8 @@ struct TcInstance {
     }
 };
 
-// Every tile shape of the 16-bit kinds (KDT 0 = fp16, 1 = bf16), with B
-// multicast across two pairs (mc 2 with cta_group 2) and the K split across
-// 2, 4 or 8 single CTAs (mc with cta_group 1).
+// Every tile shape of the 16-bit kinds (KDT 0 = fp16, 1 = bf16), and the K
+// split across 2, 4 or 8 single CTAs (mc with cta_group 1).
 #define HG_TC_DISPATCH(KDT, CALL)                                                          \
     if (mc == 1 && cta_group == 1 && block_n == 64) return TcInstance<1, 64, KDT>::CALL;   \
     if (mc == 1 && cta_group == 1 && block_n == 128) return TcInstance<1, 128, KDT>::CALL; \
@@ -91,7 +90,6 @@ struct TcInstance {
     if (mc == 1 && cta_group == 2 && block_n == 128) return TcInstance<2, 128, KDT>::CALL; \
     if (mc == 1 && cta_group == 2 && block_n == 224) return TcInstance<2, 224, KDT>::CALL; \
     if (mc == 1 && cta_group == 2 && block_n == 256) return TcInstance<2, 256, KDT>::CALL; \
-    if (mc == 2 && cta_group == 2 && block_n == 256) return TcInstance<2, 256, KDT, 2>::CALL; \
     if (mc == 2 && cta_group == 1 && block_n == 128) return TcInstance<1, 128, KDT, 2>::CALL; \
     if (mc == 4 && cta_group == 1 && block_n == 128) return TcInstance<1, 128, KDT, 4>::CALL; \
     if (mc == 2 && cta_group == 1 && block_n == 256) return TcInstance<1, 256, KDT, 2>::CALL; \
@@ -99,7 +97,7 @@ struct TcInstance {
     if (mc == 8 && cta_group == 1 && block_n == 256) return TcInstance<1, 256, KDT, 8>::CALL;
 
 // The tf32 (KDT 2) and fp8 (KDT 3 = E4M3, 4 = E5M2) tile shapes: whole
-// 64-column chunks, no B multicast.
+// 64-column chunks, no K split.
 #define HG_TC_DISPATCH_K(KDT, CALL)                                                        \
     if (mc == 1 && cta_group == 1 && block_n == 64) return TcInstance<1, 64, KDT>::CALL;   \
     if (mc == 1 && cta_group == 1 && block_n == 128) return TcInstance<1, 128, KDT>::CALL; \

@@ -52,6 +52,13 @@
  *     is available from hgemm_last_error() on the same thread.
  *   - There is no CPU fallback: a device that is not compute capability 10.3
  *     gives HGEMM_ERR_UNSUPPORTED_DEVICE.
+ *   - Per device, the library keeps state for the life of the process: the
+ *     device addresses of its status word and of hgemm_noalloc's array, its
+ *     memory pool, hgemm_host's streams and the kernels' shared-memory
+ *     settings. It looks them up on first use and never again, so it must
+ *     not be called on a device after cudaDeviceReset() on that device in
+ *     the same process (the cached addresses would belong to the destroyed
+ *     context).
  */
 #ifndef HGEMM_H_
 #define HGEMM_H_
@@ -210,15 +217,14 @@ uint64_t hgemm_noalloc_scratch_bytes(void);
  *                  are cut into equal contiguous ranges, one per cluster;
  *                  3 = stream-K over every tile; 4 = stream-K over the
  *                  leftover tiles of the partial last wave only.
- *   multicast:     CTA pairs per cluster (cta_group 2, block_n 256 only):
- *                  0 = planner's choice, 1 = one pair, 2 = two pairs stacked
- *                  along M that load their shared B columns once, by TMA
- *                  multicast (tiles of 512 rows).
+ *   multicast:     reserved, 0 or 1 (any other value is
+ *                  HGEMM_ERR_INVALID_ARG). No operand tile is multicast
+ *                  across the CTAs of a cluster: every TMA load lands in the
+ *                  shared memory of the CTA that issues it.
  *   split_k:       CTAs per cluster that split each tile's K loop: 0 =
  *                  planner's choice, 1 = none, 2, 4 or 8 = a cluster of that
  *                  many single CTAs (cta_group 1, block_n 128 or 256, at least
- *                  32 columns per CTA; 16-bit dtypes; no stream-K or
- *                  multicast) per tile. CTA r multiplies K blocks
+ *                  32 columns per CTA; 16-bit dtypes; no stream-K) per tile. CTA r multiplies K blocks
  *                  [r n / s, (r + 1) n / s) of the tile's n; the fp32 partial
  *                  sums meet through distributed shared memory and each CTA
  *                  adds all of them, in rank order, for 1/s of the tile's
@@ -296,7 +302,7 @@ hgemm_status_t hgemm_host(const void* hA, const void* hB, void* hC, int64_t M, i
  */
 typedef struct {
     int32_t cta_group;     /* 1 or 2 */
-    int32_t block_m;       /* rows of C per tile: 128 * cta_group * multicast */
+    int32_t block_m;       /* rows of C per tile: 128 * cta_group */
     int32_t block_n;       /* columns of C per tile */
     int32_t block_k;       /* K per pipeline stage (64) */
     int32_t stages;        /* depth of the shared-memory ring */
@@ -304,7 +310,7 @@ typedef struct {
     int32_t tiles_m;       /* ceil(M / block_m) */
     int32_t tiles_n;       /* ceil(N / block_n) */
     int32_t num_tiles;     /* tiles_m * tiles_n */
-    int32_t grid_ctas;     /* CTAs launched (a multiple of cta_group * multicast * split_k) */
+    int32_t grid_ctas;     /* CTAs launched (a multiple of cta_group * split_k) */
     int32_t smem_bytes;    /* dynamic shared memory per CTA */
     int32_t tmem_cols;     /* tensor-memory columns allocated per CTA */
     int32_t repack_a;      /* 1 if A goes through the 16-byte-pitch workspace */
@@ -316,15 +322,18 @@ typedef struct {
                               sk_extra clusters take one more) */
     int32_t sk_extra;
     int32_t num_kb;        /* 64-deep K blocks per tile: ceil(K / 64) */
-    int32_t multicast;     /* CTA pairs per cluster sharing B by multicast (1 = none) */
-    int32_t split_k;       /* CTAs per cluster splitting a tile's K loop (1 = none). hgemm_plan
-                              assumes a cluster per tile fits; a launch whose planner-chosen
-                              split finds fewer clusters resident takes whole tiles instead */
+    int32_t multicast;     /* always 1 (reserved; no operand multicast) */
+    int32_t split_k;       /* CTAs per cluster splitting a tile's K loop (1 = none). A
+                              planner-chosen split needs one resident cluster per tile; where
+                              fewer fit on the device, the launch takes half the split on the
+                              same tiles, then whole tiles (see hgemm_plan) */
     int64_t workspace_bytes; /* stream-ordered workspace: repacked operands + fp32 partials */
 } hgemm_plan_t;
 
-/* Fill *out with the plan hgemm_ex would use. sm_count > 0 plans for that many
- * SMs without touching a device (pointers are then assumed 16-byte aligned). */
+/* Fill *out with the plan hgemm_ex would use (pointers are assumed 16-byte
+ * aligned). sm_count <= 0 plans for the current device, after the K-split
+ * fallback above (the split the launch keeps). sm_count > 0 plans for that
+ * many SMs without touching a device and assumes a cluster per tile fits. */
 hgemm_status_t hgemm_plan(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dtype,
                           const hgemm_config_t* cfg, int32_t sm_count, hgemm_plan_t* out);
 

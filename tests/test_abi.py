@@ -174,7 +174,7 @@ def test_plan_stream_k(lib):
 
 
 def _check_schedule(p):
-    clusters = p["grid_ctas"] // (p["cta_group"] * p["multicast"] * p["split_k"])
+    clusters = p["grid_ctas"] // (p["cta_group"] * p["split_k"])
     kb = p["num_kb"]
     seen = {}
     units_of = {}
@@ -220,7 +220,6 @@ def _check_schedule(p):
     ((1024, 1280, 704), dict(cta_group=2, block_n=224, max_clusters=5, stream_k=3), 152),
     ((300, 700, 130), dict(cta_group=1, block_n=64, stream_k=3), 152),
     ((777, 999, 4444), dict(stream_k=2), 37),
-    ((4096, 4096, 4096), dict(cta_group=2, block_n=256, multicast=2, stream_k=2), 152),
     ((4096, 4096, 4096), dict(cta_group=2, block_n=256, stream_k=4), 152),
     ((1024, 1280, 704), dict(cta_group=1, block_n=128, max_clusters=7, stream_k=4), 152),
     ((128, 8192, 8192), dict(split_k=4), 152),
@@ -370,9 +369,11 @@ def test_plan_tf32(lib):
     assert binding.plan(4096, 4096, 4096, "tf32", sm_count=152)["workspace_bytes"] == 0
     assert binding.plan(64, 1022, 1024, "tf32", sm_count=152)["repack_b"] == 1
     assert binding.plan(64, 1024, 1000, "tf32", sm_count=152)["repack_a"] == 0
-    # B multicast across pairs is built for 16-bit B only
-    with pytest.raises(binding.HgemmError):
-        binding.plan(1024, 1024, 1024, "tf32", binding.Config(cta_group=2, block_n=256, multicast=2), sm_count=152)
+    # no operand multicast is built: the field is reserved (0 or 1), for every dtype
+    for dt in ("bf16", "f16", "tf32", "e4m3"):
+        with pytest.raises(binding.HgemmError):
+            binding.plan(1024, 1024, 1024, dt, binding.Config(cta_group=2, block_n=256, multicast=2), sm_count=152)
+        assert binding.plan(1024, 1024, 1024, dt, binding.Config(multicast=1), sm_count=152)["multicast"] == 1
     # an unknown dtype code is refused by the library itself
     out = binding._Plan()
     assert lib.hgemm_plan(64, 64, 64, 5, None, 152, ctypes.byref(out)) == 1

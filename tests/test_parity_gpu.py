@@ -23,10 +23,8 @@ CONFIGS = [
     hg.Config(cta_group=2, block_n=128),
     hg.Config(cta_group=2, block_n=224),
     hg.Config(cta_group=2, block_n=256),
-    hg.Config(cta_group=2, block_n=256, multicast=2),
-
 ]
-CFG_IDS = ["cg1_n64", "cg1_n128", "cg1_n256", "cg2_n128", "cg2_n224", "cg2_n256", "cg2_n256_mc2"]
+CFG_IDS = ["cg1_n64", "cg1_n128", "cg1_n256", "cg2_n128", "cg2_n224", "cg2_n256"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -205,10 +203,13 @@ def test_split_k_store_modes_and_repeat(store_mode):
 @pytest.mark.parametrize("shape", [(128, 4864, 8192), (100, 4736, 8200)])
 def test_split_k_planner_fallback(shape):
     # the planner's split of 4 on 37-38 tiles: fewer clusters of 4 are
-    # resident than tiles, so the launch takes a split of 2 (or whole tiles)
+    # resident than tiles, so the launch takes a split of 2 (or whole tiles),
+    # and the plan for the current device reports the split it keeps
     M, N, K = shape
+    p152 = hg.plan(M, N, K, "bf16", sm_count=152)
+    assert p152["split_k"] == 4 and p152["num_tiles"] * 4 <= 152 and p152["num_tiles"] > 32
     p = hg.plan(M, N, K, "bf16")
-    assert p["split_k"] == 4 and p["num_tiles"] * 4 <= 152 and p["num_tiles"] > 32
+    assert p["split_k"] in (1, 2) and p["num_tiles"] == p152["num_tiles"]
     A, B = operands(M, N, K, "bf16", 21)
     check_full(A, B, "bf16")
 

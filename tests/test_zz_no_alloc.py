@@ -122,3 +122,62 @@ def test_other_dtypes_in_scratch(lib, dtype):
     hg.hgemm_noalloc(A, B, C1, M, N, K, dtype)
     torch.cuda.synchronize()
     assert torch.equal(C0, C1)
+
+
+# Driver node types (CUgraphNodeType) that allocate or free memory.
+_CU_GRAPH_NODE_TYPE_MEM_ALLOC = 10
+_CU_GRAPH_NODE_TYPE_MEM_FREE = 11
+
+
+def _capture_node_types(fn, stream):
+    """Record `fn()` (which enqueues on `stream`) by stream capture through the
+    driver API and return the type of every node of the captured graph."""
+    cu = ctypes.CDLL("libcuda.so.1")
+    s = ctypes.c_void_p(stream.cuda_stream)
+    assert cu.cuStreamBeginCapture_v2(s, 1) == 0          # CU_STREAM_CAPTURE_MODE_THREAD_LOCAL
+    try:
+        fn()
+    finally:
+        graph = ctypes.c_void_p()
+        rc = cu.cuStreamEndCapture(s, ctypes.byref(graph))
+    assert rc == 0
+    try:
+        n = ctypes.c_size_t(0)
+        assert cu.cuGraphGetNodes(graph, None, ctypes.byref(n)) == 0
+        nodes = (ctypes.c_void_p * max(1, n.value))()
+        assert cu.cuGraphGetNodes(graph, nodes, ctypes.byref(n)) == 0
+        types = []
+        for i in range(n.value):
+            t = ctypes.c_int(-1)
+            assert cu.cuGraphNodeGetType(ctypes.c_void_p(nodes[i]), ctypes.byref(t)) == 0
+            types.append(t.value)
+        return types
+    finally:
+        cu.cuGraphDestroy(graph)
+
+
+def test_noalloc_capture_has_no_allocation_node(lib):
+    # K = 1001: A's rows are not 16-byte multiples, so the call repacks A into
+    # its workspace; captured, hgemm_noalloc must take that workspace from the
+    # fixed array (no allocation or free node), while hgemm draws it from its
+    # pool (an allocation node).
+    M, N, K = 300, 512, 1001
+    A = inputs.generate((M, K), "bf16", 35, 0).cuda()
+    B = inputs.generate((K, N), "bf16", 35, 1).cuda()
+    assert hg.plan(M, N, K, "bf16")["repack_a"] == 1
+    C_eager = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    C_cap = torch.full((M, N), 9.0, dtype=torch.bfloat16, device="cuda")
+    # the first call on the device looks up the array's address: before any capture
+    assert _call(lib, lib.hgemm_noalloc, A, B, C_eager, M, N, K, "bf16") == 0
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        types = _capture_node_types(lambda: _call(lib, lib.hgemm_noalloc, A, B, C_cap, M, N, K, "bf16"), s)
+    assert types, "nothing was captured"
+    assert _CU_GRAPH_NODE_TYPE_MEM_ALLOC not in types and _CU_GRAPH_NODE_TYPE_MEM_FREE not in types, types
+    # the pool-backed entry point, captured the same way, does allocate
+    with torch.cuda.stream(s):
+        types_pool = _capture_node_types(lambda: _call(lib, lib.hgemm, A, B, C_cap, M, N, K, "bf16"), s)
+    assert _CU_GRAPH_NODE_TYPE_MEM_ALLOC in types_pool, types_pool
+    torch.cuda.synchronize()
+    assert torch.all(C_cap == 9.0)   # a captured call only records work
