@@ -1,4 +1,5 @@
-"""CPU oracle for the FP8 GEMM variant with per-channel scales.
+"""CPU oracle for the FP8 GEMM variants: per-channel scales, and one scale
+per square sub-block.
 
 TEST INFRASTRUCTURE ONLY. Nothing in the product path may import or call this
 module: only the tests, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU legs
@@ -23,8 +24,8 @@ Readings (the pages leave these open):
   NaNs. A and B share one format.
 * Scales are per channel: one fp32 factor per row of A (``a_scale[i]``) and
   one per column of B (``b_scale[j]``). Both are constant along K, so they
-  factor out of the sum; the section 4.3 sub-block scales (32 x 32 or
-  64 x 64 blocks, varying along K) are not this variant.
+  factor out of the sum. The section 4.3 sub-block scales (32 x 32 or
+  64 x 64 blocks, varying along K) are the block-scaled variant below.
 * C is bfloat16 (the series' output type), rounded once to nearest even.
 
 The oracle is the definition in fp64 (each fp8 x fp8 product is exact):
@@ -33,6 +34,23 @@ The oracle is the definition in fp64 (each fp8 x fp8 product is exact):
     C[i][j]   = RNE_bf16(C64[i][j])
 
 The bf16 rounding is the half-precision oracle's own ``round_rne``.
+
+Block-scaled variant ("深度学习加速核心：GEMM优化从分块到TensorCore的实战解析",
+section 4.3: FP8 data is usually scaled block-wise, one factor per 32 x 32
+or 64 x 64 sub-block, mapping its values into the format's range; section
+5.2, the third mishap: a 16-bit sub-block scale overflowed to infinity, and
+32-bit scales fixed it). Readings:
+* The value of A's element (i, k) is decode(A[i][k]) * a_scale[i // bs][k // bs]
+  and that of B's element (k, j) is decode(B[k][j]) * b_scale[k // bs][j // bs]:
+  a_scale is ceil(M / bs) x ceil(K / bs), b_scale ceil(K / bs) x ceil(N / bs),
+  both row-major fp32; bs is 32 or 64 (the two sizes the page names). The
+  last block of a dimension that is not a multiple of bs is partial.
+* The product is that of the dequantised matrices, C rounded once to bf16.
+  The oracle is that definition written out in fp64 (dequantise, then the
+  plain product; the 28-bit dequantised values are exact in fp64):
+
+    C64 = (decode(A) * a_scale[i // bs][k // bs]) @ (decode(B) * b_scale[k // bs][j // bs])
+    C   = RNE_bf16(C64)
 """
 
 from __future__ import annotations
@@ -41,7 +59,9 @@ import numpy as np
 
 from .hgemm_oracle import round_rne
 
-__all__ = ["FORMATS", "decode", "gemm_f64", "gemm", "abs_gemm", "tolerance"]
+__all__ = ["FORMATS", "decode", "gemm_f64", "gemm", "abs_gemm", "tolerance", "SCALE_BLOCKS",
+           "scale_grid", "dequantise_a", "dequantise_b", "gemm_blockscaled_f64", "gemm_blockscaled",
+           "abs_gemm_blockscaled", "tolerance_blockscaled"]
 
 # name -> (exponent bits, fraction bits, bias, has_infinity)
 FORMATS = {"e4m3": (4, 3, 7, False), "e5m2": (5, 2, 15, True)}
@@ -123,3 +143,88 @@ def tolerance(S: np.ndarray, C64: np.ndarray, K: int) -> np.ndarray:
     e = np.frexp(np.where(ref > 0, ref, 1.0))[1] - 1
     ulp_bf16 = np.ldexp(1.0, np.maximum(e, -126) - 7)
     return (K + 1) * u * S + ulp_bf16
+
+
+# ---------------------------------------------------------------------------
+# Block-scaled variant: one fp32 factor per bs x bs sub-block of A and of B.
+
+SCALE_BLOCKS = (32, 64)
+
+
+def scale_grid(rows: int, cols: int, block: int) -> tuple:
+    """Shape of the scale array of a rows x cols operand: one factor per
+    block x block sub-block, the last block of each dimension partial."""
+    return (-(-rows // block), -(-cols // block))
+
+
+def _check_blocks(A, B, a_scale, b_scale, block):
+    A = np.asarray(A)
+    B = np.asarray(B)
+    if block not in SCALE_BLOCKS:
+        raise ValueError(f"block must be one of {SCALE_BLOCKS}")
+    if A.ndim != 2 or B.ndim != 2 or A.shape[1] != B.shape[0]:
+        raise ValueError(f"shapes {A.shape} and {B.shape} do not chain (M x K) . (K x N)")
+    if A.dtype != np.uint8 or B.dtype != np.uint8:
+        raise TypeError("operands are uint8 bit patterns")
+    M, K = A.shape
+    N = B.shape[1]
+    sa = np.asarray(a_scale, dtype=np.float32).astype(np.float64)
+    sb = np.asarray(b_scale, dtype=np.float32).astype(np.float64)
+    if sa.shape != scale_grid(M, K, block) or sb.shape != scale_grid(K, N, block):
+        raise ValueError(f"a_scale must be {scale_grid(M, K, block)} and b_scale {scale_grid(K, N, block)}")
+    return A, B, sa, sb
+
+
+def dequantise_a(A, fmt: str, a_scale, block: int) -> np.ndarray:
+    """Values of A (M x K, fp64): decode(A[i][k]) * a_scale[i // block][k // block]."""
+    A = np.asarray(A)
+    sa = np.asarray(a_scale, dtype=np.float32).astype(np.float64)
+    i = np.arange(A.shape[0]) // block
+    k = np.arange(A.shape[1]) // block
+    return decode(A, fmt) * sa[i[:, None], k[None, :]]
+
+
+def dequantise_b(B, fmt: str, b_scale, block: int) -> np.ndarray:
+    """Values of B (K x N, fp64): decode(B[k][j]) * b_scale[k // block][j // block]."""
+    B = np.asarray(B)
+    sb = np.asarray(b_scale, dtype=np.float32).astype(np.float64)
+    k = np.arange(B.shape[0]) // block
+    j = np.arange(B.shape[1]) // block
+    return decode(B, fmt) * sb[k[:, None], j[None, :]]
+
+
+def gemm_blockscaled_f64(A, B, fmt: str, a_scale, b_scale, block: int) -> np.ndarray:
+    """The product of the dequantised operands, in fp64 (M x N)."""
+    A, B, sa, sb = _check_blocks(A, B, a_scale, b_scale, block)
+    if A.shape[1] == 0:
+        return np.zeros((A.shape[0], B.shape[1]), dtype=np.float64)
+    return dequantise_a(A, fmt, sa, block) @ dequantise_b(B, fmt, sb, block)
+
+
+def gemm_blockscaled(A, B, fmt: str, a_scale, b_scale, block: int) -> np.ndarray:
+    """The oracle's block-scaled C as bfloat16 bit patterns (uint16)."""
+    return round_rne(gemm_blockscaled_f64(A, B, fmt, a_scale, b_scale, block), "bf16")
+
+
+def abs_gemm_blockscaled(A, B, fmt: str, a_scale, b_scale, block: int) -> np.ndarray:
+    """sum_k |A64[i][k]| |B64[k][j]| of the dequantised operands (fp64)."""
+    A, B, sa, sb = _check_blocks(A, B, a_scale, b_scale, block)
+    if A.shape[1] == 0:
+        return np.zeros((A.shape[0], B.shape[1]), dtype=np.float64)
+    return np.abs(dequantise_a(A, fmt, sa, block)) @ np.abs(dequantise_b(B, fmt, sb, block))
+
+
+def tolerance_blockscaled(S: np.ndarray, C64: np.ndarray, K: int, block: int) -> np.ndarray:
+    """Per-element bound on |C_gpu - C_oracle| (both as values) for a GPU that
+    sums each K block's exact fp8 products in fp32 (in any order: fewer than K
+    additions in all, relative error <= 2^-23 each), forms each block's factor
+    a_scale * b_scale in fp32 and adds factor * partial into an fp32
+    accumulator (one rounding per block, ceil(K / block) blocks), then rounds
+    once to bf16: (K + ceil(K / block) + 2) 2^-23 S, with S the sum of
+    |A64| |B64|, plus one bf16 ulp of |C64| for the two roundings to bf16."""
+    u = 2.0 ** -23
+    nkb = -(-int(K) // int(block))
+    ref = np.abs(np.asarray(C64, dtype=np.float64))
+    e = np.frexp(np.where(ref > 0, ref, 1.0))[1] - 1
+    ulp_bf16 = np.ldexp(1.0, np.maximum(e, -126) - 7)
+    return (K + nkb + 2) * u * S + ulp_bf16
