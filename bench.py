@@ -2,9 +2,18 @@
 
 One step = the 4096^3 GEMM once in bf16 and once in fp16 (A, B row-major,
 entries U[-1, 1) from seed 1, fp32 accumulation, C in the input dtype), each
-through the C ABI with operands resident in HBM. L2 is flushed (a 256 MiB
-device write) before every GEMM; only the GEMM is inside the CUDA-event
-interval. `value` = 2MNK x GEMMs / summed GEMM time, over all ranks.
+through the C ABI with operands resident in HBM. L2 is flushed before every
+GEMM: a 256 MiB device write evicts every operand line, then (the default,
+``--l2 clean``) a 256 MiB read of another buffer replaces the write's dirty
+lines with clean ones, so the timed GEMM does not pay for writing back the
+flush's data. Only the GEMM is inside the CUDA-event interval. `value` =
+2MNK x GEMMs / summed GEMM time, over all ranks.
+
+The roofline object names the bound from the workload's arithmetic
+intensity (flops per algorithmic byte, 2(MK + KN) + 2MN bytes for 16-bit
+operands) against the ridge of the measured peaks: below it the GEMM is
+HBM-bound and `achieved` is GB/s of algorithmic bytes, above it tensor-bound
+and `achieved` is TFLOP/s; the other roofline is reported beside it.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME]
@@ -101,27 +110,117 @@ def read_peaks():
 
 
 # ------------------------------------------------------------------ clocks
+# NVML clock-event reason bits (nvmlClocksEventReason*), read only.
+_NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                 0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
+class _Nvml:
+    """Read-only NVML queries through the driver's libnvidia-ml (ctypes): SM
+    clock, maximum SM clock, power and clock-event reasons of one GPU."""
+
+    def __init__(self, cuda_index: int):
+        import ctypes
+
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.handle = ctypes.c_void_p()
+        found = False
+        try:  # the GPU this process uses, by UUID (NVML numbers every GPU of the machine)
+            import torch
+            u = str(torch.cuda.get_device_properties(cuda_index).uuid)
+            for name in (u if u.startswith("GPU-") else "GPU-" + u, u):
+                if self.lib.nvmlDeviceGetHandleByUUID(name.encode(), ctypes.byref(self.handle)) == 0:
+                    found = True
+                    break
+        except Exception:
+            pass
+        if not found and self.lib.nvmlDeviceGetHandleByIndex_v2(cuda_index, ctypes.byref(self.handle)) != 0:
+            raise OSError("no NVML handle")
+        mx = ctypes.c_uint(0)
+        self.max_mhz = float(mx.value) if self.lib.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx)) == 0 \
+            else None
+        self._reasons = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def sample(self):
+        ct = self.ct
+        mhz, mw, rs = ct.c_uint(0), ct.c_uint(0), ct.c_ulonglong(0)
+        ok = self.lib.nvmlDeviceGetClockInfo(self.handle, 1, ct.byref(mhz)) == 0   # NVML_CLOCK_SM
+        pw = float(mw.value) / 1000.0 if self.lib.nvmlDeviceGetPowerUsage(self.handle, ct.byref(mw)) == 0 else None
+        reasons = [n for b, n in _NVML_REASONS.items() if rs.value & b] \
+            if self._reasons(self.handle, ct.byref(rs)) == 0 else []
+        return (float(mhz.value) if ok else None, pw, reasons)
+
+
 class ClockSampler:
+    """SM clocks, power and throttle reasons sampled during the timed region:
+    read-only NVML queries every 5 ms from a thread (ctypes releases the GIL
+    during each query), else `nvidia-smi -lms 100`. `sample_now()` adds one
+    sample on demand (the launch loop calls it while the GPU is still busy)."""
+
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_index: int):
+    def __init__(self, device_index: int, period_s: float = 0.005):
         self.dev = device_index
+        self.period = period_s
         self.proc = None
+        self.nvml = None
+        self.samples = []      # (sm_mhz, power_w, [reasons])
+        self.max_mhz = None
+        self.source = None
+
+    def sample_now(self):
+        if self.nvml is not None:
+            try:
+                self.samples.append(self.nvml.sample())
+            except Exception:
+                pass
+
+    def _loop(self):
+        import time as _t
+        while not self._stop.is_set():
+            self.sample_now()
+            _t.sleep(self.period)
 
     def __enter__(self):
+        import threading
+        try:
+            self.nvml = _Nvml(self.dev)
+            self.max_mhz = self.nvml.max_mhz
+            self.source = "nvml"
+            self._stop = threading.Event()
+            self.sample_now()
+            self._thread = threading.Thread(target=self._loop, daemon=True)
+            self._thread.start()
+            return self
+        except Exception:
+            self.nvml = None
+        import shutil
+        exe = shutil.which("nvidia-smi") or next(
+            (p for p in ("/usr/bin/nvidia-smi", "/usr/local/nvidia/bin/nvidia-smi") if os.path.exists(p)), None)
+        if exe is None:
+            return self
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                [exe, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                  "-lms", "100", "-i", str(self.dev)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi"
         except OSError:
             self.proc = None
         return self
 
     def __exit__(self, *exc):
-        self.samples = []
+        if self.nvml is not None:
+            self.sample_now()
+            self._stop.set()
+            self._thread.join(timeout=2)
+            return False
         if self.proc is None:
             return False
         self.proc.terminate()
@@ -130,29 +229,28 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in out.strip().splitlines():
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) >= 9:
-                self.samples.append(parts)
+            if len(parts) < 9:
+                continue
+            num = lambda v: float(v) if v.replace(".", "").isdigit() else None
+            if num(parts[2]) is not None:
+                self.max_mhz = max(self.max_mhz or 0.0, num(parts[2]))
+            self.samples.append((num(parts[1]), num(parts[3]),
+                                 [n for n, v in zip(names, parts[5:9]) if v.lower() == "active"]))
         return False
 
     def summary(self):
-        if not getattr(self, "samples", None):
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
-                    "samples": 0}
-        sm = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
-        mx = [float(s[2]) for s in self.samples if s[2].replace(".", "").isdigit()]
-        reasons = set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for s in self.samples:
-            for name, v in zip(names, s[5:9]):
-                if v.lower() == "active":
-                    reasons.add(name)
-        pw = [float(s[3]) for s in self.samples if s[3].replace(".", "").isdigit()]
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(self.samples),
-                "power_w_max": max(pw) if pw else None}
+        sm = [s[0] for s in self.samples if s[0] is not None]
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz,
+                    "reasons": ["no clock samples (NVML and nvidia-smi unavailable)"], "samples": 0}
+        pw = [s[1] for s in self.samples if s[1] is not None]
+        reasons = sorted({r for s in self.samples for r in s[2]})
+        return {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(sm), "power_w_max": max(pw) if pw else None,
+                "source": self.source}
 
 
 # ------------------------------------------------------- multi-rank timing
@@ -215,7 +313,14 @@ def run_ours(args, rank, world, local_rank):
         ops.append(dict(M=M, N=N, K=K, dt=dt, hA=A, hB=B, A=A.to(dev), B=B.to(dev), sa=sa, sb=sb,
                         C=torch.empty((M, N), dtype=cdt, device=dev)))
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    clean = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev) if args.l2 == "clean" else None
+    sink = torch.empty((), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+
+    def flush_l2():
+        flush.zero_()                      # a write larger than L2: no operand line stays
+        if clean is not None:
+            torch.sum(clean, 0, out=sink)  # a read larger than L2: no dirty line of the write stays
 
     def one_gemm(o):
         if o.get("kind") == "conv":
@@ -227,7 +332,7 @@ def run_ours(args, rank, world, local_rank):
 
     for _ in range(args.warmup):
         for o in ops:
-            flush.zero_()
+            flush_l2()
             one_gemm(o)
     torch.cuda.synchronize(dev)
     hg.get_device_status(local_rank, reset=True)
@@ -243,11 +348,12 @@ def run_ours(args, rank, world, local_rank):
         i = 0
         for _ in range(args.steps):
             for o in ops:
-                flush.zero_()
+                flush_l2()
                 starts[i].record(stream)
                 one_gemm(o)
                 ends[i].record(stream)
                 i += 1
+        clk.sample_now()                   # the queued GEMMs are still running
         torch.cuda.synchronize(dev)
         wall = time.perf_counter() - wall0
     if world > 1:
@@ -302,11 +408,26 @@ def run_ours(args, rank, world, local_rank):
 
     peaks, peak_src = read_peaks()
     value = job_throughput(world, args.steps, step_flops, total_ms)
-    avg_launch_ms = total_ms / n_ev
-    achieved = step_flops / len(ops) / (avg_launch_ms * 1e-3) / 1e12
+    step_s = total_ms / args.steps * 1e-3
+    achieved = step_flops / step_s / 1e12
+    # algorithmic bytes: each operand read once, C written once (for a
+    # convolution: x, the filters and y, not the im2col matrix)
+    step_bytes = sum(ESIZE[o["dt"]] * (o["hA"].numel() + o["hB"].numel()) + C_ESIZE[o["dt"]] * o["C"].numel()
+                     for o in ops)
+    achieved_gbs = step_bytes / step_s / 1e9
     dts = {o["dt"] for o in ops}
     ratio = min(NOMINAL_RATIO[d] for d in dts)
     peak = round(float(peaks["bf16_tflops"]) * ratio, 1)
+    hbm_peak = float(peaks["hbm_gbs"])
+    # the ridge of the two measured peaks: flops per byte where HBM and the
+    # tensor cores take equally long
+    ridge = peak * 1e12 / (hbm_peak * 1e9)
+    intensity = step_flops / step_bytes
+    tensor_roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                   "frac": round(achieved / peak, 4)}
+    hbm_roof = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(achieved_gbs / hbm_peak, 4),
+                "peak_source": f"{peak_src} device copy bandwidth (hbm_gbs)"}
     peak_desc = (f"{peak_src} bf16 dense (cuBLAS burst); fp16 has the same nominal rate (ratio 1)"
                  if ratio == 1.0 else
                  f"{peak_src} bf16 dense (cuBLAS burst) x nominal fp8/bf16 ratio 4.5/2.25" if ratio > 1.0 else
@@ -334,23 +455,23 @@ def run_ours(args, rank, world, local_rank):
             "workload": DESCRIPTIONS.get(args.workload, args.workload),
             "gemms_per_step": len(ops),
             "shapes": [[o["M"], o["N"], o["K"], o["dt"]] for o in ops],
-            "l2": f"flushed before every GEMM ({L2_FLUSH_BYTES >> 20} MiB device write, outside the timed interval)",
+            "l2": (f"flushed before every GEMM, outside the timed interval: a {L2_FLUSH_BYTES >> 20} MiB device "
+                   f"write" + (f", then a {L2_FLUSH_BYTES >> 20} MiB read of another buffer (no dirty line of "
+                               f"the write left to write back)" if args.l2 == "clean" else "")),
             "parallelism": f"independent problem per GPU x{world}" if world > 1 else "single GPU",
         },
         "pct_of_peak": round(100.0 * value / world / peak, 2),
         "per_gemm": {k: {"ms": round(v["ms"], 5), "tflops": round(v["tflops"], 1)} for k, v in per_kind.items()},
-        "roofline": {
-            "bound": "tensor",
-            "kernel": "hg::hgemm_tc_kernel",
-            "achieved": round(achieved, 1),
-            "peak": peak,
-            "peak_source": peak_desc,
-            "unit": "TFLOP/s",
-            "frac": round(achieved / peak, 4),
-            "traffic": None,
-            "algorithmic_bytes_per_launch": (ESIZE[ops[0]["dt"]] * (ops[0]["hA"].numel() + ops[0]["hB"].numel()) +
-                                             C_ESIZE[ops[0]["dt"]] * ops[0]["M"] * ops[0]["N"]),
-        },
+        "roofline": dict(
+            (hbm_roof if intensity < ridge else dict(tensor_roof, peak_source=peak_desc)),
+            kernel="hg::hgemm_tc_kernel",
+            traffic=None,
+            algorithmic_bytes_per_launch=step_bytes // len(ops),
+            algorithmic_flops_per_launch=step_flops // len(ops),
+            intensity_flop_per_byte=round(intensity, 1),
+            ridge_flop_per_byte=round(ridge, 1),
+            other=(dict(tensor_roof, peak_source=peak_desc) if intensity < ridge else hbm_roof),
+        ),
         "clocks": clocks,
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
@@ -546,8 +667,13 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--traffic-file", default=os.path.join(ROOT, "profiles", "traffic_square4096.json"))
+    ap.add_argument("--traffic-file", default=None,
+                    help="ncu DRAM-traffic record (default: profiles/traffic_<workload>.json)")
+    ap.add_argument("--l2", choices=["clean", "dirty"], default="clean",
+                    help="clean: flush by a write then a read larger than L2; dirty: the write alone")
     args = ap.parse_args()
+    if args.traffic_file is None:
+        args.traffic_file = os.path.join(ROOT, "profiles", f"traffic_{args.workload}.json")
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
 
