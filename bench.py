@@ -68,7 +68,13 @@ WORKLOADS = {
     # the FP8 variant: E4M3 operands (uniform over [-8, 8) rounded to E4M3),
     # per-channel scales uniform in [0.5, 2), bf16 C
     "fp8_4096": [(4096, 4096, 4096, "e4m3", "uniform", 8.0, 1)],
+    # the block-scaled FP8 variant: the same operands, one fp32 factor per
+    # 64 x 64 (or 32 x 32) sub-block of A and of B, uniform in [0.5, 2)
+    "fp8bs_4096": [(4096, 4096, 4096, "e4m3", "uniform", 8.0, 1)],
+    "fp8bs32_4096": [(4096, 4096, 4096, "e4m3", "uniform", 8.0, 1)],
 }
+# block-scaled workloads: name -> scale block
+BLOCK_SCALED = {"fp8bs_4096": 64, "fp8bs32_4096": 32}
 # convolution workloads (im2col + GEMM): name -> (N, H, W, C, R, S, K, stride, pad, dtype, seed)
 CONV_WORKLOADS = {
     "conv3x3_resnet": (32, 28, 28, 256, 3, 3, 512, 1, 1, "bf16", 1),
@@ -77,12 +83,20 @@ DESCRIPTIONS = {
     "square4096": "GEMM M=N=K=4096, once bf16 and once fp16, A/B row-major, U[-1,1) seed 1",
     "tf32_4096": "TF32 GEMM M=N=K=4096, fp32 A/B/C row-major, U[-1,1) seed 1",
     "fp8_4096": "FP8 GEMM M=N=K=4096, E4M3 A/B row-major (U[-8,8) rounded), per-channel scales, bf16 C, seed 1",
+    "fp8bs_4096": ("block-scaled FP8 GEMM M=N=K=4096, E4M3 A/B row-major (U[-8,8) rounded), one fp32 factor "
+                   "per 64x64 sub-block of A and of B (U[0.5,2)), bf16 C, seed 1"),
+    "fp8bs32_4096": ("block-scaled FP8 GEMM M=N=K=4096, E4M3 A/B row-major (U[-8,8) rounded), one fp32 factor "
+                     "per 32x32 sub-block of A and of B (U[0.5,2)), bf16 C, seed 1"),
     "conv3x3_resnet": ("conv2d as a GEMM (implicit, TMA im2col): x 32x28x28x256 (NHWC), w 3x3x256x512 (RSCK), "
                        "stride 1, pad 1, bf16, U[-1,1) seed 1"),
 }
 METRICS = {
     "tf32_4096": "TF32 GEMM TFLOP/s at M=N=K=4096 (fp32 in and out); % of GB300 dense tf32 tensor-core peak",
     "fp8_4096": "FP8 (E4M3) GEMM TFLOP/s at M=N=K=4096 with per-channel scales; % of GB300 dense fp8 tensor-core peak",
+    "fp8bs_4096": ("block-scaled FP8 (E4M3, fp32 scale per 64x64 sub-block) GEMM TFLOP/s at M=N=K=4096; "
+                   "% of GB300 dense fp8 tensor-core peak"),
+    "fp8bs32_4096": ("block-scaled FP8 (E4M3, fp32 scale per 32x32 sub-block) GEMM TFLOP/s at M=N=K=4096; "
+                     "% of GB300 dense fp8 tensor-core peak"),
     "conv3x3_resnet": ("conv2d as an implicit GEMM (TMA im2col) TFLOP/s, 2*N*P*Q*K*R*S*C flops; "
                        "% of GB300 dense bf16 tensor-core peak"),
 }
@@ -298,12 +312,18 @@ def run_ours(args, rank, world, local_rank):
         ops.append(dict(kind="conv", M=cN * cP * cQ, N=cK, K=cR * cS * cC, dt=dt, hA=x, hB=w, A=x.to(dev),
                         B=w.to(dev), sa=None, sb=None, conv=(cN, cH, cW, cC, cK, cR, cS, cst, cpd),
                         C=torch.empty((cN, cP, cQ, cK), dtype=inputs.TORCH_DTYPES[dt], device=dev)))
+    bs = BLOCK_SCALED.get(args.workload, 0)
     for (M, N, K, dt, dist, sigma, seed) in gemms:
         if dt in FP8:
             A = torch.from_numpy(inputs.generate_fp8((M, K), dt, seed, 0, sigma))
             B = torch.from_numpy(inputs.generate_fp8((K, N), dt, seed, 1, sigma))
-            sa = torch.from_numpy(inputs.generate_scales(M, seed, 2)).to(dev)
-            sb = torch.from_numpy(inputs.generate_scales(N, seed, 3)).to(dev)
+            if bs:
+                ga, gb = (-(-M // bs), -(-K // bs)), (-(-K // bs), -(-N // bs))
+                sa = torch.from_numpy(inputs.generate_scales(ga[0] * ga[1], seed, 2).reshape(ga)).to(dev)
+                sb = torch.from_numpy(inputs.generate_scales(gb[0] * gb[1], seed, 3).reshape(gb)).to(dev)
+            else:
+                sa = torch.from_numpy(inputs.generate_scales(M, seed, 2)).to(dev)
+                sb = torch.from_numpy(inputs.generate_scales(N, seed, 3)).to(dev)
             cdt = torch.bfloat16
         else:
             A = inputs.generate((M, K), dt, seed, 0, dist, sigma)
@@ -325,6 +345,9 @@ def run_ours(args, rank, world, local_rank):
     def one_gemm(o):
         if o.get("kind") == "conv":
             hg.hgemm_conv2d(o["A"], o["B"], o["C"], *o["conv"], o["dt"], stream)
+        elif o["dt"] in FP8 and bs:
+            hg.hgemm_fp8_blockscaled(o["A"], o["B"], o["C"], o["sa"], o["sb"], o["M"], o["N"], o["K"], bs, o["dt"],
+                                     None, stream)
         elif o["dt"] in FP8:
             hg.hgemm_fp8(o["A"], o["B"], o["C"], o["sa"], o["sb"], o["M"], o["N"], o["K"], o["dt"], None, stream)
         else:
@@ -380,7 +403,7 @@ def run_ours(args, rank, world, local_rank):
         pinned.append((o["hA"].pin_memory(), o["hB"].pin_memory(),
                        torch.empty((o["M"], o["N"]), dtype=o["C"].dtype).pin_memory()))
     def host_step(o, pa, pb, pc):
-        if o.get("kind") == "conv":
+        if o.get("kind") == "conv" or bs:
             # host x, w -> device, convolution, y -> host, through the binding
             o["A"].copy_(pa, non_blocking=True)
             o["B"].copy_(pb, non_blocking=True)
@@ -475,7 +498,9 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks,
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "path": "hgemm_host: pinned host A,B -> device, GEMM, C -> pinned host, per GEMM"},
+                "path": ("pinned host operands -> device (cudaMemcpyAsync), the GEMM through the binding, "
+                         "C -> pinned host, per GEMM" if (bs or args.workload in CONV_WORKLOADS) else
+                         "hgemm_host: pinned host A,B -> device, GEMM, C -> pinned host, per GEMM")},
         "gpu_launches": n_ev,
         "wall_s_timed_region": round(wall, 4),
     }
@@ -532,9 +557,21 @@ def _oracle_sample(workload, rows, cols):
     from half_precision_dense_gb300 import inputs
 
     out = []
+    bs = BLOCK_SCALED.get(workload, 0)
     for (M, N, K, dt, dist, sigma, seed) in WORKLOADS[workload]:
         ri = np.linspace(0, M - 1, min(rows, M)).astype(np.int64)
         ci = np.linspace(0, N - 1, min(cols, N)).astype(np.int64)
+        if dt in FP8 and bs:
+            # the leading rows x cols block of C (whole scale blocks), with
+            # the factor grids of its operands
+            r, c = min(M, -(-rows // bs) * bs), min(N, -(-cols // bs) * bs)
+            A = inputs.generate_fp8((M, K), dt, seed, 0, sigma)[:r]
+            B = inputs.generate_fp8((K, N), dt, seed, 1, sigma)[:, :c]
+            ga, gb = (-(-M // bs), -(-K // bs)), (-(-K // bs), -(-N // bs))
+            sa = inputs.generate_scales(ga[0] * ga[1], seed, 2).reshape(ga)[: -(-r // bs)]
+            sb = inputs.generate_scales(gb[0] * gb[1], seed, 3).reshape(gb)[:, : -(-c // bs)]
+            out.append((np.ascontiguousarray(A), np.ascontiguousarray(B), dt, K, ("blocks", sa, sb, bs)))
+            continue
         if dt in FP8:
             A = inputs.generate_fp8((M, K), dt, seed, 0, sigma)
             B = inputs.generate_fp8((K, N), dt, seed, 1, sigma)
@@ -561,6 +598,8 @@ def _oracle_step(sample):
     for (a, b, dt, K, scales) in sample:
         if dt == "f32":
             tf32_oracle.gemm(a, b)
+        elif dt in FP8 and isinstance(scales[0], str):
+            fp8_oracle.gemm_blockscaled(a, b, dt, scales[1], scales[2], scales[3])
         elif dt in FP8:
             fp8_oracle.gemm(a, b, dt, scales[0], scales[1])
         else:
@@ -602,6 +641,8 @@ def _sample_desc(side, workload):
                 f"computed by the CPU oracle from the convolution's definition (fp64 taps + bit-level RNE)")
     dts = {g[3] for g in WORKLOADS[workload]}
     how = ("numpy fp64 product of the tf32-truncated operands, rounded to fp32" if dts == {"f32"} else
+           "fp8 decode, per-sub-block fp32 factors, numpy fp64 product, bit-level RNE to bf16"
+           if dts <= set(FP8) and workload in BLOCK_SCALED else
            "fp8 decode, numpy fp64 product, per-channel scales, bit-level RNE to bf16" if dts <= set(FP8) else
            "numpy fp64 product + bit-level RNE")
     return (f"each step: the {side} x {side} block of C at evenly spaced rows and columns of every "

@@ -93,6 +93,11 @@ def load_library():
         lib.hgemm_fp8_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ctypes.c_int,
                                      ctypes.POINTER(_Config), vp]
         lib.hgemm_fp8_ex.restype = ctypes.c_int
+        lib.hgemm_fp8_blockscaled.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, ctypes.c_int, vp]
+        lib.hgemm_fp8_blockscaled.restype = ctypes.c_int
+        lib.hgemm_fp8_blockscaled_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, ctypes.c_int,
+                                                 ctypes.POINTER(_Config), vp]
+        lib.hgemm_fp8_blockscaled_ex.restype = ctypes.c_int
         lib.hgemm_conv2d.argtypes = [vp, vp, vp] + [i32] * 9 + [ctypes.c_int, vp]
         lib.hgemm_conv2d.restype = ctypes.c_int
         lib.hgemm_conv2d_set_mode.argtypes = [ctypes.c_int32]
@@ -201,6 +206,22 @@ def hgemm_fp8(A, B, C, a_scale, b_scale, M: int, N: int, K: int, dtype, config: 
     else:
         _check(lib.hgemm_fp8_ex(_ptr(A), _ptr(B), _ptr(C), _ptr(a_scale), _ptr(b_scale), M, N, K, code,
                                 ctypes.byref(config._c()), _stream(stream)))
+
+
+def hgemm_fp8_blockscaled(A, B, C, a_scale, b_scale, M: int, N: int, K: int, block: int, dtype,
+                          config: Config | None = None, stream=None) -> None:
+    """C (bf16) = the product of A and B dequantised with one fp32 factor per
+    block x block sub-block (block 32 or 64): a_scale is ceil(M/block) x
+    ceil(K/block), b_scale ceil(K/block) x ceil(N/block), both row-major fp32
+    device arrays (see include/hgemm.h)."""
+    lib = load_library()
+    code = _dtype_code(dtype)
+    if config is None:
+        _check(lib.hgemm_fp8_blockscaled(_ptr(A), _ptr(B), _ptr(C), _ptr(a_scale), _ptr(b_scale), M, N, K,
+                                         int(block), code, _stream(stream)))
+    else:
+        _check(lib.hgemm_fp8_blockscaled_ex(_ptr(A), _ptr(B), _ptr(C), _ptr(a_scale), _ptr(b_scale), M, N, K,
+                                            int(block), code, ctypes.byref(config._c()), _stream(stream)))
 
 
 def hgemm_conv2d(x, w, y, N: int, H: int, W: int, C: int, K: int, R: int, S: int, stride: int, pad: int,

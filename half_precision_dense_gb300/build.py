@@ -21,7 +21,8 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_DIR = os.path.join(PKG, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "libhgemm.so")
 
-SOURCES = ["hgemm_api.cu", "hgemm_tc_bf16.cu", "hgemm_tc_f16.cu", "hgemm_tc_tf32.cu", "hgemm_tc_fp8.cu", "hgemm_aux.cu",
+SOURCES = ["hgemm_api.cu", "hgemm_tc_bf16.cu", "hgemm_tc_f16.cu", "hgemm_tc_tf32.cu", "hgemm_tc_fp8.cu", "hgemm_tc_fp8bs.cu",
+           "hgemm_aux.cu",
            "hgemm_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",

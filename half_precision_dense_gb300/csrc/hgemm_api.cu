@@ -626,10 +626,14 @@ hgemm_status_t fit_split_to_device(int64_t M, int64_t N, int64_t K, hgemm_dtype_
 // aligned base: the library's own im2col matrix), so A needs no repack.
 // `conv` (implicit-GEMM convolution): A is the activations x behind an
 // im2col-mode tensor map; hgemm_conv2d has checked the operands.
+// `bs_block` (32 or 64; 0 = none): the block-scaled fp8 GEMM, a_scale and
+// b_scale being the fp32 grids of one factor per bs_block x bs_block
+// sub-block of A and of B (hgemm_fp8_blockscaled has checked them).
 hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
                    hgemm_dtype_t dtype, const hgemm_config_t* cfg, cudaStream_t stream,
                    void* scratch = nullptr, size_t scratch_bytes = 0, const float* a_scale = nullptr,
-                   const float* b_scale = nullptr, int64_t lda_in = 0, const hg::ConvShape* conv = nullptr) {
+                   const float* b_scale = nullptr, int64_t lda_in = 0, const hg::ConvShape* conv = nullptr,
+                   int bs_block = 0) {
     t_last_error.clear();
     hgemm_status_t st = conv ? HGEMM_OK : check_args(A, B, C, M, N, K, dtype);
     if (st != HGEMM_OK || M == 0 || N == 0) return st;
@@ -649,7 +653,24 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
     hgemm_plan_t pl;
     const bool a_bad = (lda_in > 0 || conv) ? false : misaligned16(A, K, es);
     const bool b_bad = misaligned16(B, N, es), c_bad = misaligned16(C, N, ces);
-    if ((st = make_plan(M, N, K, dtype, cfg, info.sms, a_bad, b_bad, c_bad, &pl, !conv)) != HGEMM_OK) return st;
+    hgemm_config_t bs_cfg{};
+    if (bs_block) {
+        // block-scaled fp8: 128-column tiles, whole tiles; a CTA pair per
+        // 256-row tile unless the problem has a single 128-row tile row
+        if (cfg) bs_cfg = *cfg;   // fields checked by hgemm_fp8_blockscaled_ex
+        if (bs_cfg.cta_group == 0) bs_cfg.cta_group = M > 128 ? 2 : 1;
+        bs_cfg.block_n = 128;
+        bs_cfg.split_k = 1;
+        bs_cfg.stream_k = 1;
+        cfg = &bs_cfg;
+    }
+    if ((st = make_plan(M, N, K, dtype, cfg, info.sms, a_bad, b_bad, c_bad, &pl, !conv && !bs_block)) != HGEMM_OK)
+        return st;
+    if (bs_block) {
+        pl.stages = hg::fp8bs_stages(pl.cta_group);
+        pl.smem_bytes = hg::fp8bs_smem_bytes(pl.cta_group);
+        pl.tmem_cols = hg::fp8bs_tmem_cols();
+    }
     if (conv && pl.split_k > 1) {
         t_last_error = "split_k is not built for the convolution";
         return HGEMM_ERR_INVALID_ARG;
@@ -660,7 +681,10 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
     // the planner assumed. The kernel's cluster multiplier is the CTAs
     // splitting K.
     int resident = 0;
-    if ((st = fit_split_to_device(M, N, K, dtype, cfg, info.sms, a_bad, b_bad, c_bad, &pl, &resident)) != HGEMM_OK)
+    if (bs_block)
+        resident = hg::max_active_clusters_fp8bs(static_cast<int>(dtype), pl.cta_group, bs_block);
+    else if ((st = fit_split_to_device(M, N, K, dtype, cfg, info.sms, a_bad, b_bad, c_bad, &pl, &resident)) !=
+             HGEMM_OK)
         return st;
     const int cg = pl.cta_group, bn = pl.block_n, mc = pl.split_k > 1 ? pl.split_k : 1;
     const int64_t num_kb = cdiv(K, bk);
@@ -740,16 +764,56 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
          (st = encode_2d(&tb2, dtype, b_use, K, N, ldb, static_cast<uint32_t>(b_last), ubk,
                          dtype == HGEMM_TF32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B)) !=
              HGEMM_OK) ||
-        (pl.store_mode == 1 &&
+        (pl.store_mode == 1 && !bs_block &&
          (st = encode_2d(&tc, c_dtype_of(dtype), C, M, N, N, static_cast<uint32_t>(128 / ces), hg::kEpiBoxRows)) !=
              HGEMM_OK) ||
         // the 32-column last chunk of a 16-bit C (fp32 C leaves in 32-column
         // boxes throughout, through tc)
-        (pl.store_mode == 1 && bn % 64 != 0 && ces == 2 &&
+        (pl.store_mode == 1 && !bs_block && bn % 64 != 0 && ces == 2 &&
          (st = encode_2d(&tc32, c_dtype_of(dtype), C, M, N, N, 32, hg::kEpiBoxRows, CU_TENSOR_MAP_SWIZZLE_64B)) !=
              HGEMM_OK)) {
         if (work && work != scratch) cudaFreeAsync(work, stream);
         return st;
+    }
+
+    if (bs_block) {
+        hg::Fp8bsParams q{};
+        q.M = static_cast<int32_t>(M);
+        q.N = static_cast<int32_t>(N);
+        q.K = static_cast<int32_t>(K);
+        q.tiles_m = pl.tiles_m;
+        q.tiles_n = pl.tiles_n;
+        q.num_tiles = pl.num_tiles;
+        q.group_m = pl.group_m;
+        q.num_kb = static_cast<int32_t>(cdiv(K, bk));
+        q.num_sb = static_cast<int32_t>(cdiv(K, bs_block));
+        q.sa_rows = static_cast<int32_t>(cdiv(M, bs_block));
+        q.sb_cols = static_cast<int32_t>(cdiv(N, bs_block));
+        // kind::f8f6f4: D fp32, A and B format (0 E4M3, 1 E5M2), A K-major,
+        // B MN-major, N = 128, M = 128 per CTA
+        const uint32_t f8 = dtype == HGEMM_E5M2 ? 1u : 0u;
+        q.idesc = (1u << 4) | (f8 << 7) | (f8 << 10) | (1u << 16) | (static_cast<uint32_t>(bn >> 3) << 17) |
+                  (static_cast<uint32_t>((128 * cg) >> 4) << 24);
+        q.a_scale = a_scale;
+        q.b_scale = b_scale;
+        q.C = static_cast<uint16_t*>(C);
+        q.ldc = N;
+        q.c_vec = c_bad ? 0 : 1;
+        q.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+        q.sched.num_tiles = pl.num_tiles;
+        q.sched.dp_tiles = pl.dp_tiles;
+        q.sched.num_kb = q.num_kb;
+        q.sched.clusters = clusters;
+        q.sched.sk_base = 0;
+        q.sched.sk_extra = 0;
+        if ((e = hg::status_word_ptr(&q.status)) != cudaSuccess) {
+            if (work && work != scratch) cudaFreeAsync(work, stream);
+            return cuda_fail(e, "status word");
+        }
+        e = hg::launch_fp8bs(static_cast<int>(dtype), cg, bs_block, ta, tb, tb2, q, clusters, stream);
+        if (work && work != scratch) cudaFreeAsync(work, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+        return HGEMM_OK;
     }
 
     TcParams p{};
@@ -873,6 +937,39 @@ hgemm_status_t hgemm_fp8_ex(const void* A, const void* B, void* C, const float* 
         return HGEMM_ERR_INVALID_ARG;
     }
     return run(A, B, C, M, N, K, dtype, cfg, static_cast<cudaStream_t>(stream), nullptr, 0, a_scale, b_scale);
+}
+
+hgemm_status_t hgemm_fp8_blockscaled_ex(const void* A, const void* B, void* C, const float* a_scale,
+                                        const float* b_scale, int64_t M, int64_t N, int64_t K, int32_t block,
+                                        hgemm_dtype_t dtype, const hgemm_config_t* cfg, void* stream) {
+    t_last_error.clear();
+    if (!is_fp8(dtype)) {
+        t_last_error = "hgemm_fp8_blockscaled takes HGEMM_E4M3 or HGEMM_E5M2";
+        return HGEMM_ERR_INVALID_ARG;
+    }
+    if (block != 32 && block != 64) {
+        t_last_error = "the scale block is 32 or 64";
+        return HGEMM_ERR_INVALID_ARG;
+    }
+    if (cfg && ((cfg->block_n != 0 && cfg->block_n != 128) || cfg->split_k > 1 || cfg->stream_k > 1 ||
+                cfg->store_mode != 0 || cfg->cta_group < 0 || cfg->cta_group > 2)) {
+        t_last_error = "the block-scaled fp8 GEMM takes cta_group 1 or 2, block_n 128, whole tiles and its "
+                       "own stores";
+        return HGEMM_ERR_INVALID_ARG;
+    }
+    if (M > 0 && N > 0 && K > 0 &&
+        (!a_scale || !b_scale || (reinterpret_cast<uintptr_t>(a_scale) & 3u) || (reinterpret_cast<uintptr_t>(b_scale) & 3u))) {
+        t_last_error = "a_scale and b_scale must be 4-byte aligned device arrays";
+        return HGEMM_ERR_INVALID_ARG;
+    }
+    return run(A, B, C, M, N, K, dtype, cfg, static_cast<cudaStream_t>(stream), nullptr, 0, a_scale, b_scale, 0,
+               nullptr, block);
+}
+
+hgemm_status_t hgemm_fp8_blockscaled(const void* A, const void* B, void* C, const float* a_scale,
+                                     const float* b_scale, int64_t M, int64_t N, int64_t K, int32_t block,
+                                     hgemm_dtype_t dtype, void* stream) {
+    return hgemm_fp8_blockscaled_ex(A, B, C, a_scale, b_scale, M, N, K, block, dtype, nullptr, stream);
 }
 
 hgemm_status_t hgemm_conv2d(const void* x, const void* w, void* y, int32_t N, int32_t H, int32_t W, int32_t C,

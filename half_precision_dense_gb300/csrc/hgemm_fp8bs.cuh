@@ -1,0 +1,364 @@
+// hgemm_fp8bs.cuh - the block-scaled FP8 GEMM kernel for sm_103a:
+//
+//   C[i][j] = bf16( sum_kb  a_scale[i / bs][kb] * b_scale[kb][j / bs]
+//                           * sum_{k in block kb} A[i][k] * B[k][j] )
+//
+// A (M x K) and B (K x N) are row-major E4M3 or E5M2 patterns, each
+// bs x bs sub-block of A and of B carrying one fp32 factor (bs = 32 or 64):
+// "深度学习加速核心：GEMM优化从分块到TensorCore的实战解析", section 4.3 (FP8 data
+// is scaled block-wise, one factor per 32 x 32 or 64 x 64 sub-block) and
+// section 5.2, the third mishap (the factors must be 32-bit: a 16-bit one
+// overflowed). C is bfloat16, rounded once to nearest even.
+//
+// A factor that varies along K cannot be taken out of one tensor-core sum,
+// and the hardware's own block-scaled MMA kinds take only power-of-two (UE8M0)
+// factors. So the sum is split at the scale blocks:
+//
+//   MMA warp   for each scale block (bs / 32 kind::f8f6f4 MMAs of K = 32) it
+//              writes the block's fp32 partial sum into one of four 128-column
+//              TMEM buffers (accumulate flag off for the block's first MMA) and
+//              commits that buffer's `full` barrier; the tensor core therefore
+//              runs up to four scale blocks ahead of the epilogue.
+//   epilogue   warp w owns TMEM lane quarter w % 4 (32 rows of C, one per
+//              thread) and the 64 columns of half w / 4. For each scale block
+//              it loads its part of the partial (tcgen05.ld), hands the buffer
+//              back, forms the factors a_scale * b_scale in fp32 (one per
+//              32-column load: the row block is warp-uniform because a quarter's
+//              32 rows lie in one scale block) and adds factor x partial into
+//              64 fp32 registers with packed two-lane FMAs (fma.rn.f32x2).
+//              After the last block it rounds to bf16 and stores its row.
+//   producers  as in the main kernel: TMA loads of 128 x 128-byte A boxes and
+//              128-row B atoms (read MN-major in the 128-byte swizzle), two
+//              warps on alternate stages of a 7-stage ring.
+//
+// Tiles are 128 x 128 per CTA, or 256 x 128 for a CTA pair (cta_group::2,
+// each CTA feeding 64 B columns). Every wait is bounded as in the main kernel.
+#pragma once
+
+#include "hgemm_tc.cuh"
+
+namespace hg {
+
+struct Fp8bsParams {
+    int32_t M, N, K;
+    int32_t tiles_m, tiles_n, num_tiles, group_m;
+    int32_t num_kb;                 // stages of K: ceil(K / 128)
+    int32_t num_sb;                 // scale blocks along K: ceil(K / bs)
+    int32_t sa_rows;                // ceil(M / bs): rows of the a_scale grid
+    int32_t sb_cols;                // ceil(N / bs): columns of the b_scale grid (its row pitch)
+    uint32_t idesc;                 // tcgen05 instruction descriptor (kind::f8f6f4, N = 128)
+    const float* a_scale;           // sa_rows x num_sb, row-major
+    const float* b_scale;           // num_sb x sb_cols, row-major
+    uint16_t* C;                    // bf16 C, ldc elements between rows
+    int64_t ldc;
+    int32_t c_vec;                  // 1: C 16-byte aligned and N a multiple of 8 (16-byte stores)
+    uint64_t timeout_ns;
+    unsigned long long* status;
+    Schedule sched;                 // whole tiles only
+};
+
+template <int CG>
+struct Fp8bsCfg {
+    static constexpr int BN = 128;
+    using Base = TcCfg<CG, BN, 1, 1>;           // the fp8 stage layout of the main kernel
+    static constexpr int kParts = 4;            // TMEM partial-sum buffers of BN columns
+    static constexpr int kTmemCols = kParts * BN;
+    static constexpr int kBarBytes = 256;
+    static constexpr int kStagesFit = (kSmemLimit - 1024 - kBarBytes) / Base::kStageBytes;
+    static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+    static constexpr int kSmemBytes = 1024 + kStages * Base::kStageBytes + kBarBytes;
+    static_assert(kTmemCols <= 512, "tensor memory");
+    static_assert((2 * kStages + 2 * kParts + 1) * 8 + 8 <= kBarBytes, "barrier area");
+    static_assert(kSmemBytes <= kSmemLimit, "shared memory");
+};
+
+// d = s * a + d on two fp32 lanes at once (d0, d1 += s * (a0, a1)), each lane
+// one fused multiply-add rounded to nearest even.
+__device__ __forceinline__ void fma2_bcast(float& d0, float& d1, float s, float a0, float a1) {
+    asm("{\n\t.reg .b64 d, a, s;\n\t"
+        "mov.b64 d, {%0, %1};\n\t"
+        "mov.b64 a, {%3, %4};\n\t"
+        "mov.b64 s, {%2, %2};\n\t"
+        "fma.rn.f32x2 d, s, a, d;\n\t"
+        "mov.b64 {%0, %1}, d;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "f"(s), "f"(a0), "f"(a1));
+}
+
+template <int CG, int kGs, int kDt>
+__global__ void __launch_bounds__(kThreads, 1)
+hgemm_fp8bs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmB2, const Fp8bsParams p) {
+#if defined(__CUDA_ARCH__) && defined(__CUDA_ARCH_FEAT_SM103_ALL)
+    using Cfg = Fp8bsCfg<CG>;
+    using Base = typename Cfg::Base;
+    constexpr int S = Cfg::kStages;
+    constexpr int R = Cfg::kParts;
+    constexpr int BN = Cfg::BN;
+    constexpr int kSbPerStage = Base::kBK / kGs;   // scale blocks in a 128-deep stage
+    constexpr int kMmaPerSb = kGs / Base::kUK;     // K = 32 MMAs per scale block
+    static_assert(kGs == 32 || kGs == 64, "scale block");
+    static_assert(kDt == 3 || kDt == 4, "fp8 operands");
+    static_assert(Base::kBAtoms == 1, "one B atom per stage");
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* const smem = smem_raw + (base - raw);
+    const uint32_t sA = base;
+    const uint32_t sB = sA + S * Base::kABytes;
+    const uint32_t sBar = sB + S * Base::kBBytes;
+    const uint32_t bar_full = sBar;                  // [S]
+    const uint32_t bar_empty = sBar + 8 * S;         // [S]
+    const uint32_t bar_pfull = sBar + 16 * S;        // [R] partial buffer written
+    const uint32_t bar_pempty = bar_pfull + 8 * R;   // [R] partial buffer read
+    const uint32_t bar_drain = bar_pempty + 8 * R;
+    uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(smem + (bar_drain + 8 - base));
+    volatile uint32_t* const abort_flag = tmem_slot + 1;
+
+    const int warp = static_cast<int>(threadIdx.x >> 5);
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t rank = (CG > 1) ? cluster_ctarank() : 0u;   // rank in the CTA pair
+    const int cluster_id = static_cast<int>(blockIdx.x) / CG;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        for (int b = 0; b < R; ++b) {
+            mbar_init(bar_pfull + 8 * b, 1);
+            mbar_init(bar_pempty + 8 * b, kEpiWarps * CG);
+        }
+        mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init_cluster();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        if (Base::kBPartial) tma_prefetch_desc(&tmB2);
+    }
+    if (warp == kMmaWarp) tmem_alloc<CG>(smem_addr(tmem_slot), Cfg::kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    if constexpr (CG > 1) cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+    const Waiter w{abort_flag, p.timeout_ns, p.status};
+
+    if (warp == kProducerWarp || warp == kProducerWarp2) {
+        // ------------------------------------------------------------ producer
+        const uint32_t pid = warp == kProducerWarp ? 0u : 1u;
+        uint32_t stage = pid, phase = 0, g = 0;
+        bool ok = true;
+        WorkUnit wu;
+        for (int lu = 0; ok && next_unit(p.sched, cluster_id, lu, wu); ++lu) {
+            int32_t tm, tn;
+            tile_coord(wu.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+            const int32_t m0 = tm * kBlockMCta * CG + static_cast<int32_t>(rank) * kBlockMCta;
+            const int32_t n0 = tn * BN + static_cast<int32_t>(rank) * Base::kBnCta;
+            for (int kb = 0; kb < p.num_kb; ++kb, ++g) {
+                if ((g & 1u) != pid) continue;
+                if (!wait_bar_warp(bar_empty + 8 * stage, phase ^ 1u, w, kRoleProducer, stage)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t a_dst = sA + stage * Base::kABytes;
+                const uint32_t b_dst = sB + stage * Base::kBBytes;
+                const uint32_t fb = bar_full + 8 * stage;
+                const int32_t k0 = kb * Base::kBK;
+                const CUtensorMap* bmap = Base::kBPartial ? &tmB2 : &tmB;
+                if (elect_one_sync()) {
+                    if constexpr (CG == 1) {
+                        mbar_arrive_expect_tx(fb, Base::kTxBytes);
+                        tma_load_2d(a_dst, &tmA, fb, k0, m0);
+                        tma_load_2d(b_dst, bmap, fb, n0, k0);
+                    } else {
+                        const uint32_t fb_leader = mapa_shared(fb, 0);
+                        if (rank == 0) mbar_arrive_expect_tx(fb, Base::kTxBytes);
+                        tma_load_2d_pair(a_dst, &tmA, fb_leader, k0, m0);
+                        tma_load_2d_pair(b_dst, bmap, fb_leader, n0, k0);
+                    }
+                }
+                __syncwarp();
+                stage += 2;
+                if (stage >= static_cast<uint32_t>(S)) {
+                    stage -= S;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (!ok) {
+            // loads already issued still land in this CTA's shared memory
+            const uint64_t t0 = globaltimer_ns();
+            while (globaltimer_ns() - t0 < 50000ull) {}
+        }
+    } else if (warp == kMmaWarp) {
+        // ----------------------------------------------------------------- MMA
+        if (rank == 0) {
+            uint32_t stage = 0, phase = 0, pb = 0, pph = 0;
+            bool ok = true, issued = false;
+            const uint64_t a_desc0 = sdesc_sw128(sA, 16u, 1024u);
+            const uint64_t b_desc0 = sdesc_sw128(sB, Base::kBAtomBytes, 1024u);
+            WorkUnit wu;
+            for (int it = 0; ok && next_unit(p.sched, cluster_id, it, wu); ++it) {
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bar_warp(bar_full + 8 * stage, phase, w, kRoleMma, stage)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = a_desc0 + ((stage * Base::kABytes) >> 4);
+                    const uint64_t bd = b_desc0 + ((stage * Base::kBBytes) >> 4);
+                    const int rem = p.num_sb - kb * kSbPerStage;
+                    const int nsb = rem < kSbPerStage ? rem : kSbPerStage;
+                    for (int j = 0; j < nsb; ++j) {
+                        if (!wait_bar_warp(bar_pempty + 8 * pb, pph ^ 1u, w, kRoleMma, 32 + pb)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t d_tmem = tmem_base + pb * BN;
+                        if (elect_one_sync()) {
+#pragma unroll
+                            for (int mm = 0; mm < kMmaPerSb; ++mm) {
+                                const uint32_t kk = static_cast<uint32_t>(j * kMmaPerSb + mm);
+                                umma_f8<CG>(d_tmem, ad + 2u * kk, bd + 8u * Base::kUK * kk, p.idesc, mm > 0 ? 1u : 0u);
+                            }
+                            if constexpr (CG == 1) umma_commit(bar_pfull + 8 * pb);
+                            else umma_commit_pair(bar_pfull + 8 * pb, static_cast<uint16_t>(0x3u));
+                        }
+                        __syncwarp();
+                        issued = true;
+                        if (++pb == static_cast<uint32_t>(R)) {
+                            pb = 0;
+                            pph ^= 1u;
+                        }
+                    }
+                    if (!ok) break;
+                    if (elect_one_sync()) {
+                        if constexpr (CG == 1) umma_commit(bar_empty + 8 * stage);
+                        else umma_commit_pair(bar_empty + 8 * stage, static_cast<uint16_t>(0x3u));
+                    }
+                    __syncwarp();
+                    if (++stage == static_cast<uint32_t>(S)) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok && issued) {
+                // TMEM may only be freed once every issued MMA has completed.
+                if (elect_one_sync()) {
+                    if constexpr (CG == 1) umma_commit(bar_drain);
+                    else umma_commit_pair(bar_drain, static_cast<uint16_t>(0x1u));
+                }
+                __syncwarp();
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(bar_drain, 0) && globaltimer_ns() - t0 < p.timeout_ns) {}
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int quarter = warp & 3;
+        const int colhalf = warp >> 2;
+        uint32_t pb = 0, pph = 0;
+        bool ok = true;
+        WorkUnit wu;
+        for (int it = 0; ok && next_unit(p.sched, cluster_id, it, wu); ++it) {
+            int32_t tm, tn;
+            tile_coord(wu.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+            const int32_t row_base = tm * kBlockMCta * CG + static_cast<int32_t>(rank) * kBlockMCta + quarter * 32;
+            const int32_t col_base = tn * BN + 64 * colhalf;
+            // Scale rows and columns of this warp (warp-uniform; clamped for
+            // rows and columns past the matrix, whose partial sums are zero).
+            int32_t rb = row_base / kGs;
+            if (rb > p.sa_rows - 1) rb = p.sa_rows - 1;
+            int32_t cb0 = col_base / kGs, cb1 = (col_base + 32) / kGs;
+            if (cb0 > p.sb_cols - 1) cb0 = p.sb_cols - 1;
+            if (cb1 > p.sb_cols - 1) cb1 = p.sb_cols - 1;
+            const float* sa_row = p.a_scale + static_cast<int64_t>(rb) * p.num_sb;
+            const float* sb_c0 = p.b_scale + cb0;
+            const float* sb_c1 = p.b_scale + cb1;
+            float acc[64];
+#pragma unroll
+            for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
+            float nsa = __ldg(sa_row), nsb0 = __ldg(sb_c0), nsb1 = __ldg(sb_c1);
+            const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
+            for (int sbk = 0; sbk < p.num_sb; ++sbk) {
+                const float csa = nsa, csb0 = nsb0, csb1 = nsb1;
+                if (sbk + 1 < p.num_sb) {
+                    // next block's factors, loaded while this block's partial is awaited
+                    nsa = __ldg(sa_row + sbk + 1);
+                    nsb0 = __ldg(sb_c0 + static_cast<int64_t>(sbk + 1) * p.sb_cols);
+                    nsb1 = __ldg(sb_c1 + static_cast<int64_t>(sbk + 1) * p.sb_cols);
+                }
+                if (!wait_bar_warp(bar_pfull + 8 * pb, pph, w, kRoleEpilogue, 32 + pb)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t r0[32], r1[32];
+                const uint32_t t_col = tmem_base + pb * BN + 64u * static_cast<uint32_t>(colhalf) + t_lane;
+                tmem_ld_32x32b_x32(t_col, r0);
+                tmem_ld_32x32b_x32(t_col + 32u, r1);
+                tmem_ld_wait();
+                reg_fence(r0);
+                reg_fence(r1);
+                // the buffer's reads are done: hand it back to the MMA warp
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) release_accumulator<CG>(bar_pempty + 8 * pb, 0);
+                if (++pb == static_cast<uint32_t>(R)) {
+                    pb = 0;
+                    pph ^= 1u;
+                }
+                const float s0 = csa * csb0;
+                const float s1 = csa * csb1;
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    fma2_bcast(acc[i], acc[i + 1], s0, __uint_as_float(r0[i]), __uint_as_float(r0[i + 1]));
+                    fma2_bcast(acc[32 + i], acc[33 + i], s1, __uint_as_float(r1[i]), __uint_as_float(r1[i + 1]));
+                }
+            }
+            if (!ok) break;
+            // Round to bf16 and store this thread's row: 64 columns from col_base.
+            const int32_t row = row_base + static_cast<int32_t>(lane);
+            if (row < p.M) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    pk[i] = pack_rn<kDt>(__float_as_uint(acc[2 * i]), __float_as_uint(acc[2 * i + 1]));
+                uint16_t* crow = p.C + static_cast<int64_t>(row) * p.ldc;
+                if (p.c_vec) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int32_t col = col_base + 8 * j;
+                        if (col < p.N)
+                            *reinterpret_cast<uint4*>(crow + col) =
+                                make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) {
+                        const int32_t col = col_base + i;
+                        if (col < p.N)
+                            crow[col] = static_cast<uint16_t>((i & 1) ? (pk[i >> 1] >> 16) : (pk[i >> 1] & 0xFFFFu));
+                    }
+                }
+            }
+        }
+    }
+
+    // ------------------------------------------------------------ teardown
+    __syncthreads();
+    if constexpr (CG > 1) cluster_sync();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc<CG>(tmem_base, Cfg::kTmemCols);
+    }
+#endif
+}
+
+}  // namespace hg

@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include "hgemm.h"
+#include "hgemm_fp8bs.cuh"
 #include "hgemm_tc.cuh"
 
 namespace hg {
@@ -39,6 +40,16 @@ cudaError_t launch_tc_fp8(int kind, int cta_group, int block_n, int mc, const CU
                           const CUtensorMap& b, const CUtensorMap& c, const CUtensorMap& c32, const CUtensorMap& b2,
                           const TcParams& p, int clusters, cudaStream_t stream);
 int max_active_clusters_fp8(int kind, int cta_group, int block_n, int mc);
+
+// The block-scaled fp8 kernel (hgemm_fp8bs.cuh): kind 3 = E4M3, 4 = E5M2;
+// cta_group 1 (128 x 128 tiles) or 2 (256 x 128); gs = 32 or 64 (scale block).
+// B is read in place (MN-major); `b2` loads a pair CTA's 64-column half atom.
+cudaError_t launch_fp8bs(int kind, int cta_group, int gs, const CUtensorMap& a, const CUtensorMap& b,
+                         const CUtensorMap& b2, const Fp8bsParams& p, int clusters, cudaStream_t stream);
+int max_active_clusters_fp8bs(int kind, int cta_group, int gs);
+int fp8bs_stages(int cta_group);
+int fp8bs_smem_bytes(int cta_group);
+int fp8bs_tmem_cols();
 
 // Shared-memory ring depth and bytes of an instantiation (host constants) for
 // operands of `esize` bytes (2: fp16/bf16, 4: tf32, 1: fp8).

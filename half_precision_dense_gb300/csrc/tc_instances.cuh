@@ -9,15 +9,12 @@
 
 namespace hg {
 
-template <int CG, int BN, int kDt, int MC = 1>
-struct TcInstance {
-    // The kernel's own configuration (its operand size sets the stage bytes
-    // and the ring depth), so the launch reserves the shared memory it uses.
-    using Cfg = TcCfg<CG, BN, elem_bytes(kDt), (CG == 1 && MC > 1) ? MC : 1>;
-    static constexpr int kCluster = CG * MC;
-    static constexpr auto kernel() { return &hgemm_tc_kernel<CG, BN, kDt, MC>; }
-
-    // The dynamic shared-memory opt-in is per device; set it once per device.
+// Launch bookkeeping of one persistent cluster kernel: the dynamic
+// shared-memory opt-in (per device, set once), the launch configuration
+// (one cluster of kCluster CTAs per work slot) and the resident clusters
+// (queried once per device).
+template <auto kKernel, int kCluster, int kSmemBytes>
+struct ClusterKernel {
     static cudaError_t prepare() {
         static std::mutex mu;
         static uint64_t done_mask = 0;
@@ -27,8 +24,7 @@ struct TcInstance {
         std::lock_guard<std::mutex> lk(mu);
         const uint64_t bit = 1ull << (dev & 63);
         if (done_mask & bit) return cudaSuccess;
-        e = cudaFuncSetAttribute(kernel(), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Cfg::kSmemBytes);
+        e = cudaFuncSetAttribute(kKernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e == cudaSuccess) done_mask |= bit;
         return e;
     }
@@ -38,7 +34,7 @@ struct TcInstance {
         cfg = cudaLaunchConfig_t{};
         cfg.gridDim = dim3(static_cast<unsigned>(clusters * kCluster), 1, 1);
         cfg.blockDim = dim3(kThreads, 1, 1);
-        cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+        cfg.dynamicSmemBytes = kSmemBytes;
         cfg.stream = stream;
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = kCluster;
@@ -48,18 +44,16 @@ struct TcInstance {
         cfg.numAttrs = 1;
     }
 
-    static cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                              const CUtensorMap& c32, const CUtensorMap& b2, const TcParams& p, int clusters,
-                              cudaStream_t stream) {
+    template <typename... Args>
+    static cudaError_t launch(int clusters, cudaStream_t stream, const Args&... args) {
         cudaError_t e = prepare();
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t cfg;
         cudaLaunchAttribute attr[1];
         fill_config(cfg, attr, clusters, stream);
-        return cudaLaunchKernelEx(&cfg, kernel(), a, b, c, c32, b2, p);
+        return cudaLaunchKernelEx(&cfg, kKernel, args...);
     }
 
-    // Resident clusters per device, queried once per device.
     static int max_clusters() {
         static std::mutex mu;
         static int cache[64] = {};
@@ -74,11 +68,27 @@ struct TcInstance {
         cudaLaunchAttribute attr[1];
         fill_config(cfg, attr, 1, nullptr);
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, kernel(), &cfg) != cudaSuccess) return 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kKernel, &cfg) != cudaSuccess) return 0;
         std::lock_guard<std::mutex> lk(mu);
         cache[dev] = n;
         return n;
     }
+};
+
+template <int CG, int BN, int kDt, int MC = 1>
+struct TcInstance {
+    // The kernel's own configuration (its operand size sets the stage bytes
+    // and the ring depth), so the launch reserves the shared memory it uses.
+    using Cfg = TcCfg<CG, BN, elem_bytes(kDt), (CG == 1 && MC > 1) ? MC : 1>;
+    using K = ClusterKernel<&hgemm_tc_kernel<CG, BN, kDt, MC>, CG * MC, Cfg::kSmemBytes>;
+
+    static cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                              const CUtensorMap& c32, const CUtensorMap& b2, const TcParams& p, int clusters,
+                              cudaStream_t stream) {
+        return K::launch(clusters, stream, a, b, c, c32, b2, p);
+    }
+
+    static int max_clusters() { return K::max_clusters(); }
 };
 
 // Every tile shape of the 16-bit kinds (KDT 0 = fp16, 1 = bf16), and the K

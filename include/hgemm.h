@@ -276,6 +276,48 @@ hgemm_status_t hgemm_fp8_ex(const void* A, const void* B, void* C, const float* 
                             int64_t M, int64_t N, int64_t K, hgemm_dtype_t dtype, const hgemm_config_t* cfg,
                             void* stream);
 
+/*
+ * hgemm_fp8_blockscaled - the FP8 GEMM with one fp32 scale per sub-block
+ * ("深度学习加速核心：GEMM优化从分块到TensorCore的实战解析", section 4.3: FP8
+ * data is scaled block-wise, one factor per 32 x 32 or 64 x 64 sub-block;
+ * section 5.2, the third mishap: the factors must be 32-bit, a 16-bit one
+ * overflowed to infinity):
+ *
+ *     C[i][j] = round_to_nearest_even_bf16( sum_k A64[i][k] * B64[k][j] )
+ *     A64[i][k] = A[i][k] * a_scale[i / block][k / block]
+ *     B64[k][j] = B[k][j] * b_scale[k / block][j / block]
+ *
+ * A (M x K) and B (K x N): row-major 8-bit E4M3 or E5M2 patterns (dtype
+ * HGEMM_E4M3 or HGEMM_E5M2, one format for both), device. C: row-major
+ * bfloat16 (M x N), device, written. block: 32 or 64. a_scale: device fp32
+ * array of ceil(M / block) x ceil(K / block) factors, row-major (factor of A's
+ * sub-block (i / block, k / block)); b_scale: device fp32 array of
+ * ceil(K / block) x ceil(N / block) factors, row-major. Both are read only,
+ * 4-byte aligned, owned by the caller; a partial last block of a dimension
+ * has one factor like the others.
+ *
+ * Each block's products are summed in fp32 by the tensor cores, multiplied
+ * by its factor a_scale * b_scale (formed in fp32) and added into an fp32
+ * accumulator; C is that accumulator rounded once. Tiles are 128 x 128 (one
+ * CTA) or 256 x 128 (a CTA pair). A or B whose row pitch is not a multiple
+ * of 16 bytes (K or N not a multiple of 16) is copied into the library's
+ * stream-ordered workspace first, as for hgemm(). Errors as for hgemm(); a
+ * dtype other than HGEMM_E4M3 / HGEMM_E5M2, a block other than 32 or 64, or
+ * a NULL or misaligned scale array (with M, N, K > 0) is
+ * HGEMM_ERR_INVALID_ARG. K == 0 writes zeros to C.
+ */
+hgemm_status_t hgemm_fp8_blockscaled(const void* A, const void* B, void* C, const float* a_scale,
+                                     const float* b_scale, int64_t M, int64_t N, int64_t K, int32_t block,
+                                     hgemm_dtype_t dtype, void* stream);
+
+/*
+ * hgemm_fp8_blockscaled with a forced configuration: cta_group (1 or 2),
+ * group_m and max_clusters are honoured; block_n must be 0 or 128, split_k
+ * and stream_k 0 or 1, store_mode 0 (HGEMM_ERR_INVALID_ARG otherwise).
+ */
+hgemm_status_t hgemm_fp8_blockscaled_ex(const void* A, const void* B, void* C, const float* a_scale,
+                                        const float* b_scale, int64_t M, int64_t N, int64_t K, int32_t block,
+                                        hgemm_dtype_t dtype, const hgemm_config_t* cfg, void* stream);
 
 /*
  * hgemm_host - the same product for operands in HOST memory.

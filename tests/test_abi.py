@@ -67,6 +67,24 @@ def test_invalid_arguments_rejected_without_device(lib, args):
     assert st == 1, binding.STATUS_NAMES.get(st)
 
 
+def test_fp8_blockscaled_arguments_rejected_without_device(lib):
+    f = lib.hgemm_fp8_blockscaled
+    A, B, C, sa, sb = 1 << 20, 2 << 20, 3 << 20, 4 << 20, 5 << 20
+    assert f(A, B, C, sa, sb, 64, 64, 64, 16, 3, None) == 1        # block 16
+    assert f(A, B, C, sa, sb, 64, 64, 64, 32, 1, None) == 1        # bf16 is not fp8
+    assert f(A, B, C, None, sb, 64, 64, 64, 32, 3, None) == 1      # no a_scale
+    assert f(A, B, C, sa, None, 64, 64, 64, 64, 4, None) == 1      # no b_scale
+    assert f(A, B, C, sa + 2, sb, 64, 64, 64, 32, 3, None) == 1    # misaligned a_scale
+    bad_cfg = binding.Config(block_n=256)._c()
+    assert lib.hgemm_fp8_blockscaled_ex(A, B, C, sa, sb, 64, 64, 64, 32, 3, ctypes.byref(bad_cfg), None) == 1
+    # empty shapes need no scales
+    assert f(None, None, C, None, None, 0, 64, 64, 32, 3, None) == 0
+    import torch
+    if not torch.cuda.is_available():
+        # a well-formed call without a GB300 fails loudly (no CPU fallback)
+        assert f(A, B, C, sa, sb, 64, 64, 64, 32, 3, None) == 2
+
+
 def test_overlap_rejected(lib):
     base = 1 << 20
     # C = [base, base + 2*4*4) overlaps A = [base + 16, ...)
