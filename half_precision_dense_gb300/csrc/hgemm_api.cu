@@ -806,6 +806,7 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
         q.sched.clusters = clusters;
         q.sched.sk_base = 0;
         q.sched.sk_extra = 0;
+        q.trace = g_trace.load(std::memory_order_relaxed);
         if ((e = hg::status_word_ptr(&q.status)) != cudaSuccess) {
             if (work && work != scratch) cudaFreeAsync(work, stream);
             return cuda_fail(e, "status word");

@@ -19,17 +19,24 @@
 //              TMEM buffers (accumulate flag off for the block's first MMA) and
 //              commits that buffer's `full` barrier; the tensor core therefore
 //              runs up to four scale blocks ahead of the epilogue.
-//   epilogue   warp w owns TMEM lane quarter w % 4 (32 rows of C, one per
-//              thread) and the 64 columns of half w / 4. For each scale block
-//              it loads its part of the partial (tcgen05.ld), hands the buffer
-//              back, forms the factors a_scale * b_scale in fp32 (one per
-//              32-column load: the row block is warp-uniform because a quarter's
-//              32 rows lie in one scale block) and adds factor x partial into
-//              64 fp32 registers with packed two-lane FMAs (fma.rn.f32x2).
-//              After the last block it rounds to bf16 and stores its row.
+//   epilogue   kBsEpiWarps warps; warp w owns TMEM lane quarter w % 4 (32 rows
+//              of C, one per thread) and the 128 / (kBsEpiWarps / 4) columns of
+//              column group w / 4. For each scale block it loads its part of
+//              the partial (tcgen05.ld), hands the buffer back, forms the factor
+//              a_scale * b_scale in fp32 (one per 32-column load: the row block
+//              is warp-uniform because a quarter's 32 rows lie in one scale
+//              block) and adds factor x partial into fp32 registers with packed
+//              two-lane FMAs (fma.rn.f32x2). After the last block it rounds to
+//              bf16 and stores its row.
 //   producers  as in the main kernel: TMA loads of 128 x 128-byte A boxes and
 //              128-row B atoms (read MN-major in the 128-byte swizzle), two
 //              warps on alternate stages of a 7-stage ring.
+//
+// The epilogue's fp32 work per scale block equals the tensor core's (128 x 128
+// FMAs per CTA at 128 per clock against 128 cycles of MMA for 64-deep blocks),
+// so its speed rests on hiding the ~200-cycle tcgen05.ld latency: 16 warps
+// (4 per SM sub-partition, 32 columns each) run their per-block chains out of
+// step, where 8 warps of 64 columns left most of each chain exposed.
 //
 // Tiles are 128 x 128 per CTA, or 256 x 128 for a CTA pair (cta_group::2,
 // each CTA feeding 64 B columns). Every wait is bounded as in the main kernel.
@@ -38,6 +45,19 @@
 #include "hgemm_tc.cuh"
 
 namespace hg {
+
+// Warp roles of the block-scaled kernel: epilogue warps first, then the two
+// producers and the MMA warp.
+#ifndef HG_FP8BS_EPI_WARPS
+#define HG_FP8BS_EPI_WARPS 16
+#endif
+constexpr int kBsEpiWarps = HG_FP8BS_EPI_WARPS;
+constexpr int kBsCols = 128 / (kBsEpiWarps / 4);   // columns per epilogue warp
+constexpr int kBsProducer = kBsEpiWarps;
+constexpr int kBsMma = kBsEpiWarps + 1;
+constexpr int kBsProducer2 = kBsEpiWarps + 2;
+constexpr int kBsThreads = 32 * (kBsEpiWarps + 3);
+static_assert(kBsEpiWarps == 8 || kBsEpiWarps == 16, "epilogue warps");
 
 struct Fp8bsParams {
     int32_t M, N, K;
@@ -55,7 +75,21 @@ struct Fp8bsParams {
     uint64_t timeout_ns;
     unsigned long long* status;
     Schedule sched;                 // whole tiles only
+    unsigned long long* trace;      // per-block clock64 records (builds with HG_TRACE only), or null
 };
+
+// Traced builds: clock64 stamps of the first 64 scale blocks of CTAs 0 and 1
+// (record (cta, block), field f).
+enum : int { kBsMmaWaited = 0, kBsMmaCommitted = 1, kBsEpiWaited = 2, kBsEpiLoaded = 3, kBsEpiDone = 4,
+             kBsEpiLastWaited = 5, kBsProdIssued = 6, kBsMmaFull = 7 };
+__device__ __forceinline__ void bs_trace(const Fp8bsParams& p, int blk, int field) {
+#ifdef HG_TRACE
+    if (p.trace && blockIdx.x < 2 && blk < 64)
+        p.trace[(static_cast<int64_t>(blockIdx.x) * 64 + blk) * 8 + field] = static_cast<unsigned long long>(clock64());
+#else
+    (void)p; (void)blk; (void)field;
+#endif
+}
 
 template <int CG>
 struct Fp8bsCfg {
@@ -86,7 +120,7 @@ __device__ __forceinline__ void fma2_bcast(float& d0, float& d1, float s, float 
 }
 
 template <int CG, int kGs, int kDt>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kBsThreads, 1)
 hgemm_fp8bs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmB2, const Fp8bsParams p) {
 #if defined(__CUDA_ARCH__) && defined(__CUDA_ARCH_FEAT_SM103_ALL)
@@ -128,18 +162,18 @@ hgemm_fp8bs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         }
         for (int b = 0; b < R; ++b) {
             mbar_init(bar_pfull + 8 * b, 1);
-            mbar_init(bar_pempty + 8 * b, kEpiWarps * CG);
+            mbar_init(bar_pempty + 8 * b, kBsEpiWarps * CG);
         }
         mbar_init(bar_drain, 1);
         *abort_flag = 0;
         fence_mbarrier_init_cluster();
     }
-    if (warp == kProducerWarp && lane == 0) {
+    if (warp == kBsProducer && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
         if (Base::kBPartial) tma_prefetch_desc(&tmB2);
     }
-    if (warp == kMmaWarp) tmem_alloc<CG>(smem_addr(tmem_slot), Cfg::kTmemCols);
+    if (warp == kBsMma) tmem_alloc<CG>(smem_addr(tmem_slot), Cfg::kTmemCols);
     tc_fence_before();
     __syncthreads();
     if constexpr (CG > 1) cluster_sync();
@@ -147,9 +181,9 @@ hgemm_fp8bs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
     const Waiter w{abort_flag, p.timeout_ns, p.status};
 
-    if (warp == kProducerWarp || warp == kProducerWarp2) {
+    if (warp == kBsProducer || warp == kBsProducer2) {
         // ------------------------------------------------------------ producer
-        const uint32_t pid = warp == kProducerWarp ? 0u : 1u;
+        const uint32_t pid = warp == kBsProducer ? 0u : 1u;
         uint32_t stage = pid, phase = 0, g = 0;
         bool ok = true;
         WorkUnit wu;
@@ -194,10 +228,11 @@ hgemm_fp8bs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             const uint64_t t0 = globaltimer_ns();
             while (globaltimer_ns() - t0 < 50000ull) {}
         }
-    } else if (warp == kMmaWarp) {
+    } else if (warp == kBsMma) {
         // ----------------------------------------------------------------- MMA
         if (rank == 0) {
             uint32_t stage = 0, phase = 0, pb = 0, pph = 0;
+            int nblk = 0;
             bool ok = true, issued = false;
             const uint64_t a_desc0 = sdesc_sw128(sA, 16u, 1024u);
             const uint64_t b_desc0 = sdesc_sw128(sB, Base::kBAtomBytes, 1024u);
@@ -208,6 +243,7 @@ hgemm_fp8bs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                         ok = false;
                         break;
                     }
+                    if (lane == 0) bs_trace(p, nblk, kBsMmaFull);
                     tc_fence_after();
                     const uint64_t ad = a_desc0 + ((stage * Base::kABytes) >> 4);
                     const uint64_t bd = b_desc0 + ((stage * Base::kBBytes) >> 4);
@@ -218,6 +254,7 @@ hgemm_fp8bs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                             ok = false;
                             break;
                         }
+                        if (lane == 0) bs_trace(p, nblk, kBsMmaWaited);
                         tc_fence_after();
                         const uint32_t d_tmem = tmem_base + pb * BN;
                         if (elect_one_sync()) {
@@ -230,6 +267,8 @@ hgemm_fp8bs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                             else umma_commit_pair(bar_pfull + 8 * pb, static_cast<uint16_t>(0x3u));
                         }
                         __syncwarp();
+                        if (lane == 0) bs_trace(p, nblk, kBsMmaCommitted);
+                        ++nblk;
                         issued = true;
                         if (++pb == static_cast<uint32_t>(R)) {
                             pb = 0;
@@ -261,51 +300,64 @@ hgemm_fp8bs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         }
     } else {
         // ------------------------------------------------------------ epilogue
+        constexpr int kLoads = kBsCols / 32;    // 32-column TMEM loads per block
         const int quarter = warp & 3;
-        const int colhalf = warp >> 2;
+        const int colgrp = warp >> 2;
         uint32_t pb = 0, pph = 0;
+        int nblk = 0;
         bool ok = true;
         WorkUnit wu;
         for (int it = 0; ok && next_unit(p.sched, cluster_id, it, wu); ++it) {
             int32_t tm, tn;
             tile_coord(wu.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
             const int32_t row_base = tm * kBlockMCta * CG + static_cast<int32_t>(rank) * kBlockMCta + quarter * 32;
-            const int32_t col_base = tn * BN + 64 * colhalf;
+            const int32_t col_base = tn * BN + kBsCols * colgrp;
             // Scale rows and columns of this warp (warp-uniform; clamped for
             // rows and columns past the matrix, whose partial sums are zero).
             int32_t rb = row_base / kGs;
             if (rb > p.sa_rows - 1) rb = p.sa_rows - 1;
-            int32_t cb0 = col_base / kGs, cb1 = (col_base + 32) / kGs;
-            if (cb0 > p.sb_cols - 1) cb0 = p.sb_cols - 1;
-            if (cb1 > p.sb_cols - 1) cb1 = p.sb_cols - 1;
-            const float* sa_row = p.a_scale + static_cast<int64_t>(rb) * p.num_sb;
-            const float* sb_c0 = p.b_scale + cb0;
-            const float* sb_c1 = p.b_scale + cb1;
-            float acc[64];
+            int32_t cb[kLoads];
 #pragma unroll
-            for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
-            float nsa = __ldg(sa_row), nsb0 = __ldg(sb_c0), nsb1 = __ldg(sb_c1);
+            for (int l = 0; l < kLoads; ++l) {
+                cb[l] = (col_base + 32 * l) / kGs;
+                if (cb[l] > p.sb_cols - 1) cb[l] = p.sb_cols - 1;
+            }
+            const float* sa_row = p.a_scale + static_cast<int64_t>(rb) * p.num_sb;
+            float acc[kBsCols];
+#pragma unroll
+            for (int i = 0; i < kBsCols; ++i) acc[i] = 0.0f;
+            float nsa = __ldg(sa_row), nsb[kLoads];
+#pragma unroll
+            for (int l = 0; l < kLoads; ++l) nsb[l] = __ldg(p.b_scale + cb[l]);
             const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
             for (int sbk = 0; sbk < p.num_sb; ++sbk) {
-                const float csa = nsa, csb0 = nsb0, csb1 = nsb1;
+                const float csa = nsa;
+                float csb[kLoads];
+#pragma unroll
+                for (int l = 0; l < kLoads; ++l) csb[l] = nsb[l];
                 if (sbk + 1 < p.num_sb) {
                     // next block's factors, loaded while this block's partial is awaited
                     nsa = __ldg(sa_row + sbk + 1);
-                    nsb0 = __ldg(sb_c0 + static_cast<int64_t>(sbk + 1) * p.sb_cols);
-                    nsb1 = __ldg(sb_c1 + static_cast<int64_t>(sbk + 1) * p.sb_cols);
+#pragma unroll
+                    for (int l = 0; l < kLoads; ++l)
+                        nsb[l] = __ldg(p.b_scale + static_cast<int64_t>(sbk + 1) * p.sb_cols + cb[l]);
                 }
                 if (!wait_bar_warp(bar_pfull + 8 * pb, pph, w, kRoleEpilogue, 32 + pb)) {
                     ok = false;
                     break;
                 }
+                if (lane == 0 && warp == 0) bs_trace(p, nblk, kBsEpiWaited);
+                if (lane == 0 && warp == kBsEpiWarps - 1) bs_trace(p, nblk, kBsEpiLastWaited);
                 tc_fence_after();
-                uint32_t r0[32], r1[32];
-                const uint32_t t_col = tmem_base + pb * BN + 64u * static_cast<uint32_t>(colhalf) + t_lane;
-                tmem_ld_32x32b_x32(t_col, r0);
-                tmem_ld_32x32b_x32(t_col + 32u, r1);
+                uint32_t r[kBsCols];
+                const uint32_t t_col = tmem_base + pb * BN + static_cast<uint32_t>(kBsCols * colgrp) + t_lane;
+#pragma unroll
+                for (int l = 0; l < kLoads; ++l)
+                    tmem_ld_32x32b_x32(t_col + 32u * l, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * l));
                 tmem_ld_wait();
-                reg_fence(r0);
-                reg_fence(r1);
+#pragma unroll
+                for (int l = 0; l < kLoads; ++l) reg_fence(*reinterpret_cast<uint32_t(*)[32]>(r + 32 * l));
+                if (lane == 0 && warp == 0) bs_trace(p, nblk, kBsEpiLoaded);
                 // the buffer's reads are done: hand it back to the MMA warp
                 tc_fence_before();
                 __syncwarp();
@@ -314,26 +366,32 @@ hgemm_fp8bs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                     pb = 0;
                     pph ^= 1u;
                 }
-                const float s0 = csa * csb0;
-                const float s1 = csa * csb1;
 #pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    fma2_bcast(acc[i], acc[i + 1], s0, __uint_as_float(r0[i]), __uint_as_float(r0[i + 1]));
-                    fma2_bcast(acc[32 + i], acc[33 + i], s1, __uint_as_float(r1[i]), __uint_as_float(r1[i + 1]));
+                for (int l = 0; l < kLoads; ++l) {
+                    const float sf = csa * csb[l];
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2)
+                        fma2_bcast(acc[32 * l + i], acc[32 * l + i + 1], sf, __uint_as_float(r[32 * l + i]),
+                                   __uint_as_float(r[32 * l + i + 1]));
                 }
+                if (lane == 0 && warp == 0) {
+                    asm volatile("" :: "f"(acc[0]), "f"(acc[kBsCols - 1]));
+                    bs_trace(p, nblk, kBsEpiDone);
+                }
+                ++nblk;
             }
             if (!ok) break;
-            // Round to bf16 and store this thread's row: 64 columns from col_base.
+            // Round to bf16 and store this thread's row: kBsCols columns from col_base.
             const int32_t row = row_base + static_cast<int32_t>(lane);
             if (row < p.M) {
-                uint32_t pk[32];
+                uint32_t pk[kBsCols / 2];
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
+                for (int i = 0; i < kBsCols / 2; ++i)
                     pk[i] = pack_rn<kDt>(__float_as_uint(acc[2 * i]), __float_as_uint(acc[2 * i + 1]));
                 uint16_t* crow = p.C + static_cast<int64_t>(row) * p.ldc;
                 if (p.c_vec) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
+                    for (int j = 0; j < kBsCols / 8; ++j) {
                         const int32_t col = col_base + 8 * j;
                         if (col < p.N)
                             *reinterpret_cast<uint4*>(crow + col) =
@@ -341,7 +399,7 @@ hgemm_fp8bs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                     }
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) {
+                    for (int i = 0; i < kBsCols; ++i) {
                         const int32_t col = col_base + i;
                         if (col < p.N)
                             crow[col] = static_cast<uint16_t>((i & 1) ? (pk[i >> 1] >> 16) : (pk[i >> 1] & 0xFFFFu));
@@ -354,7 +412,7 @@ hgemm_fp8bs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     // ------------------------------------------------------------ teardown
     __syncthreads();
     if constexpr (CG > 1) cluster_sync();
-    if (warp == kMmaWarp) {
+    if (warp == kBsMma) {
         tc_fence_after();
         tmem_dealloc<CG>(tmem_base, Cfg::kTmemCols);
     }

@@ -113,13 +113,15 @@ constexpr int kTraceUnits = 32;
 constexpr int kTraceFields = 8;
 enum : int { kTrProdFirst = 0, kTrMmaFirst = 1, kTrMmaLast = 2, kTrEpiStart = 3, kTrEpiTmemFree = 4,
              kTrEpiEnd = 5, kTrUnit = 6, kTrSetup = 7 };
-// Epilogue detail of a CTA's first unit (warp 0): slot 16 + c, field f.
-enum : int { kTcLdDone = 0, kTcWaitRead = 1, kTcStaged = 2, kTcIssued = 3 };
+// Epilogue detail of a CTA's first unit (warp 0): slot 16 + c, field f, in
+// SM clock cycles (clock64; %globaltimer is too coarse for a chunk's steps).
+enum : int { kTcLdDone = 0, kTcWaitRead = 1, kTcStaged = 2, kTcIssued = 3, kTcStart = 4, kTcPacked = 5,
+             kTcStored = 6 };
 __device__ __forceinline__ void trace_chunk(const TcParams& p, int it, int c, int field) {
 #ifdef HG_TRACE
-    if (p.trace && it == 0 && c < 16)
+    if (p.trace && it == 0 && c < 13)
         p.trace[(static_cast<int64_t>(blockIdx.x) * kTraceUnits + 16 + c) * kTraceFields + field] =
-            globaltimer_ns();
+            static_cast<unsigned long long>(clock64());
 #else
     (void)p; (void)it; (void)c; (void)field;
 #endif
@@ -778,6 +780,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             tc_fence_after();
             if (warp == 0 && lane == 0) {
                 trace_stamp(p, it, kTrEpiStart);
+                trace_chunk(p, it, 12, kTcStart);
 #ifdef HG_TRACE
                 if (p.trace && it < kTraceUnits)
                     p.trace[(static_cast<int64_t>(blockIdx.x) * kTraceUnits + it) * kTraceFields + kTrUnit] =
@@ -945,6 +948,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 // last chunk of a tile whose width is an odd multiple of 32.
                 const bool half = Cfg::kHalfLast && c == Cfg::kChunks - 1;
                 const bool last = c + 2 >= Cfg::kChunks;
+                if (warp == 0 && lane == 0) trace_chunk(p, it, c, kTcStart);
                 if (bulk_adds && lane == 0) {
                     // chunk c of a partial block: float4s [16c * 32, 16(c + 1) * 32)
                     const uint32_t bytes = half ? 4096u : 8192u;
@@ -1152,6 +1156,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     pk[i] = pack_rn<kDt>(r0[2 * i], r0[2 * i + 1]);
                     pk[16 + i] = pack_rn<kDt>(r1[2 * i], r1[2 * i + 1]);
                 }
+                if (warp == 0 && lane == 0) trace_chunk(p, it, c, kTcPacked);
                 const int32_t ccol = col0 + 64 * c;
                 if (p.store_mode == 3) {
                     // Direct 16-byte stores: thread `lane` writes its own row of the
@@ -1231,6 +1236,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         }
                     }
                     __syncwarp();
+                    if (warp == 0 && lane == 0) trace_chunk(p, it, c, kTcStored);
                 } else {
                     __syncwarp();
                     const uint32_t width = half ? 32u : 64u;
@@ -1258,6 +1264,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             }
             if (warp == 0 && lane == 0) {
                 trace_stamp(p, it, kTrEpiEnd);
+                trace_chunk(p, it, 12, kTcStored);
                 if (is_split && owner) trace_slot(p, 30, 1);
             }
             preload_if_owner(it + 2);

@@ -6,7 +6,7 @@
 namespace hg {
 
 template <int CG, int kGs, int kDt>
-using Fp8bsInstance = ClusterKernel<&hgemm_fp8bs_kernel<CG, kGs, kDt>, CG, Fp8bsCfg<CG>::kSmemBytes>;
+using Fp8bsInstance = ClusterKernel<&hgemm_fp8bs_kernel<CG, kGs, kDt>, CG, Fp8bsCfg<CG>::kSmemBytes, kBsThreads>;
 
 #define HG_FP8BS_DISPATCH(CALL)                                                               \
     if (kind == 3 && cta_group == 1 && gs == 32) return Fp8bsInstance<1, 32, 3>::CALL;        \

@@ -13,7 +13,7 @@ namespace hg {
 // shared-memory opt-in (per device, set once), the launch configuration
 // (one cluster of kCluster CTAs per work slot) and the resident clusters
 // (queried once per device).
-template <auto kKernel, int kCluster, int kSmemBytes>
+template <auto kKernel, int kCluster, int kSmemBytes, int kBlockThreads = kThreads>
 struct ClusterKernel {
     static cudaError_t prepare() {
         static std::mutex mu;
@@ -33,7 +33,7 @@ struct ClusterKernel {
                             cudaStream_t stream) {
         cfg = cudaLaunchConfig_t{};
         cfg.gridDim = dim3(static_cast<unsigned>(clusters * kCluster), 1, 1);
-        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.blockDim = dim3(kBlockThreads, 1, 1);
         cfg.dynamicSmemBytes = kSmemBytes;
         cfg.stream = stream;
         attr[0].id = cudaLaunchAttributeClusterDimension;
