@@ -510,13 +510,20 @@ def run_ours(args, rank, world, local_rank):
     line["roofline"]["plan"] = {"cta_group": plan_key[0], "block_n": plan_key[1],
                                 "stream_k_tiles": plan_key[2], "grid_ctas": plan_key[3],
                                 "split_k": plan["split_k"], "store_mode": plan["store_mode"]}
+    if bs:
+        # the block-scaled kernel plans its own tiles: 128 columns, a CTA pair
+        # per 256-row tile unless there is a single 128-row tile row
+        cg = 2 if o["M"] > 128 else 1
+        line["roofline"]["kernel"] = "hg::hgemm_fp8bs_kernel"
+        line["roofline"]["plan"] = {"cta_group": cg, "block_n": 128, "scale_block": bs}
+        plan_key = None
     if args.traffic_file and os.path.exists(args.traffic_file):
         # DRAM bytes from an ncu capture count only while the kernel and plan
         # they were taken on are the ones running now.
         try:
             with open(args.traffic_file) as f:
                 tr = json.load(f)
-            if (tr.get("plan") == plan_key and tr.get("kernel_rev") == KERNEL_REV and
+            if (plan_key is not None and tr.get("plan") == plan_key and tr.get("kernel_rev") == KERNEL_REV and
                     tr.get("dtype", "bf16") in {o["dt"] for o in ops}):
                 line["roofline"]["traffic"] = tr.get("dram_bytes_per_launch")
                 line["roofline"]["traffic_source"] = tr.get("source")

@@ -9,33 +9,58 @@ namespace hg {
 
 __device__ unsigned long long g_status_word;
 
+// Bytes [o, o + 16) of the 32 bytes a|b (o < 16), as one 16-byte vector:
+// word i of the result is the funnel shift of words o/4 + i and o/4 + i + 1
+// right by 8 (o % 4) bits.
+__device__ __forceinline__ uint4 bytes_from(const uint4& a, const uint4& b, uint32_t o) {
+    const uint32_t sh = (o & 3u) * 8u;
+    switch (o >> 2) {
+        case 0:
+            return make_uint4(__funnelshift_r(a.x, a.y, sh), __funnelshift_r(a.y, a.z, sh),
+                              __funnelshift_r(a.z, a.w, sh), __funnelshift_r(a.w, b.x, sh));
+        case 1:
+            return make_uint4(__funnelshift_r(a.y, a.z, sh), __funnelshift_r(a.z, a.w, sh),
+                              __funnelshift_r(a.w, b.x, sh), __funnelshift_r(b.x, b.y, sh));
+        case 2:
+            return make_uint4(__funnelshift_r(a.z, a.w, sh), __funnelshift_r(a.w, b.x, sh),
+                              __funnelshift_r(b.x, b.y, sh), __funnelshift_r(b.y, b.z, sh));
+        default:
+            return make_uint4(__funnelshift_r(a.w, b.x, sh), __funnelshift_r(b.x, b.y, sh),
+                              __funnelshift_r(b.y, b.z, sh), __funnelshift_r(b.z, b.w, sh));
+    }
+}
+
 // Copy a rows x cols matrix of E-byte values (E = 1, 2 or 4) with row pitch
 // `cols` (any base alignment of E bytes) into `dst` with row pitch `dst_ld`
-// (16-byte aligned base, dst_ld * E a multiple of 16). Each thread moves 16
-// bytes of one row: E-byte loads (the source rows are not 16-byte aligned),
-// one 16-byte store. Elements past `cols` in the destination row are not
-// written.
+// (16-byte aligned base, dst_ld * E a multiple of 16). Each thread writes 16
+// bytes of one row. Its source bytes start at some offset o inside an
+// aligned 16-byte block: it loads that block and the next with 16-byte loads
+// (neighbouring threads share them in L1) and shifts them into place, so the
+// copy reads the source with aligned vector loads whatever its pitch. A chunk
+// that would read past the end of the source, or the row's ragged last chunk,
+// is copied element by element. Elements past `cols` in the destination row
+// are not written.
 template <typename T>
 __global__ void repack_rows_kernel(const T* __restrict__ src, int64_t rows, int64_t cols,
                                    T* __restrict__ dst, int64_t dst_ld) {
     constexpr int kPer = 16 / sizeof(T);
     const int64_t chunks = (cols + kPer - 1) / kPer;
+    const uintptr_t src_end = reinterpret_cast<uintptr_t>(src + rows * cols);
     for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
         const T* s = src + r * cols;
         T* d = dst + r * dst_ld;
         for (int64_t ch = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; ch < chunks;
              ch += static_cast<int64_t>(gridDim.x) * blockDim.x) {
             const int64_t c0 = ch * kPer;
-            if (c0 + kPer <= cols) {
-                union {
-                    T v[kPer];
-                    uint4 u;
-                } packed;
-#pragma unroll
-                for (int i = 0; i < kPer; ++i) packed.v[i] = s[c0 + i];
-                *reinterpret_cast<uint4*>(d + c0) = packed.u;
+            const uintptr_t a = reinterpret_cast<uintptr_t>(s + c0);
+            const uintptr_t ab = a & ~static_cast<uintptr_t>(15);
+            const uint32_t o = static_cast<uint32_t>(a - ab);
+            if (c0 + kPer <= cols && ab + (o ? 32u : 16u) <= src_end) {
+                const uint4 lo = *reinterpret_cast<const uint4*>(ab);
+                const uint4 v = o ? bytes_from(lo, *reinterpret_cast<const uint4*>(ab + 16), o) : lo;
+                *reinterpret_cast<uint4*>(d + c0) = v;
             } else {
-                for (int64_t c = c0; c < cols; ++c) d[c] = s[c];
+                for (int64_t c = c0; c < cols && c < c0 + kPer; ++c) d[c] = s[c];
             }
         }
     }

@@ -16,27 +16,35 @@
 //
 //   MMA warp   for each scale block (bs / 32 kind::f8f6f4 MMAs of K = 32) it
 //              writes the block's fp32 partial sum into one of four 128-column
-//              TMEM buffers (accumulate flag off for the block's first MMA) and
-//              commits that buffer's `full` barrier; the tensor core therefore
-//              runs up to four scale blocks ahead of the epilogue.
+//              TMEM buffers (accumulate flag off for the block's first MMA).
+//              The buffers go back and forth in pairs: one wait and one commit
+//              per two blocks, because every hand-off between two warps costs
+//              about 300 cycles however little they do (a bare skeleton of
+//              this ring, measured), against 128 cycles of tensor work in a
+//              64-deep block. The tensor core runs up to two pairs ahead.
 //   epilogue   kBsEpiWarps warps; warp w owns TMEM lane quarter w % 4 (32 rows
 //              of C, one per thread) and the 128 / (kBsEpiWarps / 4) columns of
 //              column group w / 4. For each scale block it loads its part of
-//              the partial (tcgen05.ld), hands the buffer back, forms the factor
-//              a_scale * b_scale in fp32 (one per 32-column load: the row block
-//              is warp-uniform because a quarter's 32 rows lie in one scale
-//              block) and adds factor x partial into fp32 registers with packed
-//              two-lane FMAs (fma.rn.f32x2). After the last block it rounds to
-//              bf16 and stores its row.
+//              the partial (tcgen05.ld), forms the factor a_scale * b_scale in
+//              fp32 (one per 32-column load: the row block is warp-uniform
+//              because a quarter's 32 rows lie in one scale block) and adds
+//              factor x partial into fp32 registers (fmaf); a pair's buffers
+//              go back once both are read. The factors come from a per-warp
+//              ring in shared memory that cp.async fills several blocks ahead.
+//              After the last block it rounds to bf16 and stores its row.
 //   producers  as in the main kernel: TMA loads of 128 x 128-byte A boxes and
 //              128-row B atoms (read MN-major in the 128-byte swizzle), two
 //              warps on alternate stages of a 7-stage ring.
 //
 // The epilogue's fp32 work per scale block equals the tensor core's (128 x 128
 // FMAs per CTA at 128 per clock against 128 cycles of MMA for 64-deep blocks),
-// so its speed rests on hiding the ~200-cycle tcgen05.ld latency: 16 warps
-// (4 per SM sub-partition, 32 columns each) run their per-block chains out of
-// step, where 8 warps of 64 columns left most of each chain exposed.
+// and each warp's block is a serial chain: a TMEM load (~200-240 cycles
+// before its data can be used), then the FMAs. The next block's load cannot
+// be issued before the current block's FMAs without a second 64-register
+// buffer, which the register file does not hold beside the accumulators; so
+// the chain sets the pace (measured about 600 cycles per 64-deep block, 0.24
+// of the tensor rate). 8 warps of 64 columns measured 5-9 % faster than 16
+// warps of 32 (kBsEpiWarps = 16 builds with HG_FP8BS_EPI_WARPS=16).
 //
 // Tiles are 128 x 128 per CTA, or 256 x 128 for a CTA pair (cta_group::2,
 // each CTA feeding 64 B columns). Every wait is bounded as in the main kernel.
@@ -49,7 +57,7 @@ namespace hg {
 // Warp roles of the block-scaled kernel: epilogue warps first, then the two
 // producers and the MMA warp.
 #ifndef HG_FP8BS_EPI_WARPS
-#define HG_FP8BS_EPI_WARPS 16
+#define HG_FP8BS_EPI_WARPS 8
 #endif
 constexpr int kBsEpiWarps = HG_FP8BS_EPI_WARPS;
 constexpr int kBsCols = 128 / (kBsEpiWarps / 4);   // columns per epilogue warp
@@ -57,6 +65,8 @@ constexpr int kBsProducer = kBsEpiWarps;
 constexpr int kBsMma = kBsEpiWarps + 1;
 constexpr int kBsProducer2 = kBsEpiWarps + 2;
 constexpr int kBsThreads = 32 * (kBsEpiWarps + 3);
+constexpr int kBsScaleAhead = kBsEpiWarps == 16 ? 4 : 8;   // scale blocks fetched ahead per warp (even)
+constexpr int kBsRingBytes = kBsEpiWarps * kBsScaleAhead * 16;  // 16-byte slots: a_scale, b_scale(s)
 static_assert(kBsEpiWarps == 8 || kBsEpiWarps == 16, "epilogue warps");
 
 struct Fp8bsParams {
@@ -98,26 +108,13 @@ struct Fp8bsCfg {
     static constexpr int kParts = 4;            // TMEM partial-sum buffers of BN columns
     static constexpr int kTmemCols = kParts * BN;
     static constexpr int kBarBytes = 256;
-    static constexpr int kStagesFit = (kSmemLimit - 1024 - kBarBytes) / Base::kStageBytes;
+    static constexpr int kStagesFit = (kSmemLimit - 1024 - kBarBytes - kBsRingBytes) / Base::kStageBytes;
     static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
-    static constexpr int kSmemBytes = 1024 + kStages * Base::kStageBytes + kBarBytes;
+    static constexpr int kSmemBytes = 1024 + kStages * Base::kStageBytes + kBarBytes + kBsRingBytes;
     static_assert(kTmemCols <= 512, "tensor memory");
     static_assert((2 * kStages + 2 * kParts + 1) * 8 + 8 <= kBarBytes, "barrier area");
     static_assert(kSmemBytes <= kSmemLimit, "shared memory");
 };
-
-// d = s * a + d on two fp32 lanes at once (d0, d1 += s * (a0, a1)), each lane
-// one fused multiply-add rounded to nearest even.
-__device__ __forceinline__ void fma2_bcast(float& d0, float& d1, float s, float a0, float a1) {
-    asm("{\n\t.reg .b64 d, a, s;\n\t"
-        "mov.b64 d, {%0, %1};\n\t"
-        "mov.b64 a, {%3, %4};\n\t"
-        "mov.b64 s, {%2, %2};\n\t"
-        "fma.rn.f32x2 d, s, a, d;\n\t"
-        "mov.b64 {%0, %1}, d;\n\t}"
-        : "+f"(d0), "+f"(d1)
-        : "f"(s), "f"(a0), "f"(a1));
-}
 
 template <int CG, int kGs, int kDt>
 __global__ void __launch_bounds__(kBsThreads, 1)
@@ -131,6 +128,7 @@ hgemm_fp8bs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     constexpr int BN = Cfg::BN;
     constexpr int kSbPerStage = Base::kBK / kGs;   // scale blocks in a 128-deep stage
     constexpr int kMmaPerSb = kGs / Base::kUK;     // K = 32 MMAs per scale block
+    constexpr int kGroups = R / 2;                  // hand-offs in flight: pairs of buffers
     static_assert(kGs == 32 || kGs == 64, "scale block");
     static_assert(kDt == 3 || kDt == 4, "fp8 operands");
     static_assert(Base::kBAtoms == 1, "one B atom per stage");
@@ -148,6 +146,7 @@ hgemm_fp8bs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     const uint32_t bar_pempty = bar_pfull + 8 * R;   // [R] partial buffer read
     const uint32_t bar_drain = bar_pempty + 8 * R;
     uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(smem + (bar_drain + 8 - base));
+    const uint32_t sRing = sBar + Cfg::kBarBytes;    // epilogue warps' scale rings
     volatile uint32_t* const abort_flag = tmem_slot + 1;
 
     const int warp = static_cast<int>(threadIdx.x >> 5);
@@ -160,7 +159,7 @@ hgemm_fp8bs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
         }
-        for (int b = 0; b < R; ++b) {
+        for (int b = 0; b < kGroups; ++b) {
             mbar_init(bar_pfull + 8 * b, 1);
             mbar_init(bar_pempty + 8 * b, kBsEpiWarps * CG);
         }
@@ -249,19 +248,26 @@ hgemm_fp8bs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                     const uint64_t bd = b_desc0 + ((stage * Base::kBBytes) >> 4);
                     const int rem = p.num_sb - kb * kSbPerStage;
                     const int nsb = rem < kSbPerStage ? rem : kSbPerStage;
-                    for (int j = 0; j < nsb; ++j) {
+                    // Groups of two scale blocks (a stage holds 2 or 4; the
+                    // last group of a K loop with an odd block count has one):
+                    // one wait for the group's two buffers, one commit.
+                    for (int j0 = 0; j0 < nsb; j0 += 2) {
                         if (!wait_bar_warp(bar_pempty + 8 * pb, pph ^ 1u, w, kRoleMma, 32 + pb)) {
                             ok = false;
                             break;
                         }
                         if (lane == 0) bs_trace(p, nblk, kBsMmaWaited);
                         tc_fence_after();
-                        const uint32_t d_tmem = tmem_base + pb * BN;
+                        const int nj = nsb - j0 < 2 ? nsb - j0 : 2;
                         if (elect_one_sync()) {
+                            for (int jj = 0; jj < nj; ++jj) {
+                                const uint32_t d_tmem = tmem_base + (2u * pb + static_cast<uint32_t>(jj)) * BN;
 #pragma unroll
-                            for (int mm = 0; mm < kMmaPerSb; ++mm) {
-                                const uint32_t kk = static_cast<uint32_t>(j * kMmaPerSb + mm);
-                                umma_f8<CG>(d_tmem, ad + 2u * kk, bd + 8u * Base::kUK * kk, p.idesc, mm > 0 ? 1u : 0u);
+                                for (int mm = 0; mm < kMmaPerSb; ++mm) {
+                                    const uint32_t kk = static_cast<uint32_t>((j0 + jj) * kMmaPerSb + mm);
+                                    umma_f8<CG>(d_tmem, ad + 2u * kk, bd + 8u * Base::kUK * kk, p.idesc,
+                                                mm > 0 ? 1u : 0u);
+                                }
                             }
                             if constexpr (CG == 1) umma_commit(bar_pfull + 8 * pb);
                             else umma_commit_pair(bar_pfull + 8 * pb, static_cast<uint16_t>(0x3u));
@@ -270,7 +276,7 @@ hgemm_fp8bs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                         if (lane == 0) bs_trace(p, nblk, kBsMmaCommitted);
                         ++nblk;
                         issued = true;
-                        if (++pb == static_cast<uint32_t>(R)) {
+                        if (++pb == static_cast<uint32_t>(kGroups)) {
                             pb = 0;
                             pph ^= 1u;
                         }
@@ -326,22 +332,63 @@ hgemm_fp8bs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             float acc[kBsCols];
 #pragma unroll
             for (int i = 0; i < kBsCols; ++i) acc[i] = 0.0f;
-            float nsa = __ldg(sa_row), nsb[kLoads];
-#pragma unroll
-            for (int l = 0; l < kLoads; ++l) nsb[l] = __ldg(p.b_scale + cb[l]);
-            const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
-            for (int sbk = 0; sbk < p.num_sb; ++sbk) {
-                const float csa = nsa;
-                float csb[kLoads];
-#pragma unroll
-                for (int l = 0; l < kLoads; ++l) csb[l] = nsb[l];
-                if (sbk + 1 < p.num_sb) {
-                    // next block's factors, loaded while this block's partial is awaited
-                    nsa = __ldg(sa_row + sbk + 1);
-#pragma unroll
-                    for (int l = 0; l < kLoads; ++l)
-                        nsb[l] = __ldg(p.b_scale + static_cast<int64_t>(sbk + 1) * p.sb_cols + cb[l]);
+            // Block blk's factors go to slot blk % kBsScaleAhead of this warp's
+            // ring: lane 0 copies a_scale, lanes 1..kLoads the b_scale of each
+            // 32-column load. One commit group per block, in every lane.
+            const uint32_t ring = sRing + static_cast<uint32_t>(warp * kBsScaleAhead * 16);
+            const int32_t my_cb = kLoads == 1 ? cb[0] : (lane == 1 ? cb[0] : cb[kLoads - 1]);
+            auto fetch = [&](int blk) {
+                if (blk < p.num_sb) {
+                    const uint32_t slot = ring + static_cast<uint32_t>((blk % kBsScaleAhead) * 16);
+                    if (lane == 0) cp_async_4(slot, sa_row + blk);
+                    else if (lane <= static_cast<uint32_t>(kLoads))
+                        cp_async_4(slot + 4u * lane, p.b_scale + static_cast<int64_t>(blk) * p.sb_cols + my_cb);
                 }
+                cp_async_commit();
+            };
+#pragma unroll
+            for (int j = 0; j < kBsScaleAhead; ++j) fetch(j);
+            const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
+            const uint32_t t_cols = static_cast<uint32_t>(kBsCols * colgrp) + t_lane;
+            // acc += factor * partial for one block held in r (kLoads 32-column loads)
+            auto accumulate = [&](const uint32_t (&r)[kBsCols], float sa_f, const float (&sb_f)[kLoads]) {
+#pragma unroll
+                for (int l = 0; l < kLoads; ++l) {
+                    const float sf = sa_f * sb_f[l];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) acc[32 * l + i] = fmaf(sf, __uint_as_float(r[32 * l + i]), acc[32 * l + i]);
+                }
+            };
+            auto load_block = [&](uint32_t buf, uint32_t (&r)[kBsCols]) {
+#pragma unroll
+                for (int l = 0; l < kLoads; ++l)
+                    tmem_ld_32x32b_x32(tmem_base + buf * BN + t_cols + 32u * l, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * l));
+                tmem_ld_wait();
+#pragma unroll
+                for (int l = 0; l < kLoads; ++l) reg_fence(*reinterpret_cast<uint32_t(*)[32]>(r + 32 * l));
+            };
+            // Blocks come in pairs (2g, 2g + 1) that share one hand-off; a K
+            // loop with an odd block count ends in a pair of one.
+            const int ngroups = (p.num_sb + 1) / 2;
+            for (int g = 0; g < ngroups; ++g) {
+                const int b0 = 2 * g;
+                const bool two = b0 + 1 < p.num_sb;
+                // both blocks' factor copies have landed once at most
+                // kBsScaleAhead - 2 commit groups are pending
+                cp_async_wait<kBsScaleAhead - 2>();
+                __syncwarp();
+                const uint32_t slot0 = ring + static_cast<uint32_t>((b0 % kBsScaleAhead) * 16);
+                const uint32_t slot1 = ring + static_cast<uint32_t>(((b0 + 1) % kBsScaleAhead) * 16);
+                const float sa0 = ld_shared_f32(slot0), sa1 = ld_shared_f32(slot1);
+                float sb0[kLoads], sb1[kLoads];
+#pragma unroll
+                for (int l = 0; l < kLoads; ++l) {
+                    sb0[l] = ld_shared_f32(slot0 + 4u * (l + 1));
+                    sb1[l] = ld_shared_f32(slot1 + 4u * (l + 1));
+                }
+                __syncwarp();
+                fetch(b0 + kBsScaleAhead);       // the two slots just read
+                fetch(b0 + 1 + kBsScaleAhead);
                 if (!wait_bar_warp(bar_pfull + 8 * pb, pph, w, kRoleEpilogue, 32 + pb)) {
                     ok = false;
                     break;
@@ -350,36 +397,26 @@ hgemm_fp8bs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                 if (lane == 0 && warp == kBsEpiWarps - 1) bs_trace(p, nblk, kBsEpiLastWaited);
                 tc_fence_after();
                 uint32_t r[kBsCols];
-                const uint32_t t_col = tmem_base + pb * BN + static_cast<uint32_t>(kBsCols * colgrp) + t_lane;
-#pragma unroll
-                for (int l = 0; l < kLoads; ++l)
-                    tmem_ld_32x32b_x32(t_col + 32u * l, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * l));
-                tmem_ld_wait();
-#pragma unroll
-                for (int l = 0; l < kLoads; ++l) reg_fence(*reinterpret_cast<uint32_t(*)[32]>(r + 32 * l));
+                load_block(2u * pb, r);
                 if (lane == 0 && warp == 0) bs_trace(p, nblk, kBsEpiLoaded);
-                // the buffer's reads are done: hand it back to the MMA warp
+                accumulate(r, sa0, sb0);
+                if (two) load_block(2u * pb + 1u, r);
+                // the pair's reads are done: hand its two buffers back to the MMA warp
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) release_accumulator<CG>(bar_pempty + 8 * pb, 0);
-                if (++pb == static_cast<uint32_t>(R)) {
+                if (++pb == static_cast<uint32_t>(kGroups)) {
                     pb = 0;
                     pph ^= 1u;
                 }
-#pragma unroll
-                for (int l = 0; l < kLoads; ++l) {
-                    const float sf = csa * csb[l];
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2)
-                        fma2_bcast(acc[32 * l + i], acc[32 * l + i + 1], sf, __uint_as_float(r[32 * l + i]),
-                                   __uint_as_float(r[32 * l + i + 1]));
-                }
+                if (two) accumulate(r, sa1, sb1);
                 if (lane == 0 && warp == 0) {
                     asm volatile("" :: "f"(acc[0]), "f"(acc[kBsCols - 1]));
                     bs_trace(p, nblk, kBsEpiDone);
                 }
                 ++nblk;
             }
+            cp_async_wait<0>();
             if (!ok) break;
             // Round to bf16 and store this thread's row: kBsCols columns from col_base.
             const int32_t row = row_base + static_cast<int32_t>(lane);
