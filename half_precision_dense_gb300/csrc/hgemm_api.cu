@@ -416,7 +416,7 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dt, cons
     std::memset(pl, 0, sizeof(*pl));
     hgemm_config_t c{};
     if (cfg) c = *cfg;
-    if (c.group_m < 0 || c.max_clusters < 0 || c.store_mode < 0 || c.store_mode > 4 || c.stream_k < 0 ||
+    if (c.group_m < 0 || c.max_clusters < 0 || c.store_mode < 0 || c.store_mode > 5 || c.stream_k < 0 ||
         c.stream_k > 4 || c.split_k < 0 || c.split_k > 8) {
         t_last_error = "negative or unknown config field";
         return HGEMM_ERR_INVALID_ARG;
@@ -502,8 +502,17 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dt, cons
     // 53.2 -> 46.7, 16384x16384x64 156 -> 105. At K = 1024 the two modes
     // tie (4096x4096x1024: 30.8 us each).
     const int64_t num_kb_plan = cdiv(K, bk_of(dt));
-    pl->store_mode = (c.store_mode != 0) ? c.store_mode : c_unaligned ? 2 : num_kb_plan <= 8 ? 1 : 4;
-    if (c_unaligned && pl->store_mode != 2) {
+    // A C whose rows are not 16-byte aligned: 16-bit C takes realigned
+    // 16-byte stores with element stores at the ragged ends (5); fp32 C (tf32)
+    // plain element stores (2). Measured against element stores: 1000 x 4095
+    // x 4104 53.2 against 55.4 us, 3000 x 1001 x 2048 32.8 against 34.6.
+    const bool c16 = c_esize_of(dt) == 2;
+    pl->store_mode = (c.store_mode != 0) ? c.store_mode : c_unaligned ? (c16 ? 5 : 2) : num_kb_plan <= 8 ? 1 : 4;
+    if (pl->store_mode == 5 && !c16) {
+        t_last_error = "store_mode 5 is for 16-bit C";
+        return HGEMM_ERR_INVALID_ARG;
+    }
+    if (c_unaligned && pl->store_mode != 2 && pl->store_mode != 5) {
         t_last_error = "vector and TMA stores need a 16-byte aligned C with a 16-byte row pitch";
         return HGEMM_ERR_INVALID_ARG;
     }
@@ -807,6 +816,7 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
         q.sched.sk_base = 0;
         q.sched.sk_extra = 0;
         q.trace = g_trace.load(std::memory_order_relaxed);
+        q.pdl = (pl.repack_a || pl.repack_b) ? 1 : 0;
         if ((e = hg::status_word_ptr(&q.status)) != cudaSuccess) {
             if (work && work != scratch) cudaFreeAsync(work, stream);
             return cuda_fail(e, "status word");
@@ -864,11 +874,13 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
                   ? reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(work) + wl.off_flags)
                   : nullptr;
     p.epoch = next_epoch();
+    bool cleared_flags = false;
     if (p.flags) {
         // A graph replays this launch with the same epoch, so flags left by
         // the previous replay would already read as published: a captured
         // launch clears its flags first (an eager launch's epoch is new).
         cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        cleared_flags = true;   // conservatively: a memset may sit between the copy and the GEMM
         if ((e = cudaStreamIsCapturing(stream, &cs)) != cudaSuccess ||
             (cs == cudaStreamCaptureStatusActive &&
              (e = cudaMemsetAsync(p.flags, 0, static_cast<size_t>(flag_bytes(pl)), stream)) != cudaSuccess)) {
@@ -878,6 +890,10 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
     }
     p.inject = g_inject.load(std::memory_order_relaxed);
     p.trace = g_trace.load(std::memory_order_relaxed);
+    // right after an operand copy on the same stream (no flag clearing in
+    // between), the GEMM launches as its programmatic dependent: its launch
+    // and set-up overlap the copy's tail
+    p.pdl = ((pl.repack_a || pl.repack_b) && !cleared_flags) ? 1 : 0;
     if ((e = hg::status_word_ptr(&p.status)) != cudaSuccess) {
         if (work && work != scratch) cudaFreeAsync(work, stream);
         return cuda_fail(e, "status word");

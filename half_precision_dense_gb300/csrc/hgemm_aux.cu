@@ -9,27 +9,6 @@ namespace hg {
 
 __device__ unsigned long long g_status_word;
 
-// Bytes [o, o + 16) of the 32 bytes a|b (o < 16), as one 16-byte vector:
-// word i of the result is the funnel shift of words o/4 + i and o/4 + i + 1
-// right by 8 (o % 4) bits.
-__device__ __forceinline__ uint4 bytes_from(const uint4& a, const uint4& b, uint32_t o) {
-    const uint32_t sh = (o & 3u) * 8u;
-    switch (o >> 2) {
-        case 0:
-            return make_uint4(__funnelshift_r(a.x, a.y, sh), __funnelshift_r(a.y, a.z, sh),
-                              __funnelshift_r(a.z, a.w, sh), __funnelshift_r(a.w, b.x, sh));
-        case 1:
-            return make_uint4(__funnelshift_r(a.y, a.z, sh), __funnelshift_r(a.z, a.w, sh),
-                              __funnelshift_r(a.w, b.x, sh), __funnelshift_r(b.x, b.y, sh));
-        case 2:
-            return make_uint4(__funnelshift_r(a.z, a.w, sh), __funnelshift_r(a.w, b.x, sh),
-                              __funnelshift_r(b.x, b.y, sh), __funnelshift_r(b.y, b.z, sh));
-        default:
-            return make_uint4(__funnelshift_r(a.w, b.x, sh), __funnelshift_r(b.x, b.y, sh),
-                              __funnelshift_r(b.y, b.z, sh), __funnelshift_r(b.z, b.w, sh));
-    }
-}
-
 // Copy a rows x cols matrix of E-byte values (E = 1, 2 or 4) with row pitch
 // `cols` (any base alignment of E bytes) into `dst` with row pitch `dst_ld`
 // (16-byte aligned base, dst_ld * E a multiple of 16). Each thread writes 16
@@ -43,6 +22,8 @@ __device__ __forceinline__ uint4 bytes_from(const uint4& a, const uint4& b, uint
 template <typename T>
 __global__ void repack_rows_kernel(const T* __restrict__ src, int64_t rows, int64_t cols,
                                    T* __restrict__ dst, int64_t dst_ld) {
+    // the GEMM that reads the copy may start its set-up now
+    grid_launch_dependents();
     constexpr int kPer = 16 / sizeof(T);
     const int64_t chunks = (cols + kPer - 1) / kPer;
     const uintptr_t src_end = reinterpret_cast<uintptr_t>(src + rows * cols);

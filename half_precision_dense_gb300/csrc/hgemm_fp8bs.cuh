@@ -86,6 +86,7 @@ struct Fp8bsParams {
     unsigned long long* status;
     Schedule sched;                 // whole tiles only
     unsigned long long* trace;      // per-block clock64 records (builds with HG_TRACE only), or null
+    int32_t pdl;                    // host: launched as a programmatic dependent of an operand copy
 };
 
 // Traced builds: clock64 stamps of the first 64 scale blocks of CTAs 0 and 1
@@ -177,6 +178,7 @@ hgemm_fp8bs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     __syncthreads();
     if constexpr (CG > 1) cluster_sync();
     tc_fence_after();
+    grid_dependency_wait();   // after an operand copy launched just before this kernel
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
     const Waiter w{abort_flag, p.timeout_ns, p.status};
 

@@ -82,7 +82,10 @@ struct TcParams {
     uint32_t idesc;                 // tcgen05 instruction descriptor
     int32_t store_mode;             // 1: TMA stores of C; 2: plain element stores through `C`;
                                     // 3: direct 16-byte stores through `C` (aligned C only);
-                                    // 4: smem-staged, coalesced 16-byte stores (aligned C only)
+                                    // 4: smem-staged, coalesced 16-byte stores (aligned C only);
+                                    // 5: smem-staged 16-byte stores realigned to each row's
+                                    //    start, element stores at the ragged ends (16-bit C,
+                                    //    any pitch)
     uint16_t* C;                    // used by store modes 2-4 (fp32 elements for tf32)
     const float* a_scale;           // fp8: one factor per row of A, or null (1)
     const float* b_scale;           // fp8: one factor per column of B, or null (1)
@@ -105,6 +108,8 @@ struct TcParams {
                                     // that are never published; 2 = a K-split cluster's rank 0
                                     // withholds its ring-free arrival (the waits run out)
     unsigned long long* trace;      // timeline records (builds with HG_TRACE only), or null
+    int32_t pdl;                    // host: launched as a programmatic dependent of the kernel
+                                    // before it on the stream (an operand copy)
 };
 
 // Timeline records of a traced build: per CTA, per unit it takes (up to
@@ -389,6 +394,74 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
     for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i]));
 }
 
+// Store mode 5, one warp's 32 rows x 64 (or 32, `half`) columns of 16-bit C
+// from its swizzled staging box, for a C whose rows do not start on 16-byte
+// boundaries (a row pitch that is not a multiple of 8 elements). A row's
+// 16 * nseg bytes start at offset o (even) in a 16-byte segment: lane g of the
+// row's nseg lanes writes the aligned segment g (g >= 1 when o > 0), assembled
+// from box chunks g - 1 and g and shifted into place, and one of the row's
+// eight edge elements (the head [0, 8 - o/2) and the tail, which share a
+// segment with the neighbouring chunk of the row), so every lane does the
+// same work and nothing outside these columns is written. Kept out of line:
+// only an unaligned C calls it, and inlined it would take registers from the
+// main loop of every instantiation.
+// Element i (0..7) of eight 16-bit values packed in a 16-byte vector.
+__device__ __forceinline__ uint16_t u16_of(const uint4& v, int32_t i) {
+    const uint32_t w = (i >> 1) == 0 ? v.x : (i >> 1) == 1 ? v.y : (i >> 1) == 2 ? v.z : v.w;
+    return static_cast<uint16_t>((i & 1) ? (w >> 16) : (w & 0xFFFFu));
+}
+
+static __device__ __noinline__ void store_chunk_realigned(const uint8_t* box_ptr, uint16_t* C, int64_t ldc,
+                                                          int32_t M, int32_t N, int32_t row0, int32_t ccol,
+                                                          bool half, uint32_t lane) {
+    const uint32_t nseg = half ? 4u : 8u;       // 16-byte chunks per box row
+    const int32_t nel = 8 * static_cast<int32_t>(nseg);
+    const int32_t nvalid = N - ccol;            // columns of the chunk inside C
+    if (nvalid <= 0) return;
+#pragma unroll 2
+    for (uint32_t piece = lane; piece < 32u * nseg; piece += 32u) {
+        const uint32_t rr = piece / nseg, g = piece % nseg;
+        const int32_t row = row0 + static_cast<int32_t>(rr);
+        if (row >= M) continue;
+        uint16_t* const crow = C + static_cast<int64_t>(row) * ldc + ccol;
+        const uint32_t o = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(crow) & 15u);   // even
+        const uint32_t sw = half ? ((rr >> 1) & 3u) : (rr & 7u);
+        const uint8_t* const brow = box_ptr + rr * (half ? 64u : 128u);
+        const uint4 cg = *reinterpret_cast<const uint4*>(brow + ((g ^ sw) << 4));
+        if (o == 0) {
+            const int32_t e0 = 8 * static_cast<int32_t>(g);
+            if (e0 + 8 <= nvalid) {
+                *reinterpret_cast<uint4*>(crow + e0) = cg;
+            } else {
+                for (int32_t e = e0; e < nvalid && e < e0 + 8; ++e) crow[e] = u16_of(cg, e - e0);
+            }
+            continue;
+        }
+        const int32_t half_o = static_cast<int32_t>(o >> 1);
+        if (g > 0) {
+            // the aligned segment holding elements [8g - o/2, 8g - o/2 + 8)
+            const int32_t e0 = 8 * static_cast<int32_t>(g) - half_o;
+            const uint4 cp = *reinterpret_cast<const uint4*>(brow + (((g - 1u) ^ sw) << 4));
+            const uint4 v = bytes_from(cp, cg, 16u - o);
+            if (e0 + 8 <= nvalid) {
+                *reinterpret_cast<uint4*>(crow + e0) = v;
+            } else {
+                for (int32_t e = e0; e < nvalid && e < e0 + 8; ++e) crow[e] = u16_of(v, e - e0);
+            }
+        }
+        // edge element k = g (and k = g + 4 for a 32-column chunk, whose row
+        // has four lanes): head elements [0, 8 - o/2), then the tail
+        for (uint32_t k = g; k < 8u; k += nseg) {
+            const int32_t e = static_cast<int32_t>(k) < 8 - half_o ? static_cast<int32_t>(k)
+                                                                   : nel - 8 + static_cast<int32_t>(k);
+            if (e < nvalid) {
+                const uint32_t ue = static_cast<uint32_t>(e);
+                crow[e] = *reinterpret_cast<const uint16_t*>(brow + (((ue >> 3) ^ sw) << 4) + ((ue & 7u) << 1));
+            }
+        }
+    }
+}
+
 // MC > 1 (single CTAs only: CG = 1, MC = 2, 4 or 8): the MC CTAs of a
 // cluster split one 128 x BN tile's K loop (split-K within the cluster) and
 // reduce their fp32 partial sums through distributed shared memory; that puts
@@ -488,6 +561,9 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     __syncthreads();
     if constexpr (kCluster > 1) cluster_sync();
     tc_fence_after();
+    // Launched as a programmatic dependent of an operand copy, the kernel has
+    // run its set-up alongside the copy; global memory is read only after it.
+    grid_dependency_wait();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
     const Waiter w{abort_flag, p.timeout_ns, p.status};
     if (threadIdx.x == 0) trace_stamp(p, 0, kTrSetup);
@@ -891,7 +967,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                             const uint32_t lo = pack_rn<kDt>(__float_as_uint(acc4.x), __float_as_uint(acc4.y));
                             const uint32_t hi = pack_rn<kDt>(__float_as_uint(acc4.z), __float_as_uint(acc4.w));
                             uint16_t* dst = p.C + static_cast<int64_t>(row) * p.ldc + col;
-                            if (p.store_mode != 2 && col + 4 <= p.N) {
+                            if (p.store_mode != 2 && p.store_mode != 5 && col + 4 <= p.N) {
                                 // C 16-byte aligned with a 16-byte pitch, col a
                                 // multiple of 4: an 8-byte aligned store
                                 *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
@@ -1237,6 +1313,10 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     }
                     __syncwarp();
                     if (warp == 0 && lane == 0) trace_chunk(p, it, c, kTcStored);
+                } else if (p.store_mode == 5) {
+                    __syncwarp();
+                    store_chunk_realigned(box_ptr, p.C, p.ldc, p.M, p.N, row0, ccol, half, lane);
+                    __syncwarp();
                 } else {
                     __syncwarp();
                     const uint32_t width = half ? 32u : 64u;

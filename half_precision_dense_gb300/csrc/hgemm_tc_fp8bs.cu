@@ -20,7 +20,7 @@ using Fp8bsInstance = ClusterKernel<&hgemm_fp8bs_kernel<CG, kGs, kDt>, CG, Fp8bs
 
 cudaError_t launch_fp8bs(int kind, int cta_group, int gs, const CUtensorMap& a, const CUtensorMap& b,
                          const CUtensorMap& b2, const Fp8bsParams& p, int clusters, cudaStream_t stream) {
-    HG_FP8BS_DISPATCH(launch(clusters, stream, a, b, b2, p))
+    HG_FP8BS_DISPATCH(launch(clusters, stream, p.pdl != 0, a, b, b2, p))
     return cudaErrorInvalidValue;
 }
 

@@ -18,6 +18,19 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
+// ------------------------------------------------ programmatic dependent launch
+// Wait until the grids this one depends on have completed and their memory
+// is visible (a no-op for a kernel not launched as a programmatic dependent).
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Let a programmatic dependent of this grid launch (its set-up may then run
+// alongside this grid; it waits for this grid's completion before reading).
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------- cluster
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
@@ -211,6 +224,27 @@ __device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
     float v;
     asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
     return v;
+}
+
+// Bytes [o, o + 16) of the 32 bytes a|b (o < 16), as one 16-byte vector:
+// word i of the result is the funnel shift of words o/4 + i and o/4 + i + 1
+// right by 8 (o % 4) bits.
+__device__ __forceinline__ uint4 bytes_from(const uint4& a, const uint4& b, uint32_t o) {
+    const uint32_t sh = (o & 3u) * 8u;
+    switch (o >> 2) {
+        case 0:
+            return make_uint4(__funnelshift_r(a.x, a.y, sh), __funnelshift_r(a.y, a.z, sh),
+                              __funnelshift_r(a.z, a.w, sh), __funnelshift_r(a.w, b.x, sh));
+        case 1:
+            return make_uint4(__funnelshift_r(a.y, a.z, sh), __funnelshift_r(a.z, a.w, sh),
+                              __funnelshift_r(a.w, b.x, sh), __funnelshift_r(b.x, b.y, sh));
+        case 2:
+            return make_uint4(__funnelshift_r(a.z, a.w, sh), __funnelshift_r(a.w, b.x, sh),
+                              __funnelshift_r(b.x, b.y, sh), __funnelshift_r(b.y, b.z, sh));
+        default:
+            return make_uint4(__funnelshift_r(a.w, b.x, sh), __funnelshift_r(b.x, b.y, sh),
+                              __funnelshift_r(b.y, b.z, sh), __funnelshift_r(b.z, b.w, sh));
+    }
 }
 
 __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {

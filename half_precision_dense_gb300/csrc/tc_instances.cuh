@@ -29,8 +29,11 @@ struct ClusterKernel {
         return e;
     }
 
+    // `pdl`: programmatic dependent launch, the kernel may start before the
+    // preceding kernel on the stream ends (it waits with griddepcontrol.wait
+    // before reading global memory).
     static void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int clusters,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, bool pdl = false) {
         cfg = cudaLaunchConfig_t{};
         cfg.gridDim = dim3(static_cast<unsigned>(clusters * kCluster), 1, 1);
         cfg.blockDim = dim3(kBlockThreads, 1, 1);
@@ -40,17 +43,19 @@ struct ClusterKernel {
         attr[0].val.clusterDim.x = kCluster;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = pdl ? 2 : 1;
     }
 
     template <typename... Args>
-    static cudaError_t launch(int clusters, cudaStream_t stream, const Args&... args) {
+    static cudaError_t launch(int clusters, cudaStream_t stream, bool pdl, const Args&... args) {
         cudaError_t e = prepare();
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t cfg;
-        cudaLaunchAttribute attr[1];
-        fill_config(cfg, attr, clusters, stream);
+        cudaLaunchAttribute attr[2];
+        fill_config(cfg, attr, clusters, stream, pdl);
         return cudaLaunchKernelEx(&cfg, kKernel, args...);
     }
 
@@ -65,7 +70,7 @@ struct ClusterKernel {
         }
         if (prepare() != cudaSuccess) return 0;
         cudaLaunchConfig_t cfg;
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         fill_config(cfg, attr, 1, nullptr);
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, kKernel, &cfg) != cudaSuccess) return 0;
@@ -85,7 +90,7 @@ struct TcInstance {
     static cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                               const CUtensorMap& c32, const CUtensorMap& b2, const TcParams& p, int clusters,
                               cudaStream_t stream) {
-        return K::launch(clusters, stream, a, b, c, c32, b2, p);
+        return K::launch(clusters, stream, p.pdl != 0, a, b, c, c32, b2, p);
     }
 
     static int max_clusters() { return K::max_clusters(); }

@@ -97,8 +97,10 @@ typedef enum {
  * pointers aligned to it).
  *
  * Workspace: operands whose row pitch (K or N elements) or base address is
- * not a multiple of 16 bytes are first copied into a
- * 16-byte-pitched workspace (such a C is written with plain stores), and when
+ * not a multiple of 16 bytes are first copied into a 16-byte-pitched
+ * workspace by a copy kernel, and the GEMM launches as its programmatic
+ * dependent (its set-up overlaps the copy's tail); such a C is written with
+ * realigned 16-byte and element stores (store_mode 5 below), and when
  * tiles are shared by stream-K ranges the parts' fp32 partial sums go through
  * the workspace too. It comes from a stream-ordered memory pool owned
  * by the library (one per device, cudaMallocFromPoolAsync / cudaFreeAsync on
@@ -206,9 +208,13 @@ uint64_t hgemm_noalloc_scratch_bytes(void);
  *                  straight from registers, 4 = 16-byte vector stores of whole
  *                  rows read back from the swizzled smem box (1, 3 and 4 need
  *                  a 16-byte aligned C whose row pitch is a multiple of 16
- *                  bytes). The planner takes 4 for such a C (1 when the K
- *                  loop has at most 8 blocks: the epilogue then sets the
- *                  pace, and TMA stores are faster), else 2.
+ *                  bytes), 5 = the staged rows written as the aligned 16-byte
+ *                  segments they cover, shifted into place, with element
+ *                  stores at each row's ragged ends (16-bit C of any pitch).
+ *                  The planner takes 4 for an aligned C (1 when the K loop
+ *                  has at most 8 blocks: the epilogue then sets the pace, and
+ *                  TMA stores are faster); for any other C, 5 (16-bit C) or 2
+ *                  (fp32 C).
  *   stream_k:      how the tiles past the last whole wave are shared:
  *                  0 = planner's choice; 1 = never (whole tiles only, spread
  *                  over as few clusters as keep the wave count); 2 = stream-K
@@ -357,7 +363,7 @@ typedef struct {
     int32_t tmem_cols;     /* tensor-memory columns allocated per CTA */
     int32_t repack_a;      /* 1 if A goes through the 16-byte-pitch workspace */
     int32_t repack_b;      /* 1 if B does (B is otherwise read in place, MN-major, for every dtype) */
-    int32_t store_mode;    /* 1 = TMA, 2 = plain, 3 = vector, 4 = staged vector stores */
+    int32_t store_mode;    /* 1 = TMA, 2 = plain, 3 = vector, 4 = staged vector, 5 = realigned staged stores */
     int32_t dp_tiles;      /* tiles computed whole, round-robin (the first dp_tiles in raster order) */
     int32_t sk_tiles;      /* tiles after them shared by stream-K ranges (0 = none) */
     int32_t sk_blocks;     /* K blocks per cluster in the stream-K phase (the first

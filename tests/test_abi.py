@@ -141,7 +141,8 @@ def test_plan_shapes(lib):
     # aligned C: rows written back from the staging box by 16-byte stores
     assert p["repack_a"] == 0 and p["repack_b"] == 0 and p["store_mode"] == 4
     t = binding.plan(1000, 4095, 4104, "bf16", sm_count=148)
-    assert t["repack_b"] == 1 and t["repack_a"] == 0 and t["store_mode"] == 2
+    # an unaligned 16-bit C: realigned 16-byte stores with element stores at the ragged ends
+    assert t["repack_b"] == 1 and t["repack_a"] == 0 and t["store_mode"] == 5
     forced = binding.plan(512, 512, 512, "f16",
                           binding.Config(cta_group=1, block_n=64, max_clusters=3), sm_count=148)
     assert (forced["cta_group"], forced["block_n"], forced["grid_ctas"]) == (1, 64, 3)
@@ -320,8 +321,8 @@ def test_split_share_partitions_the_k_range(lib, n, parts):
 def test_plan_short_k_uses_tma_stores(lib, shape, store_mode, tile):
     p = binding.plan(*shape, "bf16", sm_count=152)
     assert p["store_mode"] == store_mode and (p["cta_group"], p["block_n"]) == tile
-    # an unaligned C keeps plain stores; a forced mode is kept
-    assert binding.plan(shape[0], shape[1] + 1, shape[2], "bf16", sm_count=152)["store_mode"] == 2
+    # an unaligned 16-bit C takes the realigned stores; a forced mode is kept
+    assert binding.plan(shape[0], shape[1] + 1, shape[2], "bf16", sm_count=152)["store_mode"] == 5
     assert binding.plan(*shape, "bf16", binding.Config(store_mode=3), sm_count=152)["store_mode"] == 3
 
 
@@ -411,8 +412,17 @@ def test_plan_fp8(lib):
     # K = 1000 bytes is not a 16-byte pitch (A repacked); 1008 is
     assert binding.plan(64, 1024, 1000, "e4m3", sm_count=152)["repack_a"] == 1
     assert binding.plan(64, 1024, 1008, "e4m3", sm_count=152)["repack_a"] == 0
-    # C is bf16: N = 1004 gives a 2008-byte pitch, not a multiple of 16 -> plain stores
-    assert binding.plan(64, 1004, 1024, "e5m2", sm_count=152)["store_mode"] == 2
+    # C is bf16: N = 1004 gives a 2008-byte pitch, not a multiple of 16 -> realigned stores
+    assert binding.plan(64, 1004, 1024, "e5m2", sm_count=152)["store_mode"] == 5
+    # fp32 C (tf32) with an unaligned pitch keeps plain stores; mode 5 is for 16-bit C only
+    assert binding.plan(64, 1001, 1024, "tf32", sm_count=152)["store_mode"] == 2
+    with pytest.raises(binding.HgemmError):
+        binding.plan(64, 1024, 1024, "tf32", binding.Config(store_mode=5), sm_count=152)
+    # on an unaligned 16-bit C only the element and realigned modes are accepted
+    for mode in (1, 3, 4):
+        with pytest.raises(binding.HgemmError):
+            binding.plan(64, 1001, 1024, "bf16", binding.Config(store_mode=mode), sm_count=152)
+    assert binding.plan(64, 1001, 1024, "bf16", binding.Config(store_mode=2), sm_count=152)["store_mode"] == 2
     # every dtype takes the 224-wide pair tile (its last chunk is 32 columns)
     for dt in ("tf32", "e4m3", "e5m2", "bf16", "f16"):
         assert binding.plan(1024, 1024, 1024, dt, binding.Config(cta_group=2, block_n=224),

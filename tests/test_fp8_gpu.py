@@ -123,7 +123,7 @@ def test_persistent_loop(cfg):
 
 
 @pytest.mark.parametrize("block_n", [224, 256])
-@pytest.mark.parametrize("store_mode", [1, 2, 3, 4])
+@pytest.mark.parametrize("store_mode", [1, 2, 3, 4, 5])
 def test_store_modes(store_mode, block_n):
     # 224: the last 32-column chunk of every tile goes through each store path
     check(700, 1024, 512, "e4m3", 4, hg.Config(cta_group=2, block_n=block_n, store_mode=store_mode))

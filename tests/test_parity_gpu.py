@@ -245,10 +245,11 @@ def test_raster_groups(group_m):
 
 
 @pytest.mark.parametrize("cfg", CONFIGS, ids=CFG_IDS)
-@pytest.mark.parametrize("store_mode", [2, 3, 4])
+@pytest.mark.parametrize("store_mode", [2, 3, 4, 5])
 def test_store_modes_match(cfg, store_mode):
-    # plain 2-byte stores, direct 16-byte vector stores and smem-staged
-    # coalesced stores, ragged M and N
+    # plain 2-byte stores, direct 16-byte vector stores, smem-staged
+    # coalesced stores and realigned staged stores (on an aligned C), ragged
+    # M and N
     c = hg.Config(cfg.cta_group, cfg.block_n, 0, 0, store_mode, 0, cfg.multicast)
     A, B = operands(700, 520, 300, "bf16", 8)
     check_full(A, B, "bf16", c)
@@ -267,6 +268,38 @@ def test_unaligned_pitches(shape):
     M, N, K = shape
     A, B = operands(M, N, K, "bf16", 9)
     check_full(A, B, "bf16")
+
+
+@pytest.mark.parametrize("cfg", CONFIGS, ids=CFG_IDS)
+@pytest.mark.parametrize("store_mode", [2, 5])
+@pytest.mark.parametrize("N", [4095, 1001, 777, 130])
+def test_unaligned_c_store_modes(cfg, store_mode, N):
+    # row pitches of N 16-bit elements that are not multiples of 8: every row
+    # starts at a different offset inside a 16-byte segment; the realigned
+    # stores (5) must touch exactly the columns of C, as the element stores (2)
+    # do (the canary bands around C stay intact), on ragged M and N
+    M, K = 300, 200
+    A, B = operands(M, N, K, "bf16", 36)
+    check_full(A, B, "bf16", hg.Config(cfg.cta_group, cfg.block_n, 0, 0, store_mode, 0, 0))
+
+
+def test_unaligned_c_offset_base_and_split_k():
+    # a C base 2 bytes past a 16-byte boundary with an aligned pitch (every
+    # row misaligned the same way), through the planner's realigned stores,
+    # and the K split's own stores on the same C
+    M, N, K = 200, 264, 1536
+    A, B = operands(M, N, K, "f16", 37)
+    a, b = inputs.bits(A), inputs.bits(B)
+    ref64 = oracle.gemm_f64(a, b, "f16")
+    for cfg in (None, hg.Config(block_n=128, split_k=2)):
+        dC = torch.zeros(M * N + 9, dtype=torch.float16, device="cuda")
+        C = dC[1:1 + M * N]
+        hg.hgemm_ex(A.cuda(), B.cuda(), C, M, N, K, "f16", cfg)
+        torch.cuda.synchronize()
+        assert dC[0].item() == 0 and torch.count_nonzero(dC[1 + M * N:]).item() == 0
+        got = inputs.bits(C.view(M, N).cpu())
+        r = compare(got, oracle.round_rne(ref64, "f16"), ref64, "f16", K)
+        assert r["ok"], r
 
 
 def test_unaligned_base_pointers():
