@@ -317,9 +317,18 @@ int64_t pitch16(int64_t cols, int esize) {
     return (cols + per - 1) / per * per;
 }
 
+// Rows of an operand copy: padded to 128 bytes, so that every row of a TMA
+// box starts on a 128-byte line. A pitch that is an odd multiple of 16 bytes
+// costs the GEMM's loads 10-20 % (1000 x 4096 x K bf16, A read in place:
+// K = 4104 33.6 us, 4112 29.3, 4128 28.6, 4160 28.3).
+int64_t pitch128(int64_t cols, int esize) {
+    const int64_t per = 128 / esize;
+    return (cols + per - 1) / per * per;
+}
+
 WorkspaceLayout workspace_layout(const hgemm_plan_t& pl, int64_t M, int64_t N, int64_t K, int esize) {
     WorkspaceLayout w{};
-    const int64_t lda = pitch16(K, esize), ldb = pitch16(N, esize);
+    const int64_t lda = pitch128(K, esize), ldb = pitch128(N, esize);
     int64_t off = 0;
     w.off_a = off;
     off += pl.repack_a ? align256(esize * M * lda) : 0;
@@ -708,11 +717,11 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
     }
     const int clusters = pl.grid_ctas / (cg * mc);
 
-    // Workspace: 16-byte-pitched copies of operands TMA cannot address, and
+    // Workspace: 128-byte-pitched copies of operands TMA cannot address, and
     // the fp32 partial sums of a K-split tail.
     const WorkspaceLayout wl = workspace_layout(pl, M, N, K, es);
-    const int64_t lda = lda_in > 0 ? lda_in : pl.repack_a ? pitch16(K, es) : K;
-    const int64_t ldb = pl.repack_b ? pitch16(N, es) : N;
+    const int64_t lda = lda_in > 0 ? lda_in : pl.repack_a ? pitch128(K, es) : K;
+    const int64_t ldb = pl.repack_b ? pitch128(N, es) : N;
     void* work = nullptr;
     const void* a_use = A;
     const void* b_use = B;

@@ -5,7 +5,7 @@
 // disallowed, real-time or embedded pipelines that fix their memory at start
 // and treat any later allocation as a fault, and hosts whose device memory is
 // owned by another runtime's pool. For them, hgemm_noalloc() takes the
-// workspace the GEMM may need - the 16-byte-pitch copy of an operand whose
+// workspace the GEMM may need - the 128-byte-pitch copy of an operand whose
 // rows TMA cannot address, and the fp32 partial sums of a stream-K schedule
 // (hgemm_noalloc_ex with a config) - from a fixed array compiled into this
 // library instead of from the stream-ordered allocator.

@@ -97,8 +97,8 @@ typedef enum {
  * pointers aligned to it).
  *
  * Workspace: operands whose row pitch (K or N elements) or base address is
- * not a multiple of 16 bytes are first copied into a 16-byte-pitched
- * workspace by a copy kernel, and the GEMM launches as its programmatic
+ * not a multiple of 16 bytes are first copied into a workspace whose rows
+ * start on 128-byte boundaries by a copy kernel, and the GEMM launches as its programmatic
  * dependent (its set-up overlaps the copy's tail); such a C is written with
  * realigned 16-byte and element stores (store_mode 5 below), and when
  * tiles are shared by stream-K ranges the parts' fp32 partial sums go through
@@ -166,7 +166,7 @@ void hgemm_conv2d_set_mode(int32_t mode);
  * another runtime's pool.
  *
  * Same operation and arguments as hgemm(), and the same results. The only
- * workspace the GEMM can need (the 16-byte-pitch copy of A or B when a row
+ * workspace the GEMM can need (the 128-byte-pitch copy of A or B when a row
  * pitch or base address is not 16-byte aligned, and the fp32 partial sums of
  * the stream-K phase) comes from a fixed 64 MiB array inside the library
  * (hgemm_noalloc_scratch_bytes()); the call makes no cudaMalloc,
@@ -175,7 +175,7 @@ void hgemm_conv2d_set_mode(int32_t mode);
  *     HGEMM_ERR_INVALID_ARG (hgemm_last_error() gives the sizes) and enqueues
  *     nothing. The stream-K partial sums need at most one 128 x 256 fp32
  *     block per CTA (under 20 MiB), so the limit only bites on unaligned
- *     operands (their 16-byte-pitch copies).
+ *     operands (their 128-byte-pitch copies).
  *   - Every call on a device shares that device's array, which keeps the last
  *     call's contents (nothing in it needs to start at zero: stream-K parts
  *     mark their partial sums with a number unique to each launch, so stale
@@ -361,7 +361,7 @@ typedef struct {
     int32_t grid_ctas;     /* CTAs launched (a multiple of cta_group * split_k) */
     int32_t smem_bytes;    /* dynamic shared memory per CTA */
     int32_t tmem_cols;     /* tensor-memory columns allocated per CTA */
-    int32_t repack_a;      /* 1 if A goes through the 16-byte-pitch workspace */
+    int32_t repack_a;      /* 1 if A goes through the workspace (rows padded to 128 bytes) */
     int32_t repack_b;      /* 1 if B does (B is otherwise read in place, MN-major, for every dtype) */
     int32_t store_mode;    /* 1 = TMA, 2 = plain, 3 = vector, 4 = staged vector, 5 = realigned staged stores */
     int32_t dp_tiles;      /* tiles computed whole, round-robin (the first dp_tiles in raster order) */
