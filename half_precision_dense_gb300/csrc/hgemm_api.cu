@@ -326,6 +326,21 @@ int64_t pitch128(int64_t cols, int esize) {
     return (cols + per - 1) / per * per;
 }
 
+// A's rows an odd multiple of 16 bytes apart: TMA can address them, but
+// with 224-wide pair tiles, whose stages already ask for about as many bytes
+// per cycle as the SM's loads deliver, the K-major A loads then run 10-20 %
+// slower (every other 128-byte box row straddles two 32-byte sectors at both
+// ends). The copy into 128-byte rows pays for itself once N is large enough.
+// Measured on GB300 (bf16, L2 flushed, copied vs in place, same box):
+// 4096 x 4096 x 4104 92.0 vs 98.9 us, 1000 x 4095 x 4104 52.3 vs 54.5,
+// 1000 x 4096 x 4104 33.8 vs 34.5; 2048 x 2048 x 2056 27.1 vs 25.5 (a loss);
+// with 256-wide tiles no cost to remove (8192 x 8192 x 8200 in place 595 us,
+// as fast as 8192^3; copied 614). B (MN-major boxes) showed no such cost:
+// 4096 x 4104 x 4096 83.6 us in place, 89.5 copied.
+bool a_pitch_slow(int64_t N, int64_t K, int esize, int block_n, int split) {
+    return ((K * esize) & 31) == 16 && N >= 3584 && block_n == 224 && split <= 1;
+}
+
 WorkspaceLayout workspace_layout(const hgemm_plan_t& pl, int64_t M, int64_t N, int64_t K, int esize) {
     WorkspaceLayout w{};
     const int64_t lda = pitch128(K, esize), ldb = pitch128(N, esize);
@@ -421,7 +436,7 @@ int auto_split(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dt, int sms) {
 
 hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dt, const hgemm_config_t* cfg, int sms,
                          bool a_unaligned, bool b_unaligned, bool c_unaligned, hgemm_plan_t* pl,
-                         bool allow_auto_split = true) {
+                         bool allow_auto_split = true, bool a_copy_ok = true) {
     std::memset(pl, 0, sizeof(*pl));
     hgemm_config_t c{};
     if (cfg) c = *cfg;
@@ -499,7 +514,7 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dt, cons
         return HGEMM_ERR_INVALID_ARG;
     }
     schedule_plan(pl, clusters, c.stream_k, cdiv(K, bk_of(dt)));
-    pl->repack_a = a_unaligned ? 1 : 0;
+    pl->repack_a = (a_unaligned || (a_copy_ok && a_pitch_slow(N, K, esize_of(dt), bn, split))) ? 1 : 0;
     pl->repack_b = b_unaligned ? 1 : 0;
     // Default for an aligned C: rows written back from the swizzled staging box
     // with 16-byte vector stores (4). They go out through the load/store path,
@@ -569,6 +584,7 @@ bool misaligned16(const void* p, int64_t cols, int esize) {
     return (reinterpret_cast<uintptr_t>(p) & 15u) != 0 || ((cols * esize) & 15) != 0;
 }
 
+
 bool overlaps(const void* a, int64_t abytes, const void* b, int64_t bbytes) {
     const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
     return a0 < b0 + static_cast<uintptr_t>(bbytes) && b0 < a0 + static_cast<uintptr_t>(abytes);
@@ -620,7 +636,8 @@ int resident_clusters(hgemm_dtype_t dtype, const hgemm_plan_t& q) {
 // whole tiles. A split asked for in `cfg` is kept (the launch then fails
 // with a message). *resident receives the resident clusters of the final plan.
 hgemm_status_t fit_split_to_device(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dtype, const hgemm_config_t* cfg,
-                                   int sms, bool a_bad, bool b_bad, bool c_bad, hgemm_plan_t* pl, int* resident) {
+                                   int sms, bool a_bad, bool b_bad, bool c_bad, hgemm_plan_t* pl, int* resident,
+                                   bool a_copy_ok = true) {
     *resident = resident_clusters(dtype, *pl);
     while (pl->split_k > 1 && !(cfg && cfg->split_k > 1) && *resident > 0 && *resident < pl->num_tiles) {
         hgemm_config_t smaller{};
@@ -630,7 +647,7 @@ hgemm_status_t fit_split_to_device(int64_t M, int64_t N, int64_t K, hgemm_dtype_
             smaller.cta_group = 1;
             smaller.block_n = pl->block_n;
         }
-        hgemm_status_t st = make_plan(M, N, K, dtype, &smaller, sms, a_bad, b_bad, c_bad, pl, false);
+        hgemm_status_t st = make_plan(M, N, K, dtype, &smaller, sms, a_bad, b_bad, c_bad, pl, false, a_copy_ok);
         if (st != HGEMM_OK) return st;
         *resident = resident_clusters(dtype, *pl);
     }
@@ -669,7 +686,9 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
     }
 
     hgemm_plan_t pl;
-    const bool a_bad = (lda_in > 0 || conv) ? false : misaligned16(A, K, es);
+    // A given as the library's im2col matrix (lda_in) or read by im2col copies is not copied
+    const bool a_copy_ok = !(lda_in > 0 || conv);
+    const bool a_bad = a_copy_ok && misaligned16(A, K, es);
     const bool b_bad = misaligned16(B, N, es), c_bad = misaligned16(C, N, ces);
     hgemm_config_t bs_cfg{};
     if (bs_block) {
@@ -682,7 +701,8 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
         bs_cfg.stream_k = 1;
         cfg = &bs_cfg;
     }
-    if ((st = make_plan(M, N, K, dtype, cfg, info.sms, a_bad, b_bad, c_bad, &pl, !conv && !bs_block)) != HGEMM_OK)
+    if ((st = make_plan(M, N, K, dtype, cfg, info.sms, a_bad, b_bad, c_bad, &pl, !conv && !bs_block, a_copy_ok)) !=
+        HGEMM_OK)
         return st;
     if (bs_block) {
         pl.stages = hg::fp8bs_stages(pl.cta_group);
@@ -701,8 +721,8 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
     int resident = 0;
     if (bs_block)
         resident = hg::max_active_clusters_fp8bs(static_cast<int>(dtype), pl.cta_group, bs_block);
-    else if ((st = fit_split_to_device(M, N, K, dtype, cfg, info.sms, a_bad, b_bad, c_bad, &pl, &resident)) !=
-             HGEMM_OK)
+    else if ((st = fit_split_to_device(M, N, K, dtype, cfg, info.sms, a_bad, b_bad, c_bad, &pl, &resident,
+                                       a_copy_ok)) != HGEMM_OK)
         return st;
     const int cg = pl.cta_group, bn = pl.block_n, mc = pl.split_k > 1 ? pl.split_k : 1;
     const int64_t num_kb = cdiv(K, bk);
@@ -717,6 +737,13 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
     }
     const int clusters = pl.grid_ctas / (cg * mc);
 
+    // A copy of A made only for speed (a_pitch_slow) is dropped when it would
+    // not fit in a caller's fixed scratch.
+    if (scratch && pl.repack_a && !a_bad &&
+        static_cast<size_t>(workspace_layout(pl, M, N, K, es).total) > scratch_bytes) {
+        pl.repack_a = 0;
+        pl.workspace_bytes = workspace_layout(pl, M, N, K, es).total;
+    }
     // Workspace: 128-byte-pitched copies of operands TMA cannot address, and
     // the fp32 partial sums of a K-split tail.
     const WorkspaceLayout wl = workspace_layout(pl, M, N, K, es);
@@ -744,19 +771,21 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
             }
         }
         uint8_t* w8 = static_cast<uint8_t*>(work);
-        if (pl.repack_a) {
-            if ((e = hg::launch_repack(A, M, K, es, w8 + wl.off_a, lda, stream)) != cudaSuccess) {
-                if (work != scratch) cudaFreeAsync(work, stream);
-                return cuda_fail(e, "repack A");
+        if (pl.repack_a || pl.repack_b) {
+            // both copies in one launch
+            hg::RepackJob ja{}, jb{};
+            if (pl.repack_a) {
+                ja = {static_cast<const uint8_t*>(A), M, es * K, w8 + wl.off_a, es * lda};
+                a_use = w8 + wl.off_a;
             }
-            a_use = w8 + wl.off_a;
-        }
-        if (pl.repack_b) {
-            if ((e = hg::launch_repack(B, K, N, es, w8 + wl.off_b, ldb, stream)) != cudaSuccess) {
-                if (work != scratch) cudaFreeAsync(work, stream);
-                return cuda_fail(e, "repack B");
+            if (pl.repack_b) {
+                jb = {static_cast<const uint8_t*>(B), K, es * N, w8 + wl.off_b, es * ldb};
+                b_use = w8 + wl.off_b;
             }
-            b_use = w8 + wl.off_b;
+            if ((e = hg::launch_repack(ja, jb, stream)) != cudaSuccess) {
+                if (work != scratch) cudaFreeAsync(work, stream);
+                return cuda_fail(e, "repack");
+            }
         }
     }
 
@@ -1053,8 +1082,8 @@ hgemm_status_t hgemm_conv2d(const void* x, const void* w, void* y, int32_t N, in
     DeviceInfo info;
     hgemm_status_t st = device_info(&dev, &info);
     if (st != HGEMM_OK) return st;
-    // the im2col matrix: M rows of Kg elements, padded to a 16-byte pitch
-    const int64_t lda = pitch16(Kg, es);
+    // the im2col matrix: M rows of Kg elements, padded to a 128-byte pitch
+    const int64_t lda = pitch128(Kg, es);
     cudaMemPool_t pool;
     if ((st = pool_for_device(dev, &pool)) != HGEMM_OK) return st;
     void* A = nullptr;

@@ -11,7 +11,8 @@ __device__ unsigned long long g_status_word;
 
 // Copy `rows` rows of `row_bytes` bytes (row r at src + r row_bytes: any
 // alignment) into rows `dst_pitch` bytes apart (dst and dst_pitch multiples
-// of 16). One warp per row; lane l writes the row's 16-byte segments l,
+// of 16), for up to two matrices in one launch (a RepackJob each). One warp
+// per row; lane l writes the row's 16-byte segments l,
 // l + 32, ..., kRepackBatch of them per pass. A segment's bytes start at
 // offset `off` inside an aligned 16-byte source block and run into the next
 // block: every source block is read once, with an aligned 16-byte load, by
@@ -41,44 +42,46 @@ __device__ __forceinline__ uint4 shfl_u4(const uint4& v, int src) {
                       __shfl_sync(0xffffffffu, v.z, src), __shfl_sync(0xffffffffu, v.w, src));
 }
 
-__global__ void __launch_bounds__(256) repack_rows_kernel(const uint8_t* __restrict__ src, int64_t rows,
-                                                          int64_t row_bytes, uint8_t* __restrict__ dst,
-                                                          int64_t dst_pitch) {
-    // the GEMM that reads the copy may start its set-up now
+__global__ void __launch_bounds__(256) repack_rows_kernel(RepackJob a, RepackJob b) {
+    // the GEMM that reads the copies may start its set-up now
     grid_launch_dependents();
     const uint32_t lane = threadIdx.x & 31u;
     const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    const uint8_t* const end = src + rows * row_bytes;
-    const int64_t nseg = (row_bytes + 15) / 16;
-    for (int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; r < rows; r += nw) {
-        const uint8_t* const row = src + r * row_bytes;
+    // rows of job a, then rows of job b (warp-uniform choice)
+    for (int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; i < a.rows + b.rows;
+         i += nw) {
+        const RepackJob& j = i < a.rows ? a : b;
+        const int64_t r = i < a.rows ? i : i - a.rows;
+        const uint8_t* const end = j.src + j.rows * j.row_bytes;
+        const int64_t nseg = (j.row_bytes + 15) / 16;
+        const uint8_t* const row = j.src + r * j.row_bytes;
         const uint32_t off = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(row) & 15u);
         const uint8_t* const base = row - off;
-        uint8_t* const d = dst + r * dst_pitch;
+        uint8_t* const d = j.dst + r * j.dst_pitch;
         for (int64_t t0 = 0; t0 < nseg; t0 += 32 * kRepackBatch) {
             uint4 v[kRepackBatch];
 #pragma unroll
-            for (int j = 0; j < kRepackBatch; ++j) {
-                const int64_t t = t0 + 32 * j + lane;
-                v[j] = t <= nseg ? load_block(base + 16 * t, end) : make_uint4(0u, 0u, 0u, 0u);
+            for (int q = 0; q < kRepackBatch; ++q) {
+                const int64_t t = t0 + 32 * q + lane;
+                v[q] = t <= nseg ? load_block(base + 16 * t, end) : make_uint4(0u, 0u, 0u, 0u);
             }
             const int64_t tx = t0 + 32 * kRepackBatch;
             const uint4 x = (lane == 31u && off != 0u && tx <= nseg) ? load_block(base + 16 * tx, end)
                                                                       : make_uint4(0u, 0u, 0u, 0u);
             if (off == 0u) {
 #pragma unroll
-                for (int j = 0; j < kRepackBatch; ++j) {
-                    const int64_t t = t0 + 32 * j + lane;
-                    if (t < nseg) *reinterpret_cast<uint4*>(d + 16 * t) = v[j];
+                for (int q = 0; q < kRepackBatch; ++q) {
+                    const int64_t t = t0 + 32 * q + lane;
+                    if (t < nseg) *reinterpret_cast<uint4*>(d + 16 * t) = v[q];
                 }
             } else {
 #pragma unroll
-                for (int j = 0; j < kRepackBatch; ++j) {
-                    uint4 hi = shfl_down_u4(v[j], 1);
-                    const uint4 nx = shfl_u4(v[j + 1 < kRepackBatch ? j + 1 : j], 0);
-                    if (lane == 31u) hi = j + 1 < kRepackBatch ? nx : x;
-                    const int64_t t = t0 + 32 * j + lane;
-                    if (t < nseg) *reinterpret_cast<uint4*>(d + 16 * t) = bytes_from(v[j], hi, off);
+                for (int q = 0; q < kRepackBatch; ++q) {
+                    uint4 hi = shfl_down_u4(v[q], 1);
+                    const uint4 nx = shfl_u4(v[q + 1 < kRepackBatch ? q + 1 : q], 0);
+                    if (lane == 31u) hi = q + 1 < kRepackBatch ? nx : x;
+                    const int64_t t = t0 + 32 * q + lane;
+                    if (t < nseg) *reinterpret_cast<uint4*>(d + 16 * t) = bytes_from(v[q], hi, off);
                 }
             }
         }
@@ -216,15 +219,16 @@ __global__ void zero_kernel(uint16_t* __restrict__ dst, int64_t count) {
         dst[i] = 0;
 }
 
-cudaError_t launch_repack(const void* src, int64_t rows, int64_t cols, int esize, void* dst,
-                          int64_t dst_ld, cudaStream_t stream) {
-    if (rows <= 0 || cols <= 0) return cudaSuccess;
-    if (esize != 1 && esize != 2 && esize != 4) return cudaErrorInvalidValue;
+cudaError_t launch_repack(const RepackJob& a, const RepackJob& b, cudaStream_t stream) {
+    const int64_t rows = (a.rows > 0 ? a.rows : 0) + (b.rows > 0 ? b.rows : 0);
+    if (rows == 0) return cudaSuccess;
     // one warp per row, up to 64 rows per SM at once
     int64_t blocks = (rows + 7) / 8;
     if (blocks > 152 * 8) blocks = 152 * 8;
-    repack_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        static_cast<const uint8_t*>(src), rows, cols * esize, static_cast<uint8_t*>(dst), dst_ld * esize);
+    RepackJob ja = a, jb = b;
+    if (ja.rows < 0) ja.rows = 0;
+    if (jb.rows < 0) jb.rows = 0;
+    repack_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(ja, jb);
     return cudaGetLastError();
 }
 

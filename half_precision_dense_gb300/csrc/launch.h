@@ -57,11 +57,17 @@ int tc_stages(int cta_group, int block_n, int esize, int split);
 int tc_smem_bytes(int cta_group, int block_n, int esize, int split);
 int tc_tmem_cols(int cta_group, int block_n);
 
-// Auxiliary kernels (hgemm_aux.cu). The repack copies rows of `cols`
-// elements of `esize` (1, 2 or 4) bytes from a dense source into rows `dst_ld`
-// elements apart (dst 16-byte aligned, dst_ld * esize a multiple of 16).
-cudaError_t launch_repack(const void* src, int64_t rows, int64_t cols, int esize, void* dst,
-                          int64_t dst_ld, cudaStream_t stream);
+// Auxiliary kernels (hgemm_aux.cu). The repack copies `rows` rows of
+// `row_bytes` bytes (any alignment, row r at src + r row_bytes) into rows
+// `dst_pitch` bytes apart (dst and dst_pitch multiples of 16); one launch
+// takes up to two matrices (rows = 0: none).
+struct RepackJob {
+    const uint8_t* src;
+    int64_t rows, row_bytes;
+    uint8_t* dst;
+    int64_t dst_pitch;
+};
+cudaError_t launch_repack(const RepackJob& a, const RepackJob& b, cudaStream_t stream);
 cudaError_t launch_zero(uint16_t* dst, int64_t count, cudaStream_t stream);
 // Convolution geometry (channels-last): x N x H x W x C, filters R x S x C x K,
 // output N x P x Q x K.

@@ -98,8 +98,11 @@ typedef enum {
  *
  * Workspace: operands whose row pitch (K or N elements) or base address is
  * not a multiple of 16 bytes are first copied into a workspace whose rows
- * start on 128-byte boundaries by a copy kernel, and the GEMM launches as its programmatic
- * dependent (its set-up overlaps the copy's tail); such a C is written with
+ * start on 128-byte boundaries by one copy kernel, and the GEMM launches as
+ * its programmatic dependent (its set-up overlaps the copy's tail). A whose
+ * rows are an odd multiple of 16 bytes apart is copied too when the plan
+ * takes 224-wide pair tiles and N >= 3584 (its loads run 10-20 % slower in
+ * place; hgemm_plan's repack_a tells); such a C is written with
  * realigned 16-byte and element stores (store_mode 5 below), and when
  * tiles are shared by stream-K ranges the parts' fp32 partial sums go through
  * the workspace too. It comes from a stream-ordered memory pool owned
@@ -173,7 +176,8 @@ void hgemm_conv2d_set_mode(int32_t mode);
  * cudaMallocAsync, cudaFree or other allocating call.
  *   - A shape whose workspace would exceed the array returns
  *     HGEMM_ERR_INVALID_ARG (hgemm_last_error() gives the sizes) and enqueues
- *     nothing. The stream-K partial sums need at most one 128 x 256 fp32
+ *     nothing; a copy of A made only for speed is left out instead when it
+ *     would not fit (A is then read in place). The stream-K partial sums need at most one 128 x 256 fp32
  *     block per CTA (under 20 MiB), so the limit only bites on unaligned
  *     operands (their 128-byte-pitch copies).
  *   - Every call on a device shares that device's array, which keeps the last

@@ -140,9 +140,22 @@ def test_plan_shapes(lib):
     assert p["smem_bytes"] <= 232448 and p["stages"] >= 2
     # aligned C: rows written back from the staging box by 16-byte stores
     assert p["repack_a"] == 0 and p["repack_b"] == 0 and p["store_mode"] == 4
-    t = binding.plan(1000, 4095, 4104, "bf16", sm_count=148)
-    # an unaligned 16-bit C: realigned 16-byte stores with element stores at the ragged ends
-    assert t["repack_b"] == 1 and t["repack_a"] == 0 and t["store_mode"] == 5
+    t = binding.plan(1000, 4095, 4104, "bf16", sm_count=152)
+    # an unaligned 16-bit C: realigned 16-byte stores with element stores at
+    # the ragged ends; B copied (8190-byte rows), and A too: its 8208-byte rows
+    # are an odd multiple of 16 bytes, which slows its loads on 224-wide pair
+    # tiles, and N is large
+    assert (t["cta_group"], t["block_n"]) == (2, 224)
+    assert t["repack_b"] == 1 and t["repack_a"] == 1 and t["store_mode"] == 5
+    # that A copy only on 224-wide tiles, where N repays it, only for A, only
+    # for odd multiples of 16 bytes
+    p = binding.plan(4096, 4096, 4104, "bf16", sm_count=152)
+    assert p["block_n"] == 224 and p["repack_a"] == 1
+    p = binding.plan(4096, 4096, 4104, "bf16", binding.Config(cta_group=2, block_n=256), sm_count=152)
+    assert p["repack_a"] == 0
+    assert binding.plan(2048, 2048, 2056, "bf16", sm_count=152)["repack_a"] == 0
+    assert binding.plan(4096, 4096, 4112, "bf16", sm_count=152)["repack_a"] == 0
+    assert binding.plan(4096, 4104, 4096, "bf16", sm_count=152)["repack_b"] == 0
     forced = binding.plan(512, 512, 512, "f16",
                           binding.Config(cta_group=1, block_n=64, max_clusters=3), sm_count=148)
     assert (forced["cta_group"], forced["block_n"], forced["grid_ctas"]) == (1, 64, 3)

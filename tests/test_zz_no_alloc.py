@@ -70,7 +70,8 @@ def test_noalloc_matches_hgemm_on_consecutive_calls(lib):
 
 
 def test_noalloc_rejects_workspace_beyond_its_scratch(lib):
-    # B of 8200 x 4097 needs 8200 * 4104 * 2 bytes (> 64 MiB) once repacked
+    # B of 8200 x 4097 needs 8200 * 4160 * 2 bytes (> 64 MiB) once copied into
+    # 128-byte rows
     M, N, K = 1, 4097, 8200
     A = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
     B = torch.zeros((K, N), dtype=torch.bfloat16, device="cuda")
@@ -80,6 +81,28 @@ def test_noalloc_rejects_workspace_beyond_its_scratch(lib):
     assert b"scratch" in lib.hgemm_last_error()
     torch.cuda.synchronize()
     assert torch.all(C == 7.0)  # nothing was enqueued
+
+
+def test_noalloc_reads_a_in_place_when_its_optional_copy_does_not_fit(lib):
+    # A's 8208-byte rows (an odd multiple of 16 bytes) on 224-wide pair tiles:
+    # hgemm copies A into 128-byte rows for speed. 8192 x 4160 x 2 bytes do not
+    # fit the fixed scratch, so the no-alloc call reads A in place instead of
+    # refusing the shape (the copy is not needed for correctness)
+    M, N, K = 8192, 4096, 4104
+    cfg = hg.Config(cta_group=2, block_n=224)
+    assert hg.plan(M, N, K, "bf16", cfg)["repack_a"] == 1
+    A = inputs.generate((M, K), "bf16", 38, 0)
+    B = inputs.generate((K, N), "bf16", 38, 1)
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    hg.hgemm_noalloc(A.cuda(), B.cuda(), C, M, N, K, "bf16", config=cfg)
+    torch.cuda.synchronize()
+    got = inputs.bits(C.cpu())
+    rows = np.unique(np.concatenate([np.random.default_rng(5).integers(0, M, 24), [0, 255, 256, M - 1]]))
+    ref, ref64 = oracle.gemm_rows(inputs.bits(A), inputs.bits(B), "bf16", rows)
+    r = compare(got[rows], ref, ref64, "bf16", K)
+    assert r["ok"], r
+    st, info = hg.get_device_status(0)
+    assert st == 0, (st, info)
 
 
 @pytest.mark.parametrize("mode", [2, 3, 4])
