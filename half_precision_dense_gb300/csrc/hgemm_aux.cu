@@ -13,7 +13,8 @@ __device__ unsigned long long g_status_word;
 // alignment) into rows `dst_pitch` bytes apart (dst and dst_pitch multiples
 // of 16), for up to two matrices in one launch (a RepackJob each). One warp
 // per row; lane l writes the row's 16-byte segments l,
-// l + 32, ..., kRepackBatch of them per pass. A segment's bytes start at
+// l + 32, ..., kRepackBatch of them per pass (8: 64 registers of data, four
+// 256-thread blocks per SM; 16 was 2-3 us slower on every copied shape tried). A segment's bytes start at
 // offset `off` inside an aligned 16-byte source block and run into the next
 // block: every source block is read once, with an aligned 16-byte load, by
 // the lane whose segment starts in it, and the next block comes from the
@@ -26,7 +27,7 @@ __device__ unsigned long long g_status_word;
 // that loaded both blocks itself: 1000 x 4095 x 4104 bf16 (B copied) 57.0 ->
 // 50.5 us end to end; L2 eviction hints (source evict-first, copy
 // evict-last) changed nothing.
-constexpr int kRepackBatch = 16;
+constexpr int kRepackBatch = 8;
 
 __device__ __forceinline__ uint4 load_block(const uint8_t* b, const uint8_t* end) {
     return b < end ? __ldg(reinterpret_cast<const uint4*>(b)) : make_uint4(0u, 0u, 0u, 0u);
