@@ -524,14 +524,20 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dt, cons
     // loop (at most 8 blocks) leaves the epilogue setting the pace, and there
     // TMA stores are faster: 4096x4096x64 19.1 -> 16.6 us, 8192x8192x256
     // 53.2 -> 46.7, 16384x16384x64 156 -> 105. At K = 1024 the two modes
-    // tie (4096x4096x1024: 30.8 us each).
+    // tie (4096x4096x1024: 30.8 us each). So is a single wave of tiles,
+    // whose last epilogue nothing overlaps: 2048^3 22.9 -> 21.2 us,
+    // 2048x2048x1024 15.2 -> 14.9 (3072^3, 1.3 waves: a tie).
     const int64_t num_kb_plan = cdiv(K, bk_of(dt));
+    const bool one_wave = static_cast<int64_t>(pl->num_tiles) * cluster_ctas(*pl) <= pl->grid_ctas;
     // A C whose rows are not 16-byte aligned: 16-bit C takes realigned
     // 16-byte stores with element stores at the ragged ends (5); fp32 C (tf32)
     // plain element stores (2). Measured against element stores: 1000 x 4095
     // x 4104 53.2 against 55.4 us, 3000 x 1001 x 2048 32.8 against 34.6.
     const bool c16 = c_esize_of(dt) == 2;
-    pl->store_mode = (c.store_mode != 0) ? c.store_mode : c_unaligned ? (c16 ? 5 : 2) : num_kb_plan <= 8 ? 1 : 4;
+    pl->store_mode = (c.store_mode != 0)   ? c.store_mode
+                     : c_unaligned           ? (c16 ? 5 : 2)
+                     : (num_kb_plan <= 8 || one_wave) ? 1
+                                                      : 4;
     if (pl->store_mode == 5 && !c16) {
         t_last_error = "store_mode 5 is for 16-bit C";
         return HGEMM_ERR_INVALID_ARG;
