@@ -490,8 +490,12 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     // The split's reduction: 16-bit C, whole 64-column chunks, column slices
     // of at least eight 16-byte units, every CTA's slice received in the ring.
     static_assert(!kSplit || (kDt <= 1 && !Cfg::kHalfLast && BN / MC >= 32 &&
-                              kBlockMCta * BN * 4 <= S * Cfg::kStageBytes),
+                              kBlockMCta * BN * 4 + kEpiWarps * 8192 <= S * Cfg::kStageBytes),
                   "K split shapes");
+    // K split: the blocks of partial sums received from the cluster (MC of
+    // them, 128 rows x BN / MC fp32 each) fill the ring from its start; each
+    // epilogue warp's 8 KB staging area for the chunk it sends follows.
+    constexpr uint32_t kSplitStageOffset = static_cast<uint32_t>(kBlockMCta * BN * 4);
     static_assert(!kSplit || (2 * S + 7) * 8 + 8 + 8 * kEpiWarps + 24 <= Cfg::kBarBytes, "barrier area");
     static_assert(S >= 2, "the two producers take alternate stages");
 
@@ -891,8 +895,13 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         if (q != crank) mbar_arrive_cluster(mapa_shared(bar_rok, q));
                 }
                 // 2. Once every peer's ring is free, send each owner its columns.
+                if (warp == 0 && lane == 0) {
+                    trace_chunk(p, it, 12, kTcStart);
+                    trace_chunk(p, it, 0, kTcStart);
+                }
                 bool ok = wait_bar_cluster_warp(bar_rok, 0, w, kRoleEpilogue, 96);
-                const uint32_t r = static_cast<uint32_t>(quarter * 32) + lane;    // tile row
+                if (warp == 0 && lane == 0) trace_chunk(p, it, 0, kTcLdDone);
+                if (lane == 0) trace_chunk(p, it, 1 + warp, kTcLdDone);
                 for (int c = colhalf; c < Cfg::kChunks && ok; c += 2) {
                     uint32_t r0[32], r1[32];
                     tmem_ld_32x32b_x32(t_row + 64u * c, r0);
@@ -900,6 +909,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     tmem_ld_wait();
                     reg_fence(r0);
                     reg_fence(r1);
+                    if (lane == 0) trace_chunk(p, it, 1 + warp, kTcPacked);
                     if (kb_hi == kb_lo) {
                         // no K block in this CTA's share: its partial sum is zero
 #pragma unroll
@@ -908,23 +918,58 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                             r1[i] = 0u;
                         }
                     }
+                    // Stage the chunk in this warp's own 32 x 256-byte area, a
+                    // row per lane (16-byte unit j of row l at j ^ (l % 8):
+                    // each 8-lane phase covers the 32 banks once), then read it
+                    // back row-contiguously: every cluster store then writes a
+                    // whole 128- or 256-byte row slice of the owner's block, not
+                    // 32 scattered 16-byte pieces (measured: 2700 cycles per
+                    // warp for a chunk's stores the scattered way).
+                    const uint32_t stage = sA + kSplitStageOffset + static_cast<uint32_t>(warp) * 8192u;
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        const uint32_t col = 64u * static_cast<uint32_t>(c) + 4u * static_cast<uint32_t>(j);
-                        const uint32_t owner_cta = col / kSliceCols;
-                        const uint32_t u = (col % kSliceCols) / 4u;
-                        const uint32_t off = crank * kBlockBytes + r * kRowBytes + ((u ^ (r & 7u)) << 4);
                         const uint32_t* v = j < 8 ? r0 + 4 * j : r1 + 4 * (j - 8);
-                        st_cluster_v4(mapa_shared(sA + off, owner_cta), __uint_as_float(v[0]), __uint_as_float(v[1]),
-                                      __uint_as_float(v[2]), __uint_as_float(v[3]));
+                        st_shared_v4(stage + lane * 256u + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4), v[0], v[1],
+                                     v[2], v[3]);
                     }
+                    __syncwarp();
+                    // units of the chunk per owner row: 16 (the chunk lies in
+                    // one owner's slice) or 8 (it spans two 32-column slices)
+                    constexpr uint32_t kU = kSliceCols >= 64u ? 16u : kSliceCols / 4u;
+                    constexpr uint32_t kRowsPerStore = 32u / kU;
+                    const uint32_t uu = lane % kU;                       // unit within the owner's part
+                    const uint32_t rsub = lane / kU;                     // row within the store
+#pragma unroll
+                    for (uint32_t part = 0; part < 16u / kU; ++part) {
+                        const uint32_t col = 64u * static_cast<uint32_t>(c) + 4u * (part * kU);  // first column of the part
+                        const uint32_t owner_cta = col / kSliceCols;
+                        const uint32_t u_slice = (col % kSliceCols) / 4u + uu;   // unit within the slice row
+                        const uint32_t u_chunk = part * kU + uu;                // unit within the chunk
+                        const uint32_t dst_base = owner_cta == crank ? sA : mapa_shared(sA, owner_cta);
+#pragma unroll 4
+                        for (uint32_t i = 0; i < 32u / kRowsPerStore; ++i) {
+                            const uint32_t rl = i * kRowsPerStore + rsub;                 // row in the warp's 32
+                            const float4 q4 = ld_shared_f4(stage + rl * 256u + ((u_chunk ^ (rl & 7u)) << 4));
+                            const uint32_t rt = static_cast<uint32_t>(quarter * 32) + rl;  // row in the tile
+                            const uint32_t off = crank * kBlockBytes + rt * kRowBytes + ((u_slice ^ (rt & 7u)) << 4);
+                            if (owner_cta == crank)
+                                st_shared_v4(dst_base + off, __float_as_uint(q4.x), __float_as_uint(q4.y),
+                                             __float_as_uint(q4.z), __float_as_uint(q4.w));
+                            else
+                                st_cluster_v4(dst_base + off, q4.x, q4.y, q4.z, q4.w);
+                        }
+                    }
+                    __syncwarp();
                 }
                 tc_fence_before();
                 __syncwarp();
+                if (warp == 0 && lane == 0) trace_chunk(p, it, 0, kTcWaitRead);
+                if (lane == 0) trace_chunk(p, it, 1 + warp, kTcWaitRead);
                 if (lane == 0) {
                     release_accumulator<CG>(bar_tempty + 8 * acc, leader);
                     // 3. This warp's parts are sent (release at cluster scope).
                     if (ok) mbar_arrive_cluster(mapa_shared(bar_sent, crank));
+                    trace_chunk(p, it, 1 + warp, kTcStaged);
                 }
                 // Warp 0 collects the eight warps' arrivals (a bounded wait: a
                 // warp that gave up never arrives) and publishes the CTA's parts
@@ -938,11 +983,13 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                             mbar_arrive_cluster(mapa_shared(bar_rdy, q));
                     }
                     ok = ok && sent;
+                    if (lane == 0) trace_chunk(p, it, 0, kTcStaged);
                 }
                 // 4. Every CTA's block of this CTA's columns is in: sum the
                 //    blocks in rank order (the same order on every run), round,
                 //    store.
                 ok = wait_bar_cluster_warp(bar_rdy, 0, w, kRoleEpilogue, 97) && ok;
+                if (warp == 0 && lane == 0) trace_chunk(p, it, 0, kTcIssued);
                 if (ok) {
                     const int32_t row_base = tm * kBlockMCta;
                     const int32_t col_base = col0 + static_cast<int32_t>(crank * kSliceCols);
@@ -981,7 +1028,10 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         }
                     }
                 }
-                if (warp == 0 && lane == 0) trace_stamp(p, it, kTrEpiEnd);
+                if (warp == 0 && lane == 0) {
+                    trace_chunk(p, it, 0, kTcStored);
+                    trace_stamp(p, it, kTrEpiEnd);
+                }
                 continue;
             }
             const bool is_split = wu.kind != 0;
