@@ -416,21 +416,24 @@ void choose_shape(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dt, int sms, in
 }
 
 // The planner's K split: clusters of `s` single CTAs on 128-wide tiles when
-// the K loop is long (at least 128 blocks, 32 per CTA) and the tiles, s CTAs
+// the K loop is long (at least 64 blocks, 16 per CTA) and the tiles, s CTAs
 // each, still fit on the SMs; the widest such s of 4 and 2. Measured on GB300
-// (bf16, L2 flushed, against the planner's whole tiles): 128 x 4096 x 14336
-// 57.1 -> 40.7 us (split 4), 128 x 2048 x 8192 35.8 -> 25.9 (4), 1024 x 1024
-// x 8192 34.4 -> 29.2 (2), 128 x 8192 x 8192 45.1 -> 41.4 (2), 16 and 64 x
-// 8192 x 8192 -10 % (2); at K = 4096 a tie (128 x 4096 x 4096: 23.0 -> 22.5),
-// at K = 2048 a loss (128 x 8192 x 2048: 18.1 -> 20.4). 256-wide split tiles
-// measured slower than 128-wide ones on every shape tried.
+// (bf16, L2 flushed, interleaved, against the planner's whole tiles):
+// 128 x 4096 x 14336 57.1 -> 40.7 us (split 4), 128 x 2048 x 8192 35.8 ->
+// 25.9 (4), 1024 x 1024 x 8192 34.4 -> 29.2 (2), 128 x 8192 x 8192 45.1 ->
+// 41.4 (2), 16 and 64 x 8192 x 8192 -10 % (2). Once the split's exchange
+// sent whole row slices, K = 4096 gained too: 128 x 4096 x 4096 23.0 ->
+// 20.7 (4), 256 x 4096 x 4096 23.1 -> 20.8 (2), 512 x 2048 x 4096 23.1 ->
+// 20.9 (2), 1024 x 1024 x 4096 23.1 -> 21.0 (2), 64 x 8192 x 4096 24.1 ->
+// 23.3 (2); K = 2048 still loses (128 x 8192 x 2048: 16.8 -> 18.6). 256-wide
+// split tiles measured slower than 128-wide ones on every shape tried.
 int auto_split(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dt, int sms) {
     if (esize_of(dt) != 2) return 1;
     const int64_t num_kb = cdiv(K, bk_of(dt));
-    if (num_kb < 128) return 1;
+    if (num_kb < 64) return 1;
     const int64_t tiles = cdiv(M, 128) * cdiv(N, 128);
     for (int s : {4, 2})
-        if (tiles * s <= sms && num_kb / s >= 32) return s;
+        if (tiles * s <= sms && num_kb / s >= 16) return s;
     return 1;
 }
 

@@ -182,9 +182,11 @@ def test_plan_stream_k(lib):
     # split over a cluster of two (the planner never picks stream-K)
     sk = binding.plan(128, 8192, 8192, "bf16", sm_count=152)
     assert (sk["cta_group"], sk["block_n"], sk["sk_tiles"], sk["grid_ctas"], sk["split_k"]) == (1, 128, 0, 128, 2)
-    # a shorter K loop: the narrowest one-CTA tiles that keep every tile in
-    # one wave, whole
+    # 64 K blocks: still split (32 per CTA); a shorter K loop: the narrowest
+    # one-CTA tiles that keep every tile in one wave, whole
     sk = binding.plan(128, 8192, 4096, "bf16", sm_count=152)
+    assert (sk["cta_group"], sk["block_n"], sk["sk_tiles"], sk["grid_ctas"], sk["split_k"]) == (1, 128, 0, 128, 2)
+    sk = binding.plan(128, 8192, 2048, "bf16", sm_count=152)
     assert (sk["cta_group"], sk["block_n"], sk["sk_tiles"], sk["grid_ctas"], sk["split_k"]) == (1, 64, 0, 128, 1)
     wide = binding.plan(128, 16384, 8192, "bf16", sm_count=152)
     assert (wide["cta_group"], wide["block_n"], wide["sk_tiles"]) == (1, 128, 0)
@@ -288,7 +290,9 @@ def test_plan_split_k_clusters(lib):
     ((128, 4096, 14336), "bf16", 4),    # 32 tiles x 4 CTAs, 56 K blocks each
     ((128, 2048, 8192), "f16", 4),
     ((1024, 1024, 8192), "bf16", 2),    # 64 tiles: a split of 4 would need 256 SMs
-    ((128, 8192, 4096), "bf16", 1),     # 64 K blocks: too short a loop to split
+    ((128, 8192, 4096), "bf16", 2),     # 64 K blocks, 32 per CTA
+    ((128, 4096, 4096), "bf16", 4),     # 32 tiles x 4 CTAs, 16 K blocks each
+    ((128, 8192, 2048), "bf16", 1),     # 32 K blocks: too short a loop to split
     ((8192, 8192, 8192), "bf16", 1),    # enough tiles already
     ((128, 4096, 14336), "tf32", 1),    # 16-bit kinds only
     ((128, 4096, 14336), "e4m3", 1),
