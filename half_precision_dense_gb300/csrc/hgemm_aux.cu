@@ -11,10 +11,11 @@ __device__ unsigned long long g_status_word;
 
 // Copy `rows` rows of `row_bytes` bytes (row r at src + r row_bytes: any
 // alignment) into rows `dst_pitch` bytes apart (dst and dst_pitch multiples
-// of 16), for up to two matrices in one launch (a RepackJob each). One warp
-// per row; lane l writes the row's 16-byte segments l,
-// l + 32, ..., kRepackBatch of them per pass (8: 64 registers of data, four
-// 256-thread blocks per SM; 16 was 2-3 us slower on every copied shape tried). A segment's bytes start at
+// of 16), for up to two matrices in one launch (a RepackJob each). A warp
+// copies one pass of a row at a time: lane l writes the pass's 16-byte
+// segments l, l + 32, ..., kRepackBatch of them (8: 64 registers of data,
+// three 256-thread blocks per SM; 16 was 2-3 us slower on every copied shape
+// tried). A segment's bytes start at
 // offset `off` inside an aligned 16-byte source block and run into the next
 // block: every source block is read once, with an aligned 16-byte load, by
 // the lane whose segment starts in it, and the next block comes from the
@@ -28,6 +29,7 @@ __device__ unsigned long long g_status_word;
 // 50.5 us end to end; L2 eviction hints (source evict-first, copy
 // evict-last) changed nothing.
 constexpr int kRepackBatch = 8;
+constexpr int kRepackBlocksPerSm = 3;   // 256-thread blocks resident per SM (register bound)
 
 __device__ __forceinline__ uint4 load_block(const uint8_t* b, const uint8_t* end) {
     return b < end ? __ldg(reinterpret_cast<const uint4*>(b)) : make_uint4(0u, 0u, 0u, 0u);
@@ -43,47 +45,55 @@ __device__ __forceinline__ uint4 shfl_u4(const uint4& v, int src) {
                       __shfl_sync(0xffffffffu, v.z, src), __shfl_sync(0xffffffffu, v.w, src));
 }
 
-__global__ void __launch_bounds__(256) repack_rows_kernel(RepackJob a, RepackJob b) {
+// Work unit: one pass (32 x kRepackBatch segments, 4 KB) of one row; the
+// units of job a's rows, then job b's, are spread over the warps in turn, so
+// a launch ends at most one short unit after its last full round.
+__global__ void __launch_bounds__(256, kRepackBlocksPerSm) repack_rows_kernel(RepackJob a, RepackJob b) {
     // the GEMM that reads the copies may start its set-up now
     grid_launch_dependents();
     const uint32_t lane = threadIdx.x & 31u;
     const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    // rows of job a, then rows of job b (warp-uniform choice)
-    for (int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; i < a.rows + b.rows;
-         i += nw) {
-        const RepackJob& j = i < a.rows ? a : b;
-        const int64_t r = i < a.rows ? i : i - a.rows;
+    constexpr int64_t kPassSegs = 32 * kRepackBatch;
+    const int64_t passes_a = (a.row_bytes + 16 * kPassSegs - 1) / (16 * kPassSegs);
+    const int64_t passes_b = (b.row_bytes + 16 * kPassSegs - 1) / (16 * kPassSegs);
+    const int64_t units_a = a.rows * passes_a;
+    const int64_t units = units_a + b.rows * passes_b;
+    for (int64_t u = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; u < units; u += nw) {
+        const bool in_a = u < units_a;                      // warp-uniform
+        const RepackJob& j = in_a ? a : b;
+        const int64_t passes = in_a ? passes_a : passes_b;
+        const int64_t ui = in_a ? u : u - units_a;
+        const int64_t r = ui / passes;
+        const int64_t t0 = (ui - r * passes) * kPassSegs;
         const uint8_t* const end = j.src + j.rows * j.row_bytes;
         const int64_t nseg = (j.row_bytes + 15) / 16;
         const uint8_t* const row = j.src + r * j.row_bytes;
         const uint32_t off = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(row) & 15u);
         const uint8_t* const base = row - off;
         uint8_t* const d = j.dst + r * j.dst_pitch;
-        for (int64_t t0 = 0; t0 < nseg; t0 += 32 * kRepackBatch) {
-            uint4 v[kRepackBatch];
+        uint4 v[kRepackBatch];
+#pragma unroll
+        for (int q = 0; q < kRepackBatch; ++q) {
+            const int64_t t = t0 + 32 * q + lane;
+            v[q] = t <= nseg ? load_block(base + 16 * t, end) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        const int64_t tx = t0 + kPassSegs;
+        const uint4 x = (lane == 31u && off != 0u && tx <= nseg) ? load_block(base + 16 * tx, end)
+                                                                  : make_uint4(0u, 0u, 0u, 0u);
+        if (off == 0u) {
 #pragma unroll
             for (int q = 0; q < kRepackBatch; ++q) {
                 const int64_t t = t0 + 32 * q + lane;
-                v[q] = t <= nseg ? load_block(base + 16 * t, end) : make_uint4(0u, 0u, 0u, 0u);
+                if (t < nseg) *reinterpret_cast<uint4*>(d + 16 * t) = v[q];
             }
-            const int64_t tx = t0 + 32 * kRepackBatch;
-            const uint4 x = (lane == 31u && off != 0u && tx <= nseg) ? load_block(base + 16 * tx, end)
-                                                                      : make_uint4(0u, 0u, 0u, 0u);
-            if (off == 0u) {
+        } else {
 #pragma unroll
-                for (int q = 0; q < kRepackBatch; ++q) {
-                    const int64_t t = t0 + 32 * q + lane;
-                    if (t < nseg) *reinterpret_cast<uint4*>(d + 16 * t) = v[q];
-                }
-            } else {
-#pragma unroll
-                for (int q = 0; q < kRepackBatch; ++q) {
-                    uint4 hi = shfl_down_u4(v[q], 1);
-                    const uint4 nx = shfl_u4(v[q + 1 < kRepackBatch ? q + 1 : q], 0);
-                    if (lane == 31u) hi = q + 1 < kRepackBatch ? nx : x;
-                    const int64_t t = t0 + 32 * q + lane;
-                    if (t < nseg) *reinterpret_cast<uint4*>(d + 16 * t) = bytes_from(v[q], hi, off);
-                }
+            for (int q = 0; q < kRepackBatch; ++q) {
+                uint4 hi = shfl_down_u4(v[q], 1);
+                const uint4 nx = shfl_u4(v[q + 1 < kRepackBatch ? q + 1 : q], 0);
+                if (lane == 31u) hi = q + 1 < kRepackBatch ? nx : x;
+                const int64_t t = t0 + 32 * q + lane;
+                if (t < nseg) *reinterpret_cast<uint4*>(d + 16 * t) = bytes_from(v[q], hi, off);
             }
         }
     }
@@ -221,14 +231,21 @@ __global__ void zero_kernel(uint16_t* __restrict__ dst, int64_t count) {
 }
 
 cudaError_t launch_repack(const RepackJob& a, const RepackJob& b, cudaStream_t stream) {
-    const int64_t rows = (a.rows > 0 ? a.rows : 0) + (b.rows > 0 ? b.rows : 0);
-    if (rows == 0) return cudaSuccess;
-    // one warp per row, up to 64 rows per SM at once
-    int64_t blocks = (rows + 7) / 8;
-    if (blocks > 152 * 8) blocks = 152 * 8;
     RepackJob ja = a, jb = b;
     if (ja.rows < 0) ja.rows = 0;
     if (jb.rows < 0) jb.rows = 0;
+    constexpr int64_t kPassBytes = 16 * 32 * kRepackBatch;
+    const int64_t units = ja.rows * ((ja.row_bytes + kPassBytes - 1) / kPassBytes) +
+                          jb.rows * ((jb.row_bytes + kPassBytes - 1) / kPassBytes);
+    if (units == 0) return cudaSuccess;
+    // one unit per warp at a time, on the blocks that fit at once
+    int sms = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms <= 0)
+        sms = 152;
+    int64_t blocks = (units + 7) / 8;
+    const int64_t resident = static_cast<int64_t>(sms) * kRepackBlocksPerSm;
+    if (blocks > resident) blocks = resident;
     repack_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(ja, jb);
     return cudaGetLastError();
 }
