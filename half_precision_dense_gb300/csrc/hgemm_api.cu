@@ -212,7 +212,9 @@ constexpr double kPairFixedSec = 1.0e-6;
 // Epilogue time of a tile: a fixed part (the accumulator hand-over, the
 // first TMEM load) plus a part per 64-column chunk that each epilogue warp
 // converts and stores (a CTA's 8 warps take its chunks two at a time); a CTA
-// pair hands tensor memory back across the pair, 1.6 times as long. A tile
+// pair hands tensor memory back across the pair, 1.75 times as long (1.6
+// picked pair tiles for 8192 x 8192 x 64: 36.1 us against 32.3 for 1 x 256,
+// interleaved; 4096 x 4096 x 64 and x 128 kept 1 x 256 either way). A tile
 // takes at least this long even when its K loop is short: the epilogue of
 // one tile overlaps the mainloop of the next, so the slower of the two sets
 // the pace. Fitted on GB300 to K = 64 shapes with TMA stores of C (the
@@ -224,7 +226,7 @@ constexpr double kEpiChunkSec = 0.8e-6;
 double tile_seconds(int cg, int bn, int64_t num_kb) {
     const double mainloop = 2.0 * 128 * bn * (num_kb * hg::kBlockK) / (kSmFlops * shape_efficiency(cg, bn));
     const int chunks_per_warp = ((bn / cg + 63) / 64 + 1) / 2;
-    const double epilogue = (kEpiTileSec + kEpiChunkSec * chunks_per_warp) * (cg == 2 ? 1.6 : 1.0);
+    const double epilogue = (kEpiTileSec + kEpiChunkSec * chunks_per_warp) * (cg == 2 ? 1.75 : 1.0);
     return mainloop > epilogue ? mainloop : epilogue;
 }
 
