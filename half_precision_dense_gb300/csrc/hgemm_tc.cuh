@@ -547,7 +547,9 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         for (int e = 0; e < kEpiWarps; ++e) mbar_init(bar_part + 8 * e, 1);
         if constexpr (kSplit) {
             mbar_init(bar_rok, MC - 1);
-            mbar_init(bar_rdy, MC);
+            // 128-wide tiles: the peers' parts arrive by bulk copies counted
+            // in bytes on bar_rdy, armed once by this CTA
+            mbar_init(bar_rdy, Cfg::kChunks == 2 ? 1 : MC);
             mbar_init(bar_sent, kEpiWarps);
         }
         *abort_flag = 0;
@@ -890,6 +892,9 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 // 1. This CTA's MMAs have completed (tmem_full): its ring may
                 //    be written by the peers. Test hook: rank 0 never says so,
                 //    and its peers' waits run out.
+                constexpr bool kBulkExchange = Cfg::kChunks == 2;   // one chunk per warp
+                if (kBulkExchange && warp == 0 && lane == 0)
+                    mbar_arrive_expect_tx(bar_rdy, static_cast<uint32_t>(MC - 1) * kBlockBytes);
                 if (warp == 0 && lane == 0 && !(p.inject == 2 && crank == 0)) {
                     for (uint32_t q = 0; q < static_cast<uint32_t>(MC); ++q)
                         if (q != crank) mbar_arrive_cluster(mapa_shared(bar_rok, q));
@@ -902,6 +907,72 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 bool ok = wait_bar_cluster_warp(bar_rok, 0, w, kRoleEpilogue, 96);
                 if (warp == 0 && lane == 0) trace_chunk(p, it, 0, kTcLdDone);
                 if (lane == 0) trace_chunk(p, it, 1 + warp, kTcLdDone);
+                if constexpr (kBulkExchange) {
+                    // 128-wide tiles: each warp holds one 64-column chunk, one
+                    // or two owners' whole slice rows (32 rows each). Its own
+                    // columns go straight into its own block; a peer's part is
+                    // laid out in the staging area exactly as the owner's
+                    // block holds it (row r at r * row bytes, unit u at
+                    // u ^ (r % 8)), then moved by one bulk copy, which counts
+                    // its bytes on the owner's bar_rdy.
+                    const int c = colhalf;
+                    uint32_t r0[32], r1[32];
+                    tmem_ld_32x32b_x32(t_row + 64u * c, r0);
+                    tmem_ld_32x32b_x32(t_row + 64u * c + 32u, r1);
+                    tmem_ld_wait();
+                    reg_fence(r0);
+                    reg_fence(r1);
+                    if (kb_hi == kb_lo) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            r0[i] = 0u;
+                            r1[i] = 0u;
+                        }
+                    }
+                    if (lane == 0) trace_chunk(p, it, 1 + warp, kTcPacked);
+                    constexpr uint32_t kPartCols = kSliceCols >= 64u ? 64u : kSliceCols;
+                    constexpr uint32_t kPartUnits = kPartCols / 4u;
+                    constexpr uint32_t kPartBytes = 32u * kRowBytes;                // 32 rows of the owner's slice
+                    static_assert(kRowBytes == kPartCols * 4u, "a part is whole slice rows");
+                    const uint32_t stage = sA + kSplitStageOffset + static_cast<uint32_t>(warp) * 8192u;
+                    const uint32_t rows_off = static_cast<uint32_t>(quarter * 32) * kRowBytes;
+#pragma unroll
+                    for (uint32_t part = 0; part < 64u / kPartCols; ++part) {
+                        const uint32_t col = 64u * static_cast<uint32_t>(c) + part * kPartCols;
+                        const uint32_t owner_cta = col / kSliceCols;
+                        const bool own = owner_cta == crank;
+                        const uint32_t dst = own ? sA + crank * kBlockBytes + rows_off : stage + part * kPartBytes;
+#pragma unroll
+                        for (uint32_t j = 0; j < kPartUnits; ++j) {
+                            const uint32_t ju = part * kPartUnits + j;               // unit within the chunk
+                            const uint32_t* v = ju < 8 ? r0 + 4 * ju : r1 + 4 * (ju - 8);
+                            st_shared_v4(dst + lane * kRowBytes + ((j ^ (lane & 7u)) << 4), v[0], v[1], v[2], v[3]);
+                        }
+                        if (!own && ok) {
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0)
+                                bulk_copy_to_peer(mapa_shared(sA + crank * kBlockBytes + rows_off, owner_cta), dst,
+                                                  kPartBytes, mapa_shared(bar_rdy, owner_cta));
+                        }
+                        __syncwarp();
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        trace_chunk(p, it, 1 + warp, kTcWaitRead);
+                        if (warp == 0) trace_chunk(p, it, 0, kTcWaitRead);
+                        release_accumulator<CG>(bar_tempty + 8 * acc, leader);
+                        // 3. This warp's own columns are in its own block.
+                        mbar_arrive_local(bar_sent);
+                        trace_chunk(p, it, 1 + warp, kTcStaged);
+                    }
+                    // 4. Every warp's own columns, and every peer's bytes.
+                    ok = wait_bar(bar_sent, 0, w, kRoleEpilogue, 98) && ok;
+                    if (warp == 0 && lane == 0) trace_chunk(p, it, 0, kTcStaged);
+                    ok = wait_bar(bar_rdy, 0, w, kRoleEpilogue, 97) && ok;
+                    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                } else {
                 for (int c = colhalf; c < Cfg::kChunks && ok; c += 2) {
                     uint32_t r0[32], r1[32];
                     tmem_ld_32x32b_x32(t_row + 64u * c, r0);
@@ -989,6 +1060,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 //    blocks in rank order (the same order on every run), round,
                 //    store.
                 ok = wait_bar_cluster_warp(bar_rdy, 0, w, kRoleEpilogue, 97) && ok;
+                }   // per-thread cluster stores (256-wide tiles)
                 if (warp == 0 && lane == 0) trace_chunk(p, it, 0, kTcIssued);
                 if (ok) {
                     const int32_t row_base = tm * kBlockMCta;

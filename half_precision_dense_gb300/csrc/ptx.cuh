@@ -65,6 +65,12 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  :: "r"(bar), "r"(bytes) : "memory");
 }
 
+// Arrive once on this CTA's barrier (release at CTA scope: this thread's
+// earlier shared-memory writes are visible to the threads its phase frees).
+__device__ __forceinline__ void mbar_arrive_local(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+
 // Arrive once on a barrier given by its shared::cluster address (own or peer CTA).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
@@ -201,6 +207,17 @@ __device__ __forceinline__ void bulk_wait_group() {
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  :: "r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar) : "memory");
+}
+
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
+// from this CTA's shared memory to shared memory of a CTA of the cluster
+// (`dst_cluster`, a shared::cluster address); the bytes are signalled on that
+// CTA's barrier `bar_cluster`. The source must stay unchanged until the
+// receiver has seen them.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
+                                                  uint32_t bar_cluster) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(dst_cluster), "r"(src), "r"(bytes), "r"(bar_cluster) : "memory");
 }
 
 // 4-byte asynchronous copy global -> this CTA's shared memory (cp.async;
