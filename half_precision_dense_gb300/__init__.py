@@ -8,7 +8,7 @@ arguments to it. Importing this package loads nothing; the binding loads the
 library on first use and raises if it is missing.
 """
 
-__version__ = "0.1.0"
+__version__ = "0.2.0"
 
 _BINDING_NAMES = {
     "hgemm", "hgemm_ex", "hgemm_fp8", "hgemm_conv2d", "conv2d_nhwc", "hgemm_noalloc", "hgemm_host", "matmul", "status_string", "version",

@@ -37,7 +37,8 @@ class _Config(ctypes.Structure):
     _fields_ = [("cta_group", ctypes.c_int32), ("block_n", ctypes.c_int32),
                 ("group_m", ctypes.c_int32), ("max_clusters", ctypes.c_int32),
                 ("store_mode", ctypes.c_int32), ("stream_k", ctypes.c_int32),
-                ("multicast", ctypes.c_int32), ("split_k", ctypes.c_int32)]
+                ("multicast", ctypes.c_int32), ("split_k", ctypes.c_int32),
+                ("epi_warps", ctypes.c_int32)]
 
 
 class _Plan(ctypes.Structure):
@@ -45,7 +46,7 @@ class _Plan(ctypes.Structure):
         "cta_group", "block_m", "block_n", "block_k", "stages", "group_m", "tiles_m", "tiles_n",
         "num_tiles", "grid_ctas", "smem_bytes", "tmem_cols", "repack_a", "repack_b", "store_mode",
         "dp_tiles", "sk_tiles", "sk_blocks", "sk_extra", "num_kb", "multicast", "split_k")] + \
-        [("workspace_bytes", ctypes.c_int64)]
+        [("workspace_bytes", ctypes.c_int64), ("epi_warps", ctypes.c_int32)]
 
 
 @dataclass
@@ -59,10 +60,11 @@ class Config:
     stream_k: int = 0
     multicast: int = 0
     split_k: int = 0
+    epi_warps: int = 0
 
     def _c(self) -> _Config:
         return _Config(self.cta_group, self.block_n, self.group_m, self.max_clusters, self.store_mode,
-                       self.stream_k, self.multicast, self.split_k)
+                       self.stream_k, self.multicast, self.split_k, self.epi_warps)
 
 
 def library_path() -> str:

@@ -220,13 +220,31 @@ constexpr double kPairFixedSec = 1.0e-6;
 // the pace. Fitted on GB300 to K = 64 shapes with TMA stores of C (the
 // planner's store path for short K loops), per tile and wave: 1x64 1.08 us,
 // 1x128 1.18-1.23, 1x256 1.8-2.0, pair 256 1.83-1.98.
+// With 16 epilogue warps (32-column chunks, four warps per lane quarter) a
+// CTA's warps take its 32-column chunks four at a time, each costing half a
+// 64-column chunk, and a pair's hand-over no longer shows: fitted to 16-warp
+// tiles on GB300 (interleaved, TMA stores), 8192 x 8192 x 256 pair 256 35.3
+// us against 1 x 256 39.1, 4096 x 4096 x 64 1 x 256 13.7 against pair 256
+// 14.8, 2048 x 2048 x 1024 1 x 256 14.8 against pair 256 15.4.
 constexpr double kEpiTileSec = 0.35e-6;
 constexpr double kEpiChunkSec = 0.8e-6;
 
-double tile_seconds(int cg, int bn, int64_t num_kb) {
+// The tiles that take 16 epilogue warps: 16-bit C on single 256-wide or
+// pair 224- and 256-wide tiles (whole tiles, no K split).
+bool epi16_tile(int cg, int bn, hgemm_dtype_t dt) {
+    return esize_of(dt) == 2 && ((cg == 1 && bn == 256) || (cg == 2 && (bn == 224 || bn == 256)));
+}
+
+double tile_seconds(int cg, int bn, int64_t num_kb, int ew) {
     const double mainloop = 2.0 * 128 * bn * (num_kb * hg::kBlockK) / (kSmFlops * shape_efficiency(cg, bn));
-    const int chunks_per_warp = ((bn / cg + 63) / 64 + 1) / 2;
-    const double epilogue = (kEpiTileSec + kEpiChunkSec * chunks_per_warp) * (cg == 2 ? 1.75 : 1.0);
+    double epilogue;
+    if (ew == 16) {
+        const int chunks32_per_warp = (bn / 32 + 3) / 4;
+        epilogue = kEpiTileSec + kEpiChunkSec * 0.5 * chunks32_per_warp;
+    } else {
+        const int chunks_per_warp = ((bn / cg + 63) / 64 + 1) / 2;
+        epilogue = (kEpiTileSec + kEpiChunkSec * chunks_per_warp) * (cg == 2 ? 1.75 : 1.0);
+    }
     return mainloop > epilogue ? mainloop : epilogue;
 }
 
@@ -246,8 +264,8 @@ int64_t stream_k_tiles(int64_t tiles, int64_t clusters, int mode) {
 // (each cluster's equal share of K blocks, plus the owners' fix-up: reading
 // the partners' partial sums after the last unit).
 double schedule_seconds(int cg, int bn, int64_t tiles, int64_t clusters, int64_t num_kb,
-                        int64_t sk_tiles) {
-    const double tile_sec = tile_seconds(cg, bn, num_kb);
+                        int64_t sk_tiles, int ew) {
+    const double tile_sec = tile_seconds(cg, bn, num_kb, sk_tiles > 0 ? 8 : ew);
     const int64_t dp = tiles - sk_tiles;
     double t = static_cast<double>((dp + clusters - 1) / clusters) * tile_sec;
     if (sk_tiles > 0) {
@@ -376,7 +394,7 @@ double estimate_seconds(int64_t M, int64_t N, int64_t K, int cg, int bn, int64_t
     pl.split_k = 1;
     pl.num_tiles = static_cast<int32_t>(tiles);
     schedule_plan(&pl, clusters, 0, kb);
-    return schedule_seconds(cg, bn, tiles, pl.grid_ctas / cg, kb, pl.sk_tiles);
+    return schedule_seconds(cg, bn, tiles, pl.grid_ctas / cg, kb, pl.sk_tiles, epi16_tile(cg, bn, dt) ? 16 : 8);
 }
 
 void choose_shape(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dt, int sms, int max_clusters, int* cg_out,
@@ -551,6 +569,17 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dt, cons
         t_last_error = "vector and TMA stores need a 16-byte aligned C with a 16-byte row pitch";
         return HGEMM_ERR_INVALID_ARG;
     }
+    // Epilogue warps. A short K loop on single 256-wide tiles leaves the
+    // epilogue setting the pace, and each warp's chain of TMEM load,
+    // conversion, staging and store is latency-bound: 16 warps on 32-column
+    // chunks keep twice the chunks in flight.
+    const bool epi16_ok = epi16_tile(cg, bn, dt) && split == 1 && pl->sk_tiles == 0;
+    if (c.epi_warps != 0 && c.epi_warps != 8 && !(c.epi_warps == 16 && epi16_ok)) {
+        t_last_error = "epi_warps: 0, 8, or 16 with cta_group 1, block_n 256, a 16-bit dtype, no K split and "
+                       "no stream-K";
+        return HGEMM_ERR_INVALID_ARG;
+    }
+    pl->epi_warps = c.epi_warps != 0 ? c.epi_warps : epi16_ok ? 16 : 8;
     pl->workspace_bytes = workspace_layout(*pl, M, N, K, esize_of(dt)).total;
     return HGEMM_OK;
 }
@@ -635,10 +664,11 @@ hgemm_status_t check_args(const void* A, const void* B, void* C, int64_t M, int6
 // device (0 if the query fails).
 int resident_clusters(hgemm_dtype_t dtype, const hgemm_plan_t& q) {
     const int qm = q.split_k > 1 ? q.split_k : 1;
-    return dtype == HGEMM_BF16   ? hg::max_active_clusters_bf16(q.cta_group, q.block_n, qm)
-           : dtype == HGEMM_TF32 ? hg::max_active_clusters_tf32(q.cta_group, q.block_n, qm)
-           : is_fp8(dtype)       ? hg::max_active_clusters_fp8(static_cast<int>(dtype), q.cta_group, q.block_n, qm)
-                                 : hg::max_active_clusters_f16(q.cta_group, q.block_n, qm);
+    const int ew = q.epi_warps == 16 ? 16 : 8;
+    return dtype == HGEMM_BF16   ? hg::max_active_clusters_bf16(q.cta_group, q.block_n, qm, ew)
+           : dtype == HGEMM_TF32 ? hg::max_active_clusters_tf32(q.cta_group, q.block_n, qm, ew)
+           : is_fp8(dtype)       ? hg::max_active_clusters_fp8(static_cast<int>(dtype), q.cta_group, q.block_n, qm, ew)
+                                 : hg::max_active_clusters_f16(q.cta_group, q.block_n, qm, ew);
 }
 
 // The planner's K split needs one resident cluster per tile. Where fewer
@@ -745,6 +775,14 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
         }
         schedule_plan(&pl, resident, cfg ? cfg->stream_k : 0, num_kb);
         pl.workspace_bytes = workspace_layout(pl, M, N, K, es).total;
+        if (pl.epi_warps == 16 && pl.sk_tiles > 0) {
+            // stream-K units take the 8-warp epilogue
+            if (cfg && cfg->epi_warps == 16) {
+                t_last_error = "epi_warps 16 needs whole tiles, and stream-K remains on the resident clusters";
+                return HGEMM_ERR_INVALID_ARG;
+            }
+            pl.epi_warps = 8;
+        }
     }
     const int clusters = pl.grid_ctas / (cg * mc);
 
@@ -825,9 +863,9 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
         (pl.store_mode == 1 && !bs_block &&
          (st = encode_2d(&tc, c_dtype_of(dtype), C, M, N, N, static_cast<uint32_t>(128 / ces), hg::kEpiBoxRows)) !=
              HGEMM_OK) ||
-        // the 32-column last chunk of a 16-bit C (fp32 C leaves in 32-column
-        // boxes throughout, through tc)
-        (pl.store_mode == 1 && !bs_block && bn % 64 != 0 && ces == 2 &&
+        // the 32-column last chunk of a 16-bit C, or every chunk with 16
+        // epilogue warps (fp32 C leaves in 32-column boxes throughout, through tc)
+        (pl.store_mode == 1 && !bs_block && (bn % 64 != 0 || pl.epi_warps == 16) && ces == 2 &&
          (st = encode_2d(&tc32, c_dtype_of(dtype), C, M, N, N, 32, hg::kEpiBoxRows, CU_TENSOR_MAP_SWIZZLE_64B)) !=
              HGEMM_OK)) {
         if (work && work != scratch) cudaFreeAsync(work, stream);
@@ -948,11 +986,12 @@ hgemm_status_t run(const void* A, const void* B, void* C, int64_t M, int64_t N, 
         return cuda_fail(e, "status word");
     }
 
-    e = dtype == HGEMM_BF16   ? hg::launch_tc_bf16(cg, bn, mc, ta, tb, tc, tc32, tb2, p, clusters, stream)
-        : dtype == HGEMM_TF32 ? hg::launch_tc_tf32(cg, bn, mc, ta, tb, tc, tc32, tb2, p, clusters, stream)
-        : is_fp8(dtype)       ? hg::launch_tc_fp8(static_cast<int>(dtype), cg, bn, mc, ta, tb, tc, tc32, tb2, p, clusters,
-                                                  stream)
-                            : hg::launch_tc_f16(cg, bn, mc, ta, tb, tc, tc32, tb2, p, clusters, stream);
+    const int ew = pl.epi_warps == 16 ? 16 : 8;
+    e = dtype == HGEMM_BF16   ? hg::launch_tc_bf16(cg, bn, mc, ew, ta, tb, tc, tc32, tb2, p, clusters, stream)
+        : dtype == HGEMM_TF32 ? hg::launch_tc_tf32(cg, bn, mc, ew, ta, tb, tc, tc32, tb2, p, clusters, stream)
+        : is_fp8(dtype)       ? hg::launch_tc_fp8(static_cast<int>(dtype), cg, bn, mc, ew, ta, tb, tc, tc32, tb2, p,
+                                                  clusters, stream)
+                            : hg::launch_tc_f16(cg, bn, mc, ew, ta, tb, tc, tc32, tb2, p, clusters, stream);
     if (work && work != scratch) cudaFreeAsync(work, stream);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     return HGEMM_OK;
@@ -1357,6 +1396,6 @@ const char* hgemm_status_string(hgemm_status_t s) {
 
 const char* hgemm_last_error(void) { return t_last_error.c_str(); }
 
-int32_t hgemm_version(void) { return 100; }
+int32_t hgemm_version(void) { return 200; }
 
 }  // extern "C"

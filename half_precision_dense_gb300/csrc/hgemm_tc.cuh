@@ -21,6 +21,8 @@
 // Roles (352 threads, one CTA per SM):
 //   warps 0-7  epilogue: warp w reads TMEM lanes 32(w % 4)..+31 (C rows of the
 //              tile) and every other 64-column chunk, starting at chunk w / 4
+//              (a short-K variant has 16 epilogue warps on 32-column chunks;
+//              the other roles' warp numbers then move up by 8)
 //   warps 8,10 producers: each warp takes alternate stages (even / odd K
 //              blocks); one elected lane issues the TMA loads of A and B
 //   warp 9     MMA: allocates TMEM; in the leader CTA the warp runs the loop and
@@ -468,8 +470,8 @@ static __device__ __noinline__ void store_chunk_realigned(const uint8_t* box_ptr
 // MC SMs on each tile of a shape with too few tiles to fill the GPU (a skinny
 // M), each reading 1/MC of the tile's operands. Every operand copy lands in
 // the issuing CTA's own shared memory (no cluster multicast).
-template <int CG, int BN, int kDt, int MC>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int CG, int BN, int kDt, int MC, int kEW = kEpiWarps>
+__global__ void __launch_bounds__(32 * (kEW + 3), 1)
 hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC32,
                 const __grid_constant__ CUtensorMap tmB2,
@@ -498,6 +500,24 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     constexpr uint32_t kSplitStageOffset = static_cast<uint32_t>(kBlockMCta * BN * 4);
     static_assert(!kSplit || (2 * S + 7) * 8 + 8 + 8 * kEpiWarps + 24 <= Cfg::kBarBytes, "barrier area");
     static_assert(S >= 2, "the two producers take alternate stages");
+    // Epilogue warps: 8 (two per TMEM lane quarter, 64-column chunks), or 16
+    // (four per quarter, 32-column chunks) for short K loops on 224- and
+    // 256-wide tiles, where the epilogue sets the pace and each warp's chain of TMEM
+    // load, conversion, staging and store is latency-bound: twice the warps
+    // keep twice the chunks in flight. The producers and the MMA warp follow.
+    constexpr int EW = kEW;
+    static_assert(EW == 8 || (EW == 16 && MC == 1 && kDt <= 1 && BN % 32 == 0),
+                  "16 epilogue warps: 16-bit C, no K split");
+    constexpr int kProd = EW, kMma = EW + 1, kProd2 = EW + 2;
+    constexpr int kChunkCols = EW == 16 ? 32 : 64;           // columns of an epilogue chunk
+    constexpr int NCH = (BN + kChunkCols - 1) / kChunkCols;  // chunks per tile
+    constexpr int kColGroups = EW / 4;                       // warps per lane quarter
+    constexpr uint32_t kBoxBytes = static_cast<uint32_t>(kEpiBoxRows * kChunkCols * 2);
+    static_assert(EW * kBoxBytes == static_cast<uint32_t>(Cfg::kEpiBytes) || kSplit, "staging boxes");
+    // One partial-sum barrier per epilogue warp, for stream-K owners (8
+    // epilogue warps only: a 16-warp instance takes whole tiles).
+    constexpr int kPartBars = EW == 8 ? EW : 0;
+    static_assert((2 * S + 7) * 8 + 8 + 8 * kPartBars <= Cfg::kBarBytes, "barrier area");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
@@ -515,8 +535,8 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const uint32_t bar_pre = bar_drain + 8;                     // [2]
     uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(smem + (bar_pre + 16 - base));
     volatile uint32_t* const abort_flag = tmem_slot + 1;
-    const uint32_t bar_part = bar_pre + 24;                     // [kEpiWarps]
-    const uint32_t bar_rok = bar_part + 8 * kEpiWarps;          // K split: peers' rings free
+    const uint32_t bar_part = bar_pre + 24;                     // [kPartBars]
+    const uint32_t bar_rok = bar_part + 8 * kPartBars;          // K split: peers' rings free
     const uint32_t bar_rdy = bar_rok + 8;                       // K split: all CTAs' sums landed
     const uint32_t bar_sent = bar_rdy + 8;                      // K split: this CTA's warps sent
 
@@ -540,29 +560,29 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bar_tfull + 8 * a, 1);
-            mbar_init(bar_tempty + 8 * a, kEpiWarps * CG);
+            mbar_init(bar_tempty + 8 * a, EW * CG);
         }
         mbar_init(bar_drain, 1);
-        for (int a = 0; a < 2; ++a) mbar_init(bar_pre + 8 * a, kEpiWarps * CG);
-        for (int e = 0; e < kEpiWarps; ++e) mbar_init(bar_part + 8 * e, 1);
+        for (int a = 0; a < 2; ++a) mbar_init(bar_pre + 8 * a, EW * CG);
+        for (int e = 0; e < kPartBars; ++e) mbar_init(bar_part + 8 * e, 1);
         if constexpr (kSplit) {
             mbar_init(bar_rok, MC - 1);
             // 128-wide tiles: the peers' parts arrive by bulk copies counted
             // in bytes on bar_rdy, armed once by this CTA
             mbar_init(bar_rdy, Cfg::kChunks == 2 ? 1 : MC);
-            mbar_init(bar_sent, kEpiWarps);
+            mbar_init(bar_sent, EW);
         }
         *abort_flag = 0;
         fence_mbarrier_init_cluster();
     }
-    if (warp == kProducerWarp && lane == 0) {
+    if (warp == kProd && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
         if (Cfg::kBPartial) tma_prefetch_desc(&tmB2);
         if (p.store_mode == 1) tma_prefetch_desc(&tmC);
-        if (p.store_mode == 1 && Cfg::kHalfLast && kDt != 2) tma_prefetch_desc(&tmC32);  // 16-bit C only
+        if (p.store_mode == 1 && (Cfg::kHalfLast || EW == 16) && kDt != 2) tma_prefetch_desc(&tmC32);  // 16-bit C only
     }
-    if (warp == kMmaWarp) tmem_alloc<CG>(smem_addr(tmem_slot), Cfg::kTmemCols);
+    if (warp == kMma) tmem_alloc<CG>(smem_addr(tmem_slot), Cfg::kTmemCols);
     tc_fence_before();
     __syncthreads();
     if constexpr (kCluster > 1) cluster_sync();
@@ -574,7 +594,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const Waiter w{abort_flag, p.timeout_ns, p.status};
     if (threadIdx.x == 0) trace_stamp(p, 0, kTrSetup);
 
-    if (warp == kProducerWarp || warp == kProducerWarp2) {
+    if (warp == kProd || warp == kProd2) {
         // ------------------------------------------------------------ producer
         // Two producer warps take alternate K blocks of the CTA's sequence
         // (block g of the sequence goes to stage g mod S): one warp needs
@@ -584,7 +604,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         // the loop and one elected lane issues the copies: with warp-uniform
         // coordinates the copies issue faster than from a lone lane.
         {
-            const uint32_t pid = warp == kProducerWarp ? 0u : 1u;
+            const uint32_t pid = warp == kProd ? 0u : 1u;
             uint32_t stage = pid, phase = 0;
             uint32_t g = 0;
             bool ok = true;
@@ -666,7 +686,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 while (globaltimer_ns() - t0 < 50000ull) {}
             }
         }
-    } else if (warp == kMmaWarp) {
+    } else if (warp == kMma) {
         // ----------------------------------------------------------------- MMA
         // The leader CTA's MMA warp runs the loop as a whole warp and one
         // elected lane issues each stage's tcgen05.mma and commit: with
@@ -782,10 +802,12 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     } else {
         // ------------------------------------------------------------ epilogue
         // Warp w reads TMEM lane quarter w % 4 (rows 32(w % 4) .. +31 of the
-        // CTA's tile) and every other 64-column chunk, starting at chunk w / 4.
+        // CTA's tile) and every (EW / 4)-th chunk, starting at chunk w / 4:
+        // every other 64-column chunk with 8 warps, every fourth 32-column
+        // chunk with 16.
         const int quarter = warp & 3;
-        const int colhalf = warp >> 2;
-        const uint32_t box = sEpi + static_cast<uint32_t>(warp) * kEpiBoxBytes;
+        const int colhalf = warp >> 2;        // the warp's column group (0 .. kColGroups - 1)
+        const uint32_t box = sEpi + static_cast<uint32_t>(warp) * kBoxBytes;
         uint8_t* const box_ptr = smem + (box - base);
         // Stream-K owner unit `j` (the cluster's last): before its MMAs start,
         // put the partners' partial sums into its accumulator buffer (this
@@ -849,8 +871,10 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             }
         };
         auto preload_if_owner = [&](int j) {
-            WorkUnit ou;
-            if (next_unit(p.sched, cluster_id, j, ou) && ou.kind == 1) preload_owner(j, ou);
+            if constexpr (EW == 8) {   // stream-K: 8 epilogue warps only
+                WorkUnit ou;
+                if (next_unit(p.sched, cluster_id, j, ou) && ou.kind == 1) preload_owner(j, ou);
+            }
         };
         preload_if_owner(0);
         preload_if_owner(1);
@@ -1067,7 +1091,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     const int32_t col_base = col0 + static_cast<int32_t>(crank * kSliceCols);
 #pragma unroll 1
                     for (int f = warp * 32 + static_cast<int>(lane); f < kBlockMCta * kUnitsPerRow;
-                         f += kEpiWarps * 32) {
+                         f += EW * 32) {
                         const uint32_t rr = static_cast<uint32_t>(f / kUnitsPerRow);
                         const uint32_t u = static_cast<uint32_t>(f % kUnitsPerRow);
                         const uint32_t off = rr * kRowBytes + ((u ^ (rr & 7u)) << 4);
@@ -1106,9 +1130,9 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 }
                 continue;
             }
-            const bool is_split = wu.kind != 0;
+            const bool is_split = EW == 8 && wu.kind != 0;   // stream-K units: 8 epilogue warps only
             const bool owner = wu.kind != 2;
-            if (colhalf >= Cfg::kChunks) {
+            if (colhalf >= NCH) {
                 // No chunk for this warp (a 64-wide tile): release at once.
                 __syncwarp();
                 if (lane == 0) release_accumulator<CG>(bar_tempty + 8 * acc, leader);
@@ -1141,11 +1165,12 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             const uint32_t part_buf = sA + static_cast<uint32_t>(warp) * static_cast<uint32_t>(n_part) * 8192u;
             uint32_t part_phase = 0;
 #pragma unroll 1
-            for (int c = colhalf; c < Cfg::kChunks; c += 2) {
+            for (int c = colhalf; c < NCH; c += kColGroups) {
                 // A chunk is 64 columns (two 32-column TMEM loads), or 32 for the
-                // last chunk of a tile whose width is an odd multiple of 32.
-                const bool half = Cfg::kHalfLast && c == Cfg::kChunks - 1;
-                const bool last = c + 2 >= Cfg::kChunks;
+                // last chunk of a tile whose width is an odd multiple of 32, and
+                // for every chunk with 16 epilogue warps.
+                const bool half = EW == 16 || (Cfg::kHalfLast && c == NCH - 1);
+                const bool last = c + kColGroups >= NCH;
                 if (warp == 0 && lane == 0) trace_chunk(p, it, c, kTcStart);
                 if (bulk_adds && lane == 0) {
                     // chunk c of a partial block: float4s [16c * 32, 16(c + 1) * 32)
@@ -1160,8 +1185,8 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                                   bytes, bar_part + 8 * warp);
                 }
                 uint32_t r0[32], r1[32];
-                tmem_ld_32x32b_x32(t_row + 64u * c, r0);
-                if (!half) tmem_ld_32x32b_x32(t_row + 64u * c + 32u, r1);
+                tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(kChunkCols * c), r0);
+                if (!half) tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(kChunkCols * c) + 32u, r1);
                 tmem_ld_wait();
                 reg_fence(r0);
                 if (half) {
@@ -1355,7 +1380,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     pk[16 + i] = pack_rn<kDt>(r1[2 * i], r1[2 * i + 1]);
                 }
                 if (warp == 0 && lane == 0) trace_chunk(p, it, c, kTcPacked);
-                const int32_t ccol = col0 + 64 * c;
+                const int32_t ccol = col0 + kChunkCols * c;
                 if (p.store_mode == 3) {
                     // Direct 16-byte stores: thread `lane` writes its own row of the
                     // chunk (C is 16-byte aligned with a pitch of a multiple of 8
@@ -1479,7 +1504,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     // ------------------------------------------------------------ teardown
     __syncthreads();
     if constexpr (kCluster > 1) cluster_sync();
-    if (warp == kMmaWarp) {
+    if (warp == kMma) {
         tc_fence_after();
         tmem_dealloc<CG>(tmem_base, Cfg::kTmemCols);
     }

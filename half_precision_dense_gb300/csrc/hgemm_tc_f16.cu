@@ -3,14 +3,14 @@
 
 namespace hg {
 
-cudaError_t launch_tc_f16(int cta_group, int block_n, int mc, const CUtensorMap& a, const CUtensorMap& b,
+cudaError_t launch_tc_f16(int cta_group, int block_n, int mc, int epi, const CUtensorMap& a, const CUtensorMap& b,
                           const CUtensorMap& c, const CUtensorMap& c32, const CUtensorMap& b2, const TcParams& p, int clusters,
                           cudaStream_t stream) {
     HG_TC_DISPATCH(0, launch(a, b, c, c32, b2, p, clusters, stream))
     return cudaErrorInvalidValue;
 }
 
-int max_active_clusters_f16(int cta_group, int block_n, int mc) {
+int max_active_clusters_f16(int cta_group, int block_n, int mc, int epi) {
     HG_TC_DISPATCH(0, max_clusters())
     return 0;
 }

@@ -3,7 +3,7 @@
 
 namespace hg {
 
-cudaError_t launch_tc_fp8(int kind, int cta_group, int block_n, int mc, const CUtensorMap& a,
+cudaError_t launch_tc_fp8(int kind, int cta_group, int block_n, int mc, int epi, const CUtensorMap& a,
                           const CUtensorMap& b, const CUtensorMap& c, const CUtensorMap& c32, const CUtensorMap& b2,
                           const TcParams& p, int clusters, cudaStream_t stream) {
     if (kind == 3) {
@@ -14,7 +14,7 @@ cudaError_t launch_tc_fp8(int kind, int cta_group, int block_n, int mc, const CU
     return cudaErrorInvalidValue;
 }
 
-int max_active_clusters_fp8(int kind, int cta_group, int block_n, int mc) {
+int max_active_clusters_fp8(int kind, int cta_group, int block_n, int mc, int epi) {
     if (kind == 3) {
         HG_TC_DISPATCH_F8(3, max_clusters())
     } else if (kind == 4) {

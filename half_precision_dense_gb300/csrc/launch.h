@@ -12,34 +12,35 @@
 
 namespace hg {
 
-// Launch the tcgen05 kernel for (cta_group, block_n, mc) with `clusters` CTA
-// clusters (of cta_group * mc CTAs) on `stream`. Returns cudaErrorInvalidValue
-// for a combination that is not instantiated.
+// Launch the tcgen05 kernel for (cta_group, block_n, mc, epi) with `clusters`
+// CTA clusters (of cta_group * mc CTAs) on `stream`; `epi` is the number of
+// epilogue warps (8, or 16 for 16-bit C on single 256-wide tiles). Returns
+// cudaErrorInvalidValue for a combination that is not instantiated.
 // `c` stores 64-column chunks of C; `c32` the 32-column last chunk of tiles
 // whose width is an odd multiple of 32; `b2` loads the part-full last B
 // atom of a CTA (its box is that atom's used columns; unused otherwise).
-cudaError_t launch_tc_bf16(int cta_group, int block_n, int mc, const CUtensorMap& a, const CUtensorMap& b,
+cudaError_t launch_tc_bf16(int cta_group, int block_n, int mc, int epi, const CUtensorMap& a, const CUtensorMap& b,
                            const CUtensorMap& c, const CUtensorMap& c32, const CUtensorMap& b2, const TcParams& p,
                            int clusters, cudaStream_t stream);
-cudaError_t launch_tc_f16(int cta_group, int block_n, int mc, const CUtensorMap& a, const CUtensorMap& b,
+cudaError_t launch_tc_f16(int cta_group, int block_n, int mc, int epi, const CUtensorMap& a, const CUtensorMap& b,
                           const CUtensorMap& c, const CUtensorMap& c32, const CUtensorMap& b2, const TcParams& p,
                           int clusters, cudaStream_t stream);
 // tf32: fp32 A, B and C; (cta_group, block_n) in (1, 64|128|256), (2, 128|256); mc 1.
-cudaError_t launch_tc_tf32(int cta_group, int block_n, int mc, const CUtensorMap& a, const CUtensorMap& b,
+cudaError_t launch_tc_tf32(int cta_group, int block_n, int mc, int epi, const CUtensorMap& a, const CUtensorMap& b,
                            const CUtensorMap& c, const CUtensorMap& c32, const CUtensorMap& b2, const TcParams& p,
                            int clusters, cudaStream_t stream);
 
 // Most CTA clusters of the (cta_group, block_n) kernel that can be resident at
 // once on the current device (0 on error).
-int max_active_clusters_bf16(int cta_group, int block_n, int mc);
-int max_active_clusters_f16(int cta_group, int block_n, int mc);
-int max_active_clusters_tf32(int cta_group, int block_n, int mc);
+int max_active_clusters_bf16(int cta_group, int block_n, int mc, int epi);
+int max_active_clusters_f16(int cta_group, int block_n, int mc, int epi);
+int max_active_clusters_tf32(int cta_group, int block_n, int mc, int epi);
 // fp8: kind 3 = E4M3, 4 = E5M2 operands (B row-major, read MN-major), bf16 C;
 // the tf32 tile shapes.
-cudaError_t launch_tc_fp8(int kind, int cta_group, int block_n, int mc, const CUtensorMap& a,
+cudaError_t launch_tc_fp8(int kind, int cta_group, int block_n, int mc, int epi, const CUtensorMap& a,
                           const CUtensorMap& b, const CUtensorMap& c, const CUtensorMap& c32, const CUtensorMap& b2,
                           const TcParams& p, int clusters, cudaStream_t stream);
-int max_active_clusters_fp8(int kind, int cta_group, int block_n, int mc);
+int max_active_clusters_fp8(int kind, int cta_group, int block_n, int mc, int epi);
 
 // The block-scaled fp8 kernel (hgemm_fp8bs.cuh): kind 3 = E4M3, 4 = E5M2;
 // cta_group 1 (128 x 128 tiles) or 2 (256 x 128); gs = 32 or 64 (scale block).

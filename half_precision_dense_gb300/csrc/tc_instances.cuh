@@ -80,12 +80,12 @@ struct ClusterKernel {
     }
 };
 
-template <int CG, int BN, int kDt, int MC = 1>
+template <int CG, int BN, int kDt, int MC = 1, int EW = kEpiWarps>
 struct TcInstance {
     // The kernel's own configuration (its operand size sets the stage bytes
     // and the ring depth), so the launch reserves the shared memory it uses.
     using Cfg = TcCfg<CG, BN, elem_bytes(kDt), (CG == 1 && MC > 1) ? MC : 1>;
-    using K = ClusterKernel<&hgemm_tc_kernel<CG, BN, kDt, MC>, CG * MC, Cfg::kSmemBytes>;
+    using K = ClusterKernel<&hgemm_tc_kernel<CG, BN, kDt, MC, EW>, CG * MC, Cfg::kSmemBytes, 32 * (EW + 3)>;
 
     static cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                               const CUtensorMap& c32, const CUtensorMap& b2, const TcParams& p, int clusters,
@@ -96,33 +96,40 @@ struct TcInstance {
     static int max_clusters() { return K::max_clusters(); }
 };
 
-// Every tile shape of the 16-bit kinds (KDT 0 = fp16, 1 = bf16), and the K
-// split across 2, 4 or 8 single CTAs (mc with cta_group 1).
+// Every tile shape of the 16-bit kinds (KDT 0 = fp16, 1 = bf16), the K split
+// across 2, 4 or 8 single CTAs (mc with cta_group 1), and the single 256-wide
+// and pair 224- and 256-wide tiles with 16 epilogue warps (epi == 16).
 #define HG_TC_DISPATCH(KDT, CALL)                                                          \
-    if (mc == 1 && cta_group == 1 && block_n == 64) return TcInstance<1, 64, KDT>::CALL;   \
-    if (mc == 1 && cta_group == 1 && block_n == 128) return TcInstance<1, 128, KDT>::CALL; \
-    if (mc == 1 && cta_group == 1 && block_n == 256) return TcInstance<1, 256, KDT>::CALL; \
-    if (mc == 1 && cta_group == 2 && block_n == 128) return TcInstance<2, 128, KDT>::CALL; \
-    if (mc == 1 && cta_group == 2 && block_n == 224) return TcInstance<2, 224, KDT>::CALL; \
-    if (mc == 1 && cta_group == 2 && block_n == 256) return TcInstance<2, 256, KDT>::CALL; \
-    if (mc == 2 && cta_group == 1 && block_n == 128) return TcInstance<1, 128, KDT, 2>::CALL; \
-    if (mc == 4 && cta_group == 1 && block_n == 128) return TcInstance<1, 128, KDT, 4>::CALL; \
-    if (mc == 2 && cta_group == 1 && block_n == 256) return TcInstance<1, 256, KDT, 2>::CALL; \
-    if (mc == 4 && cta_group == 1 && block_n == 256) return TcInstance<1, 256, KDT, 4>::CALL; \
-    if (mc == 8 && cta_group == 1 && block_n == 256) return TcInstance<1, 256, KDT, 8>::CALL;
+    if (epi == 16 && mc == 1 && cta_group == 1 && block_n == 256)                          \
+        return TcInstance<1, 256, KDT, 1, 16>::CALL;                                       \
+    if (epi == 16 && mc == 1 && cta_group == 2 && block_n == 224)                          \
+        return TcInstance<2, 224, KDT, 1, 16>::CALL;                                       \
+    if (epi == 16 && mc == 1 && cta_group == 2 && block_n == 256)                          \
+        return TcInstance<2, 256, KDT, 1, 16>::CALL;                                       \
+    if (epi == 8 && mc == 1 && cta_group == 1 && block_n == 64) return TcInstance<1, 64, KDT>::CALL; \
+    if (epi == 8 && mc == 1 && cta_group == 1 && block_n == 128) return TcInstance<1, 128, KDT>::CALL; \
+    if (epi == 8 && mc == 1 && cta_group == 1 && block_n == 256) return TcInstance<1, 256, KDT>::CALL; \
+    if (epi == 8 && mc == 1 && cta_group == 2 && block_n == 128) return TcInstance<2, 128, KDT>::CALL; \
+    if (epi == 8 && mc == 1 && cta_group == 2 && block_n == 224) return TcInstance<2, 224, KDT>::CALL; \
+    if (epi == 8 && mc == 1 && cta_group == 2 && block_n == 256) return TcInstance<2, 256, KDT>::CALL; \
+    if (epi == 8 && mc == 2 && cta_group == 1 && block_n == 128) return TcInstance<1, 128, KDT, 2>::CALL; \
+    if (epi == 8 && mc == 4 && cta_group == 1 && block_n == 128) return TcInstance<1, 128, KDT, 4>::CALL; \
+    if (epi == 8 && mc == 2 && cta_group == 1 && block_n == 256) return TcInstance<1, 256, KDT, 2>::CALL; \
+    if (epi == 8 && mc == 4 && cta_group == 1 && block_n == 256) return TcInstance<1, 256, KDT, 4>::CALL; \
+    if (epi == 8 && mc == 8 && cta_group == 1 && block_n == 256) return TcInstance<1, 256, KDT, 8>::CALL;
 
 // The tf32 (KDT 2) and fp8 (KDT 3 = E4M3, 4 = E5M2) tile shapes: whole
-// 64-column chunks, no K split.
+// 64-column chunks, no K split, 8 epilogue warps.
 #define HG_TC_DISPATCH_K(KDT, CALL)                                                        \
-    if (mc == 1 && cta_group == 1 && block_n == 64) return TcInstance<1, 64, KDT>::CALL;   \
-    if (mc == 1 && cta_group == 1 && block_n == 128) return TcInstance<1, 128, KDT>::CALL; \
-    if (mc == 1 && cta_group == 1 && block_n == 256) return TcInstance<1, 256, KDT>::CALL; \
-    if (mc == 1 && cta_group == 2 && block_n == 128) return TcInstance<2, 128, KDT>::CALL; \
-    if (mc == 1 && cta_group == 2 && block_n == 256) return TcInstance<2, 256, KDT>::CALL;
+    if (epi == 8 && mc == 1 && cta_group == 1 && block_n == 64) return TcInstance<1, 64, KDT>::CALL;   \
+    if (epi == 8 && mc == 1 && cta_group == 1 && block_n == 128) return TcInstance<1, 128, KDT>::CALL; \
+    if (epi == 8 && mc == 1 && cta_group == 1 && block_n == 256) return TcInstance<1, 256, KDT>::CALL; \
+    if (epi == 8 && mc == 1 && cta_group == 2 && block_n == 128) return TcInstance<2, 128, KDT>::CALL; \
+    if (epi == 8 && mc == 1 && cta_group == 2 && block_n == 256) return TcInstance<2, 256, KDT>::CALL;
 // tf32 and fp8 also take the 224-wide pair tile.
 #define HG_TC_DISPATCH_F8(KDT, CALL)                                                      \
     HG_TC_DISPATCH_K(KDT, CALL)                                                            \
-    if (mc == 1 && cta_group == 2 && block_n == 224) return TcInstance<2, 224, KDT>::CALL;
+    if (epi == 8 && mc == 1 && cta_group == 2 && block_n == 224) return TcInstance<2, 224, KDT>::CALL;
 #define HG_TC_DISPATCH_TF32(CALL) HG_TC_DISPATCH_F8(2, CALL)
 
 }  // namespace hg

@@ -240,6 +240,13 @@ uint64_t hgemm_noalloc_scratch_bytes(void);
  *                  adds all of them, in rank order, for 1/s of the tile's
  *                  columns. Needs a cluster per tile (HGEMM_ERR_INVALID_ARG
  *                  otherwise).
+ *   epi_warps:     epilogue warps per CTA: 0 = planner's choice, 8 (each
+ *                  reads 64-column chunks of the accumulator), or 16 (32-column
+ *                  chunks, twice the chunks in flight; cta_group 1, block_n
+ *                  256, fp16 or bf16, no K split, no stream-K). The planner
+ *                  takes 16 for such tiles when the K loop has at most 8
+ *                  blocks, else 8. Any other value, or 16 outside those
+ *                  limits, is HGEMM_ERR_INVALID_ARG.
  */
 typedef struct {
     int32_t cta_group;
@@ -250,6 +257,7 @@ typedef struct {
     int32_t stream_k;
     int32_t multicast;
     int32_t split_k;
+    int32_t epi_warps;
 } hgemm_config_t;
 
 /* hgemm with an explicit configuration (cfg may be NULL = all zero). */
@@ -380,6 +388,7 @@ typedef struct {
                               fewer fit on the device, the launch takes half the split on the
                               same tiles, then whole tiles (see hgemm_plan) */
     int64_t workspace_bytes; /* stream-ordered workspace: repacked operands + fp32 partials */
+    int32_t epi_warps;     /* epilogue warps per CTA (8 or 16) */
 } hgemm_plan_t;
 
 /* Fill *out with the plan hgemm_ex would use (pointers are assumed 16-byte

@@ -48,7 +48,7 @@ def test_library_is_sm103a_only():
 
 
 def test_version_and_strings(lib):
-    assert binding.version() == 100
+    assert binding.version() == 200
     for s, frag in [(0, "OK"), (1, "INVALID_ARG"), (2, "UNSUPPORTED_DEVICE"), (5, "TIMEOUT")]:
         assert frag in binding.status_string(s)
 
@@ -329,7 +329,7 @@ def test_split_share_partitions_the_k_range(lib, n, parts):
 @pytest.mark.parametrize("shape,store_mode,tile", [
     ((4096, 4096, 64), 1, (1, 256)),      # one K block per tile: the epilogue sets the pace
     ((8192, 8192, 64), 1, (1, 256)),      # single CTAs beat pairs on short K loops
-    ((8192, 8192, 256), 1, (1, 256)),
+    ((8192, 8192, 256), 1, (2, 256)),     # 16-warp pair tiles
     ((16384, 16384, 64), 1, (1, 256)),
     ((8192, 8192, 512), 1, (2, 256)),
     ((4096, 4096, 512), 1, (2, 224)),     # 8 blocks: still TMA stores
@@ -342,6 +342,45 @@ def test_plan_short_k_uses_tma_stores(lib, shape, store_mode, tile):
     # an unaligned 16-bit C takes the realigned stores; a forced mode is kept
     assert binding.plan(shape[0], shape[1] + 1, shape[2], "bf16", sm_count=152)["store_mode"] == 5
     assert binding.plan(*shape, "bf16", binding.Config(store_mode=3), sm_count=152)["store_mode"] == 3
+
+
+@pytest.mark.parametrize("shape,dtype,epi", [
+    ((4096, 4096, 64), "bf16", 16),       # single 256-wide tiles, one K block
+    ((8192, 8192, 256), "f16", 16),
+    ((16384, 16384, 64), "bf16", 16),
+    ((8192, 8192, 512), "bf16", 16),      # pair tiles
+    ((4096, 4096, 4096), "bf16", 16),     # a long K loop
+    ((128, 8192, 8192), "bf16", 8),       # a K split
+    ((1024, 1024, 1024), "bf16", 8),      # 64-wide tiles
+    ((4096, 4096, 64), "tf32", 8),        # fp32 C
+    ((4096, 4096, 128), "fp8_e4m3", 8),
+])
+def test_plan_epilogue_warps(lib, shape, dtype, epi):
+    assert binding.plan(*shape, dtype, sm_count=152)["epi_warps"] == epi
+
+
+def test_plan_epilogue_warps_forced(lib):
+    one = binding.Config(cta_group=1, block_n=256)
+    assert binding.plan(4096, 4096, 4096, "bf16", binding.Config(cta_group=1, block_n=256, epi_warps=16),
+                        sm_count=152)["epi_warps"] == 16
+    assert binding.plan(4096, 4096, 64, "bf16", binding.Config(epi_warps=8), sm_count=152)["epi_warps"] == 8
+    assert binding.plan(4096, 4096, 64, "bf16", one, sm_count=152)["epi_warps"] == 16
+    assert binding.plan(4096, 4096, 64, "bf16", binding.Config(cta_group=2, block_n=224, epi_warps=16),
+                        sm_count=152)["epi_warps"] == 16
+    for bad in (binding.Config(cta_group=2, block_n=128, epi_warps=16),      # 128-wide pair tiles
+                binding.Config(cta_group=1, block_n=128, epi_warps=16),      # 128-wide tiles
+                binding.Config(cta_group=1, block_n=256, epi_warps=12),      # not 8 or 16
+                binding.Config(cta_group=1, block_n=256, stream_k=3, epi_warps=16)):
+        with pytest.raises(binding.HgemmError):
+            binding.plan(4096, 4096, 64, "bf16", bad, sm_count=152)
+    with pytest.raises(binding.HgemmError):
+        binding.plan(4096, 4096, 64, "tf32", binding.Config(cta_group=1, block_n=256, epi_warps=16), sm_count=152)
+    with pytest.raises(binding.HgemmError):
+        binding.plan(128, 8192, 8192, "bf16", binding.Config(cta_group=1, block_n=256, split_k=2, epi_warps=16),
+                     sm_count=152)
+    # stream-K leaves the planner's default at 8
+    assert binding.plan(4096, 4096, 64, "bf16", binding.Config(cta_group=1, block_n=256, stream_k=3),
+                        sm_count=152)["epi_warps"] == 8
 
 
 def test_plan_skinny_prefers_narrow_tiles(lib):

@@ -255,6 +255,48 @@ def test_store_modes_match(cfg, store_mode):
     check_full(A, B, "bf16", c)
 
 
+EPI16 = [(1, 256), (2, 224), (2, 256)]
+EPI16_IDS = ["cg1_n256", "cg2_n224", "cg2_n256"]
+
+
+@pytest.mark.parametrize("tile", EPI16, ids=EPI16_IDS)
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("store_mode", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("shape", [(700, 520, 64), (1000, 1800, 300), (4096, 4096, 64)])
+def test_sixteen_epilogue_warps(tile, dtype, store_mode, shape):
+    # 16 epilogue warps on 32-column chunks of 224- and 256-wide tiles, every
+    # store mode, ragged M and N, short and longer K loops, and the
+    # persistent loop (a cap on the clusters: several tiles per CTA, both
+    # accumulator buffers)
+    M, N, K = shape
+    A, B = operands(M, N, K, dtype, 60)
+    for mc in ((0, 3) if M * N < 4_000_000 else (0,)):
+        check_full(A, B, dtype, hg.Config(cta_group=tile[0], block_n=tile[1], max_clusters=mc,
+                                          store_mode=store_mode, epi_warps=16))
+
+
+@pytest.mark.parametrize("tile", EPI16, ids=EPI16_IDS)
+@pytest.mark.parametrize("N", [4095, 777])
+def test_sixteen_epilogue_warps_unaligned_c(tile, N):
+    # a C pitch that is not a multiple of 16 bytes: realigned stores (5)
+    A, B = operands(300, N, 128, "bf16", 61)
+    check_full(A, B, "bf16", hg.Config(cta_group=tile[0], block_n=tile[1], epi_warps=16))
+
+
+def test_sixteen_epilogue_warps_bit_exact_and_planner_default():
+    # small integers: every product and sum is exact, so 16 and 8 warps,
+    # and the planner's own choice, agree bit for bit with the oracle
+    M, N, K = 1536, 2304, 192
+    A, B = int_operands(M, N, K, "bf16", 62)
+    assert hg.plan(M, N, K, "bf16")["epi_warps"] == 16
+    outs = [check_full(A, B, "bf16", cfg)[0] for cfg in
+            (None, hg.Config(cta_group=1, block_n=256, epi_warps=8),
+             hg.Config(cta_group=1, block_n=256, epi_warps=16, max_clusters=5))]
+    ref = oracle.round_rne(oracle.gemm_f64(inputs.bits(A), inputs.bits(B), "bf16"), "bf16")
+    for o in outs:
+        assert np.array_equal(o, ref)
+
+
 @pytest.mark.parametrize("store_mode", [1, 3, 4])
 def test_store_modes_with_stream_k(store_mode):
     c = hg.Config(2, 224, 0, 3, store_mode, 3)
