@@ -48,7 +48,7 @@ UNIT = "TFLOP/s"
 L2_FLUSH_BYTES = 256 << 20
 # Bumped whenever the code of the kernel instance a traffic record describes, or its default launch (store
 # path), changes, so ncu figures taken on an older kernel are not reported as current.
-KERNEL_REV = 14
+KERNEL_REV = 15
 
 # name -> list of (M, N, K, dtype, dist, sigma, seed) GEMMs making up one step
 WORKLOADS = {
@@ -509,7 +509,8 @@ def run_ours(args, rank, world, local_rank):
     plan_key = [plan["cta_group"], plan["block_n"], plan["sk_tiles"], plan["grid_ctas"]]
     line["roofline"]["plan"] = {"cta_group": plan_key[0], "block_n": plan_key[1],
                                 "stream_k_tiles": plan_key[2], "grid_ctas": plan_key[3],
-                                "split_k": plan["split_k"], "store_mode": plan["store_mode"]}
+                                "split_k": plan["split_k"], "store_mode": plan["store_mode"],
+                                "epi_warps": plan["epi_warps"]}
     if bs:
         # the block-scaled kernel plans its own tiles: 128 columns, a CTA pair
         # per 256-row tile unless there is a single 128-row tile row
