@@ -331,12 +331,6 @@ struct WorkspaceLayout {
     int64_t off_a, off_b, off_part, off_flags, total;
 };
 
-// Rows of `cols` elements padded to a 16-byte pitch.
-int64_t pitch16(int64_t cols, int esize) {
-    const int64_t per = 16 / esize;
-    return (cols + per - 1) / per * per;
-}
-
 // Rows of an operand copy: padded to 128 bytes, so that every row of a TMA
 // box starts on a 128-byte line. A pitch that is an odd multiple of 16 bytes
 // costs the GEMM's loads 10-20 % (1000 x 4096 x K bf16, A read in place:
