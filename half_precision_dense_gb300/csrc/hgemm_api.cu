@@ -229,10 +229,11 @@ constexpr double kPairFixedSec = 1.0e-6;
 constexpr double kEpiTileSec = 0.35e-6;
 constexpr double kEpiChunkSec = 0.8e-6;
 
-// The tiles that take 16 epilogue warps: 16-bit C on single 256-wide or
-// pair 224- and 256-wide tiles (whole tiles, no K split).
+// The tiles that take 16 epilogue warps: a 16-bit C (fp16, bf16, and the
+// bf16 C of fp8) on single 256-wide or pair 224- and 256-wide tiles (whole
+// tiles, no K split).
 bool epi16_tile(int cg, int bn, hgemm_dtype_t dt) {
-    return esize_of(dt) == 2 && ((cg == 1 && bn == 256) || (cg == 2 && (bn == 224 || bn == 256)));
+    return c_esize_of(dt) == 2 && ((cg == 1 && bn == 256) || (cg == 2 && (bn == 224 || bn == 256)));
 }
 
 double tile_seconds(int cg, int bn, int64_t num_kb, int ew) {
@@ -569,8 +570,8 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dt, cons
     // chunks keep twice the chunks in flight.
     const bool epi16_ok = epi16_tile(cg, bn, dt) && split == 1 && pl->sk_tiles == 0;
     if (c.epi_warps != 0 && c.epi_warps != 8 && !(c.epi_warps == 16 && epi16_ok)) {
-        t_last_error = "epi_warps: 0, 8, or 16 with cta_group 1, block_n 256, a 16-bit dtype, no K split and "
-                       "no stream-K";
+        t_last_error = "epi_warps: 0, 8, or 16 with a 16-bit C on single 256-wide or pair 224- and 256-wide "
+                       "tiles, no K split and no stream-K";
         return HGEMM_ERR_INVALID_ARG;
     }
     pl->epi_warps = c.epi_warps != 0 ? c.epi_warps : epi16_ok ? 16 : 8;

@@ -501,12 +501,13 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     static_assert(!kSplit || (2 * S + 7) * 8 + 8 + 8 * kEpiWarps + 24 <= Cfg::kBarBytes, "barrier area");
     static_assert(S >= 2, "the two producers take alternate stages");
     // Epilogue warps: 8 (two per TMEM lane quarter, 64-column chunks), or 16
-    // (four per quarter, 32-column chunks) for short K loops on 224- and
-    // 256-wide tiles, where the epilogue sets the pace and each warp's chain of TMEM
+    // (four per quarter, 32-column chunks) on 224- and 256-wide tiles of a
+    // 16-bit C (fp16, bf16, and the bf16 C of fp8), where the epilogue sets
+    // the pace of short K loops and of a last wave and each warp's chain of TMEM
     // load, conversion, staging and store is latency-bound: twice the warps
     // keep twice the chunks in flight. The producers and the MMA warp follow.
     constexpr int EW = kEW;
-    static_assert(EW == 8 || (EW == 16 && MC == 1 && kDt <= 1 && BN % 32 == 0),
+    static_assert(EW == 8 || (EW == 16 && MC == 1 && kDt != 2 && BN % 32 == 0),
                   "16 epilogue warps: 16-bit C, no K split");
     constexpr int kProd = EW, kMma = EW + 1, kProd2 = EW + 2;
     constexpr int kChunkCols = EW == 16 ? 32 : 64;           // columns of an epilogue chunk
@@ -1363,14 +1364,17 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     // per-channel scales applied in fp32 once the sum is done
                     const int32_t srow = row0 + static_cast<int32_t>(lane);
                     const float sa = (p.a_scale && srow < p.M) ? __ldg(p.a_scale + srow) : 1.0f;
-                    const int32_t scol = col0 + 64 * c;
+                    const int32_t scol = col0 + kChunkCols * c;
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const int32_t c0i = scol + i, c1i = scol + 32 + i;
+                        const int32_t c0i = scol + i;
                         const float sb0 = (p.b_scale && c0i < p.N) ? __ldg(p.b_scale + c0i) : 1.0f;
-                        const float sb1 = (p.b_scale && c1i < p.N) ? __ldg(p.b_scale + c1i) : 1.0f;
                         r0[i] = __float_as_uint(__uint_as_float(r0[i]) * (sa * sb0));
-                        r1[i] = __float_as_uint(__uint_as_float(r1[i]) * (sa * sb1));
+                        if (!half) {
+                            const int32_t c1i = scol + 32 + i;
+                            const float sb1 = (p.b_scale && c1i < p.N) ? __ldg(p.b_scale + c1i) : 1.0f;
+                            r1[i] = __float_as_uint(__uint_as_float(r1[i]) * (sa * sb1));
+                        }
                     }
                 }
                 uint32_t pk[32];

@@ -14,7 +14,7 @@ namespace hg {
 
 // Launch the tcgen05 kernel for (cta_group, block_n, mc, epi) with `clusters`
 // CTA clusters (of cta_group * mc CTAs) on `stream`; `epi` is the number of
-// epilogue warps (8, or 16 for 16-bit C on single 256-wide tiles). Returns
+// epilogue warps (8, or 16 for a 16-bit C on 224- and 256-wide tiles). Returns
 // cudaErrorInvalidValue for a combination that is not instantiated.
 // `c` stores 64-column chunks of C; `c32` the 32-column last chunk of tiles
 // whose width is an odd multiple of 32; `b2` loads the part-full last B

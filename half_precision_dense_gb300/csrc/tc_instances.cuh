@@ -118,8 +118,8 @@ struct TcInstance {
     if (epi == 8 && mc == 4 && cta_group == 1 && block_n == 256) return TcInstance<1, 256, KDT, 4>::CALL; \
     if (epi == 8 && mc == 8 && cta_group == 1 && block_n == 256) return TcInstance<1, 256, KDT, 8>::CALL;
 
-// The tf32 (KDT 2) and fp8 (KDT 3 = E4M3, 4 = E5M2) tile shapes: whole
-// 64-column chunks, no K split, 8 epilogue warps.
+// The tf32 (KDT 2) and fp8 (KDT 3 = E4M3, 4 = E5M2) tile shapes: no K split,
+// 8 epilogue warps (and 16 for fp8, below).
 #define HG_TC_DISPATCH_K(KDT, CALL)                                                        \
     if (epi == 8 && mc == 1 && cta_group == 1 && block_n == 64) return TcInstance<1, 64, KDT>::CALL;   \
     if (epi == 8 && mc == 1 && cta_group == 1 && block_n == 128) return TcInstance<1, 128, KDT>::CALL; \
@@ -127,9 +127,19 @@ struct TcInstance {
     if (epi == 8 && mc == 1 && cta_group == 2 && block_n == 128) return TcInstance<2, 128, KDT>::CALL; \
     if (epi == 8 && mc == 1 && cta_group == 2 && block_n == 256) return TcInstance<2, 256, KDT>::CALL;
 // tf32 and fp8 also take the 224-wide pair tile.
-#define HG_TC_DISPATCH_F8(KDT, CALL)                                                      \
+#define HG_TC_DISPATCH_W(KDT, CALL)                                                       \
     HG_TC_DISPATCH_K(KDT, CALL)                                                            \
     if (epi == 8 && mc == 1 && cta_group == 2 && block_n == 224) return TcInstance<2, 224, KDT>::CALL;
-#define HG_TC_DISPATCH_TF32(CALL) HG_TC_DISPATCH_F8(2, CALL)
+#define HG_TC_DISPATCH_TF32(CALL) HG_TC_DISPATCH_W(2, CALL)
+// fp8 writes a bf16 C: 16 epilogue warps on the single 256-wide and pair
+// 224- and 256-wide tiles, as for the 16-bit kinds.
+#define HG_TC_DISPATCH_F8(KDT, CALL)                                                      \
+    HG_TC_DISPATCH_W(KDT, CALL)                                                            \
+    if (epi == 16 && mc == 1 && cta_group == 1 && block_n == 256)                          \
+        return TcInstance<1, 256, KDT, 1, 16>::CALL;                                       \
+    if (epi == 16 && mc == 1 && cta_group == 2 && block_n == 224)                          \
+        return TcInstance<2, 224, KDT, 1, 16>::CALL;                                       \
+    if (epi == 16 && mc == 1 && cta_group == 2 && block_n == 256)                          \
+        return TcInstance<2, 256, KDT, 1, 16>::CALL;
 
 }  // namespace hg

@@ -242,10 +242,11 @@ uint64_t hgemm_noalloc_scratch_bytes(void);
  *                  otherwise).
  *   epi_warps:     epilogue warps per CTA: 0 = planner's choice, 8 (each
  *                  reads 64-column chunks of the accumulator), or 16 (32-column
- *                  chunks, twice the chunks in flight; cta_group 1, block_n
- *                  256, fp16 or bf16, no K split, no stream-K). The planner
- *                  takes 16 for such tiles when the K loop has at most 8
- *                  blocks, else 8. Any other value, or 16 outside those
+ *                  chunks, twice the chunks in flight; a 16-bit C, i.e. fp16,
+ *                  bf16 or fp8 with its bf16 C, on cta_group 1 with block_n
+ *                  256 or cta_group 2 with block_n 224 or 256; no K split, no
+ *                  stream-K). The planner takes 16 wherever those limits
+ *                  allow, else 8. Any other value, or 16 outside those
  *                  limits, is HGEMM_ERR_INVALID_ARG.
  */
 typedef struct {

@@ -353,7 +353,9 @@ def test_plan_short_k_uses_tma_stores(lib, shape, store_mode, tile):
     ((128, 8192, 8192), "bf16", 8),       # a K split
     ((1024, 1024, 1024), "bf16", 8),      # 64-wide tiles
     ((4096, 4096, 64), "tf32", 8),        # fp32 C
-    ((4096, 4096, 128), "fp8_e4m3", 8),
+    ((4096, 4096, 128), "fp8_e4m3", 16),  # fp8 writes a bf16 C
+    ((4096, 4096, 4096), "fp8_e5m2", 16),
+    ((128, 8192, 8192), "fp8_e4m3", 8),   # 64-wide tiles
 ])
 def test_plan_epilogue_warps(lib, shape, dtype, epi):
     assert binding.plan(*shape, dtype, sm_count=152)["epi_warps"] == epi
@@ -375,6 +377,8 @@ def test_plan_epilogue_warps_forced(lib):
             binding.plan(4096, 4096, 64, "bf16", bad, sm_count=152)
     with pytest.raises(binding.HgemmError):
         binding.plan(4096, 4096, 64, "tf32", binding.Config(cta_group=1, block_n=256, epi_warps=16), sm_count=152)
+    assert binding.plan(4096, 4096, 64, "fp8_e4m3", binding.Config(cta_group=2, block_n=224, epi_warps=16),
+                        sm_count=152)["epi_warps"] == 16
     with pytest.raises(binding.HgemmError):
         binding.plan(128, 8192, 8192, "bf16", binding.Config(cta_group=1, block_n=256, split_k=2, epi_warps=16),
                      sm_count=152)

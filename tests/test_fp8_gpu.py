@@ -129,6 +129,16 @@ def test_store_modes(store_mode, block_n):
     check(700, 1024, 512, "e4m3", 4, hg.Config(cta_group=2, block_n=block_n, store_mode=store_mode))
 
 
+@pytest.mark.parametrize("epi", [8, 16])
+@pytest.mark.parametrize("tile", [(1, 256), (2, 224), (2, 256)], ids=["cg1_n256", "cg2_n224", "cg2_n256"])
+@pytest.mark.parametrize("fmt", FMTS)
+def test_epilogue_warps(tile, epi, fmt):
+    # the wide tiles with 8 epilogue warps on 64-column chunks and 16 on
+    # 32-column chunks (the planner's default for them), ragged M and N, the
+    # persistent loop
+    check(1000, 520, 336, fmt, 10, hg.Config(cta_group=tile[0], block_n=tile[1], max_clusters=3, epi_warps=epi))
+
+
 @pytest.mark.parametrize("block_n", [224, 256])
 @pytest.mark.parametrize("mode,clusters", [(2, 3), (3, 5), (4, 7)])
 def test_stream_k(mode, clusters, block_n):

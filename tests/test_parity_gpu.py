@@ -276,6 +276,17 @@ def test_sixteen_epilogue_warps(tile, dtype, store_mode, shape):
 
 
 @pytest.mark.parametrize("tile", EPI16, ids=EPI16_IDS)
+@pytest.mark.parametrize("store_mode", [1, 2, 3, 4, 5])
+def test_eight_epilogue_warps_on_wide_tiles(tile, store_mode):
+    # the 8-warp epilogue (64-column chunks) that the planner no longer takes
+    # for these tiles, forced: every store mode, ragged M and N, the
+    # persistent loop
+    A, B = operands(700, 520, 300, "bf16", 63)
+    check_full(A, B, "bf16", hg.Config(cta_group=tile[0], block_n=tile[1], max_clusters=2, store_mode=store_mode,
+                                       epi_warps=8))
+
+
+@pytest.mark.parametrize("tile", EPI16, ids=EPI16_IDS)
 @pytest.mark.parametrize("N", [4095, 777])
 def test_sixteen_epilogue_warps_unaligned_c(tile, N):
     # a C pitch that is not a multiple of 16 bytes: realigned stores (5)
