@@ -126,7 +126,7 @@ enum : int { kTcLdDone = 0, kTcWaitRead = 1, kTcStaged = 2, kTcIssued = 3, kTcSt
              kTcStored = 6 };
 __device__ __forceinline__ void trace_chunk(const TcParams& p, int it, int c, int field) {
 #ifdef HG_TRACE
-    if (p.trace && it == 0 && c < 13)
+    if (p.trace && it == 0 && (c < 10 || c == 12))
         p.trace[(static_cast<int64_t>(blockIdx.x) * kTraceUnits + 16 + c) * kTraceFields + field] =
             static_cast<unsigned long long>(clock64());
 #else
@@ -161,6 +161,9 @@ __device__ __forceinline__ void trace_wait_total(const TcParams& p, int field, l
 // (0: partners' marks seen, 1: chunk loop done, 2: last store drained, 3+j:
 // warp 0's j-th chunk done), slot 29 = the first partner unit (0: epilogue
 // start, 1: partial sums published).
+// Launch-level stamps of a traced build (%globaltimer): kernel entry, all
+// roles done, teardown barrier passed, tensor memory freed.
+constexpr int kTrLaunchSlot = 26;
 __device__ __forceinline__ void trace_slot(const TcParams& p, int slot, int field) {
 #ifdef HG_TRACE
     if (p.trace)
@@ -521,6 +524,7 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     static_assert((2 * S + 7) * 8 + 8 + 8 * kPartBars <= Cfg::kBarBytes, "barrier area");
 
     extern __shared__ uint8_t smem_raw[];
+    if (threadIdx.x == 0) trace_slot(p, kTrLaunchSlot, 0);   // entry
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* const smem = smem_raw + (base - raw);
@@ -1506,11 +1510,14 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     }
 
     // ------------------------------------------------------------ teardown
+    if (threadIdx.x == 0) trace_slot(p, kTrLaunchSlot, 1);   // roles done
     __syncthreads();
     if constexpr (kCluster > 1) cluster_sync();
+    if (threadIdx.x == 0) trace_slot(p, kTrLaunchSlot, 2);   // teardown barrier passed
     if (warp == kMma) {
         tc_fence_after();
         tmem_dealloc<CG>(tmem_base, Cfg::kTmemCols);
+        if (lane == 0) trace_slot(p, kTrLaunchSlot, 3);      // tensor memory freed
     }
 #endif
 }
