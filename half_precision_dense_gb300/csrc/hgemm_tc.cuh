@@ -18,11 +18,12 @@
 //   grid swizzle (SWIZZLE_W)                 persistent CTAs walking a grouped raster
 //   Cs staging + SWIZZLE_C + float4 stores   tcgen05.ld -> cvt.rn -> swizzled smem -> row stores
 //
-// Roles (352 threads, one CTA per SM):
+// Roles (352 threads with 8 epilogue warps, 608 with 16; one CTA per SM):
 //   warps 0-7  epilogue: warp w reads TMEM lanes 32(w % 4)..+31 (C rows of the
 //              tile) and every other 64-column chunk, starting at chunk w / 4
-//              (a short-K variant has 16 epilogue warps on 32-column chunks;
-//              the other roles' warp numbers then move up by 8)
+//              (16 epilogue warps, for a 16-bit C on 224- and 256-wide tiles,
+//              take every fourth 32-column chunk; the other roles' warp
+//              numbers then move up by 8)
 //   warps 8,10 producers: each warp takes alternate stages (even / odd K
 //              blocks); one elected lane issues the TMA loads of A and B
 //   warp 9     MMA: allocates TMEM; in the leader CTA the warp runs the loop and
@@ -63,12 +64,9 @@ constexpr int kUmmaK = 16;        // K of one kind::f16 MMA
 // always 128 B of K.
 __host__ __device__ constexpr int elem_bytes(int dt) { return dt == 2 ? 4 : dt >= 3 ? 1 : 2; }
 __host__ __device__ constexpr int block_k(int dt) { return 128 / elem_bytes(dt); }
-constexpr int kEpiWarps = 8;      // two per TMEM lane quarter, splitting the columns
+constexpr int kEpiWarps = 8;      // default: two per TMEM lane quarter, splitting the columns
 constexpr int kEpiQuarters = 4;   // TMEM lane quarters (32 rows each)
-constexpr int kProducerWarp = 8;   // first producer: even K blocks of the CTA's sequence
-constexpr int kMmaWarp = 9;
-constexpr int kProducerWarp2 = 10; // second producer: odd K blocks
-constexpr int kThreads = 352;
+constexpr int kThreads = 32 * (kEpiWarps + 3);  // + two producers and the MMA warp
 constexpr int kEpiBoxRows = 32;   // one epilogue warp's rows
 constexpr int kEpiBoxCols = 64;   // 128 B of half-precision values
 constexpr int kEpiBoxBytes = kEpiBoxRows * kEpiBoxCols * 2;
