@@ -436,6 +436,57 @@ def test_epilogue_staging_layout_is_conflict_free_and_tma_compatible():
             assert addr == tma
 
 
+@pytest.mark.parametrize("ew,chunk_cols", [(8, 64), (16, 32)])
+@pytest.mark.parametrize("bn", [64, 128, 224, 256])
+def test_epilogue_chunks_cover_each_tile_column_once(ew, chunk_cols, bn):
+    """The epilogue's work split, as the kernel computes it: warp w takes TMEM
+    lane quarter w % 4 and chunks w // 4, w // 4 + ew // 4, ... of chunk_cols
+    columns (a 32-column last chunk when 64-column chunks do not divide the
+    tile). Every (quarter, column) of the tile is written by exactly one
+    warp, and each warp's last chunk is the one that hands the accumulator
+    back."""
+    if ew == 16 and bn < 224:
+        return  # 16 warps serve the 224- and 256-wide tiles only
+    nch = (bn + chunk_cols - 1) // chunk_cols
+    groups = ew // 4
+    owner = {}
+    for w in range(ew):
+        quarter, colhalf = w & 3, w >> 2
+        mine = list(range(colhalf, nch, groups))
+        for c in mine:
+            last = c + groups >= nch
+            assert last == (c == mine[-1])
+            half = chunk_cols == 32 or (bn % 64 != 0 and c == nch - 1)
+            width = 32 if half else 64
+            for col in range(chunk_cols * c, chunk_cols * c + width):
+                if col < bn:
+                    assert (quarter, col) not in owner
+                    owner[(quarter, col)] = w
+    assert len(owner) == 4 * bn
+
+
+def test_epilogue_32_column_box_is_conflict_free_and_tma_compatible():
+    """The 32-column staging box (16 epilogue warps, and the last chunk of a
+    224-wide tile): lane l owns row l (64 B); its 16-byte chunk j goes to
+    chunk j ^ ((l / 2) % 4). Each 8-lane phase of a 16-byte store covers all
+    32 banks once; the layout is the TMA 64-byte swizzle (chunk bits 4-5 of
+    the address XOR bits 7-8); and sixteen 2 KB boxes fill the same 32 KB as
+    eight 4 KB ones."""
+    for j in range(4):
+        for phase in range(4):
+            banks = []
+            for l in range(8 * phase, 8 * phase + 8):
+                addr = l * 64 + ((j ^ ((l >> 1) & 3)) << 4)
+                banks.extend(bank_of(addr + 4 * w) for w in range(4))
+            assert sorted(banks) == list(range(32))
+    for l in range(32):
+        for j in range(4):
+            addr = l * 64 + ((j ^ ((l >> 1) & 3)) << 4)
+            logical = l * 64 + j * 16
+            assert addr == logical ^ (((logical >> 7) & 3) << 4)
+    assert 16 * 32 * 32 * 2 == 8 * 32 * 64 * 2
+
+
 def test_plan_tf32(lib):
     # fp32 operands: 32 K values per 128-byte stage row, same tiles and ring
     p = binding.plan(4096, 4096, 4096, "tf32", sm_count=152)
