@@ -503,10 +503,10 @@ hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     static_assert(S >= 2, "the two producers take alternate stages");
     // Epilogue warps: 8 (two per TMEM lane quarter, 64-column chunks), or 16
     // (four per quarter, 32-column chunks) on 224- and 256-wide tiles of a
-    // 16-bit C (fp16, bf16, and the bf16 C of fp8), where the epilogue sets
-    // the pace of short K loops and of a last wave and each warp's chain of TMEM
-    // load, conversion, staging and store is latency-bound: twice the warps
-    // keep twice the chunks in flight. The producers and the MMA warp follow.
+    // 16-bit C (fp16, bf16, and the bf16 C of fp8). Each warp's chain of TMEM
+    // load, conversion, staging and store is latency-bound, and the epilogue
+    // sets the pace of short K loops and of a last wave: twice the warps keep
+    // twice the chunks in flight. The producers and the MMA warp follow.
     constexpr int EW = kEW;
     static_assert(EW == 8 || (EW == 16 && MC == 1 && kDt != 2 && BN % 32 == 0),
                   "16 epilogue warps: 16-bit C, no K split");
