@@ -575,6 +575,18 @@ hgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, hgemm_dtype_t dt, cons
         return HGEMM_ERR_INVALID_ARG;
     }
     pl->epi_warps = c.epi_warps != 0 ? c.epi_warps : epi16_ok ? 16 : 8;
+    const int mc = split > 1 ? split : 1;
+    const bool compiled =
+        dt == HGEMM_BF16   ? hg::tc_instance_exists_bf16(cg, bn, mc, pl->epi_warps)
+        : dt == HGEMM_F16  ? hg::tc_instance_exists_f16(cg, bn, mc, pl->epi_warps)
+        : dt == HGEMM_TF32 ? hg::tc_instance_exists_tf32(cg, bn, mc, pl->epi_warps)
+                           : hg::tc_instance_exists_fp8(static_cast<int>(dt), cg, bn, mc, pl->epi_warps);
+    if (!compiled) {
+        t_last_error = "no kernel is compiled for cta_group " + std::to_string(cg) + ", block_n " +
+                       std::to_string(bn) + ", split " + std::to_string(mc) + ", " +
+                       std::to_string(pl->epi_warps) + " epilogue warps";
+        return HGEMM_ERR_INVALID_ARG;
+    }
     pl->workspace_bytes = workspace_layout(*pl, M, N, K, esize_of(dt)).total;
     return HGEMM_OK;
 }

@@ -15,4 +15,9 @@ int max_active_clusters_bf16(int cta_group, int block_n, int mc, int epi) {
     return 0;
 }
 
+bool tc_instance_exists_bf16(int cta_group, int block_n, int mc, int epi) {
+    HG_TC_DISPATCH(1, exists())
+    return false;
+}
+
 }  // namespace hg

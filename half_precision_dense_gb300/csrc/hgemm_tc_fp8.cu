@@ -23,4 +23,13 @@ int max_active_clusters_fp8(int kind, int cta_group, int block_n, int mc, int ep
     return 0;
 }
 
+bool tc_instance_exists_fp8(int kind, int cta_group, int block_n, int mc, int epi) {
+    if (kind == 3) {
+        HG_TC_DISPATCH_F8(3, exists())
+    } else if (kind == 4) {
+        HG_TC_DISPATCH_F8(4, exists())
+    }
+    return false;
+}
+
 }  // namespace hg

@@ -42,6 +42,13 @@ cudaError_t launch_tc_fp8(int kind, int cta_group, int block_n, int mc, int epi,
                           const TcParams& p, int clusters, cudaStream_t stream);
 int max_active_clusters_fp8(int kind, int cta_group, int block_n, int mc, int epi);
 
+// Whether the kernel instance for (cta_group, block_n, mc, epi) is compiled
+// (host only, no device needed): the planner refuses a plan without one.
+bool tc_instance_exists_bf16(int cta_group, int block_n, int mc, int epi);
+bool tc_instance_exists_f16(int cta_group, int block_n, int mc, int epi);
+bool tc_instance_exists_tf32(int cta_group, int block_n, int mc, int epi);
+bool tc_instance_exists_fp8(int kind, int cta_group, int block_n, int mc, int epi);
+
 // The block-scaled fp8 kernel (hgemm_fp8bs.cuh): kind 3 = E4M3, 4 = E5M2;
 // cta_group 1 (128 x 128 tiles) or 2 (256 x 128); gs = 32 or 64 (scale block).
 // B is read in place (MN-major); `b2` loads a pair CTA's 64-column half atom.

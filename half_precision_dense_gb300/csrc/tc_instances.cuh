@@ -94,6 +94,7 @@ struct TcInstance {
     }
 
     static int max_clusters() { return K::max_clusters(); }
+    static bool exists() { return true; }   // host-only: the instance is compiled
 };
 
 // Every tile shape of the 16-bit kinds (KDT 0 = fp16, 1 = bf16), the K split

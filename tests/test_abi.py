@@ -387,6 +387,32 @@ def test_plan_epilogue_warps_forced(lib):
                         sm_count=152)["epi_warps"] == 8
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "tf32", "fp8_e4m3", "fp8_e5m2"])
+@pytest.mark.parametrize("sms", [152, 148, 132, 64])
+def test_every_planned_kernel_is_compiled(lib, dtype, sms):
+    """The planner refuses a configuration whose kernel instance is not
+    compiled; none of its own choices may be refused, over shapes from one
+    tile to the projection GEMMs (skinny, short K, ragged, long K)."""
+    dims = [1, 100, 128, 129, 1000, 2048, 4095, 4096, 8192, 16384]
+    ks = [1, 64, 100, 512, 4096, 4104, 14336]
+    for M in dims:
+        for N in dims[::2]:
+            for K in ks:
+                p = binding.plan(M, N, K, dtype, sm_count=sms)
+                assert p["epi_warps"] in (8, 16)
+
+
+def test_plan_refuses_a_kernel_that_is_not_compiled(lib):
+    # 16 epilogue warps exist for fp8's 224-wide pair tile but not for a
+    # 128-wide one; the K split exists for 128- and 256-wide single tiles only
+    binding.plan(4096, 4096, 4096, "fp8_e4m3", binding.Config(cta_group=2, block_n=224, epi_warps=16), sm_count=152)
+    with pytest.raises(binding.HgemmError):
+        binding.plan(4096, 4096, 4096, "fp8_e4m3", binding.Config(cta_group=2, block_n=128, epi_warps=16),
+                     sm_count=152)
+    with pytest.raises(binding.HgemmError):
+        binding.plan(128, 4096, 4096, "bf16", binding.Config(cta_group=1, block_n=64, split_k=2), sm_count=152)
+
+
 def test_plan_skinny_prefers_narrow_tiles(lib):
     p = binding.plan(128, 8192, 8192, "bf16", sm_count=148)
     assert p["block_m"] == 128  # one tile row: no half-empty CTA pairs
