@@ -200,7 +200,9 @@ uint64_t hgemm_noalloc_scratch_bytes(void);
 
 /*
  * Launch configuration, for tuning sweeps and tests. Zero in any field means
- * "let the planner choose".
+ * "let the planner choose". A configuration whose fields are each valid but
+ * whose combination has no compiled kernel is HGEMM_ERR_INVALID_ARG (from
+ * hgemm_plan as from the GEMM calls; hgemm_last_error names it).
  *   cta_group:     1 = one CTA per 128-row tile; 2 = a CTA pair (cluster of 2)
  *                  sharing a 256-row tile through tcgen05 cta_group::2.
  *   block_n:       columns of C per tile: 64, 128 or 256 with cta_group 1;
