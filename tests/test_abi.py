@@ -585,6 +585,73 @@ def _split_slot(q, r, col, bn, parts):
     return col // s, q * 128 * s * 4 + r * s * 4 + ((u ^ (r & 7)) << 4)
 
 
+def _realigned_store_model(half, o, nvalid, rows=32):
+    """The realigned stores of a staged chunk (store mode 5), as the kernel
+    issues them: one 16-byte box chunk g of row rr per piece, the aligned
+    16-byte segment that ends in it shifted into place from chunks g - 1 and
+    g, and element stores for a row's head and tail. Returns per row the
+    element writes {element: [values]} and the vector stores' byte offsets
+    from the row start (the row starts o bytes past a 16-byte boundary)."""
+    nseg = 4 if half else 8
+    nel = 8 * nseg
+    val = lambda rr, e: (rr << 8) | e
+    def box_bytes(rr):
+        sw = ((rr >> 1) & 3) if half else (rr & 7)
+        b = bytearray(64 if half else 128)
+        for e in range(nel):
+            a = (((e >> 3) ^ sw) << 4) + ((e & 7) << 1)
+            b[a:a + 2] = val(rr, e).to_bytes(2, "little")
+        return b, sw
+    writes = {rr: {} for rr in range(rows)}
+    vec = {rr: [] for rr in range(rows)}
+    for piece in range(32 * nseg):
+        rr, g = piece // nseg, piece % nseg
+        if rr >= rows:
+            continue
+        brow, sw = box_bytes(rr)
+        chunk = lambda j: bytes(brow[((j ^ sw) << 4):((j ^ sw) << 4) + 16])
+        elems = lambda sixteen: [int.from_bytes(sixteen[2 * i:2 * i + 2], "little") for i in range(8)]
+        def put(e0, sixteen):
+            vals = elems(sixteen)
+            if e0 + 8 <= nvalid:
+                vec[rr].append(o + 2 * e0)
+                for i in range(8):
+                    writes[rr].setdefault(e0 + i, []).append(vals[i])
+            else:
+                for e in range(e0, min(nvalid, e0 + 8)):
+                    writes[rr].setdefault(e, []).append(vals[e - e0])
+        if o == 0:
+            put(8 * g, chunk(g))
+            continue
+        half_o = o >> 1
+        if g > 0:
+            put(8 * g - half_o, (chunk(g - 1) + chunk(g))[16 - o:32 - o])
+        for k in range(g, 8, nseg):
+            e = k if k < 8 - half_o else nel - 8 + k
+            if e < nvalid:
+                ue = e
+                a = (((ue >> 3) ^ sw) << 4) + ((ue & 7) << 1)
+                writes[rr].setdefault(e, []).append(int.from_bytes(brow[a:a + 2], "little"))
+    return writes, vec, val, nel
+
+
+@pytest.mark.parametrize("half", [False, True])
+@pytest.mark.parametrize("o", [0, 2, 4, 6, 8, 10, 12, 14])
+def test_realigned_stores_write_each_element_once(half, o):
+    """Store mode 5 on the CPU: for every even misalignment of the row start
+    and every number of columns left in C, each element of the chunk inside C
+    is written exactly once with its own value, nothing past C's last column
+    is written, and every 16-byte store is aligned."""
+    nel = 32 if half else 64
+    for nvalid in list(range(1, nel + 1)) + [nel + 5]:
+        writes, vec, val, _ = _realigned_store_model(half, o, nvalid)
+        for rr in range(32):
+            want = set(range(min(nel, nvalid)))
+            assert set(writes[rr]) == want, (o, nvalid, rr)
+            for e, vs in writes[rr].items():
+                assert vs == [val(rr, e)], (o, nvalid, rr, e, vs)
+            assert all(off % 16 == 0 for off in vec[rr]), (o, nvalid, rr)
+
 @pytest.mark.parametrize("bn,parts", SPLIT_SHAPES)
 def test_split_reduction_layout_covers_each_owner_block_once(bn, parts):
     s = bn // parts
