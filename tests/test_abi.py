@@ -585,6 +585,70 @@ def _split_slot(q, r, col, bn, parts):
     return col // s, q * 128 * s * 4 + r * s * 4 + ((u ^ (r & 7)) << 4)
 
 
+def _repack_model(src, src_addr, rows, row_bytes, dst_pitch, batch=8):
+    """The operand copy (repack_rows_kernel) on the CPU, as the kernel issues
+    it: a warp per pass of kPassSegs = 32 * batch 16-byte segments of a row;
+    lane l loads the aligned source blocks t0 + 32q + l (t <= nseg, nothing
+    at or past the end of the source), lane 31 also block t0 + kPassSegs,
+    and each segment t < nseg is bytes [off, off + 16) of block t followed by
+    block t + 1, taken from the next lane, the next batch's lane 0, or lane
+    31's extra block. src_addr is the device address of src[0]."""
+    pass_segs = 32 * batch
+    end = src_addr + rows * row_bytes
+    nseg = (row_bytes + 15) // 16
+    passes = (row_bytes + 16 * pass_segs - 1) // (16 * pass_segs)
+    dst = bytearray(rows * dst_pitch)
+    loads = []
+    def block(addr):
+        if addr >= end:
+            return bytes(16)
+        loads.append(addr)
+        # bytes outside the source (before its start or past its end, inside
+        # the same aligned block) are not the copy's: model them as 0
+        return bytes(src[a - src_addr] if 0 <= a - src_addr < len(src) else 0 for a in range(addr, addr + 16))
+    for r in range(rows):
+        row = src_addr + r * row_bytes
+        off = row & 15
+        base = row - off
+        for ps in range(passes):
+            t0 = ps * pass_segs
+            v = [[block(base + 16 * (t0 + 32 * q + l)) if t0 + 32 * q + l <= nseg else bytes(16) for l in range(32)]
+                 for q in range(batch)]
+            tx = t0 + pass_segs
+            x = block(base + 16 * tx) if off != 0 and tx <= nseg else bytes(16)
+            for q in range(batch):
+                for l in range(32):
+                    t = t0 + 32 * q + l
+                    if t >= nseg:
+                        continue
+                    if off == 0:
+                        seg = v[q][l]
+                    else:
+                        hi = v[q][l + 1] if l < 31 else (v[q + 1][0] if q + 1 < batch else x)
+                        seg = (v[q][l] + hi)[off:off + 16]
+                    dst[r * dst_pitch + 16 * t: r * dst_pitch + 16 * t + 16] = seg
+    return dst, loads
+
+
+@pytest.mark.parametrize("row_bytes", [1, 2, 15, 16, 17, 100, 4095, 4096, 4097, 8190, 8208])
+def test_operand_copy_model_reproduces_every_row(row_bytes):
+    """The operand copy on the CPU, for every misalignment of the source and
+    rows whose pitch drifts across 16-byte boundaries (one and several passes
+    per row): each row of the destination starts with the source row, and no
+    load touches a 16-byte block at or past the source's end."""
+    rows = 5
+    pitch = -(-row_bytes // 128) * 128
+    rng = np.random.default_rng(row_bytes)
+    src = rng.integers(0, 256, rows * row_bytes + 32, dtype=np.uint8).tobytes()
+    for mis in range(16):
+        addr = 4096 + mis
+        body = src[:rows * row_bytes]
+        dst, loads = _repack_model(body, addr, rows, row_bytes, pitch)
+        for r in range(rows):
+            assert dst[r * pitch:r * pitch + row_bytes] == body[r * row_bytes:(r + 1) * row_bytes], (mis, r)
+        end = addr + rows * row_bytes
+        assert all(a % 16 == 0 and addr - (addr & 15) <= a < end for a in loads)
+
 def _realigned_store_model(half, o, nvalid, rows=32):
     """The realigned stores of a staged chunk (store mode 5), as the kernel
     issues them: one 16-byte box chunk g of row rr per piece, the aligned
