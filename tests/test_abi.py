@@ -649,6 +649,39 @@ def test_operand_copy_model_reproduces_every_row(row_bytes):
         end = addr + rows * row_bytes
         assert all(a % 16 == 0 and addr - (addr & 15) <= a < end for a in loads)
 
+@pytest.mark.parametrize("cpieces", [1, 2, 3, 4, 5, 8, 16, 31, 32, 33, 64])
+@pytest.mark.parametrize("warps", [1, 3, 8])
+def test_im2col_lane_split_writes_each_piece_once(cpieces, warps):
+    """The vector im2col's work split on the CPU: a warp takes `group`
+    (row, tap) segments at once when a tap has fewer than 32 16-byte pieces
+    (lane = segment within the group, piece), else one segment with its lanes
+    striding over the pieces; the padding columns are one more segment per
+    row. Every piece of every segment is written exactly once, by any number
+    of warps in the grid."""
+    rows, taps, pad_pieces = 7, 9, 3
+    segs = taps + 1
+    total = rows * segs
+    group = 1 if cpieces >= 32 else 32 // cpieces
+    step = 32 if cpieces >= 32 else cpieces
+    seen = {}
+    for wid in range(warps):
+        for lane in range(32):
+            sub = 0 if cpieces >= 32 else lane // cpieces
+            sl = lane if cpieces >= 32 else lane - sub * cpieces
+            g0 = wid * group
+            while g0 < total:
+                g = g0 + sub
+                if sub < group and g < total:
+                    m, seg = divmod(g, segs)
+                    n_pieces = pad_pieces if seg == taps else cpieces
+                    for j in range(sl, n_pieces, step):
+                        seen[(m, seg, j)] = seen.get((m, seg, j), 0) + 1
+                g0 += warps * group
+    want = {(m, seg, j) for m in range(rows) for seg in range(segs)
+            for j in range(pad_pieces if seg == taps else cpieces)}
+    assert set(seen) == want
+    assert all(v == 1 for v in seen.values())
+
 def _realigned_store_model(half, o, nvalid, rows=32):
     """The realigned stores of a staged chunk (store mode 5), as the kernel
     issues them: one 16-byte box chunk g of row rr per piece, the aligned
